@@ -1,0 +1,110 @@
+"""Planted mistakes in the oracle (on the CPU) must be caught by the pins.
+
+Each case patches one plausible error into the oracle: a swapped nibble order, a wrong
+magnitude, a transposed high-plane field, a wrong GQA index, a dropped window term, a
+missing max subtraction in the chunk combine. It then runs the pin tests that should fail
+and checks that at least one does.
+"""
+import numpy as np
+import pytest
+
+import oracle.attention as A
+import oracle.quant as Q
+from tests import test_oracle_pins as P
+
+
+def _fails(*tests):
+    for t in tests:
+        try:
+            t()
+        except AssertionError:
+            return True
+    return False
+
+
+def test_swapped_nibble_order_is_caught(monkeypatch):
+    def bad_pack(n):
+        n = np.asarray(n).astype(np.uint8) & 0xF
+        return (n[..., 1::2] | (n[..., 0::2] << 4)).astype(np.uint8)
+    monkeypatch.setattr(Q, "pack_nibbles", bad_pack)
+    assert _fails(lambda: P.test_q4_0_nibble_position(3))
+
+
+def test_magnitude_7_is_caught(monkeypatch):
+    orig = Q._symmetric_codes
+
+    def bad_quant(x):
+        xb = Q._blocks(x)
+        amax = np.max(np.abs(xb), axis=-1)
+        s16 = Q.fp16_round(amax / np.float32(7.0))
+        q = orig(xb, s16.astype(np.float32), -8, 7)
+        return Q.pack_nibbles(q & 0xF).reshape(x.shape[:-1] + (-1,)), s16
+    monkeypatch.setattr(Q, "quantize_q4_0", bad_quant)
+    assert _fails(P.test_q4_0_every_code_through_read_formula, P.test_q4_0_saturation_and_half_even)
+
+
+def test_q6_high_plane_interleave_is_caught(monkeypatch):
+    orig = Q.quantize_q6_0
+
+    def bad(x):
+        p, s = orig(x)
+        pb = p.reshape(p.shape[:-1] + (-1, 24)).copy()
+        hb = pb[..., 16:].astype(np.uint16)
+        # bit pairs in the reverse order inside each high byte
+        rev = ((hb & 3) << 6) | (((hb >> 2) & 3) << 4) | (((hb >> 4) & 3) << 2) | ((hb >> 6) & 3)
+        pb[..., 16:] = rev.astype(np.uint8)
+        return pb.reshape(p.shape), s
+    monkeypatch.setattr(Q, "quantize_q6_0", bad)
+    assert _fails(lambda: P.test_q6_0_plane_positions(1))
+
+
+def test_fwht_sign_error_is_caught(monkeypatch):
+    orig = Q.fwht
+
+    def bad(x, dtype=np.float32):
+        y = orig(x, dtype)
+        y[..., -1] = -y[..., -1]
+        return y
+    monkeypatch.setattr(Q, "fwht", bad)
+    assert _fails(lambda: P.test_fwht_equals_dense_sylvester(8))
+
+
+def test_wrong_gqa_index_is_caught(monkeypatch):
+    def bad(q, k_hat, v_hat, alpha, kv_len, causal=False, q_pos0=0):
+        Hkv = k_hat.shape[1]
+        # query head h reading kv head h % H_kv instead of h // (H_q / H_kv)
+        perm = np.array([h % Hkv for h in range(q.shape[1])])
+        g = q.shape[1] // Hkv
+        k2 = np.repeat(k_hat, g, axis=1)[:, [p * g for p in perm]]
+        v2 = np.repeat(v_hat, g, axis=1)[:, [p * g for p in perm]]
+        return orig(q, k2, v2, alpha, kv_len, causal, q_pos0)
+    orig = A.attend_dense
+    monkeypatch.setattr(A, "attend_dense", bad)
+    assert _fails(P.test_gqa_mapping_reads_kv_head_q_over_gqa)
+
+
+def test_dropped_window_is_caught(monkeypatch):
+    orig = A.attend_hadamard
+
+    def bad(q32, k_payload, k_scale, v_payload, v_scale, k_ring, v_ring, n_recent, *a, **kw):
+        return orig(q32, k_payload, k_scale, v_payload, v_scale, None, None, 0, *a, **kw)
+    monkeypatch.setattr(A, "attend_hadamard", bad)
+    assert _fails(P.test_hadamard_full_window_is_exact_attention)
+
+
+def test_combine_without_rescale_is_caught(monkeypatch):
+    def bad(ms, ls, os_):
+        ls, os_ = np.asarray(ls), np.asarray(os_)
+        return np.sum(os_, axis=0) / np.sum(ls, axis=0)[:, None]
+    monkeypatch.setattr(A, "lse_combine", bad)
+    assert _fails(lambda: P.test_split_k_equals_single_pass(16))
+
+
+def test_transposed_causal_limit_is_caught(monkeypatch):
+    def bad(n_q, kv_len, causal, q_pos0):
+        t = np.arange(kv_len)[None, :]
+        if not causal:
+            return np.ones((n_q, kv_len), bool)
+        return t < (q_pos0 + np.arange(n_q))[:, None]          # off by one: excludes the diagonal
+    monkeypatch.setattr(A, "visible_mask", bad)
+    assert _fails(P.test_attention_brute_force_gqa_causal)
