@@ -1,0 +1,175 @@
+/*
+ * kvq.h - sub-byte KV-cache quantization and packed-cache decode attention for GB300 (sm_103a).
+ *
+ * A stateless C library. The caller owns every buffer (device memory for the cache, inputs,
+ * outputs and workspace); the library validates arguments on the host, then enqueues CUDA
+ * kernels on the caller's stream and returns. It allocates nothing and never synchronises.
+ * Every entry point is re-entrant.
+ *
+ * Pages this follows (cited by title and section):
+ *   [FT]  FreeToken PR #268 "feat(kvcache): sub-byte Q4_0 and Q6_0 KV cache quantization",
+ *         "Storage layouts" and the q4_0 max_magnitude paragraph; packed buffer plus separate
+ *         scale buffer per spec ("Changes": mha_pool).
+ *   [TR]  tract discussion #2402 "Heads-up / RFC: int4 + Hadamard KV-cache quantization
+ *         (CPU + Metal)", "What's done", "Architecture: Data flow (decode)", "Why this quant
+ *         scheme", "Causality & mixed precision", "NNEF surface" (axis, scale, causal, n_recent).
+ *   [OTQ] "Open-TQ-Metal: Fused Compressed-Domain Attention for Long-Context LLM Inference on
+ *         Apple Silicon", per-group asymmetric int4 background; Section 3 (fused kernel, GQA
+ *         mapping kv_head = head / gqa, split-K into ceil(S/512) chunks, partial + reduce phases).
+ *
+ * Conventions
+ *   - All device pointers must be 16-byte aligned; the workspace 256-byte aligned.
+ *   - Element order is row-major C order in the shapes given below.
+ *   - Errors are returned as kvq_status; nothing is printed, nothing aborts. A failed call
+ *     enqueues nothing. kvq_last_error() gives a one-line reason for the calling thread's
+ *     last failure. KVQ_ECUDA reports a launch error seen right after enqueueing.
+ *   - Inputs must be finite; NaN/Inf inputs give unspecified codes and outputs.
+ *   - head_dim must be 128 or 256.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. NULL means the legacy default stream. */
+typedef struct CUstream_st *kvq_stream_t;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_EINVAL = 1,        /* null pointer, negative size, bad enum value, kv_len == 0 */
+  KVQ_ESHAPE = 2,        /* head_dim not 128/256, H_q not a multiple of H_kv, bad chunk */
+  KVQ_ECAPACITY = 3,     /* pos0 + n_new > capacity, kv_len > capacity */
+  KVQ_EUNSUPPORTED = 4,  /* layout/dtype combination not provided */
+  KVQ_EALIGN = 5,        /* a pointer is not 16-byte aligned (workspace: 256) */
+  KVQ_ECUDA = 6,         /* a CUDA launch failed */
+  KVQ_EWORKSPACE = 7     /* workspace_bytes smaller than kvq_attend_workspace_bytes() */
+} kvq_status;
+
+typedef enum {
+  /* [FT] q4_0: per 32 values along head_dim, 16 payload bytes (byte j = value 2j in the low
+   * nibble, value 2j+1 in the high nibble; the nibble is read back as (v ^ 0x8) - 0x8) and one
+   * fp16 scale = amax / 8; codes clamped to [-8, 7]. */
+  KVQ_Q4_0 = 0,
+  /* [FT] q6_0: per 32 values a 16-byte low plane (low four bits, q4_0 nibble order) followed by
+   * an 8-byte high plane (top two bits, value 4k+i at bits 2i of byte k), one fp16 scale =
+   * amax / 32; read back as (v ^ 0x20) - 0x20 with v = low | high << 4; codes in [-32, 31]. */
+  KVQ_Q6_0 = 1,
+  /* [TR] per-token symmetric int4 in a fixed Hadamard basis: y = FWHT(x) * fp32(1/sqrt(D))
+   * (radix-2 butterflies, half-span 1, 2, ..., D/2), one f32 scale s = amax(|y|) / 7 per token,
+   * codes rint(y / s) in [-7, 7] packed in q4_0 nibble order (D/2 bytes per token). Scores
+   * are the exact integer dot int8(q_rot) . int4(k_rot) times the scales. An optional ring
+   * of the newest n_recent rotated rows is kept in exact f32. */
+  KVQ_HAD_INT4 = 2,
+  /* [OTQ] per-group asymmetric int4, g = 32: fp16 scale = (max - min) / 15 and fp16
+   * zero-point = min per group; codes rint((x - zero) / scale) in [0, 15], unsigned, q4_0
+   * nibble order; value = code * scale + zero. */
+  KVQ_ASYM4_G32 = 3
+} kvq_layout;
+
+typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_F16 = 2 } kvq_dtype;
+
+/*
+ * A caller-owned packed cache for one attention layer. Planes (K and V each):
+ *   payload  u8  [batch][n_kv_heads][capacity][kvq_row_bytes(layout, head_dim)]
+ *   scale    f16 [batch][n_kv_heads][capacity][head_dim/32]      (Q4_0, Q6_0, ASYM4_G32)
+ *            f32 [batch][n_kv_heads][capacity]                   (HAD_INT4)
+ *   zero     f16 [batch][n_kv_heads][capacity][head_dim/32]      (ASYM4_G32 only, else NULL)
+ *   recent   f32 [batch][n_kv_heads][n_recent][head_dim]         (HAD_INT4 with n_recent > 0,
+ *                                                                 else NULL)
+ * Payload and scales sit in separate buffers ([FT] "packed buffer + separate scale buffer").
+ * The cache is preallocated at `capacity` tokens and appended in place ([OTQ]: per-step
+ * concatenation instead of preallocated slices cost 18%).
+ */
+typedef struct kvq_cache {
+  int32_t layout;      /* kvq_layout */
+  int32_t batch;
+  int32_t n_kv_heads;
+  int32_t head_dim;    /* 128 or 256 */
+  int32_t capacity;    /* tokens per (batch, kv head) */
+  int32_t n_recent;    /* HAD_INT4: size of the exact-f32 ring (0 = pure int4); others: 0 */
+  void *k_payload, *v_payload;
+  void *k_scale, *v_scale;
+  void *k_zero, *v_zero;
+  float *k_recent, *v_recent;
+} kvq_cache;
+
+/* Payload bytes of one token row of one head; 0 for an unknown layout or head_dim. */
+size_t kvq_row_bytes(int32_t layout, int32_t head_dim);
+
+/* Bytes of each plane of one of K or V: out_sizes = {payload, scale, zero, recent}.
+ * Unused planes report 0. */
+kvq_status kvq_cache_bytes(int32_t layout, int32_t batch, int32_t n_kv_heads, int32_t head_dim,
+                           int32_t capacity, int32_t n_recent, size_t out_sizes[4]);
+
+/*
+ * Store (append) n_new tokens per (batch, kv head) at positions [pos0, pos0 + n_new).
+ *   k_new, v_new: device [batch][n_kv_heads][n_new][head_dim] in `dtype` (f32, bf16 or f16).
+ * Quantisation is exact and deterministic: re-storing a token writes identical bytes.
+ * HAD_INT4 with n_recent > 0 also writes the rotated f32 rows of the last
+ * min(n_new, n_recent) tokens to ring slot (position mod n_recent); attention with the window
+ * therefore expects kv_len equal to the end of the latest store.
+ * One kernel launch covers K and V. n_new == 0 is a no-op.
+ */
+kvq_status kvq_store_q4_0(const kvq_cache *cache, const void *k_new, const void *v_new,
+                          int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
+kvq_status kvq_store_q6_0(const kvq_cache *cache, const void *k_new, const void *v_new,
+                          int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
+kvq_status kvq_store_hadamard_int4(const kvq_cache *cache, const void *k_new, const void *v_new,
+                                   int32_t dtype, int32_t n_new, int32_t pos0,
+                                   kvq_stream_t stream);
+kvq_status kvq_store_asym4_g32(const kvq_cache *cache, const void *k_new, const void *v_new,
+                               int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
+
+/* Workspace bytes kvq_decode_attend needs for these arguments (0 on invalid arguments).
+ * chunk 0 means the default of 512 tokens. */
+size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q,
+                                  int32_t kv_len, int32_t chunk);
+
+/*
+ * Fused split-K decode attention over the packed cache; the dequantised K/V matrix is never
+ * written anywhere ([OTQ] Section 3: fused compressed-domain attention).
+ *   q    device [batch][n_q_heads][n_q][head_dim] in q_dtype
+ *   out  device f32 [batch][n_q_heads][n_q][head_dim]
+ * Query head h reads kv head h / (n_q_heads / n_kv_heads) ([OTQ] GQA mapping). Row i of each
+ * head attends tokens t < kv_len and, when causal != 0, t <= q_pos0 + i ([TR] causal
+ * masking); a causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len.
+ * score = attn_scale * q . k_hat. Phase 1 splits the tokens into chunks of `chunk` tokens
+ * (0 -> 512; else a multiple of 64 in [64, 8192]) and writes per (row, chunk) the running
+ * max, the sum of exponentials and the unnormalised output to the workspace; phase 2
+ * combines them with the online-softmax correction ([OTQ] Section 3.2). HAD_INT4: the query
+ * is rotated and quantised to int8 (one f32 scale per row, amax / 127), body tokens are
+ * scored by the exact integer dot, the newest min(n_recent, kv_len) tokens by exact f32
+ * from the ring, and phase 2 un-rotates the output ([TR] data flow).
+ * The two phases are separate launches on `stream`; the workspace must not be shared with
+ * another call in flight.
+ */
+kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                             int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t causal,
+                             int32_t q_pos0, float attn_scale, int32_t chunk, float *out,
+                             void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * HAD_INT4 test hook: the exact integer-domain body scores int8(q_rot) . int4(k_rot).
+ *   scores_out device i32 [batch][n_q_heads][n_q][kv_len - min(n_recent, kv_len)]
+ *   s_q_out    device f32 [batch][n_q_heads][n_q]   (the per-row int8 scale of q_rot)
+ */
+kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                int32_t n_q_heads, int32_t n_q, int32_t kv_len,
+                                int32_t *scores_out, float *s_q_out, kvq_stream_t stream);
+
+/* Static description of a status code. */
+const char *kvq_status_string(int32_t status);
+
+/* One-line reason for the calling thread's most recent failed call ("" if none). */
+const char *kvq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

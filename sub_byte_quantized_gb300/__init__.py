@@ -1,0 +1,10 @@
+"""Sub-byte KV-cache quantization and packed-cache decode attention for GB300 (sm_103a).
+
+The compute path is the CUDA library libkvq.so (C ABI in include/kvq.h); this package only
+marshals torch tensors into its calls. Importing the package does not load the library; the
+first call does, and raises if it is missing.
+"""
+from .api import (  # noqa: F401
+    KVCache, store, decode_attend, attend_workspace_bytes, debug_scores_i32, row_bytes, cache_plane_bytes,
+)
+from ._lib import KvqError, LAYOUT_IDS, EXPORTS  # noqa: F401

@@ -1,0 +1,155 @@
+"""Thin torch-facing wrappers over the C ABI: they check tensor placement/shape, pass raw
+pointers and the current CUDA stream, and nothing else. Every computation runs in libkvq.so.
+
+torch is used for device memory (cache planes, workspace) and streams only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import math
+
+import torch
+
+from . import _lib as L
+
+_DTYPES = {torch.float32: L.KVQ_F32, torch.bfloat16: L.KVQ_BF16, torch.float16: L.KVQ_F16}
+_STORE_FN = {L.KVQ_Q4_0: "kvq_store_q4_0", L.KVQ_Q6_0: "kvq_store_q6_0",
+             L.KVQ_HAD_INT4: "kvq_store_hadamard_int4", L.KVQ_ASYM4_G32: "kvq_store_asym4_g32"}
+
+
+def _layout_id(layout) -> int:
+    return L.LAYOUT_IDS[layout] if isinstance(layout, str) else int(layout)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream if isinstance(s, torch.cuda.Stream) else int(s)
+
+
+def _need_cuda(name: str, t: torch.Tensor) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def row_bytes(layout, head_dim: int) -> int:
+    return int(L.lib().kvq_row_bytes(_layout_id(layout), head_dim))
+
+
+def cache_plane_bytes(layout, batch, n_kv_heads, head_dim, capacity, n_recent=0) -> dict:
+    out = (C.c_size_t * 4)()
+    L.check(L.lib().kvq_cache_bytes(_layout_id(layout), batch, n_kv_heads, head_dim, capacity, n_recent, out),
+            "kvq_cache_bytes")
+    return {"payload": out[0], "scale": out[1], "zero": out[2], "recent": out[3]}
+
+
+class KVCache:
+    """Device planes of one layer's packed cache plus the C struct describing them.
+
+    Planes (K and V each): payload u8 [B][H_kv][cap][row_bytes]; scale f16 [B][H_kv][cap][D/32]
+    (f32 [B][H_kv][cap] for had_int4); zero f16 (asym4_g32); recent f32 [B][H_kv][n_recent][D]
+    (had_int4 with n_recent > 0).
+    """
+
+    def __init__(self, layout, batch: int, n_kv_heads: int, head_dim: int, capacity: int, n_recent: int = 0,
+                 device="cuda"):
+        self.layout = _layout_id(layout)
+        self.batch, self.n_kv_heads, self.head_dim, self.capacity = batch, n_kv_heads, head_dim, capacity
+        self.n_recent = n_recent if self.layout == L.KVQ_HAD_INT4 else 0
+        sizes = cache_plane_bytes(self.layout, batch, n_kv_heads, head_dim, capacity, self.n_recent)
+        rb = row_bytes(self.layout, head_dim)
+        nb = head_dim // 32
+        dev = torch.device(device)
+        shp = (batch, n_kv_heads, capacity)
+        self.planes = {}
+        for t in ("k", "v"):
+            pl = {"payload": torch.zeros(shp + (rb,), dtype=torch.uint8, device=dev)}
+            if self.layout == L.KVQ_HAD_INT4:
+                pl["scale"] = torch.zeros(shp, dtype=torch.float32, device=dev)
+                if self.n_recent:
+                    pl["recent"] = torch.zeros((batch, n_kv_heads, self.n_recent, head_dim), dtype=torch.float32,
+                                               device=dev)
+            else:
+                pl["scale"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
+                if self.layout == L.KVQ_ASYM4_G32:
+                    pl["zero"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
+            assert pl["payload"].numel() == sizes["payload"]
+            self.planes[t] = pl
+        self.struct = L.KvqCache(
+            self.layout, batch, n_kv_heads, head_dim, capacity, self.n_recent,
+            _ptr(self.planes["k"]["payload"]), _ptr(self.planes["v"]["payload"]),
+            _ptr(self.planes["k"]["scale"]), _ptr(self.planes["v"]["scale"]),
+            _ptr(self.planes["k"].get("zero")), _ptr(self.planes["v"].get("zero")),
+            _ptr(self.planes["k"].get("recent")), _ptr(self.planes["v"].get("recent")))
+
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for pl in self.planes.values() for t in pl.values())
+
+    def read_bytes(self, kv_len: int) -> int:
+        """Packed bytes (payload + scales [+ zeros] [+ window]) one attention call reads."""
+        per_tok = row_bytes(self.layout, self.head_dim)
+        if self.layout == L.KVQ_HAD_INT4:
+            n_w = min(self.n_recent, kv_len)
+            return 2 * self.batch * self.n_kv_heads * ((kv_len - n_w) * (per_tok + 4) + n_w * self.head_dim * 4)
+        per_tok += 2 * (self.head_dim // 32) * (2 if self.layout == L.KVQ_ASYM4_G32 else 1)
+        return 2 * self.batch * self.n_kv_heads * kv_len * per_tok
+
+
+def store(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int, stream=None) -> None:
+    """Append k_new/v_new [B][H_kv][n_new][D] at positions [pos0, pos0 + n_new)."""
+    _need_cuda("k_new", k_new)
+    _need_cuda("v_new", v_new)
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same shape and dtype")
+    B, H, n_new, D = k_new.shape
+    if (B, H, D) != (cache.batch, cache.n_kv_heads, cache.head_dim):
+        raise ValueError("k_new shape does not match the cache")
+    fn = getattr(L.lib(), _STORE_FN[cache.layout])
+    L.check(fn(C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, pos0,
+               _stream(stream)), _STORE_FN[cache.layout])
+
+
+def attend_workspace_bytes(cache: KVCache, n_q_heads: int, n_q: int, kv_len: int, chunk: int = 0) -> int:
+    return int(L.lib().kvq_attend_workspace_bytes(C.byref(cache.struct), n_q_heads, n_q, kv_len, chunk))
+
+
+def decode_attend(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = False, q_pos0: int = 0,
+                  attn_scale: float | None = None, chunk: int = 0, out: torch.Tensor | None = None,
+                  workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Split-K attention of q [B][H_q][n_q][D] over the first kv_len cached tokens -> f32 out."""
+    _need_cuda("q", q)
+    B, Hq, n_q, D = q.shape
+    if B != cache.batch or D != cache.head_dim:
+        raise ValueError("q shape does not match the cache")
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    _need_cuda("out", out)
+    need = attend_workspace_bytes(cache, Hq, n_q, kv_len, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need_cuda("workspace", workspace)
+    L.check(L.lib().kvq_decode_attend(C.byref(cache.struct), q.data_ptr(), _DTYPES[q.dtype], Hq, n_q, kv_len,
+                                      int(bool(causal)), q_pos0, float(attn_scale), chunk, out.data_ptr(),
+                                      workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                      _stream(stream)), "kvq_decode_attend")
+    return out
+
+
+def debug_scores_i32(cache: KVCache, q: torch.Tensor, kv_len: int, stream=None):
+    """Hadamard-int4 exact integer body scores [B][H_q][n_q][kv_len - n_window] and the int8 row scales."""
+    _need_cuda("q", q)
+    B, Hq, n_q, D = q.shape
+    n_body = kv_len - min(cache.n_recent, kv_len)
+    buf = torch.empty(B * Hq * n_q * max(n_body, 1), dtype=torch.int32, device=q.device)
+    s_q = torch.empty((B, Hq, n_q), dtype=torch.float32, device=q.device)
+    L.check(L.lib().kvq_debug_scores_i32(C.byref(cache.struct), q.data_ptr(), _DTYPES[q.dtype], Hq, n_q, kv_len,
+                                         buf.data_ptr(), s_q.data_ptr(), _stream(stream)),
+            "kvq_debug_scores_i32")
+    return buf[:B * Hq * n_q * n_body].view(B, Hq, n_q, n_body), s_q

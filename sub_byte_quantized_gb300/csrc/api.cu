@@ -1,0 +1,251 @@
+// C ABI of the library: host-side validation, workspace layout and kernel launches.
+// Nothing here allocates, synchronises or prints; failures return a kvq_status and record a
+// one-line reason readable through kvq_last_error().
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kvq_internal.cuh"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+kvq_status fail(kvq_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t row_bytes_of(int layout, int D) {
+  if (D != 128 && D != 256) return 0;
+  const int nb = D / kvq::kBlock;
+  switch (layout) {
+    case KVQ_Q4_0: return 16 * (size_t)nb;
+    case KVQ_Q6_0: return 24 * (size_t)nb;
+    case KVQ_HAD_INT4: return (size_t)D / 2;
+    case KVQ_ASYM4_G32: return 16 * (size_t)nb;
+    default: return 0;
+  }
+}
+
+kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (c->layout < KVQ_Q4_0 || c->layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
+  if (c->head_dim != 128 && c->head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", c->head_dim);
+  if (c->batch < 1 || c->n_kv_heads < 1 || c->capacity < 1)
+    return fail(KVQ_EINVAL, "batch, n_kv_heads and capacity must be >= 1");
+  if (c->n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
+  if (c->layout != KVQ_HAD_INT4 && c->n_recent != 0)
+    return fail(KVQ_EUNSUPPORTED, "n_recent is a Hadamard-int4 option");
+  const void *ptrs[] = {c->k_payload, c->v_payload, c->k_scale, c->v_scale};
+  for (const void *p : ptrs) {
+    if (!p) return fail(KVQ_EINVAL, "payload/scale pointer is NULL");
+    if (!aligned(p, 16)) return fail(KVQ_EALIGN, "payload/scale pointer not 16-byte aligned");
+  }
+  if (c->layout == KVQ_ASYM4_G32) {
+    if (!c->k_zero || !c->v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
+    if (!aligned(c->k_zero, 16) || !aligned(c->v_zero, 16)) return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
+  }
+  if (c->layout == KVQ_HAD_INT4 && c->n_recent > 0) {
+    if (!c->k_recent || !c->v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
+    if (!aligned(c->k_recent, 16) || !aligned(c->v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
+  }
+  v.layout = c->layout; v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim; v.cap = c->capacity;
+  v.n_recent = c->layout == KVQ_HAD_INT4 ? c->n_recent : 0;
+  v.row_bytes = (int)row_bytes_of(c->layout, c->head_dim);
+  v.payload[0] = static_cast<uint8_t *>(c->k_payload);
+  v.payload[1] = static_cast<uint8_t *>(c->v_payload);
+  v.scale[0] = c->k_scale; v.scale[1] = c->v_scale;
+  v.zero[0] = static_cast<__half *>(c->k_zero);
+  v.zero[1] = static_cast<__half *>(c->v_zero);
+  v.ring[0] = c->k_recent; v.ring[1] = c->v_recent;
+  return KVQ_OK;
+}
+
+kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_new, const void *v_new, int dtype,
+                        int n_new, int pos0, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::CacheView v;
+  kvq_status st = check_cache(cache, v);
+  if (st != KVQ_OK) return st;
+  if (v.layout != want_layout) return fail(KVQ_EUNSUPPORTED, "cache layout %d does not match this store", v.layout);
+  if (dtype < KVQ_F32 || dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown dtype %d", dtype);
+  if (n_new < 0 || pos0 < 0) return fail(KVQ_EINVAL, "n_new and pos0 must be >= 0");
+  if ((long long)pos0 + n_new > v.cap) return fail(KVQ_ECAPACITY, "pos0 + n_new = %lld > capacity %d",
+                                                  (long long)pos0 + n_new, v.cap);
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new) return fail(KVQ_EINVAL, "k_new/v_new is NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(KVQ_EALIGN, "k_new/v_new not 16-byte aligned");
+  cudaError_t e = kvq::launch_store(v, k_new, v_new, dtype, n_new, pos0, stream);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "store launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+// Resolve the attention arguments and the workspace layout. When `ws` is NULL only sizes are
+// computed (returned through `need`).
+kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv_len, int causal, int q_pos0,
+                          int chunk, kvq::AttendArgs &a, size_t &need, void *ws) {
+  kvq_status st = check_cache(cache, a.cache);
+  if (st != KVQ_OK) return st;
+  const kvq::CacheView &c = a.cache;
+  if (n_q_heads < 1 || n_q < 1) return fail(KVQ_EINVAL, "n_q_heads and n_q must be >= 1");
+  if (n_q_heads % c.H) return fail(KVQ_ESHAPE, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, c.H);
+  if (kv_len < 1) return fail(KVQ_EINVAL, "kv_len must be >= 1");
+  if (kv_len > c.cap) return fail(KVQ_ECAPACITY, "kv_len %d > capacity %d", kv_len, c.cap);
+  if (causal && (q_pos0 < 0 || (long long)q_pos0 + n_q > kv_len))
+    return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
+  if (chunk == 0) chunk = 512;
+  if (chunk < 64 || chunk > 8192 || chunk % 64) return fail(KVQ_ESHAPE, "chunk %d not a multiple of 64 in [64, 8192]", chunk);
+  a.Hq = n_q_heads; a.gqa = n_q_heads / c.H; a.n_q = n_q;
+  a.kv_len = kv_len;
+  a.n_win = c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0;
+  a.n_body = kv_len - a.n_win;
+  a.causal = causal ? 1 : 0;
+  a.q_pos0 = causal ? q_pos0 : 0;
+  a.chunk = chunk;
+  a.n_chunks = (a.n_body + chunk - 1) / chunk;
+  a.C = a.n_chunks + (a.n_win > 0 ? 1 : 0);
+  const size_t rows = (size_t)c.B * n_q_heads * n_q;
+  size_t off = 0;
+  const size_t o_m = off; off = round_up(off + rows * a.C * sizeof(float), 256);
+  const size_t o_l = off; off = round_up(off + rows * a.C * sizeof(float), 256);
+  const size_t o_o = off; off = round_up(off + rows * a.C * (size_t)c.D * sizeof(float), 256);
+  size_t o_q8 = 0, o_sq = 0, o_qr = 0;
+  if (c.layout == KVQ_HAD_INT4) {
+    o_q8 = off; off = round_up(off + rows * (size_t)c.D, 256);
+    o_sq = off; off = round_up(off + rows * sizeof(float), 256);
+    o_qr = off; off = round_up(off + rows * (size_t)c.D * sizeof(float), 256);
+  }
+  need = off;
+  if (ws) {
+    char *w = static_cast<char *>(ws);
+    a.part_m = reinterpret_cast<float *>(w + o_m);
+    a.part_l = reinterpret_cast<float *>(w + o_l);
+    a.part_o = reinterpret_cast<float *>(w + o_o);
+    a.q8 = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<int8_t *>(w + o_q8) : nullptr;
+    a.s_q = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<float *>(w + o_sq) : nullptr;
+    a.q_rot = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<float *>(w + o_qr) : nullptr;
+  }
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_row_bytes(int32_t layout, int32_t head_dim) { return row_bytes_of(layout, head_dim); }
+
+kvq_status kvq_cache_bytes(int32_t layout, int32_t batch, int32_t n_kv_heads, int32_t head_dim, int32_t capacity,
+                           int32_t n_recent, size_t out_sizes[4]) {
+  g_last_error[0] = 0;
+  if (!out_sizes) return fail(KVQ_EINVAL, "out_sizes is NULL");
+  const size_t rb = row_bytes_of(layout, head_dim);
+  if (layout < KVQ_Q4_0 || layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", layout);
+  if (!rb) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", head_dim);
+  if (batch < 1 || n_kv_heads < 1 || capacity < 1 || n_recent < 0) return fail(KVQ_EINVAL, "bad sizes");
+  const size_t rows = (size_t)batch * n_kv_heads * capacity;
+  const size_t nb = (size_t)head_dim / kvq::kBlock;
+  out_sizes[0] = rows * rb;
+  out_sizes[1] = layout == KVQ_HAD_INT4 ? rows * sizeof(float) : rows * nb * 2;
+  out_sizes[2] = layout == KVQ_ASYM4_G32 ? rows * nb * 2 : 0;
+  out_sizes[3] = layout == KVQ_HAD_INT4 ? (size_t)batch * n_kv_heads * n_recent * head_dim * sizeof(float) : 0;
+  return KVQ_OK;
+}
+
+kvq_status kvq_store_q4_0(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype, int32_t n_new,
+                          int32_t pos0, kvq_stream_t stream) {
+  return store_common(KVQ_Q4_0, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
+kvq_status kvq_store_q6_0(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype, int32_t n_new,
+                          int32_t pos0, kvq_stream_t stream) {
+  return store_common(KVQ_Q6_0, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
+kvq_status kvq_store_hadamard_int4(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
+                                   int32_t n_new, int32_t pos0, kvq_stream_t stream) {
+  return store_common(KVQ_HAD_INT4, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
+kvq_status kvq_store_asym4_g32(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
+                               int32_t n_new, int32_t pos0, kvq_stream_t stream) {
+  return store_common(KVQ_ASYM4_G32, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
+
+size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t kv_len,
+                                  int32_t chunk) {
+  kvq::AttendArgs a;
+  size_t need = 0;
+  if (resolve_attend(cache, n_q_heads, n_q, kv_len, 0, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  return need;
+}
+
+kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                             int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                             float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  size_t need = 0;
+  kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  if (q_dtype < KVQ_F32 || q_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown q dtype %d", q_dtype);
+  if (!q || !out || !workspace) return fail(KVQ_EINVAL, "q/out/workspace is NULL");
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(KVQ_EALIGN, "q/out not 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(KVQ_EALIGN, "workspace not 256-byte aligned");
+  if (workspace_bytes < need) return fail(KVQ_EWORKSPACE, "workspace %zu < required %zu", workspace_bytes, need);
+  if (!(attn_scale == attn_scale) || attn_scale > 3.0e38f || attn_scale < -3.0e38f)
+    return fail(KVQ_EINVAL, "attn_scale must be finite");
+  resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, workspace);
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.scale = attn_scale;
+  a.out = out;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (a.cache.layout == KVQ_HAD_INT4) e = kvq::launch_had_prep(a, s);
+  if (e == cudaSuccess) e = kvq::mma_supported(a) ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
+  if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads,
+                                int32_t n_q, int32_t kv_len, int32_t *scores_out, float *s_q_out,
+                                kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  size_t need = 0;
+  kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, 0, 0, 0, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  if (a.cache.layout != KVQ_HAD_INT4) return fail(KVQ_EUNSUPPORTED, "integer scores exist for HAD_INT4 only");
+  if (q_dtype < KVQ_F32 || q_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown q dtype %d", q_dtype);
+  if (!q || !scores_out || !s_q_out) return fail(KVQ_EINVAL, "q/scores_out/s_q_out is NULL");
+  if (!aligned(q, 16) || !aligned(scores_out, 16) || !aligned(s_q_out, 16))
+    return fail(KVQ_EALIGN, "q/scores_out/s_q_out not 16-byte aligned");
+  cudaError_t e = kvq::launch_debug_scores(a.cache, q, q_dtype, n_q_heads, n_q, kv_len, a.n_body, scores_out, s_q_out,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "debug scores launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+const char *kvq_status_string(int32_t status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_EINVAL: return "invalid argument";
+    case KVQ_ESHAPE: return "unsupported shape";
+    case KVQ_ECAPACITY: return "beyond cache capacity";
+    case KVQ_EUNSUPPORTED: return "unsupported layout or option";
+    case KVQ_EALIGN: return "misaligned pointer";
+    case KVQ_ECUDA: return "CUDA launch error";
+    case KVQ_EWORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+const char *kvq_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,456 @@
+// Split-K decode attention, CUDA-core form for every layout and shape, plus the phase-2
+// LSE reduce and the Hadamard query preparation.
+//
+// Phase 1 (attend_generic_kernel): one CTA per (chunk, batch x kv head, group of 8 query
+// rows). The chunk is walked in sub-tiles of T tokens; each sub-tile of K and V is unpacked
+// from the packed cache into shared memory (nibbles / bit planes sign-extended in registers,
+// times their scales), then each warp scores its query row against the sub-tile (one token
+// per lane), keeps an online softmax (running max m, running sum l) and accumulates the
+// unnormalised output o. The dequantised rows live only in shared memory for one sub-tile;
+// nothing the size of the cache is ever written. Each (row, chunk) writes (m, l, o) to the
+// workspace.
+//
+// Hadamard int4: body tokens hold their signed int4 codes in shared memory and are scored as
+// the exact integer dot with the row's int8 query codes (sums of products of integers below
+// 2^24 are exact in float32), times alpha * s_q * s_k. The exact-f32 ring forms one extra
+// chunk scored with the float32 rotated query.
+//
+// Phase 2 (attend_reduce_kernel): per query row, M = max m_c, L = sum l_c e^(m_c - M),
+// O = sum o_c e^(m_c - M) / L over the chunks the row can see; Hadamard outputs are
+// un-rotated with the same in-warp FWHT and 1/sqrt(D).
+#include <cfloat>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kRowsPerCta = 8;       // one warp per query row
+constexpr int kThreads = kRowsPerCta * 32;
+
+// Absolute token range of chunk c: body chunks [c*chunk, min(n_body, (c+1)*chunk)), the window
+// chunk [n_body, kv_len).
+__device__ __forceinline__ void chunk_range(const AttendArgs &a, int c, int &t0, int &t1) {
+  if (c < a.n_chunks) {
+    t0 = c * a.chunk;
+    t1 = min(a.n_body, t0 + a.chunk);
+  } else {
+    t0 = a.n_body;
+    t1 = a.kv_len;
+  }
+}
+
+// Last token row i may see.
+__device__ __forceinline__ int row_limit(const AttendArgs &a, int i) {
+  return a.causal ? min(a.kv_len - 1, a.q_pos0 + i) : a.kv_len - 1;
+}
+
+// Unpack 8 values (group gi of a token row) of a packed row into f32 (value = code * scale [+ zero]).
+// For HAD_INT4 the raw signed codes are produced (the per-token scale is applied by the caller).
+__device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, int gi, float out[8]) {
+  const uint8_t *p = c.payload[kv] + row * (size_t)c.row_bytes;
+  const int blk = gi >> 2, sub = gi & 3;
+  if (c.layout == KVQ_HAD_INT4) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(p + gi * 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8);
+    return;
+  }
+  const float s = __half2float(static_cast<const __half *>(c.scale[kv])[row * (c.D / kBlock) + blk]);
+  if (c.layout == KVQ_Q4_0) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(p + blk * 16 + sub * 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8) * s;
+  } else if (c.layout == KVQ_Q6_0) {
+    const uint32_t lo = *reinterpret_cast<const uint32_t *>(p + blk * 24 + sub * 4);
+    const uint32_t hi = *reinterpret_cast<const uint16_t *>(p + blk * 24 + 16 + sub * 2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t v = ((lo >> (4 * i)) & 0xFu) | (((hi >> (2 * i)) & 0x3u) << 4);
+      out[i] = (float)((int)(v ^ 0x20u) - 0x20) * s;
+    }
+  } else {  // ASYM4_G32
+    const float z = __half2float(c.zero[kv][row * (c.D / kBlock) + blk]);
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(p + blk * 16 + sub * 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = fmaf((float)((w >> (4 * i)) & 0xFu), s, z);
+  }
+}
+
+// D: head dim; T: tokens per shared-memory sub-tile.
+template <int D, int T>
+__global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) {
+  extern __shared__ __align__(16) float smem[];
+  float *Ks = smem;                          // [T][D + 1]
+  float *Vs = Ks + T * (D + 1);              // [T][D]
+  float *Qs = Vs + T * D;                    // [8][D]
+  float *ks = Qs + kRowsPerCta * D;          // [T] HAD body: per-token K scale
+  float *vs = ks + T;                        // [T] HAD body: per-token V scale
+
+  const CacheView &c = a.cache;
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  // Let the phase-2 grid be scheduled early; it still waits for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
+  const int chunk_id = blockIdx.x;
+  const int bh = blockIdx.y;                 // b * H_kv + kv head
+  const int b = bh / c.H, kvh = bh - b * c.H;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = a.gqa * a.n_q;
+  const int r = blockIdx.z * kRowsPerCta + warp;       // row within the GQA group
+  const bool row_ok = r < R;
+  const int hq = kvh * a.gqa + (row_ok ? r / a.n_q : 0);
+  const int qi = row_ok ? r % a.n_q : 0;
+  const size_t grow = ((size_t)b * a.Hq + hq) * a.n_q + qi;   // global query row
+
+  int t0, t1;
+  chunk_range(a, chunk_id, t0, t1);
+  const bool is_win = chunk_id >= a.n_chunks;
+  const bool had = c.layout == KVQ_HAD_INT4;
+  const int lim = row_ok ? row_limit(a, qi) : -1;
+  // Highest token any row of this CTA may see.
+  int cta_lim = -1;
+  for (int w = 0; w < kRowsPerCta; ++w) {
+    const int rr = blockIdx.z * kRowsPerCta + w;
+    if (rr < R) cta_lim = max(cta_lim, row_limit(a, rr % a.n_q));
+  }
+  if (t0 > cta_lim) return;                  // no row sees this chunk: phase 2 skips it too
+  const int t_end = min(t1, cta_lim + 1);
+
+  // Query row into shared memory: HAD body -> int8 codes; HAD window -> rotated f32; else q.
+  constexpr int VPL = D / 32;
+  if (row_ok) {
+    for (int d = lane; d < D; d += 32) {
+      float qv;
+      if (had) {
+        qv = is_win ? a.q_rot[grow * D + d] : (float)a.q8[grow * D + d];
+      } else if (a.q_dtype == KVQ_F32) {
+        qv = static_cast<const float *>(a.q)[grow * D + d];
+      } else if (a.q_dtype == KVQ_BF16) {
+        qv = bf16_bits_to_f32(static_cast<const uint16_t *>(a.q)[grow * D + d]);
+      } else {
+        qv = __half2float(static_cast<const __half *>(a.q)[grow * D + d]);
+      }
+      Qs[warp * D + d] = qv;
+    }
+  }
+  const float sq = (had && !is_win && row_ok) ? a.s_q[grow] : 1.0f;
+
+  float m = -INFINITY, l = 0.0f;
+  float o[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) o[i] = 0.0f;
+
+  const size_t head_row0 = (size_t)bh * c.cap;          // cache row of token 0
+  for (int tb = t0; tb < t_end; tb += T) {
+    const int nt = min(T, t_end - tb);
+    __syncthreads();                                     // previous sub-tile fully consumed
+    // Unpack K and V rows [tb, tb + nt) into shared memory.
+    for (int idx = threadIdx.x; idx < 2 * T * (D / 8); idx += kThreads) {
+      const int kv = idx >= T * (D / 8);
+      const int rem = idx - kv * T * (D / 8);
+      const int t = rem / (D / 8), gi = rem - t * (D / 8);
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (t >= nt && gi == 0) (kv ? vs : ks)[t] = 0.0f;   // tail tokens weigh exactly zero
+      if (t < nt) {
+        const int tok = tb + t;
+        if (is_win) {
+          const float *src = c.ring[kv] + ((size_t)bh * c.n_recent + (size_t)(tok % c.n_recent)) * D + gi * 8;
+          const float4 x0 = *reinterpret_cast<const float4 *>(src), x1 = *reinterpret_cast<const float4 *>(src + 4);
+          v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        } else {
+          unpack8(c, kv, head_row0 + tok, gi, v);
+          if (had && gi == 0) {
+            const float s = static_cast<const float *>(c.scale[kv])[head_row0 + tok];
+            (kv ? vs : ks)[t] = s;
+          }
+        }
+      }
+      if (kv == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) Ks[t * (D + 1) + gi * 8 + i] = v[i];
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) Vs[t * D + gi * 8 + i] = v[i];
+      }
+    }
+    __syncthreads();
+    if (!row_ok) continue;
+
+    // Scores: lane handles tokens lane, lane + 32, ...
+    constexpr int TPL = T / 32;
+    float s[TPL];
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < TPL; ++j) {
+      const int t = lane + 32 * j;
+      const int tok = tb + t;
+      float acc = 0.0f;
+      const float *kr = Ks + t * (D + 1);
+      const float *qr = Qs + warp * D;
+#pragma unroll 8
+      for (int d = 0; d < D; ++d) acc = fmaf(qr[d], kr[d], acc);
+      float sc;
+      if (had && !is_win) {
+        sc = a.scale * sq * ks[t] * acc;       // acc is the exact integer dot
+      } else {
+        sc = a.scale * acc;
+      }
+      const bool vis = t < nt && tok <= lim;
+      s[j] = vis ? sc : -INFINITY;
+      tmax = fmaxf(tmax, s[j]);
+    }
+#pragma unroll
+    for (int mk = 16; mk; mk >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, mk));
+    if (tmax == -INFINITY) continue;             // nothing visible for this row in the sub-tile
+    const float m_new = fmaxf(m, tmax);
+    const float corr = __expf(m - m_new);        // m = -inf -> 0
+    l *= corr;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) o[i] *= corr;
+    m = m_new;
+    float p[TPL];
+    float psum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < TPL; ++j) {
+      p[j] = s[j] == -INFINITY ? 0.0f : __expf(s[j] - m);
+      psum += p[j];
+      if (had && !is_win) p[j] *= vs[lane + 32 * j];    // fold the V token scale into p
+    }
+#pragma unroll
+    for (int mk = 16; mk; mk >>= 1) psum += __shfl_xor_sync(0xffffffffu, psum, mk);
+    l += psum;
+    // o[d] += sum_t p_t V[t][d]; lane owns dims lane + 32 i.
+#pragma unroll
+    for (int j = 0; j < TPL; ++j) {
+      for (int src = 0; src < 32; ++src) {
+        const float pt = __shfl_sync(0xffffffffu, p[j], src);
+        const float *vr = Vs + (src + 32 * j) * D;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) o[i] = fmaf(pt, vr[lane + 32 * i], o[i]);
+      }
+    }
+  }
+  if (!row_ok || t0 > lim) return;               // this row does not see the chunk
+  const size_t pi = grow * a.C + chunk_id;
+  if (lane == 0) {
+    a.part_m[pi] = m;
+    a.part_l[pi] = l;
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) a.part_o[pi * D + lane + 32 * i] = o[i];
+}
+
+// Phase 2: one CTA of 8 warps per query row; warps split the chunks, lanes split D.
+template <int D>
+__global__ void __launch_bounds__(256) attend_reduce_kernel(AttendArgs a) {
+  constexpr int VPL = D / 32;
+  __shared__ float sm_m[8], sm_l[8];
+  __shared__ __align__(16) float sm_o[8][D];
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+  const size_t grow = blockIdx.x;                       // (b * Hq + h) * n_q + i
+  const int qi = (int)(grow % a.n_q);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lim = row_limit(a, qi);
+  // chunks this row sees
+  int nc = 0;
+  for (int c = 0; c < a.C; ++c) {
+    int t0, t1;
+    chunk_range(a, c, t0, t1);
+    if (t0 <= lim && t1 > t0) nc = c + 1;
+  }
+  float M = -INFINITY;
+  for (int c = warp; c < nc; c += 8) {
+    int t0, t1;
+    chunk_range(a, c, t0, t1);
+    if (t0 <= lim && t1 > t0) M = fmaxf(M, a.part_m[grow * a.C + c]);
+  }
+  float L = 0.0f, O[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
+  // per-warp max first, then block max
+  if (lane == 0) sm_m[warp] = M;
+  __syncthreads();
+  M = sm_m[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, sm_m[w]);
+  for (int c = warp; c < nc; c += 8) {
+    int t0, t1;
+    chunk_range(a, c, t0, t1);
+    if (!(t0 <= lim && t1 > t0)) continue;
+    const size_t pi = grow * a.C + c;
+    const float w = __expf(a.part_m[pi] - M);
+    L = fmaf(a.part_l[pi], w, L);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) O[i] = fmaf(a.part_o[pi * D + lane + 32 * i], w, O[i]);
+  }
+  if (lane == 0) sm_l[warp] = L;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) sm_o[warp][lane + 32 * i] = O[i];
+  __syncthreads();
+  if (warp != 0) return;
+  float Lt = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) Lt += sm_l[w];
+  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+  if (a.cache.layout == KVQ_HAD_INT4) {
+    // un-rotate: out = FWHT(O) / sqrt(D); lane holds VPL consecutive dims
+    float x[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) acc += sm_o[w][lane * VPL + i];
+      x[i] = acc * inv;
+    }
+    warp_fwht<VPL>(x, lane);
+    const float cD = inv_sqrt_dim(D);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) a.out[grow * D + lane * VPL + i] = x[i] * cD;
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) acc += sm_o[w][lane + 32 * i];
+      a.out[grow * D + lane + 32 * i] = acc * inv;
+    }
+  }
+}
+
+// Hadamard query preparation: one warp per query row.
+template <int V>
+__global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows) {
+  const int lane = threadIdx.x & 31;
+  const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (r >= rows) return;
+  constexpr int D = V * 32;
+  float x[V];
+  if (V == 4) load4_f32(a.q, a.q_dtype, (size_t)r * D + lane * 4, x);
+  else load8_f32(a.q, a.q_dtype, (size_t)r * D + lane * 8, x);
+  warp_fwht<V>(x, lane);
+  const float cD = inv_sqrt_dim(D);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    x[i] = __fmul_rn(x[i], cD);
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    int q = 0;
+    if (s > 0.0f) q = (int)fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.0f), 127.0f);
+    a.q8[(size_t)r * D + lane * V + i] = (int8_t)q;
+    a.q_rot[(size_t)r * D + lane * V + i] = x[i];
+  }
+  if (lane == 0) a.s_q[r] = s;
+}
+
+// Debug hook: exact int32 body scores. One CTA of 128 threads per (query row, 128 tokens);
+// warp 0 first prepares the row (FWHT, int8 codes) into shared memory.
+template <int V>
+__global__ void __launch_bounds__(128) debug_scores_kernel(CacheView c, const void *q, int q_dtype, int Hq,
+                                                           int n_q, int n_body, int32_t *scores,
+                                                           float *s_q_out) {
+  constexpr int D = V * 32;
+  __shared__ int q8s[D];
+  const int row = blockIdx.y;                    // (b * Hq + h) * n_q + i
+  const int gqa = Hq / c.H;
+  const int b = row / (Hq * n_q);
+  const int h = (row / n_q) % Hq;
+  const int kvh = h / gqa;
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float x[V];
+    if (V == 4) load4_f32(q, q_dtype, (size_t)row * D + lane * 4, x);
+    else load8_f32(q, q_dtype, (size_t)row * D + lane * 8, x);
+    warp_fwht<V>(x, lane);
+    const float cD = inv_sqrt_dim(D);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      x[i] = __fmul_rn(x[i], cD);
+      amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      int qq = 0;
+      if (s > 0.0f) qq = (int)fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.0f), 127.0f);
+      q8s[lane * V + i] = qq;
+    }
+    if (lane == 0 && blockIdx.x == 0) s_q_out[row] = s;
+  }
+  __syncthreads();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n_body) return;
+  const uint8_t *p = c.payload[0] + ((size_t)(b * c.H + kvh) * c.cap + t) * (size_t)c.row_bytes;
+  int acc = 0;
+  for (int g = 0; g < D / 8; ++g) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(p + g * 4);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += q8s[g * 8 + i] * ((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8);
+  }
+  scores[(size_t)row * n_body + t] = acc;
+}
+
+template <int D, int T>
+cudaError_t launch_generic_dt(const AttendArgs &a, cudaStream_t st) {
+  const size_t smem = sizeof(float) * ((size_t)T * (D + 1) + (size_t)T * D + kRowsPerCta * D + 2 * T);
+  cudaError_t e = cudaFuncSetAttribute(attend_generic_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int R = a.gqa * a.n_q;
+  dim3 grid(a.C, a.cache.B * a.cache.H, (R + kRowsPerCta - 1) / kRowsPerCta);
+  attend_generic_kernel<D, T><<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st) {
+  return a.cache.D == 128 ? launch_generic_dt<128, 64>(a, st) : launch_generic_dt<256, 32>(a, st);
+}
+
+cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl) {
+  const unsigned rows = (unsigned)((size_t)a.cache.B * a.Hq * a.n_q);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (a.cache.D == 128) return cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128>, a);
+  return cudaLaunchKernelEx(&cfg, attend_reduce_kernel<256>, a);
+}
+
+cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st) {
+  const int rows = a.cache.B * a.Hq * a.n_q;
+  const unsigned blocks = (unsigned)(((size_t)rows * 32 + 255) / 256);
+  if (a.cache.D == 128) had_prep_kernel<4><<<blocks, 256, 0, st>>>(a, rows);
+  else had_prep_kernel<8><<<blocks, 256, 0, st>>>(a, rows);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, int Hq, int n_q, int kv_len,
+                                int n_body, int32_t *scores, float *s_q, cudaStream_t st) {
+  (void)kv_len;
+  const int rows = c.B * Hq * n_q;
+  dim3 grid((unsigned)max(1, (n_body + 127) / 128), (unsigned)rows);
+  if (c.D == 128) debug_scores_kernel<4><<<grid, 128, 0, st>>>(c, q, q_dtype, Hq, n_q, n_body, scores, s_q);
+  else debug_scores_kernel<8><<<grid, 128, 0, st>>>(c, q, q_dtype, Hq, n_q, n_body, scores, s_q);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

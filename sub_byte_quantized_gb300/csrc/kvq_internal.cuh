@@ -1,0 +1,134 @@
+// Internal declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kBlock = 32;          // values per Q4_0 / Q6_0 / asymmetric block
+
+// Device-side view of a cache; index 0 = K, 1 = V.
+struct CacheView {
+  int layout, B, H, D, cap, n_recent;
+  int row_bytes;
+  uint8_t *payload[2];
+  void *scale[2];
+  __half *zero[2];
+  float *ring[2];
+};
+
+// Arguments of one decode-attention call, resolved on the host.
+struct AttendArgs {
+  CacheView cache;
+  const void *q;
+  int q_dtype;
+  int Hq, gqa, n_q;         // query heads, H_q / H_kv, query rows per head
+  int kv_len, n_win, n_body; // n_win = HAD ring tokens in use, n_body = kv_len - n_win
+  int causal, q_pos0;
+  float scale;              // attention scale alpha
+  int chunk, n_chunks;      // body chunks = ceil(n_body / chunk); + 1 window chunk if n_win
+  int C;                    // total partials per row
+  float *out;
+  // workspace regions
+  float *part_m, *part_l, *part_o;   // [rows][C], [rows][C], [rows][C][D]
+  int8_t *q8;                         // HAD: [rows][D]
+  float *s_q, *q_rot;                 // HAD: [rows], [rows][D]
+};
+
+// Launchers (return cudaGetLastError() after enqueueing).
+cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype,
+                         int n_new, int pos0, cudaStream_t st);
+cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st);
+cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st);
+cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl);
+cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, int Hq, int n_q,
+                                int kv_len, int n_body, int32_t *scores, float *s_q,
+                                cudaStream_t st);
+// Tensor-core phase 1 for the shapes it covers; returns cudaErrorNotSupported when it does not
+// cover the call (the caller then uses the generic kernel).
+bool mma_supported(const AttendArgs &a);
+cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st);
+
+// ----------------------------------------------------------------- device helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Load 8 consecutive input elements starting at element index `e` (8-aligned) as f32.
+__device__ __forceinline__ void load8_f32(const void *base, int dtype, size_t e, float v[8]) {
+  if (dtype == KVQ_F32) {
+    const float4 *p = reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e);
+    float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(base) + e));
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (dtype == KVQ_BF16) {
+        v[2 * k] = bf16_bits_to_f32(u[k] & 0xFFFFu);
+        v[2 * k + 1] = bf16_bits_to_f32(u[k] >> 16);
+      } else {
+        v[2 * k] = __half2float(__ushort_as_half((unsigned short)(u[k] & 0xFFFFu)));
+        v[2 * k + 1] = __half2float(__ushort_as_half((unsigned short)(u[k] >> 16)));
+      }
+    }
+  }
+}
+
+// Load 4 consecutive elements (4-aligned) as f32.
+__device__ __forceinline__ void load4_f32(const void *base, int dtype, size_t e, float v[4]) {
+  if (dtype == KVQ_F32) {
+    float4 a = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(base) + e));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  } else {
+    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(base) + e));
+    const uint32_t u[2] = {w.x, w.y};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (dtype == KVQ_BF16) {
+        v[2 * k] = bf16_bits_to_f32(u[k] & 0xFFFFu);
+        v[2 * k + 1] = bf16_bits_to_f32(u[k] >> 16);
+      } else {
+        v[2 * k] = __half2float(__ushort_as_half((unsigned short)(u[k] & 0xFFFFu)));
+        v[2 * k + 1] = __half2float(__ushort_as_half((unsigned short)(u[k] >> 16)));
+      }
+    }
+  }
+}
+
+// fp32 nearest to 1/sqrt(D) for the orthonormal Hadamard rotation (D = 128 or 256).
+__device__ __forceinline__ float inv_sqrt_dim(int D) {
+  return D == 128 ? 0x1.6a09e6p-4f : 0x1.0p-4f;
+}
+
+// In-warp unnormalised FWHT of a D-vector held as V = D/32 consecutive values per lane
+// (element lane*V + i). Butterflies (a, b) -> (a + b, a - b) with half-span 1, 2, ..., D/2 in
+// ascending order; every add/subtract rounded once.
+template <int V>
+__device__ __forceinline__ void warp_fwht(float (&x)[V], int lane) {
+#pragma unroll
+  for (int h = 1; h < V; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = __fadd_rn(a, b);
+        x[i + h] = __fsub_rn(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+      x[i] = (lane & m) ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+  }
+}
+
+}  // namespace kvq

@@ -1,0 +1,210 @@
+// Store (append) kernels: quantise new K/V rows and write them into the packed cache.
+//
+// Bit-exactness: every value is produced by one IEEE float32 operation at a time
+// (__fdiv_rn / __fsub_rn / __fmul_rn, rintf = round half to even, __float2half_rn), and this
+// file is compiled with -fmad=false so no multiply-add is ever contracted.
+//
+// Q4_0 / Q6_0 / asymmetric: 4 threads per 32-value block, 8 values per thread; the block's
+// amax (or min/max) is reduced over those 4 lanes with shuffles. Loads are 16-byte vectors,
+// stores are the thread's 4 payload bytes (+ 2 high-plane bytes for Q6_0).
+// Hadamard int4: one warp per token row; the FWHT runs in registers and shuffles.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr float kF16Max = 65504.0f;
+
+struct StoreGeom {
+  int B, H, D, cap, n_new, pos0, row_bytes, nb;
+  long long rows_per_tensor;   // B * H * n_new
+};
+
+// Decompose a global row id into (tensor, input row offset, cache row).
+__device__ __forceinline__ void row_coords(const StoreGeom &g, long long r, int &kv, long long &in_row,
+                                           long long &cache_row, int &j) {
+  kv = r >= g.rows_per_tensor ? 1 : 0;
+  const long long rr = r - (long long)kv * g.rows_per_tensor;
+  const long long bh = rr / g.n_new;
+  j = (int)(rr - bh * g.n_new);
+  in_row = rr;
+  cache_row = bh * g.cap + g.pos0 + j;
+}
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+__device__ __forceinline__ float quad_min(float v) {
+  v = fminf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fminf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+
+__device__ __forceinline__ __half f16_sat(float x) {
+  return __float2half_rn(fminf(fmaxf(x, -kF16Max), kF16Max));
+}
+
+// q = clamp(rint(x / s), lo, hi), or 0 when s == 0.
+__device__ __forceinline__ int sym_code(float x, float s, int lo, int hi) {
+  if (!(s > 0.0f)) return 0;
+  const float r = rintf(__fdiv_rn(x, s));
+  return (int)fminf(fmaxf(r, (float)lo), (float)hi);
+}
+
+// LAYOUT: KVQ_Q4_0, KVQ_Q6_0 or KVQ_ASYM4_G32.
+template <int LAYOUT>
+__global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const void *__restrict__ k_new,
+                                                          const void *__restrict__ v_new, int dtype,
+                                                          StoreGeom g) {
+  const int tpr = g.D / 8;                                 // threads per row
+  const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long r = gt / tpr;
+  const int tr = (int)(gt - r * tpr);                      // thread within row
+  // Threads past the last row still take part in the quad shuffles (full-warp masks) but load
+  // and store nothing.
+  const bool valid = r < 2 * g.rows_per_tensor;
+  int kv = 0, j = 0;
+  long long in_row = 0, cache_row = 0;
+  if (valid) row_coords(g, r, kv, in_row, cache_row, j);
+  const int blk = tr >> 2, lb = tr & 3;
+
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (valid) load8_f32(kv ? v_new : k_new, dtype, (size_t)in_row * g.D + (size_t)tr * 8, v);
+  uint8_t *prow = c.payload[kv] + (size_t)cache_row * g.row_bytes;
+  __half *srow = static_cast<__half *>(c.scale[kv]) + (size_t)cache_row * g.nb;
+
+  if (LAYOUT == KVQ_ASYM4_G32) {
+    float mn = v[0], mx = v[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) { mn = fminf(mn, v[i]); mx = fmaxf(mx, v[i]); }
+    mn = quad_min(mn);
+    mx = quad_max(mx);
+    const __half sh = f16_sat(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+    const __half zh = f16_sat(mn);
+    const float s = __half2float(sh), z = __half2float(zh);
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int q = 0;
+      if (s > 0.0f) {
+        const float rr = rintf(__fdiv_rn(__fsub_rn(v[i], z), s));
+        q = (int)fminf(fmaxf(rr, 0.0f), 15.0f);
+      }
+      w |= (uint32_t)q << (4 * i);
+    }
+    if (!valid) return;
+    *reinterpret_cast<uint32_t *>(prow + blk * 16 + lb * 4) = w;
+    if (lb == 0) {
+      srow[blk] = sh;
+      c.zero[kv][(size_t)cache_row * g.nb + blk] = zh;
+    }
+    return;
+  }
+
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = quad_max(amax);
+  if (LAYOUT == KVQ_Q4_0) {
+    const __half sh = f16_sat(__fdiv_rn(amax, 8.0f));
+    const float s = __half2float(sh);
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w |= ((uint32_t)sym_code(v[i], s, -8, 7) & 0xFu) << (4 * i);
+    if (!valid) return;
+    *reinterpret_cast<uint32_t *>(prow + blk * 16 + lb * 4) = w;
+    if (lb == 0) srow[blk] = sh;
+  } else {  // Q6_0
+    const __half sh = f16_sat(__fdiv_rn(amax, 32.0f));
+    const float s = __half2float(sh);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t u = (uint32_t)sym_code(v[i], s, -32, 31) & 0x3Fu;
+      lo |= (u & 0xFu) << (4 * i);
+      hi |= ((u >> 4) & 0x3u) << (2 * i);      // values 4k..4k+3 -> byte k, bits 0,2,4,6
+    }
+    if (!valid) return;
+    uint8_t *bp = prow + blk * 24;
+    *reinterpret_cast<uint32_t *>(bp + lb * 4) = lo;
+    *reinterpret_cast<uint16_t *>(bp + 16 + lb * 2) = (uint16_t)hi;
+    if (lb == 0) srow[blk] = sh;
+  }
+}
+
+// Hadamard int4: one warp per token row, V = D/32 values per lane.
+template <int V>
+__global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void *__restrict__ k_new,
+                                                        const void *__restrict__ v_new, int dtype,
+                                                        StoreGeom g) {
+  const int lane = threadIdx.x & 31;
+  const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (r >= 2 * g.rows_per_tensor) return;                  // whole warp exits together
+  int kv, j;
+  long long in_row, cache_row;
+  row_coords(g, r, kv, in_row, cache_row, j);
+  float x[V];
+  const void *src = kv ? v_new : k_new;
+  if (V == 4) {
+    load4_f32(src, dtype, (size_t)in_row * g.D + lane * 4, x);
+  } else {
+    load8_f32(src, dtype, (size_t)in_row * g.D + lane * 8, x);
+  }
+  warp_fwht<V>(x, lane);
+  const float cD = inv_sqrt_dim(g.D);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    x[i] = __fmul_rn(x[i], cD);
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  const float s = __fdiv_rn(amax, 7.0f);
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < V; ++i) w |= ((uint32_t)sym_code(x[i], s, -7, 7) & 0xFu) << (4 * i);
+  uint8_t *prow = c.payload[kv] + (size_t)cache_row * g.row_bytes;
+  if (V == 4) {
+    *reinterpret_cast<uint16_t *>(prow + lane * 2) = (uint16_t)w;
+  } else {
+    *reinterpret_cast<uint32_t *>(prow + lane * 4) = w;
+  }
+  if (lane == 0) static_cast<float *>(c.scale[kv])[cache_row] = s;
+  // Exact-f32 ring of the newest tokens: only the last min(n_new, n_recent) rows of this call,
+  // so no two rows of one call write the same slot.
+  if (c.n_recent > 0 && j >= g.n_new - c.n_recent) {
+    const long long bh = cache_row / g.cap;
+    float *dst = c.ring[kv] + ((size_t)bh * c.n_recent + (size_t)((g.pos0 + j) % c.n_recent)) * g.D + lane * V;
+#pragma unroll
+    for (int i = 0; i < V; i += 4)
+      *reinterpret_cast<float4 *>(dst + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype, int n_new,
+                         int pos0, cudaStream_t st) {
+  StoreGeom g;
+  g.B = c.B; g.H = c.H; g.D = c.D; g.cap = c.cap; g.n_new = n_new; g.pos0 = pos0;
+  g.row_bytes = c.row_bytes; g.nb = c.D / kBlock;
+  g.rows_per_tensor = (long long)c.B * c.H * n_new;
+  const long long rows = 2 * g.rows_per_tensor;
+  if (c.layout == KVQ_HAD_INT4) {
+    const long long blocks = (rows * 32 + 255) / 256;
+    if (c.D == 128) store_had_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+    else store_had_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+  } else {
+    const long long threads = rows * (c.D / 8);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    switch (c.layout) {
+      case KVQ_Q4_0: store_block_kernel<KVQ_Q4_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
+      case KVQ_Q6_0: store_block_kernel<KVQ_Q6_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
+      default: store_block_kernel<KVQ_ASYM4_G32><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,99 @@
+"""The C ABI library loads and exports every entry point include/kvq.h declares; host-side
+validation rejects bad arguments before touching the device (no GPU needed for these)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sub_byte_quantized_gb300 import _lib
+    if not os.path.exists(_lib.LIB_PATH):
+        from sub_byte_quantized_gb300.build import build_library
+        build_library()
+    return _lib.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    names = header_functions()
+    assert len(names) >= 11
+    from sub_byte_quantized_gb300._lib import EXPORTS
+    assert sorted(EXPORTS) == names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_sizes(L):
+    assert L.kvq_row_bytes(0, 128) == 64 and L.kvq_row_bytes(1, 256) == 192
+    assert L.kvq_row_bytes(2, 128) == 64 and L.kvq_row_bytes(3, 128) == 64
+    assert L.kvq_row_bytes(0, 96) == 0 and L.kvq_row_bytes(9, 128) == 0
+    out = (C.c_size_t * 4)()
+    assert L.kvq_cache_bytes(0, 1, 8, 128, 131072, 0, out) == 0
+    # 128K-token Llama-70B layer: 64 B payload + 8 B scales per token per kv head, K or V
+    assert out[0] == 8 * 131072 * 64 and out[1] == 8 * 131072 * 8 and out[2] == 0 and out[3] == 0
+    assert L.kvq_cache_bytes(2, 8, 8, 128, 4096, 64, out) == 0
+    assert out[1] == 8 * 8 * 4096 * 4 and out[3] == 8 * 8 * 64 * 128 * 4
+    assert L.kvq_cache_bytes(3, 1, 8, 128, 16, 0, out) == 0 and out[2] == 8 * 16 * 4 * 2
+
+
+def _cache(layout=0, D=128, cap=64, ptr=4096):
+    from sub_byte_quantized_gb300._lib import KvqCache
+    return KvqCache(layout, 1, 2, D, cap, 0, ptr, ptr, ptr, ptr, ptr, ptr, None, None)
+
+
+def test_validation_without_device(L):
+    from sub_byte_quantized_gb300._lib import KvqCache
+    p = C.byref
+    # NULL cache
+    assert L.kvq_store_q4_0(None, 16, 16, 1, 1, 0, None) == 1
+    assert b"NULL" in L.kvq_last_error()
+    # wrong layout for this store
+    c = _cache(layout=1)
+    assert L.kvq_store_q4_0(p(c), 16, 16, 1, 1, 0, None) == 4
+    # capacity
+    c = _cache()
+    assert L.kvq_store_q4_0(p(c), 16, 16, 1, 10, 60, None) == 3
+    # misaligned input
+    assert L.kvq_store_q4_0(p(c), 17, 16, 1, 1, 0, None) == 5
+    # bad head_dim
+    c = _cache(D=96)
+    assert L.kvq_store_q4_0(p(c), 16, 16, 1, 1, 0, None) == 2
+    # misaligned plane
+    c = _cache(ptr=4100)
+    assert L.kvq_store_q4_0(p(c), 16, 16, 1, 1, 0, None) == 5
+    # n_new == 0 is a no-op
+    c = _cache()
+    assert L.kvq_store_q4_0(p(c), None, None, 1, 0, 0, None) == 0
+    # attention: kv_len 0, beyond capacity, H_q not a multiple of H_kv, causal bounds, workspace
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 0, 0, 0, 1.0, 0, 16, 256, 1 << 20, None) == 1
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 65, 0, 0, 1.0, 0, 16, 256, 1 << 20, None) == 3
+    assert L.kvq_decode_attend(p(c), 16, 1, 7, 1, 8, 0, 0, 1.0, 0, 16, 256, 1 << 20, None) == 2
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 4, 8, 1, 6, 1.0, 0, 16, 256, 1 << 20, None) == 1
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 8, 0, 0, 1.0, 100, 16, 256, 1 << 20, None) == 2
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 16, None) == 7
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 128 + 16, 1 << 20, None) == 5
+    assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 8, 0, 0, float("nan"), 0, 16, 256, 1 << 20, None) == 1
+    # debug scores only for the Hadamard layout
+    assert L.kvq_debug_scores_i32(p(c), 16, 1, 8, 1, 8, 16, 16, None) == 4
+    # n_recent belongs to the Hadamard layout only
+    c = KvqCache(0, 1, 2, 128, 64, 8, 4096, 4096, 4096, 4096, None, None, None, None)
+    assert L.kvq_store_q4_0(p(c), 16, 16, 1, 1, 0, None) == 4
+    assert L.kvq_status_string(7) == b"workspace too small"
+
+
+def test_workspace_size_formula(L):
+    c = _cache(cap=131072)
+    # rows = 1*8*1, chunks = 256: m + l + o, each region rounded up to 256 bytes
+    ws = L.kvq_attend_workspace_bytes(C.byref(c), 8, 1, 131072, 0)
+    rows, Cc = 8, 256
+    assert ws == 2 * ((rows * Cc * 4 + 255) // 256 * 256) + (rows * Cc * 128 * 4 + 255) // 256 * 256

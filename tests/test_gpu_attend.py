@@ -1,0 +1,176 @@
+"""Decode attention through the C ABI vs the oracle's float64 attention.
+
+Tolerance: |gpu - oracle| <= 2e-3 + 1e-3 * |oracle| elementwise. Hadamard integer-domain scores
+and the int8 query scales are compared bit-exactly.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import sub_byte_quantized_gb300 as kvq
+from oracle import attention as OA
+from synth import WORKLOADS, make_inputs
+from tests.gpu_helpers import check_close, device_inputs, fill_both, planes_equal
+
+pytestmark = pytest.mark.gpu
+
+
+def run_case(w, kv_len=None, n_q=None, chunk=0, q_dtype=None, fill=None, check_planes=True):
+    inp = make_inputs(w, kv_len=kv_len, n_q=n_q)
+    S = inp["k"].shape[2]
+    dc, oc, d = fill_both(w, inp, fill=fill)
+    q = d["q"]
+    qf = inp["q"]
+    if q_dtype == "f32":
+        q = q.float().contiguous()
+    elif q_dtype == "f16":
+        q = q.half().contiguous()
+        qf = q.float().cpu().numpy()
+    n_q_rows = inp["q"].shape[2]
+    q_pos0 = S - n_q_rows if w.causal else 0
+    out = kvq.decode_attend(dc, q, S, causal=w.causal, q_pos0=q_pos0, attn_scale=w.alpha, chunk=chunk)
+    torch.cuda.synchronize()
+    if check_planes:
+        planes_equal(dc, oc, S)
+    ref = oc.attend(qf, w.alpha, S, causal=w.causal, q_pos0=q_pos0)
+    if isinstance(ref, tuple):
+        ref = ref[0]
+    return check_close(out.cpu().numpy(), ref, w.name), (dc, oc, d, inp, out)
+
+
+@pytest.mark.parametrize("name,kv_len,n_q,fill", [
+    ("c1_q4_0_tiny", None, None, None),
+    ("c2_q4_0_llama3_8b", 1500, None, 1499),
+    ("c3_had_int4_decode", 1100, None, 1099),
+    ("c3_had_int4_prefill", 1100, 64, 1036),
+    ("c4_q6_0_gemma", 1300, None, 1299),
+    ("c5_q4_0_llama70b_128k", 2100, None, 2099),
+    ("c5_asym4_g32_llama70b_128k", 2100, None, 2099),
+])
+def test_workloads_reduced(name, kv_len, n_q, fill):
+    """Every workload at a size the oracle finishes in seconds: several 512-token chunks plus a
+    ragged tail, filled in bulk and then appended like the full workload."""
+    w = WORKLOADS[name]
+    if name == "c3_had_int4_prefill":
+        w = w.scaled(q_pos0=kv_len - n_q)
+    run_case(w, kv_len, n_q, fill=fill)
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 512, 1024])
+def test_chunk_sizes(chunk):
+    run_case(WORKLOADS["c2_q4_0_llama3_8b"].scaled(batch=1), 1000, chunk=chunk)
+
+
+@pytest.mark.parametrize("q_dtype", ["f32", "f16"])
+@pytest.mark.parametrize("layout", ["q4_0", "q6_0", "had_int4", "asym4_g32"])
+def test_query_dtypes(layout, q_dtype):
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=1, n_recent=32 if layout == "had_int4" else 0)
+    run_case(w, 700, q_dtype=q_dtype)
+
+
+@pytest.mark.parametrize("layout", ["q4_0", "q6_0", "had_int4", "asym4_g32"])
+@pytest.mark.parametrize("kv_len", [1, 2, 63, 64, 65, 513])
+def test_edge_lengths(layout, kv_len):
+    w = WORKLOADS["c1_q4_0_tiny"].scaled(layout=layout, n_recent=16 if layout == "had_int4" else 0)
+    run_case(w, kv_len, chunk=64)
+
+
+def test_hadamard_window_covers_everything():
+    w = WORKLOADS["c3_had_int4_decode"].scaled(batch=2, n_recent=512)
+    run_case(w, 300)                      # n_recent >= kv_len: all tokens exact f32
+
+
+def test_hadamard_no_window():
+    w = WORKLOADS["c3_had_int4_decode"].scaled(batch=2, n_recent=0)
+    run_case(w, 777)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_causal_prefill_rows(D):
+    """Causal rows whose limits cross chunk boundaries, including row 0 at position 0."""
+    for layout in ("q4_0", "had_int4", "q6_0"):
+        w = WORKLOADS["c3_had_int4_prefill"].scaled(layout=layout, head_dim=D, batch=1,
+                                                    n_recent=8 if layout == "had_int4" else 0)
+        run_case(w.scaled(q_pos0=0), kv_len=200, n_q=200, fill=0, chunk=64)
+        run_case(w.scaled(q_pos0=100), kv_len=300, n_q=200, fill=100, chunk=64)
+
+
+def test_hadamard_integer_scores_bit_exact():
+    w = WORKLOADS["c3_had_int4_prefill"]
+    S, nq = 1100, 64
+    inp = make_inputs(w, kv_len=S, n_q=nq)
+    dc, oc, d = fill_both(w, inp, fill=S - nq)
+    scores, s_q = kvq.debug_scores_i32(dc, d["q"], S)
+    torch.cuda.synchronize()
+    _, ref_scores = oc.attend(inp["q"], w.alpha, S, causal=True, q_pos0=S - nq)
+    _, ref_sq, _ = OA.prep_q_hadamard(inp["q"])
+    assert np.array_equal(s_q.cpu().numpy().view(np.uint32), ref_sq.view(np.uint32))
+    assert np.array_equal(scores.cpu().numpy().astype(np.int64), ref_scores)
+
+
+def test_causal_limit_equals_truncated_cache():
+    """attend(causal, row limit L) == attend(kv_len = L + 1) bitwise (same chunking)."""
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(batch=1)
+    S = 1200
+    inp = make_inputs(w, kv_len=S, n_q=1)
+    dc, oc, d = fill_both(w, inp)
+    q = d["q"]
+    for L in (0, 511, 512, 700, 1199):
+        a = kvq.decode_attend(dc, q, L + 1, causal=True, q_pos0=L, attn_scale=w.alpha)
+        b = kvq.decode_attend(dc, q, L + 1, causal=False, attn_scale=w.alpha)
+        c = kvq.decode_attend(dc, q, S, causal=True, q_pos0=L, attn_scale=w.alpha) if L + 1 <= S else None
+        torch.cuda.synchronize()
+        assert torch.equal(a, b)
+        ref = oc.attend(inp["q"], w.alpha, L + 1)
+        check_close(c.cpu().numpy(), ref, f"limit {L}")
+
+
+def test_repeatable():
+    w = WORKLOADS["c5_q4_0_llama70b_128k"]
+    inp = make_inputs(w, kv_len=3000)
+    dc, oc, d = fill_both(w, inp)
+    a = kvq.decode_attend(dc, d["q"], 3000)
+    b = kvq.decode_attend(dc, d["q"], 3000)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _oracle_rows_for_kv_head(w, inp, kvh, kv_len, q_pos0=0):
+    """Oracle output of the query heads that read kv head `kvh`, from that head's cache only."""
+    g = w.gqa
+    sub = {n: inp[n][:, kvh:kvh + 1] for n in ("k", "v")}
+    oc = OA.OracleCache(w.layout, inp["k"].shape[0], 1, w.head_dim, kv_len, n_recent=w.n_recent)
+    n_fill = w.n_fill
+    for lo, hi in ((0, n_fill), (n_fill, kv_len)):
+        if hi > lo:
+            oc.store(sub["k"][:, :, lo:hi], sub["v"][:, :, lo:hi], lo)
+    q = inp["q"][:, kvh * g:(kvh + 1) * g]
+    ref = oc.attend(q, w.alpha, kv_len, causal=w.causal, q_pos0=q_pos0)
+    return ref[0] if isinstance(ref, tuple) else ref
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["c1_q4_0_tiny", "c2_q4_0_llama3_8b", "c3_had_int4_decode", "c3_had_int4_prefill",
+                                  "c4_q6_0_gemma", "c5_q4_0_llama70b_128k", "c5_asym4_g32_llama70b_128k"])
+def test_workloads_full_size_sampled(name):
+    """Full-size workloads in the benchmark's launch configuration (bulk fill, append, chunk
+    512); the oracle recomputes every query head of two kv heads (first and last)."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    B, H, S, D = inp["k"].shape
+    d = device_inputs(inp)
+    dc = kvq.KVCache(w.layout, B, H, D, S, n_recent=w.n_recent)
+    n_fill = w.n_fill
+    for lo, hi in ((0, n_fill), (n_fill, S)):
+        if hi > lo:
+            kvq.store(dc, d["k"][:, :, lo:hi].contiguous(), d["v"][:, :, lo:hi].contiguous(), lo)
+    n_q = inp["q"].shape[2]
+    q_pos0 = S - n_q if w.causal else 0
+    out = kvq.decode_attend(dc, d["q"], S, causal=w.causal, q_pos0=q_pos0, attn_scale=w.alpha).cpu().numpy()
+    for kvh in sorted({0, H - 1}):
+        ref = _oracle_rows_for_kv_head(w, inp, kvh, S, q_pos0)
+        got = out[:, kvh * w.gqa:(kvh + 1) * w.gqa]
+        check_close(got, ref, f"{name} kv head {kvh}")
