@@ -162,6 +162,15 @@ kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q
                                 int32_t n_q_heads, int32_t n_q, int32_t kv_len,
                                 int32_t *scores_out, float *s_q_out, kvq_stream_t stream);
 
+/*
+ * Measurement hook (no counterpart on the pages): while both events are non-NULL, every
+ * kvq_decode_attend call made by this thread records `phase1_begin` on its stream right before
+ * the phase-1 launch and `phase1_end` right after it, so a caller can time the streaming kernel
+ * alone with cudaEventElapsedTime. The events are cudaEvent_t handles created by the caller;
+ * passing NULL for either disables recording. Thread-local; returns KVQ_OK.
+ */
+kvq_status kvq_profile_phase1_events(void *phase1_begin, void *phase1_end);
+
 /* Static description of a status code. */
 const char *kvq_status_string(int32_t status);
 

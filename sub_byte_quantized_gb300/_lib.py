@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ESHAPE", 3: "KVQ_ECAPACITY
 # Every symbol the header declares (checked by the CPU test suite).
 EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0", "kvq_store_hadamard_int4",
            "kvq_store_asym4_g32", "kvq_attend_workspace_bytes", "kvq_decode_attend", "kvq_debug_scores_i32",
-           "kvq_status_string", "kvq_last_error")
+           "kvq_status_string", "kvq_last_error", "kvq_profile_phase1_events")
 
 
 class KvqCache(C.Structure):
@@ -64,6 +64,7 @@ def lib() -> C.CDLL:
     L.kvq_debug_scores_i32.restype = I32
     L.kvq_status_string.argtypes, L.kvq_status_string.restype = [I32], C.c_char_p
     L.kvq_last_error.argtypes, L.kvq_last_error.restype = [], C.c_char_p
+    L.kvq_profile_phase1_events.argtypes, L.kvq_profile_phase1_events.restype = [P, P], I32
     _lib = L
     return L
 

@@ -10,6 +10,7 @@
 namespace {
 
 thread_local char g_last_error[256] = "";
+thread_local cudaEvent_t g_ev_begin = nullptr, g_ev_end = nullptr;
 
 kvq_status fail(kvq_status st, const char *fmt, ...) {
   va_list ap;
@@ -207,7 +208,10 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (a.cache.layout == KVQ_HAD_INT4) e = kvq::launch_had_prep(a, s);
+  const bool prof = g_ev_begin && g_ev_end;
+  if (e == cudaSuccess && prof) e = cudaEventRecord(g_ev_begin, s);
   if (e == cudaSuccess) e = kvq::mma_supported(a) ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
+  if (e == cudaSuccess && prof) e = cudaEventRecord(g_ev_end, s);
   if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
@@ -247,5 +251,11 @@ const char *kvq_status_string(int32_t status) {
 }
 
 const char *kvq_last_error(void) { return g_last_error; }
+
+kvq_status kvq_profile_phase1_events(void *phase1_begin, void *phase1_end) {
+  g_ev_begin = static_cast<cudaEvent_t>(phase1_begin);
+  g_ev_end = static_cast<cudaEvent_t>(phase1_end);
+  return KVQ_OK;
+}
 
 }  // extern "C"

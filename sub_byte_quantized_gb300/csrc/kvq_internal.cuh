@@ -11,6 +11,7 @@
 namespace kvq {
 
 constexpr int kBlock = 32;          // values per Q4_0 / Q6_0 / asymmetric block
+constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-up
 
 // Device-side view of a cache; index 0 = K, 1 = V.
 struct CacheView {
