@@ -209,9 +209,13 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
   cudaError_t e = cudaSuccess;
   if (a.cache.layout == KVQ_HAD_INT4) e = kvq::launch_had_prep(a, s);
   const bool prof = g_ev_begin && g_ev_end;
-  if (e == cudaSuccess && prof) e = cudaEventRecord(g_ev_begin, s);
+  // Under stream capture an event record must be external to become a graph node.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (e == cudaSuccess && prof) e = cudaStreamIsCapturing(s, &cap);
+  const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  if (e == cudaSuccess && prof) e = cudaEventRecordWithFlags(g_ev_begin, s, rec_flags);
   if (e == cudaSuccess) e = kvq::mma_supported(a) ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
-  if (e == cudaSuccess && prof) e = cudaEventRecord(g_ev_end, s);
+  if (e == cudaSuccess && prof) e = cudaEventRecordWithFlags(g_ev_end, s, rec_flags);
   if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;

@@ -1,10 +1,554 @@
-// Tensor-core phase 1 (filled in below as shapes are covered).
+// Tensor-core phase 1 of the split-K decode attention for 4-bit block layouts (Q4_0 and the
+// asymmetric g=32 layout), head_dim 128, up to 8 query rows per kv head (the GQA group times
+// the query rows of the call).
+//
+// Why tensor cores: every kv head is shared by gqa query heads, so per packed K/V element the
+// step does 4*gqa flops (QK and PV); at gqa 8 that is ~57 flops per packed byte, beyond what
+// the CUDA cores sustain at HBM rate. The group is a dense contraction, done with
+// mma.sync.m16n8k16 (f16 in, f32 accumulate):
+//   QK:  S^T[16 tokens][8 rows] += K[16 tokens][16 dims] . Q^T[16 dims][8 rows]
+//   PV:  O^T[16 dims][8 rows]   += V^T[16 dims][16 tokens] . P'^T[16 tokens][8 rows]
+// Exactness: 4-bit codes are exact in f16; queries given in bf16/f16 are exact in f16 after a
+// per-row power-of-two prescale (f32 queries are split into hi + lo f16 parts); the block
+// scale of K (per token and 32-dim block) multiplies each block's f32 partial sum; the block
+// scale of V is folded into the probabilities, P' = p * s_v, split into hi + lo f16 parts.
+//
+// Data movement: each warp owns a contiguous slice of 64-token stages of the chunk and pulls
+// them HBM -> shared memory with 16-byte cp.async (two stages in flight per warp). Payload rows
+// (64 bytes) are placed with a 64-byte XOR swizzle (16-byte column ^= (row / 2) % 4) so that the
+// ldmatrix reads (8 rows x 16 bytes per phase) are bank-conflict free. ldmatrix gives each lane
+// the nibble words of its fragment: plain for K (one token, 8 consecutive dims), transposed for
+// V (two tokens, 4 consecutive dims). The nibbles become f16 pairs with one lop3 (mask + magic
+// exponent 0x6400, the Q4_0 sign flip folded in) and one f16 subtract/fma, all exact.
+//
+// Each CTA handles one chunk of one (batch, kv head); its four warps combine their online
+// softmax states in shared memory and write one (m, l, o) partial per query row.
+#include <cfloat>
+#include <climits>
+
 #include "kvq_internal.cuh"
 
 namespace kvq {
+namespace {
 
-bool mma_supported(const AttendArgs &) { return false; }
+constexpr int kWarps = 4;
+constexpr int kStage = 64;              // tokens per pipeline stage
+constexpr int kD = 128;
+constexpr int kRowBytes = 64;
+constexpr int kOffV = 4096, kOffSK = 8192, kOffSV = 8704, kOffZK = 9216, kOffZV = 9728;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
-cudaError_t launch_attend_mma(const AttendArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+template <bool ASYM>
+__host__ __device__ constexpr int stage_bytes() { return ASYM ? 10240 : 9216; }
+template <bool ASYM>
+__host__ __device__ constexpr int smem_bytes() { return kWarps * 2 * stage_bytes<ASYM>(); }
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+               "{%0,%1,%2,%3};\n"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+template <int LUT>
+__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, %4;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(LUT));
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+// Eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
+// (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the code values: Q4_0 (signed: (n ^ 8) - 8) or
+// the unsigned asymmetric code n.
+template <bool ASYM>
+__device__ __forceinline__ void unpack8(uint32_t w, uint32_t (&o)[4]) {
+  const __half2 one16 = __float2half2_rn(0.0625f);
+  const uint32_t w8 = w >> 8;
+  if (!ASYM) {
+    // (w & mask) ^ (magic | 8-in-each-field): 1024 + (n ^ 8) (or 1024 + 16 (n ^ 8))
+    const __half2 off_lo = __float2half2_rn(-1032.0f), off_hi = __float2half2_rn(-72.0f);
+    o[0] = h2_as_u32(__hadd2(u32_as_h2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u)), off_lo));
+    o[1] = h2_as_u32(__hfma2(u32_as_h2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u)), one16, off_hi));
+    o[2] = h2_as_u32(__hadd2(u32_as_h2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u)), off_lo));
+    o[3] = h2_as_u32(__hfma2(u32_as_h2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u)), one16, off_hi));
+  } else {
+    const __half2 off_lo = __float2half2_rn(-1024.0f), off_hi = __float2half2_rn(-64.0f);
+    o[0] = h2_as_u32(__hadd2(u32_as_h2(lop3<0xea>(w, 0x000F000Fu, 0x64006400u)), off_lo));
+    o[1] = h2_as_u32(__hfma2(u32_as_h2(lop3<0xea>(w, 0x00F000F0u, 0x64006400u)), one16, off_hi));
+    o[2] = h2_as_u32(__hadd2(u32_as_h2(lop3<0xea>(w8, 0x000F000Fu, 0x64006400u)), off_lo));
+    o[3] = h2_as_u32(__hfma2(u32_as_h2(lop3<0xea>(w8, 0x00F000F0u, 0x64006400u)), one16, off_hi));
+  }
+}
+
+__device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
+  const int qi = r % a.n_q;
+  return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+}
+
+// Byte offset of (row, 16-byte column j) inside a swizzled 64-byte-row slab.
+__device__ __forceinline__ uint32_t swz(int row, int j) {
+  return (uint32_t)(row * kRowBytes + ((j ^ ((row >> 1) & 3)) << 4));
+}
+
+template <bool ASYM, bool QSPLIT>
+__global__ void __launch_bounds__(kWarps * 32, 2) attend_mma_kernel(AttendArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
+  const CacheView &cv = a.cache;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int chunk_id = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const int R = a.gqa * a.n_q;
+
+  const int t0 = chunk_id * a.chunk;
+  const int t1 = min(a.n_body, t0 + a.chunk);
+  int cta_lim = -1, min_lim = INT_MAX;
+  for (int r = 0; r < R; ++r) {
+    const int l = row_limit_of(a, r);
+    cta_lim = max(cta_lim, l);
+    min_lim = min(min_lim, l);
+  }
+  if (t0 > cta_lim) return;                            // no row sees this chunk (phase 2 skips it)
+  const int t_end = min(t1, cta_lim + 1);
+  const int n_stages = (t_end - t0 + kStage - 1) / kStage;
+  const int n_mine = warp < n_stages ? (n_stages - warp + kWarps - 1) / kWarps : 0;
+
+  // ---- query fragments (B operand of QK): row g of the group, dims 32b + 8c + 0..7
+  uint32_t bq_hi[8][2], bq_lo[QSPLIT ? 8 : 1][2];
+  float qsum[4];                                        // ASYM: per-block sum of q (row g)
+  float row_alpha;                                      // alpha * 2^e * log2(e) for row g
+  {
+    float x[4][8];
+    const bool live = g < R;
+    const int hq = kvh * a.gqa + (live ? g / a.n_q : 0);
+    const int qi = live ? g % a.n_q : 0;
+    const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
+    float mx = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      if (live) {
+        load8_f32(a.q, a.q_dtype, grow * kD + 32 * b + 8 * c, x[b]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[b][i] = 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[b][i]));
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    // power-of-two prescale so that the row's largest |q| lands in [2^13, 2^14): exact, and
+    // safe from f16 overflow; the inverse scale goes into the row's alpha.
+    int e = 0;
+    if (mx > 0.0f) e = max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - 13, -100);
+    const float pre = ldexpf(1.0f, -e), post = ldexpf(1.0f, e);
+    row_alpha = a.scale * post * kLog2e;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float s = 0.0f;
+      float h[8], l[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float v = x[b][i] * pre;
+        s += v;
+        h[i] = __half2float(__float2half_rn(v));
+        l[i] = v - h[i];
+      }
+      qsum[b] = s;
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+        bq_hi[2 * b + st][0] = pack_f16x2(h[2 * st], h[2 * st + 4]);
+        bq_hi[2 * b + st][1] = pack_f16x2(h[2 * st + 1], h[2 * st + 5]);
+        if (QSPLIT) {
+          bq_lo[2 * b + st][0] = pack_f16x2(l[2 * st], l[2 * st + 4]);
+          bq_lo[2 * b + st][1] = pack_f16x2(l[2 * st + 1], l[2 * st + 5]);
+        }
+      }
+    }
+    if (ASYM) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 1);
+        qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 2);
+      }
+    }
+  }
+  // the thread's two S^T columns are query rows 2c and 2c+1
+  const int r0 = 2 * c, r1 = 2 * c + 1;
+  const float alpha0 = __shfl_sync(0xffffffffu, row_alpha, r0 * 4);
+  const float alpha1 = __shfl_sync(0xffffffffu, row_alpha, r1 * 4);
+  float zq0[4], zq1[4];
+  if (ASYM) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      // alpha * zero-point contributions use the prescaled row sums
+      zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4);
+      zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4);
+    }
+  }
+  const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
+  const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
+
+  // ---- per-warp stage pipeline
+  uint8_t *wbuf = smem + warp * 2 * stage_bytes<ASYM>();
+  const size_t head_row0 = (size_t)bh * cv.cap;
+  const uint8_t *kp = cv.payload[0] + head_row0 * kRowBytes;
+  const uint8_t *vp = cv.payload[1] + head_row0 * kRowBytes;
+  const __half *ksc = static_cast<const __half *>(cv.scale[0]) + head_row0 * 4;
+  const __half *vsc = static_cast<const __half *>(cv.scale[1]) + head_row0 * 4;
+  const __half *kz = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
+  const __half *vz = ASYM ? cv.zero[1] + head_row0 * 4 : nullptr;
+
+  auto issue = [&](int i) {
+    if (i < n_mine) {
+      const int ts = t0 + (warp + i * kWarps) * kStage;
+      uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
+      const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int q = lane + 32 * k;                     // 16-byte piece: row q/4, column q%4
+        const int row = q >> 2, j = q & 3;
+        const bool ok = ts + row < t_end;
+        const size_t off = (size_t)(ok ? ts + row : t0) * kRowBytes + 16 * j;
+        cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
+        cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int row = lane + 32 * k;
+        const bool ok = ts + row < t_end;
+        const size_t off = (size_t)(ok ? ts + row : t0) * 4;
+        cp_async8(smem_addr(sb + kOffSK + row * 8), ksc + off, ok ? 8 : 0);
+        cp_async8(smem_addr(sb + kOffSV + row * 8), vsc + off, ok ? 8 : 0);
+        if (ASYM) {
+          cp_async8(smem_addr(sb + kOffZK + row * 8), kz + off, ok ? 8 : 0);
+          cp_async8(smem_addr(sb + kOffZV + row * 8), vz + off, ok ? 8 : 0);
+        }
+      }
+    }
+    cp_async_commit();                                   // always one group per call
+  };
+
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+  float O[4][2][4];                                      // [block][half][c0..c3]
+  float zacc0[4], zacc1[4];                              // ASYM: sum p * z_v per block, rows r0/r1
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    zacc0[b] = 0.0f;
+    zacc1[b] = 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) O[b][h][k] = 0.0f;
+  }
+
+  issue(0);
+  issue(1);
+  for (int i = 0; i < n_mine; ++i) {
+    cp_async_wait1();
+    __syncwarp();
+    const uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
+    const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
+    const int ts = t0 + (warp + i * kWarps) * kStage;
+
+    // ---------------- scores S^T for the 4 tiles of the stage
+    float s[4][4];
+#pragma unroll
+    for (int tile = 0; tile < 4; ++tile) {
+      uint32_t kw[2][4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int mi = lane >> 3;
+        const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+        ldsm_x4(sK + swz(row, 2 * half + (mi >> 1)), kw[half]);
+      }
+      const uint2 skg = *reinterpret_cast<const uint2 *>(sb + kOffSK + (tile * 16 + g) * 8);
+      const uint2 skg8 = *reinterpret_cast<const uint2 *>(sb + kOffSK + (tile * 16 + g + 8) * 8);
+      const float2 sg01 = __half22float2(u32_as_h2(skg.x)), sg23 = __half22float2(u32_as_h2(skg.y));
+      const float2 s801 = __half22float2(u32_as_h2(skg8.x)), s823 = __half22float2(u32_as_h2(skg8.y));
+      const float skg_f[4] = {sg01.x, sg01.y, sg23.x, sg23.y};
+      const float skg8_f[4] = {s801.x, s801.y, s823.x, s823.y};
+      float zg_f[4], zg8_f[4];
+      if (ASYM) {
+        const uint2 zg = *reinterpret_cast<const uint2 *>(sb + kOffZK + (tile * 16 + g) * 8);
+        const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + kOffZK + (tile * 16 + g + 8) * 8);
+        const float2 a01 = __half22float2(u32_as_h2(zg.x)), a23 = __half22float2(u32_as_h2(zg.y));
+        const float2 b01 = __half22float2(u32_as_h2(zg8.x)), b23 = __half22float2(u32_as_h2(zg8.y));
+        zg_f[0] = a01.x; zg_f[1] = a01.y; zg_f[2] = a23.x; zg_f[3] = a23.y;
+        zg8_f[0] = b01.x; zg8_f[1] = b01.y; zg8_f[2] = b23.x; zg8_f[3] = b23.y;
+      }
+      float acc_s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        // kw[b/2][(b%2)*2 + 0] = (token g, block b); [.. + 1] = (token g+8, block b)
+        uint32_t ug[4], u8[4];
+        unpack8<ASYM>(kw[b >> 1][(b & 1) * 2 + 0], ug);
+        unpack8<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
+        const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
+        const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
+        mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
+        if (QSPLIT) {
+          mma16816(d, A0, bq_lo[2 * b][0], bq_lo[2 * b][1]);
+          mma16816(d, A1, bq_lo[2 * b + 1][0], bq_lo[2 * b + 1][1]);
+        }
+        acc_s[0] = fmaf(skg_f[b], d[0], acc_s[0]);
+        acc_s[1] = fmaf(skg_f[b], d[1], acc_s[1]);
+        acc_s[2] = fmaf(skg8_f[b], d[2], acc_s[2]);
+        acc_s[3] = fmaf(skg8_f[b], d[3], acc_s[3]);
+        if (ASYM) {
+          acc_s[0] = fmaf(zg_f[b], zq0[b], acc_s[0]);
+          acc_s[1] = fmaf(zg_f[b], zq1[b], acc_s[1]);
+          acc_s[2] = fmaf(zg8_f[b], zq0[b], acc_s[2]);
+          acc_s[3] = fmaf(zg8_f[b], zq1[b], acc_s[3]);
+        }
+      }
+      s[tile][0] = acc_s[0] * alpha0;
+      s[tile][1] = acc_s[1] * alpha1;
+      s[tile][2] = acc_s[2] * alpha0;
+      s[tile][3] = acc_s[3] * alpha1;
+    }
+    // ---------------- mask (only at the chunk tail or a causal boundary)
+    if (ts + kStage > t1 || ts + kStage - 1 > min_lim) {
+#pragma unroll
+      for (int tile = 0; tile < 4; ++tile) {
+        const int ta = ts + tile * 16 + g, tb = ta + 8;
+        if (!(ta < t1 && ta <= lim0)) s[tile][0] = -INFINITY;
+        if (!(ta < t1 && ta <= lim1)) s[tile][1] = -INFINITY;
+        if (!(tb < t1 && tb <= lim0)) s[tile][2] = -INFINITY;
+        if (!(tb < t1 && tb <= lim1)) s[tile][3] = -INFINITY;
+      }
+    }
+    // ---------------- online softmax (base 2), rows r0 / r1
+    float mx0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
+    mx0 = fmaxf(mx0, fmaxf(fmaxf(s[2][0], s[2][2]), fmaxf(s[3][0], s[3][2])));
+    float mx1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+    mx1 = fmaxf(mx1, fmaxf(fmaxf(s[2][1], s[2][3]), fmaxf(s[3][1], s[3][3])));
+#pragma unroll
+    for (int k = 4; k < 32; k <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, k));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, k));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+    const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= corr0;
+    l1 *= corr1;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      zacc0[b] *= corr0;
+      zacc1[b] *= corr1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        O[b][h][0] *= corr0;
+        O[b][h][1] *= corr1;
+        O[b][h][2] *= corr0;
+        O[b][h][3] *= corr1;
+      }
+    }
+#pragma unroll
+    for (int tile = 0; tile < 4; ++tile) {
+      s[tile][0] = ex2(s[tile][0] - mu0);
+      s[tile][1] = ex2(s[tile][1] - mu1);
+      s[tile][2] = ex2(s[tile][2] - mu0);
+      s[tile][3] = ex2(s[tile][3] - mu1);
+      l0 += s[tile][0] + s[tile][2];
+      l1 += s[tile][1] + s[tile][3];
+    }
+
+    // ---------------- O^T += V^T . (P * s_v)^T per 32-dim block
+#pragma unroll
+    for (int tile = 0; tile < 4; ++tile) {
+      uint32_t vw[2][4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int mi = lane >> 3;
+        const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+        ldsm_x4_t(sV + swz(row, 2 * half + (mi >> 1)), vw[half]);
+      }
+      const uint2 svg = *reinterpret_cast<const uint2 *>(sb + kOffSV + (tile * 16 + g) * 8);
+      const uint2 svg8 = *reinterpret_cast<const uint2 *>(sb + kOffSV + (tile * 16 + g + 8) * 8);
+      const float2 v01 = __half22float2(u32_as_h2(svg.x)), v23 = __half22float2(u32_as_h2(svg.y));
+      const float2 w01 = __half22float2(u32_as_h2(svg8.x)), w23 = __half22float2(u32_as_h2(svg8.y));
+      const float svg_f[4] = {v01.x, v01.y, v23.x, v23.y};
+      const float svg8_f[4] = {w01.x, w01.y, w23.x, w23.y};
+      if (ASYM) {
+        const uint2 zg = *reinterpret_cast<const uint2 *>(sb + kOffZV + (tile * 16 + g) * 8);
+        const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + kOffZV + (tile * 16 + g + 8) * 8);
+        const float2 a01 = __half22float2(u32_as_h2(zg.x)), a23 = __half22float2(u32_as_h2(zg.y));
+        const float2 b01 = __half22float2(u32_as_h2(zg8.x)), b23 = __half22float2(u32_as_h2(zg8.y));
+        const float zv_g[4] = {a01.x, a01.y, a23.x, a23.y};
+        const float zv_g8[4] = {b01.x, b01.y, b23.x, b23.y};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          zacc0[b] = fmaf(s[tile][0], zv_g[b], fmaf(s[tile][2], zv_g8[b], zacc0[b]));
+          zacc1[b] = fmaf(s[tile][1], zv_g[b], fmaf(s[tile][3], zv_g8[b], zacc1[b]));
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float p0 = s[tile][0] * svg_f[b], p1 = s[tile][1] * svg_f[b];
+        const float p2 = s[tile][2] * svg8_f[b], p3 = s[tile][3] * svg8_f[b];
+        const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
+        const float2 f01 = __half22float2(u32_as_h2(h01)), f23 = __half22float2(u32_as_h2(h23));
+        const uint32_t l01 = pack_f16x2(p0 - f01.x, p1 - f01.y), l23 = pack_f16x2(p2 - f23.x, p3 - f23.y);
+        const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23), bl0 = movm_t(l01), bl1 = movm_t(l23);
+        // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
+        uint32_t ua[4], ub[4];
+        unpack8<ASYM>(vw[b >> 1][(b & 1) * 2 + 0], ua);
+        unpack8<ASYM>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+        const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};   // dims 4g+0 (row g), 4g+1 (row g+8)
+        const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};   // dims 4g+2, 4g+3
+        mma16816(O[b][0], A0, bh0, bh1);
+        mma16816(O[b][0], A0, bl0, bl1);
+        mma16816(O[b][1], A1, bh0, bh1);
+        mma16816(O[b][1], A1, bl0, bl1);
+      }
+    }
+    __syncwarp();                                        // buffer fully read before reuse
+    issue(i + 2);
+  }
+
+  // ---------------- warp state: reduce l (and the zero-point sums) over the token lanes
+#pragma unroll
+  for (int k = 4; k < 32; k <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, k);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, k);
+    if (ASYM) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        zacc0[b] += __shfl_xor_sync(0xffffffffu, zacc0[b], k);
+        zacc1[b] += __shfl_xor_sync(0xffffffffu, zacc1[b], k);
+      }
+    }
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();                                       // every warp is done with its stages
+
+  // ---------------- combine the warps in shared memory: cm/cl [warp][8], co [warp][8][128]
+  float *cm = reinterpret_cast<float *>(smem);
+  float *cl = cm + kWarps * 8;
+  float *co = cl + kWarps * 8;
+  if (g == 0) {
+    cm[warp * 8 + r0] = m0;
+    cm[warp * 8 + r1] = m1;
+    cl[warp * 8 + r0] = l0;
+    cl[warp * 8 + r1] = l1;
+  }
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int d = 32 * b + 4 * g + 2 * h;
+      float z0 = 0.0f, z1 = 0.0f;
+      if (ASYM) {
+        z0 = zacc0[b];
+        z1 = zacc1[b];
+      }
+      co[(warp * 8 + r0) * kD + d] = O[b][h][0] + z0;
+      co[(warp * 8 + r1) * kD + d] = O[b][h][1] + z1;
+      co[(warp * 8 + r0) * kD + d + 1] = O[b][h][2] + z0;
+      co[(warp * 8 + r1) * kD + d + 1] = O[b][h][3] + z1;
+    }
+  }
+  __syncthreads();
+  const int d = threadIdx.x;                             // 128 threads <-> 128 dims
+  for (int r = 0; r < R; ++r) {
+    if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
+    float L = 0.0f, acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float wt = cm[w * 8 + r] == -INFINITY ? 0.0f : ex2(cm[w * 8 + r] - M);
+      L = fmaf(cl[w * 8 + r], wt, L);
+      acc = fmaf(co[(w * 8 + r) * kD + d], wt, acc);
+    }
+    const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
+    const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
+    const size_t pi = grow * a.C + chunk_id;
+    a.part_o[pi * kD + d] = acc;
+    if (d == 0) {
+      a.part_m[pi] = M * kLn2;                           // natural-log units, like the other kernels
+      a.part_l[pi] = L;
+    }
+  }
+}
+
+template <bool ASYM, bool QSPLIT>
+cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
+  static bool configured[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(attend_mma_kernel<ASYM, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<ASYM>());
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  dim3 grid(a.n_chunks, a.cache.B * a.cache.H);
+  attend_mma_kernel<ASYM, QSPLIT><<<grid, kWarps * 32, smem_bytes<ASYM>(), st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_supported(const AttendArgs &a) {
+  return (a.cache.layout == KVQ_Q4_0 || a.cache.layout == KVQ_ASYM4_G32) && a.cache.D == kD &&
+         a.gqa * a.n_q <= 8 && a.n_body > 0 && a.chunk % kStage == 0;
+}
+
+cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
+  const bool asym = a.cache.layout == KVQ_ASYM4_G32;
+  const bool split = a.q_dtype == KVQ_F32;
+  if (asym) return split ? launch_t<true, true>(a, st) : launch_t<true, false>(a, st);
+  return split ? launch_t<false, true>(a, st) : launch_t<false, false>(a, st);
+}
 
 }  // namespace kvq
