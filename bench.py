@@ -272,7 +272,8 @@ def main():
     n_rep = max(2, math.ceil(3 * L2_BYTES / (2 * B * H * S * 72)) + 1)
     caches = make_caches("q4_0", n_rep)
     read_bytes = caches[0].read_bytes(S)
-    ws = torch.empty(kvq.attend_workspace_bytes(caches[0], w.n_q_heads, 1, S), dtype=torch.uint8, device=dev)
+    chunk = kvq.attend_chunk(caches[0], S, 0)          # automatic split: one chunk per resident warp
+    ws = torch.empty(kvq.attend_workspace_bytes(caches[0], w.n_q_heads, 1, S, chunk), dtype=torch.uint8, device=dev)
     out = torch.empty((B, w.n_q_heads, 1, D), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     L = _lib.lib()
@@ -282,7 +283,7 @@ def main():
         kvq.store(c, k_new, v_new, S - 1, stream=stream)
         if ev is not None:
             L.kvq_profile_phase1_events(ev[0].cuda_event, ev[1].cuda_event)
-        kvq.decode_attend(c, q, S, attn_scale=w.alpha, out=out, workspace=ws, stream=stream)
+        kvq.decode_attend(c, q, S, attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
         if ev is not None:
             L.kvq_profile_phase1_events(None, None)
 
@@ -290,6 +291,9 @@ def main():
     use_graph = not args.no_graph
     ph_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with torch.cuda.stream(stream):
+        for a, b in ph_ev:      # create the events (torch only times events it has recorded once)
+            a.record(stream)
+            b.record(stream)
         for i in range(max(W, 3)):
             step(i)
     torch.cuda.synchronize(dev)
@@ -348,7 +352,8 @@ def main():
         "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "Llama-3.1-70B layer, 128K context, Q4_0 KV (bf16 Student-t(4) K/V, 4 outlier "
-                               "channels x10, N(0,1) Q), B1 Hq64 Hkv8 D128, chunk 512",
+                               "channels x10, N(0,1) Q), B1 Hq64 Hkv8 D128",
+                   "chunk": chunk, "chunk_rule": "automatic: one split-K chunk per resident warp (multiple of 64)",
                    "kv_len": S, "layout": "q4_0", "step": "append 1 token (K,V) + split-K decode attention",
                    "read_bytes_per_step": read_bytes,
                    "l2": f"inputs larger than L2: {n_rep} cache replicas rotated "
@@ -382,34 +387,46 @@ def main():
                 dq.copy_(hq, non_blocking=True)
                 c = caches[i % n_rep]
                 kvq.store(c, dk, dv, S - 1, stream=stream)
-                kvq.decode_attend(c, dq, S, attn_scale=w.alpha, out=out, workspace=ws, stream=stream)
+                kvq.decode_attend(c, dq, S, attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
                 hout.copy_(out, non_blocking=True)
             stream.synchronize()
         t_e2e = (time.perf_counter() - t0) / n_e2e
         line["e2e"] = {"value": read_bytes / t_e2e / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": hk.numel() * 2 + hv.numel() * 2 + hq.numel() * 2,
                        "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e}
+        line["variants"] = {}
+
+        def time_plain(cs, wsb, ch, n):
+            with torch.cuda.stream(stream):
+                for i in range(5):
+                    kvq.store(cs[i % n_rep], k_new, v_new, S - 1, stream=stream)
+                    kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
+                                      stream=stream)
+                torch.cuda.synchronize(dev)
+                ev0.record(stream)
+                for i in range(n):
+                    kvq.store(cs[i % n_rep], k_new, v_new, S - 1, stream=stream)
+                    kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
+                                      stream=stream)
+                ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            return ev0.elapsed_time(ev1) / n
+        ws512 = torch.empty(kvq.attend_workspace_bytes(caches[0], w.n_q_heads, 1, S, 512), dtype=torch.uint8,
+                            device=dev)
+        c_ms = time_plain(caches, ws512, 512, min(K, 1000))
+        line["variants"]["q4_0_chunk512"] = {"us_per_layer": c_ms * 1e3, "gbs": read_bytes / (c_ms / 1e3) / 1e9,
+                                             "timing": "stream launches", "chunk": 512}
         # asymmetric g=32 variant of the same layer (same device timing protocol, plain launches)
         del caches
         torch.cuda.empty_cache()
         acaches = make_caches("asym4_g32", n_rep)
         a_bytes = acaches[0].read_bytes(S)
-        aws = torch.empty(kvq.attend_workspace_bytes(acaches[0], w.n_q_heads, 1, S), dtype=torch.uint8, device=dev)
-        with torch.cuda.stream(stream):
-            for i in range(5):
-                kvq.store(acaches[i % n_rep], k_new, v_new, S - 1, stream=stream)
-                kvq.decode_attend(acaches[i % n_rep], q, S, attn_scale=w.alpha, out=out, workspace=aws, stream=stream)
-            torch.cuda.synchronize(dev)
-            nv = min(K, 1000)
-            ev0.record(stream)
-            for i in range(nv):
-                kvq.store(acaches[i % n_rep], k_new, v_new, S - 1, stream=stream)
-                kvq.decode_attend(acaches[i % n_rep], q, S, attn_scale=w.alpha, out=out, workspace=aws, stream=stream)
-            ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        a_ms = ev0.elapsed_time(ev1) / nv
-        line["variants"] = {"asym4_g32": {"us_per_layer": a_ms * 1e3, "read_bytes_per_step": a_bytes,
-                                          "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches"}}
+        aws = torch.empty(kvq.attend_workspace_bytes(acaches[0], w.n_q_heads, 1, S, chunk), dtype=torch.uint8,
+                          device=dev)
+        a_ms = time_plain(acaches, aws, chunk, min(K, 1000))
+        line["variants"]["asym4_g32"] = {"us_per_layer": a_ms * 1e3, "read_bytes_per_step": a_bytes,
+                                         "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches",
+                                         "chunk": chunk}
         if world == 1:
             line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
     if rank == 0:

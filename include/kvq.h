@@ -125,10 +125,14 @@ kvq_status kvq_store_hadamard_int4(const kvq_cache *cache, const void *k_new, co
 kvq_status kvq_store_asym4_g32(const kvq_cache *cache, const void *k_new, const void *v_new,
                                int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
 
-/* Workspace bytes kvq_decode_attend needs for these arguments (0 on invalid arguments).
- * chunk 0 means the default of 512 tokens. */
+/* Workspace bytes kvq_decode_attend needs for these arguments on the current device (0 on
+ * invalid arguments). chunk 0 means the automatic chunk described at kvq_decode_attend. */
 size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q,
                                   int32_t kv_len, int32_t chunk);
+
+/* The chunk length kvq_decode_attend uses for these arguments on the current device (`chunk`
+ * itself when non-zero and valid, the automatic choice for 0); 0 on invalid arguments. */
+int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t kv_len, int32_t chunk);
 
 /*
  * Fused split-K decode attention over the packed cache; the dequantised K/V matrix is never
@@ -139,8 +143,10 @@ size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int
  * head attends tokens t < kv_len and, when causal != 0, t <= q_pos0 + i ([TR] causal
  * masking); a causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len.
  * score = attn_scale * q . k_hat. Phase 1 splits the tokens into chunks of `chunk` tokens
- * (0 -> 512; else a multiple of 64 in [64, 8192]) and writes per (row, chunk) the running
- * max, the sum of exponentials and the unnormalised output to the workspace; phase 2
+ * (a multiple of 64 in [64, 8192], e.g. 512 as in [OTQ]; 0 = automatic: the smallest multiple
+ * of 64 that covers all (batch, kv head) bodies with one chunk per resident warp of the current
+ * device, so the split depends on the device's SM count) and writes per (row, chunk) the
+ * running max, the sum of exponentials and the unnormalised output to the workspace; phase 2
  * combines them with the online-softmax correction ([OTQ] Section 3.2). HAD_INT4: the query
  * is rotated and quantised to int8 (one f32 scale per row, amax / 127), body tokens are
  * scored by the exact integer dot, the newest min(n_recent, kv_len) tokens by exact f32
@@ -166,7 +172,9 @@ kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q
  * Measurement hook (no counterpart on the pages): while both events are non-NULL, every
  * kvq_decode_attend call made by this thread records `phase1_begin` on its stream right before
  * the phase-1 launch and `phase1_end` right after it, so a caller can time the streaming kernel
- * alone with cudaEventElapsedTime. The events are cudaEvent_t handles created by the caller;
+ * alone with cudaEventElapsedTime. The records are external event records, so under stream
+ * capture they become event-record nodes of the graph and time every replay. The events are
+ * cudaEvent_t handles created by the caller (with timing enabled);
  * passing NULL for either disables recording. Thread-local; returns KVQ_OK.
  */
 kvq_status kvq_profile_phase1_events(void *phase1_begin, void *phase1_end);

@@ -89,6 +89,19 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
   return KVQ_OK;
 }
 
+// Automatic split-K chunk: the smallest multiple of 64 tokens such that one chunk per warp
+// covers the body of every (batch, kv head) in a single wave of resident warps (12 per SM).
+int auto_chunk(int n_body, int n_heads) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long warps = (long long)sms * 12;
+  const long long per = ((long long)(n_body > 0 ? n_body : 1) * n_heads + warps - 1) / warps;
+  long long chunk = (per + 63) / 64 * 64;
+  if (chunk < 64) chunk = 64;
+  if (chunk > 8192) chunk = 8192;
+  return (int)chunk;
+}
+
 // Resolve the attention arguments and the workspace layout. When `ws` is NULL only sizes are
 // computed (returned through `need`).
 kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv_len, int causal, int q_pos0,
@@ -102,7 +115,8 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
   if (kv_len > c.cap) return fail(KVQ_ECAPACITY, "kv_len %d > capacity %d", kv_len, c.cap);
   if (causal && (q_pos0 < 0 || (long long)q_pos0 + n_q > kv_len))
     return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
-  if (chunk == 0) chunk = 512;
+  if (chunk == 0) chunk = auto_chunk(kv_len - (c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0),
+                                     c.B * c.H);
   if (chunk < 64 || chunk > 8192 || chunk % 64) return fail(KVQ_ESHAPE, "chunk %d not a multiple of 64 in [64, 8192]", chunk);
   a.Hq = n_q_heads; a.gqa = n_q_heads / c.H; a.n_q = n_q;
   a.kv_len = kv_len;
@@ -183,6 +197,13 @@ size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int
   size_t need = 0;
   if (resolve_attend(cache, n_q_heads, n_q, kv_len, 0, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
   return need;
+}
+
+int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t kv_len, int32_t chunk) {
+  kvq::AttendArgs a;
+  size_t need = 0;
+  if (resolve_attend(cache, cache ? cache->n_kv_heads : 1, 1, kv_len, 0, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  return a.chunk;
 }
 
 kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,

@@ -15,9 +15,7 @@
 // 2^24 are exact in float32), times alpha * s_q * s_k. The exact-f32 ring forms one extra
 // chunk scored with the float32 rotated query.
 //
-// Phase 2 (attend_reduce_kernel): per query row, M = max m_c, L = sum l_c e^(m_c - M),
-// O = sum o_c e^(m_c - M) / L over the chunks the row can see; Hadamard outputs are
-// un-rotated with the same in-warp FWHT and 1/sqrt(D).
+// Phase 2 (the LSE reduce) lives in reduce.cu.
 #include <cfloat>
 
 #include "kvq_internal.cuh"
@@ -91,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   // Let the phase-2 grid be scheduled early; it still waits for this grid to finish.
   asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // upstream store / query prep complete
 #endif
   const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;                 // b * H_kv + kv head
@@ -241,85 +240,6 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
   for (int i = 0; i < VPL; ++i) a.part_o[pi * D + lane + 32 * i] = o[i];
 }
 
-// Phase 2: one CTA of 8 warps per query row; warps split the chunks, lanes split D.
-template <int D>
-__global__ void __launch_bounds__(256) attend_reduce_kernel(AttendArgs a) {
-  constexpr int VPL = D / 32;
-  __shared__ float sm_m[8], sm_l[8];
-  __shared__ __align__(16) float sm_o[8][D];
-#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-#endif
-  const size_t grow = blockIdx.x;                       // (b * Hq + h) * n_q + i
-  const int qi = (int)(grow % a.n_q);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int lim = row_limit(a, qi);
-  // chunks this row sees
-  int nc = 0;
-  for (int c = 0; c < a.C; ++c) {
-    int t0, t1;
-    chunk_range(a, c, t0, t1);
-    if (t0 <= lim && t1 > t0) nc = c + 1;
-  }
-  float M = -INFINITY;
-  for (int c = warp; c < nc; c += 8) {
-    int t0, t1;
-    chunk_range(a, c, t0, t1);
-    if (t0 <= lim && t1 > t0) M = fmaxf(M, a.part_m[grow * a.C + c]);
-  }
-  float L = 0.0f, O[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
-  // per-warp max first, then block max
-  if (lane == 0) sm_m[warp] = M;
-  __syncthreads();
-  M = sm_m[0];
-#pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, sm_m[w]);
-  for (int c = warp; c < nc; c += 8) {
-    int t0, t1;
-    chunk_range(a, c, t0, t1);
-    if (!(t0 <= lim && t1 > t0)) continue;
-    const size_t pi = grow * a.C + c;
-    const float w = __expf(a.part_m[pi] - M);
-    L = fmaf(a.part_l[pi], w, L);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) O[i] = fmaf(a.part_o[pi * D + lane + 32 * i], w, O[i]);
-  }
-  if (lane == 0) sm_l[warp] = L;
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) sm_o[warp][lane + 32 * i] = O[i];
-  __syncthreads();
-  if (warp != 0) return;
-  float Lt = 0.0f;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) Lt += sm_l[w];
-  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
-  if (a.cache.layout == KVQ_HAD_INT4) {
-    // un-rotate: out = FWHT(O) / sqrt(D); lane holds VPL consecutive dims
-    float x[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) acc += sm_o[w][lane * VPL + i];
-      x[i] = acc * inv;
-    }
-    warp_fwht<VPL>(x, lane);
-    const float cD = inv_sqrt_dim(D);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) a.out[grow * D + lane * VPL + i] = x[i] * cD;
-  } else {
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      float acc = 0.0f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) acc += sm_o[w][lane + 32 * i];
-      a.out[grow * D + lane + 32 * i] = acc * inv;
-    }
-  }
-}
-
 // Hadamard query preparation: one warp per query row.
 template <int V>
 __global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows) {
@@ -416,31 +336,23 @@ cudaError_t launch_generic_dt(const AttendArgs &a, cudaStream_t st) {
     configured[dev] = true;
   }
   const int R = a.gqa * a.n_q;
-  dim3 grid(a.C, a.cache.B * a.cache.H, (R + kRowsPerCta - 1) / kRowsPerCta);
-  attend_generic_kernel<D, T><<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.C, a.cache.B * a.cache.H, (R + kRowsPerCta - 1) / kRowsPerCta);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_generic_kernel<D, T>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st) {
   return a.cache.D == 128 ? launch_generic_dt<128, 64>(a, st) : launch_generic_dt<256, 32>(a, st);
-}
-
-cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl) {
-  const unsigned rows = (unsigned)((size_t)a.cache.B * a.Hq * a.n_q);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  if (a.cache.D == 128) return cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128>, a);
-  return cudaLaunchKernelEx(&cfg, attend_reduce_kernel<256>, a);
 }
 
 cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st) {

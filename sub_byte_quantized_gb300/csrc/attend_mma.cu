@@ -13,16 +13,18 @@
 // scale of K (per token and 32-dim block) multiplies each block's f32 partial sum; the block
 // scale of V is folded into the probabilities, P' = p * s_v, split into hi + lo f16 parts.
 //
-// Data movement: each warp owns a contiguous slice of 64-token stages of the chunk and pulls
-// them HBM -> shared memory with 16-byte cp.async (two stages in flight per warp). Payload rows
+// Data movement: each warp pulls its chunk HBM -> shared memory in 64-token stages with
+// 16-byte cp.async (two stages in flight per warp). Payload rows
 // (64 bytes) are placed with a 64-byte XOR swizzle (16-byte column ^= (row / 2) % 4) so that the
 // ldmatrix reads (8 rows x 16 bytes per phase) are bank-conflict free. ldmatrix gives each lane
 // the nibble words of its fragment: plain for K (one token, 8 consecutive dims), transposed for
 // V (two tokens, 4 consecutive dims). The nibbles become f16 pairs with one lop3 (mask + magic
 // exponent 0x6400, the Q4_0 sign flip folded in) and one f16 subtract/fma, all exact.
 //
-// Each CTA handles one chunk of one (batch, kv head); its four warps combine their online
-// softmax states in shared memory and write one (m, l, o) partial per query row.
+// Each warp handles one whole chunk of one (batch, kv head): it streams the chunk through
+// its private two-stage shared-memory ring, keeps the online softmax state in registers and
+// writes one (m, l, o) partial per query row. A CTA is four such independent warps (four
+// consecutive chunks of the same kv head); there is no block-level barrier.
 #include <cfloat>
 #include <climits>
 
@@ -66,11 +68,11 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
 }
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
   uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
 }
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
                "{%0,%1,%2,%3};\n"
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -93,26 +95,39 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// f16x2 constants (bit patterns): 1/16, -1032, -72, -1024, -64 in both halves.
+constexpr uint32_t kH16th = 0x2C002C00u, kHm1032 = 0xE408E408u, kHm72 = 0xD480D480u;
+constexpr uint32_t kHm1024 = 0xE400E400u, kHm64 = 0xD400D400u;
+
 // Eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
 // (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the code values: Q4_0 (signed: (n ^ 8) - 8) or
-// the unsigned asymmetric code n.
+// the unsigned asymmetric code n. One lop3 places a field in the mantissa under the exponent
+// of 1024 (0x6400); one f16 add/fma removes the offset.
 template <bool ASYM>
 __device__ __forceinline__ void unpack8(uint32_t w, uint32_t (&o)[4]) {
-  const __half2 one16 = __float2half2_rn(0.0625f);
   const uint32_t w8 = w >> 8;
   if (!ASYM) {
-    // (w & mask) ^ (magic | 8-in-each-field): 1024 + (n ^ 8) (or 1024 + 16 (n ^ 8))
-    const __half2 off_lo = __float2half2_rn(-1032.0f), off_hi = __float2half2_rn(-72.0f);
-    o[0] = h2_as_u32(__hadd2(u32_as_h2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u)), off_lo));
-    o[1] = h2_as_u32(__hfma2(u32_as_h2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u)), one16, off_hi));
-    o[2] = h2_as_u32(__hadd2(u32_as_h2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u)), off_lo));
-    o[3] = h2_as_u32(__hfma2(u32_as_h2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u)), one16, off_hi));
+    // (w & mask) ^ (0x6400 | 8 in each field): 1024 + (n ^ 8), or 1024 + 16 (n ^ 8) for the high field
+    o[0] = hadd2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u), kHm1032);
+    o[1] = hfma2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
+    o[2] = hadd2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u), kHm1032);
+    o[3] = hfma2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
   } else {
-    const __half2 off_lo = __float2half2_rn(-1024.0f), off_hi = __float2half2_rn(-64.0f);
-    o[0] = h2_as_u32(__hadd2(u32_as_h2(lop3<0xea>(w, 0x000F000Fu, 0x64006400u)), off_lo));
-    o[1] = h2_as_u32(__hfma2(u32_as_h2(lop3<0xea>(w, 0x00F000F0u, 0x64006400u)), one16, off_hi));
-    o[2] = h2_as_u32(__hadd2(u32_as_h2(lop3<0xea>(w8, 0x000F000Fu, 0x64006400u)), off_lo));
-    o[3] = h2_as_u32(__hfma2(u32_as_h2(lop3<0xea>(w8, 0x00F000F0u, 0x64006400u)), one16, off_hi));
+    o[0] = hadd2(lop3<0xea>(w, 0x000F000Fu, 0x64006400u), kHm1024);
+    o[1] = hfma2(lop3<0xea>(w, 0x00F000F0u, 0x64006400u), kH16th, kHm64);
+    o[2] = hadd2(lop3<0xea>(w8, 0x000F000Fu, 0x64006400u), kHm1024);
+    o[3] = hfma2(lop3<0xea>(w8, 0x00F000F0u, 0x64006400u), kH16th, kHm64);
   }
 }
 
@@ -127,31 +142,33 @@ __device__ __forceinline__ uint32_t swz(int row, int j) {
 }
 
 template <bool ASYM, bool QSPLIT>
-__global__ void __launch_bounds__(kWarps * 32, 2) attend_mma_kernel(AttendArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // upstream store complete before any read
 #endif
   const CacheView &cv = a.cache;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int chunk_id = blockIdx.x;
+  // One chunk per warp; the warps of a CTA are independent (no block-level barrier below).
+  const int chunk_id = blockIdx.x * kWarps + warp;
+  if (chunk_id >= a.n_chunks) return;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
   const int R = a.gqa * a.n_q;
 
   const int t0 = chunk_id * a.chunk;
   const int t1 = min(a.n_body, t0 + a.chunk);
-  int cta_lim = -1, min_lim = INT_MAX;
+  int w_lim = -1, min_lim = INT_MAX;
   for (int r = 0; r < R; ++r) {
     const int l = row_limit_of(a, r);
-    cta_lim = max(cta_lim, l);
+    w_lim = max(w_lim, l);
     min_lim = min(min_lim, l);
   }
-  if (t0 > cta_lim) return;                            // no row sees this chunk (phase 2 skips it)
-  const int t_end = min(t1, cta_lim + 1);
-  const int n_stages = (t_end - t0 + kStage - 1) / kStage;
-  const int n_mine = warp < n_stages ? (n_stages - warp + kWarps - 1) / kWarps : 0;
+  if (t0 > w_lim) return;                              // no row sees this chunk (phase 2 skips it)
+  const int t_end = min(t1, w_lim + 1);
+  const int n_mine = (t_end - t0 + kStage - 1) / kStage;
 
   // ---- query fragments (B operand of QK): row g of the group, dims 32b + 8c + 0..7
   uint32_t bq_hi[8][2], bq_lo[QSPLIT ? 8 : 1][2];
@@ -241,7 +258,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attend_mma_kernel(AttendArgs a
 
   auto issue = [&](int i) {
     if (i < n_mine) {
-      const int ts = t0 + (warp + i * kWarps) * kStage;
+      const int ts = t0 + i * kStage;
       uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
       const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
 #pragma unroll
@@ -289,7 +306,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attend_mma_kernel(AttendArgs a
     __syncwarp();
     const uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
     const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
-    const int ts = t0 + (warp + i * kWarps) * kStage;
+    const int ts = t0 + i * kStage;
 
     // ---------------- scores S^T for the 4 tiles of the stage
     float s[4][4];
@@ -466,55 +483,27 @@ __global__ void __launch_bounds__(kWarps * 32, 2) attend_mma_kernel(AttendArgs a
     }
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-  __syncthreads();                                       // every warp is done with its stages
 
-  // ---------------- combine the warps in shared memory: cm/cl [warp][8], co [warp][8][128]
-  float *cm = reinterpret_cast<float *>(smem);
-  float *cl = cm + kWarps * 8;
-  float *co = cl + kWarps * 8;
-  if (g == 0) {
-    cm[warp * 8 + r0] = m0;
-    cm[warp * 8 + r1] = m1;
-    cl[warp * 8 + r0] = l0;
-    cl[warp * 8 + r1] = l1;
-  }
+  // ---------------- this warp's partial for query rows r0 / r1
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int d = 32 * b + 4 * g + 2 * h;
-      float z0 = 0.0f, z1 = 0.0f;
-      if (ASYM) {
-        z0 = zacc0[b];
-        z1 = zacc1[b];
-      }
-      co[(warp * 8 + r0) * kD + d] = O[b][h][0] + z0;
-      co[(warp * 8 + r1) * kD + d] = O[b][h][1] + z1;
-      co[(warp * 8 + r0) * kD + d + 1] = O[b][h][2] + z0;
-      co[(warp * 8 + r1) * kD + d + 1] = O[b][h][3] + z1;
-    }
-  }
-  __syncthreads();
-  const int d = threadIdx.x;                             // 128 threads <-> 128 dims
-  for (int r = 0; r < R; ++r) {
-    if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
-    float L = 0.0f, acc = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float wt = cm[w * 8 + r] == -INFINITY ? 0.0f : ex2(cm[w * 8 + r] - M);
-      L = fmaf(cl[w * 8 + r], wt, L);
-      acc = fmaf(co[(w * 8 + r) * kD + d], wt, acc);
-    }
+  for (int k = 0; k < 2; ++k) {
+    const int r = k ? r1 : r0;
+    if (r >= R || t0 > row_limit_of(a, r)) continue;     // phase 2 reads no partial for it
     const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
-    const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
-    const size_t pi = grow * a.C + chunk_id;
-    a.part_o[pi * kD + d] = acc;
-    if (d == 0) {
-      a.part_m[pi] = M * kLn2;                           // natural-log units, like the other kernels
-      a.part_l[pi] = L;
+    const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
+    float *po = a.part_o + pi * kD;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float z = ASYM ? (k ? zacc1[b] : zacc0[b]) : 0.0f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int d = 32 * b + 4 * g + 2 * h;
+        *reinterpret_cast<float2 *>(po + d) = make_float2(O[b][h][k] + z, O[b][h][k + 2] + z);
+      }
+    }
+    if (g == 0) {
+      a.part_m[pi] = (k ? m1 : m0) * kLn2;               // natural-log units, like the other kernels
+      a.part_l[pi] = k ? l1 : l0;
     }
   }
 }
@@ -532,9 +521,17 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  dim3 grid(a.n_chunks, a.cache.B * a.cache.H);
-  attend_mma_kernel<ASYM, QSPLIT><<<grid, kWarps * 32, smem_bytes<ASYM>(), st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.n_chunks + kWarps - 1) / kWarps, a.cache.B * a.cache.H);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem_bytes<ASYM>();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<ASYM, QSPLIT>, a);
 }
 
 }  // namespace

@@ -1,0 +1,130 @@
+// Phase 2 of the split-K decode attention: combine the per-chunk partials (m_c, l_c, o_c) of
+// every query row with the online-softmax correction
+//   M = max_c m_c,  L = sum_c l_c e^(m_c - M),  out = sum_c o_c e^(m_c - M) / L,
+// over the chunks the row can see (a chunk beyond a row's causal limit has no partial). For the
+// Hadamard layout the combined output is still in the rotated basis and is un-rotated here
+// (in-warp FWHT times 1/sqrt(D)).
+//
+// Grid: one CTA per (query row, 32-dim slice) -- one CTA per row for the Hadamard layout, whose
+// un-rotation needs the whole row. Eight warps split the chunks; each lane owns one (or D/32)
+// output dims and keeps a running (M, L, O) over batches of eight chunks whose loads are all in
+// flight together. The warps are combined in shared memory.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kBatch = 8;
+
+template <int D, bool HAD>
+__global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a) {
+  constexpr int DS = HAD ? D : 32;         // dims per CTA
+  constexpr int VPL = DS / 32;             // dims per lane
+  __shared__ float sm_m[kWarps], sm_l[kWarps];
+  __shared__ __align__(16) float sm_o[kWarps][DS];
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.wait;" ::: "memory");     // phase-1 partials are complete
+#endif
+  const size_t row = blockIdx.x;                          // (b * H_q + h) * n_q + i
+  const int qi = (int)(row % a.n_q);
+  const int d0 = HAD ? 0 : blockIdx.y * 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lim = a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+  const int n_vis_body = min(a.n_chunks, lim / a.chunk + 1);
+  const bool win_vis = a.n_win > 0 && a.n_body <= lim;
+  const float *pm = a.part_m + row * a.C;
+  const float *pl = a.part_l + row * a.C;
+  const float *po = a.part_o + row * a.C * (size_t)D;
+
+  float M = -INFINITY, L = 0.0f, O[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
+  for (int base = warp; base < a.C; base += kWarps * kBatch) {
+    float mc[kBatch], lc[kBatch], oc[kBatch][VPL];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = base + u * kWarps;
+      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : win_vis);
+      mc[u] = vis ? pm[c] : -INFINITY;
+      lc[u] = vis ? pl[c] : 0.0f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int d = HAD ? lane * VPL + i : d0 + lane;
+        oc[u][i] = vis ? po[(size_t)c * D + d] : 0.0f;
+      }
+    }
+    float bm = M;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, mc[u]);
+    if (bm == -INFINITY) continue;
+    const float corr = __expf(M - bm);                    // M = -inf -> 0
+    L *= corr;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) O[i] *= corr;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float w = __expf(mc[u] - bm);                 // invisible chunks: exp(-inf) = 0
+      L = fmaf(lc[u], w, L);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) O[i] = fmaf(oc[u][i], w, O[i]);
+    }
+    M = bm;
+  }
+  if (lane == 0) {
+    sm_m[warp] = M;
+    sm_l[warp] = L;
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) sm_o[warp][HAD ? lane * VPL + i : lane] = O[i];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = sm_m[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) Mt = fmaxf(Mt, sm_m[w]);
+  float Lt = 0.0f, x[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) x[i] = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float wt = sm_m[w] == -INFINITY ? 0.0f : __expf(sm_m[w] - Mt);
+    Lt = fmaf(sm_l[w], wt, Lt);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) x[i] = fmaf(sm_o[w][HAD ? lane * VPL + i : lane], wt, x[i]);
+  }
+  const float inv = Lt > 0.0f ? 1.0f / Lt : 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) x[i] *= inv;
+  if (HAD) {
+    warp_fwht<VPL>(x, lane);
+    const float cD = inv_sqrt_dim(D);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) a.out[row * D + lane * VPL + i] = x[i] * cD;
+  } else {
+    a.out[row * D + d0 + lane] = x[0];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl) {
+  const unsigned rows = (unsigned)((size_t)a.cache.B * a.Hq * a.n_q);
+  const bool had = a.cache.layout == KVQ_HAD_INT4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows, had ? 1 : a.cache.D / 32);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  if (a.cache.D == 128)
+    return had ? cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128, true>, a)
+               : cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128, false>, a);
+  return had ? cudaLaunchKernelEx(&cfg, attend_reduce_kernel<256, true>, a)
+             : cudaLaunchKernelEx(&cfg, attend_reduce_kernel<256, false>, a);
+}
+
+}  // namespace kvq

@@ -56,6 +56,9 @@ template <int LAYOUT>
 __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const void *__restrict__ k_new,
                                                           const void *__restrict__ v_new, int dtype,
                                                           StoreGeom g) {
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.launch_dependents;");   // attention may launch and wait on us
+#endif
   const int tpr = g.D / 8;                                 // threads per row
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long r = gt / tpr;
@@ -137,6 +140,9 @@ template <int V>
 __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void *__restrict__ k_new,
                                                         const void *__restrict__ v_new, int dtype,
                                                         StoreGeom g) {
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.launch_dependents;");   // attention may launch and wait on us
+#endif
   const int lane = threadIdx.x & 31;
   const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (r >= 2 * g.rows_per_tensor) return;                  // whole warp exits together

@@ -94,6 +94,19 @@ def test_validation_without_device(L):
 def test_workspace_size_formula(L):
     c = _cache(cap=131072)
     # rows = 1*8*1, chunks = 256: m + l + o, each region rounded up to 256 bytes
-    ws = L.kvq_attend_workspace_bytes(C.byref(c), 8, 1, 131072, 0)
+    ws = L.kvq_attend_workspace_bytes(C.byref(c), 8, 1, 131072, 512)
     rows, Cc = 8, 256
     assert ws == 2 * ((rows * Cc * 4 + 255) // 256 * 256) + (rows * Cc * 128 * 4 + 255) // 256 * 256
+
+
+def test_auto_chunk_is_a_multiple_of_64():
+    c = _cache(cap=131072)
+    for kv_len in (1, 100, 4096, 131072):
+        ws = L_ws = None
+        from sub_byte_quantized_gb300 import _lib
+        Lb = _lib.lib()
+        auto = Lb.kvq_attend_workspace_bytes(C.byref(c), 8, 1, kv_len, 0)
+        assert auto > 0
+        # the automatic chunk equals one of the explicit multiples of 64
+        sizes = {Lb.kvq_attend_workspace_bytes(C.byref(c), 8, 1, kv_len, ch) for ch in range(64, 8193, 64)}
+        assert auto in sizes
