@@ -179,6 +179,32 @@ kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q
  */
 kvq_status kvq_profile_phase1_events(void *phase1_begin, void *phase1_end);
 
+/* Bytes of the device scratch array built into the library for kvq_decode_attend_static. */
+#define KVQ_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * kvq_decode_attend with no workspace argument, for callers that cannot allocate device memory
+ * themselves: for instance a plugin running inside a host engine that owns the whole device
+ * memory pool and hands out nothing beyond a layer's inputs and outputs, or code on a
+ * latency-critical thread that must not enter the CUDA allocator. This entry point has no
+ * counterpart in the paper; it exists only for such callers.
+ *   Arguments, layouts and results are those of kvq_decode_attend. The split-K partials live in
+ *   one device array of KVQ_STATIC_SCRATCH_BYTES that is part of the library: every device that
+ *   loads the library holds it until the process exits. A call whose partials would not fit
+ *   (see kvq_attend_workspace_bytes) returns KVQ_EWORKSPACE and enqueues nothing.
+ *   Nothing is allocated or freed: no cudaMalloc/cudaFree or allocating library routine runs.
+ *   The first call made with a given device current looks up the array's device address on that
+ *   device (cudaGetSymbolAddress) and keeps it; make that first call before any stream capture.
+ *   Every call, on every stream, shares the one array, and it keeps the last call's contents
+ *   (the kernels write every partial before reading it, so nothing needs clearing). Calls whose
+ *   work overlaps on the GPU (other streams, or concurrent host threads) race on the array and
+ *   give undefined results: serialise them.
+ */
+kvq_status kvq_decode_attend_static(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                    int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t causal,
+                                    int32_t q_pos0, float attn_scale, int32_t chunk, float *out,
+                                    kvq_stream_t stream);
+
 /* Static description of a status code. */
 const char *kvq_status_string(int32_t status);
 

@@ -147,6 +147,29 @@ def decode_attend(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = F
     return out
 
 
+def decode_attend_static(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = False, q_pos0: int = 0,
+                         attn_scale: float | None = None, chunk: int = 0, out: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """decode_attend without a workspace: the library's built-in device scratch holds the partials.
+
+    For callers that cannot allocate device memory of their own. Calls share that scratch, so
+    calls that overlap on the GPU race; the first call on a device must precede stream capture.
+    """
+    _need_cuda("q", q)
+    B, Hq, n_q, D = q.shape
+    if B != cache.batch or D != cache.head_dim:
+        raise ValueError("q shape does not match the cache")
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    _need_cuda("out", out)
+    L.check(L.lib().kvq_decode_attend_static(C.byref(cache.struct), q.data_ptr(), _DTYPES[q.dtype], Hq, n_q,
+                                             kv_len, int(bool(causal)), q_pos0, float(attn_scale), chunk,
+                                             out.data_ptr(), _stream(stream)), "kvq_decode_attend_static")
+    return out
+
+
 def debug_scores_i32(cache: KVCache, q: torch.Tensor, kv_len: int, stream=None):
     """Hadamard-int4 exact integer body scores [B][H_q][n_q][kv_len - n_window] and the int8 row scales."""
     _need_cuda("q", q)

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "kvq_internal.cuh"
 
@@ -284,3 +285,67 @@ kvq_status kvq_profile_phase1_events(void *phase1_begin, void *phase1_end) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ allocation-free attention
+// kvq_decode_attend_static: the same two-phase attention as kvq_decode_attend, for callers that
+// cannot hand the library a workspace of their own. Its scratch is one file-scope device array
+// of KVQ_STATIC_SCRATCH_BYTES, present on every device that loads the library for the life of
+// the process. Host code resolves the array's device address with cudaGetSymbolAddress (the
+// array's name is only a host-side stand-in) once per device, on the first call made with that
+// device current, and keeps it.
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[KVQ_STATIC_SCRATCH_BYTES];
+std::mutex g_static_mu;
+void *g_static_ptr[kvq::kMaxDevices] = {};
+
+cudaError_t static_scratch_of_current_device(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kvq::kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" kvq_status kvq_decode_attend_static(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                               int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t causal,
+                                               int32_t q_pos0, float attn_scale, int32_t chunk, float *out,
+                                               kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  size_t need = 0;
+  kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  if (q_dtype < KVQ_F32 || q_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown q dtype %d", q_dtype);
+  if (!q || !out) return fail(KVQ_EINVAL, "q/out is NULL");
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(KVQ_EALIGN, "q/out not 16-byte aligned");
+  if (!(attn_scale == attn_scale) || attn_scale > 3.0e38f || attn_scale < -3.0e38f)
+    return fail(KVQ_EINVAL, "attn_scale must be finite");
+  if (need > (size_t)KVQ_STATIC_SCRATCH_BYTES)
+    return fail(KVQ_EWORKSPACE, "call needs %zu bytes of scratch; the built-in scratch holds %zu", need,
+                (size_t)KVQ_STATIC_SCRATCH_BYTES);
+  void *ws = nullptr;
+  cudaError_t e = static_scratch_of_current_device(&ws);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "built-in scratch address: %s", cudaGetErrorString(e));
+  resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, ws);
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.scale = attn_scale;
+  a.out = out;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (a.cache.layout == KVQ_HAD_INT4) e = kvq::launch_had_prep(a, s);
+  if (e == cudaSuccess) e = kvq::mma_supported(a) ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
+  if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
