@@ -143,9 +143,10 @@ int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t kv_len, int32_t chunk);
  * head attends tokens t < kv_len and, when causal != 0, t <= q_pos0 + i ([TR] causal
  * masking); a causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len.
  * score = attn_scale * q . k_hat. Phase 1 splits the tokens into chunks of `chunk` tokens
- * (a multiple of 64 in [64, 8192], e.g. 512 as in [OTQ]; 0 = automatic: the smallest multiple
- * of 64 that covers all (batch, kv head) bodies with one chunk per resident warp of the current
- * device, so the split depends on the device's SM count) and writes per (row, chunk) the
+ * (a multiple of 64 in [64, 8192], e.g. 512 as in [OTQ]; 0 = automatic: four times the
+ * smallest multiple of 64 that covers all (batch, kv head) bodies with one slice per resident
+ * warp of the current device, so the split depends on the device's SM count) and writes per
+ * (row, chunk) the
  * running max, the sum of exponentials and the unnormalised output to the workspace; phase 2
  * combines them with the online-softmax correction ([OTQ] Section 3.2). HAD_INT4: the query
  * is rotated and quantised to int8 (one f32 scale per row, amax / 127), body tokens are

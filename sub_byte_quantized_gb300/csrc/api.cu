@@ -90,15 +90,15 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
   return KVQ_OK;
 }
 
-// Automatic split-K chunk: the smallest multiple of 64 tokens such that one chunk per warp
-// covers the body of every (batch, kv head) in a single wave of resident warps (12 per SM).
+// Automatic split-K chunk: four times the smallest multiple of 64 tokens that lets one slice per
+// resident warp of the tensor-core kernel (four warps per chunk) cover the body of every (batch, kv head) in a
+// single wave.
 int auto_chunk(int n_body, int n_heads) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long warps = (long long)sms * 12;
+  const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
   const long long per = ((long long)(n_body > 0 ? n_body : 1) * n_heads + warps - 1) / warps;
-  long long chunk = (per + 63) / 64 * 64;
-  if (chunk < 64) chunk = 64;
+  long long chunk = 4 * ((per + 63) / 64 * 64);
   if (chunk > 8192) chunk = 8192;
   return (int)chunk;
 }

@@ -21,10 +21,10 @@
 // V (two tokens, 4 consecutive dims). The nibbles become f16 pairs with one lop3 (mask + magic
 // exponent 0x6400, the Q4_0 sign flip folded in) and one f16 subtract/fma, all exact.
 //
-// Each warp handles one whole chunk of one (batch, kv head): it streams the chunk through
-// its private two-stage shared-memory ring, keeps the online softmax state in registers and
-// writes one (m, l, o) partial per query row. A CTA is four such independent warps (four
-// consecutive chunks of the same kv head); there is no block-level barrier.
+// Each CTA handles one chunk of one (batch, kv head); each of its four warps streams a contiguous
+// quarter of the chunk through a private two-stage shared-memory ring and keeps its online
+// softmax state in registers. At the end the warps combine their states in shared memory and
+// the CTA writes one (m, l, o) partial per query row.
 #include <cfloat>
 #include <climits>
 
@@ -34,15 +34,18 @@ namespace kvq {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStage = 64;              // tokens per pipeline stage
+constexpr int kStage = 64;              // tokens per pipeline stage (four 16-token tiles)
+constexpr int kTiles = kStage / 16;
+constexpr int kMinBlocks = KVQ_MMA_MIN_BLOCKS; // resident CTAs per SM
 constexpr int kD = 128;
 constexpr int kRowBytes = 64;
-constexpr int kOffV = 4096, kOffSK = 8192, kOffSV = 8704, kOffZK = 9216, kOffZV = 9728;
+constexpr int kOffV = kStage * 64, kOffSK = 2 * kStage * 64, kOffSV = kOffSK + kStage * 8;
+constexpr int kOffZK = kOffSV + kStage * 8, kOffZV = kOffZK + kStage * 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <bool ASYM>
-__host__ __device__ constexpr int stage_bytes() { return ASYM ? 10240 : 9216; }
+__host__ __device__ constexpr int stage_bytes() { return 2 * kStage * 64 + (ASYM ? 4 : 2) * kStage * 8; }
 template <bool ASYM>
 __host__ __device__ constexpr int smem_bytes() { return kWarps * 2 * stage_bytes<ASYM>(); }
 
@@ -116,7 +119,11 @@ constexpr uint32_t kHm1024 = 0xE400E400u, kHm64 = 0xD400D400u;
 // of 1024 (0x6400); one f16 add/fma removes the offset.
 template <bool ASYM>
 __device__ __forceinline__ void unpack8(uint32_t w, uint32_t (&o)[4]) {
+#if KVQ_SHIFT_ON_FMA_PIPE
+  const uint32_t w8 = __umulhi(w, 1u << 24);             // w >> 8 on the integer multiply-add pipe
+#else
   const uint32_t w8 = w >> 8;
+#endif
   if (!ASYM) {
     // (w & mask) ^ (0x6400 | 8 in each field): 1024 + (n ^ 8), or 1024 + 16 (n ^ 8) for the high field
     o[0] = hadd2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u), kHm1032);
@@ -142,7 +149,7 @@ __device__ __forceinline__ uint32_t swz(int row, int j) {
 }
 
 template <bool ASYM, bool QSPLIT>
-__global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
@@ -151,9 +158,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
   const CacheView &cv = a.cache;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  // One chunk per warp; the warps of a CTA are independent (no block-level barrier below).
-  const int chunk_id = blockIdx.x * kWarps + warp;
-  if (chunk_id >= a.n_chunks) return;
+  // One chunk per CTA; warp w takes a contiguous quarter of the chunk's 64-token stages.
+  const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
   const int R = a.gqa * a.n_q;
@@ -168,7 +174,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
   }
   if (t0 > w_lim) return;                              // no row sees this chunk (phase 2 skips it)
   const int t_end = min(t1, w_lim + 1);
-  const int n_mine = (t_end - t0 + kStage - 1) / kStage;
+  const int n_stages = (t_end - t0 + kStage - 1) / kStage;
+  const int spw = (n_stages + kWarps - 1) / kWarps;      // stages per warp
+  const int s_first = min(n_stages, warp * spw);
+  const int n_mine = min(n_stages, s_first + spw) - s_first;
+  const int tw0 = t0 + s_first * kStage;                 // this warp's first token
 
   // ---- query fragments (B operand of QK): row g of the group, dims 32b + 8c + 0..7
   uint32_t bq_hi[8][2], bq_lo[QSPLIT ? 8 : 1][2];
@@ -258,11 +268,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
 
   auto issue = [&](int i) {
     if (i < n_mine) {
-      const int ts = t0 + i * kStage;
+      const int ts = tw0 + i * kStage;
       uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
       const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kStage / 8; ++k) {
         const int q = lane + 32 * k;                     // 16-byte piece: row q/4, column q%4
         const int row = q >> 2, j = q & 3;
         const bool ok = ts + row < t_end;
@@ -271,7 +281,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
         cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
       }
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < kStage / 32; ++k) {
         const int row = lane + 32 * k;
         const bool ok = ts + row < t_end;
         const size_t off = (size_t)(ok ? ts + row : t0) * 4;
@@ -306,12 +316,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
     __syncwarp();
     const uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
     const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
-    const int ts = t0 + i * kStage;
+    const int ts = tw0 + i * kStage;
 
     // ---------------- scores S^T for the 4 tiles of the stage
-    float s[4][4];
+    float s[kTiles][4];
 #pragma unroll
-    for (int tile = 0; tile < 4; ++tile) {
+    for (int tile = 0; tile < kTiles; ++tile) {
       uint32_t kw[2][4];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
     // ---------------- mask (only at the chunk tail or a causal boundary)
     if (ts + kStage > t1 || ts + kStage - 1 > min_lim) {
 #pragma unroll
-      for (int tile = 0; tile < 4; ++tile) {
+      for (int tile = 0; tile < kTiles; ++tile) {
         const int ta = ts + tile * 16 + g, tb = ta + 8;
         if (!(ta < t1 && ta <= lim0)) s[tile][0] = -INFINITY;
         if (!(ta < t1 && ta <= lim1)) s[tile][1] = -INFINITY;
@@ -378,10 +388,12 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
       }
     }
     // ---------------- online softmax (base 2), rows r0 / r1
-    float mx0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-    mx0 = fmaxf(mx0, fmaxf(fmaxf(s[2][0], s[2][2]), fmaxf(s[3][0], s[3][2])));
-    float mx1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
-    mx1 = fmaxf(mx1, fmaxf(fmaxf(s[2][1], s[2][3]), fmaxf(s[3][1], s[3][3])));
+    float mx0 = fmaxf(s[0][0], s[0][2]), mx1 = fmaxf(s[0][1], s[0][3]);
+#pragma unroll
+    for (int tile = 1; tile < kTiles; ++tile) {
+      mx0 = fmaxf(mx0, fmaxf(s[tile][0], s[tile][2]));
+      mx1 = fmaxf(mx1, fmaxf(s[tile][1], s[tile][3]));
+    }
 #pragma unroll
     for (int k = 4; k < 32; k <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, k));
@@ -407,7 +419,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
       }
     }
 #pragma unroll
-    for (int tile = 0; tile < 4; ++tile) {
+    for (int tile = 0; tile < kTiles; ++tile) {
       s[tile][0] = ex2(s[tile][0] - mu0);
       s[tile][1] = ex2(s[tile][1] - mu1);
       s[tile][2] = ex2(s[tile][2] - mu0);
@@ -418,7 +430,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
 
     // ---------------- O^T += V^T . (P * s_v)^T per 32-dim block
 #pragma unroll
-    for (int tile = 0; tile < 4; ++tile) {
+    for (int tile = 0; tile < kTiles; ++tile) {
       uint32_t vw[2][4];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -483,27 +495,48 @@ __global__ void __launch_bounds__(kWarps * 32, 3) attend_mma_kernel(AttendArgs a
     }
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();                                       // every warp is done with its stages
 
-  // ---------------- this warp's partial for query rows r0 / r1
+  // ---------------- combine the four warps in shared memory: cm/cl [warp][8], co [warp][8][128]
+  float *cm = reinterpret_cast<float *>(smem);
+  float *cl = cm + kWarps * 8;
+  float *co = cl + kWarps * 8;
+  if (g == 0) {
+    cm[warp * 8 + r0] = m0;
+    cm[warp * 8 + r1] = m1;
+    cl[warp * 8 + r0] = l0;
+    cl[warp * 8 + r1] = l1;
+  }
 #pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int r = k ? r1 : r0;
-    if (r >= R || t0 > row_limit_of(a, r)) continue;     // phase 2 reads no partial for it
+  for (int b = 0; b < 4; ++b) {
+    const float z0 = ASYM ? zacc0[b] : 0.0f, z1 = ASYM ? zacc1[b] : 0.0f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int d = 32 * b + 4 * g + 2 * h;
+      *reinterpret_cast<float2 *>(co + (warp * 8 + r0) * kD + d) = make_float2(O[b][h][0] + z0, O[b][h][2] + z0);
+      *reinterpret_cast<float2 *>(co + (warp * 8 + r1) * kD + d) = make_float2(O[b][h][1] + z1, O[b][h][3] + z1);
+    }
+  }
+  __syncthreads();
+  const int d = threadIdx.x;                             // 128 threads <-> 128 dims
+  for (int r = 0; r < R; ++r) {
+    if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
+    float L = 0.0f, acc = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float wt = cm[w * 8 + r] == -INFINITY ? 0.0f : ex2(cm[w * 8 + r] - M);
+      L = fmaf(cl[w * 8 + r], wt, L);
+      acc = fmaf(co[(w * 8 + r) * kD + d], wt, acc);
+    }
     const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
     const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
-    float *po = a.part_o + pi * kD;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float z = ASYM ? (k ? zacc1[b] : zacc0[b]) : 0.0f;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int d = 32 * b + 4 * g + 2 * h;
-        *reinterpret_cast<float2 *>(po + d) = make_float2(O[b][h][k] + z, O[b][h][k + 2] + z);
-      }
-    }
-    if (g == 0) {
-      a.part_m[pi] = (k ? m1 : m0) * kLn2;               // natural-log units, like the other kernels
-      a.part_l[pi] = k ? l1 : l0;
+    a.part_o[pi * kD + d] = acc;
+    if (d == 0) {
+      a.part_m[pi] = M * kLn2;                           // natural-log units, like the other kernels
+      a.part_l[pi] = L;
     }
   }
 }
@@ -522,7 +555,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.n_chunks + kWarps - 1) / kWarps, a.cache.B * a.cache.H);
+  cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = smem_bytes<ASYM>();
   cfg.stream = st;

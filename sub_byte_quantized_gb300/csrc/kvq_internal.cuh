@@ -13,6 +13,16 @@ namespace kvq {
 constexpr int kBlock = 32;          // values per Q4_0 / Q6_0 / asymmetric block
 constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-up
 
+// Tensor-core phase 1: resident CTAs (of four warps) per SM the kernel is built for; the
+// automatic split-K chunk sizes one wave of that many warps.
+#ifndef KVQ_MMA_MIN_BLOCKS
+#define KVQ_MMA_MIN_BLOCKS 3
+#endif
+#ifndef KVQ_SHIFT_ON_FMA_PIPE
+#define KVQ_SHIFT_ON_FMA_PIPE 0
+#endif
+constexpr int kMmaWarpsPerSm = 4 * KVQ_MMA_MIN_BLOCKS;
+
 // Device-side view of a cache; index 0 = K, 1 = V.
 struct CacheView {
   int layout, B, H, D, cap, n_recent;
