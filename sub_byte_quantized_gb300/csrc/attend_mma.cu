@@ -11,7 +11,8 @@
 // Exactness: 4-bit codes are exact in f16; queries given in bf16/f16 are exact in f16 after a
 // per-row power-of-two prescale (f32 queries are split into hi + lo f16 parts); the block
 // scale of K (per token and 32-dim block) multiplies each block's f32 partial sum; the block
-// scale of V is folded into the probabilities, P' = p * s_v, split into hi + lo f16 parts.
+// scale of V is folded into the probabilities, P' = p * s_v, kept as hi + lo f16 parts (p is
+// split once per tile, and each block's scale is applied with an exact f16 TwoProduct).
 //
 // Data movement: each warp pulls its chunk HBM -> shared memory in 64-token stages with
 // 16-byte cp.async (two stages in flight per warp). Payload rows
@@ -106,6 +107,12 @@ __device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t d;
   asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
 
@@ -271,25 +278,47 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       const int ts = tw0 + i * kStage;
       uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
       const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
+      if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
+        const uint8_t *kps = kp + (size_t)ts * kRowBytes, *vps = vp + (size_t)ts * kRowBytes;
 #pragma unroll
-      for (int k = 0; k < kStage / 8; ++k) {
-        const int q = lane + 32 * k;                     // 16-byte piece: row q/4, column q%4
-        const int row = q >> 2, j = q & 3;
-        const bool ok = ts + row < t_end;
-        const size_t off = (size_t)(ok ? ts + row : t0) * kRowBytes + 16 * j;
-        cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
-        cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
-      }
+        for (int k = 0; k < kStage / 8; ++k) {
+          const int q = lane + 32 * k;                   // 16-byte piece: row q/4, column q%4
+          const int row = q >> 2, j = q & 3;
+          cp_async16(sK + swz(row, j), kps + 16 * q, 16);
+          cp_async16(sV + swz(row, j), vps + 16 * q, 16);
+        }
 #pragma unroll
-      for (int k = 0; k < kStage / 32; ++k) {
-        const int row = lane + 32 * k;
-        const bool ok = ts + row < t_end;
-        const size_t off = (size_t)(ok ? ts + row : t0) * 4;
-        cp_async8(smem_addr(sb + kOffSK + row * 8), ksc + off, ok ? 8 : 0);
-        cp_async8(smem_addr(sb + kOffSV + row * 8), vsc + off, ok ? 8 : 0);
-        if (ASYM) {
-          cp_async8(smem_addr(sb + kOffZK + row * 8), kz + off, ok ? 8 : 0);
-          cp_async8(smem_addr(sb + kOffZV + row * 8), vz + off, ok ? 8 : 0);
+        for (int k = 0; k < kStage / 32; ++k) {
+          const int row = lane + 32 * k;
+          const size_t off = (size_t)(ts + row) * 4;
+          cp_async8(smem_addr(sb + kOffSK + row * 8), ksc + off, 8);
+          cp_async8(smem_addr(sb + kOffSV + row * 8), vsc + off, 8);
+          if (ASYM) {
+            cp_async8(smem_addr(sb + kOffZK + row * 8), kz + off, 8);
+            cp_async8(smem_addr(sb + kOffZV + row * 8), vz + off, 8);
+          }
+        }
+      } else {                                           // tail stage: rows past t_end are zero-filled
+#pragma unroll
+        for (int k = 0; k < kStage / 8; ++k) {
+          const int q = lane + 32 * k;
+          const int row = q >> 2, j = q & 3;
+          const bool ok = ts + row < t_end;
+          const size_t off = (size_t)(ok ? ts + row : t0) * kRowBytes + 16 * j;
+          cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
+          cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kStage / 32; ++k) {
+          const int row = lane + 32 * k;
+          const bool ok = ts + row < t_end;
+          const size_t off = (size_t)(ok ? ts + row : t0) * 4;
+          cp_async8(smem_addr(sb + kOffSK + row * 8), ksc + off, ok ? 8 : 0);
+          cp_async8(smem_addr(sb + kOffSV + row * 8), vsc + off, ok ? 8 : 0);
+          if (ASYM) {
+            cp_async8(smem_addr(sb + kOffZK + row * 8), kz + off, ok ? 8 : 0);
+            cp_async8(smem_addr(sb + kOffZV + row * 8), vz + off, ok ? 8 : 0);
+          }
         }
       }
     }
@@ -438,12 +467,29 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
         ldsm_x4_t(sV + swz(row, 2 * half + (mi >> 1)), vw[half]);
       }
-      const uint2 svg = *reinterpret_cast<const uint2 *>(sb + kOffSV + (tile * 16 + g) * 8);
-      const uint2 svg8 = *reinterpret_cast<const uint2 *>(sb + kOffSV + (tile * 16 + g + 8) * 8);
-      const float2 v01 = __half22float2(u32_as_h2(svg.x)), v23 = __half22float2(u32_as_h2(svg.y));
-      const float2 w01 = __half22float2(u32_as_h2(svg8.x)), w23 = __half22float2(u32_as_h2(svg8.y));
-      const float svg_f[4] = {v01.x, v01.y, v23.x, v23.y};
-      const float svg8_f[4] = {w01.x, w01.y, w23.x, w23.y};
+      // p -> exact hi + lo f16 parts, transposed once into the B layout: each f16 pair holds one
+      // query row g and two consecutive tokens (2c, 2c+1) or (2c+8, 2c+9)
+      uint32_t bh0, bh1, bl0, bl1;
+      {
+        const uint32_t h01 = pack_f16x2(s[tile][0], s[tile][1]), h23 = pack_f16x2(s[tile][2], s[tile][3]);
+        const float2 f01 = __half22float2(u32_as_h2(h01)), f23 = __half22float2(u32_as_h2(h23));
+        const uint32_t l01 = pack_f16x2(s[tile][0] - f01.x, s[tile][1] - f01.y);
+        const uint32_t l23 = pack_f16x2(s[tile][2] - f23.x, s[tile][3] - f23.y);
+        bh0 = movm_t(h01);
+        bh1 = movm_t(h23);
+        bl0 = movm_t(l01);
+        bl1 = movm_t(l23);
+      }
+      // V block scales paired the same way: (s_v[2c][b], s_v[2c+1][b]), (s_v[2c+8][b], s_v[2c+9][b])
+      const uint8_t *svb = sb + kOffSV + tile * 16 * 8;
+      const uint2 sa = *reinterpret_cast<const uint2 *>(svb + (2 * c) * 8);
+      const uint2 sbv = *reinterpret_cast<const uint2 *>(svb + (2 * c + 1) * 8);
+      const uint2 sc = *reinterpret_cast<const uint2 *>(svb + (2 * c + 8) * 8);
+      const uint2 sd = *reinterpret_cast<const uint2 *>(svb + (2 * c + 9) * 8);
+      const uint32_t sp0[4] = {__byte_perm(sa.x, sbv.x, 0x5410), __byte_perm(sa.x, sbv.x, 0x7632),
+                               __byte_perm(sa.y, sbv.y, 0x5410), __byte_perm(sa.y, sbv.y, 0x7632)};
+      const uint32_t sp1[4] = {__byte_perm(sc.x, sd.x, 0x5410), __byte_perm(sc.x, sd.x, 0x7632),
+                               __byte_perm(sc.y, sd.y, 0x5410), __byte_perm(sc.y, sd.y, 0x7632)};
       if (ASYM) {
         const uint2 zg = *reinterpret_cast<const uint2 *>(sb + kOffZV + (tile * 16 + g) * 8);
         const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + kOffZV + (tile * 16 + g + 8) * 8);
@@ -459,22 +505,21 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       }
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const float p0 = s[tile][0] * svg_f[b], p1 = s[tile][1] * svg_f[b];
-        const float p2 = s[tile][2] * svg8_f[b], p3 = s[tile][3] * svg8_f[b];
-        const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
-        const float2 f01 = __half22float2(u32_as_h2(h01)), f23 = __half22float2(u32_as_h2(h23));
-        const uint32_t l01 = pack_f16x2(p0 - f01.x, p1 - f01.y), l23 = pack_f16x2(p2 - f23.x, p3 - f23.y);
-        const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23), bl0 = movm_t(l01), bl1 = movm_t(l23);
+        // P' = (p_hi + p_lo) * s_v split into hi + lo f16 exactly enough (TwoProduct with f16 fma):
+        //   hi = rn(p_hi * s),  r = p_hi * s - hi (exact),  lo = rn(p_lo * s + r)
+        const uint32_t hi0 = hmul2(bh0, sp0[b]), hi1 = hmul2(bh1, sp1[b]);
+        const uint32_t r0 = hfma2(bh0, sp0[b], hi0 ^ 0x80008000u), r1 = hfma2(bh1, sp1[b], hi1 ^ 0x80008000u);
+        const uint32_t lo0 = hfma2(bl0, sp0[b], r0), lo1 = hfma2(bl1, sp1[b], r1);
         // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
         uint32_t ua[4], ub[4];
         unpack8<ASYM>(vw[b >> 1][(b & 1) * 2 + 0], ua);
         unpack8<ASYM>(vw[b >> 1][(b & 1) * 2 + 1], ub);
         const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};   // dims 4g+0 (row g), 4g+1 (row g+8)
         const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};   // dims 4g+2, 4g+3
-        mma16816(O[b][0], A0, bh0, bh1);
-        mma16816(O[b][0], A0, bl0, bl1);
-        mma16816(O[b][1], A1, bh0, bh1);
-        mma16816(O[b][1], A1, bl0, bl1);
+        mma16816(O[b][0], A0, hi0, hi1);
+        mma16816(O[b][0], A0, lo0, lo1);
+        mma16816(O[b][1], A1, hi0, hi1);
+        mma16816(O[b][1], A1, lo0, lo1);
       }
     }
     __syncwarp();                                        // buffer fully read before reuse
