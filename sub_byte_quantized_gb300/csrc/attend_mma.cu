@@ -145,6 +145,27 @@ __device__ __forceinline__ void unpack8(uint32_t w, uint32_t (&o)[4]) {
   }
 }
 
+// K operand: the same four pairs as unpack8, but each code u (Q4_0: u = n ^ 8, the code plus 8;
+// asymmetric: u = n) is placed in the mantissa of an f16 with a zero exponent, i.e. the exact
+// subnormal u * 2^-24 (high fields: 16 u * 2^-24). One lop3 per pair, no f16 arithmetic. The
+// query entries facing high fields are divided by 16, the 2^-24 goes into the row's scale and
+// the Q4_0 offset -8 * sum(q) into the accumulator's initial value.
+template <bool ASYM>
+__device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  if (!ASYM) {
+    o[0] = lop3<0x6a>(w, 0x000F000Fu, 0x00080008u);
+    o[1] = lop3<0x6a>(w, 0x00F000F0u, 0x00800080u);
+    o[2] = lop3<0x6a>(w8, 0x000F000Fu, 0x00080008u);
+    o[3] = lop3<0x6a>(w8, 0x00F000F0u, 0x00800080u);
+  } else {
+    o[0] = w & 0x000F000Fu;
+    o[1] = w & 0x00F000F0u;
+    o[2] = w8 & 0x000F000Fu;
+    o[3] = w8 & 0x00F000F0u;
+  }
+}
+
 __device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
   const int qi = r % a.n_q;
   return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
@@ -189,8 +210,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
 
   // ---- query fragments (B operand of QK): row g of the group, dims 32b + 8c + 0..7
   uint32_t bq_hi[8][2], bq_lo[QSPLIT ? 8 : 1][2];
-  float qsum[4];                                        // ASYM: per-block sum of q (row g)
-  float row_alpha;                                      // alpha * 2^e * log2(e) for row g
+  float qsum[4];                                        // per-block sum of the prescaled q (row g)
+  float row_alpha;                                      // alpha * 2^e * 2^24 * log2(e) for row g
   {
     float x[4][8];
     const bool live = g < R;
@@ -214,9 +235,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     // power-of-two prescale so that the row's largest |q| lands in [2^13, 2^14): exact, and
     // safe from f16 overflow; the inverse scale goes into the row's alpha.
     int e = 0;
-    if (mx > 0.0f) e = max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - 13, -100);
+    if (mx > 0.0f) e = min(max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - 13, -100), 100);
     const float pre = ldexpf(1.0f, -e), post = ldexpf(1.0f, e);
-    row_alpha = a.scale * post * kLog2e;
+    row_alpha = a.scale * post * 16777216.0f * kLog2e;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       float s = 0.0f;
@@ -231,33 +252,37 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       qsum[b] = s;
 #pragma unroll
       for (int st = 0; st < 2; ++st) {
+        // odd dims face the high 4-bit fields (16 u * 2^-24): their query entries are / 16
         bq_hi[2 * b + st][0] = pack_f16x2(h[2 * st], h[2 * st + 4]);
-        bq_hi[2 * b + st][1] = pack_f16x2(h[2 * st + 1], h[2 * st + 5]);
+        bq_hi[2 * b + st][1] = pack_f16x2(h[2 * st + 1] * 0.0625f, h[2 * st + 5] * 0.0625f);
         if (QSPLIT) {
           bq_lo[2 * b + st][0] = pack_f16x2(l[2 * st], l[2 * st + 4]);
-          bq_lo[2 * b + st][1] = pack_f16x2(l[2 * st + 1], l[2 * st + 5]);
+          bq_lo[2 * b + st][1] = pack_f16x2(l[2 * st + 1] * 0.0625f, l[2 * st + 5] * 0.0625f);
         }
       }
     }
-    if (ASYM) {
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 1);
-        qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 2);
-      }
+    for (int b = 0; b < 4; ++b) {
+      qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 1);
+      qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 2);
     }
   }
   // the thread's two S^T columns are query rows 2c and 2c+1
   const int r0 = 2 * c, r1 = 2 * c + 1;
   const float alpha0 = __shfl_sync(0xffffffffu, row_alpha, r0 * 4);
   const float alpha1 = __shfl_sync(0xffffffffu, row_alpha, r1 * 4);
+  // zq: per-block row sums of q in accumulator units (x 2^-24). ASYM: multiplied by each token's
+  // zero-point; Q4_0: -8 zq is the accumulator's initial value (the codes enter as code + 8).
   float zq0[4], zq1[4];
-  if (ASYM) {
+  {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      // alpha * zero-point contributions use the prescaled row sums
-      zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4);
-      zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4);
+      zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * 5.9604644775390625e-8f;
+      zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * 5.9604644775390625e-8f;
+      if (!ASYM) {
+        zq0[b] *= -8.0f;
+        zq1[b] *= -8.0f;
+      }
     }
   }
   const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
@@ -378,11 +403,19 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       for (int b = 0; b < 4; ++b) {
         // kw[b/2][(b%2)*2 + 0] = (token g, block b); [.. + 1] = (token g+8, block b)
         uint32_t ug[4], u8[4];
-        unpack8<ASYM>(kw[b >> 1][(b & 1) * 2 + 0], ug);
-        unpack8<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
+        unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 0], ug);
+        unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
         const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
         const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        float d[4];
+        if (ASYM) {
+          d[0] = d[1] = d[2] = d[3] = 0.0f;
+        } else {
+          d[0] = zq0[b];
+          d[1] = zq1[b];
+          d[2] = zq0[b];
+          d[3] = zq1[b];
+        }
         mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
         mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
         if (QSPLIT) {
@@ -435,16 +468,19 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     m1 = mn1;
     l0 *= corr0;
     l1 *= corr1;
+    // once the running maxima settle, corr is exactly 1 for every row: skip the rescale
+    if (__any_sync(0xffffffffu, corr0 != 1.0f || corr1 != 1.0f)) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      zacc0[b] *= corr0;
-      zacc1[b] *= corr1;
+      for (int b = 0; b < 4; ++b) {
+        zacc0[b] *= corr0;
+        zacc1[b] *= corr1;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        O[b][h][0] *= corr0;
-        O[b][h][1] *= corr1;
-        O[b][h][2] *= corr0;
-        O[b][h][3] *= corr1;
+        for (int h = 0; h < 2; ++h) {
+          O[b][h][0] *= corr0;
+          O[b][h][1] *= corr1;
+          O[b][h][2] *= corr0;
+          O[b][h][3] *= corr1;
+        }
       }
     }
 #pragma unroll
