@@ -96,7 +96,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
-__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
 
 __device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
@@ -116,40 +115,27 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// f16x2 constants (bit patterns): 1/16, -1032, -72, -1024, -64 in both halves.
+// f16x2 constants (bit patterns): 1/16, -1032, -72 in both halves.
 constexpr uint32_t kH16th = 0x2C002C00u, kHm1032 = 0xE408E408u, kHm72 = 0xD480D480u;
-constexpr uint32_t kHm1024 = 0xE400E400u, kHm64 = 0xD400D400u;
 
-// Eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
-// (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the code values: Q4_0 (signed: (n ^ 8) - 8) or
-// the unsigned asymmetric code n. One lop3 places a field in the mantissa under the exponent
-// of 1024 (0x6400); one f16 add/fma removes the offset.
-template <bool ASYM>
-__device__ __forceinline__ void unpack8(uint32_t w, uint32_t (&o)[4]) {
-#if KVQ_SHIFT_ON_FMA_PIPE
-  const uint32_t w8 = __umulhi(w, 1u << 24);             // w >> 8 on the integer multiply-add pipe
-#else
+// Q4_0 V operand: eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
+// (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the signed code values (n ^ 8) - 8. One lop3 places
+// a field in the mantissa under the exponent of 1024 (0x6400) with the sign flip folded in; one
+// f16 add/fma removes the offset.
+__device__ __forceinline__ void unpack8_q4(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w8 = w >> 8;
-#endif
-  if (!ASYM) {
-    // (w & mask) ^ (0x6400 | 8 in each field): 1024 + (n ^ 8), or 1024 + 16 (n ^ 8) for the high field
-    o[0] = hadd2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u), kHm1032);
-    o[1] = hfma2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
-    o[2] = hadd2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u), kHm1032);
-    o[3] = hfma2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
-  } else {
-    o[0] = hadd2(lop3<0xea>(w, 0x000F000Fu, 0x64006400u), kHm1024);
-    o[1] = hfma2(lop3<0xea>(w, 0x00F000F0u, 0x64006400u), kH16th, kHm64);
-    o[2] = hadd2(lop3<0xea>(w8, 0x000F000Fu, 0x64006400u), kHm1024);
-    o[3] = hfma2(lop3<0xea>(w8, 0x00F000F0u, 0x64006400u), kH16th, kHm64);
-  }
+  o[0] = hadd2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u), kHm1032);
+  o[1] = hfma2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
+  o[2] = hadd2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u), kHm1032);
+  o[3] = hfma2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
 }
 
-// K operand: the same four pairs as unpack8, but each code u (Q4_0: u = n ^ 8, the code plus 8;
-// asymmetric: u = n) is placed in the mantissa of an f16 with a zero exponent, i.e. the exact
-// subnormal u * 2^-24 (high fields: 16 u * 2^-24). One lop3 per pair, no f16 arithmetic. The
-// query entries facing high fields are divided by 16, the 2^-24 goes into the row's scale and
-// the Q4_0 offset -8 * sum(q) into the accumulator's initial value.
+// K and asymmetric-V operands: the same four pairs as unpack8_q4, but each code u (Q4_0: u = n ^ 8,
+// the code plus 8; asymmetric: u = n) is placed in the mantissa of an f16 with a zero exponent,
+// i.e. the exact subnormal u * 2^-24 (high fields: 16 u * 2^-24). One lop3 per pair, no f16
+// arithmetic. For K the query entries facing high fields are divided by 16, the 2^-24 goes into
+// the row's scale and the Q4_0 offset -8 * sum(q) into the accumulator's initial value; for V the
+// output is rescaled in the epilogue and the zero-point term comes from its own small mma.
 template <bool ASYM>
 __device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w8 = w >> 8;
@@ -352,11 +338,14 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   float O[4][2][4];                                      // [block][half][c0..c3]
-  float zacc0[4], zacc1[4];                              // ASYM: sum p * z_v per block, rows r0/r1
+  // ASYM: Dw[b][r] = sum_t p_t * z_v[t][b] (the zero-point term), from a small extra mma per
+  // tile: rows 0-3 of its accumulator are the four blocks (held by lanes with g < 4), columns
+  // the query rows.
+  float Dw[4] = {0.f, 0.f, 0.f, 0.f};
+  // selector pairing halfword (g & 1) of two words, and which word (g < 2: blocks 0,1)
+  const uint32_t wsel = (g & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    zacc0[b] = 0.0f;
-    zacc1[b] = 0.0f;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -470,10 +459,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     l1 *= corr1;
     // once the running maxima settle, corr is exactly 1 for every row: skip the rescale
     if (__any_sync(0xffffffffu, corr0 != 1.0f || corr1 != 1.0f)) {
+      Dw[0] *= corr0;
+      Dw[1] *= corr1;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        zacc0[b] *= corr0;
-        zacc1[b] *= corr1;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           O[b][h][0] *= corr0;
@@ -527,17 +516,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       const uint32_t sp1[4] = {__byte_perm(sc.x, sd.x, 0x5410), __byte_perm(sc.x, sd.x, 0x7632),
                                __byte_perm(sc.y, sd.y, 0x5410), __byte_perm(sc.y, sd.y, 0x7632)};
       if (ASYM) {
-        const uint2 zg = *reinterpret_cast<const uint2 *>(sb + kOffZV + (tile * 16 + g) * 8);
-        const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + kOffZV + (tile * 16 + g + 8) * 8);
-        const float2 a01 = __half22float2(u32_as_h2(zg.x)), a23 = __half22float2(u32_as_h2(zg.y));
-        const float2 b01 = __half22float2(u32_as_h2(zg8.x)), b23 = __half22float2(u32_as_h2(zg8.y));
-        const float zv_g[4] = {a01.x, a01.y, a23.x, a23.y};
-        const float zv_g8[4] = {b01.x, b01.y, b23.x, b23.y};
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          zacc0[b] = fmaf(s[tile][0], zv_g[b], fmaf(s[tile][2], zv_g8[b], zacc0[b]));
-          zacc1[b] = fmaf(s[tile][1], zv_g[b], fmaf(s[tile][3], zv_g8[b], zacc1[b]));
-        }
+        // W operand (zero-points): rows g < 4 hold block g's z_v for tokens (2c, 2c+1) and
+        // (2c+8, 2c+9)
+        const uint8_t *zvb = sb + kOffZV + tile * 16 * 8;
+        const uint2 wa = *reinterpret_cast<const uint2 *>(zvb + (2 * c) * 8);
+        const uint2 wb = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 1) * 8);
+        const uint2 wc = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 8) * 8);
+        const uint2 wd = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 9) * 8);
+        const bool lo2 = g < 2;
+        uint32_t w0 = __byte_perm(lo2 ? wa.x : wa.y, lo2 ? wb.x : wb.y, wsel);
+        uint32_t w1 = __byte_perm(lo2 ? wc.x : wc.y, lo2 ? wd.x : wd.y, wsel);
+        if (g >= 4) w0 = w1 = 0u;
+        const uint32_t Aw[4] = {w0, 0u, w1, 0u};
+        mma16816(Dw, Aw, bh0, bh1);
+        mma16816(Dw, Aw, bl0, bl1);
       }
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -547,9 +539,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         const uint32_t r0 = hfma2(bh0, sp0[b], hi0 ^ 0x80008000u), r1 = hfma2(bh1, sp1[b], hi1 ^ 0x80008000u);
         const uint32_t lo0 = hfma2(bl0, sp0[b], r0), lo1 = hfma2(bl1, sp1[b], r1);
         // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
+        // Q4_0: exact signed code values (f16 fix-up); asymmetric: subnormal codes u * 2^-24
         uint32_t ua[4], ub[4];
-        unpack8<ASYM>(vw[b >> 1][(b & 1) * 2 + 0], ua);
-        unpack8<ASYM>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+        if (ASYM) {
+          unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 0], ua);
+          unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+        } else {
+          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
+          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
+        }
         const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};   // dims 4g+0 (row g), 4g+1 (row g+8)
         const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};   // dims 4g+2, 4g+3
         mma16816(O[b][0], A0, hi0, hi1);
@@ -567,13 +565,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   for (int k = 4; k < 32; k <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, k);
     l1 += __shfl_xor_sync(0xffffffffu, l1, k);
-    if (ASYM) {
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        zacc0[b] += __shfl_xor_sync(0xffffffffu, zacc0[b], k);
-        zacc1[b] += __shfl_xor_sync(0xffffffffu, zacc1[b], k);
-      }
-    }
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
   __syncthreads();                                       // every warp is done with its stages
@@ -588,14 +579,24 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     cl[warp * 8 + r0] = l0;
     cl[warp * 8 + r1] = l1;
   }
+  // Q4_0: O holds the values directly. Asymmetric: the V codes entered as u * 2^-24 (even dims,
+  // low fields) or 16 u * 2^-24 (odd dims, high fields); value = u s_v + z_v adds the W term.
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    const float z0 = ASYM ? zacc0[b] : 0.0f, z1 = ASYM ? zacc1[b] : 0.0f;
+    float w0 = 0.0f, w1 = 0.0f, se = 1.0f, so = 1.0f;
+    if (ASYM) {
+      w0 = __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);   // (block b, row r0)
+      w1 = __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);   // (block b, row r1)
+      se = 16777216.0f;
+      so = 1048576.0f;
+    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int d = 32 * b + 4 * g + 2 * h;
-      *reinterpret_cast<float2 *>(co + (warp * 8 + r0) * kD + d) = make_float2(O[b][h][0] + z0, O[b][h][2] + z0);
-      *reinterpret_cast<float2 *>(co + (warp * 8 + r1) * kD + d) = make_float2(O[b][h][1] + z1, O[b][h][3] + z1);
+      *reinterpret_cast<float2 *>(co + (warp * 8 + r0) * kD + d) =
+          make_float2(fmaf(O[b][h][0], se, w0), fmaf(O[b][h][2], so, w0));
+      *reinterpret_cast<float2 *>(co + (warp * 8 + r1) * kD + d) =
+          make_float2(fmaf(O[b][h][1], se, w1), fmaf(O[b][h][3], so, w1));
     }
   }
   __syncthreads();

@@ -18,9 +18,6 @@ constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-
 #ifndef KVQ_MMA_MIN_BLOCKS
 #define KVQ_MMA_MIN_BLOCKS 3
 #endif
-#ifndef KVQ_SHIFT_ON_FMA_PIPE
-#define KVQ_SHIFT_ON_FMA_PIPE 0
-#endif
 constexpr int kMmaWarpsPerSm = 4 * KVQ_MMA_MIN_BLOCKS;
 
 // Device-side view of a cache; index 0 = K, 1 = V.
