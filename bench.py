@@ -1,23 +1,28 @@
 #!/usr/bin/env python3
-"""Decode-layer benchmark: 128K-context Llama-3.1-70B-shaped attention layer over a Q4_0 cache.
+"""Decode-layer benchmark of the packed sub-byte KV cache.
 
-One step = one decode layer-call: append the new token's K and V (Q4_0 store, 1 launch) and run
-the split-K decode attention over all 131072 cached tokens (phase 1 + LSE reduce). The metric
-is the effective HBM bandwidth on packed KV (payload + fp16 scales) read per step, and the
-microseconds per layer-call.
+Default workload: a 128K-context Llama-3.1-70B-shaped attention layer over a Q4_0 cache. One step
+= one decode layer-call: append the new token's K and V (one store launch) and run the split-K
+decode attention over all 131072 cached tokens (phase 1 + LSE reduce). The metric is the
+effective HBM bandwidth on packed KV (payload + fp16 scales) read per step; microseconds per
+layer-call come with it. `--workload` selects another of the seeded workloads (the Llama-3-8B
+layer, the Hadamard decode or causal prefill chunk, the Q6_0 Gemma-like layer, the asymmetric
+128K layer); the default line is the 128K Q4_0 one.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
 
 Prints exactly one JSON line on rank 0. Under torchrun every rank runs its own replica of the
-workload (independent layers, no collective on the data path): weak scaling, the time is the
-max over ranks.
+workload (independent layer-calls, no collective on the data path): weak scaling, value = all
+ranks' bytes over the max-over-ranks time.
 
 Timing: W untimed warm-up steps (plus an untimed soak of --soak-s seconds so clock samples
 exist), then exactly K steps bracketed by a barrier and a device synchronise, timed with CUDA
 events on the launching stream. The K steps are captured once in a CUDA graph of the library's
-own launches and replayed. Steps rotate over several cache replicas whose total size exceeds
-L2, so no step reads a cache that is still L2-resident. Phase 1 (the streaming kernel) is
-also timed per launch with CUDA events recorded around it inside the timed region.
+own launches and replayed. Steps rotate over cache replicas whose total size exceeds L2 (for the
+small workloads whose replicas would be too many, the config says the cache is L2-resident).
+Phase 1 (the streaming kernel) is timed per launch with CUDA events in a second pass of the same
+K steps (an event between two kernels ends their programmatic launch overlap, so that pass is
+not the headline).
 """
 from __future__ import annotations
 
@@ -42,11 +47,24 @@ sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
 
+DEFAULT_WORKLOAD = "c5_q4_0_llama70b_128k"
 METRIC = "int4-KV decode attention µs/layer and effective HBM GB/s (% peak) at 128K"
-WORKLOAD = "c5_q4_0_llama70b_128k"
-VARIANT = "c5_asym4_g32_llama70b_128k"
-FALLBACK_HBM_GBS = 6800.0
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
 L2_BYTES = 129 * 2 ** 20
+DESCRIPTIONS = {
+    "c1_q4_0_tiny": "Q4_0 tiny: B1 Hq8 Hkv2 D128 S512 decode, f32 N(0,1) K/V/Q, 2 K outlier channels x8",
+    "c2_q4_0_llama3_8b": "Llama-3-8B layer: B4 Hq32 Hkv8 D128 S8192, Q4_0, bf16 Student-t(4) K/V, 4 outlier ch x10; "
+                         "append 1 token then decode-attend",
+    "c3_had_int4_decode": "Hadamard per-token int4, Qwen3-1.7B shape: B8 Hq16 Hkv8 D128 S4096, n_recent 64 f32 window",
+    "c3_had_int4_prefill": "Hadamard per-token int4, Qwen3-1.7B shape: causal prefill chunk of 256 rows at 3840 "
+                           "(B8 Hq16 Hkv8 D128, kv_len 4096, n_recent 64)",
+    "c4_q6_0_gemma": "Q6_0 Gemma-like: B2 Hq16 Hkv8 D256 S32768, attention scale 1.0, unit-RMS Q/K rows, bf16 "
+                     "Student-t(3) K/V",
+    "c5_q4_0_llama70b_128k": "Llama-3.1-70B layer, 128K context, Q4_0 KV (bf16 Student-t(4) K/V, 4 outlier channels "
+                             "x10, N(0,1) Q), B1 Hq64 Hkv8 D128",
+    "c5_asym4_g32_llama70b_128k": "Llama-3.1-70B layer, 128K context, per-group asymmetric int4 g=32 KV, "
+                                  "B1 Hq64 Hkv8 D128",
+}
 
 
 def parse():
@@ -55,8 +73,9 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(DESCRIPTIONS))
     p.add_argument("--soak-s", type=float, default=1.0, help="untimed soak before timing (0 = none)")
-    p.add_argument("--quick", action="store_true", help="device timing only (no e2e, variant, CPU baseline)")
+    p.add_argument("--quick", action="store_true", help="device timing only (no e2e, variants, CPU baseline)")
     p.add_argument("--no-graph", action="store_true", help="plain stream launches instead of a CUDA graph")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
     return p.parse_args()
@@ -67,14 +86,14 @@ def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         d = json.load(open(path))
-        return float(d["hbm_gbs"]), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def kernel_traffic(kernel_file: str, launches_per_unit=1.0):
-    """dram bytes per launch from the committed ncu summary of `kernel_file`, or None when the
-    kernel source changed since the counters were taken."""
-    path = os.path.join(ROOT, "profiles", "attend_phase1_c5_q4_0_128k.md")
+def kernel_traffic(profile: str, kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary `profile`, or None when the kernel
+    source changed since the counters were taken (the summary records the source's sha256)."""
+    path = os.path.join(ROOT, "profiles", profile)
     src = os.path.join(ROOT, "sub_byte_quantized_gb300", "csrc", kernel_file)
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
@@ -86,6 +105,21 @@ def kernel_traffic(kernel_file: str, launches_per_unit=1.0):
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_hash.group(1):
         return None
     return int(m_bytes.group(1))
+
+
+def aggregate(world: int, units_per_rank: float, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: all ranks' units over the (max-over-ranks) elapsed time, per second."""
+    return world * units_per_rank * steps / (elapsed_ms / 1e3)
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The maximum of `value` over all ranks of the default process group (identity for one rank)."""
+    import torch
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 class ClockSampler:
@@ -142,27 +176,57 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ CPU oracle baseline
-def oracle_sample(w, inp, n_heads: int):
-    """Prepare an oracle cache of the first `n_heads` kv heads (untimed) and return a step function:
-    append the last token (oracle store) + oracle decode attention over the full cache."""
+# ------------------------------------------------------------------ workload geometry
+class Spec:
+    """Shapes of one step of a workload: the cache holds S tokens; a step appends tokens
+    [fill, S) and attends n_q query rows per head (causal from q_pos0 for the prefill chunk)."""
+
+    def __init__(self, w, inp):
+        self.w = w
+        self.B, self.H, self.S, self.D = inp["k"].shape
+        self.fill = w.n_fill
+        self.n_q = inp["q"].shape[2]
+        self.causal = w.causal
+        self.q_pos0 = self.S - self.n_q if w.causal else 0
+        self.n_win = min(w.n_recent, self.S) if w.layout == "had_int4" else 0
+        nb = self.D // 32
+        row = {"q4_0": 16 * nb + 2 * nb, "q6_0": 24 * nb + 2 * nb, "asym4_g32": 16 * nb + 4 * nb,
+               "had_int4": self.D // 2 + 4}[w.layout]
+        # algorithmic bytes one attention call reads: every packed K/V row (+ scales) once; window
+        # tokens as their exact f32 rows
+        self.read_bytes = 2 * self.B * self.H * ((self.S - self.n_win) * row + self.n_win * self.D * 4)
+        # algorithmic flops of the attention call: QK and PV over every visible (row, token) pair
+        vis = 0
+        for i in range(self.n_q):
+            vis += min(self.S, self.q_pos0 + i + 1) if self.causal else self.S
+        self.flops = 4 * self.D * vis * w.n_q_heads * self.B
+
+
+# ------------------------------------------------------------------ CPU oracle (baseline and reference arm)
+def oracle_step(w, inp, n_heads: int, kv_len: int | None = None):
+    """Prepare (untimed) an oracle cache of the first `n_heads` kv heads over the workload's tokens
+    (or its first kv_len) and return a step: the oracle store of the appended tokens + the oracle
+    attention of those heads' query rows."""
     from oracle import attention as OA
-    S = inp["k"].shape[2]
-    sub_k, sub_v = inp["k"][:, :n_heads], inp["v"][:, :n_heads]
-    oc = OA.OracleCache(w.layout, w.batch, n_heads, w.head_dim, S)
-    oc.store(sub_k[:, :, :S - 1], sub_v[:, :, :S - 1], 0)
+    S = inp["k"].shape[2] if kv_len is None else kv_len
+    n_q = inp["q"].shape[2]
+    fill = min(w.n_fill, S - 1)
+    k, v = inp["k"][:, :n_heads, :S], inp["v"][:, :n_heads, :S]
+    oc = OA.OracleCache(w.layout, w.batch, n_heads, w.head_dim, S, n_recent=w.n_recent)
+    oc.store(k[:, :, :fill], v[:, :, :fill], 0)
     q = inp["q"][:, :n_heads * w.gqa]
+    causal = w.causal and S - n_q >= 0
+    q_pos0 = S - n_q if causal else 0
 
     def step():
-        oc.store(sub_k[:, :, S - 1:], sub_v[:, :, S - 1:], S - 1)
-        return oc.attend(q, w.alpha, S)
+        oc.store(k[:, :, fill:], v[:, :, fill:], fill)
+        return oc.attend(q, w.alpha, S, causal=causal, q_pos0=q_pos0)
     return step
 
 
-def cpu_baseline(w, inp, budget_s: float):
-    step = oracle_sample(w, inp, 1)
-    S = inp["k"].shape[2]
-    bytes_per = (S * 2 * (64 + 8)) * w.batch          # one kv head's packed K+V read by a step
+def cpu_baseline(w, inp, spec, budget_s: float):
+    step = oracle_step(w, inp, 1)
+    per = spec.read_bytes / spec.H          # one kv head's share of the step's packed bytes
     times = []
     t_all = time.perf_counter()
     while not times or (time.perf_counter() - t_all < budget_s and len(times) < 20):
@@ -170,39 +234,32 @@ def cpu_baseline(w, inp, budget_s: float):
         step()
         times.append(time.perf_counter() - t0)
     tm = statistics.median(times)
-    return {"value": bytes_per / tm / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"oracle store of the appended token + float64 decode attention of 1 of 8 kv heads "
-                      f"(8 query heads) over {S} tokens; median of {len(times)} runs, {tm * 1e3:.0f} ms each, "
-                      f"{bytes_per} packed bytes per run",
-            "us_per_layer_equiv": tm * 8 * 1e6}
+    return {"value": per / tm / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"oracle (numpy, one thread): store of the appended tokens + float64 attention of 1 of "
+                      f"{spec.H} kv heads over {spec.S} tokens; median of {len(times)} runs of {tm * 1e3:.0f} ms, "
+                      f"{per:.0f} packed bytes each",
+            "us_per_layer_equiv": tm * spec.H * 1e6}
 
 
-# ------------------------------------------------------------------ reference arm (the oracle)
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from synth import WORKLOADS, make_inputs
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     inp = make_inputs(w)
-    # bound the run: each step is one kv head over a token sample sized so that W + K steps
-    # take about two minutes in total
-    S = inp["k"].shape[2]
-    probe = oracle_sample(w, inp, 1)
+    spec = Spec(w, inp)
+    # bound the run: each step is one kv head over a prefix of the tokens, sized so that the
+    # W + K steps take about two minutes in total
+    probe = oracle_step(w, inp, 1)
     t0 = time.perf_counter()
     probe()
     t_full = time.perf_counter() - t0
     per_step = 120.0 / max(1, args.steps + args.warmup)
     frac = min(1.0, per_step / max(t_full, 1e-6))
-    S_s = max(1024, int(S * frac) // 512 * 512)
-    if S_s < S:
-        from synth import Workload  # noqa: F401
-        ws = w.scaled(kv_len=S_s, fill=S_s - 1)
-        sub = {k: (v[:, :, :S_s] if k in ("k", "v") else v) for k, v in inp.items()}
-        step = oracle_sample(ws, sub, 1)
-    else:
-        step = probe
-    bytes_per = S_s * 2 * (64 + 8) * w.batch
+    S_s = spec.S if frac >= 1.0 else max(min(spec.S, 1024), int(spec.S * frac) // 64 * 64)
+    step = probe if S_s == spec.S else oracle_step(w, inp, 1, kv_len=S_s)
+    bytes_per = spec.read_bytes / spec.H * S_s / spec.S
     for _ in range(args.warmup):
         step()
     t0 = time.perf_counter()
@@ -210,14 +267,15 @@ def run_reference(args):
         step()
     el = time.perf_counter() - t0
     value = bytes_per * args.steps / el / 1e9
-    sample = (f"CPU oracle (numpy, 1 thread): per step, oracle store of 1 appended token + float64 decode "
-              f"attention of 1 kv head (8 query heads) over {S_s} of {S} tokens ({bytes_per} packed bytes)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "Llama-3.1-70B layer, 128K context, Q4_0 KV (bf16 Student-t(4) K/V, "
-                                   "4 outlier channels x10), B1 Hq64 Hkv8 D128",
-                       "kv_len": S, "sampled_kv_len": S_s, "layout": "q4_0"},
+    sample = (f"CPU oracle (numpy, one thread): per step, the oracle store of the appended tokens + float64 "
+              f"attention of 1 of {spec.H} kv heads over {S_s} of {spec.S} tokens ({bytes_per:.0f} packed bytes)")
+    line = {"impl": "reference", "metric": METRIC if args.workload == DEFAULT_WORKLOAD else
+            f"{w.layout} KV attention µs/layer and effective HBM GB/s ({args.workload})",
+            "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS[args.workload], "kv_len": spec.S, "sampled_kv_len": S_s,
+                       "layout": w.layout},
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -249,41 +307,48 @@ def main():
         if world > 1:
             dist.barrier()
 
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     inp = make_inputs(w)
-    B, H, S, D = inp["k"].shape
+    spec = Spec(w, inp)
+    B, H, S, D, fill = spec.B, spec.H, spec.S, spec.D, spec.fill
 
     def to_dev(name):
-        return torch.from_numpy(np.ascontiguousarray(inp[name + "_bits"]).view(np.int16)).view(torch.bfloat16).to(dev)
+        if w.dtype == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(inp[name + "_bits"]).view(np.int16)).view(
+                torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(inp[name])).to(dev)
 
     kd, vd, q = to_dev("k"), to_dev("v"), to_dev("q")
-    k_new = kd[:, :, S - 1:].contiguous()
-    v_new = vd[:, :, S - 1:].contiguous()
+    k_new = kd[:, :, fill:].contiguous()               # the step's appended tokens
+    v_new = vd[:, :, fill:].contiguous()
 
     def make_caches(layout, n):
         caches = []
         for _ in range(n):
-            c = kvq.KVCache(layout, B, H, D, S, device=dev)
-            kvq.store(c, kd[:, :, :S - 1].contiguous(), vd[:, :, :S - 1].contiguous(), 0)
-            kvq.store(c, k_new, v_new, S - 1)
+            c = kvq.KVCache(layout, B, H, D, S, n_recent=w.n_recent, device=dev)
+            kvq.store(c, kd[:, :, :fill].contiguous(), vd[:, :, :fill].contiguous(), 0)
+            kvq.store(c, k_new, v_new, fill)
             caches.append(c)
         return caches
 
-    n_rep = max(2, math.ceil(3 * L2_BYTES / (2 * B * H * S * 72)) + 1)
-    caches = make_caches("q4_0", n_rep)
-    read_bytes = caches[0].read_bytes(S)
-    chunk = kvq.attend_chunk(caches[0], S, 0)          # automatic split: one chunk per resident warp
-    ws = torch.empty(kvq.attend_workspace_bytes(caches[0], w.n_q_heads, 1, S, chunk), dtype=torch.uint8, device=dev)
-    out = torch.empty((B, w.n_q_heads, 1, D), dtype=torch.float32, device=dev)
+    cache_bytes = spec.read_bytes
+    n_rep = min(64, max(2, math.ceil(3 * L2_BYTES / max(cache_bytes, 1)) + 1))
+    l2_resident = n_rep * cache_bytes < 2 * L2_BYTES
+    caches = make_caches(w.layout, n_rep)
+    chunk = kvq.attend_chunk(caches[0], S, 0)
+    ws = torch.empty(max(256, kvq.attend_workspace_bytes(caches[0], w.n_q_heads, spec.n_q, S, chunk)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((B, w.n_q_heads, spec.n_q, D), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     L = _lib.lib()
 
     def step(i, ev=None):
         c = caches[i % n_rep]
-        kvq.store(c, k_new, v_new, S - 1, stream=stream)
+        kvq.store(c, k_new, v_new, fill, stream=stream)
         if ev is not None:
             L.kvq_profile_phase1_events(ev[0].cuda_event, ev[1].cuda_event)
-        kvq.decode_attend(c, q, S, attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
+        kvq.decode_attend(c, q, S, causal=spec.causal, q_pos0=spec.q_pos0, attn_scale=w.alpha, chunk=chunk,
+                          out=out, workspace=ws, stream=stream)
         if ev is not None:
             L.kvq_profile_phase1_events(None, None)
 
@@ -308,7 +373,7 @@ def main():
                 step(i, ph_ev[i])
         soak_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(soak_graph, stream=stream):
-            for i in range(64):
+            for i in range(16):
                 step(i)
     torch.cuda.synchronize(dev)
 
@@ -321,7 +386,7 @@ def main():
                 if use_graph:
                     soak_graph.replay()
                 else:
-                    for i in range(64):
+                    for i in range(16):
                         step(i)
                 torch.cuda.synchronize(dev)
         barrier()
@@ -337,8 +402,6 @@ def main():
         torch.cuda.synchronize(dev)
         barrier()
         elapsed_ms = ev0.elapsed_time(ev1)
-        # phase-1 durations: the same K steps again, with CUDA events around every phase-1 launch
-        # (an event between two kernels ends their launch overlap, so this pass is not the headline)
         if use_graph:
             with torch.cuda.stream(stream):
                 ev0.record(stream)
@@ -347,48 +410,55 @@ def main():
             torch.cuda.synchronize(dev)
         ev_pass_ms = ev0.elapsed_time(ev1)
         time.sleep(0.25)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist if world > 1 else None, dev)
     ph_ms = [a.elapsed_time(b) for a, b in ph_ev]
     ph_mean = statistics.fmean(ph_ms)
     ms_step = elapsed_ms / K
-    value = world * read_bytes * K / (elapsed_ms / 1e3) / 1e9
-    peak, peak_kind = measured_peaks()
-    achieved = read_bytes / (ph_mean / 1e3) / 1e9
-    traffic = kernel_traffic("attend_mma.cu")
-    kinds = 3                                   # store + phase 1 + reduce per step
-
+    value = aggregate(world, spec.read_bytes, K, elapsed_ms) / 1e9
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    prefill = spec.causal and spec.n_q > 1
+    if prefill:
+        achieved = spec.flops / (ph_mean / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": achieved / bf16_peak, "flops_per_launch": spec.flops,
+                "peak_note": "dense bf16 peak; f16 mma has the same nominal rate"}
+    else:
+        achieved = spec.read_bytes / (ph_mean / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak}
+    traffic = None
+    if args.workload == DEFAULT_WORKLOAD:
+        traffic = kernel_traffic("attend_phase1_c5_q4_0_128k.md", "attend_mma.cu")
+    roof.update({"peak_kind": peak_kind, "traffic": traffic, "kernel": "attend phase 1 (split-K chunk partials)",
+                 "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
+                 "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3,
+                 "phase1_pass_us_per_step": ev_pass_ms / K * 1e3})
+    launches = 3 + (1 if w.layout == "had_int4" else 0)   # store, [query prep], phase 1, reduce
+    l2_note = (f"cache L2-resident ({n_rep} replicas x {cache_bytes / 2**20:.1f} MiB)" if l2_resident else
+               f"inputs larger than L2: {n_rep} cache replicas rotated ({n_rep * cache_bytes / 2**20:.0f} MiB > "
+               f"{L2_BYTES / 2**20:.0f} MiB L2)")
     line = {
-        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "metric": METRIC if args.workload == DEFAULT_WORKLOAD else
+        f"{w.layout} KV attention µs/layer and effective HBM GB/s ({args.workload})",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "Llama-3.1-70B layer, 128K context, Q4_0 KV (bf16 Student-t(4) K/V, 4 outlier "
-                               "channels x10, N(0,1) Q), B1 Hq64 Hkv8 D128",
-                   "chunk": chunk, "chunk_rule": "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp, one wave",
-                   "kv_len": S, "layout": "q4_0", "step": "append 1 token (K,V) + split-K decode attention",
-                   "read_bytes_per_step": read_bytes,
-                   "l2": f"inputs larger than L2: {n_rep} cache replicas rotated "
-                         f"({n_rep * read_bytes / 2**20:.0f} MiB > {L2_BYTES / 2**20:.0f} MiB L2)",
+        "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload, "layout": w.layout,
+                   "kv_len": S, "n_q": spec.n_q, "causal": spec.causal, "chunk": chunk,
+                   "chunk_rule": "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp",
+                   "step": f"append {S - fill} token(s) (K,V) + split-K attention",
+                   "read_bytes_per_step": spec.read_bytes, "flops_per_step": spec.flops, "l2": l2_note,
                    "timing": ("CUDA graph of the K library steps; phase 1 timed by events in a second pass "
                               "of the same K steps") if use_graph else "stream launches with phase-1 events",
                    "soak_s": args.soak_s, "parallelism": f"replicas x{world}"},
-        "pct_of_peak": value / world / peak,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": traffic, "kernel": "attend phase 1 (split-K chunk partials)",
-                     "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
-                     "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3,
-                     "phase1_pass_us_per_step": ev_pass_ms / K * 1e3},
+        "pct_of_peak": value / world / hbm_peak,
+        "roofline": roof,
         "clocks": clk.summary(),
-        "gpu_launches": kinds * K,
+        "gpu_launches": launches * K,
     }
 
     if not args.quick and rank == 0:
         # end to end through the public API from pinned host buffers, one sync per step
-        hk = k_new.cpu().pin_memory()
-        hv = v_new.cpu().pin_memory()
-        hq = q.cpu().pin_memory()
+        hk, hv, hq = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q.cpu().pin_memory()
         hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
         dk, dv, dq = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q)
         n_e2e = min(K, 500)
@@ -401,53 +471,63 @@ def main():
                 dv.copy_(hv, non_blocking=True)
                 dq.copy_(hq, non_blocking=True)
                 c = caches[i % n_rep]
-                kvq.store(c, dk, dv, S - 1, stream=stream)
-                kvq.decode_attend(c, dq, S, attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
+                kvq.store(c, dk, dv, fill, stream=stream)
+                kvq.decode_attend(c, dq, S, causal=spec.causal, q_pos0=spec.q_pos0, attn_scale=w.alpha, chunk=chunk,
+                                  out=out, workspace=ws, stream=stream)
                 hout.copy_(out, non_blocking=True)
             stream.synchronize()
         t_e2e = (time.perf_counter() - t0) / n_e2e
-        line["e2e"] = {"value": read_bytes / t_e2e / 1e9, "unit": "GB/s",
-                       "h2d_bytes_per_step": hk.numel() * 2 + hv.numel() * 2 + hq.numel() * 2,
+        el = hk.element_size()
+        line["e2e"] = {"value": spec.read_bytes / t_e2e / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": (hk.numel() + hv.numel() + hq.numel()) * el,
                        "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e}
-        line["variants"] = {}
-
-        def time_plain(cs, wsb, ch, n):
-            with torch.cuda.stream(stream):
-                for i in range(5):
-                    kvq.store(cs[i % n_rep], k_new, v_new, S - 1, stream=stream)
-                    kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
-                                      stream=stream)
-                torch.cuda.synchronize(dev)
-                ev0.record(stream)
-                for i in range(n):
-                    kvq.store(cs[i % n_rep], k_new, v_new, S - 1, stream=stream)
-                    kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
-                                      stream=stream)
-                ev1.record(stream)
-            torch.cuda.synchronize(dev)
-            return ev0.elapsed_time(ev1) / n
-        ws512 = torch.empty(kvq.attend_workspace_bytes(caches[0], w.n_q_heads, 1, S, 512), dtype=torch.uint8,
-                            device=dev)
-        c_ms = time_plain(caches, ws512, 512, min(K, 1000))
-        line["variants"]["q4_0_chunk512"] = {"us_per_layer": c_ms * 1e3, "gbs": read_bytes / (c_ms / 1e3) / 1e9,
-                                             "timing": "stream launches", "chunk": 512}
-        # asymmetric g=32 variant of the same layer (same device timing protocol, plain launches)
-        del caches
-        torch.cuda.empty_cache()
-        acaches = make_caches("asym4_g32", n_rep)
-        a_bytes = acaches[0].read_bytes(S)
-        aws = torch.empty(kvq.attend_workspace_bytes(acaches[0], w.n_q_heads, 1, S, chunk), dtype=torch.uint8,
-                          device=dev)
-        a_ms = time_plain(acaches, aws, chunk, min(K, 1000))
-        line["variants"]["asym4_g32"] = {"us_per_layer": a_ms * 1e3, "read_bytes_per_step": a_bytes,
-                                         "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches",
-                                         "chunk": chunk}
+        if args.workload == DEFAULT_WORKLOAD:
+            line["variants"] = variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1,
+                                        min(K, 1000), chunk, make_caches, dev)
         if world == 1:
-            line["cpu_baseline"] = cpu_baseline(w, inp, args.cpu_seconds)
+            line["cpu_baseline"] = cpu_baseline(w, inp, spec, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1, n, chunk, make_caches, dev):
+    """The 128K layer with the pages' fixed 512-token chunk, and with the asymmetric g=32 layout
+    (plain stream launches, same replicas)."""
+    import torch
+    w, S, fill = spec.w, spec.S, spec.fill
+
+    def time_plain(cs, wsb, ch):
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                kvq.store(cs[i % n_rep], k_new, v_new, fill, stream=stream)
+                kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
+                                  stream=stream)
+            torch.cuda.synchronize(dev)
+            ev0.record(stream)
+            for i in range(n):
+                kvq.store(cs[i % n_rep], k_new, v_new, fill, stream=stream)
+                kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
+                                  stream=stream)
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        return ev0.elapsed_time(ev1) / n
+
+    res = {}
+    ws512 = torch.empty(kvq.attend_workspace_bytes(caches[0], w.n_q_heads, 1, S, 512), dtype=torch.uint8, device=dev)
+    c_ms = time_plain(caches, ws512, 512)
+    res["q4_0_chunk512"] = {"us_per_layer": c_ms * 1e3, "gbs": spec.read_bytes / (c_ms / 1e3) / 1e9,
+                            "timing": "stream launches", "chunk": 512}
+    caches.clear()
+    torch.cuda.empty_cache()
+    acaches = make_caches("asym4_g32", n_rep)
+    a_bytes = acaches[0].read_bytes(S)
+    aws = torch.empty(kvq.attend_workspace_bytes(acaches[0], w.n_q_heads, 1, S, chunk), dtype=torch.uint8, device=dev)
+    a_ms = time_plain(acaches, aws, chunk)
+    res["asym4_g32"] = {"us_per_layer": a_ms * 1e3, "read_bytes_per_step": a_bytes,
+                        "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches", "chunk": chunk}
+    return res
 
 
 if __name__ == "__main__":
