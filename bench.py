@@ -432,7 +432,10 @@ def main():
                  "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
                  "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3,
                  "phase1_pass_us_per_step": ev_pass_ms / K * 1e3})
-    launches = 3 + (1 if w.layout == "had_int4" else 0)   # store, [query prep], phase 1, reduce
+    # store, phase 1, reduce; the CUDA-core phase 1 (D=256, Q6_0, more than 8 query rows per kv
+    # head) adds the Hadamard query preparation
+    tensor_core = w.layout in ("q4_0", "asym4_g32", "had_int4") and D == 128 and w.gqa * spec.n_q <= 8
+    launches = 3 + (1 if w.layout == "had_int4" and not tensor_core else 0)
     l2_note = (f"cache L2-resident ({n_rep} replicas x {cache_bytes / 2**20:.1f} MiB)" if l2_resident else
                f"inputs larger than L2: {n_rep} cache replicas rotated ({n_rep * cache_bytes / 2**20:.0f} MiB > "
                f"{L2_BYTES / 2**20:.0f} MiB L2)")

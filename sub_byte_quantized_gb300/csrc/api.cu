@@ -128,6 +128,7 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
   a.chunk = chunk;
   a.n_chunks = (a.n_body + chunk - 1) / chunk;
   a.C = a.n_chunks + (a.n_win > 0 ? 1 : 0);
+  a.win_in_reduce = 0;
   const size_t rows = (size_t)c.B * n_q_heads * n_q;
   size_t off = 0;
   const size_t o_m = off; off = round_up(off + rows * a.C * sizeof(float), 256);
@@ -229,14 +230,17 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
   a.out = out;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (a.cache.layout == KVQ_HAD_INT4) e = kvq::launch_had_prep(a, s);
+  const bool mma = kvq::mma_supported(a);
+  a.win_in_reduce = mma && a.n_win > 0;          // the tensor-core kernel covers the body chunks only
+  // the tensor-core kernel prepares the Hadamard query itself; the CUDA-core one reads it
+  if (a.cache.layout == KVQ_HAD_INT4 && !mma) e = kvq::launch_had_prep(a, s);
   const bool prof = g_ev_begin && g_ev_end;
   // Under stream capture an event record must be external to become a graph node.
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (e == cudaSuccess && prof) e = cudaStreamIsCapturing(s, &cap);
   const unsigned rec_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
   if (e == cudaSuccess && prof) e = cudaEventRecordWithFlags(g_ev_begin, s, rec_flags);
-  if (e == cudaSuccess) e = kvq::mma_supported(a) ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
+  if (e == cudaSuccess) e = mma ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
   if (e == cudaSuccess && prof) e = cudaEventRecordWithFlags(g_ev_end, s, rec_flags);
   if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
@@ -343,8 +347,10 @@ extern "C" kvq_status kvq_decode_attend_static(const kvq_cache *cache, const voi
   a.scale = attn_scale;
   a.out = out;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (a.cache.layout == KVQ_HAD_INT4) e = kvq::launch_had_prep(a, s);
-  if (e == cudaSuccess) e = kvq::mma_supported(a) ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
+  const bool mma = kvq::mma_supported(a);
+  a.win_in_reduce = mma && a.n_win > 0;
+  if (a.cache.layout == KVQ_HAD_INT4 && !mma) e = kvq::launch_had_prep(a, s);
+  if (e == cudaSuccess) e = mma ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
   if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;

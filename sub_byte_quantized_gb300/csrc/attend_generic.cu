@@ -248,24 +248,13 @@ __global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows) {
   if (r >= rows) return;
   constexpr int D = V * 32;
   float x[V];
+  int q8[V];
   if (V == 4) load4_f32(a.q, a.q_dtype, (size_t)r * D + lane * 4, x);
   else load8_f32(a.q, a.q_dtype, (size_t)r * D + lane * 8, x);
-  warp_fwht<V>(x, lane);
-  const float cD = inv_sqrt_dim(D);
-  float amax = 0.0f;
+  const float s = had_query_row<V>(x, q8, lane);
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    x[i] = __fmul_rn(x[i], cD);
-    amax = fmaxf(amax, fabsf(x[i]));
-  }
-#pragma unroll
-  for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  const float s = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    int q = 0;
-    if (s > 0.0f) q = (int)fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.0f), 127.0f);
-    a.q8[(size_t)r * D + lane * V + i] = (int8_t)q;
+    a.q8[(size_t)r * D + lane * V + i] = (int8_t)q8[i];
     a.q_rot[(size_t)r * D + lane * V + i] = x[i];
   }
   if (lane == 0) a.s_q[r] = s;
@@ -287,25 +276,12 @@ __global__ void __launch_bounds__(128) debug_scores_kernel(CacheView c, const vo
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     float x[V];
+    int qq[V];
     if (V == 4) load4_f32(q, q_dtype, (size_t)row * D + lane * 4, x);
     else load8_f32(q, q_dtype, (size_t)row * D + lane * 8, x);
-    warp_fwht<V>(x, lane);
-    const float cD = inv_sqrt_dim(D);
-    float amax = 0.0f;
+    const float s = had_query_row<V>(x, qq, lane);
 #pragma unroll
-    for (int i = 0; i < V; ++i) {
-      x[i] = __fmul_rn(x[i], cD);
-      amax = fmaxf(amax, fabsf(x[i]));
-    }
-#pragma unroll
-    for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-    const float s = __fdiv_rn(amax, 127.0f);
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-      int qq = 0;
-      if (s > 0.0f) qq = (int)fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.0f), 127.0f);
-      q8s[lane * V + i] = qq;
-    }
+    for (int i = 0; i < V; ++i) q8s[lane * V + i] = qq[i];
     if (lane == 0 && blockIdx.x == 0) s_q_out[row] = s;
   }
   __syncthreads();

@@ -1,6 +1,7 @@
-// Tensor-core phase 1 of the split-K decode attention for 4-bit block layouts (Q4_0 and the
-// asymmetric g=32 layout), head_dim 128, up to 8 query rows per kv head (the GQA group times
-// the query rows of the call).
+// Tensor-core phase 1 of the split-K decode attention for the 4-bit layouts (Q4_0, the asymmetric
+// g=32 layout and the per-token Hadamard int4 body), head_dim 128, up to 8 query rows per kv head
+// (the GQA group times the query rows of the call). For the Hadamard layout the exact-f32 recent
+// window is scored in phase 2.
 //
 // Why tensor cores: every kv head is shared by gqa query heads, so per packed K/V element the
 // step does 4*gqa flops (QK and PV); at gqa 8 that is ~57 flops per packed byte, beyond what
@@ -40,15 +41,28 @@ constexpr int kTiles = kStage / 16;
 constexpr int kMinBlocks = KVQ_MMA_MIN_BLOCKS; // resident CTAs per SM
 constexpr int kD = 128;
 constexpr int kRowBytes = 64;
-constexpr int kOffV = kStage * 64, kOffSK = 2 * kStage * 64, kOffSV = kOffSK + kStage * 8;
-constexpr int kOffZK = kOffSV + kStage * 8, kOffZV = kOffZK + kStage * 8;
+constexpr int kOffV = kStage * 64, kOffSK = 2 * kStage * 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <bool ASYM>
-__host__ __device__ constexpr int stage_bytes() { return 2 * kStage * 64 + (ASYM ? 4 : 2) * kStage * 8; }
-template <bool ASYM>
-__host__ __device__ constexpr int smem_bytes() { return kWarps * 2 * stage_bytes<ASYM>(); }
+// Stage buffer: K payload, V payload (swizzled 64-byte rows), K and V scales (4 f16 per token,
+// or one f32 per token for the Hadamard layout), asymmetric zero-points (4 f16 per token).
+template <int L>
+__host__ __device__ constexpr int scale_bytes() { return L == KVQ_HAD_INT4 ? 4 : 8; }
+template <int L>
+__host__ __device__ constexpr int off_sv() { return kOffSK + kStage * scale_bytes<L>(); }
+template <int L>
+__host__ __device__ constexpr int off_zk() { return off_sv<L>() + kStage * scale_bytes<L>(); }
+template <int L>
+__host__ __device__ constexpr int off_zv() { return off_zk<L>() + kStage * 8; }
+template <int L>
+__host__ __device__ constexpr int stage_bytes() { return L == KVQ_ASYM4_G32 ? off_zv<L>() + kStage * 8 : off_zk<L>(); }
+// Hadamard: per-warp scratch for the int8 query codes of up to 8 rows and their scales
+constexpr int kQScratch = 8 * 128 + 8 * 4;
+template <int L>
+__host__ __device__ constexpr int smem_bytes() {
+  return kWarps * 2 * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,6 +72,15 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int sr
 }
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, int src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// one token's scale (or zero-point) entry: N = 8 (four fp16) or 4 (one f32) bytes
+template <int N>
+__device__ __forceinline__ void cp_async_scale(uint32_t dst, const void *src, int src_bytes) {
+  if (N == 8) cp_async8(dst, src, src_bytes);
+  else cp_async4(dst, src, src_bytes);
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
@@ -162,8 +185,11 @@ __device__ __forceinline__ uint32_t swz(int row, int j) {
   return (uint32_t)(row * kRowBytes + ((j ^ ((row >> 1) & 3)) << 4));
 }
 
-template <bool ASYM, bool QSPLIT>
+template <int LAYOUT, bool QSPLIT>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
+  constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = LAYOUT == KVQ_HAD_INT4;
+  constexpr int SCB = scale_bytes<LAYOUT>(), OFF_SV = off_sv<LAYOUT>(), OFF_ZK = off_zk<LAYOUT>();
+  constexpr int OFF_ZV = off_zv<LAYOUT>(), STAGE_BYTES = stage_bytes<LAYOUT>();
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
@@ -194,11 +220,119 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const int n_mine = min(n_stages, s_first + spw) - s_first;
   const int tw0 = t0 + s_first * kStage;                 // this warp's first token
 
+  // ---- per-warp stage pipeline
+  uint8_t *wbuf = smem + warp * 2 * STAGE_BYTES;
+  const size_t head_row0 = (size_t)bh * cv.cap;
+  const uint8_t *kp = cv.payload[0] + head_row0 * kRowBytes;
+  const uint8_t *vp = cv.payload[1] + head_row0 * kRowBytes;
+  const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
+  const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
+  const __half *kz = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
+  const __half *vz = ASYM ? cv.zero[1] + head_row0 * 4 : nullptr;
+
+  auto issue = [&](int i) {
+    if (i < n_mine) {
+      const int ts = tw0 + i * kStage;
+      uint8_t *sb = wbuf + (i & 1) * STAGE_BYTES;
+      const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
+      if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
+        const uint8_t *kps = kp + (size_t)ts * kRowBytes, *vps = vp + (size_t)ts * kRowBytes;
+#pragma unroll
+        for (int k = 0; k < kStage / 8; ++k) {
+          const int q = lane + 32 * k;                   // 16-byte piece: row q/4, column q%4
+          const int row = q >> 2, j = q & 3;
+          cp_async16(sK + swz(row, j), kps + 16 * q, 16);
+          cp_async16(sV + swz(row, j), vps + 16 * q, 16);
+        }
+#pragma unroll
+        for (int k = 0; k < kStage / 32; ++k) {
+          const int row = lane + 32 * k;
+          const size_t tok = (size_t)(ts + row);
+          cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, SCB);
+          cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, SCB);
+          if (ASYM) {
+            cp_async8(smem_addr(sb + OFF_ZK + row * 8), kz + tok * 4, 8);
+            cp_async8(smem_addr(sb + OFF_ZV + row * 8), vz + tok * 4, 8);
+          }
+        }
+      } else {                                           // tail stage: rows past t_end are zero-filled
+#pragma unroll
+        for (int k = 0; k < kStage / 8; ++k) {
+          const int q = lane + 32 * k;
+          const int row = q >> 2, j = q & 3;
+          const bool ok = ts + row < t_end;
+          const size_t off = (size_t)(ok ? ts + row : t0) * kRowBytes + 16 * j;
+          cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
+          cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
+        }
+#pragma unroll
+        for (int k = 0; k < kStage / 32; ++k) {
+          const int row = lane + 32 * k;
+          const bool ok = ts + row < t_end;
+          const size_t tok = (size_t)(ok ? ts + row : t0);
+          cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, ok ? SCB : 0);
+          cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, ok ? SCB : 0);
+          if (ASYM) {
+            cp_async8(smem_addr(sb + OFF_ZK + row * 8), kz + tok * 4, ok ? 8 : 0);
+            cp_async8(smem_addr(sb + OFF_ZV + row * 8), vz + tok * 4, ok ? 8 : 0);
+          }
+        }
+      }
+    }
+    cp_async_commit();                                   // always one group per call
+  };
+  // start streaming the first two stages before the query prologue so their latency overlaps it
+  issue(0);
+  issue(1);
+
   // ---- query fragments (B operand of QK): row g of the group, dims 32b + 8c + 0..7
   uint32_t bq_hi[8][2], bq_lo[QSPLIT ? 8 : 1][2];
   float qsum[4];                                        // per-block sum of the prescaled q (row g)
   float row_alpha;                                      // alpha * 2^e * 2^24 * log2(e) for row g
-  {
+  if (HAD) {
+    // Query preparation in the prologue: each warp rotates and quantises the R <= 8 query rows of
+    // the group (warp FWHT, int8 codes, one f32 scale per row), parks the codes in its shared
+    // scratch and reads them back in fragment order. The int8 codes are exact in f16; the row's
+    // s_q goes into its alpha and -8 * sum(q8) into the accumulator start value.
+    uint8_t *qs8 = smem + kWarps * 2 * STAGE_BYTES + warp * kQScratch;
+    float *qsq = reinterpret_cast<float *>(qs8 + 8 * 128);
+    for (int r = 0; r < R; ++r) {
+      const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
+      const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
+      float x[4];
+      int q8v[4];
+      load4_f32(a.q, a.q_dtype, grow * kD + lane * 4, x);
+      const float sq = had_query_row<4>(x, q8v, lane);
+      *reinterpret_cast<uint32_t *>(qs8 + r * 128 + lane * 4) =
+          (uint32_t)(q8v[0] & 0xFF) | ((uint32_t)(q8v[1] & 0xFF) << 8) | ((uint32_t)(q8v[2] & 0xFF) << 16) |
+          ((uint32_t)(q8v[3] & 0xFF) << 24);
+      if (lane == 0) qsq[r] = sq;
+    }
+    __syncwarp();
+    const bool live = g < R;
+    row_alpha = (live ? a.scale * qsq[g] : 0.0f) * 16777216.0f * kLog2e;
+    float qs = 0.0f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      float h[8];
+      const uint2 w8 = live ? *reinterpret_cast<const uint2 *>(qs8 + g * 128 + 32 * b + 8 * c) : make_uint2(0u, 0u);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t word = i < 4 ? w8.x : w8.y;
+        h[i] = (float)(int8_t)((word >> (8 * (i & 3))) & 0xFFu);
+        qs += h[i];
+      }
+#pragma unroll
+      for (int st = 0; st < 2; ++st) {
+        bq_hi[2 * b + st][0] = pack_f16x2(h[2 * st], h[2 * st + 4]);
+        bq_hi[2 * b + st][1] = pack_f16x2(h[2 * st + 1] * 0.0625f, h[2 * st + 5] * 0.0625f);
+      }
+      qsum[b] = 0.0f;
+    }
+    qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+    qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+    qsum[0] = qs;                                        // whole-row sum (one accumulator per token)
+  } else {
     float x[4][8];
     const bool live = g < R;
     const int hq = kvh * a.gqa + (live ? g / a.n_q : 0);
@@ -274,67 +408,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
   const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
 
-  // ---- per-warp stage pipeline
-  uint8_t *wbuf = smem + warp * 2 * stage_bytes<ASYM>();
-  const size_t head_row0 = (size_t)bh * cv.cap;
-  const uint8_t *kp = cv.payload[0] + head_row0 * kRowBytes;
-  const uint8_t *vp = cv.payload[1] + head_row0 * kRowBytes;
-  const __half *ksc = static_cast<const __half *>(cv.scale[0]) + head_row0 * 4;
-  const __half *vsc = static_cast<const __half *>(cv.scale[1]) + head_row0 * 4;
-  const __half *kz = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
-  const __half *vz = ASYM ? cv.zero[1] + head_row0 * 4 : nullptr;
 
-  auto issue = [&](int i) {
-    if (i < n_mine) {
-      const int ts = tw0 + i * kStage;
-      uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
-      const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
-      if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
-        const uint8_t *kps = kp + (size_t)ts * kRowBytes, *vps = vp + (size_t)ts * kRowBytes;
-#pragma unroll
-        for (int k = 0; k < kStage / 8; ++k) {
-          const int q = lane + 32 * k;                   // 16-byte piece: row q/4, column q%4
-          const int row = q >> 2, j = q & 3;
-          cp_async16(sK + swz(row, j), kps + 16 * q, 16);
-          cp_async16(sV + swz(row, j), vps + 16 * q, 16);
-        }
-#pragma unroll
-        for (int k = 0; k < kStage / 32; ++k) {
-          const int row = lane + 32 * k;
-          const size_t off = (size_t)(ts + row) * 4;
-          cp_async8(smem_addr(sb + kOffSK + row * 8), ksc + off, 8);
-          cp_async8(smem_addr(sb + kOffSV + row * 8), vsc + off, 8);
-          if (ASYM) {
-            cp_async8(smem_addr(sb + kOffZK + row * 8), kz + off, 8);
-            cp_async8(smem_addr(sb + kOffZV + row * 8), vz + off, 8);
-          }
-        }
-      } else {                                           // tail stage: rows past t_end are zero-filled
-#pragma unroll
-        for (int k = 0; k < kStage / 8; ++k) {
-          const int q = lane + 32 * k;
-          const int row = q >> 2, j = q & 3;
-          const bool ok = ts + row < t_end;
-          const size_t off = (size_t)(ok ? ts + row : t0) * kRowBytes + 16 * j;
-          cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
-          cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
-        }
-#pragma unroll
-        for (int k = 0; k < kStage / 32; ++k) {
-          const int row = lane + 32 * k;
-          const bool ok = ts + row < t_end;
-          const size_t off = (size_t)(ok ? ts + row : t0) * 4;
-          cp_async8(smem_addr(sb + kOffSK + row * 8), ksc + off, ok ? 8 : 0);
-          cp_async8(smem_addr(sb + kOffSV + row * 8), vsc + off, ok ? 8 : 0);
-          if (ASYM) {
-            cp_async8(smem_addr(sb + kOffZK + row * 8), kz + off, ok ? 8 : 0);
-            cp_async8(smem_addr(sb + kOffZV + row * 8), vz + off, ok ? 8 : 0);
-          }
-        }
-      }
-    }
-    cp_async_commit();                                   // always one group per call
-  };
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   float O[4][2][4];                                      // [block][half][c0..c3]
@@ -352,12 +426,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       for (int k = 0; k < 4; ++k) O[b][h][k] = 0.0f;
   }
 
-  issue(0);
-  issue(1);
   for (int i = 0; i < n_mine; ++i) {
     cp_async_wait1();
     __syncwarp();
-    const uint8_t *sb = wbuf + (i & 1) * stage_bytes<ASYM>();
+    const uint8_t *sb = wbuf + (i & 1) * STAGE_BYTES;
     const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
     const int ts = tw0 + i * kStage;
 
@@ -372,6 +444,29 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
         ldsm_x4(sK + swz(row, 2 * half + (mi >> 1)), kw[half]);
       }
+      if (HAD) {
+        // one per-token scale: all 8 k-steps accumulate the exact integer dot (x 2^-24) in two
+        // chains; score = alpha * s_q * s_k * dot
+        float dA[4] = {zq0[0], zq1[0], zq0[0], zq1[0]}, dB[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t ug[4], u8[4];
+          unpack8_sub<false>(kw[b >> 1][(b & 1) * 2 + 0], ug);
+          unpack8_sub<false>(kw[b >> 1][(b & 1) * 2 + 1], u8);
+          const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
+          const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
+          float(&d)[4] = (b & 1) ? dB : dA;
+          mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
+          mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
+        }
+        const float skg = *reinterpret_cast<const float *>(sb + kOffSK + (tile * 16 + g) * 4);
+        const float skg8 = *reinterpret_cast<const float *>(sb + kOffSK + (tile * 16 + g + 8) * 4);
+        s[tile][0] = (dA[0] + dB[0]) * skg * alpha0;
+        s[tile][1] = (dA[1] + dB[1]) * skg * alpha1;
+        s[tile][2] = (dA[2] + dB[2]) * skg8 * alpha0;
+        s[tile][3] = (dA[3] + dB[3]) * skg8 * alpha1;
+        continue;
+      }
       const uint2 skg = *reinterpret_cast<const uint2 *>(sb + kOffSK + (tile * 16 + g) * 8);
       const uint2 skg8 = *reinterpret_cast<const uint2 *>(sb + kOffSK + (tile * 16 + g + 8) * 8);
       const float2 sg01 = __half22float2(u32_as_h2(skg.x)), sg23 = __half22float2(u32_as_h2(skg.y));
@@ -380,8 +475,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       const float skg8_f[4] = {s801.x, s801.y, s823.x, s823.y};
       float zg_f[4], zg8_f[4];
       if (ASYM) {
-        const uint2 zg = *reinterpret_cast<const uint2 *>(sb + kOffZK + (tile * 16 + g) * 8);
-        const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + kOffZK + (tile * 16 + g + 8) * 8);
+        const uint2 zg = *reinterpret_cast<const uint2 *>(sb + OFF_ZK + (tile * 16 + g) * 8);
+        const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + OFF_ZK + (tile * 16 + g + 8) * 8);
         const float2 a01 = __half22float2(u32_as_h2(zg.x)), a23 = __half22float2(u32_as_h2(zg.y));
         const float2 b01 = __half22float2(u32_as_h2(zg8.x)), b23 = __half22float2(u32_as_h2(zg8.y));
         zg_f[0] = a01.x; zg_f[1] = a01.y; zg_f[2] = a23.x; zg_f[3] = a23.y;
@@ -496,17 +591,41 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       // query row g and two consecutive tokens (2c, 2c+1) or (2c+8, 2c+9)
       uint32_t bh0, bh1, bl0, bl1;
       {
-        const uint32_t h01 = pack_f16x2(s[tile][0], s[tile][1]), h23 = pack_f16x2(s[tile][2], s[tile][3]);
+        float p0 = s[tile][0], p1 = s[tile][1], p2 = s[tile][2], p3 = s[tile][3];
+        if (HAD) {                                       // per-token V scale: P' = p * s_v before the split
+          const float svg = *reinterpret_cast<const float *>(sb + OFF_SV + (tile * 16 + g) * 4);
+          const float svg8 = *reinterpret_cast<const float *>(sb + OFF_SV + (tile * 16 + g + 8) * 4);
+          p0 *= svg;
+          p1 *= svg;
+          p2 *= svg8;
+          p3 *= svg8;
+        }
+        const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
         const float2 f01 = __half22float2(u32_as_h2(h01)), f23 = __half22float2(u32_as_h2(h23));
-        const uint32_t l01 = pack_f16x2(s[tile][0] - f01.x, s[tile][1] - f01.y);
-        const uint32_t l23 = pack_f16x2(s[tile][2] - f23.x, s[tile][3] - f23.y);
+        const uint32_t l01 = pack_f16x2(p0 - f01.x, p1 - f01.y);
+        const uint32_t l23 = pack_f16x2(p2 - f23.x, p3 - f23.y);
         bh0 = movm_t(h01);
         bh1 = movm_t(h23);
         bl0 = movm_t(l01);
         bl1 = movm_t(l23);
       }
+      if (HAD) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t ua[4], ub[4];
+          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
+          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
+          const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};
+          const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};
+          mma16816(O[b][0], A0, bh0, bh1);
+          mma16816(O[b][0], A0, bl0, bl1);
+          mma16816(O[b][1], A1, bh0, bh1);
+          mma16816(O[b][1], A1, bl0, bl1);
+        }
+        continue;
+      }
       // V block scales paired the same way: (s_v[2c][b], s_v[2c+1][b]), (s_v[2c+8][b], s_v[2c+9][b])
-      const uint8_t *svb = sb + kOffSV + tile * 16 * 8;
+      const uint8_t *svb = sb + OFF_SV + tile * 16 * 8;
       const uint2 sa = *reinterpret_cast<const uint2 *>(svb + (2 * c) * 8);
       const uint2 sbv = *reinterpret_cast<const uint2 *>(svb + (2 * c + 1) * 8);
       const uint2 sc = *reinterpret_cast<const uint2 *>(svb + (2 * c + 8) * 8);
@@ -518,7 +637,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       if (ASYM) {
         // W operand (zero-points): rows g < 4 hold block g's z_v for tokens (2c, 2c+1) and
         // (2c+8, 2c+9)
-        const uint8_t *zvb = sb + kOffZV + tile * 16 * 8;
+        const uint8_t *zvb = sb + OFF_ZV + tile * 16 * 8;
         const uint2 wa = *reinterpret_cast<const uint2 *>(zvb + (2 * c) * 8);
         const uint2 wb = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 1) * 8);
         const uint2 wc = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 8) * 8);
@@ -623,7 +742,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   }
 }
 
-template <bool ASYM, bool QSPLIT>
+template <int LAYOUT, bool QSPLIT>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   static bool configured[kMaxDevices] = {};
   int dev = 0;
@@ -631,36 +750,40 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma_kernel<ASYM, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<ASYM>());
+    e = cudaFuncSetAttribute(attend_mma_kernel<LAYOUT, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<LAYOUT>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = smem_bytes<ASYM>();
+  cfg.dynamicSmemBytes = smem_bytes<LAYOUT>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<ASYM, QSPLIT>, a);
+  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, QSPLIT>, a);
 }
 
 }  // namespace
 
 bool mma_supported(const AttendArgs &a) {
-  return (a.cache.layout == KVQ_Q4_0 || a.cache.layout == KVQ_ASYM4_G32) && a.cache.D == kD &&
-         a.gqa * a.n_q <= 8 && a.n_body > 0 && a.chunk % kStage == 0;
+  const int L = a.cache.layout;
+  return (L == KVQ_Q4_0 || L == KVQ_ASYM4_G32 || L == KVQ_HAD_INT4) && a.cache.D == kD && a.gqa * a.n_q <= 8 &&
+         a.n_body > 0 && a.chunk % kStage == 0;
 }
 
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
-  const bool asym = a.cache.layout == KVQ_ASYM4_G32;
   const bool split = a.q_dtype == KVQ_F32;
-  if (asym) return split ? launch_t<true, true>(a, st) : launch_t<true, false>(a, st);
-  return split ? launch_t<false, true>(a, st) : launch_t<false, false>(a, st);
+  switch (a.cache.layout) {
+    case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4, false>(a, st);   // int8 query codes are exact
+    case KVQ_ASYM4_G32:
+      return split ? launch_t<KVQ_ASYM4_G32, true>(a, st) : launch_t<KVQ_ASYM4_G32, false>(a, st);
+    default: return split ? launch_t<KVQ_Q4_0, true>(a, st) : launch_t<KVQ_Q4_0, false>(a, st);
+  }
 }
 
 }  // namespace kvq

@@ -41,6 +41,7 @@ struct AttendArgs {
   float scale;              // attention scale alpha
   int chunk, n_chunks;      // body chunks = ceil(n_body / chunk); + 1 window chunk if n_win
   int C;                    // total partials per row
+  int win_in_reduce;        // HAD: phase 2 computes the window chunk's partial itself
   float *out;
   // workspace regions
   float *part_m, *part_l, *part_o;   // [rows][C], [rows][C], [rows][C][D]
@@ -137,6 +138,31 @@ __device__ __forceinline__ void warp_fwht(float (&x)[V], int lane) {
       x[i] = (lane & m) ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
     }
   }
+}
+
+// Hadamard query preparation of one row, in one warp: x (V = D/32 consecutive values per lane,
+// already loaded) -> rotated row q_rot = FWHT(x) * fp32(1/sqrt(D)), its int8 codes
+// clamp(rint(q_rot / s_q), -127, 127) and s_q = amax(|q_rot|) / 127, all in correctly rounded
+// float32 steps. Every kernel that needs the int8 query codes uses this one routine.
+template <int V>
+__device__ __forceinline__ float had_query_row(float (&x)[V], int (&q8)[V], int lane) {
+  warp_fwht<V>(x, lane);
+  const float cD = inv_sqrt_dim(V * 32);
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    x[i] = __fmul_rn(x[i], cD);
+    amax = fmaxf(amax, fabsf(x[i]));
+  }
+#pragma unroll
+  for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+  const float s = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    q8[i] = 0;
+    if (s > 0.0f) q8[i] = (int)fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.0f), 127.0f);
+  }
+  return s;
 }
 
 }  // namespace kvq

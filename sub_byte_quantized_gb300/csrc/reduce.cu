@@ -40,12 +40,40 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   float M = -INFINITY, L = 0.0f, O[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
+  if (HAD && a.win_in_reduce && win_vis) {
+    // The exact-f32 recent window (tokens n_body .. kv_len-1, ring slot t mod n_recent), scored
+    // with the float32 rotated query: each warp takes every eighth window token and keeps an
+    // online softmax over them; its state then joins the chunk partials below.
+    const CacheView &cv = a.cache;
+    const size_t bh = (row / a.n_q) / a.Hq * cv.H + ((row / a.n_q) % a.Hq) / a.gqa;
+    // rotated query row (the tensor-core phase 1 prepares its int8 codes itself, so rotate here)
+    float qv[VPL];
+    int q8v[VPL];
+    if (VPL == 4) load4_f32(a.q, a.q_dtype, row * D + lane * 4, qv);
+    else load8_f32(a.q, a.q_dtype, row * D + lane * 8, qv);
+    had_query_row<VPL>(qv, q8v, lane);
+    for (int t = a.n_body + warp; t <= lim && t < a.kv_len; t += kWarps) {
+      const size_t slot = (bh * cv.n_recent + (size_t)(t % cv.n_recent)) * D + lane * VPL;
+      float dot = 0.0f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) dot = fmaf(qv[i], cv.ring[0][slot + i], dot);
+#pragma unroll
+      for (int k = 16; k; k >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, k);
+      const float sc = a.scale * dot;
+      const float mn = fmaxf(M, sc);
+      const float corr = __expf(M - mn), p = __expf(sc - mn);
+      L = fmaf(L, corr, p);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) O[i] = fmaf(O[i], corr, p * cv.ring[1][slot + i]);
+      M = mn;
+    }
+  }
   for (int base = warp; base < a.C; base += kWarps * kBatch) {
     float mc[kBatch], lc[kBatch], oc[kBatch][VPL];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int c = base + u * kWarps;
-      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : win_vis);
+      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : win_vis && !a.win_in_reduce);
       mc[u] = vis ? pm[c] : -INFINITY;
       lc[u] = vis ? pl[c] : 0.0f;
 #pragma unroll
