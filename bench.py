@@ -335,7 +335,7 @@ def main():
     n_rep = min(64, max(2, math.ceil(3 * L2_BYTES / max(cache_bytes, 1)) + 1))
     l2_resident = n_rep * cache_bytes < 2 * L2_BYTES
     caches = make_caches(w.layout, n_rep)
-    chunk = kvq.attend_chunk(caches[0], S, 0)
+    chunk = kvq.attend_chunk(caches[0], w.n_q_heads, spec.n_q, S, 0)
     ws = torch.empty(max(256, kvq.attend_workspace_bytes(caches[0], w.n_q_heads, spec.n_q, S, chunk)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((B, w.n_q_heads, spec.n_q, D), dtype=torch.float32, device=dev)

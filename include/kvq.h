@@ -131,8 +131,10 @@ size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int
                                   int32_t kv_len, int32_t chunk);
 
 /* The chunk length kvq_decode_attend uses for these arguments on the current device (`chunk`
- * itself when non-zero and valid, the automatic choice for 0); 0 on invalid arguments. */
-int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t kv_len, int32_t chunk);
+ * itself when non-zero and valid, the automatic choice for 0); 0 on invalid arguments. The
+ * automatic choice depends on the layout, head_dim and query rows per kv head
+ * (n_q_heads / n_kv_heads * n_q), which select the phase-1 kernel. */
+int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t chunk);
 
 /*
  * Fused split-K decode attention over the packed cache; the dequantised K/V matrix is never

@@ -60,7 +60,7 @@ def lib() -> C.CDLL:
         f.argtypes, f.restype = [cache_p, P, P, I32, I32, I32, P], I32
     L.kvq_attend_workspace_bytes.argtypes = [cache_p, I32, I32, I32, I32]
     L.kvq_attend_workspace_bytes.restype = SZ
-    L.kvq_attend_chunk.argtypes, L.kvq_attend_chunk.restype = [cache_p, I32, I32], I32
+    L.kvq_attend_chunk.argtypes, L.kvq_attend_chunk.restype = [cache_p, I32, I32, I32, I32], I32
     L.kvq_decode_attend.argtypes = [cache_p, P, I32, I32, I32, I32, I32, I32, C.c_float, I32, P, P, SZ, P]
     L.kvq_decode_attend.restype = I32
     L.kvq_decode_attend_static.argtypes = [cache_p, P, I32, I32, I32, I32, I32, I32, C.c_float, I32, P, P]

@@ -118,9 +118,9 @@ def attend_workspace_bytes(cache: KVCache, n_q_heads: int, n_q: int, kv_len: int
     return int(L.lib().kvq_attend_workspace_bytes(C.byref(cache.struct), n_q_heads, n_q, kv_len, chunk))
 
 
-def attend_chunk(cache: KVCache, kv_len: int, chunk: int = 0) -> int:
+def attend_chunk(cache: KVCache, n_q_heads: int, n_q: int, kv_len: int, chunk: int = 0) -> int:
     """The split-K chunk length a decode_attend call with these arguments uses (0 -> automatic)."""
-    return int(L.lib().kvq_attend_chunk(C.byref(cache.struct), kv_len, chunk))
+    return int(L.lib().kvq_attend_chunk(C.byref(cache.struct), n_q_heads, n_q, kv_len, chunk))
 
 
 def decode_attend(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = False, q_pos0: int = 0,

@@ -90,15 +90,22 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
   return KVQ_OK;
 }
 
-// Automatic split-K chunk: four times the smallest multiple of 64 tokens that lets one slice per
-// resident warp of the tensor-core kernel (four warps per chunk) cover the body of every (batch, kv head) in a
-// single wave.
-int auto_chunk(int n_body, int n_heads) {
+// Automatic split-K chunk, sized so that the body of every (batch, kv head) is covered by one wave
+// of the tensor-core kernel that will run: for the 4-bit layouts four times the smallest multiple
+// of 64 tokens that gives one slice to every resident warp (four warps per chunk); for the Q6_0
+// kernel the smallest multiple of 64 that gives one chunk to every resident CTA.
+int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
-  const long long per = ((long long)(n_body > 0 ? n_body : 1) * n_heads + warps - 1) / warps;
-  long long chunk = 4 * ((per + 63) / 64 * 64);
+  const long long work = (long long)(n_body > 0 ? n_body : 1) * n_heads;
+  long long chunk;
+  if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
+    const long long ctas = (long long)sms * kvq::kMmaQ6CtasPerSm(c.D);
+    chunk = ((work + ctas - 1) / ctas + 63) / 64 * 64;
+  } else {
+    const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
+    chunk = 4 * (((work + warps - 1) / warps + 63) / 64 * 64);
+  }
   if (chunk > 8192) chunk = 8192;
   return (int)chunk;
 }
@@ -116,8 +123,9 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
   if (kv_len > c.cap) return fail(KVQ_ECAPACITY, "kv_len %d > capacity %d", kv_len, c.cap);
   if (causal && (q_pos0 < 0 || (long long)q_pos0 + n_q > kv_len))
     return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
-  if (chunk == 0) chunk = auto_chunk(kv_len - (c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0),
-                                     c.B * c.H);
+  if (chunk == 0)
+    chunk = auto_chunk(c, (n_q_heads / c.H) * n_q,
+                       kv_len - (c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0), c.B * c.H);
   if (chunk < 64 || chunk > 8192 || chunk % 64) return fail(KVQ_ESHAPE, "chunk %d not a multiple of 64 in [64, 8192]", chunk);
   a.Hq = n_q_heads; a.gqa = n_q_heads / c.H; a.n_q = n_q;
   a.kv_len = kv_len;
@@ -201,10 +209,10 @@ size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int
   return need;
 }
 
-int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t kv_len, int32_t chunk) {
+int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t chunk) {
   kvq::AttendArgs a;
   size_t need = 0;
-  if (resolve_attend(cache, cache ? cache->n_kv_heads : 1, 1, kv_len, 0, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  if (resolve_attend(cache, n_q_heads, n_q, kv_len, 0, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
   return a.chunk;
 }
 

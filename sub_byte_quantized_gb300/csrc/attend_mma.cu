@@ -31,9 +31,11 @@
 #include <climits>
 
 #include "kvq_internal.cuh"
+#include "mma_util.cuh"
 
 namespace kvq {
 namespace {
+using namespace mma;
 
 constexpr int kWarps = 4;
 constexpr int kStage = 64;              // tokens per pipeline stage (four 16-token tiles)
@@ -63,83 +65,6 @@ template <int L>
 __host__ __device__ constexpr int smem_bytes() {
   return kWarps * 2 * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
 }
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, int src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-// one token's scale (or zero-point) entry: N = 8 (four fp16) or 4 (one f32) bytes
-template <int N>
-__device__ __forceinline__ void cp_async_scale(uint32_t dst, const void *src, int src_bytes) {
-  if (N == 8) cp_async8(dst, src, src_bytes);
-  else cp_async4(dst, src, src_bytes);
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
-  uint32_t y;
-  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-               "{%0,%1,%2,%3};\n"
-               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-template <int LUT>
-__device__ __forceinline__ uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, %4;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(LUT));
-  return d;
-}
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t *>(&h);
-}
-__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
-
-__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("add.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
-__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
-// f16x2 constants (bit patterns): 1/16, -1032, -72 in both halves.
-constexpr uint32_t kH16th = 0x2C002C00u, kHm1032 = 0xE408E408u, kHm72 = 0xD480D480u;
 
 // Q4_0 V operand: eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
 // (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the signed code values (n ^ 8) - 8. One lop3 places
@@ -772,6 +697,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
 
 bool mma_supported(const AttendArgs &a) {
   const int L = a.cache.layout;
+  if (L == KVQ_Q6_0) return mma_q6_supported(a);
   return (L == KVQ_Q4_0 || L == KVQ_ASYM4_G32 || L == KVQ_HAD_INT4) && a.cache.D == kD && a.gqa * a.n_q <= 8 &&
          a.n_body > 0 && a.chunk % kStage == 0;
 }
@@ -779,6 +705,7 @@ bool mma_supported(const AttendArgs &a) {
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
   const bool split = a.q_dtype == KVQ_F32;
   switch (a.cache.layout) {
+    case KVQ_Q6_0: return launch_attend_mma_q6(a, st);
     case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4, false>(a, st);   // int8 query codes are exact
     case KVQ_ASYM4_G32:
       return split ? launch_t<KVQ_ASYM4_G32, true>(a, st) : launch_t<KVQ_ASYM4_G32, false>(a, st);

@@ -19,6 +19,12 @@ constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-
 #define KVQ_MMA_MIN_BLOCKS 3
 #endif
 constexpr int kMmaWarpsPerSm = 4 * KVQ_MMA_MIN_BLOCKS;
+// Tensor-core phase 1 for Q6_0: resident CTAs (of four warps) per SM, by head_dim (shared-memory
+// ring of three 64-token stages: 84 KB at D = 256, 45 KB at D = 128).
+__host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 : 3; }
+// Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, at most four query rows per
+// kv head (gqa * n_q).
+__host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows <= 4; }
 
 // Device-side view of a cache; index 0 = K, 1 = V.
 struct CacheView {
@@ -62,6 +68,8 @@ cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, 
 // cover the call (the caller then uses the generic kernel).
 bool mma_supported(const AttendArgs &a);
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st);
+bool mma_q6_supported(const AttendArgs &a);
+cudaError_t launch_attend_mma_q6(const AttendArgs &a, cudaStream_t st);
 
 // ----------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }

@@ -77,6 +77,18 @@ def test_edge_lengths(layout, kv_len):
     run_case(w, kv_len, chunk=64)
 
 
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("gqa,n_q,causal,q_dtype", [
+    (1, 1, False, None), (2, 1, False, "f32"), (3, 1, False, "f16"), (4, 1, False, None),
+    (2, 2, True, "f32"), (1, 4, True, None),
+])
+def test_q6_tensor_core_rows(D, gqa, n_q, causal, q_dtype):
+    """Q6_0 phase 1 on the tensor cores: one to four query rows per kv head (GQA group times query
+    rows, causal rows included), head_dim 128 and 256, chunks of three stages plus a ragged tail."""
+    w = WORKLOADS["c4_q6_0_gemma"].scaled(head_dim=D, batch=2, n_kv_heads=2, n_q_heads=2 * gqa, causal=causal)
+    run_case(w, kv_len=1001, n_q=n_q, chunk=192, q_dtype=q_dtype, fill=937)
+
+
 def test_hadamard_window_covers_everything():
     w = WORKLOADS["c3_had_int4_decode"].scaled(batch=2, n_recent=512)
     run_case(w, 300)                      # n_recent >= kv_len: all tokens exact f32
