@@ -9,8 +9,8 @@
 //   PV:  O^T[16 dims][8 cols]   += V^T[16 dims][16 tokens] . P'^T[16 tokens][8 cols]
 // With at most four query rows the eight mma columns hold each row twice: columns 0-3 the f16
 // "hi" parts, columns 4-7 the "lo" parts (q = hi + lo for f32 queries, P' = hi + lo for the
-// scaled probabilities), so one mma carries both halves; the two column groups are added after
-// the loop.
+// scaled probabilities), so one mma carries both halves; the two column groups are added at the
+// end.
 //
 // Operands: a 6-bit code u = code + 32 in [0, 63] enters as the exact f16 subnormal u * 2^-24 (low-
 // nibble positions) or 16 u * 2^-24 (high-nibble positions, whose query entries are divided by
@@ -20,11 +20,16 @@
 // (-32 * sum(q) * 2^-24 per block); for V it comes from one extra small mma per tile,
 // W[block][row] = sum_t s_v[t][block] * p[t][row], subtracted as 32 W in the epilogue.
 //
-// Data movement: a CTA of four warps streams its chunk through a three-stage shared-memory ring
-// of 64-token stages (cp.async; the low planes go to 16-byte swizzled rows read by ldmatrix,
-// the high planes to padded rows read with 32/128-bit loads); warp w takes the w-th 16-token
-// tile of every stage and keeps its own online-softmax state. The warps' states are combined
-// in shared memory at the end and the CTA writes one (m, l, o) partial per query row.
+// Work split: a CTA of eight warps streams its chunk in 64-token stages. Warps 0-3 ("K warps")
+// each score one 16-token tile of stage i (all blocks) and run the online softmax; warps 4-7
+// ("V warps") accumulate P'V for the same tiles one stage later, reading the probabilities and
+// the rescale factors that the K warps left in shared memory. The per-stage CTA barrier orders
+// the hand-off, so the two roles overlap without further synchronisation. K and V stream through
+// separate three-slot rings (16-byte cp.async of whole token rows, contiguous in the cache, into
+// rows padded by 16 bytes so that the per-lane 32/64-bit fragment reads are free of bank
+// conflicts); the copy of stage i+2 of K and stage i+1 of V is issued while stage i is scored.
+// At the end the four tile states are combined in shared memory and the CTA writes one
+// (m, l, o) partial per query row.
 #include <cfloat>
 #include <climits>
 
@@ -35,35 +40,26 @@ namespace kvq {
 namespace {
 using namespace mma;
 
-constexpr int kWarps = 4;
-constexpr int kStage = 64;   // tokens per stage: one 16-token tile per warp
-constexpr int kRing = 3;     // stages in the shared ring
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStage = 64;   // tokens per stage: four 16-token tiles
+constexpr int kRing = 3;     // slots per ring (K and V each)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
 struct Geom {
   static constexpr int NB = D / 32;            // blocks per token row
-  static constexpr int RB = 24 * NB;           // packed payload bytes per token in the cache
-  static constexpr int LB = 16 * NB;           // low-plane bytes per token in shared memory
-  static constexpr int TS = 8 * NB + 16;       // high-plane row stride in shared memory (padded)
+  static constexpr int RB = 24 * NB;           // packed payload bytes per token
+  static constexpr int PITCH = RB + 16;        // shared-memory row pitch (conflict-free reads)
   static constexpr int SB = 2 * NB;            // scale bytes per token
-  static constexpr int OFF_VLO = kStage * LB;
-  static constexpr int OFF_KHI = 2 * kStage * LB;
-  static constexpr int OFF_VHI = OFF_KHI + kStage * TS;
-  static constexpr int OFF_KSC = OFF_VHI + kStage * TS;
-  static constexpr int OFF_VSC = OFF_KSC + kStage * SB;
-  static constexpr int STAGE = OFF_VSC + kStage * SB;
-  static constexpr int SMEM = kRing * STAGE;
+  static constexpr int PIECES = kStage * RB / 16;   // 16-byte copies per plane per stage
+  static constexpr int OFF_SC = kStage * PITCH;     // scales after the rows, in each slot
+  static constexpr int SLOT = OFF_SC + kStage * SB;
+  static constexpr int OFF_V = kRing * SLOT;        // K ring, then V ring
+  static constexpr int OFF_X = 2 * kRing * SLOT;    // hand-off: [tile][slot][lane] 32 bytes
+  static constexpr int SMEM = OFF_X + 4 * 2 * 32 * 32;
 };
-
-// Byte offset of (row, 16-byte column) in the swizzled low-plane slab; ldmatrix phases (8 rows,
-// one column) hit 8 distinct 16-byte bank groups.
-template <int NB>
-__device__ __forceinline__ uint32_t lo_off(int row, int col) {
-  const int x = NB == 8 ? (row & 7) : ((row >> 1) & 3);
-  return (uint32_t)(row * 16 * NB + ((col ^ x) << 4));
-}
 
 // Eight 6-bit values -> four f16 subnormal pairs. w: eight low nibbles n0..n7 (n0 = bits 0-3),
 // h: the matching 2-bit high fields t0..t3 in byte 0 and t4..t7 in byte 2 (t_i at bits 2i of its
@@ -84,8 +80,10 @@ __device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
   return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
 }
 
+__device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
+
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32, kMmaQ6CtasPerSm(D)) attend_mma_q6_kernel(AttendArgs a) {
+__global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_kernel(AttendArgs a) {
   using G = Geom<D>;
   constexpr int NB = G::NB;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -96,6 +94,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMmaQ6CtasPerSm(D)) attend_mma_q6
   const CacheView &cv = a.cache;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int tw = warp & 3;                             // tile of the stage
+  const bool kwarp = warp < 4;                         // role: K (scores) or V (P'V)
   const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
@@ -119,362 +119,374 @@ __global__ void __launch_bounds__(kWarps * 32, kMmaQ6CtasPerSm(D)) attend_mma_q6
   const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * G::SB;
   const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * G::SB;
 
-  // ---- CTA-wide stage copy: per (token row, block pair) five copies per plane; rows past t_end
-  // are zero-filled
-  auto issue = [&](int s) {
-    if (s < n_stages) {
-      const int ts = t0 + s * kStage;
-      uint8_t *sb = smem + (s % kRing) * G::STAGE;
-      constexpr int PAIRS = NB / 2;
+  // ---- copy of one plane's stage s into a ring slot: the stage's rows are contiguous in the
+  // cache; 16-byte piece q goes to row q / (RB/16) of the padded slot. Rows past t_end are
+  // zero-filled.
+  auto copy_stage = [&](const uint8_t *pl, const uint8_t *sc, uint8_t *slot, int s) {
+    const int ts = t0 + s * kStage;
+    const uint32_t sd = smem_addr(slot);
+    if (ts + kStage <= t_end) {                          // full stage: no per-row bounds
+      const uint8_t *src = pl + (size_t)ts * G::RB;
 #pragma unroll
-      for (int j = 0; j < kStage * PAIRS / (kWarps * 32); ++j) {
-        const int u = threadIdx.x + kWarps * 32 * j;
-        const int row = u / PAIRS, k = u % PAIRS;
-        const bool ok = ts + row < t_end;
-        const int n16 = ok ? 16 : 0, n8 = ok ? 8 : 0;
-        const size_t tok = (size_t)(ok ? ts + row : t0);
-#pragma unroll
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint8_t *src = (kv ? vp : kp) + tok * G::RB + 48 * k;
-          const uint32_t lo = smem_addr(sb + (kv ? G::OFF_VLO : 0));
-          const uint32_t hi = smem_addr(sb + (kv ? G::OFF_VHI : G::OFF_KHI) + row * G::TS + 16 * k);
-          const uint32_t lo_b = lo + lo_off<NB>(row, 2 * k + 1);
-          cp_async16(lo + lo_off<NB>(row, 2 * k), src, n16);     // low plane of block 2k
-          cp_async8(hi, src + 16, n8);                          // high plane of block 2k
-          cp_async8(lo_b, src + 24, n8);                        // low plane of block 2k+1
-          cp_async8(lo_b + 8, src + 32, n8);
-          cp_async8(hi + 8, src + 40, n8);                      // high plane of block 2k+1
+      for (int j = 0; j < (G::PIECES + kThreads - 1) / kThreads; ++j) {
+        const int q = threadIdx.x + kThreads * j;
+        if (q < G::PIECES) {
+          const int row = q / (G::RB / 16);
+          cp_async16(sd + row * G::PITCH + 16 * (q - row * (G::RB / 16)), src + 16 * q, 16);
         }
       }
-      {
-        const int row = threadIdx.x & (kStage - 1), kv = threadIdx.x / kStage;
-        const bool ok = ts + row < t_end;
-        const size_t tok = (size_t)(ok ? ts + row : t0);
-        const uint8_t *src = (kv ? vsc : ksc) + tok * G::SB;
-        const uint32_t dst = smem_addr(sb + (kv ? G::OFF_VSC : G::OFF_KSC) + row * G::SB);
-        if (G::SB == 16) cp_async16(dst, src, ok ? 16 : 0);
-        else cp_async8(dst, src, ok ? 8 : 0);
+    } else {
+#pragma unroll
+      for (int j = 0; j < (G::PIECES + kThreads - 1) / kThreads; ++j) {
+        const int q = threadIdx.x + kThreads * j;
+        if (q < G::PIECES) {
+          const int row = q / (G::RB / 16), pc = q - row * (G::RB / 16);
+          const bool ok = ts + row < t_end;
+          const size_t off = ok ? (size_t)ts * G::RB + 16 * q : (size_t)t0 * G::RB;
+          cp_async16(sd + row * G::PITCH + 16 * pc, pl + off, ok ? 16 : 0);
+        }
       }
     }
-    cp_async_commit();                                   // always one group per call
+    if (threadIdx.x < kStage) {
+      const int row = threadIdx.x;
+      const bool ok = ts + row < t_end;
+      const uint8_t *src = sc + (size_t)(ok ? ts + row : t0) * G::SB;
+      const uint32_t dst = sd + G::OFF_SC + row * G::SB;
+      if (G::SB == 16) cp_async16(dst, src, ok ? 16 : 0);
+      else cp_async8(dst, src, ok ? 8 : 0);
+    }
+  };
+  // one commit group per call: K of stage s and V of stage s - 1
+  auto issue = [&](int s) {
+    if (s < n_stages) copy_stage(kp, ksc, smem + (s % kRing) * G::SLOT, s);
+    if (s >= 1 && s - 1 < n_stages) copy_stage(vp, vsc, smem + G::OFF_V + ((s - 1) % kRing) * G::SLOT, s - 1);
+    cp_async_commit();
   };
   issue(0);
   issue(1);
 
-  // ---- query fragments: lane (g, c) holds column g = row (g & 3), its f16 hi part (g < 4) or
-  // lo part (g >= 4), dims 32b + 8c + 0..7 of every block b
-  uint32_t bq[2 * NB][2];
-  float qsum[NB];
-  float row_alpha;
-  {
-    const int rq = g & 3;
-    const bool live = rq < R;
-    const int hq = kvh * a.gqa + (live ? rq / a.n_q : 0);
-    const int qi = live ? rq % a.n_q : 0;
-    const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
-    float x[NB][8];
-    float mx = 0.0f;
+  // hand-off slot of (tile, stage parity): per lane {bm0, bm1, ba0, ba1} and {corr0, corr1}
+  uint8_t *xch = smem + G::OFF_X;
+  const int r0 = 2 * (c & 1), r1 = r0 + 1;             // the thread's rows (accumulator columns 2c, 2c+1)
+
+  if (kwarp) {
+    // =============================== K warps: scores and online softmax
+    // query fragments: lane (g, c) holds column g = row (g & 3), its f16 hi part (g < 4) or lo
+    // part (g >= 4), dims 32b + 8c + 0..7 of every block b
+    uint32_t bq[2 * NB][2];
+    float qsum[NB];
+    float row_alpha;
+    {
+      const int rq = g & 3;
+      const bool live = rq < R;
+      const int hq = kvh * a.gqa + (live ? rq / a.n_q : 0);
+      const int qi = live ? rq % a.n_q : 0;
+      const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
+      float x[NB][8];
+      float mx = 0.0f;
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      if (live) {
-        load8_f32(a.q, a.q_dtype, grow * D + 32 * b + 8 * c, x[b]);
+      for (int b = 0; b < NB; ++b) {
+        if (live) {
+          load8_f32(a.q, a.q_dtype, grow * D + 32 * b + 8 * c, x[b]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) x[b][i] = 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[b][i]));
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      // power-of-two prescale: the row's largest |q| lands in [2^13, 2^14), exact and clear of
+      // f16 overflow; the inverse goes into the row's alpha
+      int e = 0;
+      if (mx > 0.0f) e = min(max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - 13, -100), 100);
+      const float pre = ldexpf(1.0f, -e), post = ldexpf(1.0f, e);
+      row_alpha = live ? a.scale * post * 16777216.0f * kLog2e : 0.0f;
+      const bool hi_col = g < 4;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        float sm = 0.0f, u[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float v = x[b][i] * pre;
+          sm += v;
+          const float h = __half2float(__float2half_rn(v));
+          u[i] = hi_col ? h : v - h;
+        }
+        qsum[b] = sm;
+#pragma unroll
+        for (int st = 0; st < 2; ++st) {
+          bq[2 * b + st][0] = pack_f16x2(u[2 * st], u[2 * st + 4]);
+          bq[2 * b + st][1] = pack_f16x2(u[2 * st + 1] * 0.0625f, u[2 * st + 5] * 0.0625f);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 1);
+        qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 2);
+      }
+    }
+    const float alpha0 = __shfl_sync(0xffffffffu, row_alpha, r0 * 4);
+    const float alpha1 = __shfl_sync(0xffffffffu, row_alpha, r1 * 4);
+    // K offset: -32 * sum(q) of the block in accumulator units (x 2^-24), in the hi columns only
+    float zq0[NB], zq1[NB];
+    {
+      const float zf = c < 2 ? -32.0f * 5.9604644775390625e-8f : 0.0f;
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * zf;
+        zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * zf;
+      }
+    }
+    const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
+    const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
+    // bytes 2c, 2c+1 of a block's eight high bytes -> bytes 0 and 2
+    const uint32_t sel_k = (uint32_t)(2 * c) | ((uint32_t)(2 * c + 1) << 8);
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+    for (int i = 0; i <= n_stages; ++i) {
+      cp_async_wait<1>();
+      __syncthreads();                                   // K(i), V(i-1) landed; the slots refilled below are free
+      issue(i + 2);
+      const int tr = 16 * tw;
+      const int ts = t0 + i * kStage + tr;
+      if (i == n_stages || ts >= t_end) continue;
+      const uint8_t *sb = smem + (i % kRing) * G::SLOT;
+      const uint8_t *kg = sb + (tr + g) * G::PITCH, *kg8 = kg + 8 * G::PITCH;
+      const uint8_t *kss = sb + G::OFF_SC;
+      uint32_t skg[NB / 2], skg8[NB / 2];                // K scales of tokens g, g+8 (f16 pairs)
+      if constexpr (NB == 8) {
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(kss + (tr + g) * G::SB);
+        const uint4 x1 = *reinterpret_cast<const uint4 *>(kss + (tr + g + 8) * G::SB);
+        skg[0] = x0.x; skg[1] = x0.y; skg[2] = x0.z; skg[3] = x0.w;
+        skg8[0] = x1.x; skg8[1] = x1.y; skg8[2] = x1.z; skg8[3] = x1.w;
       } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[b][i] = 0.0f;
+        const uint2 x0 = *reinterpret_cast<const uint2 *>(kss + (tr + g) * G::SB);
+        const uint2 x1 = *reinterpret_cast<const uint2 *>(kss + (tr + g + 8) * G::SB);
+        skg[0] = x0.x; skg[1] = x0.y;
+        skg8[0] = x1.x; skg8[1] = x1.y;
       }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx = fmaxf(mx, fabsf(x[b][i]));
-    }
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    // power-of-two prescale: the row's largest |q| lands in [2^13, 2^14), exact and clear of
-    // f16 overflow; the inverse goes into the row's alpha
-    int e = 0;
-    if (mx > 0.0f) e = min(max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - 13, -100), 100);
-    const float pre = ldexpf(1.0f, -e), post = ldexpf(1.0f, e);
-    row_alpha = live ? a.scale * post * 16777216.0f * kLog2e : 0.0f;
-    const bool hi_col = g < 4;
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      float s = 0.0f, u[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float v = x[b][i] * pre;
-        s += v;
-        const float h = __half2float(__float2half_rn(v));
-        u[i] = hi_col ? h : v - h;
-      }
-      qsum[b] = s;
-#pragma unroll
-      for (int st = 0; st < 2; ++st) {
-        bq[2 * b + st][0] = pack_f16x2(u[2 * st], u[2 * st + 4]);
-        bq[2 * b + st][1] = pack_f16x2(u[2 * st + 1] * 0.0625f, u[2 * st + 5] * 0.0625f);
-      }
-    }
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 1);
-      qsum[b] += __shfl_xor_sync(0xffffffffu, qsum[b], 2);
-    }
-  }
-  // the thread's accumulator columns 2c, 2c+1: rows r0 = 2(c & 1), r1 = r0 + 1; hi parts for
-  // c < 2, lo parts for c >= 2
-  const int r0 = 2 * (c & 1), r1 = r0 + 1;
-  const float alpha0 = __shfl_sync(0xffffffffu, row_alpha, r0 * 4);
-  const float alpha1 = __shfl_sync(0xffffffffu, row_alpha, r1 * 4);
-  // K offset: -32 * sum(q) of the block in accumulator units (x 2^-24), in the hi columns only
-  float zq0[NB], zq1[NB];
-  {
-    const float zf = c < 2 ? -32.0f * 5.9604644775390625e-8f : 0.0f;
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * zf;
-      zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * zf;
-    }
-  }
-  const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
-  const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
-  // prmt selectors: K -> bytes 2c, 2c+1 of a block's eight high bytes into bytes 0 and 2;
-  // V -> byte (g & 3) of two tokens' high words into bytes 0 and 2
-  const uint32_t sel_k = (uint32_t)(2 * c) | ((uint32_t)(2 * c + 1) << 8);
-  const uint32_t sel_v = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
-
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-  float O[NB][2][4];
-  float Dw[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int b = 0; b < NB; ++b)
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) O[b][h][k] = 0.0f;
-
-  for (int i = 0; i < n_stages; ++i) {
-    cp_async_wait<kRing - 2>();
-    __syncthreads();                                     // stage i landed; stage i-1 fully read
-    issue(i + kRing - 1);
-    const int tr = 16 * warp;                            // this warp's tile: stage rows tr..tr+15
-    const int ts = t0 + i * kStage + tr;
-    if (ts >= t_end) continue;
-    const uint8_t *sb = smem + (i % kRing) * G::STAGE;
-    const uint32_t sKlo = smem_addr(sb), sVlo = smem_addr(sb + G::OFF_VLO);
-    const uint8_t *khi = sb + G::OFF_KHI, *vhi = sb + G::OFF_VHI;
-    const uint8_t *kss = sb + G::OFF_KSC, *vss = sb + G::OFF_VSC;
-    const int mi = lane >> 3;
-    const int lrow = tr + (mi & 1) * 8 + (lane & 7);     // ldmatrix row address of this lane
-
-    // ---------------- scores S^T for the tile
-    uint32_t skg[NB / 2], skg8[NB / 2];                  // K scales of tokens g, g+8 (f16 pairs)
-    if constexpr (NB == 8) {
-      const uint4 s0 = *reinterpret_cast<const uint4 *>(kss + (tr + g) * G::SB);
-      const uint4 s1 = *reinterpret_cast<const uint4 *>(kss + (tr + g + 8) * G::SB);
-      skg[0] = s0.x; skg[1] = s0.y; skg[2] = s0.z; skg[3] = s0.w;
-      skg8[0] = s1.x; skg8[1] = s1.y; skg8[2] = s1.z; skg8[3] = s1.w;
-    } else {
-      const uint2 s0 = *reinterpret_cast<const uint2 *>(kss + (tr + g) * G::SB);
-      const uint2 s1 = *reinterpret_cast<const uint2 *>(kss + (tr + g + 8) * G::SB);
-      skg[0] = s0.x; skg[1] = s0.y;
-      skg8[0] = s1.x; skg8[1] = s1.y;
-    }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < NB / 2; ++j) {
-      uint32_t kw[4];                                    // (g, 2j), (g+8, 2j), (g, 2j+1), (g+8, 2j+1)
-      ldsm_x4(sKlo + lo_off<NB>(lrow, 2 * j + (mi >> 1)), kw);
-      const uint4 hg = *reinterpret_cast<const uint4 *>(khi + (tr + g) * G::TS + 16 * j);
-      const uint4 hg8 = *reinterpret_cast<const uint4 *>(khi + (tr + g + 8) * G::TS + 16 * j);
-      const float2 sg = __half22float2(u32_as_h2(skg[j])), sg8 = __half22float2(u32_as_h2(skg8[j]));
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int b = 2 * j + e2;
-        const uint32_t Hg = prmt(e2 ? hg.z : hg.x, e2 ? hg.w : hg.y, sel_k);
-        const uint32_t Hg8 = prmt(e2 ? hg8.z : hg8.x, e2 ? hg8.w : hg8.y, sel_k);
+      for (int b = 0; b < NB; ++b) {
+        const uint32_t wg = lds32(kg + 24 * b + 4 * c), wg8 = lds32(kg8 + 24 * b + 4 * c);
+        const uint2 hg = *reinterpret_cast<const uint2 *>(kg + 24 * b + 16);
+        const uint2 hg8 = *reinterpret_cast<const uint2 *>(kg8 + 24 * b + 16);
         uint32_t ug[4], u8[4];
-        unpack6(kw[2 * e2], Hg, ug);
-        unpack6(kw[2 * e2 + 1], Hg8, u8);
+        unpack6(wg, prmt(hg.x, hg.y, sel_k), ug);
+        unpack6(wg8, prmt(hg8.x, hg8.y, sel_k), u8);
         const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
         const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
         float d[4];
         mma16816_c(d, A0, bq[2 * b][0], bq[2 * b][1], zq0[b], zq1[b], zq0[b], zq1[b]);
         mma16816(d, A1, bq[2 * b + 1][0], bq[2 * b + 1][1]);
-        const float kg = e2 ? sg.y : sg.x, kg8 = e2 ? sg8.y : sg8.x;
-        acc[0] = fmaf(kg, d[0], acc[0]);
-        acc[1] = fmaf(kg, d[1], acc[1]);
-        acc[2] = fmaf(kg8, d[2], acc[2]);
-        acc[3] = fmaf(kg8, d[3], acc[3]);
+        const float2 sg = __half22float2(u32_as_h2(skg[b >> 1])), sg8 = __half22float2(u32_as_h2(skg8[b >> 1]));
+        const float kgs = (b & 1) ? sg.y : sg.x, kgs8 = (b & 1) ? sg8.y : sg8.x;
+        acc[0] = fmaf(kgs, d[0], acc[0]);
+        acc[1] = fmaf(kgs, d[1], acc[1]);
+        acc[2] = fmaf(kgs8, d[2], acc[2]);
+        acc[3] = fmaf(kgs8, d[3], acc[3]);
       }
-    }
-    // hi + lo columns -> whole scores of rows r0, r1 (lanes c and c ^ 2 then agree)
+      // hi + lo columns -> whole scores of rows r0, r1 (lanes c and c ^ 2 then agree)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 2);
-    float s[4] = {acc[0] * alpha0, acc[1] * alpha1, acc[2] * alpha0, acc[3] * alpha1};
-    if (ts + 16 > t1 || ts + 15 > min_lim) {
-      const int ta = ts + g, tb = ta + 8;
-      if (!(ta < t1 && ta <= lim0)) s[0] = -INFINITY;
-      if (!(ta < t1 && ta <= lim1)) s[1] = -INFINITY;
-      if (!(tb < t1 && tb <= lim0)) s[2] = -INFINITY;
-      if (!(tb < t1 && tb <= lim1)) s[3] = -INFINITY;
-    }
-    // ---------------- online softmax (base 2)
-    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+      for (int k = 0; k < 4; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], 2);
+      float s[4] = {acc[0] * alpha0, acc[1] * alpha1, acc[2] * alpha0, acc[3] * alpha1};
+      if (ts + 16 > t1 || ts + 15 > min_lim) {
+        const int ta = ts + g, tb = ta + 8;
+        if (!(ta < t1 && ta <= lim0)) s[0] = -INFINITY;
+        if (!(ta < t1 && ta <= lim1)) s[1] = -INFINITY;
+        if (!(tb < t1 && tb <= lim0)) s[2] = -INFINITY;
+        if (!(tb < t1 && tb <= lim1)) s[3] = -INFINITY;
+      }
+      // online softmax (base 2)
+      float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
-    for (int k = 4; k < 32; k <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, k));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, k));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
-    const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    l0 *= corr0;
-    l1 *= corr1;
-    if (__any_sync(0xffffffffu, corr0 != 1.0f || corr1 != 1.0f)) {
-      Dw[0] *= corr0;
-      Dw[1] *= corr1;
-#pragma unroll
-      for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          O[b][h][0] *= corr0;
-          O[b][h][1] *= corr1;
-          O[b][h][2] *= corr0;
-          O[b][h][3] *= corr1;
-        }
-    }
-    const float p0 = ex2(s[0] - mu0), p1 = ex2(s[1] - mu1), p2 = ex2(s[2] - mu0), p3 = ex2(s[3] - mu1);
-    l0 += p0 + p2;
-    l1 += p1 + p3;
-
-    // ---------------- P into the B layout: columns 0-3 hi parts, 4-7 lo parts of rows 0-3
-    uint32_t bm0, bm1, ba0, ba1;
-    {
+      for (int k = 4; k < 32; k <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, k));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, k));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float mu0 = mn0 == -INFINITY ? 0.0f : mn0, mu1 = mn1 == -INFINITY ? 0.0f : mn1;
+      const float corr0 = ex2(m0 - mu0), corr1 = ex2(m1 - mu1);
+      m0 = mn0;
+      m1 = mn1;
+      const float p0 = ex2(s[0] - mu0), p1 = ex2(s[1] - mu1), p2 = ex2(s[2] - mu0), p3 = ex2(s[3] - mu1);
+      l0 = fmaf(l0, corr0, p0 + p2);
+      l1 = fmaf(l1, corr1, p1 + p3);
+      // P into the B layout: columns 0-3 hi parts, 4-7 lo parts of rows 0-3; for the lo columns
+      // also the hi part of the same row (the scale product's error term)
       const uint32_t h01 = pack_f16x2(p0, p1), h23 = pack_f16x2(p2, p3);
       const float2 f01 = __half22float2(u32_as_h2(h01)), f23 = __half22float2(u32_as_h2(h23));
       const uint32_t l01 = pack_f16x2(p0 - f01.x, p1 - f01.y), l23 = pack_f16x2(p2 - f23.x, p3 - f23.y);
-      bm0 = movm_t(c >= 2 ? l01 : h01);                  // main part of column g
-      bm1 = movm_t(c >= 2 ? l23 : h23);
-      ba0 = movm_t(h01);                                 // hi part of row (g & 3), for the lo columns
-      ba1 = movm_t(h23);
-      if (g < 4) ba0 = ba1 = 0u;
+      uint4 pb;
+      pb.x = movm_t(c >= 2 ? l01 : h01);                 // main part of column g
+      pb.y = movm_t(c >= 2 ? l23 : h23);
+      pb.z = movm_t(h01);
+      pb.w = movm_t(h23);
+      if (g < 4) pb.z = pb.w = 0u;
+      uint8_t *xs = xch + ((tw * 2 + (i & 1)) * 32 + lane) * 32;
+      *reinterpret_cast<uint4 *>(xs) = pb;
+      *reinterpret_cast<float2 *>(xs + 16) = make_float2(corr0, corr1);
     }
-    // V scales of tokens 2c, 2c+1, 2c+8, 2c+9 (f16 pairs of blocks)
-    uint32_t va[NB / 2], vb[NB / 2], vc[NB / 2], vd[NB / 2];
-    {
-      const uint8_t *v0 = vss + (tr + 2 * c) * G::SB;
+    // reduce l over the token lanes; one lane per row pair publishes (m, l)
 #pragma unroll
-      for (int k = 0; k < NB / 2; ++k) {
-        va[k] = *reinterpret_cast<const uint32_t *>(v0 + 4 * k);
-        vb[k] = *reinterpret_cast<const uint32_t *>(v0 + G::SB + 4 * k);
-        vc[k] = *reinterpret_cast<const uint32_t *>(v0 + 8 * G::SB + 4 * k);
-        vd[k] = *reinterpret_cast<const uint32_t *>(v0 + 9 * G::SB + 4 * k);
+    for (int k = 4; k < 32; k <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, k);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, k);
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    __syncthreads();                                     // every warp is done with the rings
+    float *cm = reinterpret_cast<float *>(smem);
+    float *cl = cm + 16;
+    if (g == 0 && c < 2) {
+      cm[tw * 4 + r0] = m0;
+      cm[tw * 4 + r1] = m1;
+      cl[tw * 4 + r0] = l0;
+      cl[tw * 4 + r1] = l1;
+    }
+  } else {
+    // =============================== V warps: O^T += V^T . P'^T per block, P' = p * s_v
+    float O[NB][2][4];
+    float Dw[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) O[b][h][k] = 0.0f;
+    // byte (g & 3) of two tokens' high words into bytes 0 and 2; halfword (g & 1) of two
+    // tokens' low-plane words into one word
+    const uint32_t sel_v = (uint32_t)(g & 3) | ((uint32_t)(4 + (g & 3)) << 8);
+    const uint32_t sel_h = (g & 1) ? 0x7632u : 0x5410u;
+    const int gb = min(g, NB - 1);
+
+    for (int i = 0; i <= n_stages; ++i) {
+      cp_async_wait<1>();
+      __syncthreads();
+      issue(i + 2);
+      const int j = i - 1;                               // the stage these warps consume
+      const int tr = 16 * tw;
+      const int ts = t0 + j * kStage + tr;
+      if (j < 0 || ts >= t_end) continue;
+      const uint8_t *xs = xch + ((tw * 2 + (j & 1)) * 32 + lane) * 32;
+      const uint4 pb = *reinterpret_cast<const uint4 *>(xs);
+      const float2 cr = *reinterpret_cast<const float2 *>(xs + 16);
+      if (__any_sync(0xffffffffu, cr.x != 1.0f || cr.y != 1.0f)) {
+        Dw[0] *= cr.x;
+        Dw[1] *= cr.y;
+#pragma unroll
+        for (int b = 0; b < NB; ++b)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            O[b][h][0] *= cr.x;
+            O[b][h][1] *= cr.y;
+            O[b][h][2] *= cr.x;
+            O[b][h][3] *= cr.y;
+          }
       }
-    }
-    // W term: rows g < NB of its A operand hold block g's V scales (tokens 2c, 2c+1 / 2c+8, 2c+9)
-    {
-      const int gb = min(g, NB - 1);
-      const uint8_t *v0 = vss + (tr + 2 * c) * G::SB + 2 * gb;
-      const uint32_t wa = *reinterpret_cast<const uint16_t *>(v0);
-      const uint32_t wb = *reinterpret_cast<const uint16_t *>(v0 + G::SB);
-      const uint32_t wc = *reinterpret_cast<const uint16_t *>(v0 + 8 * G::SB);
-      const uint32_t wd = *reinterpret_cast<const uint16_t *>(v0 + 9 * G::SB);
-      const uint32_t Aw[4] = {g < NB ? (wa | (wb << 16)) : 0u, 0u, g < NB ? (wc | (wd << 16)) : 0u, 0u};
-      mma16816(Dw, Aw, bm0, bm1);
-    }
-    // ---------------- O^T += V^T . P'^T per block, P' = p * s_v as hi + lo
-    const uint8_t *vh0 = vhi + (tr + 2 * c) * G::TS + 4 * (g >> 2);
+      const uint8_t *sb = smem + G::OFF_V + (j % kRing) * G::SLOT;
+      // V rows of tokens 2c, 2c+1, 2c+8, 2c+9 and their scale rows
+      const uint8_t *va = sb + (tr + 2 * c) * G::PITCH, *vb = va + G::PITCH;
+      const uint8_t *vc = va + 8 * G::PITCH, *vd = va + 9 * G::PITCH;
+      const uint8_t *sa = sb + G::OFF_SC + (tr + 2 * c) * G::SB;
+      uint32_t s2c[NB / 2], s2c1[NB / 2], s2c8[NB / 2], s2c9[NB / 2];
+      if constexpr (NB == 8) {
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(sa), x1 = *reinterpret_cast<const uint4 *>(sa + G::SB);
+        const uint4 x8 = *reinterpret_cast<const uint4 *>(sa + 8 * G::SB), x9 = *reinterpret_cast<const uint4 *>(sa + 9 * G::SB);
+        s2c[0] = x0.x; s2c[1] = x0.y; s2c[2] = x0.z; s2c[3] = x0.w;
+        s2c1[0] = x1.x; s2c1[1] = x1.y; s2c1[2] = x1.z; s2c1[3] = x1.w;
+        s2c8[0] = x8.x; s2c8[1] = x8.y; s2c8[2] = x8.z; s2c8[3] = x8.w;
+        s2c9[0] = x9.x; s2c9[1] = x9.y; s2c9[2] = x9.z; s2c9[3] = x9.w;
+      } else {
+        const uint2 x0 = *reinterpret_cast<const uint2 *>(sa), x1 = *reinterpret_cast<const uint2 *>(sa + G::SB);
+        const uint2 x8 = *reinterpret_cast<const uint2 *>(sa + 8 * G::SB), x9 = *reinterpret_cast<const uint2 *>(sa + 9 * G::SB);
+        s2c[0] = x0.x; s2c[1] = x0.y; s2c1[0] = x1.x; s2c1[1] = x1.y;
+        s2c8[0] = x8.x; s2c8[1] = x8.y; s2c9[0] = x9.x; s2c9[1] = x9.y;
+      }
+      // W term: rows g < NB of its A operand hold block g's V scales
+      {
+        const uint32_t wa = *reinterpret_cast<const uint16_t *>(sa + 2 * gb);
+        const uint32_t wb = *reinterpret_cast<const uint16_t *>(sa + G::SB + 2 * gb);
+        const uint32_t wc = *reinterpret_cast<const uint16_t *>(sa + 8 * G::SB + 2 * gb);
+        const uint32_t wd = *reinterpret_cast<const uint16_t *>(sa + 9 * G::SB + 2 * gb);
+        const uint32_t Aw[4] = {g < NB ? (wa | (wb << 16)) : 0u, 0u, g < NB ? (wc | (wd << 16)) : 0u, 0u};
+        mma16816(Dw, Aw, pb.x, pb.y);
+      }
 #pragma unroll
-    for (int j = 0; j < NB / 2; ++j) {
-      uint32_t vw[4];                                    // (2c.., 2j), (2c+8.., 2j), (2c.., 2j+1), (2c+8.., 2j+1)
-      ldsm_x4_t(sVlo + lo_off<NB>(lrow, 2 * j + (mi >> 1)), vw);
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int b = 2 * j + e2;
-        const uint8_t *vhb = vh0 + 8 * b;
-        const uint32_t Ha = prmt(*reinterpret_cast<const uint32_t *>(vhb),
-                                 *reinterpret_cast<const uint32_t *>(vhb + G::TS), sel_v);
-        const uint32_t Hb = prmt(*reinterpret_cast<const uint32_t *>(vhb + 8 * G::TS),
-                                 *reinterpret_cast<const uint32_t *>(vhb + 9 * G::TS), sel_v);
+      for (int b = 0; b < NB; ++b) {
+        const int lo = 24 * b + 4 * (g >> 1), hi = 24 * b + 16 + 4 * (g >> 2);
+        const uint32_t wa = prmt(lds32(va + lo), lds32(vb + lo), sel_h);
+        const uint32_t wb = prmt(lds32(vc + lo), lds32(vd + lo), sel_h);
+        const uint32_t Ha = prmt(lds32(va + hi), lds32(vb + hi), sel_v);
+        const uint32_t Hb = prmt(lds32(vc + hi), lds32(vd + hi), sel_v);
         uint32_t ua[4], ub[4];
-        unpack6(vw[2 * e2], Ha, ua);
-        unpack6(vw[2 * e2 + 1], Hb, ub);
-        const uint32_t sel = e2 ? 0x7632u : 0x5410u;
-        const uint32_t sp0 = prmt(va[j], vb[j], sel), sp1 = prmt(vc[j], vd[j], sel);
+        unpack6(wa, Ha, ua);
+        unpack6(wb, Hb, ub);
+        const uint32_t sel = (b & 1) ? 0x7632u : 0x5410u;
+        const uint32_t sp0 = prmt(s2c[b >> 1], s2c1[b >> 1], sel), sp1 = prmt(s2c8[b >> 1], s2c9[b >> 1], sel);
         // hi columns: rn(p_hi s); lo columns: rn(p_lo s + (p_hi s - rn(p_hi s))), the error term
         // exact by the f16 fma
-        const uint32_t th0 = hmul2(ba0, sp0), th1 = hmul2(ba1, sp1);
-        const uint32_t x0 = hfma2(ba0, sp0, th0 ^ 0x80008000u), x1 = hfma2(ba1, sp1, th1 ^ 0x80008000u);
-        const uint32_t B0 = hfma2(bm0, sp0, x0), B1 = hfma2(bm1, sp1, x1);
+        const uint32_t th0 = hmul2(pb.z, sp0), th1 = hmul2(pb.w, sp1);
+        const uint32_t x0 = hfma2(pb.z, sp0, th0 ^ 0x80008000u), x1 = hfma2(pb.w, sp1, th1 ^ 0x80008000u);
+        const uint32_t B0 = hfma2(pb.x, sp0, x0), B1 = hfma2(pb.y, sp1, x1);
         const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};   // dims 4g (row g), 4g+1 (row g+8)
         const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};   // dims 4g+2, 4g+3
         mma16816(O[b][0], A0, B0, B1);
         mma16816(O[b][1], A1, B0, B1);
       }
     }
-  }
-
-  // ---------------- warp state: l over the token lanes, hi + lo columns of O and W
+    // hi + lo columns of O and W
 #pragma unroll
-  for (int k = 4; k < 32; k <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, k);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, k);
-  }
+    for (int b = 0; b < NB; ++b)
 #pragma unroll
-  for (int b = 0; b < NB; ++b)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+        for (int k = 0; k < 4; ++k) O[b][h][k] += __shfl_xor_sync(0xffffffffu, O[b][h][k], 2);
+    Dw[0] += __shfl_xor_sync(0xffffffffu, Dw[0], 2);
+    Dw[1] += __shfl_xor_sync(0xffffffffu, Dw[1], 2);
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+    __syncthreads();                                     // every warp is done with the rings
+    float *co = reinterpret_cast<float *>(smem) + 32;     // [tile][4][D] after cm/cl
+    // value = u * s_v - 32 s_v: even dims entered as u * 2^-24, odd dims as 16 u * 2^-24
 #pragma unroll
-      for (int k = 0; k < 4; ++k) O[b][h][k] += __shfl_xor_sync(0xffffffffu, O[b][h][k], 2);
-  Dw[0] += __shfl_xor_sync(0xffffffffu, Dw[0], 2);
-  Dw[1] += __shfl_xor_sync(0xffffffffu, Dw[1], 2);
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-  __syncthreads();                                       // every warp is done with the ring
-
-  // ---------------- combine the four warps: cm/cl [warp][4], co [warp][4][D]
-  float *cm = reinterpret_cast<float *>(smem);
-  float *cl = cm + kWarps * 4;
-  float *co = cl + kWarps * 4;
-  if (g == 0 && c < 2) {
-    cm[warp * 4 + r0] = m0;
-    cm[warp * 4 + r1] = m1;
-    cl[warp * 4 + r0] = l0;
-    cl[warp * 4 + r1] = l1;
-  }
-  // value = u * s_v - 32 s_v: even dims entered as u * 2^-24, odd dims as 16 u * 2^-24
+    for (int b = 0; b < NB; ++b) {
+      const float w0 = 32.0f * __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);
+      const float w1 = 32.0f * __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);
+      if (c < 2) {
 #pragma unroll
-  for (int b = 0; b < NB; ++b) {
-    const float w0 = 32.0f * __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);
-    const float w1 = 32.0f * __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);
-    if (c < 2) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int d = 32 * b + 4 * g + 2 * h;
-        *reinterpret_cast<float2 *>(co + (warp * 4 + r0) * D + d) =
-            make_float2(fmaf(O[b][h][0], 16777216.0f, -w0), fmaf(O[b][h][2], 1048576.0f, -w0));
-        *reinterpret_cast<float2 *>(co + (warp * 4 + r1) * D + d) =
-            make_float2(fmaf(O[b][h][1], 16777216.0f, -w1), fmaf(O[b][h][3], 1048576.0f, -w1));
+        for (int h = 0; h < 2; ++h) {
+          const int d = 32 * b + 4 * g + 2 * h;
+          *reinterpret_cast<float2 *>(co + (tw * 4 + r0) * D + d) =
+              make_float2(fmaf(O[b][h][0], 16777216.0f, -w0), fmaf(O[b][h][2], 1048576.0f, -w0));
+          *reinterpret_cast<float2 *>(co + (tw * 4 + r1) * D + d) =
+              make_float2(fmaf(O[b][h][1], 16777216.0f, -w1), fmaf(O[b][h][3], 1048576.0f, -w1));
+        }
       }
     }
   }
   __syncthreads();
+  // ---------------- combine the four tiles: cm/cl [tile][4], co [tile][4][D]
+  const float *cm = reinterpret_cast<const float *>(smem);
+  const float *cl = cm + 16;
+  const float *co = cm + 32;
   for (int r = 0; r < R; ++r) {
     if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * 4 + r]);
-    float wt[kWarps], L = 0.0f;
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 4 + r]);
+    float wt[4], L = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < 4; ++w) {
       wt[w] = cm[w * 4 + r] == -INFINITY ? 0.0f : ex2(cm[w * 4 + r] - M);
       L = fmaf(cl[w * 4 + r], wt[w], L);
     }
     const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
     const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
-#pragma unroll
-    for (int d = threadIdx.x; d < D; d += kWarps * 32) {
+    for (int d = threadIdx.x; d < D; d += kThreads) {
       float acc = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) acc = fmaf(co[(w * 4 + r) * D + d], wt[w], acc);
+      for (int w = 0; w < 4; ++w) acc = fmaf(co[(w * 4 + r) * D + d], wt[w], acc);
       a.part_o[pi * D + d] = acc;
     }
     if (threadIdx.x == 0) {
@@ -498,7 +510,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Geom<D>::SMEM;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

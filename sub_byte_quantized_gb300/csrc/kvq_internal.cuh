@@ -19,9 +19,9 @@ constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-
 #define KVQ_MMA_MIN_BLOCKS 3
 #endif
 constexpr int kMmaWarpsPerSm = 4 * KVQ_MMA_MIN_BLOCKS;
-// Tensor-core phase 1 for Q6_0: resident CTAs (of four warps) per SM, by head_dim (shared-memory
-// ring of three 64-token stages: 84 KB at D = 256, 45 KB at D = 128).
-__host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 : 3; }
+// Tensor-core phase 1 for Q6_0: resident CTAs (of eight warps) per SM (shared-memory ring of three
+// 64-token stages plus the score exchange: 92 KB at D = 256, 53 KB at D = 128).
+__host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 : 2; }
 // Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, at most four query rows per
 // kv head (gqa * n_q).
 __host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows <= 4; }
