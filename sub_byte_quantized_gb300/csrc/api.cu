@@ -90,10 +90,11 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
   return KVQ_OK;
 }
 
-// Automatic split-K chunk, sized so that the body of every (batch, kv head) is covered by one wave
-// of the tensor-core kernel that will run: for the 4-bit layouts four times the smallest multiple
-// of 64 tokens that gives one slice to every resident warp (four warps per chunk); for the Q6_0
-// kernel the smallest multiple of 64 that gives one chunk to every resident CTA.
+// Automatic split-K chunk, sized for the tensor-core kernel that will run. Decode (up to eight
+// query rows per kv head), one wave: for the 4-bit layouts four times the smallest multiple of 64
+// tokens that gives one slice to every resident warp (four warps per chunk); for the Q6_0 kernel
+// the smallest multiple of 64 that gives one chunk to every resident CTA. Many rows (Hadamard
+// prefill): about four waves of 64-row CTAs.
 int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -102,6 +103,15 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
   if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
     const long long ctas = (long long)sms * kvq::kMmaQ6CtasPerSm(c.D);
     chunk = ((work + ctas - 1) / ctas + 63) / 64 * 64;
+  } else if (kvq::prefill_shape(c.layout, c.D, rows)) {
+    // row-side kernel: CTAs of 64 query rows; split the body into enough chunks for about four
+    // waves of resident CTAs
+    const long long row_ctas = (long long)((rows + kvq::kPrefillRows - 1) / kvq::kPrefillRows) * n_heads;
+    const long long want = 4LL * sms * kvq::kPrefillCtasPerSm;
+    long long n_chunks = (want + row_ctas - 1) / row_ctas;
+    if (n_chunks < 1) n_chunks = 1;
+    const long long body = n_body > 0 ? n_body : 1;
+    chunk = ((body + n_chunks - 1) / n_chunks + 63) / 64 * 64;
   } else {
     const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
     chunk = 4 * (((work + warps - 1) / warps + 63) / 64 * 64);
@@ -239,7 +249,7 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   const bool mma = kvq::mma_supported(a);
-  a.win_in_reduce = mma && a.n_win > 0;          // the tensor-core kernel covers the body chunks only
+  a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);   // the decode tensor-core kernels cover the body chunks only
   // the tensor-core kernel prepares the Hadamard query itself; the CUDA-core one reads it
   if (a.cache.layout == KVQ_HAD_INT4 && !mma) e = kvq::launch_had_prep(a, s);
   const bool prof = g_ev_begin && g_ev_end;
@@ -356,7 +366,7 @@ extern "C" kvq_status kvq_decode_attend_static(const kvq_cache *cache, const voi
   a.out = out;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool mma = kvq::mma_supported(a);
-  a.win_in_reduce = mma && a.n_win > 0;
+  a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);
   if (a.cache.layout == KVQ_HAD_INT4 && !mma) e = kvq::launch_had_prep(a, s);
   if (e == cudaSuccess) e = mma ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
   if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);

@@ -66,40 +66,6 @@ __host__ __device__ constexpr int smem_bytes() {
   return kWarps * 2 * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
 }
 
-// Q4_0 V operand: eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
-// (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the signed code values (n ^ 8) - 8. One lop3 places
-// a field in the mantissa under the exponent of 1024 (0x6400) with the sign flip folded in; one
-// f16 add/fma removes the offset.
-__device__ __forceinline__ void unpack8_q4(uint32_t w, uint32_t (&o)[4]) {
-  const uint32_t w8 = w >> 8;
-  o[0] = hadd2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u), kHm1032);
-  o[1] = hfma2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
-  o[2] = hadd2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u), kHm1032);
-  o[3] = hfma2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
-}
-
-// K and asymmetric-V operands: the same four pairs as unpack8_q4, but each code u (Q4_0: u = n ^ 8,
-// the code plus 8; asymmetric: u = n) is placed in the mantissa of an f16 with a zero exponent,
-// i.e. the exact subnormal u * 2^-24 (high fields: 16 u * 2^-24). One lop3 per pair, no f16
-// arithmetic. For K the query entries facing high fields are divided by 16, the 2^-24 goes into
-// the row's scale and the Q4_0 offset -8 * sum(q) into the accumulator's initial value; for V the
-// output is rescaled in the epilogue and the zero-point term comes from its own small mma.
-template <bool ASYM>
-__device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
-  const uint32_t w8 = w >> 8;
-  if (!ASYM) {
-    o[0] = lop3<0x6a>(w, 0x000F000Fu, 0x00080008u);
-    o[1] = lop3<0x6a>(w, 0x00F000F0u, 0x00800080u);
-    o[2] = lop3<0x6a>(w8, 0x000F000Fu, 0x00080008u);
-    o[3] = lop3<0x6a>(w8, 0x00F000F0u, 0x00800080u);
-  } else {
-    o[0] = w & 0x000F000Fu;
-    o[1] = w & 0x00F000F0u;
-    o[2] = w8 & 0x000F000Fu;
-    o[3] = w8 & 0x00F000F0u;
-  }
-}
-
 __device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
   const int qi = r % a.n_q;
   return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
@@ -698,12 +664,14 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
 bool mma_supported(const AttendArgs &a) {
   const int L = a.cache.layout;
   if (L == KVQ_Q6_0) return mma_q6_supported(a);
+  if (prefill_supported(a)) return true;
   return (L == KVQ_Q4_0 || L == KVQ_ASYM4_G32 || L == KVQ_HAD_INT4) && a.cache.D == kD && a.gqa * a.n_q <= 8 &&
          a.n_body > 0 && a.chunk % kStage == 0;
 }
 
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
   const bool split = a.q_dtype == KVQ_F32;
+  if (prefill_supported(a)) return launch_attend_prefill(a, st);
   switch (a.cache.layout) {
     case KVQ_Q6_0: return launch_attend_mma_q6(a, st);
     case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4, false>(a, st);   // int8 query codes are exact

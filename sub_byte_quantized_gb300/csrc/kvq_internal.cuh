@@ -25,6 +25,12 @@ __host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 :
 // Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, at most four query rows per
 // kv head (gqa * n_q).
 __host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows <= 4; }
+// Row-side tensor-core kernel: 64 query rows per CTA, three resident CTAs per SM.
+constexpr int kPrefillRows = 64;
+constexpr int kPrefillCtasPerSm = 3;
+__host__ __device__ constexpr bool prefill_shape(int layout, int D, int rows) {
+  return layout == KVQ_HAD_INT4 && D == 128 && rows > 8;
+}
 
 // Device-side view of a cache; index 0 = K, 1 = V.
 struct CacheView {
@@ -70,6 +76,10 @@ bool mma_supported(const AttendArgs &a);
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st);
 bool mma_q6_supported(const AttendArgs &a);
 cudaError_t launch_attend_mma_q6(const AttendArgs &a, cudaStream_t st);
+// Tensor-core phase 1 with the query rows on the M side (more than eight rows per kv head, e.g.
+// causal prefill chunks), Hadamard int4 layout.
+bool prefill_supported(const AttendArgs &a);
+cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st);
 
 // ----------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }

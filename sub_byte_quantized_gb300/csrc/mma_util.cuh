@@ -96,5 +96,39 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 // f16x2 constants (bit patterns): 1/16, -1032, -72 in both halves.
 constexpr uint32_t kH16th = 0x2C002C00u, kHm1032 = 0xE408E408u, kHm72 = 0xD480D480u;
 
+// Q4_0 V operand: eight 4-bit fields n0..n7 of w (n0 = bits 0-3) -> four exact f16 pairs
+// (n0,n4), (n1,n5), (n2,n6), (n3,n7) holding the signed code values (n ^ 8) - 8. One lop3 places
+// a field in the mantissa under the exponent of 1024 (0x6400) with the sign flip folded in; one
+// f16 add/fma removes the offset.
+__device__ __forceinline__ void unpack8_q4(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  o[0] = hadd2(lop3<0x6a>(w, 0x000F000Fu, 0x64086408u), kHm1032);
+  o[1] = hfma2(lop3<0x6a>(w, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
+  o[2] = hadd2(lop3<0x6a>(w8, 0x000F000Fu, 0x64086408u), kHm1032);
+  o[3] = hfma2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
+}
+
+// K and asymmetric-V operands: the same four pairs as unpack8_q4, but each code u (Q4_0: u = n ^ 8,
+// the code plus 8; asymmetric: u = n) is placed in the mantissa of an f16 with a zero exponent,
+// i.e. the exact subnormal u * 2^-24 (high fields: 16 u * 2^-24). One lop3 per pair, no f16
+// arithmetic. For K the query entries facing high fields are divided by 16, the 2^-24 goes into
+// the row's scale and the Q4_0 offset -8 * sum(q) into the accumulator's initial value; for V the
+// output is rescaled in the epilogue and the zero-point term comes from its own small mma.
+template <bool ASYM>
+__device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  if (!ASYM) {
+    o[0] = lop3<0x6a>(w, 0x000F000Fu, 0x00080008u);
+    o[1] = lop3<0x6a>(w, 0x00F000F0u, 0x00800080u);
+    o[2] = lop3<0x6a>(w8, 0x000F000Fu, 0x00080008u);
+    o[3] = lop3<0x6a>(w8, 0x00F000F0u, 0x00800080u);
+  } else {
+    o[0] = w & 0x000F000Fu;
+    o[1] = w & 0x00F000F0u;
+    o[2] = w8 & 0x000F000Fu;
+    o[3] = w8 & 0x00F000F0u;
+  }
+}
+
 }  // namespace mma
 }  // namespace kvq

@@ -5,10 +5,12 @@
 // Hadamard layout the combined output is still in the rotated basis and is un-rotated here
 // (in-warp FWHT times 1/sqrt(D)).
 //
-// Grid: one CTA per (query row, 32-dim slice) -- one CTA per row for the Hadamard layout, whose
-// un-rotation needs the whole row. Eight warps split the chunks; each lane owns one (or D/32)
-// output dims and keeps a running (M, L, O) over batches of eight chunks whose loads are all in
-// flight together. The warps are combined in shared memory.
+// Two shapes. Few rows (decode): one CTA per (query row, 32-dim slice) -- one CTA per row for the
+// Hadamard layout, whose un-rotation needs the whole row. Eight warps split the chunks; each lane
+// owns one (or D/32) output dims and keeps a running (M, L, O) over batches of eight chunks whose
+// loads are all in flight together. The warps are combined in shared memory. Many rows (prefill
+// chunks, large batches): one warp per row, eight rows per CTA, the lane owning D/32 consecutive
+// dims, no shared memory.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -133,13 +135,88 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   }
 }
 
+// One warp per row (many rows; the window, if any, is a partial of its own).
+template <int D, bool HAD>
+__global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendArgs a, unsigned rows) {
+  constexpr int VPL = D / 32;
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.wait;" ::: "memory");     // phase-1 partials are complete
+#endif
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * kWarps + warp;
+  if (row >= rows) return;
+  const int qi = (int)(row % a.n_q);
+  const int lim = a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+  const int n_vis_body = min(a.n_chunks, lim / a.chunk + 1);
+  const bool win_vis = a.n_win > 0 && a.n_body <= lim;
+  const float *pm = a.part_m + row * a.C;
+  const float *pl = a.part_l + row * a.C;
+  const float *po = a.part_o + row * a.C * (size_t)D + lane * VPL;
+  float M = -INFINITY, L = 0.0f, O[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
+  for (int base = 0; base < a.C; base += kBatch) {
+    float mc[kBatch], lc[kBatch], oc[kBatch][VPL];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = base + u;
+      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : win_vis);
+      mc[u] = vis ? pm[c] : -INFINITY;
+      lc[u] = vis ? pl[c] : 0.0f;
+      if constexpr (VPL == 4) {
+        const float4 v = vis ? *reinterpret_cast<const float4 *>(po + (size_t)c * D) : make_float4(0.f, 0.f, 0.f, 0.f);
+        oc[u][0] = v.x; oc[u][1] = v.y; oc[u][2] = v.z; oc[u][3] = v.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) oc[u][i] = vis ? po[(size_t)c * D + i] : 0.0f;
+      }
+    }
+    float bm = M;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, mc[u]);
+    if (bm == -INFINITY) continue;
+    const float corr = __expf(M - bm);
+    L *= corr;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) O[i] *= corr;
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const float w = __expf(mc[u] - bm);
+      L = fmaf(lc[u], w, L);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) O[i] = fmaf(oc[u][i], w, O[i]);
+    }
+    M = bm;
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) O[i] *= inv;
+  if (HAD) {
+    warp_fwht<VPL>(O, lane);
+    const float cD = inv_sqrt_dim(D);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) O[i] *= cD;
+  }
+  float *out = a.out + row * D + lane * VPL;
+  if constexpr (VPL == 4) {
+    *reinterpret_cast<float4 *>(out) = make_float4(O[0], O[1], O[2], O[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) out[i] = O[i];
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl) {
   const unsigned rows = (unsigned)((size_t)a.cache.B * a.Hq * a.n_q);
   const bool had = a.cache.layout == KVQ_HAD_INT4;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // many rows and no window work here: one warp per row
+  const bool per_warp = !a.win_in_reduce && rows >= 4u * (unsigned)sms * kWarps;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows, had ? 1 : a.cache.D / 32);
+  cfg.gridDim = per_warp ? dim3((rows + kWarps - 1) / kWarps) : dim3(rows, had ? 1 : a.cache.D / 32);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
@@ -148,6 +225,13 @@ cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if (per_warp) {
+    if (a.cache.D == 128)
+      return had ? cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<128, true>, a, rows)
+                 : cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<128, false>, a, rows);
+    return had ? cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<256, true>, a, rows)
+               : cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<256, false>, a, rows);
+  }
   if (a.cache.D == 128)
     return had ? cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128, true>, a)
                : cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128, false>, a);

@@ -89,6 +89,30 @@ def test_q6_tensor_core_rows(D, gqa, n_q, causal, q_dtype):
     run_case(w, kv_len=1001, n_q=n_q, chunk=192, q_dtype=q_dtype, fill=937)
 
 
+@pytest.mark.parametrize("gqa,n_q,causal,n_recent,q_dtype,chunk", [
+    (2, 5, True, 8, None, 64),        # ten rows: just past the decode kernel's eight
+    (1, 16, True, 0, "f32", 128),     # no window
+    (4, 33, True, 16, "f16", 192),    # 132 rows: three 64-row CTAs, the last one ragged
+    (2, 64, False, 64, None, 0),      # many rows without causal limits, automatic chunk
+    (2, 200, True, 64, None, 0),      # causal limits crossing chunk boundaries
+])
+def test_hadamard_prefill_rows(gqa, n_q, causal, n_recent, q_dtype, chunk):
+    """Row-side tensor-core phase 1 (more than eight query rows per kv head) against the oracle:
+    the chunk's rows are appended after a bulk fill, as in a causal prefill step."""
+    w = WORKLOADS["c3_had_int4_prefill"].scaled(batch=2, n_kv_heads=2, n_q_heads=2 * gqa, n_recent=n_recent,
+                                                causal=causal)
+    run_case(w, kv_len=1000, n_q=n_q, chunk=chunk, q_dtype=q_dtype, fill=1000 - n_q)
+
+
+@pytest.mark.parametrize("layout,D", [("q4_0", 128), ("q6_0", 256), ("asym4_g32", 128)])
+def test_many_rows_reduce(layout, D):
+    """Enough query rows (B * H_q * n_q >= 4 * SMs * 8) for phase 2's one-warp-per-row form,
+    causal rows crossing chunk boundaries."""
+    w = WORKLOADS["c3_had_int4_prefill"].scaled(layout=layout, head_dim=D, batch=4, n_kv_heads=4, n_q_heads=16,
+                                                n_recent=0)
+    run_case(w, kv_len=300, n_q=80, chunk=64, fill=220)
+
+
 def test_hadamard_window_covers_everything():
     w = WORKLOADS["c3_had_int4_decode"].scaled(batch=2, n_recent=512)
     run_case(w, 300)                      # n_recent >= kv_len: all tokens exact f32
