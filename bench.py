@@ -107,6 +107,16 @@ def kernel_traffic(profile: str, kernel_file: str):
     return int(m_bytes.group(1))
 
 
+def chunk_rule(w, spec) -> str:
+    """How the automatic split-K chunk of this workload is chosen (it follows the phase-1 kernel)."""
+    rows = (w.n_q_heads // w.n_kv_heads) * spec.n_q
+    if w.layout == "q6_0" and w.head_dim in (128, 256) and rows <= 4:
+        return "automatic: one 64-token-multiple chunk per resident CTA of the Q6_0 kernel (two per SM), one wave"
+    if w.layout == "had_int4" and w.head_dim == 128 and rows > 8:
+        return "automatic: body split for about four waves of 64-query-row CTAs; the f32 window is one more chunk"
+    return "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp, one wave"
+
+
 def aggregate(world: int, units_per_rank: float, steps: int, elapsed_ms: float) -> float:
     """Whole-job throughput: all ranks' units over the (max-over-ranks) elapsed time, per second."""
     return world * units_per_rank * steps / (elapsed_ms / 1e3)
@@ -344,11 +354,10 @@ def main():
 
     def step(i, ev=None):
         c = caches[i % n_rep]
-        kvq.store(c, k_new, v_new, fill, stream=stream)
         if ev is not None:
             L.kvq_profile_phase1_events(ev[0].cuda_event, ev[1].cuda_event)
-        kvq.decode_attend(c, q, S, causal=spec.causal, q_pos0=spec.q_pos0, attn_scale=w.alpha, chunk=chunk,
-                          out=out, workspace=ws, stream=stream)
+        kvq.append_decode_attend(c, k_new, v_new, fill, q, S, causal=spec.causal, q_pos0=spec.q_pos0,
+                                 attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
         if ev is not None:
             L.kvq_profile_phase1_events(None, None)
 
@@ -447,8 +456,8 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload, "layout": w.layout,
                    "kv_len": S, "n_q": spec.n_q, "causal": spec.causal, "chunk": chunk,
-                   "chunk_rule": "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp",
-                   "step": f"append {S - fill} token(s) (K,V) + split-K attention",
+                   "chunk_rule": chunk_rule(w, spec),
+                   "step": f"append {S - fill} token(s) (K,V) + split-K attention, one library call",
                    "read_bytes_per_step": spec.read_bytes, "flops_per_step": spec.flops, "l2": l2_note,
                    "timing": ("CUDA graph of the K library steps; phase 1 timed by events in a second pass "
                               "of the same K steps") if use_graph else "stream launches with phase-1 events",
@@ -474,9 +483,8 @@ def main():
                 dv.copy_(hv, non_blocking=True)
                 dq.copy_(hq, non_blocking=True)
                 c = caches[i % n_rep]
-                kvq.store(c, dk, dv, fill, stream=stream)
-                kvq.decode_attend(c, dq, S, causal=spec.causal, q_pos0=spec.q_pos0, attn_scale=w.alpha, chunk=chunk,
-                                  out=out, workspace=ws, stream=stream)
+                kvq.append_decode_attend(c, dk, dv, fill, dq, S, causal=spec.causal, q_pos0=spec.q_pos0,
+                                         attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
                 hout.copy_(out, non_blocking=True)
             stream.synchronize()
         t_e2e = (time.perf_counter() - t0) / n_e2e
@@ -504,15 +512,13 @@ def variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1, n
     def time_plain(cs, wsb, ch):
         with torch.cuda.stream(stream):
             for i in range(5):
-                kvq.store(cs[i % n_rep], k_new, v_new, fill, stream=stream)
-                kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
-                                  stream=stream)
+                kvq.append_decode_attend(cs[i % n_rep], k_new, v_new, fill, q, S, attn_scale=w.alpha, chunk=ch,
+                                         out=out, workspace=wsb, stream=stream)
             torch.cuda.synchronize(dev)
             ev0.record(stream)
             for i in range(n):
-                kvq.store(cs[i % n_rep], k_new, v_new, fill, stream=stream)
-                kvq.decode_attend(cs[i % n_rep], q, S, attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb,
-                                  stream=stream)
+                kvq.append_decode_attend(cs[i % n_rep], k_new, v_new, fill, q, S, attn_scale=w.alpha, chunk=ch,
+                                         out=out, workspace=wsb, stream=stream)
             ev1.record(stream)
         torch.cuda.synchronize(dev)
         return ev0.elapsed_time(ev1) / n

@@ -145,10 +145,10 @@ int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q,
  * head attends tokens t < kv_len and, when causal != 0, t <= q_pos0 + i ([TR] causal
  * masking); a causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len.
  * score = attn_scale * q . k_hat. Phase 1 splits the tokens into chunks of `chunk` tokens
- * (a multiple of 64 in [64, 8192], e.g. 512 as in [OTQ]; 0 = automatic: four times the
- * smallest multiple of 64 that covers all (batch, kv head) bodies with one slice per resident
- * warp of the current device, so the split depends on the device's SM count) and writes per
- * (row, chunk) the
+ * (a multiple of 64 in [64, 8192], e.g. 512 as in [OTQ]; 0 = automatic, sized for the phase-1
+ * kernel that runs and the current device's SM count -- one wave of resident warps or CTAs for
+ * decode shapes, about four waves of 64-row CTAs for many query rows; kvq_attend_chunk returns
+ * it) and writes per (row, chunk) the
  * running max, the sum of exponentials and the unnormalised output to the workspace; phase 2
  * combines them with the online-softmax correction ([OTQ] Section 3.2). HAD_INT4: the query
  * is rotated and quantised to int8 (one f32 scale per row, amax / 127), body tokens are
@@ -161,6 +161,22 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
                              int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t causal,
                              int32_t q_pos0, float attn_scale, int32_t chunk, float *out,
                              void *workspace, size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * One decode (or prefill-chunk) step in one call: the append of n_new tokens at positions
+ * [pos0, pos0 + n_new) exactly as the cache layout's kvq_store_* (k_new/v_new and kv_dtype as
+ * there), then kvq_decode_attend with the remaining arguments, on the same stream. The result
+ * and the stored bytes are identical to those two calls. Because this call knows which token
+ * rows the append writes, the phase-1 work that does not read them starts while the append is
+ * still running. All arguments of both parts are validated before anything is launched; on an
+ * error status nothing has been launched. n_new == 0 is a plain kvq_decode_attend.
+ */
+kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, const void *v_new,
+                                    int32_t kv_dtype, int32_t n_new, int32_t pos0, const void *q,
+                                    int32_t q_dtype, int32_t n_q_heads, int32_t n_q, int32_t kv_len,
+                                    int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                                    float *out, void *workspace, size_t workspace_bytes,
+                                    kvq_stream_t stream);
 
 /*
  * HAD_INT4 test hook: the exact integer-domain body scores int8(q_rot) . int4(k_rot).

@@ -5,6 +5,6 @@ marshals torch tensors into its calls. Importing the package does not load the l
 first call does, and raises if it is missing.
 """
 from .api import (  # noqa: F401
-    KVCache, store, decode_attend, attend_workspace_bytes, attend_chunk, debug_scores_i32, row_bytes, cache_plane_bytes,
+    KVCache, store, decode_attend, append_decode_attend, attend_workspace_bytes, attend_chunk, debug_scores_i32, row_bytes, cache_plane_bytes,
 )
 from ._lib import KvqError, LAYOUT_IDS, EXPORTS  # noqa: F401

@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ESHAPE", 3: "KVQ_ECAPACITY
 EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0", "kvq_store_hadamard_int4",
            "kvq_store_asym4_g32", "kvq_attend_workspace_bytes", "kvq_decode_attend", "kvq_debug_scores_i32",
            "kvq_status_string", "kvq_last_error", "kvq_profile_phase1_events",
-           "kvq_attend_chunk", "kvq_decode_attend_static")
+           "kvq_attend_chunk", "kvq_decode_attend_static", "kvq_append_decode_attend")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ_STATIC_SCRATCH_BYTES in include/kvq.h
 
 
@@ -63,6 +63,9 @@ def lib() -> C.CDLL:
     L.kvq_attend_chunk.argtypes, L.kvq_attend_chunk.restype = [cache_p, I32, I32, I32, I32], I32
     L.kvq_decode_attend.argtypes = [cache_p, P, I32, I32, I32, I32, I32, I32, C.c_float, I32, P, P, SZ, P]
     L.kvq_decode_attend.restype = I32
+    L.kvq_append_decode_attend.argtypes = [cache_p, P, P, I32, I32, I32, P, I32, I32, I32, I32, I32, I32, C.c_float,
+                                           I32, P, P, SZ, P]
+    L.kvq_append_decode_attend.restype = I32
     L.kvq_decode_attend_static.argtypes = [cache_p, P, I32, I32, I32, I32, I32, I32, C.c_float, I32, P, P]
     L.kvq_decode_attend_static.restype = I32
     L.kvq_debug_scores_i32.argtypes = [cache_p, P, I32, I32, I32, I32, P, P, P]

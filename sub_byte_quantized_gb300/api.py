@@ -147,6 +147,39 @@ def decode_attend(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = F
     return out
 
 
+def append_decode_attend(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int, q: torch.Tensor,
+                         kv_len: int, causal: bool = False, q_pos0: int = 0, attn_scale: float | None = None,
+                         chunk: int = 0, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                         stream=None) -> torch.Tensor:
+    """store(cache, k_new, v_new, pos0) then decode_attend(cache, q, kv_len, ...) in one library
+    call (same results; the attention work that does not read the appended rows overlaps the
+    append)."""
+    _need_cuda("k_new", k_new)
+    _need_cuda("v_new", v_new)
+    _need_cuda("q", q)
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same shape and dtype")
+    Bk, H, n_new, Dk = k_new.shape
+    B, Hq, n_q, D = q.shape
+    if (Bk, H, Dk) != (cache.batch, cache.n_kv_heads, cache.head_dim) or B != cache.batch or D != cache.head_dim:
+        raise ValueError("k_new/q shape does not match the cache")
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    _need_cuda("out", out)
+    need = attend_workspace_bytes(cache, Hq, n_q, kv_len, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need_cuda("workspace", workspace)
+    L.check(L.lib().kvq_append_decode_attend(
+        C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, pos0, q.data_ptr(),
+        _DTYPES[q.dtype], Hq, n_q, kv_len, int(bool(causal)), q_pos0, float(attn_scale), chunk, out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "kvq_append_decode_attend")
+    return out
+
+
 def decode_attend_static(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = False, q_pos0: int = 0,
                          attn_scale: float | None = None, chunk: int = 0, out: torch.Tensor | None = None,
                          stream=None) -> torch.Tensor:

@@ -1,6 +1,7 @@
 // C ABI of the library: host-side validation, workspace layout and kernel launches.
 // Nothing here allocates, synchronises or prints; failures return a kvq_status and record a
 // one-line reason readable through kvq_last_error().
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -71,13 +72,13 @@ kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
   return KVQ_OK;
 }
 
-kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_new, const void *v_new, int dtype,
-                        int n_new, int pos0, kvq_stream_t stream) {
-  g_last_error[0] = 0;
-  kvq::CacheView v;
+// Validation of an append (no launch). want_layout < 0 accepts the cache's own layout.
+kvq_status check_store(int want_layout, const kvq_cache *cache, const void *k_new, const void *v_new, int dtype,
+                       int n_new, int pos0, kvq::CacheView &v) {
   kvq_status st = check_cache(cache, v);
   if (st != KVQ_OK) return st;
-  if (v.layout != want_layout) return fail(KVQ_EUNSUPPORTED, "cache layout %d does not match this store", v.layout);
+  if (want_layout >= 0 && v.layout != want_layout)
+    return fail(KVQ_EUNSUPPORTED, "cache layout %d does not match this store", v.layout);
   if (dtype < KVQ_F32 || dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown dtype %d", dtype);
   if (n_new < 0 || pos0 < 0) return fail(KVQ_EINVAL, "n_new and pos0 must be >= 0");
   if ((long long)pos0 + n_new > v.cap) return fail(KVQ_ECAPACITY, "pos0 + n_new = %lld > capacity %d",
@@ -85,7 +86,16 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
   if (n_new == 0) return KVQ_OK;
   if (!k_new || !v_new) return fail(KVQ_EINVAL, "k_new/v_new is NULL");
   if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(KVQ_EALIGN, "k_new/v_new not 16-byte aligned");
-  cudaError_t e = kvq::launch_store(v, k_new, v_new, dtype, n_new, pos0, stream);
+  return KVQ_OK;
+}
+
+kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_new, const void *v_new, int dtype,
+                        int n_new, int pos0, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::CacheView v;
+  kvq_status st = check_store(want_layout, cache, k_new, v_new, dtype, n_new, pos0, v);
+  if (st != KVQ_OK || n_new == 0) return st;
+  cudaError_t e = kvq::launch_store(v, k_new, v_new, dtype, n_new, pos0, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "store launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
@@ -147,6 +157,8 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
   a.n_chunks = (a.n_body + chunk - 1) / chunk;
   a.C = a.n_chunks + (a.n_win > 0 ? 1 : 0);
   a.win_in_reduce = 0;
+  a.fresh_lo = 0;
+  a.fresh_hi = INT_MAX;
   const size_t rows = (size_t)c.B * n_q_heads * n_q;
   size_t off = 0;
   const size_t o_m = off; off = round_up(off + rows * a.C * sizeof(float), 256);
@@ -226,11 +238,12 @@ int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q,
   return a.chunk;
 }
 
-kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
-                             int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
-                             float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream) {
-  g_last_error[0] = 0;
-  kvq::AttendArgs a;
+namespace {
+
+// Validation of an attention call and its workspace; on success `a` is fully resolved.
+kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                          int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                          float *out, void *workspace, size_t workspace_bytes, kvq::AttendArgs &a) {
   size_t need = 0;
   kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, nullptr);
   if (st != KVQ_OK) return st;
@@ -246,13 +259,21 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
   a.q_dtype = q_dtype;
   a.scale = attn_scale;
   a.out = out;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return KVQ_OK;
+}
+
+// Phase 1 (tensor-core or CUDA-core kernel) and phase 2 on `s`, with the optional phase-1 events.
+cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool events) {
   cudaError_t e = cudaSuccess;
   const bool mma = kvq::mma_supported(a);
   a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);   // the decode tensor-core kernels cover the body chunks only
-  // the tensor-core kernel prepares the Hadamard query itself; the CUDA-core one reads it
-  if (a.cache.layout == KVQ_HAD_INT4 && !mma) e = kvq::launch_had_prep(a, s);
-  const bool prof = g_ev_begin && g_ev_end;
+  // the tensor-core kernels prepare the Hadamard query themselves; the CUDA-core one reads it
+  if (a.cache.layout == KVQ_HAD_INT4 && !mma) {
+    a.fresh_lo = 0;                                      // its predecessor is then the prep kernel
+    a.fresh_hi = INT_MAX;
+    e = kvq::launch_had_prep(a, s);
+  }
+  const bool prof = events && g_ev_begin && g_ev_end;
   // Under stream capture an event record must be external to become a graph node.
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (e == cudaSuccess && prof) e = cudaStreamIsCapturing(s, &cap);
@@ -261,7 +282,46 @@ kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dt
   if (e == cudaSuccess) e = mma ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
   if (e == cudaSuccess && prof) e = cudaEventRecordWithFlags(g_ev_end, s, rec_flags);
   if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
+  return e;
+}
+
+}  // namespace
+
+kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                             int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                             float *out, void *workspace, size_t workspace_bytes, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  kvq_status st = prepare_attend(cache, q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk, out,
+                                 workspace, workspace_bytes, a);
+  if (st != KVQ_OK) return st;
+  cudaError_t e = launch_attend_sequence(a, reinterpret_cast<cudaStream_t>(stream), true);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t kv_dtype,
+                                    int32_t n_new, int32_t pos0, const void *q, int32_t q_dtype, int32_t n_q_heads,
+                                    int32_t n_q, int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale,
+                                    int32_t chunk, float *out, void *workspace, size_t workspace_bytes,
+                                    kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::CacheView v;
+  kvq_status st = check_store(-1, cache, k_new, v_new, kv_dtype, n_new, pos0, v);
+  if (st != KVQ_OK) return st;
+  kvq::AttendArgs a;
+  st = prepare_attend(cache, q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk, out, workspace,
+                      workspace_bytes, a);
+  if (st != KVQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n_new > 0) {
+    e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, pos0, s);
+    a.fresh_lo = pos0;                                   // the rows (and window slots) it writes
+    a.fresh_hi = pos0 + n_new;
+  }
+  if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "append/attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
 
@@ -364,12 +424,7 @@ extern "C" kvq_status kvq_decode_attend_static(const kvq_cache *cache, const voi
   a.q_dtype = q_dtype;
   a.scale = attn_scale;
   a.out = out;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool mma = kvq::mma_supported(a);
-  a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);
-  if (a.cache.layout == KVQ_HAD_INT4 && !mma) e = kvq::launch_had_prep(a, s);
-  if (e == cudaSuccess) e = mma ? kvq::launch_attend_mma(a, s) : kvq::launch_attend_generic(a, s);
-  if (e == cudaSuccess) e = kvq::launch_attend_reduce(a, s, true);
+  e = launch_attend_sequence(a, reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }

@@ -84,7 +84,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // upstream store complete before any read
 #endif
   const CacheView &cv = a.cache;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -103,6 +102,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     w_lim = max(w_lim, l);
     min_lim = min(min_lim, l);
   }
+  // rows appended by the preceding kernel: only the CTAs that read them wait for it
+  pdl_wait_if(t0 <= w_lim && t0 < a.fresh_hi && a.fresh_lo < min(t1, w_lim + 1));
   if (t0 > w_lim) return;                              // no row sees this chunk (phase 2 skips it)
   const int t_end = min(t1, w_lim + 1);
   const int n_stages = (t_end - t0 + kStage - 1) / kStage;

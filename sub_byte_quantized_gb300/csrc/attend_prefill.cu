@@ -81,7 +81,6 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) attend_prefill_had_ke
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // upstream store complete before any read
 #endif
   const CacheView &cv = a.cache;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -97,6 +96,9 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) attend_prefill_had_ke
   const int t1 = win ? a.kv_len : min(a.n_body, t0 + a.chunk);
   int w_lim = -1;
   for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit_of(a, r));
+  // rows appended by the preceding kernel (cache rows or window ring): only the CTAs that read
+  // them wait for it
+  pdl_wait_if(t0 <= w_lim && t0 < a.fresh_hi && a.fresh_lo < min(t1, w_lim + 1));
   if (t0 > w_lim) return;                              // no row of this CTA sees the chunk
   const int t_end = min(t1, w_lim + 1);
   const int stage_len = win ? kWinStage : kStage;

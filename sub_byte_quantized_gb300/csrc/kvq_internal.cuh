@@ -54,6 +54,10 @@ struct AttendArgs {
   int chunk, n_chunks;      // body chunks = ceil(n_body / chunk); + 1 window chunk if n_win
   int C;                    // total partials per row
   int win_in_reduce;        // HAD: phase 2 computes the window chunk's partial itself
+  // Token rows [fresh_lo, fresh_hi) were written by the kernel launched just before phase 1 (an
+  // append in the same call): only phase-1 CTAs that read them, and the first CTA, wait for it.
+  // [0, INT_MAX) when the preceding kernel is unknown (every CTA waits).
+  int fresh_lo, fresh_hi;
   float *out;
   // workspace regions
   float *part_m, *part_l, *part_o;   // [rows][C], [rows][C], [rows][C][D]
@@ -82,6 +86,16 @@ bool prefill_supported(const AttendArgs &a);
 cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st);
 
 // ----------------------------------------------------------------- device helpers
+// Programmatic dependent launch: wait for the preceding kernel (and its memory) when this CTA
+// reads rows it wrote, or when it is the grid's first CTA -- so that the grid never completes
+// before its predecessor, and later kernels that wait on this grid also see the predecessor's
+// writes.
+__device__ __forceinline__ void pdl_wait_if(bool reads_fresh) {
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  const bool first = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+  if (first || reads_fresh) asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
 // Load 8 consecutive input elements starting at element index `e` (8-aligned) as f32.

@@ -91,6 +91,21 @@ def test_validation_without_device(L):
     assert L.kvq_status_string(7) == b"workspace too small"
 
 
+def test_append_attend_validates_both_parts_first(L):
+    """The combined append + attend call rejects a bad argument of either part before launching."""
+    p = C.byref
+    c = _cache()
+    ws = 1 << 20
+    # append part: capacity, misaligned k_new, unknown K/V dtype
+    assert L.kvq_append_decode_attend(p(c), 16, 16, 1, 10, 60, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws, None) == 3
+    assert L.kvq_append_decode_attend(p(c), 17, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws, None) == 5
+    assert L.kvq_append_decode_attend(p(c), 16, 16, 9, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws, None) == 1
+    # attention part (the append alone is valid): kv_len 0, workspace too small, misaligned q
+    assert L.kvq_append_decode_attend(p(c), 16, 16, 1, 1, 7, 16, 1, 8, 1, 0, 0, 0, 1.0, 0, 16, 256, ws, None) == 1
+    assert L.kvq_append_decode_attend(p(c), 16, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 16, None) == 7
+    assert L.kvq_append_decode_attend(p(c), 16, 16, 1, 1, 7, 20, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws, None) == 5
+
+
 def test_workspace_size_formula(L):
     c = _cache(cap=131072)
     # rows = 1*8*1, chunks = 256: m + l + o, each region rounded up to 256 bytes

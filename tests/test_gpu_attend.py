@@ -113,6 +113,53 @@ def test_many_rows_reduce(layout, D):
     run_case(w, kv_len=300, n_q=80, chunk=64, fill=220)
 
 
+@pytest.mark.parametrize("name,kv_len,n_q,fill", [
+    ("c2_q4_0_llama3_8b", 1500, None, 1499),
+    ("c3_had_int4_decode", 1100, None, 1099),
+    ("c3_had_int4_prefill", 1100, 64, 1036),
+    ("c4_q6_0_gemma", 1300, None, 1299),
+    ("c5_asym4_g32_llama70b_128k", 2100, None, 2099),
+])
+def test_append_decode_attend_matches_two_calls(name, kv_len, n_q, fill):
+    """append_decode_attend == store + decode_attend, bit for bit (stored planes and outputs), and
+    within tolerance of the oracle: only the phase-1 work that reads the appended rows waits for
+    the append."""
+    w = WORKLOADS[name]
+    if w.causal:
+        w = w.scaled(q_pos0=kv_len - n_q)
+    inp = make_inputs(w, kv_len=kv_len, n_q=n_q)
+    B, H, S, D = inp["k"].shape
+    d = device_inputs(inp)
+    q_rows = inp["q"].shape[2]
+    q_pos0 = S - q_rows if w.causal else 0
+    outs = []
+    caches = []
+    for fused in (False, True):
+        c = kvq.KVCache(w.layout, B, H, D, S, n_recent=w.n_recent, device="cuda")
+        kvq.store(c, d["k"][:, :, :fill].contiguous(), d["v"][:, :, :fill].contiguous(), 0)
+        kn, vn = d["k"][:, :, fill:].contiguous(), d["v"][:, :, fill:].contiguous()
+        if fused:
+            out = kvq.append_decode_attend(c, kn, vn, fill, d["q"], S, causal=w.causal, q_pos0=q_pos0,
+                                           attn_scale=w.alpha)
+        else:
+            kvq.store(c, kn, vn, fill)
+            out = kvq.decode_attend(c, d["q"], S, causal=w.causal, q_pos0=q_pos0, attn_scale=w.alpha)
+        torch.cuda.synchronize()
+        outs.append(out.cpu())
+        caches.append(c)
+    assert torch.equal(outs[0], outs[1])
+    for t in ("k", "v"):
+        for plane, x in caches[0].planes[t].items():
+            assert torch.equal(x.cpu(), caches[1].planes[t][plane].cpu()), (t, plane)
+    oc = OA.OracleCache(w.layout, B, H, D, S, n_recent=w.n_recent)
+    oc.store(inp["k"][:, :, :fill], inp["v"][:, :, :fill], 0)
+    oc.store(inp["k"][:, :, fill:], inp["v"][:, :, fill:], fill)
+    ref = oc.attend(inp["q"], w.alpha, S, causal=w.causal, q_pos0=q_pos0)
+    if isinstance(ref, tuple):
+        ref = ref[0]
+    check_close(outs[1].numpy(), ref, w.name)
+
+
 def test_hadamard_window_covers_everything():
     w = WORKLOADS["c3_had_int4_decode"].scaled(batch=2, n_recent=512)
     run_case(w, 300)                      # n_recent >= kv_len: all tokens exact f32
