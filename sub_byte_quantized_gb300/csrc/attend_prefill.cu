@@ -321,6 +321,18 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) attend_prefill_had_ke
     for (int k = 0; k < 4; ++k) O[j][k] = 0.0f;
   const uint32_t sKT = smem_addr(smem + kOffKT), sVT = smem_addr(smem + kOffVT);
   const int mi = lane >> 3;
+  // ldmatrix addresses: every row this lane points at has (row & 7) == (lane & 7), so the tile
+  // swizzle reduces to a per-lane constant XOR a compile-time constant per chunk.
+  // K: rows 8j + (lane & 7), chunk 4m + mi.  V: rows 16kk + 8 (mi & 1) + (lane & 7), chunk 2p + (mi >> 1).
+  const uint32_t kbase = sKT + (uint32_t)(lane & 7) * kTileRow;
+  const uint32_t vbase = sVT + (uint32_t)((mi & 1) * 8 + (lane & 7)) * kTileRow;
+  const int kx = mi ^ (lane & 7), vx = (mi >> 1) ^ (lane & 7);
+  auto kofs = [&](int m) -> uint32_t {                   // chunk 4m + mi
+    return (uint32_t)((((kx ^ (((m & 1) << 2) | ((m >> 1) << 1))) & 7) | ((m >> 1) << 3)) << 4);
+  };
+  auto vofs = [&](int p) -> uint32_t {                   // chunk 2p + (mi >> 1)
+    return (uint32_t)((((vx ^ ((2 * p) ^ ((p >> 2) << 1))) & 7) | ((p >> 2) << 3)) << 4);
+  };
 
   for (int i = 0; i < n_stages; ++i) {
     cp_async_wait<kRing - 2>();
@@ -359,21 +371,27 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) attend_prefill_had_ke
       const int tsub = ts + 32 * hh;
       if (tsub > warp_lim) break;
       float s[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        // k-step pairs outermost: consecutive mma on one tile's accumulator are four apart
+        float d[4][4] = {};
 #pragma unroll
         for (int m = 0; m < 4; ++m) {                    // k-steps 2m, 2m+1
-          uint32_t kw[4];
-          ldsm_x4(sKT + toff(32 * hh + 8 * j + (lane & 7), 4 * m + mi), kw);
-          mma16816(d, aq[2 * m], kw[0], kw[1]);
-          mma16816(d, aq[2 * m + 1], kw[2], kw[3]);
+          uint32_t kw[4][4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) ldsm_x4(kbase + (32 * hh + 8 * j) * kTileRow + kofs(m), kw[j]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(d[j], aq[2 * m], kw[j][0], kw[j][1]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mma16816(d[j], aq[2 * m + 1], kw[j][2], kw[j][3]);
         }
-        const float2 sk = *reinterpret_cast<const float2 *>(skf + 32 * hh + 8 * j + 2 * c);
-        s[j][0] = d[0] * alpha_g * sk.x;
-        s[j][1] = d[1] * alpha_g * sk.y;
-        s[j][2] = d[2] * alpha_g8 * sk.x;
-        s[j][3] = d[3] * alpha_g8 * sk.y;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 sk = *reinterpret_cast<const float2 *>(skf + 32 * hh + 8 * j + 2 * c);
+          s[j][0] = d[j][0] * alpha_g * sk.x;
+          s[j][1] = d[j][1] * alpha_g * sk.y;
+          s[j][2] = d[j][2] * alpha_g8 * sk.x;
+          s[j][3] = d[j][3] * alpha_g8 * sk.y;
+        }
       }
       if (tsub + 32 > t1 || tsub + 31 > warp_min) {
 #pragma unroll
@@ -442,13 +460,22 @@ __global__ void __launch_bounds__(kWarps * 32, kCtasPerSm) attend_prefill_had_ke
           al[e] = pack_f16x2(s[j][xx] - f.x, s[j][xx + 1] - f.y);
         }
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {                    // output tiles 2p, 2p+1
-          uint32_t vw[4];                                // b0/b1 of tile 2p, b0/b1 of tile 2p+1
-          ldsm_x4_t(sVT + toff(32 * hh + 16 * kk + (mi & 1) * 8 + (lane & 7), 2 * p + (mi >> 1)), vw);
-          mma16816(O[2 * p], ah, vw[0], vw[1]);
-          mma16816(O[2 * p], al, vw[0], vw[1]);
-          mma16816(O[2 * p + 1], ah, vw[2], vw[3]);
-          mma16816(O[2 * p + 1], al, vw[2], vw[3]);
+        for (int pg = 0; pg < 2; ++pg) {                 // output tiles 8pg .. 8pg+7
+          uint32_t vw[4][4];                             // per p: b0/b1 of tile 2p, b0/b1 of tile 2p+1
+#pragma unroll
+          for (int p4 = 0; p4 < 4; ++p4)
+            ldsm_x4_t(vbase + (32 * hh + 16 * kk) * kTileRow + vofs(4 * pg + p4), vw[p4]);
+          // hi parts of the eight tiles, then the lo parts: eight mma between two on one tile
+#pragma unroll
+          for (int p4 = 0; p4 < 4; ++p4) {
+            mma16816(O[2 * (4 * pg + p4)], ah, vw[p4][0], vw[p4][1]);
+            mma16816(O[2 * (4 * pg + p4) + 1], ah, vw[p4][2], vw[p4][3]);
+          }
+#pragma unroll
+          for (int p4 = 0; p4 < 4; ++p4) {
+            mma16816(O[2 * (4 * pg + p4)], al, vw[p4][0], vw[p4][1]);
+            mma16816(O[2 * (4 * pg + p4) + 1], al, vw[p4][2], vw[p4][3]);
+          }
         }
       }
     }
