@@ -90,6 +90,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# committed ncu summaries of the phase-1 kernel per workload: (summary file, kernel source file)
+PROFILES = {
+    "c5_q4_0_llama70b_128k": ("attend_phase1_c5_q4_0_128k.md", "attend_mma.cu"),
+    "c4_q6_0_gemma": ("attend_phase1_q6_0_c4_gemma.md", "attend_mma_q6.cu"),
+    "c3_had_int4_prefill": ("attend_prefill_c3_had_int4.md", "attend_prefill.cu"),
+}
+
+
 def kernel_traffic(profile: str, kernel_file: str):
     """DRAM bytes per launch from the committed ncu summary `profile`, or None when the kernel
     source changed since the counters were taken (the summary records the source's sha256)."""
@@ -434,9 +442,7 @@ def main():
     else:
         achieved = spec.read_bytes / (ph_mean / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak}
-    traffic = None
-    if args.workload == DEFAULT_WORKLOAD:
-        traffic = kernel_traffic("attend_phase1_c5_q4_0_128k.md", "attend_mma.cu")
+    traffic = kernel_traffic(*PROFILES[args.workload]) if args.workload in PROFILES else None
     roof.update({"peak_kind": peak_kind, "traffic": traffic, "kernel": "attend phase 1 (split-K chunk partials)",
                  "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
                  "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3,
