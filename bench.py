@@ -498,6 +498,7 @@ def main():
         line["e2e"] = {"value": spec.read_bytes / t_e2e / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": (hk.numel() + hv.numel() + hq.numel()) * el,
                        "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e}
+        line["store"] = store_timings(kvq, w, kd, vd, k_new, v_new, fill, stream, dev)
         if args.workload == DEFAULT_WORKLOAD:
             line["variants"] = variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1,
                                         min(K, 1000), chunk, make_caches, dev)
@@ -507,6 +508,37 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def store_timings(kvq, w, kd, vd, k_new, v_new, fill, stream, dev):
+    """The store kernel timed on its own (CUDA events on the launching stream): the append of this
+    workload's new rows (µs per call) and a bulk fill of the cache (input GB/s: bf16/f32 K and V
+    bytes read per second; the packed bytes written are 0.28 of them for Q4_0 from bf16)."""
+    import torch
+    B, H, S, D = kd.shape
+    c = kvq.KVCache(w.layout, B, H, D, S, n_recent=w.n_recent, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kf, vf = kd[:, :, :fill].contiguous(), vd[:, :, :fill].contiguous()
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    app_ms = timed(lambda: kvq.store(c, k_new, v_new, fill, stream=stream), 200)
+    fill_ms = timed(lambda: kvq.store(c, kf, vf, 0, stream=stream), 10)
+    in_bytes = 2 * kf.numel() * kf.element_size()
+    out_bytes = c.read_bytes(fill)
+    del c
+    return {"append_tokens": S - fill, "append_us": app_ms * 1e3, "fill_tokens": fill, "fill_us": fill_ms * 1e3,
+            "fill_input_gbs": in_bytes / (fill_ms / 1e3) / 1e9, "fill_output_gbs": out_bytes / (fill_ms / 1e3) / 1e9,
+            "timing": "CUDA events around back-to-back store launches on one stream"}
 
 
 def variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1, n, chunk, make_caches, dev):

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   constexpr int VPL = DS / 32;             // dims per lane
   __shared__ float sm_m[kWarps], sm_l[kWarps];
   __shared__ __align__(16) float sm_o[kWarps][DS];
+  __shared__ __align__(16) float sm_qw[HAD ? kWarps : 1][HAD ? D : 4];   // per-warp rotated query (window)
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.wait;" ::: "memory");     // phase-1 partials are complete
 #endif
@@ -42,10 +43,14 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   float M = -INFINITY, L = 0.0f, O[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
-  if (HAD && a.win_in_reduce && win_vis) {
+  if constexpr (HAD) {
+  if (a.win_in_reduce && win_vis) {
     // The exact-f32 recent window (tokens n_body .. kv_len-1, ring slot t mod n_recent), scored
-    // with the float32 rotated query: each warp takes every eighth window token and keeps an
-    // online softmax over them; its state then joins the chunk partials below.
+    // with the float32 rotated query. Warp w takes window tokens 8w .. 8w+7 of each group of 64,
+    // all eight at once: lane l scores token l / 4 over dims (l % 4) * D/4 .. +D/4 (reduced over
+    // the token's four lanes) and accumulates its output dims lane * VPL .. +VPL for the eight
+    // tokens; the loads of a group are all in flight together. The warp's state then joins the
+    // chunk partials below.
     const CacheView &cv = a.cache;
     const size_t bh = (row / a.n_q) / a.Hq * cv.H + ((row / a.n_q) % a.Hq) / a.gqa;
     // rotated query row (the tensor-core phase 1 prepares its int8 codes itself, so rotate here)
@@ -54,21 +59,71 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
     if (VPL == 4) load4_f32(a.q, a.q_dtype, row * D + lane * 4, qv);
     else load8_f32(a.q, a.q_dtype, row * D + lane * 8, qv);
     had_query_row<VPL>(qv, q8v, lane);
-    for (int t = a.n_body + warp; t <= lim && t < a.kv_len; t += kWarps) {
-      const size_t slot = (bh * cv.n_recent + (size_t)(t % cv.n_recent)) * D + lane * VPL;
+    constexpr int QS = D / 4;                             // dims per lane in the score
+    float *sm_q = sm_qw[HAD ? warp : 0];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) sm_q[lane * VPL + i] = qv[i];
+    __syncwarp();
+    float qs[QS];
+#pragma unroll
+    for (int i = 0; i < QS; ++i) qs[i] = sm_q[(lane & 3) * QS + i];
+    const int tl = lane >> 2;                             // this lane's token within the warp's eight
+    const int n_w = a.kv_len - a.n_body;
+    for (int g0 = 0; g0 < n_w; g0 += 8 * kWarps) {
+      const int t = a.n_body + g0 + 8 * warp + tl;        // this lane's token
+      const bool tv = t < a.kv_len && t <= lim;
+      const size_t slot = (bh * cv.n_recent + (size_t)((tv ? t : a.n_body) % cv.n_recent)) * D;
+      const float *kr = cv.ring[0] + slot + (lane & 3) * QS;
       float dot = 0.0f;
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) dot = fmaf(qv[i], cv.ring[0][slot + i], dot);
+      for (int i = 0; i < QS; i += 4) {
+        const float4 k4 = tv ? *reinterpret_cast<const float4 *>(kr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        dot = fmaf(qs[i], k4.x, dot);
+        dot = fmaf(qs[i + 1], k4.y, dot);
+        dot = fmaf(qs[i + 2], k4.z, dot);
+        dot = fmaf(qs[i + 3], k4.w, dot);
+      }
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      const float sc = tv ? a.scale * dot : -INFINITY;
+      float gm = sc;
 #pragma unroll
-      for (int k = 16; k; k >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, k);
-      const float sc = a.scale * dot;
-      const float mn = fmaxf(M, sc);
-      const float corr = __expf(M - mn), p = __expf(sc - mn);
-      L = fmaf(L, corr, p);
+      for (int k = 4; k < 32; k <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, k));
+      if (gm == -INFINITY) continue;                      // no visible token in this warp's eight
+      const float mn = fmaxf(M, gm);
+      const float corr = __expf(M - mn);                  // M = -inf -> 0
+      const float p = tv ? __expf(sc - mn) : 0.0f;
+      float ps = (lane & 3) == 0 ? p : 0.0f;              // each token counted once
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) O[i] = fmaf(O[i], corr, p * cv.ring[1][slot + i]);
+      for (int k = 4; k < 32; k <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, k);
+      L = fmaf(L, corr, ps);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) O[i] *= corr;
+      // the eight V rows' slices, all loads in flight together (invalid tokens read a valid slot
+      // and get weight 0)
+      float4 vv[8][VPL / 4];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int tu = a.n_body + g0 + 8 * warp + u;
+        const int ts = tu < a.kv_len ? tu : a.n_body;
+        const float *vr = cv.ring[1] + (bh * cv.n_recent + (size_t)(ts % cv.n_recent)) * D + lane * VPL;
+#pragma unroll
+        for (int i = 0; i < VPL / 4; ++i) vv[u][i] = *reinterpret_cast<const float4 *>(vr + 4 * i);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float pu = __shfl_sync(0xffffffffu, p, 4 * u);
+#pragma unroll
+        for (int i = 0; i < VPL / 4; ++i) {
+          O[4 * i] = fmaf(pu, vv[u][i].x, O[4 * i]);
+          O[4 * i + 1] = fmaf(pu, vv[u][i].y, O[4 * i + 1]);
+          O[4 * i + 2] = fmaf(pu, vv[u][i].z, O[4 * i + 2]);
+          O[4 * i + 3] = fmaf(pu, vv[u][i].w, O[4 * i + 3]);
+        }
+      }
       M = mn;
     }
+  }
   }
   for (int base = warp; base < a.C; base += kWarps * kBatch) {
     float mc[kBatch], lc[kBatch], oc[kBatch][VPL];
