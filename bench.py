@@ -120,6 +120,8 @@ def chunk_rule(w, spec) -> str:
     rows = (w.n_q_heads // w.n_kv_heads) * spec.n_q
     if w.layout == "q6_0" and w.head_dim in (128, 256) and rows <= 4:
         return "automatic: one 64-token-multiple chunk per resident CTA of the Q6_0 kernel (two per SM), one wave"
+    if w.layout == "asym4_g32" and w.head_dim == 128 and rows <= 8:
+        return "automatic: one 64-token-multiple chunk per resident CTA of the warp-specialised kernel (two per SM), one wave"
     if w.layout == "had_int4" and w.head_dim == 128 and rows > 8:
         return "automatic: body split for about four waves of 64-query-row CTAs; the f32 window is one more chunk"
     return "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp, one wave"
@@ -570,10 +572,12 @@ def variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1, n
     torch.cuda.empty_cache()
     acaches = make_caches("asym4_g32", n_rep)
     a_bytes = acaches[0].read_bytes(S)
-    aws = torch.empty(kvq.attend_workspace_bytes(acaches[0], w.n_q_heads, 1, S, chunk), dtype=torch.uint8, device=dev)
-    a_ms = time_plain(acaches, aws, chunk)
+    achunk = kvq.attend_chunk(acaches[0], w.n_q_heads, 1, S, 0)        # its own automatic chunk
+    aws = torch.empty(kvq.attend_workspace_bytes(acaches[0], w.n_q_heads, 1, S, achunk), dtype=torch.uint8,
+                      device=dev)
+    a_ms = time_plain(acaches, aws, achunk)
     res["asym4_g32"] = {"us_per_layer": a_ms * 1e3, "read_bytes_per_step": a_bytes,
-                        "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches", "chunk": chunk}
+                        "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches", "chunk": achunk}
     return res
 
 

@@ -102,9 +102,9 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
 
 // Automatic split-K chunk, sized for the tensor-core kernel that will run. Decode (up to eight
 // query rows per kv head), one wave: for the 4-bit layouts four times the smallest multiple of 64
-// tokens that gives one slice to every resident warp (four warps per chunk); for the Q6_0 kernel
-// the smallest multiple of 64 that gives one chunk to every resident CTA. Many rows (Hadamard
-// prefill): about four waves of 64-row CTAs.
+// tokens that gives one slice to every resident warp (four warps per chunk); for the
+// warp-specialised kernels (Q6_0, asymmetric) the smallest multiple of 64 that gives one chunk to
+// every resident CTA. Many rows (Hadamard prefill): about four waves of 64-row CTAs.
 int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -122,6 +122,14 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
     if (n_chunks < 1) n_chunks = 1;
     const long long body = n_body > 0 ? n_body : 1;
     chunk = ((body + n_chunks - 1) / n_chunks + 63) / 64 * 64;
+  } else if (kvq::uses_mma4(c.layout)) {
+    // warp-specialised 4-bit kernel: one chunk per resident CTA, as many chunks per (batch, kv
+    // head) as fit one wave
+    const long long ctas = (long long)sms * kvq::kMma4CtasPerSm;
+    long long per_head = ctas / (n_heads > 0 ? n_heads : 1);
+    if (per_head < 1) per_head = 1;
+    const long long body = n_body > 0 ? n_body : 1;
+    chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
   } else {
     const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
     chunk = 4 * (((work + warps - 1) / warps + 63) / 64 * 64);

@@ -673,6 +673,7 @@ bool mma_supported(const AttendArgs &a) {
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
   const bool split = a.q_dtype == KVQ_F32;
   if (prefill_supported(a)) return launch_attend_prefill(a, st);
+  if (uses_mma4(a.cache.layout)) return launch_attend_mma4(a, st);
   switch (a.cache.layout) {
     case KVQ_Q6_0: return launch_attend_mma_q6(a, st);
     case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4, false>(a, st);   // int8 query codes are exact

@@ -19,6 +19,11 @@ constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-
 #define KVQ_MMA_MIN_BLOCKS 3
 #endif
 constexpr int kMmaWarpsPerSm = 4 * KVQ_MMA_MIN_BLOCKS;
+// Warp-specialised tensor-core phase 1 (CTAs of eight warps, two per SM; the automatic chunk gives
+// every resident CTA one chunk): used for the asymmetric layout, whose per-warp kernel runs out of
+// registers; Q4_0 and the Hadamard body keep the per-warp kernel (faster there on this part).
+constexpr int kMma4CtasPerSm = 2;
+__host__ __device__ constexpr bool uses_mma4(int layout) { return layout == KVQ_ASYM4_G32; }
 // Tensor-core phase 1 for Q6_0: resident CTAs (of eight warps) per SM (shared-memory ring of three
 // 64-token stages plus the score exchange: 92 KB at D = 256, 53 KB at D = 128).
 __host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 : 2; }
@@ -78,6 +83,7 @@ cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, 
 // cover the call (the caller then uses the generic kernel).
 bool mma_supported(const AttendArgs &a);
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st);
+cudaError_t launch_attend_mma4(const AttendArgs &a, cudaStream_t st);
 bool mma_q6_supported(const AttendArgs &a);
 cudaError_t launch_attend_mma_q6(const AttendArgs &a, cudaStream_t st);
 // Tensor-core phase 1 with the query rows on the M side (more than eight rows per kv head, e.g.
