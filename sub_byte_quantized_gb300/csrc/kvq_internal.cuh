@@ -30,11 +30,16 @@ __host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 :
 // Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, at most four query rows per
 // kv head (gqa * n_q).
 __host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows <= 4; }
-// Row-side tensor-core kernel: 64 query rows per CTA, three resident CTAs per SM.
+// Row-side tensor-core kernel: 64 query rows per CTA; three resident CTAs per SM for the Hadamard
+// layout, two for Q4_0 / asymmetric (their value tiles are hi + lo pairs).
 constexpr int kPrefillRows = 64;
 constexpr int kPrefillCtasPerSm = 3;
+#ifndef KVQ_PREFILL_BLOCK_LAYOUTS
+#define KVQ_PREFILL_BLOCK_LAYOUTS 1
+#endif
 __host__ __device__ constexpr bool prefill_shape(int layout, int D, int rows) {
-  return layout == KVQ_HAD_INT4 && D == 128 && rows > 8;
+  return (layout == KVQ_HAD_INT4 || (KVQ_PREFILL_BLOCK_LAYOUTS && (layout == KVQ_Q4_0 || layout == KVQ_ASYM4_G32))) &&
+         D == 128 && rows > 8;
 }
 
 // Device-side view of a cache; index 0 = K, 1 = V.

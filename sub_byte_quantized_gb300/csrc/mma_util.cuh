@@ -50,6 +50,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// m16n8k8: d += a . b, a0 / a1 = rows g / g+8 at k 2c, 2c+1; b0 = k 2c, 2c+1 of column g
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
 // d = a . b + c with a separate accumulator input
 __device__ __forceinline__ void mma16816_c(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
                                            float c0, float c1, float c2, float c3) {
@@ -128,6 +134,17 @@ __device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
     o[2] = w8 & 0x000F000Fu;
     o[3] = w8 & 0x00F000F0u;
   }
+}
+
+// Unsigned 4-bit fields n0..n7 of w -> four exact f16 pairs (n0,n4), (n1,n5), (n2,n6), (n3,n7)
+// holding n: the field is placed in the mantissa under the exponent of 1024 (low fields: 1024 + n,
+// high fields: 1024 + 16 n) and one f16 add / fma removes the offset.
+__device__ __forceinline__ void unpack8_u4(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  o[0] = hadd2(lop3<0xEA>(w, 0x000F000Fu, 0x64006400u), 0xE400E400u);
+  o[1] = hfma2(lop3<0xEA>(w, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
+  o[2] = hadd2(lop3<0xEA>(w8, 0x000F000Fu, 0x64006400u), 0xE400E400u);
+  o[3] = hfma2(lop3<0xEA>(w8, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
 }
 
 }  // namespace mma

@@ -160,6 +160,22 @@ def test_append_decode_attend_matches_two_calls(name, kv_len, n_q, fill):
     check_close(outs[1].numpy(), ref, w.name)
 
 
+@pytest.mark.parametrize("layout", ["q4_0", "asym4_g32"])
+@pytest.mark.parametrize("gqa,n_q,causal,q_dtype,chunk", [
+    (2, 5, True, None, 64),           # ten rows: just past the decode kernels' eight
+    (4, 33, True, "f16", 192),        # 132 rows: three 64-row CTAs, the last one ragged
+    (2, 64, False, None, 0),          # many rows without causal limits, automatic chunk
+    (2, 200, True, None, 0),          # causal limits crossing chunk boundaries
+    (1, 24, True, "f32", 128),        # f32 queries: the CUDA-core path
+])
+def test_block_layout_prefill_rows(layout, gqa, n_q, causal, q_dtype, chunk):
+    """Row-side tensor-core phase 1 for the per-block layouts (values split into f16 hi + lo tiles)
+    against the oracle, appended after a bulk fill as in a causal prefill step."""
+    w = WORKLOADS["c5_q4_0_llama70b_128k"].scaled(layout=layout, batch=2, n_kv_heads=2, n_q_heads=2 * gqa,
+                                                  causal=causal)
+    run_case(w, kv_len=1000, n_q=n_q, chunk=chunk, q_dtype=q_dtype, fill=1000 - n_q)
+
+
 def test_hadamard_window_covers_everything():
     w = WORKLOADS["c3_had_int4_decode"].scaled(batch=2, n_recent=512)
     run_case(w, 300)                      # n_recent >= kv_len: all tokens exact f32
