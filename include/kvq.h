@@ -178,6 +178,102 @@ kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, c
                                     float *out, void *workspace, size_t workspace_bytes,
                                     kvq_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Paged cache ([FT] "Scope": only the paged full-attention KV pool is quantized; "Changes":
+ * mha_pool allocates a packed buffer plus a separate scale buffer per spec). Token rows live in
+ * a pool of fixed-size pages shared by all sequences of a batch; a block table gives the pool
+ * page of each logical page of each sequence, and every sequence has its own length.
+ *   payload  u8  [n_pages][n_kv_heads][page_size][kvq_row_bytes(layout, head_dim)]
+ *   scale    f16 [n_pages][n_kv_heads][page_size][head_dim/32]   (Q4_0, Q6_0, ASYM4_G32)
+ *            f32 [n_pages][n_kv_heads][page_size]                (HAD_INT4)
+ *   zero     f16 [n_pages][n_kv_heads][page_size][head_dim/32]   (ASYM4_G32 only, else NULL)
+ *   recent   f32 [batch][n_kv_heads][n_recent][head_dim]         (HAD_INT4 with n_recent > 0:
+ *                                                                 one ring per sequence)
+ *   block_table  device i32 [batch][max_pages_per_seq]
+ * Token t of sequence b is row t % page_size of pool page block_table[b][t / page_size]. Byte
+ * layouts and quantisation are those of the contiguous cache (one token row is bit-identical).
+ * page_size is a power of two in [64, 2^20]: every 64-token stage the kernels stream is then a
+ * run of consecutive rows. The caller owns the pool and the table and keeps every entry that a
+ * call reads inside [0, n_pages); an entry outside is clamped into the pool (no access leaves
+ * it, the result is then unspecified). A sequence's logical capacity is
+ * max_pages_per_seq * page_size tokens.
+ */
+typedef struct kvq_paged_cache {
+  int32_t layout;             /* kvq_layout */
+  int32_t batch;              /* sequences (rows of the block table) */
+  int32_t n_kv_heads;
+  int32_t head_dim;           /* 128 or 256 */
+  int32_t page_size;          /* tokens per page: a power of two in [64, 2^20] */
+  int32_t n_pages;            /* pages in the pool */
+  int32_t max_pages_per_seq;  /* row length of the block table */
+  int32_t n_recent;           /* HAD_INT4: exact-f32 ring per sequence (0 = pure int4); others: 0 */
+  void *k_payload, *v_payload;
+  void *k_scale, *v_scale;
+  void *k_zero, *v_zero;
+  float *k_recent, *v_recent;
+  const int32_t *block_table;
+} kvq_paged_cache;
+
+/* Bytes of each pool plane of one of K or V: out_sizes = {payload, scale, zero, recent}. */
+kvq_status kvq_paged_cache_bytes(int32_t layout, int32_t n_pages, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t page_size, int32_t batch, int32_t n_recent, size_t out_sizes[4]);
+
+/*
+ * Append n_new tokens to every sequence: sequence b's rows go to positions
+ * [positions[b], positions[b] + n_new), through the block table.
+ *   k_new, v_new: device [batch][n_kv_heads][n_new][head_dim] in `dtype`.
+ *   positions:    device i32 [batch].
+ * Quantisation as kvq_store_* for the cache's layout (any layout; bit-identical rows). The
+ * positions are read on the device: a row whose position falls outside [0, max_pages_per_seq *
+ * page_size) is not written. HAD_INT4 with n_recent > 0 also writes the rotated f32 rows of the
+ * last min(n_new, n_recent) tokens to the sequence's ring slot (position mod n_recent).
+ * One kernel launch covers K and V. n_new == 0 is a no-op.
+ */
+kvq_status kvq_paged_store(const kvq_paged_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
+                           int32_t n_new, const int32_t *positions, kvq_stream_t stream);
+
+/* Workspace bytes / resolved chunk of kvq_paged_decode_attend for these arguments (0 on invalid
+ * arguments). max_kv_len as there. */
+size_t kvq_paged_attend_workspace_bytes(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q,
+                                        int32_t max_kv_len, int32_t chunk);
+int32_t kvq_paged_attend_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t max_kv_len,
+                               int32_t chunk);
+
+/*
+ * kvq_decode_attend over a paged cache with per-sequence lengths.
+ *   q    device [batch][n_q_heads][n_q][head_dim] in q_dtype
+ *   out  device f32 [batch][n_q_heads][n_q][head_dim]
+ *   seq_lens  device i32 [batch]: the number of cached tokens of each sequence, read on the
+ *             device and clamped into [0, max_kv_len].
+ *   max_kv_len  host: an upper bound of every seq_lens[b] (1 <= max_kv_len <= capacity); the
+ *             grid and the workspace are sized for it.
+ * Row i of each query head of sequence b attends t < seq_lens[b] and, when causal != 0,
+ * t <= seq_lens[b] - n_q + i (the n_q query rows are the sequence's newest tokens). A row that
+ * sees no token (an empty sequence, or a causal row before the sequence's start) gets zeros.
+ * HAD_INT4: the newest min(n_recent, seq_lens[b]) tokens of each sequence are read from its
+ * ring. Everything else (GQA mapping, chunking, the two phases, the workspace rule) is as
+ * kvq_decode_attend.
+ */
+kvq_status kvq_paged_decode_attend(const kvq_paged_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads,
+                                   int32_t n_q, const int32_t *seq_lens, int32_t max_kv_len, int32_t causal,
+                                   float attn_scale, int32_t chunk, float *out, void *workspace,
+                                   size_t workspace_bytes, kvq_stream_t stream);
+
+/*
+ * One paged decode (or prefill-chunk) step: append n_new tokens to the end of every sequence,
+ * at positions [seq_lens[b] - n_new, seq_lens[b]) (seq_lens = the lengths after the append),
+ * then kvq_paged_decode_attend with the remaining arguments. Result and stored bytes are those
+ * of kvq_paged_store + kvq_paged_decode_attend; as for kvq_append_decode_attend, phase-1 work
+ * that does not read the appended rows starts while the append runs. All arguments are
+ * validated before anything is launched. n_new == 0 is a plain kvq_paged_decode_attend.
+ */
+kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const void *k_new, const void *v_new,
+                                          int32_t kv_dtype, int32_t n_new, const void *q, int32_t q_dtype,
+                                          int32_t n_q_heads, int32_t n_q, const int32_t *seq_lens,
+                                          int32_t max_kv_len, int32_t causal, float attn_scale, int32_t chunk,
+                                          float *out, void *workspace, size_t workspace_bytes,
+                                          kvq_stream_t stream);
+
 /*
  * HAD_INT4 test hook: the exact integer-domain body scores int8(q_rot) . int4(k_rot).
  *   scores_out device i32 [batch][n_q_heads][n_q][kv_len - min(n_recent, kv_len)]

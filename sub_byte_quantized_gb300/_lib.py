@@ -21,7 +21,9 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ESHAPE", 3: "KVQ_ECAPACITY
 EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0", "kvq_store_hadamard_int4",
            "kvq_store_asym4_g32", "kvq_attend_workspace_bytes", "kvq_decode_attend", "kvq_debug_scores_i32",
            "kvq_status_string", "kvq_last_error", "kvq_profile_phase1_events",
-           "kvq_attend_chunk", "kvq_decode_attend_static", "kvq_append_decode_attend")
+           "kvq_attend_chunk", "kvq_decode_attend_static", "kvq_append_decode_attend",
+           "kvq_paged_cache_bytes", "kvq_paged_store", "kvq_paged_attend_workspace_bytes", "kvq_paged_attend_chunk",
+           "kvq_paged_decode_attend", "kvq_paged_append_decode_attend")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ_STATIC_SCRATCH_BYTES in include/kvq.h
 
 
@@ -32,6 +34,17 @@ class KvqCache(C.Structure):
                 ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
                 ("k_zero", C.c_void_p), ("v_zero", C.c_void_p),
                 ("k_recent", C.c_void_p), ("v_recent", C.c_void_p)]
+
+
+class KvqPagedCache(C.Structure):
+    _fields_ = [("layout", C.c_int32), ("batch", C.c_int32), ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("page_size", C.c_int32), ("n_pages", C.c_int32), ("max_pages_per_seq", C.c_int32),
+                ("n_recent", C.c_int32),
+                ("k_payload", C.c_void_p), ("v_payload", C.c_void_p),
+                ("k_scale", C.c_void_p), ("v_scale", C.c_void_p),
+                ("k_zero", C.c_void_p), ("v_zero", C.c_void_p),
+                ("k_recent", C.c_void_p), ("v_recent", C.c_void_p),
+                ("block_table", C.c_void_p)]
 
 
 class KvqError(RuntimeError):
@@ -70,6 +83,18 @@ def lib() -> C.CDLL:
     L.kvq_decode_attend_static.restype = I32
     L.kvq_debug_scores_i32.argtypes = [cache_p, P, I32, I32, I32, I32, P, P, P]
     L.kvq_debug_scores_i32.restype = I32
+    paged_p = C.POINTER(KvqPagedCache)
+    L.kvq_paged_cache_bytes.argtypes = [I32, I32, I32, I32, I32, I32, I32, C.POINTER(SZ)]
+    L.kvq_paged_cache_bytes.restype = I32
+    L.kvq_paged_store.argtypes, L.kvq_paged_store.restype = [paged_p, P, P, I32, I32, P, P], I32
+    L.kvq_paged_attend_workspace_bytes.argtypes = [paged_p, I32, I32, I32, I32]
+    L.kvq_paged_attend_workspace_bytes.restype = SZ
+    L.kvq_paged_attend_chunk.argtypes, L.kvq_paged_attend_chunk.restype = [paged_p, I32, I32, I32, I32], I32
+    L.kvq_paged_decode_attend.argtypes = [paged_p, P, I32, I32, I32, P, I32, I32, C.c_float, I32, P, P, SZ, P]
+    L.kvq_paged_decode_attend.restype = I32
+    L.kvq_paged_append_decode_attend.argtypes = [paged_p, P, P, I32, I32, P, I32, I32, I32, P, I32, I32, C.c_float,
+                                                 I32, P, P, SZ, P]
+    L.kvq_paged_append_decode_attend.restype = I32
     L.kvq_status_string.argtypes, L.kvq_status_string.restype = [I32], C.c_char_p
     L.kvq_last_error.argtypes, L.kvq_last_error.restype = [], C.c_char_p
     L.kvq_profile_phase1_events.argtypes, L.kvq_profile_phase1_events.restype = [P, P], I32

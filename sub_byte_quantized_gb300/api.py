@@ -214,3 +214,160 @@ def debug_scores_i32(cache: KVCache, q: torch.Tensor, kv_len: int, stream=None):
                                          buf.data_ptr(), s_q.data_ptr(), _stream(stream)),
             "kvq_debug_scores_i32")
     return buf[:B * Hq * n_q * n_body].view(B, Hq, n_q, n_body), s_q
+
+
+# ------------------------------------------------------------------ paged pool
+class PagedKVCache:
+    """Device planes of one layer's paged pool, its block table and the C struct describing them.
+
+    Planes (K and V each): payload u8 [n_pages][H_kv][page_size][row_bytes]; scale f16
+    [n_pages][H_kv][page_size][D/32] (f32 [n_pages][H_kv][page_size] for had_int4); zero f16
+    (asym4_g32); recent f32 [batch][H_kv][n_recent][D] (had_int4 with n_recent > 0, one ring per
+    sequence). block_table: int32 [batch][max_pages_per_seq] (pool page of each logical page),
+    owned by this object; the caller fills it (set_block_table) before storing.
+    """
+
+    def __init__(self, layout, batch: int, n_kv_heads: int, head_dim: int, page_size: int, n_pages: int,
+                 max_pages_per_seq: int, n_recent: int = 0, device="cuda"):
+        self.layout = _layout_id(layout)
+        self.batch, self.n_kv_heads, self.head_dim = batch, n_kv_heads, head_dim
+        self.page_size, self.n_pages, self.max_pages_per_seq = page_size, n_pages, max_pages_per_seq
+        self.capacity = page_size * max_pages_per_seq
+        self.n_recent = n_recent if self.layout == L.KVQ_HAD_INT4 else 0
+        out = (C.c_size_t * 4)()
+        L.check(L.lib().kvq_paged_cache_bytes(self.layout, n_pages, n_kv_heads, head_dim, page_size, batch,
+                                              self.n_recent, out), "kvq_paged_cache_bytes")
+        rb = row_bytes(self.layout, head_dim)
+        nb = head_dim // 32
+        dev = torch.device(device)
+        shp = (n_pages, n_kv_heads, page_size)
+        self.planes = {}
+        for t in ("k", "v"):
+            pl = {"payload": torch.zeros(shp + (rb,), dtype=torch.uint8, device=dev)}
+            if self.layout == L.KVQ_HAD_INT4:
+                pl["scale"] = torch.zeros(shp, dtype=torch.float32, device=dev)
+                if self.n_recent:
+                    pl["recent"] = torch.zeros((batch, n_kv_heads, self.n_recent, head_dim), dtype=torch.float32,
+                                               device=dev)
+            else:
+                pl["scale"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
+                if self.layout == L.KVQ_ASYM4_G32:
+                    pl["zero"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
+            assert pl["payload"].numel() == out[0]
+            self.planes[t] = pl
+        self.block_table = torch.zeros((batch, max_pages_per_seq), dtype=torch.int32, device=dev)
+        self.struct = L.KvqPagedCache(
+            self.layout, batch, n_kv_heads, head_dim, page_size, n_pages, max_pages_per_seq, self.n_recent,
+            _ptr(self.planes["k"]["payload"]), _ptr(self.planes["v"]["payload"]),
+            _ptr(self.planes["k"]["scale"]), _ptr(self.planes["v"]["scale"]),
+            _ptr(self.planes["k"].get("zero")), _ptr(self.planes["v"].get("zero")),
+            _ptr(self.planes["k"].get("recent")), _ptr(self.planes["v"].get("recent")),
+            _ptr(self.block_table))
+
+    def set_block_table(self, table) -> None:
+        """Copy an int [batch][max_pages_per_seq] table (pool page of each logical page)."""
+        t = torch.as_tensor(table, dtype=torch.int32)
+        if tuple(t.shape) != (self.batch, self.max_pages_per_seq):
+            raise ValueError("block table shape does not match the cache")
+        self.block_table.copy_(t)
+
+    def read_bytes(self, seq_lens) -> int:
+        """Packed bytes (payload + scales [+ zeros] [+ window]) one attention call reads."""
+        per_tok = row_bytes(self.layout, self.head_dim)
+        total = 0
+        for n in (int(x) for x in seq_lens):
+            if self.layout == L.KVQ_HAD_INT4:
+                n_w = min(self.n_recent, n)
+                total += (n - n_w) * (per_tok + 4) + n_w * self.head_dim * 4
+            else:
+                total += n * (per_tok + 2 * (self.head_dim // 32) * (2 if self.layout == L.KVQ_ASYM4_G32 else 1))
+        return 2 * self.n_kv_heads * total
+
+
+def _i32_vec(name: str, t: torch.Tensor, n: int) -> None:
+    _need_cuda(name, t)
+    if t.dtype != torch.int32 or t.numel() != n:
+        raise ValueError(f"{name} must be a CUDA int32 tensor of {n} entries")
+
+
+def paged_store(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor, positions: torch.Tensor,
+                stream=None) -> None:
+    """Append k_new/v_new [B][H_kv][n_new][D]: sequence b's rows at [positions[b], positions[b] + n_new)."""
+    _need_cuda("k_new", k_new)
+    _need_cuda("v_new", v_new)
+    _i32_vec("positions", positions, cache.batch)
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same shape and dtype")
+    B, H, n_new, D = k_new.shape
+    if (B, H, D) != (cache.batch, cache.n_kv_heads, cache.head_dim):
+        raise ValueError("k_new shape does not match the cache")
+    L.check(L.lib().kvq_paged_store(C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype],
+                                    n_new, positions.data_ptr(), _stream(stream)), "kvq_paged_store")
+
+
+def paged_attend_workspace_bytes(cache: PagedKVCache, n_q_heads: int, n_q: int, max_kv_len: int,
+                                 chunk: int = 0) -> int:
+    return int(L.lib().kvq_paged_attend_workspace_bytes(C.byref(cache.struct), n_q_heads, n_q, max_kv_len, chunk))
+
+
+def paged_attend_chunk(cache: PagedKVCache, n_q_heads: int, n_q: int, max_kv_len: int, chunk: int = 0) -> int:
+    return int(L.lib().kvq_paged_attend_chunk(C.byref(cache.struct), n_q_heads, n_q, max_kv_len, chunk))
+
+
+def _paged_out_ws(cache, q, max_kv_len, chunk, out, workspace):
+    B, Hq, n_q, D = q.shape
+    if B != cache.batch or D != cache.head_dim:
+        raise ValueError("q shape does not match the cache")
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    _need_cuda("out", out)
+    need = paged_attend_workspace_bytes(cache, Hq, n_q, max_kv_len, chunk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _need_cuda("workspace", workspace)
+    return out, workspace
+
+
+def paged_decode_attend(cache: PagedKVCache, q: torch.Tensor, seq_lens: torch.Tensor, max_kv_len: int,
+                        causal: bool = False, attn_scale: float | None = None, chunk: int = 0,
+                        out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Split-K attention of q [B][H_q][n_q][D] over each sequence's seq_lens[b] tokens -> f32 out
+    (causal rows are each sequence's newest n_q tokens)."""
+    _need_cuda("q", q)
+    _i32_vec("seq_lens", seq_lens, cache.batch)
+    Hq, n_q, D = q.shape[1], q.shape[2], q.shape[3]
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    out, workspace = _paged_out_ws(cache, q, max_kv_len, chunk, out, workspace)
+    L.check(L.lib().kvq_paged_decode_attend(
+        C.byref(cache.struct), q.data_ptr(), _DTYPES[q.dtype], Hq, n_q, seq_lens.data_ptr(), max_kv_len,
+        int(bool(causal)), float(attn_scale), chunk, out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "kvq_paged_decode_attend")
+    return out
+
+
+def paged_append_decode_attend(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                               seq_lens: torch.Tensor, max_kv_len: int, causal: bool = False,
+                               attn_scale: float | None = None, chunk: int = 0, out: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_store at [seq_lens[b] - n_new, seq_lens[b]) then paged_decode_attend, in one call."""
+    _need_cuda("k_new", k_new)
+    _need_cuda("v_new", v_new)
+    _need_cuda("q", q)
+    _i32_vec("seq_lens", seq_lens, cache.batch)
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same shape and dtype")
+    Bk, H, n_new, Dk = k_new.shape
+    if (Bk, H, Dk) != (cache.batch, cache.n_kv_heads, cache.head_dim):
+        raise ValueError("k_new shape does not match the cache")
+    Hq, n_q, D = q.shape[1], q.shape[2], q.shape[3]
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    out, workspace = _paged_out_ws(cache, q, max_kv_len, chunk, out, workspace)
+    L.check(L.lib().kvq_paged_append_decode_attend(
+        C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, q.data_ptr(),
+        _DTYPES[q.dtype], Hq, n_q, seq_lens.data_ptr(), max_kv_len, int(bool(causal)), float(attn_scale), chunk,
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "kvq_paged_append_decode_attend")
+    return out

@@ -69,6 +69,51 @@ kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
   v.zero[0] = static_cast<__half *>(c->k_zero);
   v.zero[1] = static_cast<__half *>(c->v_zero);
   v.ring[0] = c->k_recent; v.ring[1] = c->v_recent;
+  v.page_shift = -1; v.table_stride = 0; v.n_pages = 0; v.table = nullptr;
+  return KVQ_OK;
+}
+
+// Validation of a paged pool and its block table.
+kvq_status check_paged_cache(const kvq_paged_cache *c, kvq::CacheView &v) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (c->layout < KVQ_Q4_0 || c->layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
+  if (c->head_dim != 128 && c->head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", c->head_dim);
+  if (c->batch < 1 || c->n_kv_heads < 1 || c->n_pages < 1 || c->max_pages_per_seq < 1)
+    return fail(KVQ_EINVAL, "batch, n_kv_heads, n_pages and max_pages_per_seq must be >= 1");
+  int shift = -1;
+  for (int k = kvq::kMinPageShift; k <= 20; ++k)
+    if (c->page_size == (1 << k)) shift = k;
+  if (shift < 0) return fail(KVQ_ESHAPE, "page_size %d is not a power of two in [64, 2^20]", c->page_size);
+  if ((long long)c->max_pages_per_seq * c->page_size > INT_MAX)
+    return fail(KVQ_ECAPACITY, "max_pages_per_seq * page_size exceeds INT_MAX tokens");
+  if (c->n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
+  if (c->layout != KVQ_HAD_INT4 && c->n_recent != 0)
+    return fail(KVQ_EUNSUPPORTED, "n_recent is a Hadamard-int4 option");
+  const void *ptrs[] = {c->k_payload, c->v_payload, c->k_scale, c->v_scale, c->block_table};
+  for (const void *p : ptrs) {
+    if (!p) return fail(KVQ_EINVAL, "payload/scale/block_table pointer is NULL");
+    if (!aligned(p, 16)) return fail(KVQ_EALIGN, "payload/scale/block_table pointer not 16-byte aligned");
+  }
+  if (c->layout == KVQ_ASYM4_G32) {
+    if (!c->k_zero || !c->v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
+    if (!aligned(c->k_zero, 16) || !aligned(c->v_zero, 16)) return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
+  }
+  if (c->layout == KVQ_HAD_INT4 && c->n_recent > 0) {
+    if (!c->k_recent || !c->v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
+    if (!aligned(c->k_recent, 16) || !aligned(c->v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
+  }
+  v.layout = c->layout; v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim;
+  v.cap = c->max_pages_per_seq * c->page_size;
+  v.n_recent = c->layout == KVQ_HAD_INT4 ? c->n_recent : 0;
+  v.row_bytes = (int)row_bytes_of(c->layout, c->head_dim);
+  v.payload[0] = static_cast<uint8_t *>(c->k_payload);
+  v.payload[1] = static_cast<uint8_t *>(c->v_payload);
+  v.scale[0] = c->k_scale; v.scale[1] = c->v_scale;
+  v.zero[0] = static_cast<__half *>(c->k_zero);
+  v.zero[1] = static_cast<__half *>(c->v_zero);
+  v.ring[0] = c->k_recent; v.ring[1] = c->v_recent;
+  v.page_shift = shift; v.table_stride = c->max_pages_per_seq; v.n_pages = c->n_pages;
+  v.table = c->block_table;
   return KVQ_OK;
 }
 
@@ -138,18 +183,17 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
   return (int)chunk;
 }
 
-// Resolve the attention arguments and the workspace layout. When `ws` is NULL only sizes are
-// computed (returned through `need`).
-kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv_len, int causal, int q_pos0,
-                          int chunk, kvq::AttendArgs &a, size_t &need, void *ws) {
-  kvq_status st = check_cache(cache, a.cache);
-  if (st != KVQ_OK) return st;
+// Resolve the attention arguments and the workspace layout for a checked cache view `a.cache`
+// (kv_len: the call's length, or the largest per-sequence length of a paged call). When `ws` is
+// NULL only sizes are computed (returned through `need`).
+kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_pos0, bool paged, int chunk,
+                        kvq::AttendArgs &a, size_t &need, void *ws) {
   const kvq::CacheView &c = a.cache;
   if (n_q_heads < 1 || n_q < 1) return fail(KVQ_EINVAL, "n_q_heads and n_q must be >= 1");
   if (n_q_heads % c.H) return fail(KVQ_ESHAPE, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, c.H);
   if (kv_len < 1) return fail(KVQ_EINVAL, "kv_len must be >= 1");
   if (kv_len > c.cap) return fail(KVQ_ECAPACITY, "kv_len %d > capacity %d", kv_len, c.cap);
-  if (causal && (q_pos0 < 0 || (long long)q_pos0 + n_q > kv_len))
+  if (!paged && causal && (q_pos0 < 0 || (long long)q_pos0 + n_q > kv_len))
     return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
   if (chunk == 0)
     chunk = auto_chunk(c, (n_q_heads / c.H) * n_q,
@@ -167,6 +211,8 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
   a.win_in_reduce = 0;
   a.fresh_lo = 0;
   a.fresh_hi = INT_MAX;
+  a.seq_lens = nullptr;
+  a.fresh_tail = 0;
   const size_t rows = (size_t)c.B * n_q_heads * n_q;
   size_t off = 0;
   const size_t o_m = off; off = round_up(off + rows * a.C * sizeof(float), 256);
@@ -189,6 +235,21 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
     a.q_rot = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<float *>(w + o_qr) : nullptr;
   }
   return KVQ_OK;
+}
+
+kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv_len, int causal, int q_pos0,
+                          int chunk, kvq::AttendArgs &a, size_t &need, void *ws) {
+  kvq_status st = check_cache(cache, a.cache);
+  if (st != KVQ_OK) return st;
+  return resolve_core(n_q_heads, n_q, kv_len, causal, q_pos0, false, chunk, a, need, ws);
+}
+
+// Paged call: the grid is sized for max_kv_len; per-sequence lengths are read on the device.
+kvq_status resolve_paged(const kvq_paged_cache *cache, int n_q_heads, int n_q, int max_kv_len, int causal, int chunk,
+                         kvq::AttendArgs &a, size_t &need, void *ws) {
+  kvq_status st = check_paged_cache(cache, a.cache);
+  if (st != KVQ_OK) return st;
+  return resolve_core(n_q_heads, n_q, max_kv_len, causal, 0, true, chunk, a, need, ws);
 }
 
 }  // namespace
@@ -248,13 +309,9 @@ int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q,
 
 namespace {
 
-// Validation of an attention call and its workspace; on success `a` is fully resolved.
-kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
-                          int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
-                          float *out, void *workspace, size_t workspace_bytes, kvq::AttendArgs &a) {
-  size_t need = 0;
-  kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, nullptr);
-  if (st != KVQ_OK) return st;
+// The query, output, workspace and scale arguments of an attention call.
+kvq_status check_call(size_t need, const void *q, int32_t q_dtype, float attn_scale, const float *out,
+                      const void *workspace, size_t workspace_bytes) {
   if (q_dtype < KVQ_F32 || q_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown q dtype %d", q_dtype);
   if (!q || !out || !workspace) return fail(KVQ_EINVAL, "q/out/workspace is NULL");
   if (!aligned(q, 16) || !aligned(out, 16)) return fail(KVQ_EALIGN, "q/out not 16-byte aligned");
@@ -262,6 +319,18 @@ kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype
   if (workspace_bytes < need) return fail(KVQ_EWORKSPACE, "workspace %zu < required %zu", workspace_bytes, need);
   if (!(attn_scale == attn_scale) || attn_scale > 3.0e38f || attn_scale < -3.0e38f)
     return fail(KVQ_EINVAL, "attn_scale must be finite");
+  return KVQ_OK;
+}
+
+// Validation of an attention call and its workspace; on success `a` is fully resolved.
+kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                          int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                          float *out, void *workspace, size_t workspace_bytes, kvq::AttendArgs &a) {
+  size_t need = 0;
+  kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  st = check_call(need, q, q_dtype, attn_scale, out, workspace, workspace_bytes);
+  if (st != KVQ_OK) return st;
   resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, workspace);
   a.q = q;
   a.q_dtype = q_dtype;
@@ -279,6 +348,7 @@ cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool even
   if (a.cache.layout == KVQ_HAD_INT4 && !mma) {
     a.fresh_lo = 0;                                      // its predecessor is then the prep kernel
     a.fresh_hi = INT_MAX;
+    a.fresh_tail = 0;
     e = kvq::launch_had_prep(a, s);
   }
   const bool prof = events && g_ev_begin && g_ev_end;
@@ -327,6 +397,129 @@ kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, c
     e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, pos0, s);
     a.fresh_lo = pos0;                                   // the rows (and window slots) it writes
     a.fresh_hi = pos0 + n_new;
+  }
+  if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "append/attend launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+// ------------------------------------------------------------------ paged pool
+kvq_status kvq_paged_cache_bytes(int32_t layout, int32_t n_pages, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t page_size, int32_t batch, int32_t n_recent, size_t out_sizes[4]) {
+  g_last_error[0] = 0;
+  if (!out_sizes) return fail(KVQ_EINVAL, "out_sizes is NULL");
+  if (layout < KVQ_Q4_0 || layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", layout);
+  const size_t rb = row_bytes_of(layout, head_dim);
+  if (!rb) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", head_dim);
+  if (n_pages < 1 || n_kv_heads < 1 || page_size < 1 || batch < 1 || n_recent < 0) return fail(KVQ_EINVAL, "bad sizes");
+  const size_t rows = (size_t)n_pages * n_kv_heads * page_size;
+  const size_t nb = (size_t)head_dim / kvq::kBlock;
+  out_sizes[0] = rows * rb;
+  out_sizes[1] = layout == KVQ_HAD_INT4 ? rows * sizeof(float) : rows * nb * 2;
+  out_sizes[2] = layout == KVQ_ASYM4_G32 ? rows * nb * 2 : 0;
+  out_sizes[3] = layout == KVQ_HAD_INT4 ? (size_t)batch * n_kv_heads * n_recent * head_dim * sizeof(float) : 0;
+  return KVQ_OK;
+}
+
+namespace {
+
+kvq_status check_paged_store(const kvq_paged_cache *cache, const void *k_new, const void *v_new, int dtype, int n_new,
+                             const void *positions, kvq::CacheView &v) {
+  kvq_status st = check_paged_cache(cache, v);
+  if (st != KVQ_OK) return st;
+  if (dtype < KVQ_F32 || dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown dtype %d", dtype);
+  if (n_new < 0) return fail(KVQ_EINVAL, "n_new must be >= 0");
+  if (n_new > v.cap) return fail(KVQ_ECAPACITY, "n_new %d > sequence capacity %d", n_new, v.cap);
+  if (n_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !positions) return fail(KVQ_EINVAL, "k_new/v_new/positions is NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(positions, 16))
+    return fail(KVQ_EALIGN, "k_new/v_new/positions not 16-byte aligned");
+  return KVQ_OK;
+}
+
+kvq_status prepare_paged(const kvq_paged_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                         const int32_t *seq_lens, int32_t max_kv_len, int32_t causal, float attn_scale, int32_t chunk,
+                         float *out, void *workspace, size_t workspace_bytes, kvq::AttendArgs &a) {
+  size_t need = 0;
+  kvq_status st = resolve_paged(cache, n_q_heads, n_q, max_kv_len, causal, chunk, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  if (!seq_lens) return fail(KVQ_EINVAL, "seq_lens is NULL");
+  if (!aligned(seq_lens, 16)) return fail(KVQ_EALIGN, "seq_lens not 16-byte aligned");
+  st = check_call(need, q, q_dtype, attn_scale, out, workspace, workspace_bytes);
+  if (st != KVQ_OK) return st;
+  resolve_paged(cache, n_q_heads, n_q, max_kv_len, causal, chunk, a, need, workspace);
+  a.seq_lens = seq_lens;
+  a.q = q;
+  a.q_dtype = q_dtype;
+  a.scale = attn_scale;
+  a.out = out;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status kvq_paged_store(const kvq_paged_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
+                           int32_t n_new, const int32_t *positions, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::CacheView v;
+  kvq_status st = check_paged_store(cache, k_new, v_new, dtype, n_new, positions, v);
+  if (st != KVQ_OK || n_new == 0) return st;
+  cudaError_t e = kvq::launch_store(v, k_new, v_new, dtype, n_new, 0, reinterpret_cast<cudaStream_t>(stream),
+                                    positions, 0);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "store launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+size_t kvq_paged_attend_workspace_bytes(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q,
+                                        int32_t max_kv_len, int32_t chunk) {
+  kvq::AttendArgs a;
+  size_t need = 0;
+  if (resolve_paged(cache, n_q_heads, n_q, max_kv_len, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  return need;
+}
+
+int32_t kvq_paged_attend_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t max_kv_len,
+                               int32_t chunk) {
+  kvq::AttendArgs a;
+  size_t need = 0;
+  if (resolve_paged(cache, n_q_heads, n_q, max_kv_len, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  return a.chunk;
+}
+
+kvq_status kvq_paged_decode_attend(const kvq_paged_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads,
+                                   int32_t n_q, const int32_t *seq_lens, int32_t max_kv_len, int32_t causal,
+                                   float attn_scale, int32_t chunk, float *out, void *workspace,
+                                   size_t workspace_bytes, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  kvq_status st = prepare_paged(cache, q, q_dtype, n_q_heads, n_q, seq_lens, max_kv_len, causal, attn_scale, chunk,
+                                out, workspace, workspace_bytes, a);
+  if (st != KVQ_OK) return st;
+  cudaError_t e = launch_attend_sequence(a, reinterpret_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const void *k_new, const void *v_new,
+                                          int32_t kv_dtype, int32_t n_new, const void *q, int32_t q_dtype,
+                                          int32_t n_q_heads, int32_t n_q, const int32_t *seq_lens,
+                                          int32_t max_kv_len, int32_t causal, float attn_scale, int32_t chunk,
+                                          float *out, void *workspace, size_t workspace_bytes,
+                                          kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::CacheView v;
+  kvq_status st = check_paged_store(cache, k_new, v_new, kv_dtype, n_new, seq_lens, v);
+  if (st != KVQ_OK) return st;
+  kvq::AttendArgs a;
+  st = prepare_paged(cache, q, q_dtype, n_q_heads, n_q, seq_lens, max_kv_len, causal, attn_scale, chunk, out,
+                     workspace, workspace_bytes, a);
+  if (st != KVQ_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n_new > 0) {
+    // the new tokens end each sequence: positions seq_lens[b] - n_new + j
+    e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, 0, s, seq_lens, -n_new);
+    a.fresh_tail = n_new;                                 // the rows (and window slots) it writes
   }
   if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "append/attend launch: %s", cudaGetErrorString(e));

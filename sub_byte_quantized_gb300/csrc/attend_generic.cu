@@ -26,21 +26,16 @@ namespace {
 constexpr int kRowsPerCta = 8;       // one warp per query row
 constexpr int kThreads = kRowsPerCta * 32;
 
-// Absolute token range of chunk c: body chunks [c*chunk, min(n_body, (c+1)*chunk)), the window
-// chunk [n_body, kv_len).
-__device__ __forceinline__ void chunk_range(const AttendArgs &a, int c, int &t0, int &t1) {
+// Absolute token range of chunk c of a sequence: body chunks [c*chunk, min(n_body, (c+1)*chunk)),
+// the window chunk [n_body, kv_len).
+__device__ __forceinline__ void chunk_range(const AttendArgs &a, const SeqLen &sl, int c, int &t0, int &t1) {
   if (c < a.n_chunks) {
     t0 = c * a.chunk;
-    t1 = min(a.n_body, t0 + a.chunk);
+    t1 = min(sl.n_body, t0 + a.chunk);
   } else {
-    t0 = a.n_body;
-    t1 = a.kv_len;
+    t0 = sl.n_body;
+    t1 = sl.kv_len;
   }
-}
-
-// Last token row i may see.
-__device__ __forceinline__ int row_limit(const AttendArgs &a, int i) {
-  return a.causal ? min(a.kv_len - 1, a.q_pos0 + i) : a.kv_len - 1;
 }
 
 // Unpack 8 values (group gi of a token row) of a packed row into f32 (value = code * scale [+ zero]).
@@ -102,18 +97,19 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
   const int qi = row_ok ? r % a.n_q : 0;
   const size_t grow = ((size_t)b * a.Hq + hq) * a.n_q + qi;   // global query row
 
+  const SeqLen sl = seq_of(a, b);
   int t0, t1;
-  chunk_range(a, chunk_id, t0, t1);
+  chunk_range(a, sl, chunk_id, t0, t1);
   const bool is_win = chunk_id >= a.n_chunks;
   const bool had = c.layout == KVQ_HAD_INT4;
-  const int lim = row_ok ? row_limit(a, qi) : -1;
+  const int lim = row_ok ? row_limit(a, sl, qi) : -1;
   // Highest token any row of this CTA may see.
   int cta_lim = -1;
   for (int w = 0; w < kRowsPerCta; ++w) {
     const int rr = blockIdx.z * kRowsPerCta + w;
-    if (rr < R) cta_lim = max(cta_lim, row_limit(a, rr % a.n_q));
+    if (rr < R) cta_lim = max(cta_lim, row_limit(a, sl, rr % a.n_q));
   }
-  if (t0 > cta_lim) return;                  // no row sees this chunk: phase 2 skips it too
+  if (t0 > cta_lim || t0 >= t1) return;      // no row sees this chunk: phase 2 skips it too
   const int t_end = min(t1, cta_lim + 1);
 
   // Query row into shared memory: HAD body -> int8 codes; HAD window -> rotated f32; else q.
@@ -140,7 +136,6 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
 #pragma unroll
   for (int i = 0; i < VPL; ++i) o[i] = 0.0f;
 
-  const size_t head_row0 = (size_t)bh * c.cap;          // cache row of token 0
   for (int tb = t0; tb < t_end; tb += T) {
     const int nt = min(T, t_end - tb);
     __syncthreads();                                     // previous sub-tile fully consumed
@@ -158,9 +153,10 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
           const float4 x0 = *reinterpret_cast<const float4 *>(src), x1 = *reinterpret_cast<const float4 *>(src + 4);
           v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
         } else {
-          unpack8(c, kv, head_row0 + tok, gi, v);
+          const size_t crow = cache_row(c, b, kvh, tok);
+          unpack8(c, kv, crow, gi, v);
           if (had && gi == 0) {
-            const float s = static_cast<const float *>(c.scale[kv])[head_row0 + tok];
+            const float s = static_cast<const float *>(c.scale[kv])[crow];
             (kv ? vs : ks)[t] = s;
           }
         }

@@ -66,9 +66,9 @@ __host__ __device__ constexpr int smem_bytes() {
   return kWarps * 2 * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
 }
 
-__device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
-  const int qi = r % a.n_q;
-  return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+// Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
+__device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &sl, int r) {
+  return row_limit(a, sl, r % a.n_q);
 }
 
 // Byte offset of (row, 16-byte column j) inside a swizzled 64-byte-row slab.
@@ -76,7 +76,7 @@ __device__ __forceinline__ uint32_t swz(int row, int j) {
   return (uint32_t)(row * kRowBytes + ((j ^ ((row >> 1) & 3)) << 4));
 }
 
-template <int LAYOUT, bool QSPLIT>
+template <int LAYOUT, bool QSPLIT, bool PAGED>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
   constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = LAYOUT == KVQ_HAD_INT4;
   constexpr int SCB = scale_bytes<LAYOUT>(), OFF_SV = off_sv<LAYOUT>(), OFF_ZK = off_zk<LAYOUT>();
@@ -92,19 +92,20 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
   const int t0 = chunk_id * a.chunk;
-  const int t1 = min(a.n_body, t0 + a.chunk);
+  const int t1 = min(sl.n_body, t0 + a.chunk);
   int w_lim = -1, min_lim = INT_MAX;
   for (int r = 0; r < R; ++r) {
-    const int l = row_limit_of(a, r);
+    const int l = row_limit_of(a, sl, r);
     w_lim = max(w_lim, l);
     min_lim = min(min_lim, l);
   }
   // rows appended by the preceding kernel: only the CTAs that read them wait for it
-  pdl_wait_if(t0 <= w_lim && t0 < a.fresh_hi && a.fresh_lo < min(t1, w_lim + 1));
-  if (t0 > w_lim) return;                              // no row sees this chunk (phase 2 skips it)
+  pdl_wait_if(t0 <= w_lim && t0 < sl.fresh_hi && sl.fresh_lo < min(t1, w_lim + 1));
+  if (t0 > w_lim || t0 >= t1) return;                 // no row sees this chunk (phase 2 skips it)
   const int t_end = min(t1, w_lim + 1);
   const int n_stages = (t_end - t0 + kStage - 1) / kStage;
   const int spw = (n_stages + kWarps - 1) / kWarps;      // stages per warp
@@ -114,21 +115,35 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
 
   // ---- per-warp stage pipeline
   uint8_t *wbuf = smem + warp * 2 * STAGE_BYTES;
+  // contiguous cache: the planes' rows of token 0 of this (batch, kv head)
   const size_t head_row0 = (size_t)bh * cv.cap;
-  const uint8_t *kp = cv.payload[0] + head_row0 * kRowBytes;
-  const uint8_t *vp = cv.payload[1] + head_row0 * kRowBytes;
-  const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
-  const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
-  const __half *kz = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
-  const __half *vz = ASYM ? cv.zero[1] + head_row0 * 4 : nullptr;
+  const uint8_t *kp0 = cv.payload[0] + head_row0 * kRowBytes, *vp0 = cv.payload[1] + head_row0 * kRowBytes;
+  const uint8_t *ksc0 = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
+  const uint8_t *vsc0 = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
+  const __half *kz0 = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
+  const __half *vz0 = ASYM ? cv.zero[1] + head_row0 * 4 : nullptr;
 
   auto issue = [&](int i) {
     if (i < n_mine) {
       const int ts = tw0 + i * kStage;
+      // the stage's 64 rows are consecutive plane rows (a page holds at least 64 aligned tokens)
+      size_t r0 = (size_t)ts;                             // row offset from the base pointers
+      const uint8_t *kb = kp0, *vb = vp0, *ksb = ksc0, *vsb = vsc0;
+      const __half *kzb = kz0, *vzb = vz0;
+      if constexpr (PAGED) {
+        r0 = cache_row_paged(cv, bb, kvh, ts);
+        kb = cv.payload[0]; vb = cv.payload[1];
+        ksb = static_cast<const uint8_t *>(cv.scale[0]); vsb = static_cast<const uint8_t *>(cv.scale[1]);
+        kzb = cv.zero[0]; vzb = cv.zero[1];
+      }
+      const uint8_t *kp = kb + r0 * kRowBytes, *vp = vb + r0 * kRowBytes;
+      const uint8_t *ksc = ksb + r0 * SCB, *vsc = vsb + r0 * SCB;
+      const __half *kz = ASYM ? kzb + r0 * 4 : nullptr;
+      const __half *vz = ASYM ? vzb + r0 * 4 : nullptr;
       uint8_t *sb = wbuf + (i & 1) * STAGE_BYTES;
       const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
       if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
-        const uint8_t *kps = kp + (size_t)ts * kRowBytes, *vps = vp + (size_t)ts * kRowBytes;
+        const uint8_t *kps = kp, *vps = vp;
 #pragma unroll
         for (int k = 0; k < kStage / 8; ++k) {
           const int q = lane + 32 * k;                   // 16-byte piece: row q/4, column q%4
@@ -139,7 +154,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
 #pragma unroll
         for (int k = 0; k < kStage / 32; ++k) {
           const int row = lane + 32 * k;
-          const size_t tok = (size_t)(ts + row);
+          const size_t tok = (size_t)row;
           cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, SCB);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, SCB);
           if (ASYM) {
@@ -153,7 +168,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           const int q = lane + 32 * k;
           const int row = q >> 2, j = q & 3;
           const bool ok = ts + row < t_end;
-          const size_t off = (size_t)(ok ? ts + row : t0) * kRowBytes + 16 * j;
+          const size_t off = (size_t)(ok ? row : 0) * kRowBytes + 16 * j;
           cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
           cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
         }
@@ -161,7 +176,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         for (int k = 0; k < kStage / 32; ++k) {
           const int row = lane + 32 * k;
           const bool ok = ts + row < t_end;
-          const size_t tok = (size_t)(ok ? ts + row : t0);
+          const size_t tok = (size_t)(ok ? row : 0);
           cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, ok ? SCB : 0);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, ok ? SCB : 0);
           if (ASYM) {
@@ -297,11 +312,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       }
     }
   }
-  const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
-  const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
 
 
 
+
+  const int lim0 = r0 < R ? row_limit_of(a, sl, r0) : -1;
+  const int lim1 = r1 < R ? row_limit_of(a, sl, r1) : -1;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   float O[4][2][4];                                      // [block][half][c0..c3]
   // ASYM: Dw[b][r] = sum_t p_t * z_v[t][b] (the zero-point term), from a small extra mma per
@@ -613,7 +629,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   __syncthreads();
   const int d = threadIdx.x;                             // 128 threads <-> 128 dims
   for (int r = 0; r < R; ++r) {
-    if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
+    if (t0 > row_limit_of(a, sl, r)) continue;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, cm[w * 8 + r]);
@@ -634,7 +650,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   }
 }
 
-template <int LAYOUT, bool QSPLIT>
+template <int LAYOUT, bool QSPLIT, bool PAGED>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   static bool configured[kMaxDevices] = {};
   int dev = 0;
@@ -642,7 +658,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma_kernel<LAYOUT, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attend_mma_kernel<LAYOUT, QSPLIT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem_bytes<LAYOUT>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -657,7 +673,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, QSPLIT>, a);
+  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, QSPLIT, PAGED>, a);
 }
 
 }  // namespace
@@ -674,12 +690,15 @@ cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
   const bool split = a.q_dtype == KVQ_F32;
   if (prefill_supported(a)) return launch_attend_prefill(a, st);
   if (uses_mma4(a.cache.layout)) return launch_attend_mma4(a, st);
+  const bool paged = a.cache.page_shift >= 0;
   switch (a.cache.layout) {
     case KVQ_Q6_0: return launch_attend_mma_q6(a, st);
-    case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4, false>(a, st);   // int8 query codes are exact
-    case KVQ_ASYM4_G32:
-      return split ? launch_t<KVQ_ASYM4_G32, true>(a, st) : launch_t<KVQ_ASYM4_G32, false>(a, st);
-    default: return split ? launch_t<KVQ_Q4_0, true>(a, st) : launch_t<KVQ_Q4_0, false>(a, st);
+    case KVQ_HAD_INT4:                                   // int8 query codes are exact
+      return paged ? launch_t<KVQ_HAD_INT4, false, true>(a, st) : launch_t<KVQ_HAD_INT4, false, false>(a, st);
+    case KVQ_Q4_0:
+      if (split) return paged ? launch_t<KVQ_Q4_0, true, true>(a, st) : launch_t<KVQ_Q4_0, true, false>(a, st);
+      return paged ? launch_t<KVQ_Q4_0, false, true>(a, st) : launch_t<KVQ_Q4_0, false, false>(a, st);
+    default: return cudaErrorNotSupported;               // the asymmetric layout runs attend_mma4.cu
   }
 }
 

@@ -59,9 +59,9 @@ struct Geo4 {
   static_assert((64 + 32 * kD) * 4 <= OFF_X, "combine area (cm, cl, co) fits below the hand-off");
 };
 
-__device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
-  const int qi = r % a.n_q;
-  return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+// Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
+__device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &sl, int r) {
+  return row_limit(a, sl, r % a.n_q);
 }
 
 // Byte offset of (row, 16-byte column j) inside a swizzled 64-byte-row slab.
@@ -69,7 +69,7 @@ __device__ __forceinline__ uint32_t swz(int row, int j) {
   return (uint32_t)(row * kRowBytes + ((j ^ ((row >> 1) & 3)) << 4));
 }
 
-template <int LAYOUT, bool QSPLIT>
+template <int LAYOUT, bool QSPLIT, bool PAGED>
 __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(AttendArgs a) {
   using G = Geo4<LAYOUT>;
   constexpr bool ASYM = G::ASYM, HAD = G::HAD;
@@ -86,62 +86,80 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
   const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
   const int t0 = chunk_id * a.chunk;
-  const int t1 = min(a.n_body, t0 + a.chunk);
-  int w_lim = -1, min_lim = INT_MAX;
+  const int t1 = min(sl.n_body, t0 + a.chunk);
+  // the rows' limits, folded here so that nothing of the sequence's lengths stays live below:
+  // the widest and narrowest limit, this thread's two accumulator rows, and a mask of the rows
+  // that see this chunk
+  int w_lim = -1, min_lim = INT_MAX, lim0 = -1, lim1 = -1;
+  unsigned row_vis = 0u;
   for (int r = 0; r < R; ++r) {
-    const int l = row_limit_of(a, r);
+    const int l = row_limit_of(a, sl, r);
     w_lim = max(w_lim, l);
     min_lim = min(min_lim, l);
+    if (r == 2 * c) lim0 = l;
+    if (r == 2 * c + 1) lim1 = l;
+    if (t0 <= l) row_vis |= 1u << r;
   }
   // rows appended by the preceding kernel: only the CTAs that read them wait for it
-  pdl_wait_if(t0 <= w_lim && t0 < a.fresh_hi && a.fresh_lo < min(t1, w_lim + 1));
-  if (t0 > w_lim) return;                              // no row sees this chunk (phase 2 skips it)
+  pdl_wait_if(t0 <= w_lim && t0 < sl.fresh_hi && sl.fresh_lo < min(t1, w_lim + 1));
+  if (t0 > w_lim || t0 >= t1) return;                 // no row sees this chunk (phase 2 skips it)
   const int t_end = min(t1, w_lim + 1);
   const int n_stages = (t_end - t0 + kStage - 1) / kStage;
 
-  const size_t head_row0 = (size_t)bh * cv.cap;
-  const uint8_t *kp = cv.payload[0] + head_row0 * kRowBytes;
-  const uint8_t *vp = cv.payload[1] + head_row0 * kRowBytes;
-  const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
-  const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
-  const uint8_t *kz = ASYM ? reinterpret_cast<const uint8_t *>(cv.zero[0]) + head_row0 * 8 : nullptr;
-  const uint8_t *vz = ASYM ? reinterpret_cast<const uint8_t *>(cv.zero[1]) + head_row0 * 8 : nullptr;
-
-  // ---- CTA-wide copy of one plane's stage s into a ring slot: 256 16-byte payload pieces (one
-  // per thread), one scale per token (threads 0-63) and, in the same slot, the asymmetric
-  // zero-points or (K slot, Hadamard) the V scales (threads 64-127). Rows past t_end read as zero.
-  auto copy_stage = [&](const uint8_t *pl, const uint8_t *sc, const uint8_t *x2, uint8_t *slot, int s) {
+  // ---- CTA-wide copy of plane kvp's stage s into a ring slot: the payload in 16-byte pieces
+  // (iteration k of each thread covers rows 64k .. 64k+63), one scale per token (threads 0-127)
+  // and, in the same slot, the asymmetric zero-points or (K slot, Hadamard) the V scales (threads
+  // 128-255). Rows past t_end read as zero. Each 64-token half of the stage is a run of
+  // consecutive plane rows (a page holds at least 64 aligned tokens): one base row per half.
+  static_assert(kStage == 128 && kThreads == 256, "two 64-row halves, one payload piece per thread each");
+  const size_t head_row0 = (size_t)bh * cv.cap;           // contiguous cache: row of token 0
+  auto copy_stage = [&](int kvp, uint8_t *slot, int s) {
     const int ts = t0 + s * kStage;
     const uint32_t sd = smem_addr(slot);
+    const int row = threadIdx.x & (kStage - 1);          // scale / zero-point row of this thread
+    const bool second = threadIdx.x >= kStage;
+    const bool ok_row = ts + row < t_end;
+    size_t tok;                                          // plane row of that token (or a valid row)
+    if constexpr (!PAGED) {
+      const uint8_t *pl = cv.payload[kvp] + head_row0 * kRowBytes;
 #pragma unroll
-    for (int k = 0; k < kStage * kRowBytes / 16 / kThreads; ++k) {
-      const int q = threadIdx.x + kThreads * k, row = q >> 2, j = q & 3;
-      const bool ok = ts + row < t_end;
-      const size_t off = ok ? (size_t)ts * kRowBytes + 16 * q : (size_t)t0 * kRowBytes;
-      cp_async16(sd + swz(row, j), pl + off, ok ? 16 : 0);
-    }
-    if (threadIdx.x < 2 * kStage) {
-      const int row = threadIdx.x & (kStage - 1);
-      const bool second = threadIdx.x >= kStage;
-      const bool ok = ts + row < t_end;
-      const size_t tok = (size_t)(ok ? ts + row : t0);
-      if (!second) {
-        cp_async_scale<SCB>(sd + G::OFF_SC + row * SCB, sc + tok * SCB, ok ? SCB : 0);
-      } else if (x2 != nullptr && G::X2B == 8) {
-        cp_async8(sd + G::OFF_X2 + row * 8, x2 + tok * 8, ok ? 8 : 0);
-      } else if (x2 != nullptr && G::X2B == 4) {
-        cp_async4(sd + G::OFF_X2 + row * 4, x2 + tok * 4, ok ? 4 : 0);
+      for (int k = 0; k < 2; ++k) {
+        const int q = threadIdx.x + kThreads * k, r = q >> 2, j = q & 3;
+        const bool ok = ts + r < t_end;
+        const size_t off = ok ? (size_t)ts * kRowBytes + 16 * q : (size_t)t0 * kRowBytes;
+        cp_async16(sd + swz(r, j), pl + off, ok ? 16 : 0);
       }
+      tok = head_row0 + (size_t)(ok_row ? ts + row : t0);
+    } else {
+      const size_t rb0 = cache_row_paged(cv, bb, kvh, ts);
+      const size_t rb1 = ts + 64 < t_end ? cache_row_paged(cv, bb, kvh, ts + 64) : rb0;
+      const int rr = threadIdx.x >> 2, j = threadIdx.x & 3;   // row within a half, 16-byte column
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint8_t *src = cv.payload[kvp] + (k ? rb1 : rb0) * kRowBytes;
+        const bool ok = ts + 64 * k + rr < t_end;
+        cp_async16(sd + swz(64 * k + rr, j), src + (ok ? rr * kRowBytes + 16 * j : 0), ok ? 16 : 0);
+      }
+      tok = ok_row ? (row < 64 ? rb0 + row : rb1 + (row - 64)) : rb0;
+    }
+    if (!second) {
+      cp_async_scale<SCB>(sd + G::OFF_SC + row * SCB, static_cast<const uint8_t *>(cv.scale[kvp]) + tok * SCB,
+                          ok_row ? SCB : 0);
+    } else if (ASYM) {
+      cp_async8(sd + G::OFF_X2 + row * 8, reinterpret_cast<const uint8_t *>(cv.zero[kvp]) + tok * 8, ok_row ? 8 : 0);
+    } else if (HAD && kvp == 0) {
+      cp_async4(sd + G::OFF_X2 + row * 4, static_cast<const uint8_t *>(cv.scale[1]) + tok * 4, ok_row ? 4 : 0);
     }
   };
   // one commit group per call: K of stage s and V of stage s - 1
   auto issue = [&](int s) {
-    if (s < n_stages) copy_stage(kp, ksc, ASYM ? kz : vsc, smem + (s % kRing) * G::SLOT, s);
+    if (s < n_stages) copy_stage(0, smem + (s % kRing) * G::SLOT, s);
     if (s >= 1 && s - 1 < n_stages)      // V slot: the asymmetric zero-points only (Hadamard s_v rides with K)
-      copy_stage(vp, vsc, ASYM ? vz : nullptr, smem + G::OFF_V + ((s - 1) % kRing) * G::SLOT, s - 1);
+      copy_stage(1, smem + G::OFF_V + ((s - 1) % kRing) * G::SLOT, s - 1);
     cp_async_commit();
   };
   issue(0);
@@ -264,8 +282,6 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
         zq1[b] *= -8.0f;
       }
     }
-    const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
-    const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
     const int mi = lane >> 3;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
 
@@ -566,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
   const float *cl = cm + 32;
   const float *co = cm + 64;
   for (int r = 0; r < R; ++r) {
-    if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
+    if (!((row_vis >> r) & 1u)) continue;                // row does not see this chunk
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 8 + r]);
@@ -592,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
   }
 }
 
-template <int LAYOUT, bool QSPLIT>
+template <int LAYOUT, bool QSPLIT, bool PAGED>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   static bool configured[kMaxDevices] = {};
   int dev = 0;
@@ -600,7 +616,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma4_kernel<LAYOUT, QSPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attend_mma4_kernel<LAYOUT, QSPLIT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Geo4<LAYOUT>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
@@ -615,19 +631,17 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_mma4_kernel<LAYOUT, QSPLIT>, a);
+  return cudaLaunchKernelEx(&cfg, attend_mma4_kernel<LAYOUT, QSPLIT, PAGED>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_attend_mma4(const AttendArgs &a, cudaStream_t st) {
   const bool split = a.q_dtype == KVQ_F32;
-  switch (a.cache.layout) {
-    case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4, false>(a, st);   // int8 query codes are exact
-    case KVQ_ASYM4_G32:
-      return split ? launch_t<KVQ_ASYM4_G32, true>(a, st) : launch_t<KVQ_ASYM4_G32, false>(a, st);
-    default: return split ? launch_t<KVQ_Q4_0, true>(a, st) : launch_t<KVQ_Q4_0, false>(a, st);
-  }
+  const bool paged = a.cache.page_shift >= 0;
+  if (a.cache.layout != KVQ_ASYM4_G32) return cudaErrorNotSupported;   // built for the layout that uses it
+  if (split) return paged ? launch_t<KVQ_ASYM4_G32, true, true>(a, st) : launch_t<KVQ_ASYM4_G32, true, false>(a, st);
+  return paged ? launch_t<KVQ_ASYM4_G32, false, true>(a, st) : launch_t<KVQ_ASYM4_G32, false, false>(a, st);
 }
 
 }  // namespace kvq

@@ -75,14 +75,14 @@ __device__ __forceinline__ void unpack6(uint32_t w, uint32_t h, uint32_t (&o)[4]
   o[3] = lop3<0xEC>(w8, (hx << 2) & 0x03000300u, 0x00F000F0u);
 }
 
-__device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
-  const int qi = r % a.n_q;
-  return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+// Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
+__device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &sl, int r) {
+  return row_limit(a, sl, r % a.n_q);
 }
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_kernel(AttendArgs a) {
   using G = Geom<D>;
   constexpr int NB = G::NB;
@@ -98,36 +98,42 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
   const int t0 = chunk_id * a.chunk;
-  const int t1 = min(a.n_body, t0 + a.chunk);
-  int w_lim = -1, min_lim = INT_MAX;
+  const int t1 = min(sl.n_body, t0 + a.chunk);
+  // the rows' limits, folded here so that nothing of the sequence's lengths stays live below:
+  // the widest and narrowest limit, this thread's two accumulator rows, and a mask of the rows
+  // that see this chunk
+  int w_lim = -1, min_lim = INT_MAX, lim0 = -1, lim1 = -1;
+  unsigned row_vis = 0u;
   for (int r = 0; r < R; ++r) {
-    const int l = row_limit_of(a, r);
+    const int l = row_limit_of(a, sl, r);
     w_lim = max(w_lim, l);
     min_lim = min(min_lim, l);
+    if (r == 2 * (c & 1)) lim0 = l;
+    if (r == 2 * (c & 1) + 1) lim1 = l;
+    if (t0 <= l) row_vis |= 1u << r;
   }
   // rows appended by the preceding kernel: only the CTAs that read them wait for it
-  pdl_wait_if(t0 <= w_lim && t0 < a.fresh_hi && a.fresh_lo < min(t1, w_lim + 1));
-  if (t0 > w_lim) return;                              // no row sees this chunk (phase 2 skips it)
+  pdl_wait_if(t0 <= w_lim && t0 < sl.fresh_hi && sl.fresh_lo < min(t1, w_lim + 1));
+  if (t0 > w_lim || t0 >= t1) return;                 // no row sees this chunk (phase 2 skips it)
   const int t_end = min(t1, w_lim + 1);
   const int n_stages = (t_end - t0 + kStage - 1) / kStage;
 
-  const size_t head_row0 = (size_t)bh * cv.cap;
-  const uint8_t *kp = cv.payload[0] + head_row0 * G::RB;
-  const uint8_t *vp = cv.payload[1] + head_row0 * G::RB;
-  const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * G::SB;
-  const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * G::SB;
-
-  // ---- copy of one plane's stage s into a ring slot: the stage's rows are contiguous in the
-  // cache; 16-byte piece q goes to row q / (RB/16) of the padded slot. Rows past t_end are
-  // zero-filled.
-  auto copy_stage = [&](const uint8_t *pl, const uint8_t *sc, uint8_t *slot, int s) {
+  // ---- copy of plane kvp's stage s into a ring slot: the stage's rows are consecutive plane
+  // rows (a page holds at least 64 aligned tokens); 16-byte piece q goes to row q / (RB/16) of the
+  // padded slot. Rows past t_end are zero-filled.
+  const size_t head_row0 = (size_t)bh * cv.cap;           // contiguous cache: row of token 0
+  auto copy_stage = [&](int kvp, uint8_t *slot, int s) {
     const int ts = t0 + s * kStage;
+    const size_t r0 = cache_row_t<PAGED>(cv, bb, kvh, head_row0, ts);
+    const uint8_t *pl = cv.payload[kvp] + r0 * G::RB;
+    const uint8_t *sc = static_cast<const uint8_t *>(cv.scale[kvp]) + r0 * G::SB;
     const uint32_t sd = smem_addr(slot);
     if (ts + kStage <= t_end) {                          // full stage: no per-row bounds
-      const uint8_t *src = pl + (size_t)ts * G::RB;
+      const uint8_t *src = pl;
 #pragma unroll
       for (int j = 0; j < (G::PIECES + kThreads - 1) / kThreads; ++j) {
         const int q = threadIdx.x + kThreads * j;
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
         if (q < G::PIECES) {
           const int row = q / (G::RB / 16), pc = q - row * (G::RB / 16);
           const bool ok = ts + row < t_end;
-          const size_t off = ok ? (size_t)ts * G::RB + 16 * q : (size_t)t0 * G::RB;
+          const size_t off = ok ? (size_t)16 * q : 0;
           cp_async16(sd + row * G::PITCH + 16 * pc, pl + off, ok ? 16 : 0);
         }
       }
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
     if (threadIdx.x < kStage) {
       const int row = threadIdx.x;
       const bool ok = ts + row < t_end;
-      const uint8_t *src = sc + (size_t)(ok ? ts + row : t0) * G::SB;
+      const uint8_t *src = sc + (size_t)(ok ? row : 0) * G::SB;
       const uint32_t dst = sd + G::OFF_SC + row * G::SB;
       if (G::SB == 16) cp_async16(dst, src, ok ? 16 : 0);
       else cp_async8(dst, src, ok ? 8 : 0);
@@ -159,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   };
   // one commit group per call: K of stage s and V of stage s - 1
   auto issue = [&](int s) {
-    if (s < n_stages) copy_stage(kp, ksc, smem + (s % kRing) * G::SLOT, s);
-    if (s >= 1 && s - 1 < n_stages) copy_stage(vp, vsc, smem + G::OFF_V + ((s - 1) % kRing) * G::SLOT, s - 1);
+    if (s < n_stages) copy_stage(0, smem + (s % kRing) * G::SLOT, s);
+    if (s >= 1 && s - 1 < n_stages) copy_stage(1, smem + G::OFF_V + ((s - 1) % kRing) * G::SLOT, s - 1);
     cp_async_commit();
   };
   issue(0);
@@ -240,8 +246,6 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
         zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * zf;
       }
     }
-    const int lim0 = r0 < R ? row_limit_of(a, r0) : -1;
-    const int lim1 = r1 < R ? row_limit_of(a, r1) : -1;
     // bytes 2c, 2c+1 of a block's eight high bytes -> bytes 0 and 2
     const uint32_t sel_k = (uint32_t)(2 * c) | ((uint32_t)(2 * c + 1) << 8);
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   const float *cl = cm + 16;
   const float *co = cm + 32;
   for (int r = 0; r < R; ++r) {
-    if (t0 > row_limit_of(a, r)) continue;               // row does not see this chunk
+    if (!((row_vis >> r) & 1u)) continue;                // row does not see this chunk
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < 4; ++w) M = fmaxf(M, cm[w * 4 + r]);
@@ -497,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   }
 }
 
-template <int D>
+template <int D, bool PAGED>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   static bool configured[kMaxDevices] = {};
   int dev = 0;
@@ -505,7 +509,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma_q6_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geom<D>::SMEM);
+    e = cudaFuncSetAttribute(attend_mma_q6_kernel<D, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geom<D>::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -519,7 +523,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_mma_q6_kernel<D>, a);
+  return cudaLaunchKernelEx(&cfg, attend_mma_q6_kernel<D, PAGED>, a);
 }
 
 }  // namespace
@@ -530,7 +534,8 @@ bool mma_q6_supported(const AttendArgs &a) {
 }
 
 cudaError_t launch_attend_mma_q6(const AttendArgs &a, cudaStream_t st) {
-  return a.cache.D == 256 ? launch_t<256>(a, st) : launch_t<128>(a, st);
+  if (a.cache.page_shift >= 0) return a.cache.D == 256 ? launch_t<256, true>(a, st) : launch_t<128, true>(a, st);
+  return a.cache.D == 256 ? launch_t<256, false>(a, st) : launch_t<128, false>(a, st);
 }
 
 }  // namespace kvq

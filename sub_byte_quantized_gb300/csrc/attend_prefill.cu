@@ -92,12 +92,12 @@ __device__ __forceinline__ uint32_t toff(int row, int chunk) {
   return (uint32_t)(row * kTileRow + (((chunk & 8) | ((chunk ^ (row & 7) ^ ((chunk >> 3) << 1)) & 7)) << 4));
 }
 
-__device__ __forceinline__ int row_limit_of(const AttendArgs &a, int r) {
-  const int qi = r % a.n_q;
-  return a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
+// Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
+__device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &sl, int r) {
+  return row_limit(a, sl, r % a.n_q);
 }
 
-template <int LAYOUT>
+template <int LAYOUT, bool PAGED>
 __global__ void __launch_bounds__(kWarps * 32, PGeo<LAYOUT>::CTAS) attend_prefill_kernel(AttendArgs a) {
   using G = PGeo<LAYOUT>;
   constexpr bool HAD = G::HAD, ASYM = G::ASYM;
@@ -113,29 +113,24 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<LAYOUT>::CTAS) attend_prefil
   const int chunk_id = blockIdx.y;
   const int bh = blockIdx.z;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
   const bool win = HAD && chunk_id == a.n_chunks;     // the recent-window chunk
-  const int t0 = win ? a.n_body : chunk_id * a.chunk;
-  const int t1 = win ? a.kv_len : min(a.n_body, t0 + a.chunk);
+  const int t0 = win ? sl.n_body : chunk_id * a.chunk;
+  const int t1 = win ? sl.kv_len : min(sl.n_body, t0 + a.chunk);
   int w_lim = -1;
-  for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit_of(a, r));
+  for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit_of(a, sl, r));
   // rows appended by the preceding kernel (cache rows or window ring): only the CTAs that read
   // them wait for it
-  pdl_wait_if(t0 <= w_lim && t0 < a.fresh_hi && a.fresh_lo < min(t1, w_lim + 1));
-  if (t0 > w_lim) return;                              // no row of this CTA sees the chunk
+  pdl_wait_if(t0 <= w_lim && t0 < sl.fresh_hi && sl.fresh_lo < min(t1, w_lim + 1));
+  if (t0 > w_lim || t0 >= t1) return;                 // no row of this CTA sees the chunk
   const int t_end = min(t1, w_lim + 1);
   const int stage_len = win ? kWinStage : kStage;
   const int n_stages = (t_end - t0 + stage_len - 1) / stage_len;
 
-  const size_t head_row0 = (size_t)bh * cv.cap;
-  const uint8_t *kp = cv.payload[0] + head_row0 * kRowBytes;
-  const uint8_t *vp = cv.payload[1] + head_row0 * kRowBytes;
-  const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
-  const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
-  const uint8_t *kz = ASYM ? reinterpret_cast<const uint8_t *>(cv.zero[0]) + head_row0 * 8 : nullptr;
-  const uint8_t *vz = ASYM ? reinterpret_cast<const uint8_t *>(cv.zero[1]) + head_row0 * 8 : nullptr;
 
+  const size_t head_row0 = (size_t)bh * cv.cap;           // contiguous cache: row of token 0
   // ---- CTA-wide copy of stage s into ring slot s % 3; rows past t_end are zero-filled.
   // Body: 256 16-byte pieces per packed plane (two per thread), one token's scales per thread (and
   // zero-points). Window: 8 f32 K and V rows from ring slot t mod n_recent.
@@ -156,19 +151,26 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<LAYOUT>::CTAS) attend_prefil
         }
       } else {
         const int ts = t0 + s * kStage;
+        // the stage's 64 rows are consecutive plane rows (a page holds at least 64 aligned tokens)
+        const size_t r0 = cache_row_t<PAGED>(cv, bb, kvh, head_row0, ts);
+        const uint8_t *kp = cv.payload[0] + r0 * kRowBytes, *vp = cv.payload[1] + r0 * kRowBytes;
+        const uint8_t *ksc = static_cast<const uint8_t *>(cv.scale[0]) + r0 * SCB;
+        const uint8_t *vsc = static_cast<const uint8_t *>(cv.scale[1]) + r0 * SCB;
+        const uint8_t *kz = ASYM ? reinterpret_cast<const uint8_t *>(cv.zero[0]) + r0 * 8 : nullptr;
+        const uint8_t *vz = ASYM ? reinterpret_cast<const uint8_t *>(cv.zero[1]) + r0 * 8 : nullptr;
         const bool full = ts + kStage <= t_end;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
           const int q = threadIdx.x + 128 * k;          // piece: row q / 4, 16-byte column q % 4
           const int row = q >> 2;
           const bool ok = full || ts + row < t_end;
-          const size_t off = ok ? (size_t)ts * kRowBytes + 16 * q : (size_t)t0 * kRowBytes;
+          const size_t off = ok ? (size_t)16 * q : 0;
           cp_async16(smem_addr(sb + 16 * q), kp + off, ok ? 16 : 0);
           cp_async16(smem_addr(sb + G::OFF_V + 16 * q), vp + off, ok ? 16 : 0);
         }
         const int kv = threadIdx.x >> 6, row = threadIdx.x & 63;   // one token's scales per thread
         const bool ok = ts + row < t_end;
-        const size_t tok = (size_t)(ok ? ts + row : t0);
+        const size_t tok = (size_t)(ok ? row : 0);
         cp_async_scale<SCB>(smem_addr(sb + (kv ? G::OFF_SV : G::OFF_SK) + SCB * row), (kv ? vsc : ksc) + tok * SCB,
                             ok ? SCB : 0);
         if (ASYM) cp_async8(smem_addr(sb + (kv ? G::OFF_ZV : G::OFF_ZK) + 8 * row), (kv ? vz : kz) + tok * 8, ok ? 8 : 0);
@@ -228,8 +230,8 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<LAYOUT>::CTAS) attend_prefil
   }
   __syncwarp();
   const int rg = row0 + 16 * warp + g, rg8 = rg + 8;
-  const int lim_g = rg < R ? row_limit_of(a, rg) : -1;
-  const int lim_g8 = rg8 < R ? row_limit_of(a, rg8) : -1;
+  const int lim_g = rg < R ? row_limit_of(a, sl, rg) : -1;
+  const int lim_g8 = rg8 < R ? row_limit_of(a, sl, rg8) : -1;
   int warp_lim = max(lim_g, lim_g8), warp_min = INT_MAX;
   if (lim_g >= 0) warp_min = lim_g;
   if (lim_g8 >= 0) warp_min = min(warp_min, lim_g8);
@@ -661,7 +663,7 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<LAYOUT>::CTAS) attend_prefil
   }
 }
 
-template <int LAYOUT>
+template <int LAYOUT, bool PAGED>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   using G = PGeo<LAYOUT>;
   static bool configured[kMaxDevices] = {};
@@ -670,7 +672,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_prefill_kernel<LAYOUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+    e = cudaFuncSetAttribute(attend_prefill_kernel<LAYOUT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -686,7 +688,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_prefill_kernel<LAYOUT>, a);
+  return cudaLaunchKernelEx(&cfg, attend_prefill_kernel<LAYOUT, PAGED>, a);
 }
 
 }  // namespace
@@ -698,10 +700,11 @@ bool prefill_supported(const AttendArgs &a) {
 }
 
 cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st) {
+  const bool paged = a.cache.page_shift >= 0;
   switch (a.cache.layout) {
-    case KVQ_HAD_INT4: return launch_t<KVQ_HAD_INT4>(a, st);
-    case KVQ_ASYM4_G32: return launch_t<KVQ_ASYM4_G32>(a, st);
-    default: return launch_t<KVQ_Q4_0>(a, st);
+    case KVQ_HAD_INT4: return paged ? launch_t<KVQ_HAD_INT4, true>(a, st) : launch_t<KVQ_HAD_INT4, false>(a, st);
+    case KVQ_ASYM4_G32: return paged ? launch_t<KVQ_ASYM4_G32, true>(a, st) : launch_t<KVQ_ASYM4_G32, false>(a, st);
+    default: return paged ? launch_t<KVQ_Q4_0, true>(a, st) : launch_t<KVQ_Q4_0, false>(a, st);
   }
 }
 

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the C ABI).
 #pragma once
 
+#include <climits>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -42,7 +43,10 @@ __host__ __device__ constexpr bool prefill_shape(int layout, int D, int rows) {
          D == 128 && rows > 8;
 }
 
-// Device-side view of a cache; index 0 = K, 1 = V.
+// Device-side view of a cache; index 0 = K, 1 = V. Rows of the payload / scale / zero planes:
+// contiguous [B][H][cap] (page_shift < 0), or a paged pool [n_pages][H][page] addressed through
+// the block table [B][table_stride] (page = 1 << page_shift tokens, at least 64; cap is then the
+// logical capacity of one sequence, table_stride pages). The ring is per sequence either way.
 struct CacheView {
   int layout, B, H, D, cap, n_recent;
   int row_bytes;
@@ -50,7 +54,29 @@ struct CacheView {
   void *scale[2];
   __half *zero[2];
   float *ring[2];
+  int page_shift, table_stride, n_pages;
+  const int32_t *table;
 };
+constexpr int kMinPageShift = 6;    // pages of at least 64 tokens: a 64-token stage never straddles two
+
+// Plane row of token t of (batch bb, kv head kvh). A table entry outside the pool is clamped into
+// it (the caller guarantees valid entries; the clamp only keeps every access inside the pool).
+__device__ __forceinline__ size_t cache_row_paged(const CacheView &c, int bb, int kvh, int t) {
+  int pg = __ldg(c.table + (size_t)bb * c.table_stride + (t >> c.page_shift));
+  pg = min(max(pg, 0), c.n_pages - 1);
+  return (((size_t)pg * c.H + kvh) << c.page_shift) + (t & ((1 << c.page_shift) - 1));
+}
+__device__ __forceinline__ size_t cache_row(const CacheView &c, int bb, int kvh, int t) {
+  if (c.page_shift < 0) return ((size_t)bb * c.H + kvh) * c.cap + t;
+  return cache_row_paged(c, bb, kvh, t);
+}
+// The same with the layout fixed at compile time (the streaming kernels are built for both):
+// contiguous rows are head_row0 + t with head_row0 = (bb * H + kvh) * cap.
+template <bool PAGED>
+__device__ __forceinline__ size_t cache_row_t(const CacheView &c, int bb, int kvh, size_t head_row0, int t) {
+  if constexpr (PAGED) return cache_row_paged(c, bb, kvh, t);
+  else return head_row0 + t;
+}
 
 // Arguments of one decode-attention call, resolved on the host.
 struct AttendArgs {
@@ -68,6 +94,13 @@ struct AttendArgs {
   // append in the same call): only phase-1 CTAs that read them, and the first CTA, wait for it.
   // [0, INT_MAX) when the preceding kernel is unknown (every CTA waits).
   int fresh_lo, fresh_hi;
+  // Per-sequence lengths (paged calls): seq_lens [B] on the device, each clamped into
+  // [0, kv_len]; kv_len, n_win, n_body and the chunk counts are then the maxima the grid is sized
+  // for, causal rows are the sequence's newest n_q tokens (q_pos0 = length - n_q), and
+  // fresh_tail > 0 marks the newest fresh_tail tokens of every sequence as just appended.
+  // seq_lens == nullptr: every sequence has kv_len tokens.
+  const int32_t *seq_lens;
+  int fresh_tail;
   float *out;
   // workspace regions
   float *part_m, *part_l, *part_o;   // [rows][C], [rows][C], [rows][C][D]
@@ -76,8 +109,11 @@ struct AttendArgs {
 };
 
 // Launchers (return cudaGetLastError() after enqueueing).
+// Append n_new rows per (batch, kv head) at positions pos0 + j, or (seq_pos != nullptr) at the
+// per-sequence positions seq_pos[b] + pos_offset + j; rows outside [0, cap) are not written.
 cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype,
-                         int n_new, int pos0, cudaStream_t st);
+                         int n_new, int pos0, cudaStream_t st, const int32_t *seq_pos = nullptr,
+                         int pos_offset = 0);
 cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st);
 cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st);
 cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl);
@@ -108,6 +144,54 @@ __device__ __forceinline__ void pdl_wait_if(bool reads_fresh) {
 #endif
 }
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// The lengths of sequence bb that a kernel works with.
+struct SeqLen {
+  int kv_len, n_body, q_pos0, fresh_lo, fresh_hi;
+};
+__device__ __forceinline__ SeqLen seq_of(const AttendArgs &a, int bb) {
+  SeqLen s;
+  if (a.seq_lens == nullptr) {
+    s.kv_len = a.kv_len;
+    s.n_body = a.n_body;
+    s.q_pos0 = a.q_pos0;
+    s.fresh_lo = a.fresh_lo;
+    s.fresh_hi = a.fresh_hi;
+    return s;
+  }
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  // unless the preceding kernel is this call's own append (which does not write the lengths),
+  // the lengths may come from it: wait for it before reading them
+  if (a.fresh_tail == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+  const int L = min(max(__ldg(a.seq_lens + bb), 0), a.kv_len);
+  s.kv_len = L;
+  s.n_body = L - min(a.cache.n_recent, L);
+  s.q_pos0 = L - a.n_q;
+  s.fresh_lo = a.fresh_tail > 0 ? L - a.fresh_tail : 0;
+  s.fresh_hi = a.fresh_tail > 0 ? L : INT_MAX;
+  return s;
+}
+// The same for a kernel built for one cache kind: paged calls always pass per-sequence lengths,
+// contiguous calls never do, so a contiguous instantiation reads the call's values directly.
+template <bool PAGED>
+__device__ __forceinline__ SeqLen seq_of_t(const AttendArgs &a, int bb) {
+  if constexpr (PAGED) {
+    return seq_of(a, bb);
+  } else {
+    SeqLen s;
+    s.kv_len = a.kv_len;
+    s.n_body = a.n_body;
+    s.q_pos0 = a.q_pos0;
+    s.fresh_lo = a.fresh_lo;
+    s.fresh_hi = a.fresh_hi;
+    return s;
+  }
+}
+// Last token query row i (of n_q) of the sequence may see; negative when it sees none.
+__device__ __forceinline__ int row_limit(const AttendArgs &a, const SeqLen &s, int qi) {
+  return a.causal ? min(s.kv_len - 1, s.q_pos0 + qi) : s.kv_len - 1;
+}
 
 // Load 8 consecutive input elements starting at element index `e` (8-aligned) as f32.
 __device__ __forceinline__ void load8_f32(const void *base, int dtype, size_t e, float v[8]) {

@@ -33,9 +33,11 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   const int qi = (int)(row % a.n_q);
   const int d0 = HAD ? 0 : blockIdx.y * 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int lim = a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
-  const int n_vis_body = min(a.n_chunks, lim / a.chunk + 1);
-  const bool win_vis = a.n_win > 0 && a.n_body <= lim;
+  const SeqLen sl = seq_of(a, a.seq_lens ? (int)(row / ((size_t)a.Hq * a.n_q)) : 0);
+  const int lim = row_limit(a, sl, qi);                  // negative: the row sees nothing
+  const int n_chunks = a.seq_lens ? (sl.n_body + a.chunk - 1) / a.chunk : a.n_chunks;
+  const int n_vis_body = lim < 0 ? 0 : min(n_chunks, lim / a.chunk + 1);
+  const bool win_vis = sl.kv_len > sl.n_body && sl.n_body <= lim;
   const float *pm = a.part_m + row * a.C;
   const float *pl = a.part_l + row * a.C;
   const float *po = a.part_o + row * a.C * (size_t)D;
@@ -68,11 +70,11 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
 #pragma unroll
     for (int i = 0; i < QS; ++i) qs[i] = sm_q[(lane & 3) * QS + i];
     const int tl = lane >> 2;                             // this lane's token within the warp's eight
-    const int n_w = a.kv_len - a.n_body;
+    const int n_w = sl.kv_len - sl.n_body;
     for (int g0 = 0; g0 < n_w; g0 += 8 * kWarps) {
-      const int t = a.n_body + g0 + 8 * warp + tl;        // this lane's token
-      const bool tv = t < a.kv_len && t <= lim;
-      const size_t slot = (bh * cv.n_recent + (size_t)((tv ? t : a.n_body) % cv.n_recent)) * D;
+      const int t = sl.n_body + g0 + 8 * warp + tl;        // this lane's token
+      const bool tv = t < sl.kv_len && t <= lim;
+      const size_t slot = (bh * cv.n_recent + (size_t)((tv ? t : sl.n_body) % cv.n_recent)) * D;
       const float *kr = cv.ring[0] + slot + (lane & 3) * QS;
       float dot = 0.0f;
 #pragma unroll
@@ -104,8 +106,8 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
       float4 vv[8][VPL / 4];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int tu = a.n_body + g0 + 8 * warp + u;
-        const int ts = tu < a.kv_len ? tu : a.n_body;
+        const int tu = sl.n_body + g0 + 8 * warp + u;
+        const int ts = tu < sl.kv_len ? tu : sl.n_body;
         const float *vr = cv.ring[1] + (bh * cv.n_recent + (size_t)(ts % cv.n_recent)) * D + lane * VPL;
 #pragma unroll
         for (int i = 0; i < VPL / 4; ++i) vv[u][i] = *reinterpret_cast<const float4 *>(vr + 4 * i);
@@ -201,9 +203,11 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
   const size_t row = (size_t)blockIdx.x * kWarps + warp;
   if (row >= rows) return;
   const int qi = (int)(row % a.n_q);
-  const int lim = a.causal ? min(a.kv_len - 1, a.q_pos0 + qi) : a.kv_len - 1;
-  const int n_vis_body = min(a.n_chunks, lim / a.chunk + 1);
-  const bool win_vis = a.n_win > 0 && a.n_body <= lim;
+  const SeqLen sl = seq_of(a, a.seq_lens ? (int)(row / ((size_t)a.Hq * a.n_q)) : 0);
+  const int lim = row_limit(a, sl, qi);                  // negative: the row sees nothing
+  const int n_chunks = a.seq_lens ? (sl.n_body + a.chunk - 1) / a.chunk : a.n_chunks;
+  const int n_vis_body = lim < 0 ? 0 : min(n_chunks, lim / a.chunk + 1);
+  const bool win_vis = sl.kv_len > sl.n_body && sl.n_body <= lim;
   const float *pm = a.part_m + row * a.C;
   const float *pl = a.part_l + row * a.C;
   const float *po = a.part_o + row * a.C * (size_t)D + lane * VPL;

@@ -18,17 +18,26 @@ constexpr float kF16Max = 65504.0f;
 struct StoreGeom {
   int B, H, D, cap, n_new, pos0, row_bytes, nb;
   long long rows_per_tensor;   // B * H * n_new
+  // per-sequence first position seq_pos[b] + pos_offset (device), or nullptr: pos0 for every one
+  const int32_t *seq_pos;
+  int pos_offset;
 };
 
-// Decompose a global row id into (tensor, input row offset, cache row).
-__device__ __forceinline__ void row_coords(const StoreGeom &g, long long r, int &kv, long long &in_row,
-                                           long long &cache_row, int &j) {
+// Decompose a global row id into (tensor, input row, plane row, row j of the append, position,
+// batch * H + head). False when the position is outside [0, cap): a per-sequence position the
+// host could not check; such a row is computed but not written.
+__device__ __forceinline__ bool row_coords(const CacheView &c, const StoreGeom &g, long long r, int &kv,
+                                           long long &in_row, long long &crow, int &j, int &pos, long long &bh) {
   kv = r >= g.rows_per_tensor ? 1 : 0;
   const long long rr = r - (long long)kv * g.rows_per_tensor;
-  const long long bh = rr / g.n_new;
+  bh = rr / g.n_new;
   j = (int)(rr - bh * g.n_new);
   in_row = rr;
-  cache_row = bh * g.cap + g.pos0 + j;
+  const int bb = (int)(bh / g.H), kvh = (int)(bh - (long long)bb * g.H);
+  pos = (g.seq_pos ? __ldg(g.seq_pos + bb) + g.pos_offset : g.pos0) + j;
+  const bool ok = pos >= 0 && pos < g.cap;
+  crow = ok ? (long long)cache_row(c, bb, kvh, pos) : 0;
+  return ok;
 }
 
 __device__ __forceinline__ float quad_max(float v) {
@@ -65,16 +74,16 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
   const int tr = (int)(gt - r * tpr);                      // thread within row
   // Threads past the last row still take part in the quad shuffles (full-warp masks) but load
   // and store nothing.
-  const bool valid = r < 2 * g.rows_per_tensor;
-  int kv = 0, j = 0;
-  long long in_row = 0, cache_row = 0;
-  if (valid) row_coords(g, r, kv, in_row, cache_row, j);
+  bool valid = r < 2 * g.rows_per_tensor;
+  int kv = 0, j = 0, pos = 0;
+  long long in_row = 0, crow = 0, bh = 0;
+  if (valid) valid = row_coords(c, g, r, kv, in_row, crow, j, pos, bh);
   const int blk = tr >> 2, lb = tr & 3;
 
   float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (valid) load8_f32(kv ? v_new : k_new, dtype, (size_t)in_row * g.D + (size_t)tr * 8, v);
-  uint8_t *prow = c.payload[kv] + (size_t)cache_row * g.row_bytes;
-  __half *srow = static_cast<__half *>(c.scale[kv]) + (size_t)cache_row * g.nb;
+  uint8_t *prow = c.payload[kv] + (size_t)crow * g.row_bytes;
+  __half *srow = static_cast<__half *>(c.scale[kv]) + (size_t)crow * g.nb;
 
   if (LAYOUT == KVQ_ASYM4_G32) {
     float mn = v[0], mx = v[0];
@@ -99,7 +108,7 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
     *reinterpret_cast<uint32_t *>(prow + blk * 16 + lb * 4) = w;
     if (lb == 0) {
       srow[blk] = sh;
-      c.zero[kv][(size_t)cache_row * g.nb + blk] = zh;
+      c.zero[kv][(size_t)crow * g.nb + blk] = zh;
     }
     return;
   }
@@ -146,9 +155,9 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
   const int lane = threadIdx.x & 31;
   const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (r >= 2 * g.rows_per_tensor) return;                  // whole warp exits together
-  int kv, j;
-  long long in_row, cache_row;
-  row_coords(g, r, kv, in_row, cache_row, j);
+  int kv, j, pos;
+  long long in_row, crow, bh;
+  if (!row_coords(c, g, r, kv, in_row, crow, j, pos, bh)) return;   // whole warp (one row)
   float x[V];
   const void *src = kv ? v_new : k_new;
   if (V == 4) {
@@ -170,18 +179,17 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
   uint32_t w = 0;
 #pragma unroll
   for (int i = 0; i < V; ++i) w |= ((uint32_t)sym_code(x[i], s, -7, 7) & 0xFu) << (4 * i);
-  uint8_t *prow = c.payload[kv] + (size_t)cache_row * g.row_bytes;
+  uint8_t *prow = c.payload[kv] + (size_t)crow * g.row_bytes;
   if (V == 4) {
     *reinterpret_cast<uint16_t *>(prow + lane * 2) = (uint16_t)w;
   } else {
     *reinterpret_cast<uint32_t *>(prow + lane * 4) = w;
   }
-  if (lane == 0) static_cast<float *>(c.scale[kv])[cache_row] = s;
+  if (lane == 0) static_cast<float *>(c.scale[kv])[crow] = s;
   // Exact-f32 ring of the newest tokens: only the last min(n_new, n_recent) rows of this call,
   // so no two rows of one call write the same slot.
   if (c.n_recent > 0 && j >= g.n_new - c.n_recent) {
-    const long long bh = cache_row / g.cap;
-    float *dst = c.ring[kv] + ((size_t)bh * c.n_recent + (size_t)((g.pos0 + j) % c.n_recent)) * g.D + lane * V;
+    float *dst = c.ring[kv] + ((size_t)bh * c.n_recent + (size_t)(pos % c.n_recent)) * g.D + lane * V;
 #pragma unroll
     for (int i = 0; i < V; i += 4)
       *reinterpret_cast<float4 *>(dst + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
@@ -191,9 +199,10 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
 }  // namespace
 
 cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype, int n_new,
-                         int pos0, cudaStream_t st) {
+                         int pos0, cudaStream_t st, const int32_t *seq_pos, int pos_offset) {
   StoreGeom g;
   g.B = c.B; g.H = c.H; g.D = c.D; g.cap = c.cap; g.n_new = n_new; g.pos0 = pos0;
+  g.seq_pos = seq_pos; g.pos_offset = pos_offset;
   g.row_bytes = c.row_bytes; g.nb = c.D / kBlock;
   g.rows_per_tensor = (long long)c.B * c.H * n_new;
   const long long rows = 2 * g.rows_per_tensor;

@@ -125,3 +125,54 @@ def test_auto_chunk_is_a_multiple_of_64():
         # the automatic chunk equals one of the explicit multiples of 64
         sizes = {Lb.kvq_attend_workspace_bytes(C.byref(c), 8, 1, kv_len, ch) for ch in range(64, 8193, 64)}
         assert auto in sizes
+
+
+def _paged(layout=0, D=128, page=64, n_pages=8, mpp=4, ptr=4096, table=4096, n_recent=0):
+    from sub_byte_quantized_gb300._lib import KvqPagedCache
+    return KvqPagedCache(layout, 2, 2, D, page, n_pages, mpp, n_recent, ptr, ptr, ptr, ptr, ptr, ptr, None, None, table)
+
+
+def test_paged_sizes(L):
+    out = (C.c_size_t * 4)()
+    assert L.kvq_paged_cache_bytes(0, 10, 8, 128, 64, 4, 0, out) == 0
+    assert out[0] == 10 * 8 * 64 * 64 and out[1] == 10 * 8 * 64 * 8 and out[2] == 0 and out[3] == 0
+    assert L.kvq_paged_cache_bytes(2, 10, 8, 128, 64, 4, 16, out) == 0
+    assert out[1] == 10 * 8 * 64 * 4 and out[3] == 4 * 8 * 16 * 128 * 4
+    assert L.kvq_paged_cache_bytes(3, 3, 2, 256, 128, 1, 0, out) == 0 and out[2] == 3 * 2 * 128 * 8 * 2
+    assert L.kvq_paged_cache_bytes(9, 3, 2, 128, 64, 1, 0, out) == 1
+
+
+def test_paged_validation_without_device(L):
+    p = C.byref
+    ws = 1 << 20
+    # store: page size not a power of two / below 64, NULL table, misaligned table or positions
+    for page in (48, 32, 96):
+        assert L.kvq_paged_store(p(_paged(page=page)), 16, 16, 1, 1, 16, None) == 2
+    assert L.kvq_paged_store(p(_paged(table=None)), 16, 16, 1, 1, 16, None) == 1
+    assert L.kvq_paged_store(p(_paged(table=4100)), 16, 16, 1, 1, 16, None) == 5
+    assert L.kvq_paged_store(p(_paged()), 16, 16, 1, 1, 20, None) == 5
+    assert L.kvq_paged_store(p(_paged()), 16, 16, 1, 1, None, None) == 1
+    assert L.kvq_paged_store(p(_paged(n_pages=0)), 16, 16, 1, 1, 16, None) == 1
+    # more new rows than a sequence holds (4 pages x 64)
+    assert L.kvq_paged_store(p(_paged()), 16, 16, 1, 257, 16, None) == 3
+    assert L.kvq_paged_store(p(_paged()), None, None, 1, 0, None, None) == 0
+    # n_recent on a non-Hadamard layout
+    assert L.kvq_paged_store(p(_paged(n_recent=8)), 16, 16, 1, 1, 16, None) == 4
+    # attention: max_kv_len 0 / beyond the sequence capacity, NULL or misaligned seq_lens, workspace
+    c = _paged()
+    assert L.kvq_paged_decode_attend(p(c), 16, 1, 8, 1, 16, 0, 0, 1.0, 0, 16, 256, ws, None) == 1
+    assert L.kvq_paged_decode_attend(p(c), 16, 1, 8, 1, 16, 257, 0, 1.0, 0, 16, 256, ws, None) == 3
+    assert L.kvq_paged_decode_attend(p(c), 16, 1, 8, 1, None, 64, 0, 1.0, 0, 16, 256, ws, None) == 1
+    assert L.kvq_paged_decode_attend(p(c), 16, 1, 8, 1, 20, 64, 0, 1.0, 0, 16, 256, ws, None) == 5
+    assert L.kvq_paged_decode_attend(p(c), 16, 1, 8, 1, 16, 64, 0, 1.0, 0, 16, 256, 16, None) == 7
+    assert L.kvq_paged_decode_attend(p(c), 16, 1, 7, 1, 16, 64, 0, 1.0, 0, 16, 256, ws, None) == 2
+    # the combined call validates both parts first
+    assert L.kvq_paged_append_decode_attend(p(c), 17, 16, 1, 1, 16, 1, 8, 1, 16, 64, 0, 1.0, 0, 16, 256, ws,
+                                            None) == 5
+    assert L.kvq_paged_append_decode_attend(p(c), 16, 16, 1, 1, 16, 1, 8, 1, 16, 64, 0, 1.0, 0, 16, 256, 16,
+                                            None) == 7
+    # workspace: the contiguous formula at max_kv_len (rows = 2 sequences x 8 heads, 2 chunks)
+    rows, Cc = 16, 2
+    assert L.kvq_paged_attend_workspace_bytes(p(c), 8, 1, 256, 128) == \
+        2 * ((rows * Cc * 4 + 255) // 256 * 256) + (rows * Cc * 128 * 4 + 255) // 256 * 256
+    assert L.kvq_paged_attend_chunk(p(c), 8, 1, 256, 128) == 128
