@@ -64,6 +64,9 @@ DESCRIPTIONS = {
                              "x10, N(0,1) Q), B1 Hq64 Hkv8 D128",
     "c5_asym4_g32_llama70b_128k": "Llama-3.1-70B layer, 128K context, per-group asymmetric int4 g=32 KV, "
                                   "B1 Hq64 Hkv8 D128",
+    "paged_q4_0_llama3_8b_ragged": "Paged Q4_0 pool, Llama-3-8B layer shapes (Hq32 Hkv8 D128): 16 sequences with seeded "
+                                   "lengths 1024-16384 (116139 tokens), 64-token pages shuffled in the pool; append 1 "
+                                   "token per sequence then attend over each sequence's own length",
 }
 
 
@@ -244,13 +247,47 @@ def oracle_step(w, inp, n_heads: int, kv_len: int | None = None):
     return step
 
 
+def paged_oracle_step(w, inp, n_heads: int, frac: float = 1.0):
+    """The paged workload's oracle step over its first `n_heads` kv heads (and the first `frac` of
+    every sequence): an oracle paged pool filled (untimed) with all but each sequence's last token;
+    the step stores that token of every sequence and runs the paged oracle attention. Returns
+    (step, packed bytes the step's attention reads)."""
+    from oracle.paged import OraclePagedCache
+    lens = np.maximum((inp["seq_lens"] * frac).astype(np.int64), 2)
+    B, P = w.batch, w.page_size
+    mpp = -(-int(lens.max()) // P)
+    table = np.arange(B * mpp).reshape(B, mpp)
+    pc = OraclePagedCache(w.layout, B, n_heads, w.head_dim, P, B * mpp, mpp, w.n_recent, table=table)
+    D = w.head_dim
+    k_all, v_all = inp["k"][:n_heads], inp["v"][:n_heads]
+    pad = np.zeros((B, n_heads, int(lens.max()), D), np.float32)
+    kp, vp = pad.copy(), pad.copy()
+    for b in range(B):
+        o, L = int(inp["offsets"][b]), int(lens[b])
+        kp[b, :, :L] = k_all[:, o:o + L]
+        vp[b, :, :L] = v_all[:, o:o + L]
+    pc.store(kp[:, :, :-1], vp[:, :, :-1], np.zeros(B, np.int64))
+    k_new = np.stack([kp[b, :, lens[b] - 1:lens[b]] for b in range(B)])
+    v_new = np.stack([vp[b, :, lens[b] - 1:lens[b]] for b in range(B)])
+    q = inp["q"][:, :n_heads * w.gqa]
+
+    def step():
+        pc.store(k_new, v_new, lens - 1)
+        return pc.attend(q, w.alpha, lens, causal=False)
+    row = {"q4_0": 18, "q6_0": 26, "asym4_g32": 20, "had_int4": 0}[w.layout] * (D // 32) if w.layout != "had_int4" \
+        else D // 2 + 4
+    return step, 2 * n_heads * int(lens.sum()) * row
+
+
 def _oracle_all_cores_child(wname: str, budget_s: float, conn) -> None:
     """Spawned child: the same oracle step as cpu_baseline, with the BLAS threads of this process
     set to every host core by the parent (numpy loads after the environment is set)."""
-    from synth import WORKLOADS, make_inputs
+    from synth import WORKLOADS, make_inputs, make_paged_inputs
     w = WORKLOADS[wname]
-    inp = make_inputs(w)
-    step = oracle_step(w, inp, 1)
+    if w.page_size:
+        step = paged_oracle_step(w, make_paged_inputs(w), 1)[0]
+    else:
+        step = oracle_step(w, make_inputs(w), 1)
     times = []
     t_all = time.perf_counter()
     while not times or (time.perf_counter() - t_all < budget_s and len(times) < 20):
@@ -316,6 +353,8 @@ def run_reference(args):
         return
     from synth import WORKLOADS, make_inputs
     w = WORKLOADS[args.workload]
+    if w.page_size:
+        return run_reference_paged(args, w)
     inp = make_inputs(w)
     spec = Spec(w, inp)
     # bound the run: each step is one kv head over a prefix of the tokens, sized so that the
@@ -350,11 +389,47 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_paged(args, w):
+    """Reference arm of a paged workload: the paged oracle over one kv head and a prefix of every
+    sequence, sized so that the W + K steps take about two minutes."""
+    from synth import make_paged_inputs
+    inp = make_paged_inputs(w)
+    full_bytes = 2 * w.n_kv_heads * int(inp["seq_lens"].sum()) * 18 * (w.head_dim // 32)
+    probe, _ = paged_oracle_step(w, inp, 1, 0.1)
+    t0 = time.perf_counter()
+    probe()
+    t_probe = time.perf_counter() - t0
+    frac = min(1.0, 0.1 * (120.0 / max(1, args.steps + args.warmup)) / max(t_probe, 1e-6))
+    step, bytes_per = paged_oracle_step(w, inp, 1, frac)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = bytes_per * args.steps / el / 1e9
+    sample = (f"paged CPU oracle (numpy, one thread): per step, the store of each sequence's new token + float64 "
+              f"attention of 1 of {w.n_kv_heads} kv heads over {frac:.3f} of every sequence ({bytes_per:.0f} packed "
+              f"bytes of {full_bytes} for the whole layer)")
+    line = {"impl": "reference", "metric": f"paged {w.layout} KV attention µs/layer and effective HBM GB/s "
+                                           f"({args.workload})",
+            "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESCRIPTIONS[args.workload], "layout": w.layout, "sampled_fraction": frac},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ GPU arm
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    from synth import WORKLOADS
+    if WORKLOADS[args.workload].page_size:
+        return paged_main(args)
     import torch
     import torch.distributed as dist
 
@@ -628,6 +703,224 @@ def variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1, n
     res["asym4_g32"] = {"us_per_layer": a_ms * 1e3, "read_bytes_per_step": a_bytes,
                         "gbs": a_bytes / (a_ms / 1e3) / 1e9, "timing": "stream launches", "chunk": achunk}
     return res
+
+
+def paged_main(args):
+    """GPU arm of a paged workload: the same protocol as main() (graph of K library steps, phase-1
+    events in a second pass, clocks, e2e through the public API, CPU oracle baseline)."""
+    import torch
+    import torch.distributed as dist
+
+    import sub_byte_quantized_gb300 as kvq
+    from sub_byte_quantized_gb300 import _lib
+    from synth import WORKLOADS, make_paged_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = WORKLOADS[args.workload]
+    inp = make_paged_inputs(w)
+    lens = inp["seq_lens"]
+    B, H, D, P, Hq = w.batch, w.n_kv_heads, w.head_dim, w.page_size, w.n_q_heads
+    S_max, total = int(lens.max()), int(lens.sum())
+    mpp = -(-S_max // P)
+    n_pages = B * mpp
+
+    def bits(name):
+        return torch.from_numpy(np.ascontiguousarray(inp[name + "_bits"]).view(np.int16)).view(torch.bfloat16)
+
+    kf, vf, q = bits("k"), bits("v"), bits("q").to(dev)
+    # every sequence's tokens padded to S_max ([B][H][S_max][D] on the device) for the bulk fill;
+    # the new token of a step is each sequence's last one
+    kp = torch.zeros((B, H, S_max, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.zeros_like(kp)
+    for b in range(B):
+        o, L = int(inp["offsets"][b]), int(lens[b])
+        kp[b, :, :L] = kf[:, o:o + L].to(dev)
+        vp[b, :, :L] = vf[:, o:o + L].to(dev)
+    idx = torch.from_numpy(lens - 1).to(dev)
+    k_new = torch.stack([kp[b, :, int(lens[b]) - 1:int(lens[b])] for b in range(B)]).contiguous()
+    v_new = torch.stack([vp[b, :, int(lens[b]) - 1:int(lens[b])] for b in range(B)]).contiguous()
+    lens_dev = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    row = 18 * (D // 32)
+    read_bytes = 2 * H * total * row
+    flops = 4 * D * total * (Hq // H) * H
+
+    def make_pool(seed):
+        c = kvq.PagedKVCache(w.layout, B, H, D, P, n_pages, mpp, device=dev)
+        c.set_block_table(np.random.default_rng(seed).permutation(n_pages).reshape(B, mpp))
+        kvq.paged_store(c, kp[:, :, :S_max - 1].contiguous(), vp[:, :, :S_max - 1].contiguous(),
+                        torch.zeros(B, dtype=torch.int32, device=dev))
+        return c
+    n_rep = min(64, max(2, math.ceil(3 * L2_BYTES / read_bytes) + 1))
+    pools = [make_pool(w.seed + r) for r in range(n_rep)]
+    del kp, vp
+    torch.cuda.empty_cache()
+    chunk = kvq.paged_attend_chunk(pools[0], Hq, 1, S_max, total)
+    chunk_max = kvq.paged_attend_chunk(pools[0], Hq, 1, S_max, 0)
+    ws = torch.empty(max(256, kvq.paged_attend_workspace_bytes(pools[0], Hq, 1, S_max, chunk)), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((B, Hq, 1, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    L = _lib.lib()
+
+    def step(i, ev=None, c_chunk=None):
+        if ev is not None:
+            L.kvq_profile_phase1_events(ev[0].cuda_event, ev[1].cuda_event)
+        kvq.paged_append_decode_attend(pools[i % n_rep], k_new, v_new, q, lens_dev, S_max, attn_scale=w.alpha,
+                                       chunk=c_chunk or chunk, out=out, workspace=ws, stream=stream)
+        if ev is not None:
+            L.kvq_profile_phase1_events(None, None)
+
+    K, W = args.steps, args.warmup
+    ph_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for a, b in ph_ev:
+            a.record(stream)
+            b.record(stream)
+        for i in range(max(W, 3)):
+            step(i)
+    torch.cuda.synchronize(dev)
+    graph, ev_graph, soak_graph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(K):
+            step(i)
+    with torch.cuda.graph(ev_graph, stream=stream):
+        for i in range(K):
+            step(i, ph_ev[i])
+    with torch.cuda.graph(soak_graph, stream=stream):
+        for i in range(16):
+            step(i)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_end = time.perf_counter() + args.soak_s
+        with torch.cuda.stream(stream):
+            while time.perf_counter() < t_end:
+                soak_graph.replay()
+                torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        elapsed_ms = ev0.elapsed_time(ev1)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            ev_graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        ev_pass_ms = ev0.elapsed_time(ev1)
+        time.sleep(0.25)
+    elapsed_ms = max_over_ranks(elapsed_ms, dist if world > 1 else None, dev)
+    ph_ms = [a.elapsed_time(b) for a, b in ph_ev]
+    ph_mean = statistics.fmean(ph_ms)
+    ms_step = elapsed_ms / K
+    value = aggregate(world, read_bytes, K, elapsed_ms) / 1e9
+    hbm_peak, _, peak_kind = measured_peaks()
+    achieved = read_bytes / (ph_mean / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+            "peak_kind": peak_kind, "traffic": None, "kernel": "attend phase 1 (split-K chunk partials), paged",
+            "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
+            "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3, "phase1_pass_us_per_step": ev_pass_ms / K * 1e3}
+    line = {
+        "metric": f"paged {w.layout} KV attention µs/layer and effective HBM GB/s ({args.workload})",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "us_per_layer": ms_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload, "layout": w.layout,
+                   "sequences": B, "seq_lens": [int(x) for x in lens], "total_tokens": total, "page_size": P,
+                   "pool_pages": n_pages, "chunk": chunk, "chunk_rule": "kvq_paged_attend_chunk with the batch's "
+                   f"total length (max-length rule: {chunk_max})",
+                   "step": "append 1 token per sequence (K,V) + split-K attention over each sequence's length, "
+                           "one library call",
+                   "read_bytes_per_step": read_bytes, "flops_per_step": flops,
+                   "l2": f"inputs larger than L2: {n_rep} pools rotated ({n_rep * read_bytes / 2**20:.0f} MiB read)",
+                   "timing": "CUDA graph of the K library steps; phase 1 timed by events in a second pass",
+                   "soak_s": args.soak_s, "parallelism": f"replicas x{world}"},
+        "pct_of_peak": value / world / hbm_peak,
+        "roofline": roof,
+        "clocks": clk.summary(),
+        "gpu_launches": 3 * K,
+    }
+    if not args.quick and rank == 0:
+        # the max-length chunk rule on the same batch (stream launches)
+        ws_m = torch.empty(max(256, kvq.paged_attend_workspace_bytes(pools[0], Hq, 1, S_max, chunk_max)),
+                           dtype=torch.uint8, device=dev)
+
+        def plain(ch, wsb, n=200):
+            with torch.cuda.stream(stream):
+                for i in range(5):
+                    kvq.paged_append_decode_attend(pools[i % n_rep], k_new, v_new, q, lens_dev, S_max,
+                                                   attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb, stream=stream)
+                ev0.record(stream)
+                for i in range(n):
+                    kvq.paged_append_decode_attend(pools[i % n_rep], k_new, v_new, q, lens_dev, S_max,
+                                                   attn_scale=w.alpha, chunk=ch, out=out, workspace=wsb, stream=stream)
+                ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            return ev0.elapsed_time(ev1) / n
+        t_tot, t_max = plain(chunk, ws), plain(chunk_max, ws_m)
+        line["variants"] = {"total_length_chunk": {"chunk": chunk, "us_per_layer": t_tot * 1e3,
+                                                   "timing": "stream launches"},
+                            "max_length_chunk": {"chunk": chunk_max, "us_per_layer": t_max * 1e3,
+                                                 "gbs": read_bytes / (t_max / 1e3) / 1e9, "timing": "stream launches"}}
+        # end to end through the public API: new tokens, queries and the sequence lengths from pinned host
+        # memory, the output back, one sync per step
+        hk, hv, hq = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q.cpu().pin_memory()
+        hl = lens_dev.cpu().pin_memory()
+        hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+        dk, dv, dq, dl = (torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q),
+                          torch.empty_like(lens_dev))
+        n_e2e = min(K, 500)
+        for i in range(n_e2e + 3):
+            if i == 3:
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                dq.copy_(hq, non_blocking=True)
+                dl.copy_(hl, non_blocking=True)
+                kvq.paged_append_decode_attend(pools[i % n_rep], dk, dv, dq, dl, S_max, attn_scale=w.alpha,
+                                               chunk=chunk, out=out, workspace=ws, stream=stream)
+                hout.copy_(out, non_blocking=True)
+            stream.synchronize()
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+        el = hk.element_size()
+        line["e2e"] = {"value": read_bytes / t_e2e / 1e9, "unit": "GB/s",
+                       "h2d_bytes_per_step": (hk.numel() + hv.numel() + hq.numel()) * el + hl.numel() * 4,
+                       "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e}
+        if world == 1:
+            step_o, per = paged_oracle_step(w, inp, 1)
+            times = []
+            t_all = time.perf_counter()
+            while not times or (time.perf_counter() - t_all < args.cpu_seconds and len(times) < 20):
+                t0 = time.perf_counter()
+                step_o()
+                times.append(time.perf_counter() - t0)
+            tm = statistics.median(times)
+            line["cpu_baseline"] = {"value": per / tm / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"paged oracle (numpy, one thread): the store of every sequence's new "
+                                              f"token + float64 attention of 1 of {H} kv heads over all {B} "
+                                              f"sequences; median of {len(times)} runs of {tm * 1e3:.0f} ms, "
+                                              f"{per} packed bytes each"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

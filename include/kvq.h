@@ -232,12 +232,17 @@ kvq_status kvq_paged_cache_bytes(int32_t layout, int32_t n_pages, int32_t n_kv_h
 kvq_status kvq_paged_store(const kvq_paged_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
                            int32_t n_new, const int32_t *positions, kvq_stream_t stream);
 
-/* Workspace bytes / resolved chunk of kvq_paged_decode_attend for these arguments (0 on invalid
- * arguments). max_kv_len as there. */
+/* Workspace bytes of kvq_paged_decode_attend for these arguments (0 on invalid arguments).
+ * max_kv_len as there. */
 size_t kvq_paged_attend_workspace_bytes(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q,
                                         int32_t max_kv_len, int32_t chunk);
+/* The chunk kvq_paged_decode_attend uses: `chunk` itself when non-zero and valid; for chunk 0, the
+ * automatic choice. total_kv_len = the sum of the batch's sequence lengths, known to the caller's
+ * scheduler on the host; 0 means "every sequence at max_kv_len". A ragged batch gets a better
+ * balanced chunk from its true total: pass the returned value as `chunk` to the attend call (and
+ * to kvq_paged_attend_workspace_bytes). 0 on invalid arguments. */
 int32_t kvq_paged_attend_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t max_kv_len,
-                               int32_t chunk);
+                               int64_t total_kv_len, int32_t chunk);
 
 /*
  * kvq_decode_attend over a paged cache with per-sequence lengths.

@@ -89,7 +89,8 @@ def lib() -> C.CDLL:
     L.kvq_paged_store.argtypes, L.kvq_paged_store.restype = [paged_p, P, P, I32, I32, P, P], I32
     L.kvq_paged_attend_workspace_bytes.argtypes = [paged_p, I32, I32, I32, I32]
     L.kvq_paged_attend_workspace_bytes.restype = SZ
-    L.kvq_paged_attend_chunk.argtypes, L.kvq_paged_attend_chunk.restype = [paged_p, I32, I32, I32, I32], I32
+    L.kvq_paged_attend_chunk.argtypes = [paged_p, I32, I32, I32, C.c_int64, I32]
+    L.kvq_paged_attend_chunk.restype = I32
     L.kvq_paged_decode_attend.argtypes = [paged_p, P, I32, I32, I32, P, I32, I32, C.c_float, I32, P, P, SZ, P]
     L.kvq_paged_decode_attend.restype = I32
     L.kvq_paged_append_decode_attend.argtypes = [paged_p, P, P, I32, I32, P, I32, I32, I32, P, I32, I32, C.c_float,

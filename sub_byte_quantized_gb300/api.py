@@ -310,8 +310,12 @@ def paged_attend_workspace_bytes(cache: PagedKVCache, n_q_heads: int, n_q: int, 
     return int(L.lib().kvq_paged_attend_workspace_bytes(C.byref(cache.struct), n_q_heads, n_q, max_kv_len, chunk))
 
 
-def paged_attend_chunk(cache: PagedKVCache, n_q_heads: int, n_q: int, max_kv_len: int, chunk: int = 0) -> int:
-    return int(L.lib().kvq_paged_attend_chunk(C.byref(cache.struct), n_q_heads, n_q, max_kv_len, chunk))
+def paged_attend_chunk(cache: PagedKVCache, n_q_heads: int, n_q: int, max_kv_len: int, total_kv_len: int = 0,
+                       chunk: int = 0) -> int:
+    """The split-K chunk of a paged call (0 -> automatic); total_kv_len = the sum of the sequence
+    lengths (0: every sequence at max_kv_len) balances a ragged batch."""
+    return int(L.lib().kvq_paged_attend_chunk(C.byref(cache.struct), n_q_heads, n_q, max_kv_len, total_kv_len,
+                                              chunk))
 
 
 def _paged_out_ws(cache, q, max_kv_len, chunk, out, workspace):

@@ -150,10 +150,13 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
 // tokens that gives one slice to every resident warp (four warps per chunk); for the
 // warp-specialised kernels (Q6_0, asymmetric) the smallest multiple of 64 that gives one chunk to
 // every resident CTA. Many rows (Hadamard prefill): about four waves of 64-row CTAs.
-int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
+// `work` = body tokens summed over every (batch, kv head) (0: n_body for each of them); a ragged
+// batch passes its true total so the chunk fits the work that exists.
+int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long long work = 0) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long work = (long long)(n_body > 0 ? n_body : 1) * n_heads;
+  const bool total_given = work > 0;
+  if (!total_given) work = (long long)(n_body > 0 ? n_body : 1) * n_heads;
   long long chunk;
   if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
     const long long ctas = (long long)sms * kvq::kMmaQ6CtasPerSm(c.D);
@@ -165,7 +168,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
     const long long want = 4LL * sms * kvq::kPrefillCtasPerSm;
     long long n_chunks = (want + row_ctas - 1) / row_ctas;
     if (n_chunks < 1) n_chunks = 1;
-    const long long body = n_body > 0 ? n_body : 1;
+    const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
     chunk = ((body + n_chunks - 1) / n_chunks + 63) / 64 * 64;
   } else if (kvq::uses_mma4(c.layout)) {
     // warp-specialised 4-bit kernel: one chunk per resident CTA, as many chunks per (batch, kv
@@ -173,7 +176,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
     const long long ctas = (long long)sms * kvq::kMma4CtasPerSm;
     long long per_head = ctas / (n_heads > 0 ? n_heads : 1);
     if (per_head < 1) per_head = 1;
-    const long long body = n_body > 0 ? n_body : 1;
+    const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
     chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
   } else {
     const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
@@ -187,7 +190,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads) {
 // (kv_len: the call's length, or the largest per-sequence length of a paged call). When `ws` is
 // NULL only sizes are computed (returned through `need`).
 kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_pos0, bool paged, int chunk,
-                        kvq::AttendArgs &a, size_t &need, void *ws) {
+                        kvq::AttendArgs &a, size_t &need, void *ws, long long work = 0) {
   const kvq::CacheView &c = a.cache;
   if (n_q_heads < 1 || n_q < 1) return fail(KVQ_EINVAL, "n_q_heads and n_q must be >= 1");
   if (n_q_heads % c.H) return fail(KVQ_ESHAPE, "n_q_heads %d not a multiple of n_kv_heads %d", n_q_heads, c.H);
@@ -197,7 +200,8 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
     return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
   if (chunk == 0)
     chunk = auto_chunk(c, (n_q_heads / c.H) * n_q,
-                       kv_len - (c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0), c.B * c.H);
+                       kv_len - (c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0), c.B * c.H,
+                       work);
   if (chunk < 64 || chunk > 8192 || chunk % 64) return fail(KVQ_ESHAPE, "chunk %d not a multiple of 64 in [64, 8192]", chunk);
   a.Hq = n_q_heads; a.gqa = n_q_heads / c.H; a.n_q = n_q;
   a.kv_len = kv_len;
@@ -246,10 +250,15 @@ kvq_status resolve_attend(const kvq_cache *cache, int n_q_heads, int n_q, int kv
 
 // Paged call: the grid is sized for max_kv_len; per-sequence lengths are read on the device.
 kvq_status resolve_paged(const kvq_paged_cache *cache, int n_q_heads, int n_q, int max_kv_len, int causal, int chunk,
-                         kvq::AttendArgs &a, size_t &need, void *ws) {
+                         kvq::AttendArgs &a, size_t &need, void *ws, long long total_kv_len = 0) {
   kvq_status st = check_paged_cache(cache, a.cache);
   if (st != KVQ_OK) return st;
-  return resolve_core(n_q_heads, n_q, max_kv_len, causal, 0, true, chunk, a, need, ws);
+  long long work = 0;                                    // body tokens over all sequences and kv heads
+  if (total_kv_len > 0) {
+    const long long win = cache->layout == KVQ_HAD_INT4 ? (long long)cache->n_recent * cache->batch : 0;
+    work = (total_kv_len > win ? total_kv_len - win : 1) * cache->n_kv_heads;
+  }
+  return resolve_core(n_q_heads, n_q, max_kv_len, causal, 0, true, chunk, a, need, ws, work);
 }
 
 }  // namespace
@@ -479,10 +488,11 @@ size_t kvq_paged_attend_workspace_bytes(const kvq_paged_cache *cache, int32_t n_
 }
 
 int32_t kvq_paged_attend_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t max_kv_len,
-                               int32_t chunk) {
+                               int64_t total_kv_len, int32_t chunk) {
   kvq::AttendArgs a;
   size_t need = 0;
-  if (resolve_paged(cache, n_q_heads, n_q, max_kv_len, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  if (total_kv_len < 0) return 0;
+  if (resolve_paged(cache, n_q_heads, n_q, max_kv_len, 0, chunk, a, need, nullptr, total_kv_len) != KVQ_OK) return 0;
   return a.chunk;
 }
 

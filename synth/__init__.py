@@ -6,6 +6,6 @@ model activations). It holds none of the quantisation or attention arithmetic: n
 `oracle/` nor the CUDA library imports it, and it imports neither of them.
 """
 from .workloads import (  # noqa: F401
-    Workload, WORKLOADS, make_inputs, bf16_bits_from_f32, f32_from_bf16_bits,
+    Workload, WORKLOADS, make_inputs, make_paged_inputs, ragged_lengths, bf16_bits_from_f32, f32_from_bf16_bits,
     f16_bits_from_f32, f32_from_f16_bits,
 )

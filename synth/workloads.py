@@ -22,8 +22,8 @@ import math
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "bf16_bits_from_f32", "f32_from_bf16_bits",
-           "f16_bits_from_f32", "f32_from_f16_bits"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "make_paged_inputs", "ragged_lengths", "bf16_bits_from_f32",
+           "f32_from_bf16_bits", "f16_bits_from_f32", "f32_from_f16_bits"]
 
 
 # ----------------------------------------------------------------------------- dtype helpers
@@ -73,6 +73,8 @@ class Workload:
     rms_norm_qk: bool = False
     chunk: int = 512
     seed: int = 0
+    page_size: int = 0     # > 0: a paged pool of page_size-token pages, one length per sequence
+    seq_lens: tuple = ()   # per-sequence lengths of a paged workload (kv_len = their maximum)
 
     @property
     def gqa(self) -> int:
@@ -89,6 +91,14 @@ class Workload:
     def scaled(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
+
+def ragged_lengths(seed: int, n: int, lo: int, hi: int) -> tuple:
+    """n seeded sequence lengths drawn uniformly from [lo, hi] (a serving batch of mixed lengths)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return tuple(int(x) for x in rng.integers(lo, hi + 1, size=n))
+
+
+_RAGGED = ragged_lengths(1006, 16, 1024, 16384)
 
 WORKLOADS = {
     # Q4_0 tiny: B1, 8 q heads / 2 kv heads, d128, S512 decode; fp32 N(0,1), 2 K outlier channels x8.
@@ -113,6 +123,12 @@ WORKLOADS = {
     # same shape, per-group asymmetric int4 (g=32, fp16 scale + zero-point).
     "c5_asym4_g32_llama70b_128k": Workload("c5_asym4_g32_llama70b_128k", "asym4_g32", 1, 64, 8, 128, 131072,
                                            fill=131071, n_outlier=4, outlier_factor=10.0, seed=1005),
+    # serving-style paged batch of a Llama-3-8B layer (32/8 heads, d128), Q4_0: 16 sequences with
+    # seeded lengths in [1024, 16384], 64-token pages in a shuffled pool; decode: one new token per
+    # sequence, then attention over each sequence's own length.
+    "paged_q4_0_llama3_8b_ragged": Workload("paged_q4_0_llama3_8b_ragged", "q4_0", 16, 32, 8, 128, max(_RAGGED),
+                                            n_outlier=4, outlier_factor=10.0, seed=1006, page_size=64,
+                                            seq_lens=_RAGGED),
 }
 
 
@@ -173,4 +189,22 @@ def make_inputs(w: Workload, kv_len: int | None = None, n_q: int | None = None, 
             out[name] = x
         else:
             raise ValueError(w.dtype)
+    return out
+
+
+def make_paged_inputs(w: Workload) -> dict:
+    """Seeded inputs of a paged workload, drawn by the same recipe as `make_inputs` but only for
+    the tokens that exist: K/V of all sequences back to back, [H_kv][T][D] with T = sum(seq_lens)
+    (sequence b = tokens offsets[b] .. offsets[b] + seq_lens[b] - 1), and Q [B][H_q][n_q][D].
+    Keys as make_inputs (k, v, q and their *_bits) plus seq_lens and offsets (int64 arrays)."""
+    lens = np.asarray(w.seq_lens, np.int64)
+    T = int(lens.sum())
+    flat = make_inputs(w.scaled(batch=1, kv_len=T, n_q=w.n_q * w.batch))
+    out = {"dtype": flat["dtype"], "seq_lens": lens, "offsets": np.concatenate([[0], np.cumsum(lens)[:-1]])}
+    for name in ("k", "v"):
+        out[name] = flat[name][0]
+        out[name + "_bits"] = flat[name + "_bits"][0]
+    for name in ("q", "q_bits"):
+        x = flat[name][0]                                  # [H_q][B * n_q][D]
+        out[name] = np.ascontiguousarray(x.reshape(x.shape[0], w.batch, w.n_q, x.shape[-1]).transpose(1, 0, 2, 3))
     return out

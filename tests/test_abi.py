@@ -175,4 +175,10 @@ def test_paged_validation_without_device(L):
     rows, Cc = 16, 2
     assert L.kvq_paged_attend_workspace_bytes(p(c), 8, 1, 256, 128) == \
         2 * ((rows * Cc * 4 + 255) // 256 * 256) + (rows * Cc * 128 * 4 + 255) // 256 * 256
-    assert L.kvq_paged_attend_chunk(p(c), 8, 1, 256, 128) == 128
+    L.kvq_paged_attend_chunk.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_int32]
+    assert L.kvq_paged_attend_chunk(p(c), 8, 1, 256, 0, 128) == 128
+    # a ragged batch's total gives a chunk no larger than the max-length assumption's
+    big = _paged(n_pages=4096, mpp=2048)
+    auto_max = L.kvq_paged_attend_chunk(p(big), 8, 1, 131072, 0, 0)
+    auto_tot = L.kvq_paged_attend_chunk(p(big), 8, 1, 131072, 40000, 0)
+    assert auto_tot % 64 == 0 and 64 <= auto_tot <= auto_max
