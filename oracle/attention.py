@@ -169,11 +169,12 @@ def scores_int(q8: np.ndarray, k_codes: np.ndarray) -> np.ndarray:
 
 
 def attend_hadamard(q32, k_payload, k_scale, v_payload, v_scale, k_ring, v_ring, n_recent,
-                    alpha, kv_len, causal=False, q_pos0=0):
+                    alpha, kv_len, causal=False, q_pos0=0, layout="had_int4"):
     """Hadamard-int4 attention with the exact float32 recent window, float64 accumulation.
 
-    q32 [B][H_q][n_q][D] float32; k/v_payload [B][H_kv][S][D/2] uint8; k/v_scale [B][H_kv][S]
-    float32; k/v_ring [B][H_kv][n_recent][D] float32 (rotated rows) or None.
+    q32 [B][H_q][n_q][D] float32; k/v_payload [B][H_kv][S][row bytes] uint8 of `layout`
+    (had_int4: D/2 bytes, had_int2: D/4); k/v_scale [B][H_kv][S] float32; k/v_ring
+    [B][H_kv][n_recent][D] float32 (rotated rows) or None.
     Returns (out float64 [B][H_q][n_q][D], scores_i32 int64 [B][H_q][n_q][n_body]).
     """
     q32 = np.asarray(q32, np.float32)
@@ -190,8 +191,8 @@ def attend_hadamard(q32, k_payload, k_scale, v_payload, v_scale, k_ring, v_ring,
     for b in range(B):
         for h in range(Hq):
             kh = h // g
-            kc = Q.hadamard_codes(k_payload[b, kh, :n_body], D)
-            vc = Q.hadamard_codes(v_payload[b, kh, :n_body], D).astype(np.float64)
+            kc = Q.hadamard_layout_codes(layout, k_payload[b, kh, :n_body], D)
+            vc = Q.hadamard_layout_codes(layout, v_payload[b, kh, :n_body], D).astype(np.float64)
             ks = np.asarray(k_scale[b, kh, :n_body], np.float64)
             vs = np.asarray(v_scale[b, kh, :n_body], np.float64)
             i32 = scores_int(q8[b, h], kc)                                   # [nq][n_body]
@@ -225,13 +226,13 @@ class OracleCache:
 
     def __init__(self, layout, batch, n_kv_heads, head_dim, capacity, n_recent=0):
         self.layout, self.B, self.H, self.D, self.cap = layout, batch, n_kv_heads, head_dim, capacity
-        self.n_recent = n_recent if layout == "had_int4" else 0
+        self.n_recent = n_recent if layout in Q.HADAMARD else 0
         nb = head_dim // Q.BLOCK
         rb = Q.row_bytes(layout, head_dim)
         self.planes = {}
         for t in ("k", "v"):
             p = {"payload": np.zeros((batch, n_kv_heads, capacity, rb), np.uint8)}
-            if layout == "had_int4":
+            if layout in Q.HADAMARD:
                 p["scale"] = np.zeros((batch, n_kv_heads, capacity), np.float32)
                 if self.n_recent:
                     p["ring"] = np.zeros((batch, n_kv_heads, self.n_recent, head_dim), np.float32)
@@ -266,11 +267,11 @@ class OracleCache:
     def attend(self, q, alpha, kv_len, causal=False, q_pos0=0, chunk=None):
         """Attention of q [B][H_q][n_q][D] (float32 values) over the first kv_len tokens.
         Returns float64 [B][H_q][n_q][D] (and int64 body scores for Hadamard as a 2-tuple)."""
-        if self.layout == "had_int4":
+        if self.layout in Q.HADAMARD:
             k, v = self.planes["k"], self.planes["v"]
             return attend_hadamard(q, k["payload"], k["scale"], v["payload"], v["scale"],
                                    k.get("ring"), v.get("ring"), self.n_recent, alpha, kv_len,
-                                   causal, q_pos0)
+                                   causal, q_pos0, self.layout)
         K = self.dequantized("k", kv_len)
         V = self.dequantized("v", kv_len)
         if chunk:

@@ -34,14 +34,14 @@ class OraclePagedCache:
         self.layout, self.B, self.H, self.D = layout, batch, n_kv_heads, head_dim
         self.P, self.n_pages, self.max_pages = page_size, n_pages, max_pages_per_seq
         self.cap = page_size * max_pages_per_seq
-        self.n_recent = n_recent if layout == "had_int4" else 0
+        self.n_recent = n_recent if layout in Q.HADAMARD else 0
         nb = head_dim // Q.BLOCK
         rb = Q.row_bytes(layout, head_dim)
         pool = (n_pages, n_kv_heads, page_size)
         self.planes = {}
         for t in ("k", "v"):
             p = {"payload": np.zeros(pool + (rb,), np.uint8)}
-            if layout == "had_int4":
+            if layout in Q.HADAMARD:
                 p["scale"] = np.zeros(pool, np.float32)
                 if self.n_recent:
                     p["ring"] = np.zeros((batch, n_kv_heads, self.n_recent, head_dim), np.float32)

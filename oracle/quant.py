@@ -1,4 +1,5 @@
-"""Oracle quantizers: Q4_0, Q6_0, per-token Hadamard int4 and per-group asymmetric int4.
+"""Oracle quantizers: Q4_0, Q6_0, Q8_0, per-token Hadamard int4 / int2 and per-group
+asymmetric int4.
 
 TEST INFRASTRUCTURE ONLY (see the package docstring). Plain numpy, float32 IEEE arithmetic
 with round-half-to-even, one operation at a time in the order written below. Every function
@@ -19,6 +20,14 @@ Readings of points the pages leave open (each one a single constant or step here
       q = rint((x - zero) / scale) clamped to [0, 15], stored unsigned.
   R17 all-zero block (or a scale that rounds to fp16 zero) -> every code 0; fp16 scales and
       zeros saturate at +-65504; -0.0 quantises to code 0. Non-finite inputs are unspecified.
+  R22 Q8_0 (the pages give only its density, 1.0625 bytes/element): per 32 values 32 int8 code
+      bytes and one fp16 scale; by the family rule of R4/R5 (magnitude 2^(bits-1)) scale =
+      amax / 128 and codes clamped to [-128, 127], byte i = value i in two's complement, read
+      back as (v ^ 0x80) - 0x80.
+  R23 Hadamard int2 (the body below four bits that needs the exact-f32 window): the int4 layout
+      of R7 with two bits: symmetric, zero-point free, scale = amax / 1, codes in [-1, 1]; four
+      codes per byte, value 4j+i at bits 2i..2i+1 of byte j (two's complement), read back as
+      (v ^ 2) - 2.
 """
 from __future__ import annotations
 
@@ -29,7 +38,8 @@ import numpy as np
 BLOCK = 32                     # values per Q4_0/Q6_0/asym block along head_dim
 F16_MAX = np.float32(65504.0)
 
-LAYOUTS = ("q4_0", "q6_0", "had_int4", "asym4_g32")
+LAYOUTS = ("q4_0", "q6_0", "had_int4", "asym4_g32", "q8_0", "had_int2")
+HADAMARD = ("had_int4", "had_int2")       # layouts in the rotated basis with a per-token f32 scale
 
 
 # ------------------------------------------------------------------ sizes (closed forms)
@@ -43,13 +53,14 @@ def row_bytes(layout: str, head_dim: int) -> int:
     """
     nb = head_dim // BLOCK
     return {"q4_0": 16 * nb, "q6_0": 24 * nb, "had_int4": (head_dim + 1) // 2,
-            "asym4_g32": 16 * nb}[layout]
+            "asym4_g32": 16 * nb, "q8_0": 32 * nb, "had_int2": (head_dim + 3) // 4}[layout]
 
 
 def param_bytes(layout: str, head_dim: int) -> int:
     """Bytes of scale (+ zero-point) per token row of one head."""
     nb = head_dim // BLOCK
-    return {"q4_0": 2 * nb, "q6_0": 2 * nb, "had_int4": 4, "asym4_g32": 4 * nb}[layout]
+    return {"q4_0": 2 * nb, "q6_0": 2 * nb, "had_int4": 4, "asym4_g32": 4 * nb, "q8_0": 2 * nb,
+            "had_int2": 4}[layout]
 
 
 # ------------------------------------------------------------------ helpers
@@ -287,6 +298,86 @@ def dequantize_asym4_g32(payload: np.ndarray, scale: np.ndarray, zero: np.ndarra
     return x.reshape(payload.shape[:-1] + (nb * BLOCK,))
 
 
+# ------------------------------------------------------------------ Q8_0
+def quantize_q8_0(x: np.ndarray):
+    """Q8_0 (R22): per 32 values d = amax / 128 stored as fp16 (R3), q = clamp(rint(x / d),
+    -128, 127) (R1, R2), byte i of the block = q_i as a two's-complement byte.
+
+    Returns (payload uint8 [..., 32 * nb], scale float16 [..., nb]).
+    """
+    xb = _blocks(x)
+    amax = np.max(np.abs(xb), axis=-1)
+    d16 = fp16_round(amax / np.float32(128.0))
+    d = d16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.rint(xb / d)
+    q = np.where(d > 0, np.clip(r, -128, 127), 0.0).astype(np.int32)
+    payload = (q & 0xFF).astype(np.uint8)
+    return payload.reshape(x.shape[:-1] + (-1,)), d16
+
+
+def read_q8_0(v: np.ndarray) -> np.ndarray:
+    """Read-side sign extension of a Q8_0 byte: (v ^ 0x80) - 0x80 (R22)."""
+    v = np.asarray(v).astype(np.int32)
+    return (v ^ 0x80) - 0x80
+
+
+def dequantize_q8_0(payload: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    nb = scale.shape[-1]
+    p = np.asarray(payload, np.uint8).reshape(np.asarray(payload).shape[:-1] + (nb, BLOCK))
+    x = read_q8_0(p).astype(np.float64) * np.asarray(scale).astype(np.float64)[..., None]
+    return x.reshape(np.asarray(payload).shape[:-1] + (nb * BLOCK,))
+
+
+# ------------------------------------------------------------------ Hadamard int2
+def pack_pairs_of_bits(f: np.ndarray) -> np.ndarray:
+    """Four 2-bit fields per byte: field 4j+i at bits 2i..2i+1 of byte j (R23)."""
+    f = np.asarray(f, dtype=np.uint8) & 0x3
+    D = f.shape[-1]
+    pad = (-D) % 4
+    if pad:
+        f = np.concatenate([f, np.zeros(f.shape[:-1] + (pad,), np.uint8)], axis=-1)
+    f = f.reshape(f.shape[:-1] + (-1, 4))
+    return (f[..., 0] | (f[..., 1] << 2) | (f[..., 2] << 4) | (f[..., 3] << 6)).astype(np.uint8)
+
+
+def unpack_pairs_of_bits(b: np.ndarray, count: int) -> np.ndarray:
+    """Inverse of pack_pairs_of_bits: the raw 2-bit fields in value order."""
+    b = np.asarray(b, dtype=np.uint8)
+    f = np.stack([(b >> (2 * i)) & 0x3 for i in range(4)], axis=-1)
+    return f.reshape(b.shape[:-1] + (4 * b.shape[-1],))[..., :count]
+
+
+def quantize_hadamard_int2(x: np.ndarray):
+    """Per-token symmetric int2 in the Hadamard basis (R23; tract discussion #2402, "Why this quant
+    scheme" and "Causality & mixed precision": int2 is usable only with the exact-f32 window).
+
+    y = rotate(x); s = amax(|y|) (float32); q = clamp(rint(y / s), -1, 1); four codes per byte.
+    Returns (payload uint8 [..., ceil(D/4)], scale float32 [...], y float32 [..., D]).
+    """
+    y = rotate(x)
+    s = np.max(np.abs(y), axis=-1).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.rint(y / s[..., None])
+    q = np.where(s[..., None] > 0, np.clip(r, -1, 1), 0.0).astype(np.int32)
+    return pack_pairs_of_bits(q & 0x3), s, y
+
+
+def read_int2(v: np.ndarray) -> np.ndarray:
+    """Read-side sign extension of a 2-bit field: (v ^ 2) - 2 (R23)."""
+    v = np.asarray(v).astype(np.int32)
+    return (v ^ 0x2) - 0x2
+
+
+def hadamard_int2_codes(payload: np.ndarray, head_dim: int) -> np.ndarray:
+    return read_int2(unpack_pairs_of_bits(payload, head_dim))
+
+
+def hadamard_layout_codes(layout: str, payload: np.ndarray, head_dim: int) -> np.ndarray:
+    """Signed codes of a Hadamard-layout row (int4 or int2)."""
+    return hadamard_codes(payload, head_dim) if layout == "had_int4" else hadamard_int2_codes(payload, head_dim)
+
+
 # ------------------------------------------------------------------ generic entry points
 def quantize(layout: str, x: np.ndarray) -> dict:
     """Quantize rows x[..., D]; returns a dict of the stored planes for `layout`."""
@@ -302,6 +393,12 @@ def quantize(layout: str, x: np.ndarray) -> dict:
     if layout == "asym4_g32":
         p, s, z = quantize_asym4_g32(x)
         return {"payload": p, "scale": s, "zero": z}
+    if layout == "q8_0":
+        p, s = quantize_q8_0(x)
+        return {"payload": p, "scale": s}
+    if layout == "had_int2":
+        p, s, y = quantize_hadamard_int2(x)
+        return {"payload": p, "scale": s, "rot": y}
     raise ValueError(layout)
 
 
@@ -315,4 +412,9 @@ def dequantize(layout: str, planes: dict, head_dim: int) -> np.ndarray:
         return dequantize_hadamard_int4(planes["payload"], planes["scale"], head_dim)
     if layout == "asym4_g32":
         return dequantize_asym4_g32(planes["payload"], planes["scale"], planes["zero"])
+    if layout == "q8_0":
+        return dequantize_q8_0(planes["payload"], planes["scale"])
+    if layout == "had_int2":
+        return hadamard_int2_codes(planes["payload"], head_dim).astype(np.float64) * \
+            np.asarray(planes["scale"], np.float64)[..., None]
     raise ValueError(layout)

@@ -108,3 +108,33 @@ def test_transposed_causal_limit_is_caught(monkeypatch):
         return t < (q_pos0 + np.arange(n_q))[:, None]          # off by one: excludes the diagonal
     monkeypatch.setattr(A, "visible_mask", bad)
     assert _fails(P.test_attention_brute_force_gqa_causal)
+
+
+def test_q8_0_magnitude_127_is_caught(monkeypatch):
+    # the GGUF-style amax / 127 instead of the family rule's amax / 128
+    def bad(x):
+        xb = Q._blocks(x)
+        amax = np.max(np.abs(xb), axis=-1)
+        d16 = Q.fp16_round(amax / np.float32(127.0))
+        d = d16.astype(np.float32)[..., None]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            r = np.rint(xb / d)
+        q = np.where(d > 0, np.clip(r, -128, 127), 0.0).astype(np.int32)
+        return (q & 0xFF).astype(np.uint8).reshape(x.shape[:-1] + (-1,)), d16
+    monkeypatch.setattr(Q, "quantize_q8_0", bad)
+    assert _fails(P.test_q8_0_every_code_through_read_formula, lambda: P.test_q8_0_byte_position_and_saturation(1))
+
+
+def test_int2_field_order_is_caught(monkeypatch):
+    # value 4j+i at bits 6-2i instead of 2i
+    def bad(f):
+        f = np.asarray(f, dtype=np.uint8) & 0x3
+        f = f.reshape(f.shape[:-1] + (-1, 4))
+        return (f[..., 3] | (f[..., 2] << 2) | (f[..., 1] << 4) | (f[..., 0] << 6)).astype(np.uint8)
+    monkeypatch.setattr(Q, "pack_pairs_of_bits", bad)
+    assert _fails(lambda: P.test_int2_field_positions(1))
+
+
+def test_int2_read_without_sign_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "read_int2", lambda v: np.asarray(v).astype(np.int32))
+    assert _fails(P.test_int2_read_formula_every_field, P.test_hadamard_int2_codes_and_scale)

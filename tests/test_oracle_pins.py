@@ -409,3 +409,129 @@ def test_recent_window_semantics():
     assert not np.allclose(out_w, out_0)       # the window changes the result ...
     ref = A.attend_dense(q, k, v, 0.1, S)
     assert np.linalg.norm(out_w - ref) < np.linalg.norm(out_0 - ref)   # ... towards exact attention
+
+
+# ------------------------------------------------------------------ Q8_0 (reading R22)
+def test_q8_0_density_is_the_pages():
+    D = 128
+    q8 = (Q.row_bytes("q8_0", D) + Q.param_bytes("q8_0", D)) / D
+    assert q8 == GOLD["q8_0_bytes_per_element"]["value"]
+    assert (GOLD["bytes_per_token_table"]["value"]["bf16"] // 2) * q8 == GOLD["bytes_per_token_table"]["value"]["q8_0"]
+
+
+def test_q8_0_every_code_through_read_formula():
+    # all 256 codes on an exact grid: 8 blocks of 32; each block holds -128 so amax = 128 s, s = 1/16
+    codes = np.arange(-128, 128, dtype=np.float32).reshape(8, 32)
+    codes[:, 0] = -128
+    x = codes * np.float32(0.0625)
+    p, s = Q.quantize_q8_0(x.reshape(1, 256))
+    assert np.all(s.astype(np.float32) == 0.0625)
+    got = [((int(p[0, i]) ^ 0x80) - 0x80) for i in range(256)]        # two's-complement byte i
+    assert got == [int(c) for c in codes.reshape(-1)]
+    assert np.array_equal(Q.dequantize_q8_0(p, s)[0], x.reshape(-1).astype(np.float64))
+
+
+@pytest.mark.parametrize("i", [0, 1, 7, 16, 31])
+def test_q8_0_byte_position_and_saturation(i):
+    x = np.zeros(32, np.float32)
+    x[i] = 12.8                     # amax -> scale fp16(0.1); 12.8 / scale rounds to 128 -> clamps to 127
+    x[(i + 9) % 32] = -12.8         # -amax -> -128
+    x[(i + 3) % 32] = 0.25          # an ordinary code
+    p, s = Q.quantize_q8_0(x[None])
+    sc = py_half(12.8 / 128.0)
+    assert float(s[0, 0]) == sc
+    want = {i: 127, (i + 9) % 32: -128, (i + 3) % 32: int(round(0.25 / sc))}
+    for j in range(32):
+        assert Q.read_q8_0(p[0, j]) == want.get(j, 0)
+
+
+def test_q8_0_half_even_and_zero_block():
+    x = np.zeros((2, 32), np.float32)
+    x[0, 0] = 128.0                                      # scale 1
+    x[0, 1:6] = [0.5, 1.5, 2.5, -0.5, -2.5]
+    p, s = Q.quantize_q8_0(x)
+    assert [int(Q.read_q8_0(p[0, j])) for j in range(1, 6)] == [0, 2, 2, 0, -2]
+    assert not p[1].any() and float(s[1, 0]) == 0.0
+
+
+# ------------------------------------------------------------------ Hadamard int2 (reading R23)
+def test_int2_read_formula_every_field():
+    # the four 2-bit fields through (v ^ 2) - 2: 0 -> 0, 1 -> 1, 2 -> -2, 3 -> -1
+    assert [int(Q.read_int2(v)) for v in range(4)] == [0, 1, -2, -1]
+
+
+@pytest.mark.parametrize("i", [0, 1, 2, 3, 4, 126, 127])
+def test_int2_field_positions(i):
+    # value 4j+i at bits 2i..2i+1 of byte j: pack a single -1 (field 0b11) at position i
+    f = np.zeros(128, np.int32)
+    f[i] = -1
+    b = Q.pack_pairs_of_bits(f & 3)
+    assert b.shape == (32,)
+    for j in range(32):
+        assert int(b[j]) == (3 << (2 * (i % 4)) if j == i // 4 else 0)
+    assert np.array_equal(Q.hadamard_int2_codes(b, 128), f)
+
+
+def test_hadamard_int2_codes_and_scale():
+    rng = np.random.default_rng(6)
+    x = rng.standard_t(4, (64, 128)).astype(np.float32)
+    p, s, y = Q.quantize_hadamard_int2(x)
+    assert p.shape == (64, 32) and s.dtype == np.float32
+    codes = Q.hadamard_int2_codes(p, 128)
+    assert set(np.unique(codes)) <= {-1, 0, 1}
+    assert np.all(s == np.max(np.abs(y), axis=1))                       # scale = amax / 1
+    # code = the nearest of {-1, 0, 1} to y / s (half-to-even at +-0.5: to 0)
+    r = y.astype(np.float64) / s[:, None]
+    want = np.where(r > 0.5, 1, np.where(r < -0.5, -1, 0))
+    assert np.array_equal(codes, want)
+
+
+def test_hadamard_int2_full_window_is_exact_attention():
+    # every token in the exact-f32 window: the int2 body is never read
+    rng = np.random.default_rng(14)
+    B, Hq, Hkv, S, D = 1, 4, 2, 40, 128
+    k = rng.standard_t(4, (B, Hkv, S, D)).astype(np.float32)
+    v = rng.standard_t(4, (B, Hkv, S, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, 1, D)).astype(np.float32)
+    c = A.OracleCache("had_int2", B, Hkv, D, S, n_recent=64)
+    c.store(k, v, 0)
+    out, _ = c.attend(q, 1 / math.sqrt(D), S)
+    ref = A.attend_dense(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64), 1 / math.sqrt(D), S)
+    assert np.allclose(out, ref, rtol=1e-5, atol=1e-5)
+
+
+def test_hadamard_int2_body_scores_brute_force():
+    # the body scores are the exact integer dots of the int8 query codes and the int2 key codes
+    rng = np.random.default_rng(15)
+    D, S = 128, 12
+    k = rng.standard_normal((1, 1, S, D)).astype(np.float32)
+    c = A.OracleCache("had_int2", 1, 1, D, S, n_recent=0)
+    c.store(k, k, 0)
+    q = rng.standard_normal((1, 1, 2, D)).astype(np.float32)
+    _, si = c.attend(q, 0.1, S)
+    _, _, q8 = A.prep_q_hadamard(q)
+    kc = Q.hadamard_int2_codes(c.planes["k"]["payload"][0, 0], D)
+    for r in range(2):
+        for t in range(S):
+            assert si[0, 0, r, t] == sum(int(q8[0, 0, r, d]) * int(kc[t, d]) for d in range(D))
+
+
+def test_int2_needs_the_window():
+    # the reason for the window: int2 alone is far off exact attention, and a window over the
+    # newest tokens brings it closer (tract discussion #2402, "Why this quant scheme")
+    rng = np.random.default_rng(16)
+    D, S = 128, 96
+    k = rng.standard_t(4, (1, 2, S, D)).astype(np.float32)
+    v = rng.standard_t(4, (1, 2, S, D)).astype(np.float32)
+    q = (rng.standard_normal((1, 4, 1, D)) * 2).astype(np.float32)
+    ref = A.attend_dense(q, k, v, 1 / math.sqrt(D), S)
+    errs = {}
+    for nr in (0, 32):
+        c = A.OracleCache("had_int2", 1, 2, D, S, n_recent=nr)
+        c.store(k, v, 0)
+        out, _ = c.attend(q, 1 / math.sqrt(D), S)
+        errs[nr] = np.linalg.norm(out - ref) / np.linalg.norm(ref)
+    c4 = A.OracleCache("had_int4", 1, 2, D, S)
+    c4.store(k, v, 0)
+    e4 = np.linalg.norm(c4.attend(q, 1 / math.sqrt(D), S)[0] - ref) / np.linalg.norm(ref)
+    assert errs[0] > e4 and errs[32] < errs[0]
