@@ -68,7 +68,18 @@ typedef enum {
   /* [OTQ] per-group asymmetric int4, g = 32: fp16 scale = (max - min) / 15 and fp16
    * zero-point = min per group; codes rint((x - zero) / scale) in [0, 15], unsigned, q4_0
    * nibble order; value = code * scale + zero. */
-  KVQ_ASYM4_G32 = 3
+  KVQ_ASYM4_G32 = 3,
+  /* [FT] q8_0 (only its density is printed, 1.0625 bytes/element): per 32 values 32 int8 code
+   * bytes (byte i = value i, two's complement) and one fp16 scale; by the family rule of q4_0 /
+   * q6_0 (magnitude 2^(bits-1)) scale = amax / 128 and codes clamped to [-128, 127]. */
+  KVQ_Q8_0 = 4,
+  /* [TR] the Hadamard layout with a 2-bit body ("Why this quant scheme": int2 is usable only
+   * with the mixed-precision window; "Causality & mixed precision": n_recent is the lever for
+   * pushing the body below 4 bits): per-token symmetric int2 in the same rotated basis, one f32
+   * scale s = amax(|y|) per token, codes rint(y / s) in [-1, 1], four per byte (value 4j+i at
+   * bits 2i of byte j, read back as (v ^ 2) - 2; D/4 bytes per token), the same optional ring
+   * of the newest n_recent rotated rows in exact f32. Meant for a wide window. */
+  KVQ_HAD_INT2 = 5
 } kvq_layout;
 
 typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_F16 = 2 } kvq_dtype;
@@ -76,11 +87,11 @@ typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_F16 = 2 } kvq_dtype;
 /*
  * A caller-owned packed cache for one attention layer. Planes (K and V each):
  *   payload  u8  [batch][n_kv_heads][capacity][kvq_row_bytes(layout, head_dim)]
- *   scale    f16 [batch][n_kv_heads][capacity][head_dim/32]      (Q4_0, Q6_0, ASYM4_G32)
- *            f32 [batch][n_kv_heads][capacity]                   (HAD_INT4)
+ *   scale    f16 [batch][n_kv_heads][capacity][head_dim/32]      (Q4_0, Q6_0, Q8_0, ASYM4_G32)
+ *            f32 [batch][n_kv_heads][capacity]                   (HAD_INT4, HAD_INT2)
  *   zero     f16 [batch][n_kv_heads][capacity][head_dim/32]      (ASYM4_G32 only, else NULL)
- *   recent   f32 [batch][n_kv_heads][n_recent][head_dim]         (HAD_INT4 with n_recent > 0,
- *                                                                 else NULL)
+ *   recent   f32 [batch][n_kv_heads][n_recent][head_dim]         (HAD_INT4 / HAD_INT2 with
+ *                                                                 n_recent > 0, else NULL)
  * Payload and scales sit in separate buffers ([FT] "packed buffer + separate scale buffer").
  * The cache is preallocated at `capacity` tokens and appended in place ([OTQ]: per-step
  * concatenation instead of preallocated slices cost 18%).
@@ -91,7 +102,7 @@ typedef struct kvq_cache {
   int32_t n_kv_heads;
   int32_t head_dim;    /* 128 or 256 */
   int32_t capacity;    /* tokens per (batch, kv head) */
-  int32_t n_recent;    /* HAD_INT4: size of the exact-f32 ring (0 = pure int4); others: 0 */
+  int32_t n_recent;    /* HAD_INT4 / HAD_INT2: size of the exact-f32 ring (0 = none); others: 0 */
   void *k_payload, *v_payload;
   void *k_scale, *v_scale;
   void *k_zero, *v_zero;
@@ -124,6 +135,11 @@ kvq_status kvq_store_hadamard_int4(const kvq_cache *cache, const void *k_new, co
                                    kvq_stream_t stream);
 kvq_status kvq_store_asym4_g32(const kvq_cache *cache, const void *k_new, const void *v_new,
                                int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
+kvq_status kvq_store_q8_0(const kvq_cache *cache, const void *k_new, const void *v_new,
+                          int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
+kvq_status kvq_store_hadamard_int2(const kvq_cache *cache, const void *k_new, const void *v_new,
+                                   int32_t dtype, int32_t n_new, int32_t pos0,
+                                   kvq_stream_t stream);
 
 /* Workspace bytes kvq_decode_attend needs for these arguments on the current device (0 on
  * invalid arguments). chunk 0 means the automatic chunk described at kvq_decode_attend. */
@@ -280,7 +296,7 @@ kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const vo
                                           kvq_stream_t stream);
 
 /*
- * HAD_INT4 test hook: the exact integer-domain body scores int8(q_rot) . int4(k_rot).
+ * HAD_INT4 / HAD_INT2 test hook: the exact integer-domain body scores int8(q_rot) . code(k_rot).
  *   scores_out device i32 [batch][n_q_heads][n_q][kv_len - min(n_recent, kv_len)]
  *   s_q_out    device f32 [batch][n_q_heads][n_q]   (the per-row int8 scale of q_rot)
  */

@@ -14,7 +14,8 @@ from . import _lib as L
 
 _DTYPES = {torch.float32: L.KVQ_F32, torch.bfloat16: L.KVQ_BF16, torch.float16: L.KVQ_F16}
 _STORE_FN = {L.KVQ_Q4_0: "kvq_store_q4_0", L.KVQ_Q6_0: "kvq_store_q6_0",
-             L.KVQ_HAD_INT4: "kvq_store_hadamard_int4", L.KVQ_ASYM4_G32: "kvq_store_asym4_g32"}
+             L.KVQ_HAD_INT4: "kvq_store_hadamard_int4", L.KVQ_ASYM4_G32: "kvq_store_asym4_g32",
+             L.KVQ_Q8_0: "kvq_store_q8_0", L.KVQ_HAD_INT2: "kvq_store_hadamard_int2"}
 
 
 def _layout_id(layout) -> int:
@@ -52,15 +53,15 @@ class KVCache:
     """Device planes of one layer's packed cache plus the C struct describing them.
 
     Planes (K and V each): payload u8 [B][H_kv][cap][row_bytes]; scale f16 [B][H_kv][cap][D/32]
-    (f32 [B][H_kv][cap] for had_int4); zero f16 (asym4_g32); recent f32 [B][H_kv][n_recent][D]
-    (had_int4 with n_recent > 0).
+    (f32 [B][H_kv][cap] for had_int4 / had_int2); zero f16 (asym4_g32); recent f32 [B][H_kv][n_recent][D]
+    (the Hadamard layouts with n_recent > 0).
     """
 
     def __init__(self, layout, batch: int, n_kv_heads: int, head_dim: int, capacity: int, n_recent: int = 0,
                  device="cuda"):
         self.layout = _layout_id(layout)
         self.batch, self.n_kv_heads, self.head_dim, self.capacity = batch, n_kv_heads, head_dim, capacity
-        self.n_recent = n_recent if self.layout == L.KVQ_HAD_INT4 else 0
+        self.n_recent = n_recent if self.layout in L.HADAMARD_IDS else 0
         sizes = cache_plane_bytes(self.layout, batch, n_kv_heads, head_dim, capacity, self.n_recent)
         rb = row_bytes(self.layout, head_dim)
         nb = head_dim // 32
@@ -69,7 +70,7 @@ class KVCache:
         self.planes = {}
         for t in ("k", "v"):
             pl = {"payload": torch.zeros(shp + (rb,), dtype=torch.uint8, device=dev)}
-            if self.layout == L.KVQ_HAD_INT4:
+            if self.layout in L.HADAMARD_IDS:
                 pl["scale"] = torch.zeros(shp, dtype=torch.float32, device=dev)
                 if self.n_recent:
                     pl["recent"] = torch.zeros((batch, n_kv_heads, self.n_recent, head_dim), dtype=torch.float32,
@@ -93,7 +94,7 @@ class KVCache:
     def read_bytes(self, kv_len: int) -> int:
         """Packed bytes (payload + scales [+ zeros] [+ window]) one attention call reads."""
         per_tok = row_bytes(self.layout, self.head_dim)
-        if self.layout == L.KVQ_HAD_INT4:
+        if self.layout in L.HADAMARD_IDS:
             n_w = min(self.n_recent, kv_len)
             return 2 * self.batch * self.n_kv_heads * ((kv_len - n_w) * (per_tok + 4) + n_w * self.head_dim * 4)
         per_tok += 2 * (self.head_dim // 32) * (2 if self.layout == L.KVQ_ASYM4_G32 else 1)
@@ -233,7 +234,7 @@ class PagedKVCache:
         self.batch, self.n_kv_heads, self.head_dim = batch, n_kv_heads, head_dim
         self.page_size, self.n_pages, self.max_pages_per_seq = page_size, n_pages, max_pages_per_seq
         self.capacity = page_size * max_pages_per_seq
-        self.n_recent = n_recent if self.layout == L.KVQ_HAD_INT4 else 0
+        self.n_recent = n_recent if self.layout in L.HADAMARD_IDS else 0
         out = (C.c_size_t * 4)()
         L.check(L.lib().kvq_paged_cache_bytes(self.layout, n_pages, n_kv_heads, head_dim, page_size, batch,
                                               self.n_recent, out), "kvq_paged_cache_bytes")
@@ -244,7 +245,7 @@ class PagedKVCache:
         self.planes = {}
         for t in ("k", "v"):
             pl = {"payload": torch.zeros(shp + (rb,), dtype=torch.uint8, device=dev)}
-            if self.layout == L.KVQ_HAD_INT4:
+            if self.layout in L.HADAMARD_IDS:
                 pl["scale"] = torch.zeros(shp, dtype=torch.float32, device=dev)
                 if self.n_recent:
                     pl["recent"] = torch.zeros((batch, n_kv_heads, self.n_recent, head_dim), dtype=torch.float32,
@@ -276,7 +277,7 @@ class PagedKVCache:
         per_tok = row_bytes(self.layout, self.head_dim)
         total = 0
         for n in (int(x) for x in seq_lens):
-            if self.layout == L.KVQ_HAD_INT4:
+            if self.layout in L.HADAMARD_IDS:
                 n_w = min(self.n_recent, n)
                 total += (n - n_w) * (per_tok + 4) + n_w * self.head_dim * 4
             else:

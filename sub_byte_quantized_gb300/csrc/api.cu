@@ -33,6 +33,8 @@ size_t row_bytes_of(int layout, int D) {
     case KVQ_Q4_0: return 16 * (size_t)nb;
     case KVQ_Q6_0: return 24 * (size_t)nb;
     case KVQ_HAD_INT4: return (size_t)D / 2;
+    case KVQ_HAD_INT2: return (size_t)D / 4;
+    case KVQ_Q8_0: return 32 * (size_t)nb;
     case KVQ_ASYM4_G32: return 16 * (size_t)nb;
     default: return 0;
   }
@@ -40,13 +42,13 @@ size_t row_bytes_of(int layout, int D) {
 
 kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
-  if (c->layout < KVQ_Q4_0 || c->layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
+  if (c->layout < KVQ_Q4_0 || c->layout > kvq::kLastLayout) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
   if (c->head_dim != 128 && c->head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", c->head_dim);
   if (c->batch < 1 || c->n_kv_heads < 1 || c->capacity < 1)
     return fail(KVQ_EINVAL, "batch, n_kv_heads and capacity must be >= 1");
   if (c->n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
-  if (c->layout != KVQ_HAD_INT4 && c->n_recent != 0)
-    return fail(KVQ_EUNSUPPORTED, "n_recent is a Hadamard-int4 option");
+  if (!kvq::is_hadamard(c->layout) && c->n_recent != 0)
+    return fail(KVQ_EUNSUPPORTED, "n_recent is an option of the Hadamard layouts");
   const void *ptrs[] = {c->k_payload, c->v_payload, c->k_scale, c->v_scale};
   for (const void *p : ptrs) {
     if (!p) return fail(KVQ_EINVAL, "payload/scale pointer is NULL");
@@ -56,12 +58,12 @@ kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
     if (!c->k_zero || !c->v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
     if (!aligned(c->k_zero, 16) || !aligned(c->v_zero, 16)) return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
   }
-  if (c->layout == KVQ_HAD_INT4 && c->n_recent > 0) {
+  if (kvq::is_hadamard(c->layout) && c->n_recent > 0) {
     if (!c->k_recent || !c->v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
     if (!aligned(c->k_recent, 16) || !aligned(c->v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
   }
   v.layout = c->layout; v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim; v.cap = c->capacity;
-  v.n_recent = c->layout == KVQ_HAD_INT4 ? c->n_recent : 0;
+  v.n_recent = kvq::is_hadamard(c->layout) ? c->n_recent : 0;
   v.row_bytes = (int)row_bytes_of(c->layout, c->head_dim);
   v.payload[0] = static_cast<uint8_t *>(c->k_payload);
   v.payload[1] = static_cast<uint8_t *>(c->v_payload);
@@ -76,7 +78,7 @@ kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
 // Validation of a paged pool and its block table.
 kvq_status check_paged_cache(const kvq_paged_cache *c, kvq::CacheView &v) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
-  if (c->layout < KVQ_Q4_0 || c->layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
+  if (c->layout < KVQ_Q4_0 || c->layout > kvq::kLastLayout) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
   if (c->head_dim != 128 && c->head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", c->head_dim);
   if (c->batch < 1 || c->n_kv_heads < 1 || c->n_pages < 1 || c->max_pages_per_seq < 1)
     return fail(KVQ_EINVAL, "batch, n_kv_heads, n_pages and max_pages_per_seq must be >= 1");
@@ -87,8 +89,8 @@ kvq_status check_paged_cache(const kvq_paged_cache *c, kvq::CacheView &v) {
   if ((long long)c->max_pages_per_seq * c->page_size > INT_MAX)
     return fail(KVQ_ECAPACITY, "max_pages_per_seq * page_size exceeds INT_MAX tokens");
   if (c->n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
-  if (c->layout != KVQ_HAD_INT4 && c->n_recent != 0)
-    return fail(KVQ_EUNSUPPORTED, "n_recent is a Hadamard-int4 option");
+  if (!kvq::is_hadamard(c->layout) && c->n_recent != 0)
+    return fail(KVQ_EUNSUPPORTED, "n_recent is an option of the Hadamard layouts");
   const void *ptrs[] = {c->k_payload, c->v_payload, c->k_scale, c->v_scale, c->block_table};
   for (const void *p : ptrs) {
     if (!p) return fail(KVQ_EINVAL, "payload/scale/block_table pointer is NULL");
@@ -98,13 +100,13 @@ kvq_status check_paged_cache(const kvq_paged_cache *c, kvq::CacheView &v) {
     if (!c->k_zero || !c->v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
     if (!aligned(c->k_zero, 16) || !aligned(c->v_zero, 16)) return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
   }
-  if (c->layout == KVQ_HAD_INT4 && c->n_recent > 0) {
+  if (kvq::is_hadamard(c->layout) && c->n_recent > 0) {
     if (!c->k_recent || !c->v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
     if (!aligned(c->k_recent, 16) || !aligned(c->v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
   }
   v.layout = c->layout; v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim;
   v.cap = c->max_pages_per_seq * c->page_size;
-  v.n_recent = c->layout == KVQ_HAD_INT4 ? c->n_recent : 0;
+  v.n_recent = kvq::is_hadamard(c->layout) ? c->n_recent : 0;
   v.row_bytes = (int)row_bytes_of(c->layout, c->head_dim);
   v.payload[0] = static_cast<uint8_t *>(c->k_payload);
   v.payload[1] = static_cast<uint8_t *>(c->v_payload);
@@ -200,12 +202,12 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
     return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
   if (chunk == 0)
     chunk = auto_chunk(c, (n_q_heads / c.H) * n_q,
-                       kv_len - (c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0), c.B * c.H,
+                       kv_len - (kvq::is_hadamard(c.layout) ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0), c.B * c.H,
                        work);
   if (chunk < 64 || chunk > 8192 || chunk % 64) return fail(KVQ_ESHAPE, "chunk %d not a multiple of 64 in [64, 8192]", chunk);
   a.Hq = n_q_heads; a.gqa = n_q_heads / c.H; a.n_q = n_q;
   a.kv_len = kv_len;
-  a.n_win = c.layout == KVQ_HAD_INT4 ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0;
+  a.n_win = kvq::is_hadamard(c.layout) ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0;
   a.n_body = kv_len - a.n_win;
   a.causal = causal ? 1 : 0;
   a.q_pos0 = causal ? q_pos0 : 0;
@@ -223,7 +225,7 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
   const size_t o_l = off; off = round_up(off + rows * a.C * sizeof(float), 256);
   const size_t o_o = off; off = round_up(off + rows * a.C * (size_t)c.D * sizeof(float), 256);
   size_t o_q8 = 0, o_sq = 0, o_qr = 0;
-  if (c.layout == KVQ_HAD_INT4) {
+  if (kvq::is_hadamard(c.layout)) {
     o_q8 = off; off = round_up(off + rows * (size_t)c.D, 256);
     o_sq = off; off = round_up(off + rows * sizeof(float), 256);
     o_qr = off; off = round_up(off + rows * (size_t)c.D * sizeof(float), 256);
@@ -234,9 +236,9 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
     a.part_m = reinterpret_cast<float *>(w + o_m);
     a.part_l = reinterpret_cast<float *>(w + o_l);
     a.part_o = reinterpret_cast<float *>(w + o_o);
-    a.q8 = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<int8_t *>(w + o_q8) : nullptr;
-    a.s_q = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<float *>(w + o_sq) : nullptr;
-    a.q_rot = c.layout == KVQ_HAD_INT4 ? reinterpret_cast<float *>(w + o_qr) : nullptr;
+    a.q8 = kvq::is_hadamard(c.layout) ? reinterpret_cast<int8_t *>(w + o_q8) : nullptr;
+    a.s_q = kvq::is_hadamard(c.layout) ? reinterpret_cast<float *>(w + o_sq) : nullptr;
+    a.q_rot = kvq::is_hadamard(c.layout) ? reinterpret_cast<float *>(w + o_qr) : nullptr;
   }
   return KVQ_OK;
 }
@@ -255,7 +257,7 @@ kvq_status resolve_paged(const kvq_paged_cache *cache, int n_q_heads, int n_q, i
   if (st != KVQ_OK) return st;
   long long work = 0;                                    // body tokens over all sequences and kv heads
   if (total_kv_len > 0) {
-    const long long win = cache->layout == KVQ_HAD_INT4 ? (long long)cache->n_recent * cache->batch : 0;
+    const long long win = kvq::is_hadamard(cache->layout) ? (long long)cache->n_recent * cache->batch : 0;
     work = (total_kv_len > win ? total_kv_len - win : 1) * cache->n_kv_heads;
   }
   return resolve_core(n_q_heads, n_q, max_kv_len, causal, 0, true, chunk, a, need, ws, work);
@@ -272,15 +274,15 @@ kvq_status kvq_cache_bytes(int32_t layout, int32_t batch, int32_t n_kv_heads, in
   g_last_error[0] = 0;
   if (!out_sizes) return fail(KVQ_EINVAL, "out_sizes is NULL");
   const size_t rb = row_bytes_of(layout, head_dim);
-  if (layout < KVQ_Q4_0 || layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", layout);
+  if (layout < KVQ_Q4_0 || layout > kvq::kLastLayout) return fail(KVQ_EINVAL, "unknown layout %d", layout);
   if (!rb) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", head_dim);
   if (batch < 1 || n_kv_heads < 1 || capacity < 1 || n_recent < 0) return fail(KVQ_EINVAL, "bad sizes");
   const size_t rows = (size_t)batch * n_kv_heads * capacity;
   const size_t nb = (size_t)head_dim / kvq::kBlock;
   out_sizes[0] = rows * rb;
-  out_sizes[1] = layout == KVQ_HAD_INT4 ? rows * sizeof(float) : rows * nb * 2;
+  out_sizes[1] = kvq::is_hadamard(layout) ? rows * sizeof(float) : rows * nb * 2;
   out_sizes[2] = layout == KVQ_ASYM4_G32 ? rows * nb * 2 : 0;
-  out_sizes[3] = layout == KVQ_HAD_INT4 ? (size_t)batch * n_kv_heads * n_recent * head_dim * sizeof(float) : 0;
+  out_sizes[3] = kvq::is_hadamard(layout) ? (size_t)batch * n_kv_heads * n_recent * head_dim * sizeof(float) : 0;
   return KVQ_OK;
 }
 
@@ -299,6 +301,14 @@ kvq_status kvq_store_hadamard_int4(const kvq_cache *cache, const void *k_new, co
 kvq_status kvq_store_asym4_g32(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
                                int32_t n_new, int32_t pos0, kvq_stream_t stream) {
   return store_common(KVQ_ASYM4_G32, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
+kvq_status kvq_store_q8_0(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype, int32_t n_new,
+                          int32_t pos0, kvq_stream_t stream) {
+  return store_common(KVQ_Q8_0, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
+kvq_status kvq_store_hadamard_int2(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
+                                   int32_t n_new, int32_t pos0, kvq_stream_t stream) {
+  return store_common(KVQ_HAD_INT2, cache, k_new, v_new, dtype, n_new, pos0, stream);
 }
 
 size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t kv_len,
@@ -354,7 +364,7 @@ cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool even
   const bool mma = kvq::mma_supported(a);
   a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);   // the decode tensor-core kernels cover the body chunks only
   // the tensor-core kernels prepare the Hadamard query themselves; the CUDA-core one reads it
-  if (a.cache.layout == KVQ_HAD_INT4 && !mma) {
+  if (kvq::is_hadamard(a.cache.layout) && !mma) {
     a.fresh_lo = 0;                                      // its predecessor is then the prep kernel
     a.fresh_hi = INT_MAX;
     a.fresh_tail = 0;
@@ -417,16 +427,16 @@ kvq_status kvq_paged_cache_bytes(int32_t layout, int32_t n_pages, int32_t n_kv_h
                                  int32_t page_size, int32_t batch, int32_t n_recent, size_t out_sizes[4]) {
   g_last_error[0] = 0;
   if (!out_sizes) return fail(KVQ_EINVAL, "out_sizes is NULL");
-  if (layout < KVQ_Q4_0 || layout > KVQ_ASYM4_G32) return fail(KVQ_EINVAL, "unknown layout %d", layout);
+  if (layout < KVQ_Q4_0 || layout > kvq::kLastLayout) return fail(KVQ_EINVAL, "unknown layout %d", layout);
   const size_t rb = row_bytes_of(layout, head_dim);
   if (!rb) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", head_dim);
   if (n_pages < 1 || n_kv_heads < 1 || page_size < 1 || batch < 1 || n_recent < 0) return fail(KVQ_EINVAL, "bad sizes");
   const size_t rows = (size_t)n_pages * n_kv_heads * page_size;
   const size_t nb = (size_t)head_dim / kvq::kBlock;
   out_sizes[0] = rows * rb;
-  out_sizes[1] = layout == KVQ_HAD_INT4 ? rows * sizeof(float) : rows * nb * 2;
+  out_sizes[1] = kvq::is_hadamard(layout) ? rows * sizeof(float) : rows * nb * 2;
   out_sizes[2] = layout == KVQ_ASYM4_G32 ? rows * nb * 2 : 0;
-  out_sizes[3] = layout == KVQ_HAD_INT4 ? (size_t)batch * n_kv_heads * n_recent * head_dim * sizeof(float) : 0;
+  out_sizes[3] = kvq::is_hadamard(layout) ? (size_t)batch * n_kv_heads * n_recent * head_dim * sizeof(float) : 0;
   return KVQ_OK;
 }
 
@@ -544,7 +554,7 @@ kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q
   size_t need = 0;
   kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, 0, 0, 0, a, need, nullptr);
   if (st != KVQ_OK) return st;
-  if (a.cache.layout != KVQ_HAD_INT4) return fail(KVQ_EUNSUPPORTED, "integer scores exist for HAD_INT4 only");
+  if (!kvq::is_hadamard(a.cache.layout)) return fail(KVQ_EUNSUPPORTED, "integer scores exist for the Hadamard layouts only");
   if (q_dtype < KVQ_F32 || q_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown q dtype %d", q_dtype);
   if (!q || !scores_out || !s_q_out) return fail(KVQ_EINVAL, "q/scores_out/s_q_out is NULL");
   if (!aligned(q, 16) || !aligned(scores_out, 16) || !aligned(s_q_out, 16))

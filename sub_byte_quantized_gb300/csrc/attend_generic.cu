@@ -39,7 +39,8 @@ __device__ __forceinline__ void chunk_range(const AttendArgs &a, const SeqLen &s
 }
 
 // Unpack 8 values (group gi of a token row) of a packed row into f32 (value = code * scale [+ zero]).
-// For HAD_INT4 the raw signed codes are produced (the per-token scale is applied by the caller).
+// For the Hadamard layouts the raw signed codes are produced (the per-token scale is applied by
+// the caller).
 __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, int gi, float out[8]) {
   const uint8_t *p = c.payload[kv] + row * (size_t)c.row_bytes;
   const int blk = gi >> 2, sub = gi & 3;
@@ -47,6 +48,12 @@ __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, 
     const uint32_t w = *reinterpret_cast<const uint32_t *>(p + gi * 4);
 #pragma unroll
     for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8);
+    return;
+  }
+  if (c.layout == KVQ_HAD_INT2) {                       // four 2-bit fields per byte, (v ^ 2) - 2
+    const uint32_t w = *reinterpret_cast<const uint16_t *>(p + gi * 2);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (2 * i)) & 0x3u ^ 0x2u) - 2);
     return;
   }
   const float s = __half2float(static_cast<const __half *>(c.scale[kv])[row * (c.D / kBlock) + blk]);
@@ -61,6 +68,13 @@ __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, 
     for (int i = 0; i < 8; ++i) {
       const uint32_t v = ((lo >> (4 * i)) & 0xFu) | (((hi >> (2 * i)) & 0x3u) << 4);
       out[i] = (float)((int)(v ^ 0x20u) - 0x20) * s;
+    }
+  } else if (c.layout == KVQ_Q8_0) {                    // byte i = value i, (v ^ 0x80) - 0x80
+    const uint2 w = *reinterpret_cast<const uint2 *>(p + blk * 32 + sub * 8);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t b = ((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFFu;
+      out[i] = (float)((int)(b ^ 0x80u) - 0x80) * s;
     }
   } else {  // ASYM4_G32
     const float z = __half2float(c.zero[kv][row * (c.D / kBlock) + blk]);
@@ -101,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
   int t0, t1;
   chunk_range(a, sl, chunk_id, t0, t1);
   const bool is_win = chunk_id >= a.n_chunks;
-  const bool had = c.layout == KVQ_HAD_INT4;
+  const bool had = is_hadamard(c.layout);
   const int lim = row_ok ? row_limit(a, sl, qi) : -1;
   // Highest token any row of this CTA may see.
   int cta_lim = -1;
@@ -285,10 +299,18 @@ __global__ void __launch_bounds__(128) debug_scores_kernel(CacheView c, const vo
   if (t >= n_body) return;
   const uint8_t *p = c.payload[0] + ((size_t)(b * c.H + kvh) * c.cap + t) * (size_t)c.row_bytes;
   int acc = 0;
-  for (int g = 0; g < D / 8; ++g) {
-    const uint32_t w = *reinterpret_cast<const uint32_t *>(p + g * 4);
+  if (c.layout == KVQ_HAD_INT2) {
+    for (int g = 0; g < D / 8; ++g) {
+      const uint32_t w = *reinterpret_cast<const uint16_t *>(p + g * 2);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc += q8s[g * 8 + i] * ((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8);
+      for (int i = 0; i < 8; ++i) acc += q8s[g * 8 + i] * ((int)((w >> (2 * i)) & 0x3u ^ 0x2u) - 2);
+    }
+  } else {
+    for (int g = 0; g < D / 8; ++g) {
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(p + g * 4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc += q8s[g * 8 + i] * ((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8);
+    }
   }
   scores[(size_t)row * n_body + t] = acc;
 }

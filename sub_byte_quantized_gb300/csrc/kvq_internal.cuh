@@ -11,7 +11,12 @@
 
 namespace kvq {
 
-constexpr int kBlock = 32;          // values per Q4_0 / Q6_0 / asymmetric block
+constexpr int kBlock = 32;          // values per Q4_0 / Q6_0 / Q8_0 / asymmetric block
+constexpr int kLastLayout = KVQ_HAD_INT2;
+// Layouts in the fixed Hadamard basis: one f32 scale per token, rotated query, optional f32 window.
+__host__ __device__ constexpr bool is_hadamard(int layout) {
+  return layout == KVQ_HAD_INT4 || layout == KVQ_HAD_INT2;
+}
 constexpr int kMaxDevices = 64;     // per-device one-time kernel attribute set-up
 
 // Tensor-core phase 1: resident CTAs (of four warps) per SM the kernel is built for; the

@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
 
 cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl) {
   const unsigned rows = (unsigned)((size_t)a.cache.B * a.Hq * a.n_q);
-  const bool had = a.cache.layout == KVQ_HAD_INT4;
+  const bool had = is_hadamard(a.cache.layout);
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   // many rows and no window work here: one warp per row

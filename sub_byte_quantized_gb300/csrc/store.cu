@@ -4,10 +4,11 @@
 // (__fdiv_rn / __fsub_rn / __fmul_rn, rintf = round half to even, __float2half_rn), and this
 // file is compiled with -fmad=false so no multiply-add is ever contracted.
 //
-// Q4_0 / Q6_0 / asymmetric: 4 threads per 32-value block, 8 values per thread; the block's
-// amax (or min/max) is reduced over those 4 lanes with shuffles. Loads are 16-byte vectors,
-// stores are the thread's 4 payload bytes (+ 2 high-plane bytes for Q6_0).
-// Hadamard int4: one warp per token row; the FWHT runs in registers and shuffles.
+// Q4_0 / Q6_0 / Q8_0 / asymmetric: 4 threads per 32-value block, 8 values per thread; the
+// block's amax (or min/max) is reduced over those 4 lanes with shuffles. Loads are 16-byte
+// vectors, stores are the thread's 4 payload bytes (+ 2 high-plane bytes for Q6_0; 8 bytes for
+// Q8_0).
+// Hadamard int4 / int2: one warp per token row; the FWHT runs in registers and shuffles.
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -60,7 +61,7 @@ __device__ __forceinline__ int sym_code(float x, float s, int lo, int hi) {
   return (int)fminf(fmaxf(r, (float)lo), (float)hi);
 }
 
-// LAYOUT: KVQ_Q4_0, KVQ_Q6_0 or KVQ_ASYM4_G32.
+// LAYOUT: KVQ_Q4_0, KVQ_Q6_0, KVQ_Q8_0 or KVQ_ASYM4_G32.
 template <int LAYOUT>
 __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const void *__restrict__ k_new,
                                                           const void *__restrict__ v_new, int dtype,
@@ -126,6 +127,18 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
     if (!valid) return;
     *reinterpret_cast<uint32_t *>(prow + blk * 16 + lb * 4) = w;
     if (lb == 0) srow[blk] = sh;
+  } else if (LAYOUT == KVQ_Q8_0) {
+    const __half sh = f16_sat(__fdiv_rn(amax, 128.0f));
+    const float s = __half2float(sh);
+    uint32_t w0 = 0, w1 = 0;                   // byte i = value i (two's complement)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w0 |= ((uint32_t)sym_code(v[i], s, -128, 127) & 0xFFu) << (8 * i);
+      w1 |= ((uint32_t)sym_code(v[4 + i], s, -128, 127) & 0xFFu) << (8 * i);
+    }
+    if (!valid) return;
+    *reinterpret_cast<uint2 *>(prow + blk * 32 + lb * 8) = make_uint2(w0, w1);
+    if (lb == 0) srow[blk] = sh;
   } else {  // Q6_0
     const __half sh = f16_sat(__fdiv_rn(amax, 32.0f));
     const float s = __half2float(sh);
@@ -144,8 +157,9 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
   }
 }
 
-// Hadamard int4: one warp per token row, V = D/32 values per lane.
-template <int V>
+// Hadamard int4 (BITS 4: scale amax / 7, codes [-7, 7], two per byte) or int2 (BITS 2: scale
+// amax, codes [-1, 1], four per byte): one warp per token row, V = D/32 values per lane.
+template <int V, int BITS>
 __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void *__restrict__ k_new,
                                                         const void *__restrict__ v_new, int dtype,
                                                         StoreGeom g) {
@@ -175,12 +189,16 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
   }
 #pragma unroll
   for (int m = 16; m; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-  const float s = __fdiv_rn(amax, 7.0f);
-  uint32_t w = 0;
+  constexpr int QMAX = BITS == 4 ? 7 : 1;
+  const float s = __fdiv_rn(amax, (float)QMAX);
+  uint32_t w = 0;                                           // field i of the lane at bits BITS*i
 #pragma unroll
-  for (int i = 0; i < V; ++i) w |= ((uint32_t)sym_code(x[i], s, -7, 7) & 0xFu) << (4 * i);
+  for (int i = 0; i < V; ++i)
+    w |= ((uint32_t)sym_code(x[i], s, -QMAX, QMAX) & ((1u << BITS) - 1u)) << (BITS * i);
   uint8_t *prow = c.payload[kv] + (size_t)crow * g.row_bytes;
-  if (V == 4) {
+  if (V * BITS == 8) {
+    prow[lane] = (uint8_t)w;
+  } else if (V * BITS == 16) {
     *reinterpret_cast<uint16_t *>(prow + lane * 2) = (uint16_t)w;
   } else {
     *reinterpret_cast<uint32_t *>(prow + lane * 4) = w;
@@ -206,16 +224,23 @@ cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_ne
   g.row_bytes = c.row_bytes; g.nb = c.D / kBlock;
   g.rows_per_tensor = (long long)c.B * c.H * n_new;
   const long long rows = 2 * g.rows_per_tensor;
-  if (c.layout == KVQ_HAD_INT4) {
-    const long long blocks = (rows * 32 + 255) / 256;
-    if (c.D == 128) store_had_kernel<4><<<(unsigned)blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
-    else store_had_kernel<8><<<(unsigned)blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+  if (is_hadamard(c.layout)) {
+    const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
+    const bool two = c.layout == KVQ_HAD_INT2;
+    if (c.D == 128) {
+      if (two) store_had_kernel<4, 2><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+      else store_had_kernel<4, 4><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+    } else {
+      if (two) store_had_kernel<8, 2><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+      else store_had_kernel<8, 4><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
+    }
   } else {
     const long long threads = rows * (c.D / 8);
     const unsigned blocks = (unsigned)((threads + 255) / 256);
     switch (c.layout) {
       case KVQ_Q4_0: store_block_kernel<KVQ_Q4_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
       case KVQ_Q6_0: store_block_kernel<KVQ_Q6_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
+      case KVQ_Q8_0: store_block_kernel<KVQ_Q8_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
       default: store_block_kernel<KVQ_ASYM4_G32><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
     }
   }

@@ -63,17 +63,21 @@ def test_chunk_sizes(chunk):
     run_case(WORKLOADS["c2_q4_0_llama3_8b"].scaled(batch=1), 1000, chunk=chunk)
 
 
+HADAMARD = ("had_int4", "had_int2")
+ALL_LAYOUTS = ["q4_0", "q6_0", "had_int4", "asym4_g32", "q8_0", "had_int2"]
+
+
 @pytest.mark.parametrize("q_dtype", ["f32", "f16"])
-@pytest.mark.parametrize("layout", ["q4_0", "q6_0", "had_int4", "asym4_g32"])
+@pytest.mark.parametrize("layout", ALL_LAYOUTS)
 def test_query_dtypes(layout, q_dtype):
-    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=1, n_recent=32 if layout == "had_int4" else 0)
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=1, n_recent=32 if layout in HADAMARD else 0)
     run_case(w, 700, q_dtype=q_dtype)
 
 
-@pytest.mark.parametrize("layout", ["q4_0", "q6_0", "had_int4", "asym4_g32"])
+@pytest.mark.parametrize("layout", ALL_LAYOUTS)
 @pytest.mark.parametrize("kv_len", [1, 2, 63, 64, 65, 513])
 def test_edge_lengths(layout, kv_len):
-    w = WORKLOADS["c1_q4_0_tiny"].scaled(layout=layout, n_recent=16 if layout == "had_int4" else 0)
+    w = WORKLOADS["c1_q4_0_tiny"].scaled(layout=layout, n_recent=16 if layout in HADAMARD else 0)
     run_case(w, kv_len, chunk=64)
 
 
@@ -196,8 +200,9 @@ def test_causal_prefill_rows(D):
         run_case(w.scaled(q_pos0=100), kv_len=300, n_q=200, fill=100, chunk=64)
 
 
-def test_hadamard_integer_scores_bit_exact():
-    w = WORKLOADS["c3_had_int4_prefill"]
+@pytest.mark.parametrize("layout", HADAMARD)
+def test_hadamard_integer_scores_bit_exact(layout):
+    w = WORKLOADS["c3_had_int4_prefill"].scaled(layout=layout)
     S, nq = 1100, 64
     inp = make_inputs(w, kv_len=S, n_q=nq)
     dc, oc, d = fill_both(w, inp, fill=S - nq)
@@ -273,3 +278,19 @@ def test_workloads_full_size_sampled(name):
         ref = _oracle_rows_for_kv_head(w, inp, kvh, S, q_pos0)
         got = out[:, kvh * w.gqa:(kvh + 1) * w.gqa]
         check_close(got, ref, f"{name} kv head {kvh}")
+
+
+@pytest.mark.parametrize("layout,D,gqa,n_q,causal,n_recent,chunk", [
+    ("q8_0", 128, 8, 1, False, 0, 0),            # Llama-70B-like GQA 8 decode
+    ("q8_0", 256, 2, 1, False, 0, 128),
+    ("q8_0", 128, 2, 40, True, 0, 64),           # causal prefill rows
+    ("had_int2", 128, 2, 1, False, 256, 0),      # int2 body with a wide exact-f32 window
+    ("had_int2", 128, 2, 40, True, 128, 64),
+    ("had_int2", 256, 2, 1, False, 64, 128),
+])
+def test_q8_0_and_int2(layout, D, gqa, n_q, causal, n_recent, chunk):
+    """Q8_0 and the Hadamard int2 body (with the window it needs) against the oracle: decode and
+    causal prefill rows, head_dim 128 and 256, several chunks plus a ragged tail."""
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, head_dim=D, batch=2, n_kv_heads=2,
+                                              n_q_heads=2 * gqa, n_recent=n_recent, causal=causal)
+    run_case(w, kv_len=1100, n_q=n_q, chunk=chunk, fill=1100 - max(n_q, 1))

@@ -113,6 +113,8 @@ def _decode_w(layout, D=128, gqa=4, n_recent=0, causal=False):
     ("asym4_g32", 128, 128, 192, 0),     # stages starting mid-page
     ("q6_0", 256, 128, 0, 0),
     ("q6_0", 128, 64, 128, 0),
+    ("q8_0", 128, 64, 0, 0),
+    ("had_int2", 128, 64, 0, 128),
 ])
 def test_paged_decode(layout, D, page, chunk, n_recent):
     """Decode (one query row, GQA 4) over ragged sequences, one of them empty, one shorter than a

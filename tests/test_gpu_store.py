@@ -12,7 +12,8 @@ from tests.gpu_helpers import fill_both, planes_equal
 
 pytestmark = pytest.mark.gpu
 
-LAYOUTS = ["q4_0", "q6_0", "had_int4", "asym4_g32"]
+LAYOUTS = ["q4_0", "q6_0", "had_int4", "asym4_g32", "q8_0", "had_int2"]
+HADAMARD = ("had_int4", "had_int2")
 
 
 def special_rows(rng, n, D):
@@ -50,7 +51,7 @@ def test_store_bit_exact(layout, D, dtype):
         tdt = torch.float16
     else:
         tdt = torch.float32
-    n_recent = 16 if layout == "had_int4" else 0
+    n_recent = 16 if layout in HADAMARD else 0
     dc = kvq.KVCache(layout, B, H, D, cap, n_recent=n_recent)
     oc = OA.OracleCache(layout, B, H, D, cap, n_recent=n_recent)
     kd = torch.from_numpy(k).to(tdt).cuda()
@@ -65,7 +66,7 @@ def test_store_bit_exact(layout, D, dtype):
 def test_store_appends_and_restore_is_identical(layout):
     rng = np.random.default_rng(3)
     B, H, D, cap = 1, 2, 128, 300
-    n_recent = 24 if layout == "had_int4" else 0
+    n_recent = 24 if layout in HADAMARD else 0
     x = rng.standard_t(4, (B, H, cap, D)).astype(np.float32)
     y = rng.standard_t(4, (B, H, cap, D)).astype(np.float32)
     dc = kvq.KVCache(layout, B, H, D, cap, n_recent=n_recent)
