@@ -169,12 +169,12 @@ def scores_int(q8: np.ndarray, k_codes: np.ndarray) -> np.ndarray:
 
 
 def attend_hadamard(q32, k_payload, k_scale, v_payload, v_scale, k_ring, v_ring, n_recent,
-                    alpha, kv_len, causal=False, q_pos0=0, layout="had_int4"):
+                    alpha, kv_len, causal=False, q_pos0=0, layout="had_int4", v_layout=None):
     """Hadamard-int4 attention with the exact float32 recent window, float64 accumulation.
 
-    q32 [B][H_q][n_q][D] float32; k/v_payload [B][H_kv][S][row bytes] uint8 of `layout`
-    (had_int4: D/2 bytes, had_int2: D/4); k/v_scale [B][H_kv][S] float32; k/v_ring
-    [B][H_kv][n_recent][D] float32 (rotated rows) or None.
+    q32 [B][H_q][n_q][D] float32; k/v_payload [B][H_kv][S][row bytes] uint8 of `layout` (K) and
+    `v_layout` (V, default the same; had_int4: D/2 bytes, had_int2: D/4); k/v_scale [B][H_kv][S]
+    float32; k/v_ring [B][H_kv][n_recent][D] float32 (rotated rows) or None.
     Returns (out float64 [B][H_q][n_q][D], scores_i32 int64 [B][H_q][n_q][n_body]).
     """
     q32 = np.asarray(q32, np.float32)
@@ -192,7 +192,7 @@ def attend_hadamard(q32, k_payload, k_scale, v_payload, v_scale, k_ring, v_ring,
         for h in range(Hq):
             kh = h // g
             kc = Q.hadamard_layout_codes(layout, k_payload[b, kh, :n_body], D)
-            vc = Q.hadamard_layout_codes(layout, v_payload[b, kh, :n_body], D).astype(np.float64)
+            vc = Q.hadamard_layout_codes(v_layout or layout, v_payload[b, kh, :n_body], D).astype(np.float64)
             ks = np.asarray(k_scale[b, kh, :n_body], np.float64)
             vs = np.asarray(v_scale[b, kh, :n_body], np.float64)
             i32 = scores_int(q8[b, h], kc)                                   # [nq][n_body]
@@ -226,19 +226,21 @@ class OracleCache:
 
     def __init__(self, layout, batch, n_kv_heads, head_dim, capacity, n_recent=0):
         self.layout, self.B, self.H, self.D, self.cap = layout, batch, n_kv_heads, head_dim, capacity
-        self.n_recent = n_recent if layout in Q.HADAMARD else 0
+        self.lay = dict(zip(("k", "v"), Q.plane_layouts(layout)))      # each plane's own layout
+        self.n_recent = n_recent if Q.is_hadamard(layout) else 0
         nb = head_dim // Q.BLOCK
-        rb = Q.row_bytes(layout, head_dim)
         self.planes = {}
         for t in ("k", "v"):
+            lt = self.lay[t]
+            rb = Q.row_bytes(lt, head_dim)
             p = {"payload": np.zeros((batch, n_kv_heads, capacity, rb), np.uint8)}
-            if layout in Q.HADAMARD:
+            if lt in Q.HADAMARD:
                 p["scale"] = np.zeros((batch, n_kv_heads, capacity), np.float32)
                 if self.n_recent:
                     p["ring"] = np.zeros((batch, n_kv_heads, self.n_recent, head_dim), np.float32)
             else:
                 p["scale"] = np.zeros((batch, n_kv_heads, capacity, nb), np.float16)
-                if layout == "asym4_g32":
+                if lt == "asym4_g32":
                     p["zero"] = np.zeros((batch, n_kv_heads, capacity, nb), np.float16)
             self.planes[t] = p
 
@@ -249,7 +251,7 @@ class OracleCache:
         if pos0 < 0 or pos0 + n_new > self.cap:
             raise ValueError("store beyond capacity")
         for t, x in (("k", k_new), ("v", v_new)):
-            st = Q.quantize(self.layout, np.asarray(x, np.float32))
+            st = Q.quantize(self.lay[t], np.asarray(x, np.float32))
             pl = self.planes[t]
             for name in ("payload", "scale", "zero"):
                 if name in st and name in pl:
@@ -262,16 +264,16 @@ class OracleCache:
     def dequantized(self, t, kv_len):
         pl = self.planes[t]
         sub = {k: v[:, :, :kv_len] for k, v in pl.items() if k != "ring"}
-        return Q.dequantize(self.layout, sub, self.D)
+        return Q.dequantize(self.lay[t], sub, self.D)
 
     def attend(self, q, alpha, kv_len, causal=False, q_pos0=0, chunk=None):
         """Attention of q [B][H_q][n_q][D] (float32 values) over the first kv_len tokens.
         Returns float64 [B][H_q][n_q][D] (and int64 body scores for Hadamard as a 2-tuple)."""
-        if self.layout in Q.HADAMARD:
+        if Q.is_hadamard(self.layout):
             k, v = self.planes["k"], self.planes["v"]
             return attend_hadamard(q, k["payload"], k["scale"], v["payload"], v["scale"],
                                    k.get("ring"), v.get("ring"), self.n_recent, alpha, kv_len,
-                                   causal, q_pos0, self.layout)
+                                   causal, q_pos0, self.lay["k"], self.lay["v"])
         K = self.dequantized("k", kv_len)
         V = self.dequantized("v", kv_len)
         if chunk:

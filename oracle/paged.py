@@ -34,20 +34,21 @@ class OraclePagedCache:
         self.layout, self.B, self.H, self.D = layout, batch, n_kv_heads, head_dim
         self.P, self.n_pages, self.max_pages = page_size, n_pages, max_pages_per_seq
         self.cap = page_size * max_pages_per_seq
-        self.n_recent = n_recent if layout in Q.HADAMARD else 0
+        self.lay = dict(zip(("k", "v"), Q.plane_layouts(layout)))      # each plane's own layout
+        self.n_recent = n_recent if Q.is_hadamard(layout) else 0
         nb = head_dim // Q.BLOCK
-        rb = Q.row_bytes(layout, head_dim)
         pool = (n_pages, n_kv_heads, page_size)
         self.planes = {}
         for t in ("k", "v"):
-            p = {"payload": np.zeros(pool + (rb,), np.uint8)}
-            if layout in Q.HADAMARD:
+            lt = self.lay[t]
+            p = {"payload": np.zeros(pool + (Q.row_bytes(lt, head_dim),), np.uint8)}
+            if lt in Q.HADAMARD:
                 p["scale"] = np.zeros(pool, np.float32)
                 if self.n_recent:
                     p["ring"] = np.zeros((batch, n_kv_heads, self.n_recent, head_dim), np.float32)
             else:
                 p["scale"] = np.zeros(pool + (nb,), np.float16)
-                if layout == "asym4_g32":
+                if lt == "asym4_g32":
                     p["zero"] = np.zeros(pool + (nb,), np.float16)
             self.planes[t] = p
         self.table = np.zeros((batch, max_pages_per_seq), np.int64) if table is None else np.asarray(table, np.int64)
@@ -62,7 +63,7 @@ class OraclePagedCache:
         min(n_new, n_recent) rows of each sequence also go to its ring slot (position mod n_recent)."""
         n_new = k_new.shape[2]
         for t, x in (("k", k_new), ("v", v_new)):
-            st = Q.quantize(self.layout, np.asarray(x, np.float32))
+            st = Q.quantize(self.lay[t], np.asarray(x, np.float32))
             pl = self.planes[t]
             for b in range(self.B):
                 for j in range(n_new):

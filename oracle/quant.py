@@ -42,6 +42,21 @@ LAYOUTS = ("q4_0", "q6_0", "had_int4", "asym4_g32", "q8_0", "had_int2")
 HADAMARD = ("had_int4", "had_int2")       # layouts in the rotated basis with a per-token f32 scale
 
 
+def plane_layouts(layout: str):
+    """(K layout, V layout) of a cache layout name. Mixed K/V precision (Open-TQ-Metal, Section 5:
+    value quantisation costs more output quality than key quantisation) is written "k+v", e.g.
+    "q4_0+q8_0"; both planes are block layouts, or both are Hadamard layouts (one rotated basis)."""
+    k, _, v = layout.partition("+")
+    v = v or k
+    if k not in LAYOUTS or v not in LAYOUTS or ((k in HADAMARD) != (v in HADAMARD)):
+        raise ValueError(f"unsupported layout {layout!r}")
+    return k, v
+
+
+def is_hadamard(layout: str) -> bool:
+    return plane_layouts(layout)[0] in HADAMARD
+
+
 # ------------------------------------------------------------------ sizes (closed forms)
 def row_bytes(layout: str, head_dim: int) -> int:
     """Packed payload bytes of one token row of one head.

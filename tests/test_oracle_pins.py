@@ -535,3 +535,56 @@ def test_int2_needs_the_window():
     c4.store(k, v, 0)
     e4 = np.linalg.norm(c4.attend(q, 1 / math.sqrt(D), S)[0] - ref) / np.linalg.norm(ref)
     assert errs[0] > e4 and errs[32] < errs[0]
+
+
+# ------------------------------------------------------------------ mixed K/V precision
+def test_mixed_planes_are_the_single_layout_planes():
+    """A "k+v" cache stores K exactly as a cache of the K layout and V exactly as one of the V layout."""
+    rng = np.random.default_rng(21)
+    k = rng.standard_t(4, (1, 2, 40, 128)).astype(np.float32)
+    v = rng.standard_t(4, (1, 2, 40, 128)).astype(np.float32)
+    for kl, vl in (("q4_0", "q8_0"), ("q8_0", "q4_0"), ("asym4_g32", "q6_0"), ("had_int2", "had_int4")):
+        m = A.OracleCache(f"{kl}+{vl}", 1, 2, 128, 40, n_recent=8 if kl.startswith("had") else 0)
+        m.store(k, v, 0)
+        for lay, t, x in ((kl, "k", k), (vl, "v", v)):
+            single = A.OracleCache(lay, 1, 2, 128, 40, n_recent=8 if lay.startswith("had") else 0)
+            single.store(x, x, 0)
+            for name, arr in single.planes[t].items():
+                assert np.array_equal(m.planes[t][name], arr), (kl, vl, t, name)
+
+
+def test_mixed_attention_is_attention_of_each_planes_dequantisation():
+    rng = np.random.default_rng(22)
+    B, Hq, Hkv, S, D = 1, 4, 2, 50, 128
+    k = rng.standard_t(4, (B, Hkv, S, D)).astype(np.float32)
+    v = rng.standard_t(4, (B, Hkv, S, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, 2, D)).astype(np.float32)
+    m = A.OracleCache("q4_0+q8_0", B, Hkv, D, S)
+    m.store(k, v, 0)
+    got = m.attend(q, 0.1, S, causal=True, q_pos0=S - 2)
+    kd = Q.dequantize("q4_0", Q.quantize("q4_0", k), D)
+    vd = Q.dequantize("q8_0", Q.quantize("q8_0", v), D)
+    ref = A.attend_dense(q, kd, vd, 0.1, S, causal=True, q_pos0=S - 2)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mixed_rejects_a_rotated_and_an_unrotated_plane():
+    with pytest.raises(ValueError):
+        A.OracleCache("q4_0+had_int4", 1, 1, 128, 8)
+
+
+def test_value_precision_matters_more_than_key_precision():
+    """Open-TQ-Metal, Section 5: value errors reach the output directly, key errors pass through the
+    softmax; on heavy-tailed data the 4-bit K + 8-bit V cache is the closer of the two mixes."""
+    rng = np.random.default_rng(23)
+    B, Hq, Hkv, S, D = 1, 8, 2, 256, 128
+    k = rng.standard_t(4, (B, Hkv, S, D)).astype(np.float32)
+    v = rng.standard_t(4, (B, Hkv, S, D)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, 1, D)).astype(np.float32)
+    ref = A.attend_dense(q, k, v, 1 / math.sqrt(D), S)
+    err = {}
+    for lay in ("q4_0+q8_0", "q8_0+q4_0"):
+        c = A.OracleCache(lay, B, Hkv, D, S)
+        c.store(k, v, 0)
+        err[lay] = np.linalg.norm(c.attend(q, 1 / math.sqrt(D), S) - ref) / np.linalg.norm(ref)
+    assert err["q4_0+q8_0"] < err["q8_0+q4_0"]
