@@ -82,6 +82,14 @@ typedef enum {
   KVQ_HAD_INT2 = 5
 } kvq_layout;
 
+/* Mixed K/V precision ([OTQ] Section 5: value quantisation costs more output quality than key
+ * quantisation, so V may deserve more bits than K): a cache whose K plane uses layout `k` and
+ * whose V plane uses layout `v`, e.g. KVQ_MIXED(KVQ_Q4_0, KVQ_Q8_0). Both must be block layouts
+ * (Q4_0, Q6_0, Q8_0, ASYM4_G32) or both Hadamard layouts (HAD_INT4, HAD_INT2: one rotated basis,
+ * one window ring per plane). A plain layout value means the same layout for K and V. Mixed caches
+ * are stored with kvq_store and attended by every attention entry point. */
+#define KVQ_MIXED(k, v) ((int32_t)(k) | (((int32_t)(v) + 1) << 8))
+
 typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_F16 = 2 } kvq_dtype;
 
 /*
@@ -97,7 +105,8 @@ typedef enum { KVQ_F32 = 0, KVQ_BF16 = 1, KVQ_F16 = 2 } kvq_dtype;
  * concatenation instead of preallocated slices cost 18%).
  */
 typedef struct kvq_cache {
-  int32_t layout;      /* kvq_layout */
+  int32_t layout;      /* kvq_layout, or KVQ_MIXED(k layout, v layout): each plane's byte layout,
+                          scale and zero planes are then those of its own layout */
   int32_t batch;
   int32_t n_kv_heads;
   int32_t head_dim;    /* 128 or 256 */
@@ -113,7 +122,8 @@ typedef struct kvq_cache {
 size_t kvq_row_bytes(int32_t layout, int32_t head_dim);
 
 /* Bytes of each plane of one of K or V: out_sizes = {payload, scale, zero, recent}.
- * Unused planes report 0. */
+ * Unused planes report 0. `layout` is a plain layout: for a KVQ_MIXED cache ask once with the K
+ * layout (for the K planes) and once with the V layout. */
 kvq_status kvq_cache_bytes(int32_t layout, int32_t batch, int32_t n_kv_heads, int32_t head_dim,
                            int32_t capacity, int32_t n_recent, size_t out_sizes[4]);
 
@@ -137,6 +147,10 @@ kvq_status kvq_store_asym4_g32(const kvq_cache *cache, const void *k_new, const 
                                int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
 kvq_status kvq_store_q8_0(const kvq_cache *cache, const void *k_new, const void *v_new,
                           int32_t dtype, int32_t n_new, int32_t pos0, kvq_stream_t stream);
+/* The same append for a cache of any layout, KVQ_MIXED ones included (each plane quantised by
+ * its own layout; a mixed cache takes one launch per plane). */
+kvq_status kvq_store(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype,
+                     int32_t n_new, int32_t pos0, kvq_stream_t stream);
 kvq_status kvq_store_hadamard_int2(const kvq_cache *cache, const void *k_new, const void *v_new,
                                    int32_t dtype, int32_t n_new, int32_t pos0,
                                    kvq_stream_t stream);
@@ -215,7 +229,7 @@ kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, c
  * max_pages_per_seq * page_size tokens.
  */
 typedef struct kvq_paged_cache {
-  int32_t layout;             /* kvq_layout */
+  int32_t layout;             /* kvq_layout or KVQ_MIXED(k, v) */
   int32_t batch;              /* sequences (rows of the block table) */
   int32_t n_kv_heads;
   int32_t head_dim;           /* 128 or 256 */

@@ -16,6 +16,17 @@ KVQ_F32, KVQ_BF16, KVQ_F16 = 0, 1, 2
 LAYOUT_IDS = {"q4_0": KVQ_Q4_0, "q6_0": KVQ_Q6_0, "had_int4": KVQ_HAD_INT4, "asym4_g32": KVQ_ASYM4_G32,
               "q8_0": KVQ_Q8_0, "had_int2": KVQ_HAD_INT2}
 HADAMARD_IDS = (KVQ_HAD_INT4, KVQ_HAD_INT2)
+
+
+def mixed(k: int, v: int) -> int:
+    """KVQ_MIXED(k, v) of include/kvq.h: K plane in layout k, V plane in layout v."""
+    return k | ((v + 1) << 8)
+
+
+def plane_ids(layout: int):
+    """(K layout, V layout) of a layout value (plain or mixed)."""
+    k = layout & 0xFF
+    return k, ((layout >> 8) - 1) if layout >> 8 else k
 STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ESHAPE", 3: "KVQ_ECAPACITY", 4: "KVQ_EUNSUPPORTED",
                 5: "KVQ_EALIGN", 6: "KVQ_ECUDA", 7: "KVQ_EWORKSPACE"}
 
@@ -25,7 +36,8 @@ EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0
            "kvq_status_string", "kvq_last_error", "kvq_profile_phase1_events",
            "kvq_attend_chunk", "kvq_decode_attend_static", "kvq_append_decode_attend",
            "kvq_paged_cache_bytes", "kvq_paged_store", "kvq_paged_attend_workspace_bytes", "kvq_paged_attend_chunk",
-           "kvq_paged_decode_attend", "kvq_paged_append_decode_attend", "kvq_store_q8_0", "kvq_store_hadamard_int2")
+           "kvq_paged_decode_attend", "kvq_paged_append_decode_attend", "kvq_store_q8_0", "kvq_store_hadamard_int2",
+           "kvq_store")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ_STATIC_SCRATCH_BYTES in include/kvq.h
 
 
@@ -71,7 +83,7 @@ def lib() -> C.CDLL:
     L.kvq_row_bytes.argtypes, L.kvq_row_bytes.restype = [I32, I32], SZ
     L.kvq_cache_bytes.argtypes, L.kvq_cache_bytes.restype = [I32, I32, I32, I32, I32, I32, C.POINTER(SZ)], I32
     for name in ("kvq_store_q4_0", "kvq_store_q6_0", "kvq_store_hadamard_int4", "kvq_store_asym4_g32",
-                 "kvq_store_q8_0", "kvq_store_hadamard_int2"):
+                 "kvq_store_q8_0", "kvq_store_hadamard_int2", "kvq_store"):
         f = getattr(L, name)
         f.argtypes, f.restype = [cache_p, P, P, I32, I32, I32, P], I32
     L.kvq_attend_workspace_bytes.argtypes = [cache_p, I32, I32, I32, I32]

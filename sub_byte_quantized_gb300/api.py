@@ -19,7 +19,36 @@ _STORE_FN = {L.KVQ_Q4_0: "kvq_store_q4_0", L.KVQ_Q6_0: "kvq_store_q6_0",
 
 
 def _layout_id(layout) -> int:
-    return L.LAYOUT_IDS[layout] if isinstance(layout, str) else int(layout)
+    """Layout value of a name ("q4_0", or "k+v" such as "q4_0+q8_0" for mixed K/V precision) or id."""
+    if isinstance(layout, str):
+        k, _, v = layout.partition("+")
+        return L.mixed(L.LAYOUT_IDS[k], L.LAYOUT_IDS[v]) if v and v != k else L.LAYOUT_IDS[k]
+    return int(layout)
+
+
+def _plane_tensors(layout: int, lead: tuple, head_dim: int, dev, n_recent: int, ring_lead: tuple) -> dict:
+    """Zeroed device planes of one of K or V in a plain layout: payload, scale [, zero] [, recent]."""
+    rb = row_bytes(layout, head_dim)
+    nb = head_dim // 32
+    pl = {"payload": torch.zeros(lead + (rb,), dtype=torch.uint8, device=dev)}
+    if layout in L.HADAMARD_IDS:
+        pl["scale"] = torch.zeros(lead, dtype=torch.float32, device=dev)
+        if n_recent:
+            pl["recent"] = torch.zeros(ring_lead + (n_recent, head_dim), dtype=torch.float32, device=dev)
+    else:
+        pl["scale"] = torch.zeros(lead + (nb,), dtype=torch.float16, device=dev)
+        if layout == L.KVQ_ASYM4_G32:
+            pl["zero"] = torch.zeros(lead + (nb,), dtype=torch.float16, device=dev)
+    return pl
+
+
+def _plane_read_bytes(layout: int, head_dim: int, n_tokens: int, n_recent: int) -> int:
+    """Packed bytes one plane of one (batch, kv head) reads over n_tokens tokens."""
+    per_tok = row_bytes(layout, head_dim)
+    if layout in L.HADAMARD_IDS:
+        n_w = min(n_recent, n_tokens)
+        return (n_tokens - n_w) * (per_tok + 4) + n_w * head_dim * 4
+    return n_tokens * (per_tok + 2 * (head_dim // 32) * (2 if layout == L.KVQ_ASYM4_G32 else 1))
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:
@@ -60,25 +89,16 @@ class KVCache:
     def __init__(self, layout, batch: int, n_kv_heads: int, head_dim: int, capacity: int, n_recent: int = 0,
                  device="cuda"):
         self.layout = _layout_id(layout)
+        self.plane_layouts = dict(zip(("k", "v"), L.plane_ids(self.layout)))
         self.batch, self.n_kv_heads, self.head_dim, self.capacity = batch, n_kv_heads, head_dim, capacity
-        self.n_recent = n_recent if self.layout in L.HADAMARD_IDS else 0
-        sizes = cache_plane_bytes(self.layout, batch, n_kv_heads, head_dim, capacity, self.n_recent)
-        rb = row_bytes(self.layout, head_dim)
-        nb = head_dim // 32
+        self.n_recent = n_recent if self.plane_layouts["k"] in L.HADAMARD_IDS else 0
         dev = torch.device(device)
         shp = (batch, n_kv_heads, capacity)
         self.planes = {}
         for t in ("k", "v"):
-            pl = {"payload": torch.zeros(shp + (rb,), dtype=torch.uint8, device=dev)}
-            if self.layout in L.HADAMARD_IDS:
-                pl["scale"] = torch.zeros(shp, dtype=torch.float32, device=dev)
-                if self.n_recent:
-                    pl["recent"] = torch.zeros((batch, n_kv_heads, self.n_recent, head_dim), dtype=torch.float32,
-                                               device=dev)
-            else:
-                pl["scale"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
-                if self.layout == L.KVQ_ASYM4_G32:
-                    pl["zero"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
+            lt = self.plane_layouts[t]
+            sizes = cache_plane_bytes(lt, batch, n_kv_heads, head_dim, capacity, self.n_recent)
+            pl = _plane_tensors(lt, shp, head_dim, dev, self.n_recent, (batch, n_kv_heads))
             assert pl["payload"].numel() == sizes["payload"]
             self.planes[t] = pl
         self.struct = L.KvqCache(
@@ -93,12 +113,8 @@ class KVCache:
 
     def read_bytes(self, kv_len: int) -> int:
         """Packed bytes (payload + scales [+ zeros] [+ window]) one attention call reads."""
-        per_tok = row_bytes(self.layout, self.head_dim)
-        if self.layout in L.HADAMARD_IDS:
-            n_w = min(self.n_recent, kv_len)
-            return 2 * self.batch * self.n_kv_heads * ((kv_len - n_w) * (per_tok + 4) + n_w * self.head_dim * 4)
-        per_tok += 2 * (self.head_dim // 32) * (2 if self.layout == L.KVQ_ASYM4_G32 else 1)
-        return 2 * self.batch * self.n_kv_heads * kv_len * per_tok
+        return self.batch * self.n_kv_heads * sum(
+            _plane_read_bytes(self.plane_layouts[t], self.head_dim, kv_len, self.n_recent) for t in ("k", "v"))
 
 
 def store(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int, stream=None) -> None:
@@ -110,9 +126,10 @@ def store(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int, s
     B, H, n_new, D = k_new.shape
     if (B, H, D) != (cache.batch, cache.n_kv_heads, cache.head_dim):
         raise ValueError("k_new shape does not match the cache")
-    fn = getattr(L.lib(), _STORE_FN[cache.layout])
+    name = _STORE_FN.get(cache.layout, "kvq_store")       # mixed K/V layouts: the generic store
+    fn = getattr(L.lib(), name)
     L.check(fn(C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, pos0,
-               _stream(stream)), _STORE_FN[cache.layout])
+               _stream(stream)), name)
 
 
 def attend_workspace_bytes(cache: KVCache, n_q_heads: int, n_q: int, kv_len: int, chunk: int = 0) -> int:
@@ -234,26 +251,17 @@ class PagedKVCache:
         self.batch, self.n_kv_heads, self.head_dim = batch, n_kv_heads, head_dim
         self.page_size, self.n_pages, self.max_pages_per_seq = page_size, n_pages, max_pages_per_seq
         self.capacity = page_size * max_pages_per_seq
-        self.n_recent = n_recent if self.layout in L.HADAMARD_IDS else 0
-        out = (C.c_size_t * 4)()
-        L.check(L.lib().kvq_paged_cache_bytes(self.layout, n_pages, n_kv_heads, head_dim, page_size, batch,
-                                              self.n_recent, out), "kvq_paged_cache_bytes")
-        rb = row_bytes(self.layout, head_dim)
-        nb = head_dim // 32
+        self.plane_layouts = dict(zip(("k", "v"), L.plane_ids(self.layout)))
+        self.n_recent = n_recent if self.plane_layouts["k"] in L.HADAMARD_IDS else 0
         dev = torch.device(device)
         shp = (n_pages, n_kv_heads, page_size)
         self.planes = {}
         for t in ("k", "v"):
-            pl = {"payload": torch.zeros(shp + (rb,), dtype=torch.uint8, device=dev)}
-            if self.layout in L.HADAMARD_IDS:
-                pl["scale"] = torch.zeros(shp, dtype=torch.float32, device=dev)
-                if self.n_recent:
-                    pl["recent"] = torch.zeros((batch, n_kv_heads, self.n_recent, head_dim), dtype=torch.float32,
-                                               device=dev)
-            else:
-                pl["scale"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
-                if self.layout == L.KVQ_ASYM4_G32:
-                    pl["zero"] = torch.zeros(shp + (nb,), dtype=torch.float16, device=dev)
+            lt = self.plane_layouts[t]
+            out = (C.c_size_t * 4)()
+            L.check(L.lib().kvq_paged_cache_bytes(lt, n_pages, n_kv_heads, head_dim, page_size, batch,
+                                                  self.n_recent, out), "kvq_paged_cache_bytes")
+            pl = _plane_tensors(lt, shp, head_dim, dev, self.n_recent, (batch, n_kv_heads))
             assert pl["payload"].numel() == out[0]
             self.planes[t] = pl
         self.block_table = torch.zeros((batch, max_pages_per_seq), dtype=torch.int32, device=dev)
@@ -274,15 +282,8 @@ class PagedKVCache:
 
     def read_bytes(self, seq_lens) -> int:
         """Packed bytes (payload + scales [+ zeros] [+ window]) one attention call reads."""
-        per_tok = row_bytes(self.layout, self.head_dim)
-        total = 0
-        for n in (int(x) for x in seq_lens):
-            if self.layout in L.HADAMARD_IDS:
-                n_w = min(self.n_recent, n)
-                total += (n - n_w) * (per_tok + 4) + n_w * self.head_dim * 4
-            else:
-                total += n * (per_tok + 2 * (self.head_dim // 32) * (2 if self.layout == L.KVQ_ASYM4_G32 else 1))
-        return 2 * self.n_kv_heads * total
+        return self.n_kv_heads * sum(_plane_read_bytes(self.plane_layouts[t], self.head_dim, int(n), self.n_recent)
+                                     for n in seq_lens for t in ("k", "v"))
 
 
 def _i32_vec(name: str, t: torch.Tensor, n: int) -> None:

@@ -40,31 +40,52 @@ size_t row_bytes_of(int layout, int D) {
   }
 }
 
+// The K and V layouts of a cache's layout field (plain, or KVQ_MIXED(k, v)); false when invalid.
+bool split_layout(int32_t layout, int &k, int &v) {
+  k = layout & 0xFF;
+  v = (layout >> 8) ? (layout >> 8) - 1 : k;
+  if ((layout >> 8) > kvq::kLastLayout + 1 || layout < 0) return false;
+  if (k > kvq::kLastLayout || v > kvq::kLastLayout) return false;
+  return kvq::is_hadamard(k) == kvq::is_hadamard(v);
+}
+
+// Layout checks shared by the contiguous and paged caches: both planes' layouts, head_dim, the
+// window option and the plane pointers each plane's layout needs.
+kvq_status check_planes(int32_t layout, int32_t head_dim, int32_t n_recent, const void *k_zero, const void *v_zero,
+                        const float *k_recent, const float *v_recent, kvq::CacheView &v) {
+  int kl, vl;
+  if (!split_layout(layout, kl, vl)) return fail(KVQ_EINVAL, "unknown layout %d (or a rotated/unrotated mix)", layout);
+  if (head_dim != 128 && head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", head_dim);
+  if (n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
+  if (!kvq::is_hadamard(kl) && n_recent != 0) return fail(KVQ_EUNSUPPORTED, "n_recent is an option of the Hadamard layouts");
+  if (kl == KVQ_ASYM4_G32 && !k_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
+  if (vl == KVQ_ASYM4_G32 && !v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
+  if ((k_zero && !aligned(k_zero, 16)) || (v_zero && !aligned(v_zero, 16)))
+    return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
+  if (kvq::is_hadamard(kl) && n_recent > 0) {
+    if (!k_recent || !v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
+    if (!aligned(k_recent, 16) || !aligned(v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
+  }
+  v.layout = kl;
+  v.v_layout = vl;
+  v.row_bytes = (int)row_bytes_of(kl, head_dim);
+  v.v_row_bytes = (int)row_bytes_of(vl, head_dim);
+  v.n_recent = kvq::is_hadamard(kl) ? n_recent : 0;
+  return KVQ_OK;
+}
+
 kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
-  if (c->layout < KVQ_Q4_0 || c->layout > kvq::kLastLayout) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
-  if (c->head_dim != 128 && c->head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", c->head_dim);
+  kvq_status st = check_planes(c->layout, c->head_dim, c->n_recent, c->k_zero, c->v_zero, c->k_recent, c->v_recent, v);
+  if (st != KVQ_OK) return st;
   if (c->batch < 1 || c->n_kv_heads < 1 || c->capacity < 1)
     return fail(KVQ_EINVAL, "batch, n_kv_heads and capacity must be >= 1");
-  if (c->n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
-  if (!kvq::is_hadamard(c->layout) && c->n_recent != 0)
-    return fail(KVQ_EUNSUPPORTED, "n_recent is an option of the Hadamard layouts");
   const void *ptrs[] = {c->k_payload, c->v_payload, c->k_scale, c->v_scale};
   for (const void *p : ptrs) {
     if (!p) return fail(KVQ_EINVAL, "payload/scale pointer is NULL");
     if (!aligned(p, 16)) return fail(KVQ_EALIGN, "payload/scale pointer not 16-byte aligned");
   }
-  if (c->layout == KVQ_ASYM4_G32) {
-    if (!c->k_zero || !c->v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
-    if (!aligned(c->k_zero, 16) || !aligned(c->v_zero, 16)) return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
-  }
-  if (kvq::is_hadamard(c->layout) && c->n_recent > 0) {
-    if (!c->k_recent || !c->v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
-    if (!aligned(c->k_recent, 16) || !aligned(c->v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
-  }
-  v.layout = c->layout; v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim; v.cap = c->capacity;
-  v.n_recent = kvq::is_hadamard(c->layout) ? c->n_recent : 0;
-  v.row_bytes = (int)row_bytes_of(c->layout, c->head_dim);
+  v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim; v.cap = c->capacity;
   v.payload[0] = static_cast<uint8_t *>(c->k_payload);
   v.payload[1] = static_cast<uint8_t *>(c->v_payload);
   v.scale[0] = c->k_scale; v.scale[1] = c->v_scale;
@@ -78,8 +99,8 @@ kvq_status check_cache(const kvq_cache *c, kvq::CacheView &v) {
 // Validation of a paged pool and its block table.
 kvq_status check_paged_cache(const kvq_paged_cache *c, kvq::CacheView &v) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
-  if (c->layout < KVQ_Q4_0 || c->layout > kvq::kLastLayout) return fail(KVQ_EINVAL, "unknown layout %d", c->layout);
-  if (c->head_dim != 128 && c->head_dim != 256) return fail(KVQ_ESHAPE, "head_dim %d not 128/256", c->head_dim);
+  kvq_status st = check_planes(c->layout, c->head_dim, c->n_recent, c->k_zero, c->v_zero, c->k_recent, c->v_recent, v);
+  if (st != KVQ_OK) return st;
   if (c->batch < 1 || c->n_kv_heads < 1 || c->n_pages < 1 || c->max_pages_per_seq < 1)
     return fail(KVQ_EINVAL, "batch, n_kv_heads, n_pages and max_pages_per_seq must be >= 1");
   int shift = -1;
@@ -88,26 +109,13 @@ kvq_status check_paged_cache(const kvq_paged_cache *c, kvq::CacheView &v) {
   if (shift < 0) return fail(KVQ_ESHAPE, "page_size %d is not a power of two in [64, 2^20]", c->page_size);
   if ((long long)c->max_pages_per_seq * c->page_size > INT_MAX)
     return fail(KVQ_ECAPACITY, "max_pages_per_seq * page_size exceeds INT_MAX tokens");
-  if (c->n_recent < 0) return fail(KVQ_EINVAL, "n_recent < 0");
-  if (!kvq::is_hadamard(c->layout) && c->n_recent != 0)
-    return fail(KVQ_EUNSUPPORTED, "n_recent is an option of the Hadamard layouts");
   const void *ptrs[] = {c->k_payload, c->v_payload, c->k_scale, c->v_scale, c->block_table};
   for (const void *p : ptrs) {
     if (!p) return fail(KVQ_EINVAL, "payload/scale/block_table pointer is NULL");
     if (!aligned(p, 16)) return fail(KVQ_EALIGN, "payload/scale/block_table pointer not 16-byte aligned");
   }
-  if (c->layout == KVQ_ASYM4_G32) {
-    if (!c->k_zero || !c->v_zero) return fail(KVQ_EINVAL, "zero-point planes are NULL");
-    if (!aligned(c->k_zero, 16) || !aligned(c->v_zero, 16)) return fail(KVQ_EALIGN, "zero plane not 16-byte aligned");
-  }
-  if (kvq::is_hadamard(c->layout) && c->n_recent > 0) {
-    if (!c->k_recent || !c->v_recent) return fail(KVQ_EINVAL, "recent-window planes are NULL");
-    if (!aligned(c->k_recent, 16) || !aligned(c->v_recent, 16)) return fail(KVQ_EALIGN, "window plane not 16-byte aligned");
-  }
-  v.layout = c->layout; v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim;
+  v.B = c->batch; v.H = c->n_kv_heads; v.D = c->head_dim;
   v.cap = c->max_pages_per_seq * c->page_size;
-  v.n_recent = kvq::is_hadamard(c->layout) ? c->n_recent : 0;
-  v.row_bytes = (int)row_bytes_of(c->layout, c->head_dim);
   v.payload[0] = static_cast<uint8_t *>(c->k_payload);
   v.payload[1] = static_cast<uint8_t *>(c->v_payload);
   v.scale[0] = c->k_scale; v.scale[1] = c->v_scale;
@@ -124,8 +132,9 @@ kvq_status check_store(int want_layout, const kvq_cache *cache, const void *k_ne
                        int n_new, int pos0, kvq::CacheView &v) {
   kvq_status st = check_cache(cache, v);
   if (st != KVQ_OK) return st;
-  if (want_layout >= 0 && v.layout != want_layout)
-    return fail(KVQ_EUNSUPPORTED, "cache layout %d does not match this store", v.layout);
+  if (want_layout >= 0 && (v.layout != want_layout || v.v_layout != want_layout))
+    return fail(KVQ_EUNSUPPORTED, "cache layout %d does not match this store (kvq_store takes any layout)",
+                cache->layout);
   if (dtype < KVQ_F32 || dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown dtype %d", dtype);
   if (n_new < 0 || pos0 < 0) return fail(KVQ_EINVAL, "n_new and pos0 must be >= 0");
   if ((long long)pos0 + n_new > v.cap) return fail(KVQ_ECAPACITY, "pos0 + n_new = %lld > capacity %d",
@@ -257,7 +266,7 @@ kvq_status resolve_paged(const kvq_paged_cache *cache, int n_q_heads, int n_q, i
   if (st != KVQ_OK) return st;
   long long work = 0;                                    // body tokens over all sequences and kv heads
   if (total_kv_len > 0) {
-    const long long win = kvq::is_hadamard(cache->layout) ? (long long)cache->n_recent * cache->batch : 0;
+    const long long win = kvq::is_hadamard(cache->layout & 0xFF) ? (long long)cache->n_recent * cache->batch : 0;
     work = (total_kv_len > win ? total_kv_len - win : 1) * cache->n_kv_heads;
   }
   return resolve_core(n_q_heads, n_q, max_kv_len, causal, 0, true, chunk, a, need, ws, work);
@@ -310,6 +319,10 @@ kvq_status kvq_store_hadamard_int2(const kvq_cache *cache, const void *k_new, co
                                    int32_t n_new, int32_t pos0, kvq_stream_t stream) {
   return store_common(KVQ_HAD_INT2, cache, k_new, v_new, dtype, n_new, pos0, stream);
 }
+kvq_status kvq_store(const kvq_cache *cache, const void *k_new, const void *v_new, int32_t dtype, int32_t n_new,
+                     int32_t pos0, kvq_stream_t stream) {
+  return store_common(-1, cache, k_new, v_new, dtype, n_new, pos0, stream);
+}
 
 size_t kvq_attend_workspace_bytes(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t kv_len,
                                   int32_t chunk) {
@@ -361,7 +374,10 @@ kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype
 // Phase 1 (tensor-core or CUDA-core kernel) and phase 2 on `s`, with the optional phase-1 events.
 cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool events) {
   cudaError_t e = cudaSuccess;
-  const bool mma = kvq::mma_supported(a);
+  // the tensor-core kernels are built for one layout in both planes; a mixed cache takes the
+  // CUDA-core kernel
+  const bool uniform = a.cache.layout == a.cache.v_layout;
+  const bool mma = uniform && kvq::mma_supported(a);
   a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);   // the decode tensor-core kernels cover the body chunks only
   // the tensor-core kernels prepare the Hadamard query themselves; the CUDA-core one reads it
   if (kvq::is_hadamard(a.cache.layout) && !mma) {

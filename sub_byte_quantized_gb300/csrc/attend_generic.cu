@@ -42,26 +42,27 @@ __device__ __forceinline__ void chunk_range(const AttendArgs &a, const SeqLen &s
 // For the Hadamard layouts the raw signed codes are produced (the per-token scale is applied by
 // the caller).
 __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, int gi, float out[8]) {
-  const uint8_t *p = c.payload[kv] + row * (size_t)c.row_bytes;
+  const int layout = kv ? c.v_layout : c.layout;          // each plane's own layout (mixed K/V)
+  const uint8_t *p = c.payload[kv] + row * (size_t)(kv ? c.v_row_bytes : c.row_bytes);
   const int blk = gi >> 2, sub = gi & 3;
-  if (c.layout == KVQ_HAD_INT4) {
+  if (layout == KVQ_HAD_INT4) {
     const uint32_t w = *reinterpret_cast<const uint32_t *>(p + gi * 4);
 #pragma unroll
     for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8);
     return;
   }
-  if (c.layout == KVQ_HAD_INT2) {                       // four 2-bit fields per byte, (v ^ 2) - 2
+  if (layout == KVQ_HAD_INT2) {                       // four 2-bit fields per byte, (v ^ 2) - 2
     const uint32_t w = *reinterpret_cast<const uint16_t *>(p + gi * 2);
 #pragma unroll
     for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (2 * i)) & 0x3u ^ 0x2u) - 2);
     return;
   }
   const float s = __half2float(static_cast<const __half *>(c.scale[kv])[row * (c.D / kBlock) + blk]);
-  if (c.layout == KVQ_Q4_0) {
+  if (layout == KVQ_Q4_0) {
     const uint32_t w = *reinterpret_cast<const uint32_t *>(p + blk * 16 + sub * 4);
 #pragma unroll
     for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (4 * i)) & 0xFu ^ 0x8u) - 8) * s;
-  } else if (c.layout == KVQ_Q6_0) {
+  } else if (layout == KVQ_Q6_0) {
     const uint32_t lo = *reinterpret_cast<const uint32_t *>(p + blk * 24 + sub * 4);
     const uint32_t hi = *reinterpret_cast<const uint16_t *>(p + blk * 24 + 16 + sub * 2);
 #pragma unroll
@@ -69,7 +70,7 @@ __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, 
       const uint32_t v = ((lo >> (4 * i)) & 0xFu) | (((hi >> (2 * i)) & 0x3u) << 4);
       out[i] = (float)((int)(v ^ 0x20u) - 0x20) * s;
     }
-  } else if (c.layout == KVQ_Q8_0) {                    // byte i = value i, (v ^ 0x80) - 0x80
+  } else if (layout == KVQ_Q8_0) {                    // byte i = value i, (v ^ 0x80) - 0x80
     const uint2 w = *reinterpret_cast<const uint2 *>(p + blk * 32 + sub * 8);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

@@ -53,8 +53,9 @@ __host__ __device__ constexpr bool prefill_shape(int layout, int D, int rows) {
 // the block table [B][table_stride] (page = 1 << page_shift tokens, at least 64; cap is then the
 // logical capacity of one sequence, table_stride pages). The ring is per sequence either way.
 struct CacheView {
-  int layout, B, H, D, cap, n_recent;
+  int layout, B, H, D, cap, n_recent;      // layout: the K plane's (and, unless mixed, V's)
   int row_bytes;
+  int v_layout, v_row_bytes;               // the V plane's layout and row bytes
   uint8_t *payload[2];
   void *scale[2];
   __half *zero[2];

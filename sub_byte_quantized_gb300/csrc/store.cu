@@ -19,6 +19,8 @@ constexpr float kF16Max = 65504.0f;
 struct StoreGeom {
   int B, H, D, cap, n_new, pos0, row_bytes, nb;
   long long rows_per_tensor;   // B * H * n_new
+  long long n_rows;            // rows of this launch: both planes (2 * rows_per_tensor) or one
+  int kv_only;                 // -1: K and V in one launch; 0 / 1: this launch covers that plane only
   // per-sequence first position seq_pos[b] + pos_offset (device), or nullptr: pos0 for every one
   const int32_t *seq_pos;
   int pos_offset;
@@ -29,8 +31,8 @@ struct StoreGeom {
 // host could not check; such a row is computed but not written.
 __device__ __forceinline__ bool row_coords(const CacheView &c, const StoreGeom &g, long long r, int &kv,
                                            long long &in_row, long long &crow, int &j, int &pos, long long &bh) {
-  kv = r >= g.rows_per_tensor ? 1 : 0;
-  const long long rr = r - (long long)kv * g.rows_per_tensor;
+  kv = g.kv_only >= 0 ? g.kv_only : (r >= g.rows_per_tensor ? 1 : 0);
+  const long long rr = g.kv_only >= 0 ? r : r - (long long)kv * g.rows_per_tensor;
   bh = rr / g.n_new;
   j = (int)(rr - bh * g.n_new);
   in_row = rr;
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
   const int tr = (int)(gt - r * tpr);                      // thread within row
   // Threads past the last row still take part in the quad shuffles (full-warp masks) but load
   // and store nothing.
-  bool valid = r < 2 * g.rows_per_tensor;
+  bool valid = r < g.n_rows;
   int kv = 0, j = 0, pos = 0;
   long long in_row = 0, crow = 0, bh = 0;
   if (valid) valid = row_coords(c, g, r, kv, in_row, crow, j, pos, bh);
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
 #endif
   const int lane = threadIdx.x & 31;
   const long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (r >= 2 * g.rows_per_tensor) return;                  // whole warp exits together
+  if (r >= g.n_rows) return;                               // whole warp exits together
   int kv, j, pos;
   long long in_row, crow, bh;
   if (!row_coords(c, g, r, kv, in_row, crow, j, pos, bh)) return;   // whole warp (one row)
@@ -216,17 +218,15 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
 
 }  // namespace
 
-cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype, int n_new,
-                         int pos0, cudaStream_t st, const int32_t *seq_pos, int pos_offset) {
-  StoreGeom g;
-  g.B = c.B; g.H = c.H; g.D = c.D; g.cap = c.cap; g.n_new = n_new; g.pos0 = pos0;
-  g.seq_pos = seq_pos; g.pos_offset = pos_offset;
-  g.row_bytes = c.row_bytes; g.nb = c.D / kBlock;
-  g.rows_per_tensor = (long long)c.B * c.H * n_new;
-  const long long rows = 2 * g.rows_per_tensor;
-  if (is_hadamard(c.layout)) {
+namespace {
+
+// One launch of the store kernel for `layout` over both planes (kv_only < 0) or one plane.
+cudaError_t launch_store_plane(const CacheView &c, int layout, const void *k_new, const void *v_new, int dtype,
+                               StoreGeom g, cudaStream_t st) {
+  const long long rows = g.n_rows;
+  if (is_hadamard(layout)) {
     const unsigned blocks = (unsigned)((rows * 32 + 255) / 256);
-    const bool two = c.layout == KVQ_HAD_INT2;
+    const bool two = layout == KVQ_HAD_INT2;
     if (c.D == 128) {
       if (two) store_had_kernel<4, 2><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
       else store_had_kernel<4, 4><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g);
@@ -237,7 +237,7 @@ cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_ne
   } else {
     const long long threads = rows * (c.D / 8);
     const unsigned blocks = (unsigned)((threads + 255) / 256);
-    switch (c.layout) {
+    switch (layout) {
       case KVQ_Q4_0: store_block_kernel<KVQ_Q4_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
       case KVQ_Q6_0: store_block_kernel<KVQ_Q6_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
       case KVQ_Q8_0: store_block_kernel<KVQ_Q8_0><<<blocks, 256, 0, st>>>(c, k_new, v_new, dtype, g); break;
@@ -245,6 +245,32 @@ cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_ne
     }
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype, int n_new,
+                         int pos0, cudaStream_t st, const int32_t *seq_pos, int pos_offset) {
+  StoreGeom g;
+  g.B = c.B; g.H = c.H; g.D = c.D; g.cap = c.cap; g.n_new = n_new; g.pos0 = pos0;
+  g.seq_pos = seq_pos; g.pos_offset = pos_offset;
+  g.nb = c.D / kBlock;
+  g.rows_per_tensor = (long long)c.B * c.H * n_new;
+  if (c.layout == c.v_layout) {                          // one launch for K and V
+    g.row_bytes = c.row_bytes;
+    g.n_rows = 2 * g.rows_per_tensor;
+    g.kv_only = -1;
+    return launch_store_plane(c, c.layout, k_new, v_new, dtype, g, st);
+  }
+  // mixed K/V precision: one launch per plane, each with its own layout
+  g.n_rows = g.rows_per_tensor;
+  g.kv_only = 0;
+  g.row_bytes = c.row_bytes;
+  cudaError_t e = launch_store_plane(c, c.layout, k_new, v_new, dtype, g, st);
+  if (e != cudaSuccess) return e;
+  g.kv_only = 1;
+  g.row_bytes = c.v_row_bytes;
+  return launch_store_plane(c, c.v_layout, k_new, v_new, dtype, g, st);
 }
 
 }  // namespace kvq

@@ -182,3 +182,22 @@ def test_paged_validation_without_device(L):
     auto_max = L.kvq_paged_attend_chunk(p(big), 8, 1, 131072, 0, 0)
     auto_tot = L.kvq_paged_attend_chunk(p(big), 8, 1, 131072, 40000, 0)
     assert auto_tot % 64 == 0 and 64 <= auto_tot <= auto_max
+
+
+def test_mixed_layout_validation(L):
+    from sub_byte_quantized_gb300._lib import KvqCache, mixed
+    p = C.byref
+    ok = KvqCache(mixed(0, 4), 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, None, None, None)
+    # a per-layout store refuses a mixed cache (kvq_store takes any layout)
+    assert L.kvq_store_q4_0(p(ok), 16, 16, 1, 1, 0, None) == 4
+    assert b"kvq_store" in L.kvq_last_error()
+    # a rotated K with an unrotated V, an unknown V layout
+    bad = KvqCache(mixed(2, 0), 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, None, None, None)
+    assert L.kvq_store(p(bad), 16, 16, 1, 1, 0, None) == 1
+    bad = KvqCache(mixed(0, 9), 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, None, None, None)
+    assert L.kvq_store(p(bad), 16, 16, 1, 1, 0, None) == 1
+    # an asymmetric V plane needs its zero-point plane even when K has none
+    za = KvqCache(mixed(0, 3), 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, None, None, None)
+    assert L.kvq_store(p(za), 16, 16, 1, 1, 0, None) == 1
+    za = KvqCache(mixed(0, 3), 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, 4096, None, None)
+    assert L.kvq_store(p(za), 16, 16, 1, 10, 60, None) == 3          # valid planes, capacity error

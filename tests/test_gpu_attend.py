@@ -294,3 +294,16 @@ def test_q8_0_and_int2(layout, D, gqa, n_q, causal, n_recent, chunk):
     w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, head_dim=D, batch=2, n_kv_heads=2,
                                               n_q_heads=2 * gqa, n_recent=n_recent, causal=causal)
     run_case(w, kv_len=1100, n_q=n_q, chunk=chunk, fill=1100 - max(n_q, 1))
+
+
+@pytest.mark.parametrize("layout,n_recent", [
+    ("q4_0+q8_0", 0), ("q4_0+q6_0", 0), ("asym4_g32+q8_0", 0), ("q8_0+q4_0", 0), ("q6_0+asym4_g32", 0),
+    ("had_int4+had_int2", 32), ("had_int2+had_int4", 64),
+])
+@pytest.mark.parametrize("n_q,causal", [(1, False), (24, True)])
+def test_mixed_kv_precision(layout, n_recent, n_q, causal):
+    """Mixed K/V precision: each plane stored bit-exactly in its own layout, attention within
+    tolerance of the oracle; decode (GQA 4) and causal prefill rows."""
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=2, n_kv_heads=2, n_q_heads=8,
+                                              n_recent=n_recent, causal=causal)
+    run_case(w, kv_len=900, n_q=n_q, chunk=128, fill=900 - n_q)

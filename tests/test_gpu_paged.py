@@ -115,6 +115,7 @@ def _decode_w(layout, D=128, gqa=4, n_recent=0, causal=False):
     ("q6_0", 128, 64, 128, 0),
     ("q8_0", 128, 64, 0, 0),
     ("had_int2", 128, 64, 0, 128),
+    ("q4_0+q8_0", 128, 64, 0, 0),         # mixed K/V precision
 ])
 def test_paged_decode(layout, D, page, chunk, n_recent):
     """Decode (one query row, GQA 4) over ragged sequences, one of them empty, one shorter than a

@@ -123,3 +123,25 @@ def test_store_full_128k_sampled(name):
         if "zero" in planes:
             assert np.array_equal(dc.planes[t]["zero"][:, :, toks].cpu().numpy().view(np.uint16),
                                   planes["zero"].view(np.uint16))
+
+
+@pytest.mark.parametrize("layout", ["q4_0+q8_0", "asym4_g32+q6_0", "had_int4+had_int2"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_store_mixed_bit_exact(layout, dtype):
+    """A mixed K/V cache: one launch per plane, each plane bit-identical to the oracle's."""
+    rng = np.random.default_rng(zlib.crc32(f"{layout}/{dtype}".encode()))
+    B, H, D, cap, pos0, n = 2, 3, 128, 64, 5, 37
+    k = special_rows(rng, B * H * n, D).reshape(B, H, n, D)
+    v = rng.standard_t(3, (B, H, n, D)).astype(np.float32)
+    tdt = torch.float32
+    if dtype == "bf16":
+        k = torch.from_numpy(k).to(torch.bfloat16).float().numpy()
+        v = torch.from_numpy(v).to(torch.bfloat16).float().numpy()
+        tdt = torch.bfloat16
+    n_recent = 16 if layout.startswith("had") else 0
+    dc = kvq.KVCache(layout, B, H, D, cap, n_recent=n_recent)
+    oc = OA.OracleCache(layout, B, H, D, cap, n_recent=n_recent)
+    kvq.store(dc, torch.from_numpy(k).to(tdt).cuda(), torch.from_numpy(v).to(tdt).cuda(), pos0)
+    oc.store(k, v, pos0)
+    torch.cuda.synchronize()
+    planes_equal(dc, oc)
