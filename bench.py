@@ -64,6 +64,12 @@ DESCRIPTIONS = {
                              "x10, N(0,1) Q), B1 Hq64 Hkv8 D128",
     "c5_asym4_g32_llama70b_128k": "Llama-3.1-70B layer, 128K context, per-group asymmetric int4 g=32 KV, "
                                   "B1 Hq64 Hkv8 D128",
+    "c5_q8_0_llama70b_128k": "Llama-3.1-70B layer, 128K context, Q8_0 KV (8-bit codes, fp16 scale per 32 values), "
+                             "B1 Hq64 Hkv8 D128",
+    "c5_q4_0_k_q8_0_v_llama70b_128k": "Llama-3.1-70B layer, 128K context, mixed K/V precision: Q4_0 keys, Q8_0 values, "
+                                      "B1 Hq64 Hkv8 D128",
+    "c3_had_int2_decode_w256": "Hadamard per-token int2 body + 256-token exact-f32 window, Qwen3-1.7B shape: B8 Hq16 "
+                               "Hkv8 D128 S4096",
     "paged_q4_0_llama3_8b_ragged": "Paged Q4_0 pool, Llama-3-8B layer shapes (Hq32 Hkv8 D128): 16 sequences with seeded "
                                    "lengths 1024-16384 (116139 tokens), 64-token pages shuffled in the pool; append 1 "
                                    "token per sequence then attend over each sequence's own length",
@@ -211,13 +217,16 @@ class Spec:
         self.n_q = inp["q"].shape[2]
         self.causal = w.causal
         self.q_pos0 = self.S - self.n_q if w.causal else 0
-        self.n_win = min(w.n_recent, self.S) if w.layout == "had_int4" else 0
+        kl, _, vl = w.layout.partition("+")
+        planes = (kl, vl or kl)                           # each plane's layout (mixed K/V precision)
+        self.n_win = min(w.n_recent, self.S) if kl.startswith("had") else 0
         nb = self.D // 32
         row = {"q4_0": 16 * nb + 2 * nb, "q6_0": 24 * nb + 2 * nb, "asym4_g32": 16 * nb + 4 * nb,
-               "had_int4": self.D // 2 + 4}[w.layout]
+               "q8_0": 32 * nb + 2 * nb, "had_int4": self.D // 2 + 4, "had_int2": self.D // 4 + 4}
         # algorithmic bytes one attention call reads: every packed K/V row (+ scales) once; window
         # tokens as their exact f32 rows
-        self.read_bytes = 2 * self.B * self.H * ((self.S - self.n_win) * row + self.n_win * self.D * 4)
+        self.read_bytes = self.B * self.H * sum((self.S - self.n_win) * row[p] + self.n_win * self.D * 4
+                                                for p in planes)
         # algorithmic flops of the attention call: QK and PV over every visible (row, token) pair
         vis = 0
         for i in range(self.n_q):
@@ -575,8 +584,10 @@ def main():
                  "phase1_pass_us_per_step": ev_pass_ms / K * 1e3})
     # store, phase 1, reduce; the CUDA-core phase 1 (D=256, Q6_0, more than 8 query rows per kv
     # head) adds the Hadamard query preparation
+    kl, _, vl = w.layout.partition("+")
+    mixed = bool(vl) and vl != kl                      # mixed K/V precision: one store launch per plane
     tensor_core = w.layout in ("q4_0", "asym4_g32", "had_int4") and D == 128 and w.gqa * spec.n_q <= 8
-    launches = 3 + (1 if w.layout == "had_int4" and not tensor_core else 0)
+    launches = (2 if mixed else 1) + 2 + (1 if kl.startswith("had") and not tensor_core else 0)
     l2_note = (f"cache L2-resident ({n_rep} replicas x {cache_bytes / 2**20:.1f} MiB)" if l2_resident else
                f"inputs larger than L2: {n_rep} cache replicas rotated ({n_rep * cache_bytes / 2**20:.0f} MiB > "
                f"{L2_BYTES / 2**20:.0f} MiB L2)")

@@ -123,6 +123,15 @@ WORKLOADS = {
     # same shape, per-group asymmetric int4 (g=32, fp16 scale + zero-point).
     "c5_asym4_g32_llama70b_128k": Workload("c5_asym4_g32_llama70b_128k", "asym4_g32", 1, 64, 8, 128, 131072,
                                            fill=131071, n_outlier=4, outlier_factor=10.0, seed=1005),
+    # the 128K layer in Q8_0 (8-bit codes, fp16 scale per 32 values) and with mixed precision
+    # (4-bit Q4_0 keys, 8-bit Q8_0 values: V errors reach the output directly)
+    "c5_q8_0_llama70b_128k": Workload("c5_q8_0_llama70b_128k", "q8_0", 1, 64, 8, 128, 131072, fill=131071,
+                                      n_outlier=4, outlier_factor=10.0, seed=1005),
+    "c5_q4_0_k_q8_0_v_llama70b_128k": Workload("c5_q4_0_k_q8_0_v_llama70b_128k", "q4_0+q8_0", 1, 64, 8, 128, 131072,
+                                               fill=131071, n_outlier=4, outlier_factor=10.0, seed=1005),
+    # the Hadamard decode cache with a 2-bit body and a 256-token exact-f32 window
+    "c3_had_int2_decode_w256": Workload("c3_had_int2_decode_w256", "had_int2", 8, 16, 8, 128, 4096, fill=4095,
+                                        n_recent=256, n_outlier=4, outlier_factor=10.0, seed=1003),
     # serving-style paged batch of a Llama-3-8B layer (32/8 heads, d128), Q4_0: 16 sequences with
     # seeded lengths in [1024, 16384], 64-token pages in a shuffled pool; decode: one new token per
     # sequence, then attention over each sequence's own length.
