@@ -172,7 +172,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
   if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
     const long long ctas = (long long)sms * kvq::kMmaQ6CtasPerSm(c.D);
     chunk = ((work + ctas - 1) / ctas + 63) / 64 * 64;
-  } else if (kvq::prefill_shape(c.layout, c.D, rows)) {
+  } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows)) {
     // row-side kernel: CTAs of 64 query rows; split the body into enough chunks for about four
     // waves of resident CTAs
     const long long row_ctas = (long long)((rows + kvq::kPrefillRows - 1) / kvq::kPrefillRows) * n_heads;
@@ -374,10 +374,7 @@ kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype
 // Phase 1 (tensor-core or CUDA-core kernel) and phase 2 on `s`, with the optional phase-1 events.
 cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool events) {
   cudaError_t e = cudaSuccess;
-  // the tensor-core kernels are built for one layout in both planes; a mixed cache takes the
-  // CUDA-core kernel
-  const bool uniform = a.cache.layout == a.cache.v_layout;
-  const bool mma = uniform && kvq::mma_supported(a);
+  const bool mma = kvq::mma_supported(a);
   a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);   // the decode tensor-core kernels cover the body chunks only
   // the tensor-core kernels prepare the Hadamard query themselves; the CUDA-core one reads it
   if (kvq::is_hadamard(a.cache.layout) && !mma) {

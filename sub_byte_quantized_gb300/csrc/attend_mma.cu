@@ -680,8 +680,9 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
 
 bool mma_supported(const AttendArgs &a) {
   const int L = a.cache.layout;
+  if (prefill_supported(a)) return true;                 // includes the mixed K/V pairs it is built for
+  if (a.cache.v_layout != L) return false;               // the decode kernels: one layout in both planes
   if (L == KVQ_Q6_0) return mma_q6_supported(a);
-  if (prefill_supported(a)) return true;
   return (L == KVQ_Q4_0 || L == KVQ_ASYM4_G32 || L == KVQ_HAD_INT4) && a.cache.D == kD && a.gqa * a.n_q <= 8 &&
          a.n_body > 0 && a.chunk % kStage == 0;
 }

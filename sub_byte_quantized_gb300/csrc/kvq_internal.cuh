@@ -43,9 +43,22 @@ constexpr int kPrefillCtasPerSm = 3;
 #ifndef KVQ_PREFILL_BLOCK_LAYOUTS
 #define KVQ_PREFILL_BLOCK_LAYOUTS 1
 #endif
-__host__ __device__ constexpr bool prefill_shape(int layout, int D, int rows) {
-  return (layout == KVQ_HAD_INT4 || (KVQ_PREFILL_BLOCK_LAYOUTS && (layout == KVQ_Q4_0 || layout == KVQ_ASYM4_G32))) &&
-         D == 128 && rows > 8;
+// (K layout, V layout) pairs the row-side kernel is built for: one layout of Q4_0, asym, Q8_0,
+// Hadamard int4 / int2 in both planes, or the mixed pairs 4-bit keys + Q8_0 values and int2 key
+// body + int4 value body.
+__host__ __device__ constexpr bool prefill_pair(int kl, int vl) {
+  return (kl == vl && (kl == KVQ_HAD_INT4 || kl == KVQ_HAD_INT2 || kl == KVQ_Q8_0 ||
+                       (KVQ_PREFILL_BLOCK_LAYOUTS && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32)))) ||
+         (vl == KVQ_Q8_0 && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32)) || (kl == KVQ_HAD_INT2 && vl == KVQ_HAD_INT4);
+}
+// Pairs with a decode kernel of their own (at most eight query rows per kv head).
+__host__ __device__ constexpr bool decode_kernel(int kl, int vl) {
+  return kl == vl && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32 || kl == KVQ_HAD_INT4);
+}
+// The row-side kernel takes many query rows per kv head, and every row count of the pairs that
+// have no decode kernel.
+__host__ __device__ constexpr bool prefill_shape(int kl, int vl, int D, int rows) {
+  return D == 128 && prefill_pair(kl, vl) && (rows > 8 || !decode_kernel(kl, vl));
 }
 
 // Device-side view of a cache; index 0 = K, 1 = V. Rows of the payload / scale / zero planes:
@@ -137,6 +150,7 @@ cudaError_t launch_attend_mma_q6(const AttendArgs &a, cudaStream_t st);
 // causal prefill chunks), Hadamard int4 layout.
 bool prefill_supported(const AttendArgs &a);
 cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st);
+cudaError_t launch_attend_prefill_mixed(const AttendArgs &a, cudaStream_t st);
 
 // ----------------------------------------------------------------- device helpers
 // Programmatic dependent launch: wait for the preceding kernel (and its memory) when this CTA

@@ -147,5 +147,26 @@ __device__ __forceinline__ void unpack8_u4(uint32_t w, uint32_t (&o)[4]) {
   o[3] = hfma2(lop3<0xEA>(w8, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
 }
 
+// Signed 8-bit fields: a = values v0..v3, b = v4..v7 (byte i = value i, two's complement) ->
+// four exact f16 pairs (v0,v4), (v1,v5), (v2,v6), (v3,v7). The two bytes of a pair are placed
+// under the exponent of 1024 with the sign bit flipped (1024 + v + 128), then 1152 is removed.
+__device__ __forceinline__ void unpack8_s8(uint32_t a, uint32_t b, uint32_t (&o)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = prmt(a, b, (uint32_t)(((4 + i) << 8) | i));
+    o[i] = hadd2(lop3<0x6A>(t, 0x00FF00FFu, 0x64806480u), 0xE480E480u);
+  }
+}
+
+// Signed 2-bit fields f0..f7 in the low 16 bits of h (field i at bits 2i, code (f ^ 2) - 2) ->
+// four exact f16 pairs (c0,c4), (c1,c5), (c2,c6), (c3,c7): the fields' two bytes go to the two
+// 16-bit lanes, each pair is masked under the exponent of 1024 with bit 1 flipped, then 1026 is
+// removed.
+__device__ __forceinline__ void unpack8_s2(uint32_t h, uint32_t (&o)[4]) {
+  const uint32_t x = prmt(h, 0u, 0x4140u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = hadd2(lop3<0x6A>(x >> (2 * i), 0x00030003u, 0x64026402u), 0xE402E402u);
+}
+
 }  // namespace mma
 }  // namespace kvq
