@@ -20,11 +20,11 @@ Readings of points the pages leave open (each one a single constant or step here
       q = rint((x - zero) / scale) clamped to [0, 15], stored unsigned.
   R17 all-zero block (or a scale that rounds to fp16 zero) -> every code 0; fp16 scales and
       zeros saturate at +-65504; -0.0 quantises to code 0. Non-finite inputs are unspecified.
-  R22 Q8_0 (the pages give only its density, 1.0625 bytes/element): per 32 values 32 int8 code
+  R24 Q8_0 (the pages give only its density, 1.0625 bytes/element): per 32 values 32 int8 code
       bytes and one fp16 scale; by the family rule of R4/R5 (magnitude 2^(bits-1)) scale =
       amax / 128 and codes clamped to [-128, 127], byte i = value i in two's complement, read
       back as (v ^ 0x80) - 0x80.
-  R23 Hadamard int2 (the body below four bits that needs the exact-f32 window): the int4 layout
+  R25 Hadamard int2 (the body below four bits that needs the exact-f32 window): the int4 layout
       of R7 with two bits: symmetric, zero-point free, scale = amax / 1, codes in [-1, 1]; four
       codes per byte, value 4j+i at bits 2i..2i+1 of byte j (two's complement), read back as
       (v ^ 2) - 2.
@@ -315,7 +315,7 @@ def dequantize_asym4_g32(payload: np.ndarray, scale: np.ndarray, zero: np.ndarra
 
 # ------------------------------------------------------------------ Q8_0
 def quantize_q8_0(x: np.ndarray):
-    """Q8_0 (R22): per 32 values d = amax / 128 stored as fp16 (R3), q = clamp(rint(x / d),
+    """Q8_0 (R24): per 32 values d = amax / 128 stored as fp16 (R3), q = clamp(rint(x / d),
     -128, 127) (R1, R2), byte i of the block = q_i as a two's-complement byte.
 
     Returns (payload uint8 [..., 32 * nb], scale float16 [..., nb]).
@@ -332,7 +332,7 @@ def quantize_q8_0(x: np.ndarray):
 
 
 def read_q8_0(v: np.ndarray) -> np.ndarray:
-    """Read-side sign extension of a Q8_0 byte: (v ^ 0x80) - 0x80 (R22)."""
+    """Read-side sign extension of a Q8_0 byte: (v ^ 0x80) - 0x80 (R24)."""
     v = np.asarray(v).astype(np.int32)
     return (v ^ 0x80) - 0x80
 
@@ -346,7 +346,7 @@ def dequantize_q8_0(payload: np.ndarray, scale: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------------------ Hadamard int2
 def pack_pairs_of_bits(f: np.ndarray) -> np.ndarray:
-    """Four 2-bit fields per byte: field 4j+i at bits 2i..2i+1 of byte j (R23)."""
+    """Four 2-bit fields per byte: field 4j+i at bits 2i..2i+1 of byte j (R25)."""
     f = np.asarray(f, dtype=np.uint8) & 0x3
     D = f.shape[-1]
     pad = (-D) % 4
@@ -364,7 +364,7 @@ def unpack_pairs_of_bits(b: np.ndarray, count: int) -> np.ndarray:
 
 
 def quantize_hadamard_int2(x: np.ndarray):
-    """Per-token symmetric int2 in the Hadamard basis (R23; tract discussion #2402, "Why this quant
+    """Per-token symmetric int2 in the Hadamard basis (R25; tract discussion #2402, "Why this quant
     scheme" and "Causality & mixed precision": int2 is usable only with the exact-f32 window).
 
     y = rotate(x); s = amax(|y|) (float32); q = clamp(rint(y / s), -1, 1); four codes per byte.
@@ -379,7 +379,7 @@ def quantize_hadamard_int2(x: np.ndarray):
 
 
 def read_int2(v: np.ndarray) -> np.ndarray:
-    """Read-side sign extension of a 2-bit field: (v ^ 2) - 2 (R23)."""
+    """Read-side sign extension of a 2-bit field: (v ^ 2) - 2 (R25)."""
     v = np.asarray(v).astype(np.int32)
     return (v ^ 0x2) - 0x2
 

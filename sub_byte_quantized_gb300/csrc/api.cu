@@ -172,6 +172,15 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
   if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
     const long long ctas = (long long)sms * kvq::kMmaQ6CtasPerSm(c.D);
     chunk = ((work + ctas - 1) / ctas + 63) / 64 * 64;
+  } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) && rows <= 16 &&
+             !kvq::decode_kernel(c.layout, c.v_layout)) {
+    // row-side kernel in its decode form (one row block, the warps split the tokens): one chunk per
+    // resident CTA, as many chunks per (batch, kv head) as fit one wave
+    const long long ctas = (long long)sms * (kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2);
+    long long per_head = ctas / (n_heads > 0 ? n_heads : 1);
+    if (per_head < 1) per_head = 1;
+    const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
+    chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
   } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows)) {
     // row-side kernel: CTAs of 64 query rows; split the body into enough chunks for about four
     // waves of resident CTAs

@@ -411,7 +411,7 @@ def test_recent_window_semantics():
     assert np.linalg.norm(out_w - ref) < np.linalg.norm(out_0 - ref)   # ... towards exact attention
 
 
-# ------------------------------------------------------------------ Q8_0 (reading R22)
+# ------------------------------------------------------------------ Q8_0 (reading R24)
 def test_q8_0_density_is_the_pages():
     D = 128
     q8 = (Q.row_bytes("q8_0", D) + Q.param_bytes("q8_0", D)) / D
@@ -454,7 +454,7 @@ def test_q8_0_half_even_and_zero_block():
     assert not p[1].any() and float(s[1, 0]) == 0.0
 
 
-# ------------------------------------------------------------------ Hadamard int2 (reading R23)
+# ------------------------------------------------------------------ Hadamard int2 (reading R25)
 def test_int2_read_formula_every_field():
     # the four 2-bit fields through (v ^ 2) - 2: 0 -> 0, 1 -> 1, 2 -> -2, 3 -> -1
     assert [int(Q.read_int2(v)) for v in range(4)] == [0, 1, -2, -1]
