@@ -133,12 +133,24 @@ __device__ __forceinline__ void unpack_plane(const uint8_t *pay, const uint8_t *
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int e = 0; e < P::CPP; ++e) {
-      const int ch = q * P::CPP + e;                      // chunk: dims 8 ch .. 8 ch + 7
+      // 8- and 2-bit rows: half of the lanes of each 8-lane store phase take their chunks in a
+      // rotated order, so that the phase's eight 16-byte stores land in eight distinct bank groups
+      // of the swizzled tile (in plain order they would pair up: a 2-way conflict)
+      int ee = e;
+      if constexpr (P::BITS == 8) ee = e ^ ((q >> 2) & 1);
+      if constexpr (P::BITS == 2) ee = e ^ (q << 2);
+      const int ch = q * P::CPP + ee;                     // chunk: dims 8 ch .. 8 ch + 7
       uint32_t o[4];
-      if constexpr (P::BITS == 8) unpack8_s8(ws[2 * e], ws[2 * e + 1], o);
-      else if constexpr (P::BITS == 2) unpack8_s2(ws[e >> 1] >> (16 * (e & 1)), o);
-      else if constexpr (P::ASYM) unpack8_u4(ws[e], o);
-      else unpack8_q4(ws[e], o);
+      if constexpr (P::BITS == 8) {
+        unpack8_s8(ee ? ws[2] : ws[0], ee ? ws[3] : ws[1], o);
+      } else if constexpr (P::BITS == 2) {
+        const uint32_t wd = q ? ws[(e >> 1) ^ 2] : ws[e >> 1];
+        unpack8_s2(wd >> (16 * (e & 1)), o);
+      } else if constexpr (P::ASYM) {
+        unpack8_u4(ws[e], o);
+      } else {
+        unpack8_q4(ws[e], o);
+      }
       const uint32_t off = toff(row, ch);
       if constexpr (P::HAD) {
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(tile + off),
