@@ -844,7 +844,8 @@ def paged_main(args):
     hbm_peak, _, peak_kind = measured_peaks()
     achieved = read_bytes / (ph_mean / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-            "peak_kind": peak_kind, "traffic": None, "kernel": "attend phase 1 (split-K chunk partials), paged",
+            "peak_kind": peak_kind, "traffic": kernel_traffic("attend_phase1_paged_q4_0_ragged.md", "attend_mma.cu"),
+            "kernel": "attend phase 1 (split-K chunk partials), paged",
             "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
             "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3, "phase1_pass_us_per_step": ev_pass_ms / K * 1e3}
     line = {
