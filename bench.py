@@ -775,7 +775,8 @@ def paged_main(args):
     pools = [make_pool(w.seed + r) for r in range(n_rep)]
     del kp, vp
     torch.cuda.empty_cache()
-    chunk = kvq.paged_attend_chunk(pools[0], Hq, 1, S_max, total)
+    chunk = kvq.paged_attend_plan_chunk(pools[0], Hq, 1, lens)          # balanced from the host lengths
+    chunk_tot = kvq.paged_attend_chunk(pools[0], Hq, 1, S_max, total)   # from the total length only
     chunk_max = kvq.paged_attend_chunk(pools[0], Hq, 1, S_max, 0)
     ws = torch.empty(max(256, kvq.paged_attend_workspace_bytes(pools[0], Hq, 1, S_max, chunk)), dtype=torch.uint8,
                      device=dev)
@@ -855,8 +856,9 @@ def paged_main(args):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": DESCRIPTIONS[args.workload], "name": args.workload, "layout": w.layout,
                    "sequences": B, "seq_lens": [int(x) for x in lens], "total_tokens": total, "page_size": P,
-                   "pool_pages": n_pages, "chunk": chunk, "chunk_rule": "kvq_paged_attend_chunk with the batch's "
-                   f"total length (max-length rule: {chunk_max})",
+                   "pool_pages": n_pages, "chunk": chunk, "chunk_rule": "kvq_paged_attend_plan_chunk from the host "
+                   "lengths: the shortest chunk whose equal per-sequence chunks fit one wave "
+                   f"(total-length rule: {chunk_tot}, max-length rule: {chunk_max})",
                    "step": "append 1 token per sequence (K,V) + split-K attention over each sequence's length, "
                            "one library call",
                    "read_bytes_per_step": read_bytes, "flops_per_step": flops,
@@ -885,8 +887,11 @@ def paged_main(args):
                 ev1.record(stream)
             torch.cuda.synchronize(dev)
             return ev0.elapsed_time(ev1) / n
-        t_tot, t_max = plain(chunk, ws), plain(chunk_max, ws_m)
-        line["variants"] = {"total_length_chunk": {"chunk": chunk, "us_per_layer": t_tot * 1e3,
+        ws_t = torch.empty(max(256, kvq.paged_attend_workspace_bytes(pools[0], Hq, 1, S_max, chunk_tot)),
+                           dtype=torch.uint8, device=dev)
+        t_plan, t_tot, t_max = plain(chunk, ws), plain(chunk_tot, ws_t), plain(chunk_max, ws_m)
+        line["variants"] = {"planned_chunk": {"chunk": chunk, "us_per_layer": t_plan * 1e3, "timing": "stream launches"},
+                            "total_length_chunk": {"chunk": chunk_tot, "us_per_layer": t_tot * 1e3,
                                                    "timing": "stream launches"},
                             "max_length_chunk": {"chunk": chunk_max, "us_per_layer": t_max * 1e3,
                                                  "gbs": read_bytes / (t_max / 1e3) / 1e9, "timing": "stream launches"}}

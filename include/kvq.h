@@ -273,9 +273,18 @@ size_t kvq_paged_attend_workspace_bytes(const kvq_paged_cache *cache, int32_t n_
  * to kvq_paged_attend_workspace_bytes). 0 on invalid arguments. */
 int32_t kvq_paged_attend_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t max_kv_len,
                                int64_t total_kv_len, int32_t chunk);
+/* A balanced chunk for a ragged batch from the host copy of its sequence lengths (host i32
+ * [batch], the lengths the attend call will see): every sequence's body is split into
+ * ceil(body / chunk) equal chunks, and the returned chunk is the shortest (multiple of 64) whose
+ * chunks of all sequences and kv heads fit one wave of the phase-1 kernel these shapes select on
+ * the current device (else the fewest waves x chunk). Pass it as `chunk` to the attend call and
+ * to kvq_paged_attend_workspace_bytes. 0 on invalid arguments. Host only: reads no device memory. */
+int32_t kvq_paged_attend_plan_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t q_dtype,
+                                    const int32_t *host_seq_lens);
 
 /*
- * kvq_decode_attend over a paged cache with per-sequence lengths.
+ * kvq_decode_attend over a paged cache with per-sequence lengths. Each sequence's body is split
+ * into ceil(body / chunk) chunks of equal length (multiples of 64 tokens, none longer than chunk).
  *   q    device [batch][n_q_heads][n_q][head_dim] in q_dtype
  *   out  device f32 [batch][n_q_heads][n_q][head_dim]
  *   seq_lens  device i32 [batch]: the number of cached tokens of each sequence, read on the

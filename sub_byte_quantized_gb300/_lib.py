@@ -37,7 +37,7 @@ EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0
            "kvq_attend_chunk", "kvq_decode_attend_static", "kvq_append_decode_attend",
            "kvq_paged_cache_bytes", "kvq_paged_store", "kvq_paged_attend_workspace_bytes", "kvq_paged_attend_chunk",
            "kvq_paged_decode_attend", "kvq_paged_append_decode_attend", "kvq_store_q8_0", "kvq_store_hadamard_int2",
-           "kvq_store")
+           "kvq_store", "kvq_paged_attend_plan_chunk")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ_STATIC_SCRATCH_BYTES in include/kvq.h
 
 
@@ -106,6 +106,8 @@ def lib() -> C.CDLL:
     L.kvq_paged_attend_workspace_bytes.restype = SZ
     L.kvq_paged_attend_chunk.argtypes = [paged_p, I32, I32, I32, C.c_int64, I32]
     L.kvq_paged_attend_chunk.restype = I32
+    L.kvq_paged_attend_plan_chunk.argtypes = [paged_p, I32, I32, I32, P]
+    L.kvq_paged_attend_plan_chunk.restype = I32
     L.kvq_paged_decode_attend.argtypes = [paged_p, P, I32, I32, I32, P, I32, I32, C.c_float, I32, P, P, SZ, P]
     L.kvq_paged_decode_attend.restype = I32
     L.kvq_paged_append_decode_attend.argtypes = [paged_p, P, P, I32, I32, P, I32, I32, I32, P, I32, I32, C.c_float,

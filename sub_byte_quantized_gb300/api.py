@@ -320,6 +320,16 @@ def paged_attend_chunk(cache: PagedKVCache, n_q_heads: int, n_q: int, max_kv_len
                                               chunk))
 
 
+def paged_attend_plan_chunk(cache: PagedKVCache, n_q_heads: int, n_q: int, seq_lens, q_dtype=torch.bfloat16) -> int:
+    """A balanced split-K chunk for this batch from the host copy of its sequence lengths."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    if lens.size != cache.batch:
+        raise ValueError("seq_lens must have one entry per sequence")
+    return int(L.lib().kvq_paged_attend_plan_chunk(C.byref(cache.struct), n_q_heads, n_q, _DTYPES[q_dtype],
+                                                   lens.ctypes.data))
+
+
 def _paged_out_ws(cache, q, max_kv_len, chunk, out, workspace):
     B, Hq, n_q, D = q.shape
     if B != cache.batch or D != cache.head_dim:

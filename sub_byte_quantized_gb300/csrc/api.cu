@@ -511,6 +511,68 @@ kvq_status kvq_paged_store(const kvq_paged_cache *cache, const void *k_new, cons
   return KVQ_OK;
 }
 
+namespace {
+
+// Resident CTAs per SM of the phase-1 kernel a call with these shapes runs, and how many of its
+// CTAs one (batch, kv head, chunk) unit takes (the row-side kernel: one per 64-query-row block).
+void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_per_sm, int &ctas_per_unit) {
+  ctas_per_unit = 1;
+  if (c.layout == KVQ_Q6_0 && c.v_layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
+    ctas_per_sm = kvq::kMmaQ6CtasPerSm(c.D);
+  } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) &&
+             (kvq::is_hadamard(c.layout) || q_dtype != KVQ_F32)) {
+    ctas_per_sm = kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2;
+    const bool dec = rows <= 16 && !kvq::decode_kernel(c.layout, c.v_layout);
+    ctas_per_unit = dec ? 1 : (rows + kvq::kPrefillRows - 1) / kvq::kPrefillRows;
+  } else if (c.layout == c.v_layout && kvq::uses_mma4(c.layout)) {
+    ctas_per_sm = kvq::kMma4CtasPerSm;
+  } else {
+    ctas_per_sm = kvq::kMmaWarpsPerSm / 4;
+  }
+}
+
+}  // namespace
+
+int32_t kvq_paged_attend_plan_chunk(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q, int32_t q_dtype,
+                                    const int32_t *host_seq_lens) {
+  g_last_error[0] = 0;
+  kvq::CacheView v;
+  if (check_paged_cache(cache, v) != KVQ_OK) return 0;
+  if (!host_seq_lens || n_q_heads < 1 || n_q < 1 || n_q_heads % v.H) {
+    fail(KVQ_EINVAL, "host_seq_lens is NULL or bad head counts");
+    return 0;
+  }
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int per_sm = 1, per_unit = 1;
+  phase1_capacity(v, (n_q_heads / v.H) * n_q, q_dtype, per_sm, per_unit);
+  const long long capacity = (long long)sms * per_sm / per_unit;       // (head, chunk) units in one wave
+  const int cap_len = v.cap;
+  auto units = [&](int ch) {
+    long long u = 0;
+    for (int b = 0; b < v.B; ++b) {
+      const int L = host_seq_lens[b] < 0 ? 0 : (host_seq_lens[b] > cap_len ? cap_len : host_seq_lens[b]);
+      const int nb = L - (kvq::is_hadamard(v.layout) ? (v.n_recent < L ? v.n_recent : L) : 0);
+      u += nb > 0 ? (nb + ch - 1) / ch : 0;
+    }
+    return u * v.H;
+  };
+  // the shortest chunk whose units fit one wave: every CTA then has at most that many tokens
+  for (int ch = 64; ch <= 8192; ch += 64)
+    if (units(ch) <= capacity) return ch;
+  // more work than one wave at the longest chunk: the least (waves x chunk)
+  long long best = -1;
+  int best_ch = 8192;
+  for (int ch = 64; ch <= 8192; ch += 64) {
+    const long long cost = (units(ch) + capacity - 1) / capacity * ch;
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_ch = ch;
+    }
+  }
+  return best_ch;
+}
+
 size_t kvq_paged_attend_workspace_bytes(const kvq_paged_cache *cache, int32_t n_q_heads, int32_t n_q,
                                         int32_t max_kv_len, int32_t chunk) {
   kvq::AttendArgs a;

@@ -30,8 +30,8 @@ constexpr int kThreads = kRowsPerCta * 32;
 // the window chunk [n_body, kv_len).
 __device__ __forceinline__ void chunk_range(const AttendArgs &a, const SeqLen &sl, int c, int &t0, int &t1) {
   if (c < a.n_chunks) {
-    t0 = c * a.chunk;
-    t1 = min(sl.n_body, t0 + a.chunk);
+    t0 = c * sl.chunk;
+    t1 = min(sl.n_body, t0 + sl.chunk);
   } else {
     t0 = sl.n_body;
     t1 = sl.kv_len;

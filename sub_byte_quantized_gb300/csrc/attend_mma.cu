@@ -95,8 +95,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
-  const int t0 = chunk_id * a.chunk;
-  const int t1 = min(sl.n_body, t0 + a.chunk);
+  const int t0 = chunk_id * sl.chunk;
+  const int t1 = min(sl.n_body, t0 + sl.chunk);
   int w_lim = -1, min_lim = INT_MAX;
   for (int r = 0; r < R; ++r) {
     const int l = row_limit_of(a, sl, r);

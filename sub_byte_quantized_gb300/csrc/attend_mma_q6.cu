@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
-  const int t0 = chunk_id * a.chunk;
-  const int t1 = min(sl.n_body, t0 + a.chunk);
+  const int t0 = chunk_id * sl.chunk;
+  const int t1 = min(sl.n_body, t0 + sl.chunk);
   // the rows' limits, folded here so that nothing of the sequence's lengths stays live below:
   // the widest and narrowest limit, this thread's two accumulator rows, and a mask of the rows
   // that see this chunk

@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   const int R = a.gqa * a.n_q;
 
   const bool win = HAD && chunk_id == a.n_chunks;     // the recent-window chunk
-  const int t0 = win ? sl.n_body : chunk_id * a.chunk;
-  const int t1 = win ? sl.kv_len : min(sl.n_body, t0 + a.chunk);
+  const int t0 = win ? sl.n_body : chunk_id * sl.chunk;
+  const int t1 = win ? sl.kv_len : min(sl.n_body, t0 + sl.chunk);
   int w_lim = -1;
   for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit_of(a, sl, r));
   // rows appended by the preceding kernel (cache rows or window ring): only the CTAs that read

@@ -168,6 +168,7 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as
 // The lengths of sequence bb that a kernel works with.
 struct SeqLen {
   int kv_len, n_body, q_pos0, fresh_lo, fresh_hi;
+  int chunk, n_chunks;     // this sequence's split of its body (paged calls: equal chunks)
 };
 __device__ __forceinline__ SeqLen seq_of(const AttendArgs &a, int bb) {
   SeqLen s;
@@ -177,6 +178,8 @@ __device__ __forceinline__ SeqLen seq_of(const AttendArgs &a, int bb) {
     s.q_pos0 = a.q_pos0;
     s.fresh_lo = a.fresh_lo;
     s.fresh_hi = a.fresh_hi;
+    s.chunk = a.chunk;
+    s.n_chunks = a.n_chunks;
     return s;
   }
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
@@ -190,6 +193,10 @@ __device__ __forceinline__ SeqLen seq_of(const AttendArgs &a, int bb) {
   s.q_pos0 = L - a.n_q;
   s.fresh_lo = a.fresh_tail > 0 ? L - a.fresh_tail : 0;
   s.fresh_hi = a.fresh_tail > 0 ? L : INT_MAX;
+  // the body in ceil(n_body / chunk) equal chunks (multiples of 64 tokens, none longer than
+  // a.chunk), so that a short sequence's last chunk is not a sliver while its others are full
+  s.n_chunks = s.n_body > 0 ? (s.n_body + a.chunk - 1) / a.chunk : 0;
+  s.chunk = s.n_chunks > 0 ? ((s.n_body + s.n_chunks - 1) / s.n_chunks + 63) / 64 * 64 : a.chunk;
   return s;
 }
 // The same for a kernel built for one cache kind: paged calls always pass per-sequence lengths,
@@ -205,6 +212,8 @@ __device__ __forceinline__ SeqLen seq_of_t(const AttendArgs &a, int bb) {
     s.q_pos0 = a.q_pos0;
     s.fresh_lo = a.fresh_lo;
     s.fresh_hi = a.fresh_hi;
+    s.chunk = a.chunk;
+    s.n_chunks = a.n_chunks;
     return s;
   }
 }

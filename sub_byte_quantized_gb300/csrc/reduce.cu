@@ -35,8 +35,7 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const SeqLen sl = seq_of(a, a.seq_lens ? (int)(row / ((size_t)a.Hq * a.n_q)) : 0);
   const int lim = row_limit(a, sl, qi);                  // negative: the row sees nothing
-  const int n_chunks = a.seq_lens ? (sl.n_body + a.chunk - 1) / a.chunk : a.n_chunks;
-  const int n_vis_body = lim < 0 ? 0 : min(n_chunks, lim / a.chunk + 1);
+  const int n_vis_body = lim < 0 ? 0 : min(sl.n_chunks, lim / sl.chunk + 1);
   const bool win_vis = sl.kv_len > sl.n_body && sl.n_body <= lim;
   const float *pm = a.part_m + row * a.C;
   const float *pl = a.part_l + row * a.C;
@@ -205,8 +204,7 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
   const int qi = (int)(row % a.n_q);
   const SeqLen sl = seq_of(a, a.seq_lens ? (int)(row / ((size_t)a.Hq * a.n_q)) : 0);
   const int lim = row_limit(a, sl, qi);                  // negative: the row sees nothing
-  const int n_chunks = a.seq_lens ? (sl.n_body + a.chunk - 1) / a.chunk : a.n_chunks;
-  const int n_vis_body = lim < 0 ? 0 : min(n_chunks, lim / a.chunk + 1);
+  const int n_vis_body = lim < 0 ? 0 : min(sl.n_chunks, lim / sl.chunk + 1);
   const bool win_vis = sl.kv_len > sl.n_body && sl.n_body <= lim;
   const float *pm = a.part_m + row * a.C;
   const float *pl = a.part_l + row * a.C;

@@ -201,3 +201,18 @@ def test_mixed_layout_validation(L):
     assert L.kvq_store(p(za), 16, 16, 1, 1, 0, None) == 1
     za = KvqCache(mixed(0, 3), 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, 4096, None, None)
     assert L.kvq_store(p(za), 16, 16, 1, 10, 60, None) == 3          # valid planes, capacity error
+
+
+def test_paged_plan_chunk(L):
+    """The planner: the shortest multiple of 64 whose equal per-sequence chunks fit one wave."""
+    import numpy as np
+    p = C.byref
+    L.kvq_paged_attend_plan_chunk.argtypes = [C.c_void_p, C.c_int32, C.c_int32, C.c_int32, C.c_void_p]
+    c = _paged(mpp=2048, n_pages=8192)
+    lens = np.array([131072, 5], np.int32)
+    ch = L.kvq_paged_attend_plan_chunk(p(c), 8, 1, 1, lens.ctypes.data)
+    assert ch % 64 == 0 and 64 <= ch <= 8192
+    # fewer tokens never need a longer chunk
+    small = np.array([4096, 5], np.int32)
+    assert L.kvq_paged_attend_plan_chunk(p(c), 8, 1, 1, small.ctypes.data) <= ch
+    assert L.kvq_paged_attend_plan_chunk(p(c), 8, 1, 1, None) == 0

@@ -185,3 +185,18 @@ def test_paged_equals_contiguous_bitwise(layout):
     got = kvq.paged_decode_attend(pc, q, lens, S, attn_scale=w.alpha, chunk=128)
     torch.cuda.synchronize()
     assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("layout,n_recent", [("q4_0", 0), ("asym4_g32", 0), ("had_int4", 32), ("q8_0", 0)])
+def test_paged_planned_chunk_ragged(layout, n_recent):
+    """A ragged batch with the chunk from kvq_paged_attend_plan_chunk: each sequence's body in equal
+    chunks (its last chunk no longer a sliver), against the oracle."""
+    w = _decode_w(layout, 128, 4, n_recent)
+    lens = [1000, 130, 64, 777]
+    S = max(lens)
+    probe = kvq.PagedKVCache(w.layout, 4, 2, 128, 64, 4 * (-(-S // 64)), -(-S // 64), n_recent=n_recent)
+    chunk = kvq.paged_attend_plan_chunk(probe, 8, 1, lens)
+    assert chunk % 64 == 0 and 64 <= chunk <= 8192
+    del probe
+    dc, oc, out, ref = build(w, lens, 64, n_q=1, chunk=chunk)
+    check_close(out.cpu().numpy(), ref, f"paged planned chunk {layout} ({chunk})")
