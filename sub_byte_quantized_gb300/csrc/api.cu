@@ -231,7 +231,8 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
   a.q_pos0 = causal ? q_pos0 : 0;
   a.chunk = chunk;
   a.n_chunks = (a.n_body + chunk - 1) / chunk;
-  a.C = a.n_chunks + (a.n_win > 0 ? 1 : 0);
+  a.n_wchunks = (a.n_win + kvq::kWinChunk - 1) / kvq::kWinChunk;
+  a.C = a.n_chunks + a.n_wchunks;
   a.win_in_reduce = 0;
   a.fresh_lo = 0;
   a.fresh_hi = INT_MAX;

@@ -27,14 +27,14 @@ constexpr int kRowsPerCta = 8;       // one warp per query row
 constexpr int kThreads = kRowsPerCta * 32;
 
 // Absolute token range of chunk c of a sequence: body chunks [c*chunk, min(n_body, (c+1)*chunk)),
-// the window chunk [n_body, kv_len).
+// window chunk w = c - n_chunks: [n_body + w*kWinChunk, min(kv_len, n_body + (w+1)*kWinChunk)).
 __device__ __forceinline__ void chunk_range(const AttendArgs &a, const SeqLen &sl, int c, int &t0, int &t1) {
   if (c < a.n_chunks) {
     t0 = c * sl.chunk;
     t1 = min(sl.n_body, t0 + sl.chunk);
   } else {
-    t0 = sl.n_body;
-    t1 = sl.kv_len;
+    t0 = sl.n_body + (c - a.n_chunks) * kWinChunk;
+    t1 = min(sl.kv_len, t0 + kWinChunk);
   }
 }
 

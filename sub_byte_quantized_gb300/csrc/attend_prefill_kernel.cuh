@@ -31,7 +31,8 @@
 // keep the unpacker's order (0,4,1,5,2,6,3,7); the query fragments and the output columns follow
 // it. Each warp keeps the online softmax of its 16 rows.
 //
-// Hadamard: the exact-f32 recent window is one more chunk (blockIdx.y == n_chunks): its CTAs
+// Hadamard: the exact-f32 recent window is more chunks of kWinChunk tokens (blockIdx.y >=
+// n_chunks; a wide window is spread over several CTAs): their CTAs
 // stream the f32 rotated K/V rows of the ring and score them with the f32 rotated query on the
 // CUDA cores.
 #pragma once
@@ -204,9 +205,9 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
   const int R = a.gqa * a.n_q;
 
-  const bool win = HAD && chunk_id == a.n_chunks;     // the recent-window chunk
-  const int t0 = win ? sl.n_body : chunk_id * sl.chunk;
-  const int t1 = win ? sl.kv_len : min(sl.n_body, t0 + sl.chunk);
+  const bool win = HAD && chunk_id >= a.n_chunks;     // a chunk of the recent window
+  const int t0 = win ? sl.n_body + (chunk_id - a.n_chunks) * kWinChunk : chunk_id * sl.chunk;
+  const int t1 = win ? min(sl.kv_len, t0 + kWinChunk) : min(sl.n_body, t0 + sl.chunk);
   int w_lim = -1;
   for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit_of(a, sl, r));
   // rows appended by the preceding kernel (cache rows or window ring): only the CTAs that read
@@ -795,8 +796,8 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   }
   const int R = a.gqa * a.n_q;
   cudaLaunchConfig_t cfg = {};
-  // Hadamard: one more chunk index for the recent window (when present)
-  cfg.gridDim = dim3((R + kRows - 1) / kRows, a.n_chunks + (G::HAD && a.n_win > 0 ? 1 : 0), a.cache.B * a.cache.H);
+  // Hadamard: more chunk indices for the recent window (when present), kWinChunk tokens each
+  cfg.gridDim = dim3((R + kRows - 1) / kRows, a.n_chunks + (G::HAD ? a.n_wchunks : 0), a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = G::SMEM;
   cfg.stream = st;

@@ -13,6 +13,8 @@ namespace kvq {
 
 constexpr int kBlock = 32;          // values per Q4_0 / Q6_0 / Q8_0 / asymmetric block
 constexpr int kLastLayout = KVQ_HAD_INT2;
+// Tokens per chunk of the exact-f32 window (a wide window is split over several chunks).
+constexpr int kWinChunk = 64;
 // Layouts in the fixed Hadamard basis: one f32 scale per token, rotated query, optional f32 window.
 __host__ __device__ constexpr bool is_hadamard(int layout) {
   return layout == KVQ_HAD_INT4 || layout == KVQ_HAD_INT2;
@@ -106,8 +108,9 @@ struct AttendArgs {
   int kv_len, n_win, n_body; // n_win = HAD ring tokens in use, n_body = kv_len - n_win
   int causal, q_pos0;
   float scale;              // attention scale alpha
-  int chunk, n_chunks;      // body chunks = ceil(n_body / chunk); + 1 window chunk if n_win
-  int C;                    // total partials per row
+  int chunk, n_chunks;      // body chunks = ceil(n_body / chunk)
+  int n_wchunks;            // window chunks of kWinChunk tokens (0 without a window)
+  int C;                    // total partials per row: n_chunks + n_wchunks
   int win_in_reduce;        // HAD: phase 2 computes the window chunk's partial itself
   // Token rows [fresh_lo, fresh_hi) were written by the kernel launched just before phase 1 (an
   // append in the same call): only phase-1 CTAs that read them, and the first CTA, wait for it.

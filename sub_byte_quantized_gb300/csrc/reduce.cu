@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int c = base + u * kWarps;
-      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : win_vis && !a.win_in_reduce);
+      const int wt0 = sl.n_body + (c - a.n_chunks) * kWinChunk;      // window chunk's first token
+      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body
+                                                  : !a.win_in_reduce && wt0 < sl.kv_len && wt0 <= lim);
       mc[u] = vis ? pm[c] : -INFINITY;
       lc[u] = vis ? pl[c] : 0.0f;
 #pragma unroll
@@ -205,7 +207,6 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
   const SeqLen sl = seq_of(a, a.seq_lens ? (int)(row / ((size_t)a.Hq * a.n_q)) : 0);
   const int lim = row_limit(a, sl, qi);                  // negative: the row sees nothing
   const int n_vis_body = lim < 0 ? 0 : min(sl.n_chunks, lim / sl.chunk + 1);
-  const bool win_vis = sl.kv_len > sl.n_body && sl.n_body <= lim;
   const float *pm = a.part_m + row * a.C;
   const float *pl = a.part_l + row * a.C;
   const float *po = a.part_o + row * a.C * (size_t)D + lane * VPL;
@@ -217,7 +218,8 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int c = base + u;
-      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : win_vis);
+      const int wt0 = sl.n_body + (c - a.n_chunks) * kWinChunk;      // window chunk's first token
+      const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : wt0 < sl.kv_len && wt0 <= lim);
       mc[u] = vis ? pm[c] : -INFINITY;
       lc[u] = vis ? pl[c] : 0.0f;
       if constexpr (VPL == 4) {
