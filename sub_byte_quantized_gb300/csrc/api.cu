@@ -163,7 +163,8 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
 // every resident CTA. Many rows (Hadamard prefill): about four waves of 64-row CTAs.
 // `work` = body tokens summed over every (batch, kv head) (0: n_body for each of them); a ragged
 // batch passes its true total so the chunk fits the work that exists.
-int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long long work = 0) {
+// n_wchunks: window chunks per (batch, kv head) that the row-side kernel scores in the same grid.
+int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long long work = 0, int n_wchunks = 0) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const bool total_given = work > 0;
@@ -177,7 +178,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
     // row-side kernel in its decode form (one row block, the warps split the tokens): one chunk per
     // resident CTA, as many chunks per (batch, kv head) as fit one wave
     const long long ctas = (long long)sms * (kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2);
-    long long per_head = ctas / (n_heads > 0 ? n_heads : 1);
+    long long per_head = ctas / (n_heads > 0 ? n_heads : 1) - n_wchunks;   // the window's CTAs share the wave
     if (per_head < 1) per_head = 1;
     const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
     chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
@@ -219,9 +220,11 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
   if (!paged && causal && (q_pos0 < 0 || (long long)q_pos0 + n_q > kv_len))
     return fail(KVQ_EINVAL, "causal call needs 0 <= q_pos0 and q_pos0 + n_q <= kv_len");
   if (chunk == 0)
-    chunk = auto_chunk(c, (n_q_heads / c.H) * n_q,
-                       kv_len - (kvq::is_hadamard(c.layout) ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0), c.B * c.H,
-                       work);
+  {
+    const int n_win = kvq::is_hadamard(c.layout) ? (c.n_recent < kv_len ? c.n_recent : kv_len) : 0;
+    chunk = auto_chunk(c, (n_q_heads / c.H) * n_q, kv_len - n_win, c.B * c.H, work,
+                       (n_win + kvq::kWinChunk - 1) / kvq::kWinChunk);
+  }
   if (chunk < 64 || chunk > 8192 || chunk % 64) return fail(KVQ_ESHAPE, "chunk %d not a multiple of 64 in [64, 8192]", chunk);
   a.Hq = n_q_heads; a.gqa = n_q_heads / c.H; a.n_q = n_q;
   a.kv_len = kv_len;
@@ -516,8 +519,10 @@ namespace {
 
 // Resident CTAs per SM of the phase-1 kernel a call with these shapes runs, and how many of its
 // CTAs one (batch, kv head, chunk) unit takes (the row-side kernel: one per 64-query-row block).
-void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_per_sm, int &ctas_per_unit) {
+void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_per_sm, int &ctas_per_unit,
+                     bool &window_ctas) {
   ctas_per_unit = 1;
+  window_ctas = false;                                   // the decode kernels leave the window to phase 2
   if (c.layout == KVQ_Q6_0 && c.v_layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
     ctas_per_sm = kvq::kMmaQ6CtasPerSm(c.D);
   } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) &&
@@ -525,6 +530,7 @@ void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_p
     ctas_per_sm = kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2;
     const bool dec = rows <= 16 && !kvq::decode_kernel(c.layout, c.v_layout);
     ctas_per_unit = dec ? 1 : (rows + kvq::kPrefillRows - 1) / kvq::kPrefillRows;
+    window_ctas = kvq::is_hadamard(c.layout);            // the row-side kernel scores the window chunks
   } else if (c.layout == c.v_layout && kvq::uses_mma4(c.layout)) {
     ctas_per_sm = kvq::kMma4CtasPerSm;
   } else {
@@ -546,15 +552,18 @@ int32_t kvq_paged_attend_plan_chunk(const kvq_paged_cache *cache, int32_t n_q_he
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   int per_sm = 1, per_unit = 1;
-  phase1_capacity(v, (n_q_heads / v.H) * n_q, q_dtype, per_sm, per_unit);
+  bool window_ctas = false;
+  phase1_capacity(v, (n_q_heads / v.H) * n_q, q_dtype, per_sm, per_unit, window_ctas);
   const long long capacity = (long long)sms * per_sm / per_unit;       // (head, chunk) units in one wave
   const int cap_len = v.cap;
   auto units = [&](int ch) {
     long long u = 0;
     for (int b = 0; b < v.B; ++b) {
       const int L = host_seq_lens[b] < 0 ? 0 : (host_seq_lens[b] > cap_len ? cap_len : host_seq_lens[b]);
-      const int nb = L - (kvq::is_hadamard(v.layout) ? (v.n_recent < L ? v.n_recent : L) : 0);
+      const int nw = kvq::is_hadamard(v.layout) ? (v.n_recent < L ? v.n_recent : L) : 0;
+      const int nb = L - nw;
       u += nb > 0 ? (nb + ch - 1) / ch : 0;
+      if (window_ctas) u += (nw + kvq::kWinChunk - 1) / kvq::kWinChunk;
     }
     return u * v.H;
   };

@@ -287,6 +287,8 @@ def test_workloads_full_size_sampled(name):
     ("had_int2", 128, 2, 1, False, 256, 0),      # int2 body with a wide exact-f32 window
     ("had_int2", 128, 2, 40, True, 128, 64),
     ("had_int2", 256, 2, 1, False, 64, 128),
+    ("had_int2", 128, 2, 1, False, 100, 0),       # a window of one full and one ragged 64-token chunk
+    ("had_int4", 128, 4, 24, True, 200, 64),      # prefill rows over a window of four chunks, the last ragged
 ])
 def test_q8_0_and_int2(layout, D, gqa, n_q, causal, n_recent, chunk):
     """Q8_0 and the Hadamard int2 body (with the window it needs) against the oracle: decode and
