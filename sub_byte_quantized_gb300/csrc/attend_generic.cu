@@ -43,7 +43,7 @@ __device__ __forceinline__ void chunk_range(const AttendArgs &a, const SeqLen &s
 // the caller).
 __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, int gi, float out[8]) {
   const int layout = kv ? c.v_layout : c.layout;          // each plane's own layout (mixed K/V)
-  const uint8_t *p = c.payload[kv] + row * (size_t)(kv ? c.v_row_bytes : c.row_bytes);
+  const uint8_t *p = (kv ? c.payload[1] : c.payload[0]) + row * (size_t)(kv ? c.v_row_bytes : c.row_bytes);
   const int blk = gi >> 2, sub = gi & 3;
   if (layout == KVQ_HAD_INT4) {
     const uint32_t w = *reinterpret_cast<const uint32_t *>(p + gi * 4);
@@ -57,7 +57,7 @@ __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, 
     for (int i = 0; i < 8; ++i) out[i] = (float)((int)((w >> (2 * i)) & 0x3u ^ 0x2u) - 2);
     return;
   }
-  const float s = __half2float(static_cast<const __half *>(c.scale[kv])[row * (c.D / kBlock) + blk]);
+  const float s = __half2float(static_cast<const __half *>((kv ? c.scale[1] : c.scale[0]))[row * (c.D / kBlock) + blk]);
   if (layout == KVQ_Q4_0) {
     const uint32_t w = *reinterpret_cast<const uint32_t *>(p + blk * 16 + sub * 4);
 #pragma unroll
@@ -78,7 +78,7 @@ __device__ __forceinline__ void unpack8(const CacheView &c, int kv, size_t row, 
       out[i] = (float)((int)(b ^ 0x80u) - 0x80) * s;
     }
   } else {  // ASYM4_G32
-    const float z = __half2float(c.zero[kv][row * (c.D / kBlock) + blk]);
+    const float z = __half2float((kv ? c.zero[1] : c.zero[0])[row * (c.D / kBlock) + blk]);
     const uint32_t w = *reinterpret_cast<const uint32_t *>(p + blk * 16 + sub * 4);
 #pragma unroll
     for (int i = 0; i < 8; ++i) out[i] = fmaf((float)((w >> (4 * i)) & 0xFu), s, z);
@@ -164,14 +164,14 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
       if (t < nt) {
         const int tok = tb + t;
         if (is_win) {
-          const float *src = c.ring[kv] + ((size_t)bh * c.n_recent + (size_t)(tok % c.n_recent)) * D + gi * 8;
+          const float *src = (kv ? c.ring[1] : c.ring[0]) + ((size_t)bh * c.n_recent + (size_t)(tok % c.n_recent)) * D + gi * 8;
           const float4 x0 = *reinterpret_cast<const float4 *>(src), x1 = *reinterpret_cast<const float4 *>(src + 4);
           v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
         } else {
           const size_t crow = cache_row(c, b, kvh, tok);
           unpack8(c, kv, crow, gi, v);
           if (had && gi == 0) {
-            const float s = static_cast<const float *>(c.scale[kv])[crow];
+            const float s = static_cast<const float *>((kv ? c.scale[1] : c.scale[0]))[crow];
             (kv ? vs : ks)[t] = s;
           }
         }

@@ -33,10 +33,21 @@ __device__ __forceinline__ bool row_coords(const CacheView &c, const StoreGeom &
                                            long long &in_row, long long &crow, int &j, int &pos, long long &bh) {
   kv = g.kv_only >= 0 ? g.kv_only : (r >= g.rows_per_tensor ? 1 : 0);
   const long long rr = g.kv_only >= 0 ? r : r - (long long)kv * g.rows_per_tensor;
-  bh = rr / g.n_new;
-  j = (int)(rr - bh * g.n_new);
   in_row = rr;
-  const int bb = (int)(bh / g.H), kvh = (int)(bh - (long long)bb * g.H);
+  int bb, kvh;
+  if (g.rows_per_tensor <= 0x7FFFFFFFLL) {                // 32-bit index arithmetic (every realistic call)
+    const unsigned ur = (unsigned)rr, nn = (unsigned)g.n_new, hh = (unsigned)g.H;
+    const unsigned ubh = ur / nn, ubb = ubh / hh;
+    j = (int)(ur - ubh * nn);
+    bh = ubh;
+    bb = (int)ubb;
+    kvh = (int)(ubh - ubb * hh);
+  } else {
+    bh = rr / g.n_new;
+    j = (int)(rr - bh * g.n_new);
+    bb = (int)(bh / g.H);
+    kvh = (int)(bh - (long long)bb * g.H);
+  }
   pos = (g.seq_pos ? __ldg(g.seq_pos + bb) + g.pos_offset : g.pos0) + j;
   const bool ok = pos >= 0 && pos < g.cap;
   crow = ok ? (long long)cache_row(c, bb, kvh, pos) : 0;
@@ -71,10 +82,10 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");   // attention may launch and wait on us
 #endif
-  const int tpr = g.D / 8;                                 // threads per row
+  const int tpr_shift = g.D == 128 ? 4 : 5;                // D / 8 threads per row
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long r = gt / tpr;
-  const int tr = (int)(gt - r * tpr);                      // thread within row
+  const long long r = gt >> tpr_shift;
+  const int tr = (int)(gt & ((1 << tpr_shift) - 1));      // thread within row
   // Threads past the last row still take part in the quad shuffles (full-warp masks) but load
   // and store nothing.
   bool valid = r < g.n_rows;
@@ -85,8 +96,8 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
 
   float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (valid) load8_f32(kv ? v_new : k_new, dtype, (size_t)in_row * g.D + (size_t)tr * 8, v);
-  uint8_t *prow = c.payload[kv] + (size_t)crow * g.row_bytes;
-  __half *srow = static_cast<__half *>(c.scale[kv]) + (size_t)crow * g.nb;
+  uint8_t *prow = (kv ? c.payload[1] : c.payload[0]) + (size_t)crow * g.row_bytes;
+  __half *srow = static_cast<__half *>((kv ? c.scale[1] : c.scale[0])) + (size_t)crow * g.nb;
 
   if (LAYOUT == KVQ_ASYM4_G32) {
     float mn = v[0], mx = v[0];
@@ -111,7 +122,7 @@ __global__ void __launch_bounds__(256) store_block_kernel(CacheView c, const voi
     *reinterpret_cast<uint32_t *>(prow + blk * 16 + lb * 4) = w;
     if (lb == 0) {
       srow[blk] = sh;
-      c.zero[kv][(size_t)crow * g.nb + blk] = zh;
+      (kv ? c.zero[1] : c.zero[0])[(size_t)crow * g.nb + blk] = zh;
     }
     return;
   }
@@ -197,7 +208,7 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
 #pragma unroll
   for (int i = 0; i < V; ++i)
     w |= ((uint32_t)sym_code(x[i], s, -QMAX, QMAX) & ((1u << BITS) - 1u)) << (BITS * i);
-  uint8_t *prow = c.payload[kv] + (size_t)crow * g.row_bytes;
+  uint8_t *prow = (kv ? c.payload[1] : c.payload[0]) + (size_t)crow * g.row_bytes;
   if (V * BITS == 8) {
     prow[lane] = (uint8_t)w;
   } else if (V * BITS == 16) {
@@ -205,11 +216,11 @@ __global__ void __launch_bounds__(256) store_had_kernel(CacheView c, const void 
   } else {
     *reinterpret_cast<uint32_t *>(prow + lane * 4) = w;
   }
-  if (lane == 0) static_cast<float *>(c.scale[kv])[crow] = s;
+  if (lane == 0) static_cast<float *>((kv ? c.scale[1] : c.scale[0]))[crow] = s;
   // Exact-f32 ring of the newest tokens: only the last min(n_new, n_recent) rows of this call,
   // so no two rows of one call write the same slot.
   if (c.n_recent > 0 && j >= g.n_new - c.n_recent) {
-    float *dst = c.ring[kv] + ((size_t)bh * c.n_recent + (size_t)(pos % c.n_recent)) * g.D + lane * V;
+    float *dst = (kv ? c.ring[1] : c.ring[0]) + ((size_t)bh * c.n_recent + (size_t)(pos % c.n_recent)) * g.D + lane * V;
 #pragma unroll
     for (int i = 0; i < V; i += 4)
       *reinterpret_cast<float4 *>(dst + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
