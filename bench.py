@@ -613,29 +613,26 @@ def main():
     }
 
     if not args.quick and rank == 0:
-        # end to end through the public API from pinned host buffers, one sync per step
+        # end to end through the host-buffer C-ABI call: pinned host k_new, v_new and q in, the f32
+        # result back in pinned host memory; the call copies both ways and waits for its stream
         hk, hv, hq = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q.cpu().pin_memory()
         hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-        dk, dv, dq = torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q)
+        ws_h = torch.empty(kvq.append_decode_attend_host_workspace_bytes(caches[0], hk.dtype, hk.shape[2], hq.dtype,
+                                                                         w.n_q_heads, spec.n_q, S, chunk),
+                           dtype=torch.uint8, device=dev)
         n_e2e = min(K, 500)
         for i in range(n_e2e + 3):
             if i == 3:
-                torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
-            with torch.cuda.stream(stream):
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
-                dq.copy_(hq, non_blocking=True)
-                c = caches[i % n_rep]
-                kvq.append_decode_attend(c, dk, dv, fill, dq, S, causal=spec.causal, q_pos0=spec.q_pos0,
-                                         attn_scale=w.alpha, chunk=chunk, out=out, workspace=ws, stream=stream)
-                hout.copy_(out, non_blocking=True)
-            stream.synchronize()
+            kvq.append_decode_attend_host(caches[i % n_rep], hk, hv, fill, hq, S, causal=spec.causal,
+                                          q_pos0=spec.q_pos0, attn_scale=w.alpha, chunk=chunk, out=hout,
+                                          workspace=ws_h, stream=stream)
         t_e2e = (time.perf_counter() - t0) / n_e2e
         el = hk.element_size()
         line["e2e"] = {"value": spec.read_bytes / t_e2e / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": (hk.numel() + hv.numel() + hq.numel()) * el,
-                       "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e}
+                       "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e,
+                       "call": "kvq_append_decode_attend_host (host buffers, one call and one stream wait per step)"}
         line["store"] = store_timings(kvq, w, kd, vd, k_new, v_new, fill, stream, dev)
         if args.workload == DEFAULT_WORKLOAD:
             line["variants"] = variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1,
@@ -895,32 +892,27 @@ def paged_main(args):
                                                    "timing": "stream launches"},
                             "max_length_chunk": {"chunk": chunk_max, "us_per_layer": t_max * 1e3,
                                                  "gbs": read_bytes / (t_max / 1e3) / 1e9, "timing": "stream launches"}}
-        # end to end through the public API: new tokens, queries and the sequence lengths from pinned host
-        # memory, the output back, one sync per step
+        # end to end through the host-buffer C-ABI call: new tokens, queries and the sequence lengths
+        # from pinned host memory, the output back into pinned host memory, one stream wait per step
         hk, hv, hq = k_new.cpu().pin_memory(), v_new.cpu().pin_memory(), q.cpu().pin_memory()
         hl = lens_dev.cpu().pin_memory()
         hout = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-        dk, dv, dq, dl = (torch.empty_like(k_new), torch.empty_like(v_new), torch.empty_like(q),
-                          torch.empty_like(lens_dev))
+        ws_h = torch.empty(kvq.paged_append_decode_attend_host_workspace_bytes(pools[0], hk.dtype, hk.shape[2],
+                                                                               hq.dtype, Hq, 1, S_max, chunk),
+                           dtype=torch.uint8, device=dev)
         n_e2e = min(K, 500)
         for i in range(n_e2e + 3):
             if i == 3:
-                torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
-            with torch.cuda.stream(stream):
-                dk.copy_(hk, non_blocking=True)
-                dv.copy_(hv, non_blocking=True)
-                dq.copy_(hq, non_blocking=True)
-                dl.copy_(hl, non_blocking=True)
-                kvq.paged_append_decode_attend(pools[i % n_rep], dk, dv, dq, dl, S_max, attn_scale=w.alpha,
-                                               chunk=chunk, out=out, workspace=ws, stream=stream)
-                hout.copy_(out, non_blocking=True)
-            stream.synchronize()
+            kvq.paged_append_decode_attend_host(pools[i % n_rep], hk, hv, hq, hl, S_max, attn_scale=w.alpha,
+                                                chunk=chunk, out=hout, workspace=ws_h, stream=stream)
         t_e2e = (time.perf_counter() - t0) / n_e2e
         el = hk.element_size()
         line["e2e"] = {"value": read_bytes / t_e2e / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": (hk.numel() + hv.numel() + hq.numel()) * el + hl.numel() * 4,
-                       "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e}
+                       "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e,
+                       "call": "kvq_paged_append_decode_attend_host (host buffers, one call and one stream wait "
+                               "per step)"}
         if world == 1:
             step_o, per = paged_oracle_step(w, inp, 1)
             times = []

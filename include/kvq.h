@@ -318,6 +318,46 @@ kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const vo
                                           float *out, void *workspace, size_t workspace_bytes,
                                           kvq_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Host-buffer forms of the two append + attend calls, for callers whose new rows and queries are
+ * in host memory and who want the result there (no counterpart on the pages: the steps are
+ * those of the device-buffer calls above, with the copies around them).
+ *   k_new, v_new  host [batch][n_kv_heads][n_new][head_dim] in kv_dtype (unused when n_new == 0)
+ *   q             host [batch][n_q_heads][n_q][head_dim] in q_dtype
+ *   out           host f32 [batch][n_q_heads][n_q][head_dim]
+ *   seq_lens      (paged) host i32 [batch], the lengths after the append, as in
+ *                 kvq_paged_append_decode_attend
+ *   workspace     device, 256-byte aligned, at least the matching *_host_workspace_bytes: the
+ *                 attention partials followed by device staging for k_new, v_new, q, out
+ *                 (and seq_lens); the caller owns it, the call must not share it with another
+ *                 call in flight.
+ * The call copies the inputs host -> device on `stream` (cudaMemcpyAsync; page-locked host
+ * memory makes the copies asynchronous, pageable memory works but the driver stages it), enqueues
+ * the same launches as the device-buffer call (identical results and stored bytes), copies the
+ * output back and returns after cudaStreamSynchronize(stream), with `out` filled. Every argument
+ * is validated before anything is enqueued; a CUDA error from a copy, a launch or the
+ * synchronisation returns KVQ_ECUDA (then nothing can be assumed about `out` or the cache rows
+ * of the append). The host buffers may be reused as soon as the call returns.
+ */
+size_t kvq_append_decode_attend_host_workspace_bytes(const kvq_cache *cache, int32_t kv_dtype, int32_t n_new,
+                                                     int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                                                     int32_t kv_len, int32_t chunk);
+kvq_status kvq_append_decode_attend_host(const kvq_cache *cache, const void *k_new, const void *v_new,
+                                         int32_t kv_dtype, int32_t n_new, int32_t pos0, const void *q,
+                                         int32_t q_dtype, int32_t n_q_heads, int32_t n_q, int32_t kv_len,
+                                         int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                                         float *out, void *workspace, size_t workspace_bytes,
+                                         kvq_stream_t stream);
+size_t kvq_paged_append_decode_attend_host_workspace_bytes(const kvq_paged_cache *cache, int32_t kv_dtype,
+                                                           int32_t n_new, int32_t q_dtype, int32_t n_q_heads,
+                                                           int32_t n_q, int32_t max_kv_len, int32_t chunk);
+kvq_status kvq_paged_append_decode_attend_host(const kvq_paged_cache *cache, const void *k_new, const void *v_new,
+                                               int32_t kv_dtype, int32_t n_new, const void *q, int32_t q_dtype,
+                                               int32_t n_q_heads, int32_t n_q, const int32_t *seq_lens,
+                                               int32_t max_kv_len, int32_t causal, float attn_scale, int32_t chunk,
+                                               float *out, void *workspace, size_t workspace_bytes,
+                                               kvq_stream_t stream);
+
 /*
  * HAD_INT4 / HAD_INT2 test hook: the exact integer-domain body scores int8(q_rot) . code(k_rot).
  *   scores_out device i32 [batch][n_q_heads][n_q][kv_len - min(n_recent, kv_len)]

@@ -37,7 +37,9 @@ EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0
            "kvq_attend_chunk", "kvq_decode_attend_static", "kvq_append_decode_attend",
            "kvq_paged_cache_bytes", "kvq_paged_store", "kvq_paged_attend_workspace_bytes", "kvq_paged_attend_chunk",
            "kvq_paged_decode_attend", "kvq_paged_append_decode_attend", "kvq_store_q8_0", "kvq_store_hadamard_int2",
-           "kvq_store", "kvq_paged_attend_plan_chunk")
+           "kvq_store", "kvq_paged_attend_plan_chunk", "kvq_append_decode_attend_host_workspace_bytes",
+           "kvq_append_decode_attend_host", "kvq_paged_append_decode_attend_host_workspace_bytes",
+           "kvq_paged_append_decode_attend_host")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ_STATIC_SCRATCH_BYTES in include/kvq.h
 
 
@@ -113,6 +115,14 @@ def lib() -> C.CDLL:
     L.kvq_paged_append_decode_attend.argtypes = [paged_p, P, P, I32, I32, P, I32, I32, I32, P, I32, I32, C.c_float,
                                                  I32, P, P, SZ, P]
     L.kvq_paged_append_decode_attend.restype = I32
+    L.kvq_append_decode_attend_host_workspace_bytes.argtypes = [cache_p, I32, I32, I32, I32, I32, I32, I32]
+    L.kvq_append_decode_attend_host_workspace_bytes.restype = SZ
+    L.kvq_append_decode_attend_host.argtypes = L.kvq_append_decode_attend.argtypes
+    L.kvq_append_decode_attend_host.restype = I32
+    L.kvq_paged_append_decode_attend_host_workspace_bytes.argtypes = [paged_p, I32, I32, I32, I32, I32, I32, I32]
+    L.kvq_paged_append_decode_attend_host_workspace_bytes.restype = SZ
+    L.kvq_paged_append_decode_attend_host.argtypes = L.kvq_paged_append_decode_attend.argtypes
+    L.kvq_paged_append_decode_attend_host.restype = I32
     L.kvq_status_string.argtypes, L.kvq_status_string.restype = [I32], C.c_char_p
     L.kvq_last_error.argtypes, L.kvq_last_error.restype = [], C.c_char_p
     L.kvq_profile_phase1_events.argtypes, L.kvq_profile_phase1_events.restype = [P, P], I32

@@ -387,3 +387,92 @@ def paged_append_decode_attend(cache: PagedKVCache, k_new: torch.Tensor, v_new: 
         out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
         "kvq_paged_append_decode_attend")
     return out
+
+
+def _need_host(name: str, t: torch.Tensor) -> None:
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor for the host-buffer call")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _host_out_ws(q, device, need, out, workspace):
+    B, Hq, n_q, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, pin_memory=True)
+    _need_host("out", out)
+    if out.dtype != torch.float32 or tuple(out.shape) != (B, Hq, n_q, D):
+        raise ValueError("out must be a float32 host tensor of q's shape")
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+    _need_cuda("workspace", workspace)
+    return out, workspace
+
+
+def append_decode_attend_host_workspace_bytes(cache: KVCache, kv_dtype, n_new: int, q_dtype, n_q_heads: int,
+                                              n_q: int, kv_len: int, chunk: int = 0) -> int:
+    return L.lib().kvq_append_decode_attend_host_workspace_bytes(C.byref(cache.struct), _DTYPES[kv_dtype], n_new,
+                                                                 _DTYPES[q_dtype], n_q_heads, n_q, kv_len, chunk)
+
+
+def append_decode_attend_host(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int, q: torch.Tensor,
+                              kv_len: int, causal: bool = False, q_pos0: int = 0, attn_scale: float | None = None,
+                              chunk: int = 0, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """append_decode_attend with host tensors (ideally pinned): the library copies k_new, v_new and
+    q to device staging in the workspace, runs the step and copies the f32 result back into the
+    host tensor `out`, returning once it is filled."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("q", q)):
+        _need_host(n, t)
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same shape and dtype")
+    Bk, H, n_new, Dk = k_new.shape
+    B, Hq, n_q, D = q.shape
+    if (Bk, H, Dk) != (cache.batch, cache.n_kv_heads, cache.head_dim) or B != cache.batch or D != cache.head_dim:
+        raise ValueError("k_new/q shape does not match the cache")
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    need = append_decode_attend_host_workspace_bytes(cache, k_new.dtype, n_new, q.dtype, Hq, n_q, kv_len, chunk)
+    out, workspace = _host_out_ws(q, cache.planes["k"]["payload"].device, need, out, workspace)
+    L.check(L.lib().kvq_append_decode_attend_host(
+        C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, pos0, q.data_ptr(),
+        _DTYPES[q.dtype], Hq, n_q, kv_len, int(bool(causal)), q_pos0, float(attn_scale), chunk, out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "kvq_append_decode_attend_host")
+    return out
+
+
+def paged_append_decode_attend_host_workspace_bytes(cache: PagedKVCache, kv_dtype, n_new: int, q_dtype,
+                                                    n_q_heads: int, n_q: int, max_kv_len: int, chunk: int = 0) -> int:
+    return L.lib().kvq_paged_append_decode_attend_host_workspace_bytes(
+        C.byref(cache.struct), _DTYPES[kv_dtype], n_new, _DTYPES[q_dtype], n_q_heads, n_q, max_kv_len, chunk)
+
+
+def paged_append_decode_attend_host(cache: PagedKVCache, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                                    seq_lens: torch.Tensor, max_kv_len: int, causal: bool = False,
+                                    attn_scale: float | None = None, chunk: int = 0,
+                                    out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                    stream=None) -> torch.Tensor:
+    """paged_append_decode_attend with host tensors (seq_lens: host int32 [batch]); returns once the
+    host tensor `out` holds the result."""
+    for n, t in (("k_new", k_new), ("v_new", v_new), ("q", q), ("seq_lens", seq_lens)):
+        _need_host(n, t)
+    if seq_lens.dtype != torch.int32 or seq_lens.numel() != cache.batch:
+        raise ValueError(f"seq_lens must be a host int32 tensor of {cache.batch} entries")
+    if k_new.shape != v_new.shape or k_new.dtype != v_new.dtype:
+        raise ValueError("k_new and v_new must have the same shape and dtype")
+    Bk, H, n_new, Dk = k_new.shape
+    B, Hq, n_q, D = q.shape
+    if (Bk, H, Dk) != (cache.batch, cache.n_kv_heads, cache.head_dim) or B != cache.batch or D != cache.head_dim:
+        raise ValueError("k_new/q shape does not match the cache")
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    need = paged_append_decode_attend_host_workspace_bytes(cache, k_new.dtype, n_new, q.dtype, Hq, n_q, max_kv_len,
+                                                           chunk)
+    out, workspace = _host_out_ws(q, cache.planes["k"]["payload"].device, need, out, workspace)
+    L.check(L.lib().kvq_paged_append_decode_attend_host(
+        C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, q.data_ptr(),
+        _DTYPES[q.dtype], Hq, n_q, seq_lens.data_ptr(), max_kv_len, int(bool(causal)), float(attn_scale), chunk,
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "kvq_paged_append_decode_attend_host")
+    return out

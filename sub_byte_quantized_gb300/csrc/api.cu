@@ -408,6 +408,82 @@ cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool even
   return e;
 }
 
+// The append (when n_new > 0) and the attention of a validated append + attend call.
+cudaError_t launch_append_attend(const kvq::CacheView &v, kvq::AttendArgs &a, const void *k_new, const void *v_new,
+                                 int kv_dtype, int n_new, int pos0, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (n_new > 0) {
+    e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, pos0, s);
+    a.fresh_lo = pos0;                                   // the rows (and window slots) it writes
+    a.fresh_hi = pos0 + n_new;
+  }
+  if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
+  return e;
+}
+
+size_t dtype_bytes(int32_t dt) { return dt == KVQ_F32 ? 4 : 2; }
+
+// Device staging of a host-buffer call, in the caller's workspace after the attention partials:
+// k_new, v_new, q, out and (paged) seq_lens, each from a 256-byte boundary.
+struct HostStaging {
+  size_t k = 0, v = 0, q = 0, out = 0, lens = 0, total = 0;
+  size_t kv_bytes = 0, q_bytes = 0, out_bytes = 0, lens_bytes = 0;
+};
+
+HostStaging host_staging(size_t attend_need, int batch, int n_kv_heads, int head_dim, int kv_dtype, int n_new,
+                         int q_dtype, int n_q_heads, int n_q, bool paged) {
+  HostStaging h;
+  h.kv_bytes = n_new > 0 ? (size_t)batch * n_kv_heads * n_new * head_dim * dtype_bytes(kv_dtype) : 0;
+  h.q_bytes = (size_t)batch * n_q_heads * n_q * head_dim * dtype_bytes(q_dtype);
+  h.out_bytes = (size_t)batch * n_q_heads * n_q * head_dim * sizeof(float);
+  h.lens_bytes = paged ? (size_t)batch * sizeof(int32_t) : 0;
+  h.k = round_up(attend_need, 256);
+  h.v = h.k + round_up(h.kv_bytes, 256);
+  h.q = h.v + round_up(h.kv_bytes, 256);
+  h.out = h.q + round_up(h.q_bytes, 256);
+  h.lens = h.out + round_up(h.out_bytes, 256);
+  h.total = h.lens + round_up(h.lens_bytes, 256);
+  return h;
+}
+
+// The element types and row count that size a host-buffer call's staging.
+kvq_status check_host_sizes(int kv_dtype, int n_new, int q_dtype) {
+  if (q_dtype < KVQ_F32 || q_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown q dtype %d", q_dtype);
+  if (kv_dtype < KVQ_F32 || kv_dtype > KVQ_F16) return fail(KVQ_EINVAL, "unknown dtype %d", kv_dtype);
+  if (n_new < 0) return fail(KVQ_EINVAL, "n_new must be >= 0");
+  return KVQ_OK;
+}
+
+// The host-side arguments of a host-buffer call that the device entry points cannot see.
+kvq_status check_host_args(int kv_dtype, int n_new, int q_dtype, const void *k_new, const void *v_new, const void *q,
+                           const float *out, const void *workspace) {
+  const kvq_status st = check_host_sizes(kv_dtype, n_new, q_dtype);
+  if (st != KVQ_OK) return st;
+  if (n_new > 0 && (!k_new || !v_new)) return fail(KVQ_EINVAL, "k_new/v_new is NULL");
+  if (!q || !out || !workspace) return fail(KVQ_EINVAL, "q/out/workspace is NULL");
+  return KVQ_OK;
+}
+
+// Host -> staging copies of the inputs (cudaMemcpyDefault: pinned or pageable host memory).
+cudaError_t copy_in(const HostStaging &h, char *ws, const void *k_new, const void *v_new, const void *q,
+                    const void *seq_lens, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (h.kv_bytes) {
+    e = cudaMemcpyAsync(ws + h.k, k_new, h.kv_bytes, cudaMemcpyDefault, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + h.v, v_new, h.kv_bytes, cudaMemcpyDefault, s);
+  }
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + h.q, q, h.q_bytes, cudaMemcpyDefault, s);
+  if (e == cudaSuccess && h.lens_bytes) e = cudaMemcpyAsync(ws + h.lens, seq_lens, h.lens_bytes, cudaMemcpyDefault, s);
+  return e;
+}
+
+// Staging -> host copy of the output, then wait for the stream.
+cudaError_t copy_out_and_wait(const HostStaging &h, const char *ws, float *out, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(out, ws + h.out, h.out_bytes, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e;
+}
+
 }  // namespace
 
 kvq_status kvq_decode_attend(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
@@ -436,14 +512,8 @@ kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, c
   st = prepare_attend(cache, q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk, out, workspace,
                       workspace_bytes, a);
   if (st != KVQ_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
-  if (n_new > 0) {
-    e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, pos0, s);
-    a.fresh_lo = pos0;                                   // the rows (and window slots) it writes
-    a.fresh_hi = pos0 + n_new;
-  }
-  if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
+  const cudaError_t e = launch_append_attend(v, a, k_new, v_new, kv_dtype, n_new, pos0,
+                                             reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "append/attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
@@ -499,6 +569,19 @@ kvq_status prepare_paged(const kvq_paged_cache *cache, const void *q, int32_t q_
   a.scale = attn_scale;
   a.out = out;
   return KVQ_OK;
+}
+
+cudaError_t launch_paged_append_attend(const kvq::CacheView &v, kvq::AttendArgs &a, const void *k_new,
+                                       const void *v_new, int kv_dtype, int n_new, const int32_t *seq_lens,
+                                       cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if (n_new > 0) {
+    // the new tokens end each sequence: positions seq_lens[b] - n_new + j
+    e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, 0, s, seq_lens, -n_new);
+    a.fresh_tail = n_new;                                 // the rows (and window slots) it writes
+  }
+  if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
+  return e;
 }
 
 }  // namespace
@@ -628,15 +711,99 @@ kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const vo
   st = prepare_paged(cache, q, q_dtype, n_q_heads, n_q, seq_lens, max_kv_len, causal, attn_scale, chunk, out,
                      workspace, workspace_bytes, a);
   if (st != KVQ_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
-  if (n_new > 0) {
-    // the new tokens end each sequence: positions seq_lens[b] - n_new + j
-    e = kvq::launch_store(v, k_new, v_new, kv_dtype, n_new, 0, s, seq_lens, -n_new);
-    a.fresh_tail = n_new;                                 // the rows (and window slots) it writes
-  }
-  if (e == cudaSuccess) e = launch_attend_sequence(a, s, true);
+  const cudaError_t e = launch_paged_append_attend(v, a, k_new, v_new, kv_dtype, n_new, seq_lens,
+                                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "append/attend launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+// ------------------------------------------------------------------ host-buffer calls
+size_t kvq_append_decode_attend_host_workspace_bytes(const kvq_cache *cache, int32_t kv_dtype, int32_t n_new,
+                                                     int32_t q_dtype, int32_t n_q_heads, int32_t n_q,
+                                                     int32_t kv_len, int32_t chunk) {
+  kvq::AttendArgs a;
+  size_t need = 0;
+  if (resolve_attend(cache, n_q_heads, n_q, kv_len, 0, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  if (check_host_sizes(kv_dtype, n_new, q_dtype) != KVQ_OK) return 0;
+  return host_staging(need, cache->batch, cache->n_kv_heads, cache->head_dim, kv_dtype, n_new, q_dtype, n_q_heads,
+                      n_q, false).total;
+}
+
+kvq_status kvq_append_decode_attend_host(const kvq_cache *cache, const void *k_new, const void *v_new,
+                                         int32_t kv_dtype, int32_t n_new, int32_t pos0, const void *q,
+                                         int32_t q_dtype, int32_t n_q_heads, int32_t n_q, int32_t kv_len,
+                                         int32_t causal, int32_t q_pos0, float attn_scale, int32_t chunk,
+                                         float *out, void *workspace, size_t workspace_bytes,
+                                         kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  size_t need = 0;
+  kvq_status st = resolve_attend(cache, n_q_heads, n_q, kv_len, causal, q_pos0, chunk, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  st = check_host_args(kv_dtype, n_new, q_dtype, k_new, v_new, q, out, workspace);
+  if (st != KVQ_OK) return st;
+  const HostStaging h = host_staging(need, cache->batch, cache->n_kv_heads, cache->head_dim, kv_dtype, n_new,
+                                     q_dtype, n_q_heads, n_q, false);
+  if (workspace_bytes < h.total)
+    return fail(KVQ_EWORKSPACE, "workspace %zu < required %zu", workspace_bytes, h.total);
+  char *ws = static_cast<char *>(workspace);
+  // both parts validated against the staging addresses before anything is enqueued
+  kvq::CacheView v;
+  st = check_store(-1, cache, ws + h.k, ws + h.v, kv_dtype, n_new, pos0, v);
+  if (st != KVQ_OK) return st;
+  st = prepare_attend(cache, ws + h.q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk,
+                      reinterpret_cast<float *>(ws + h.out), workspace, need, a);
+  if (st != KVQ_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = copy_in(h, ws, k_new, v_new, q, nullptr, s);
+  if (e == cudaSuccess) e = launch_append_attend(v, a, ws + h.k, ws + h.v, kv_dtype, n_new, pos0, s);
+  if (e == cudaSuccess) e = copy_out_and_wait(h, ws, out, s);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "host-buffer append/attend: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+size_t kvq_paged_append_decode_attend_host_workspace_bytes(const kvq_paged_cache *cache, int32_t kv_dtype,
+                                                           int32_t n_new, int32_t q_dtype, int32_t n_q_heads,
+                                                           int32_t n_q, int32_t max_kv_len, int32_t chunk) {
+  kvq::AttendArgs a;
+  size_t need = 0;
+  if (resolve_paged(cache, n_q_heads, n_q, max_kv_len, 0, chunk, a, need, nullptr) != KVQ_OK) return 0;
+  if (check_host_sizes(kv_dtype, n_new, q_dtype) != KVQ_OK) return 0;
+  return host_staging(need, cache->batch, cache->n_kv_heads, cache->head_dim, kv_dtype, n_new, q_dtype, n_q_heads,
+                      n_q, true).total;
+}
+
+kvq_status kvq_paged_append_decode_attend_host(const kvq_paged_cache *cache, const void *k_new, const void *v_new,
+                                               int32_t kv_dtype, int32_t n_new, const void *q, int32_t q_dtype,
+                                               int32_t n_q_heads, int32_t n_q, const int32_t *seq_lens,
+                                               int32_t max_kv_len, int32_t causal, float attn_scale, int32_t chunk,
+                                               float *out, void *workspace, size_t workspace_bytes,
+                                               kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  size_t need = 0;
+  kvq_status st = resolve_paged(cache, n_q_heads, n_q, max_kv_len, causal, chunk, a, need, nullptr);
+  if (st != KVQ_OK) return st;
+  st = check_host_args(kv_dtype, n_new, q_dtype, k_new, v_new, q, out, workspace);
+  if (st != KVQ_OK) return st;
+  if (!seq_lens) return fail(KVQ_EINVAL, "seq_lens is NULL");
+  const HostStaging h = host_staging(need, cache->batch, cache->n_kv_heads, cache->head_dim, kv_dtype, n_new,
+                                     q_dtype, n_q_heads, n_q, true);
+  if (workspace_bytes < h.total)
+    return fail(KVQ_EWORKSPACE, "workspace %zu < required %zu", workspace_bytes, h.total);
+  char *ws = static_cast<char *>(workspace);
+  const int32_t *lens = reinterpret_cast<const int32_t *>(ws + h.lens);
+  kvq::CacheView v;
+  st = check_paged_store(cache, ws + h.k, ws + h.v, kv_dtype, n_new, lens, v);
+  if (st != KVQ_OK) return st;
+  st = prepare_paged(cache, ws + h.q, q_dtype, n_q_heads, n_q, lens, max_kv_len, causal, attn_scale, chunk,
+                     reinterpret_cast<float *>(ws + h.out), workspace, need, a);
+  if (st != KVQ_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = copy_in(h, ws, k_new, v_new, q, seq_lens, s);
+  if (e == cudaSuccess) e = launch_paged_append_attend(v, a, ws + h.k, ws + h.v, kv_dtype, n_new, lens, s);
+  if (e == cudaSuccess) e = copy_out_and_wait(h, ws, out, s);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "host-buffer paged append/attend: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
 

@@ -15,13 +15,16 @@
 // scale of V is folded into the probabilities, P' = p * s_v, kept as hi + lo f16 parts (p is
 // split once per tile, and each block's scale is applied with an exact f16 TwoProduct).
 //
-// Data movement: each warp pulls its chunk HBM -> shared memory in 64-token stages with
-// 16-byte cp.async (two stages in flight per warp). Payload rows
+// Data movement: each warp pulls its chunk HBM -> shared memory in 32-token stages with
+// 16-byte cp.async (two stages in flight per warp; measured on GB300, 64-token stages or deeper
+// rings, i.e. more bytes in flight, were slower at the same occupancy). Payload rows
 // (64 bytes) are placed with a 64-byte XOR swizzle (16-byte column ^= (row / 2) % 4) so that the
 // ldmatrix reads (8 rows x 16 bytes per phase) are bank-conflict free. ldmatrix gives each lane
 // the nibble words of its fragment: plain for K (one token, 8 consecutive dims), transposed for
-// V (two tokens, 4 consecutive dims). The nibbles become f16 pairs with one lop3 (mask + magic
-// exponent 0x6400, the Q4_0 sign flip folded in) and one f16 subtract/fma, all exact.
+// V (two tokens, 4 consecutive dims). K nibbles (and the Hadamard and asymmetric V nibbles)
+// become exact subnormal f16 pairs with one lop3 each, the code offset going into a separate
+// term; Q4_0 V nibbles become exact signed f16 values with one lop3 (mask + magic exponent
+// 0x6400, the sign flip folded in) and one f16 subtract/fma.
 //
 // Each CTA handles one chunk of one (batch, kv head); each of its four warps streams a contiguous
 // quarter of the chunk through a private two-stage shared-memory ring and keeps its online
@@ -38,7 +41,16 @@ namespace {
 using namespace mma;
 
 constexpr int kWarps = 4;
-constexpr int kStage = 64;              // tokens per pipeline stage (four 16-token tiles)
+#ifndef KVQ_MMA_STAGE
+#define KVQ_MMA_STAGE 32
+#endif
+constexpr int kStage = KVQ_MMA_STAGE;   // tokens per pipeline stage (16-token tiles)
+#ifndef KVQ_MMA_RING
+#define KVQ_MMA_RING 2
+#endif
+constexpr int kRing = KVQ_MMA_RING;     // stages per warp in flight
+static_assert(kStage % 16 == 0 && 64 % kStage == 0, "a stage is whole tiles and never straddles a 64-token page");
+static_assert(kRing >= 2, "at least one stage loads while another is read");
 constexpr int kTiles = kStage / 16;
 constexpr int kMinBlocks = KVQ_MMA_MIN_BLOCKS; // resident CTAs per SM
 constexpr int kD = 128;
@@ -63,8 +75,10 @@ __host__ __device__ constexpr int stage_bytes() { return L == KVQ_ASYM4_G32 ? of
 constexpr int kQScratch = 8 * 128 + 8 * 4;
 template <int L>
 __host__ __device__ constexpr int smem_bytes() {
-  return kWarps * 2 * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
+  return kWarps * kRing * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
 }
+// the warps' final (m, l, o) states reuse the stage buffers
+static_assert(kWarps * 8 * (2 + kD) * 4 <= kWarps * kRing * stage_bytes<KVQ_Q4_0>(), "combine buffer fits");
 
 // Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
 __device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &sl, int r) {
@@ -88,7 +102,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const CacheView &cv = a.cache;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
-  // One chunk per CTA; warp w takes a contiguous quarter of the chunk's 64-token stages.
+  // One chunk per CTA; warp w takes a contiguous quarter of the chunk's stages.
   const int chunk_id = blockIdx.x;
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
@@ -114,7 +128,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const int tw0 = t0 + s_first * kStage;                 // this warp's first token
 
   // ---- per-warp stage pipeline
-  uint8_t *wbuf = smem + warp * 2 * STAGE_BYTES;
+  uint8_t *wbuf = smem + warp * kRing * STAGE_BYTES;
   // contiguous cache: the planes' rows of token 0 of this (batch, kv head)
   const size_t head_row0 = (size_t)bh * cv.cap;
   const uint8_t *kp0 = cv.payload[0] + head_row0 * kRowBytes, *vp0 = cv.payload[1] + head_row0 * kRowBytes;
@@ -126,7 +140,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   auto issue = [&](int i) {
     if (i < n_mine) {
       const int ts = tw0 + i * kStage;
-      // the stage's 64 rows are consecutive plane rows (a page holds at least 64 aligned tokens)
+      // the stage's rows are consecutive plane rows (a page holds at least 64 aligned tokens)
       size_t r0 = (size_t)ts;                             // row offset from the base pointers
       const uint8_t *kb = kp0, *vb = vp0, *ksb = ksc0, *vsb = vsc0;
       const __half *kzb = kz0, *vzb = vz0;
@@ -140,7 +154,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       const uint8_t *ksc = ksb + r0 * SCB, *vsc = vsb + r0 * SCB;
       const __half *kz = ASYM ? kzb + r0 * 4 : nullptr;
       const __half *vz = ASYM ? vzb + r0 * 4 : nullptr;
-      uint8_t *sb = wbuf + (i & 1) * STAGE_BYTES;
+      uint8_t *sb = wbuf + (i % kRing) * STAGE_BYTES;
       const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
       if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
         const uint8_t *kps = kp, *vps = vp;
@@ -152,8 +166,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           cp_async16(sV + swz(row, j), vps + 16 * q, 16);
         }
 #pragma unroll
-        for (int k = 0; k < kStage / 32; ++k) {
+        for (int k = 0; k < (kStage + 31) / 32; ++k) {
           const int row = lane + 32 * k;
+          if (kStage % 32 && row >= kStage) break;
           const size_t tok = (size_t)row;
           cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, SCB);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, SCB);
@@ -173,8 +188,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
         }
 #pragma unroll
-        for (int k = 0; k < kStage / 32; ++k) {
+        for (int k = 0; k < (kStage + 31) / 32; ++k) {
           const int row = lane + 32 * k;
+          if (kStage % 32 && row >= kStage) break;
           const bool ok = ts + row < t_end;
           const size_t tok = (size_t)(ok ? row : 0);
           cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, ok ? SCB : 0);
@@ -188,9 +204,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     }
     cp_async_commit();                                   // always one group per call
   };
-  // start streaming the first two stages before the query prologue so their latency overlaps it
-  issue(0);
-  issue(1);
+  // start streaming the first stages before the query prologue so their latency overlaps it
+#pragma unroll
+  for (int i = 0; i < kRing; ++i) issue(i);
 
   // ---- query fragments (B operand of QK): row g of the group, dims 32b + 8c + 0..7
   uint32_t bq_hi[8][2], bq_lo[QSPLIT ? 8 : 1][2];
@@ -201,7 +217,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     // the group (warp FWHT, int8 codes, one f32 scale per row), parks the codes in its shared
     // scratch and reads them back in fragment order. The int8 codes are exact in f16; the row's
     // s_q goes into its alpha and -8 * sum(q8) into the accumulator start value.
-    uint8_t *qs8 = smem + kWarps * 2 * STAGE_BYTES + warp * kQScratch;
+    uint8_t *qs8 = smem + kWarps * kRing * STAGE_BYTES + warp * kQScratch;
     float *qsq = reinterpret_cast<float *>(qs8 + 8 * 128);
     for (int r = 0; r < R; ++r) {
       const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
@@ -320,9 +336,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const int lim1 = r1 < R ? row_limit_of(a, sl, r1) : -1;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   float O[4][2][4];                                      // [block][half][c0..c3]
-  // ASYM: Dw[b][r] = sum_t p_t * z_v[t][b] (the zero-point term), from a small extra mma per
-  // tile: rows 0-3 of its accumulator are the four blocks (held by lanes with g < 4), columns
-  // the query rows.
+  // Dw[b][r] = sum_t P'_t * f[t][b], the V offset term (asymmetric: f = z_v, with P' = p;
+  // Hadamard: f = 1, with P' = p s_v, where all rows hold the same sum), from a small extra mma
+  // per tile: rows 0-3 of its accumulator are the four blocks (held by lanes with g < 4),
+  // columns the query rows.
   float Dw[4] = {0.f, 0.f, 0.f, 0.f};
   // selector pairing halfword (g & 1) of two words, and which word (g < 2: blocks 0,1)
   const uint32_t wsel = (g & 1) ? 0x7632u : 0x5410u;
@@ -335,9 +352,9 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   }
 
   for (int i = 0; i < n_mine; ++i) {
-    cp_async_wait1();
+    cp_async_wait<kRing - 1>();
     __syncwarp();
-    const uint8_t *sb = wbuf + (i & 1) * STAGE_BYTES;
+    const uint8_t *sb = wbuf + (i % kRing) * STAGE_BYTES;
     const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
     const int ts = tw0 + i * kStage;
 
@@ -517,12 +534,23 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         bl0 = movm_t(l01);
         bl1 = movm_t(l23);
       }
+      // Hadamard and asymmetric V codes enter as exact subnormals u * 2^-24 (Hadamard: u = code + 8),
+      // so every output needs an offset sum_t P'_t * f_t per 32-dim block and query row, with
+      // f = -8 (Hadamard; s_v is already in P') or z_v (asymmetric). It comes from one small mma
+      // per tile: rows g < 4 of its A operand hold block g's factor for tokens (2c, 2c+1) and
+      // (2c+8, 2c+9) (rows 4-7 are don't-care outputs, rows 8-15 zero), the B operand is the p
+      // split already made; the -8 is applied in the epilogue. Q4_0 V codes become exact signed
+      // f16 values instead (lop3 + one f16 fix-up per pair): on that path the W mma's operand
+      // selection costs more registers than the fix-up saves.
       if (HAD) {
+        const uint32_t Aw[4] = {0x3C003C00u, 0u, 0x3C003C00u, 0u};     // f16 1.0 pairs
+        mma16816(Dw, Aw, bh0, bh1);
+        mma16816(Dw, Aw, bl0, bl1);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           uint32_t ua[4], ub[4];
-          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
-          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
+          unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 0], ua);
+          unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 1], ub);
           const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};
           const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};
           mma16816(O[b][0], A0, bh0, bh1);
@@ -542,18 +570,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
                                __byte_perm(sa.y, sbv.y, 0x5410), __byte_perm(sa.y, sbv.y, 0x7632)};
       const uint32_t sp1[4] = {__byte_perm(sc.x, sd.x, 0x5410), __byte_perm(sc.x, sd.x, 0x7632),
                                __byte_perm(sc.y, sd.y, 0x5410), __byte_perm(sc.y, sd.y, 0x7632)};
-      if (ASYM) {
-        // W operand (zero-points): rows g < 4 hold block g's z_v for tokens (2c, 2c+1) and
-        // (2c+8, 2c+9)
+      if (ASYM) {                                        // W operand: the V zero-points
         const uint8_t *zvb = sb + OFF_ZV + tile * 16 * 8;
         const uint2 wa = *reinterpret_cast<const uint2 *>(zvb + (2 * c) * 8);
         const uint2 wb = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 1) * 8);
         const uint2 wc = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 8) * 8);
         const uint2 wd = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 9) * 8);
-        const bool lo2 = g < 2;
-        uint32_t w0 = __byte_perm(lo2 ? wa.x : wa.y, lo2 ? wb.x : wb.y, wsel);
-        uint32_t w1 = __byte_perm(lo2 ? wc.x : wc.y, lo2 ? wd.x : wd.y, wsel);
-        if (g >= 4) w0 = w1 = 0u;
+        const bool lo2 = (g & 2) == 0;
+        const uint32_t w0 = __byte_perm(lo2 ? wa.x : wa.y, lo2 ? wb.x : wb.y, wsel);
+        const uint32_t w1 = __byte_perm(lo2 ? wc.x : wc.y, lo2 ? wd.x : wd.y, wsel);
         const uint32_t Aw[4] = {w0, 0u, w1, 0u};
         mma16816(Dw, Aw, bh0, bh1);
         mma16816(Dw, Aw, bl0, bl1);
@@ -566,7 +591,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         const uint32_t r0 = hfma2(bh0, sp0[b], hi0 ^ 0x80008000u), r1 = hfma2(bh1, sp1[b], hi1 ^ 0x80008000u);
         const uint32_t lo0 = hfma2(bl0, sp0[b], r0), lo1 = hfma2(bl1, sp1[b], r1);
         // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
-        // Q4_0: exact signed code values (f16 fix-up); asymmetric: subnormal codes u * 2^-24
         uint32_t ua[4], ub[4];
         if (ASYM) {
           unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 0], ua);
@@ -584,7 +608,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       }
     }
     __syncwarp();                                        // buffer fully read before reuse
-    issue(i + 2);
+    issue(i + kRing);
   }
 
   // ---------------- warp state: reduce l (and the zero-point sums) over the token lanes
@@ -606,16 +630,18 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     cl[warp * 8 + r0] = l0;
     cl[warp * 8 + r1] = l1;
   }
-  // Q4_0: O holds the values directly. Asymmetric: the V codes entered as u * 2^-24 (even dims,
-  // low fields) or 16 u * 2^-24 (odd dims, high fields); value = u s_v + z_v adds the W term.
+  // Q4_0: O holds the values directly. Hadamard / asymmetric: the V codes entered as u * 2^-24
+  // (even dims, low fields) or 16 u * 2^-24 (odd dims, high fields); the offset term (-8 x the
+  // W sums, or + the zero-point sums) completes each value.
+  constexpr bool SUBV = HAD || ASYM;
+  constexpr float kWf = ASYM ? 1.0f : -8.0f;
+  constexpr float se = SUBV ? 16777216.0f : 1.0f, so = SUBV ? 1048576.0f : 1.0f;
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
-    float w0 = 0.0f, w1 = 0.0f, se = 1.0f, so = 1.0f;
-    if (ASYM) {
-      w0 = __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);   // (block b, row r0)
-      w1 = __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);   // (block b, row r1)
-      se = 16777216.0f;
-      so = 1048576.0f;
+    float w0 = 0.0f, w1 = 0.0f;
+    if (SUBV) {
+      w0 = kWf * __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);   // (block b, row r0)
+      w1 = kWf * __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);   // (block b, row r1)
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {

@@ -216,3 +216,55 @@ def test_paged_plan_chunk(L):
     small = np.array([4096, 5], np.int32)
     assert L.kvq_paged_attend_plan_chunk(p(c), 8, 1, 1, small.ctypes.data) <= ch
     assert L.kvq_paged_attend_plan_chunk(p(c), 8, 1, 1, None) == 0
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+def test_host_call_workspace_and_validation(L):
+    """The host-buffer calls: workspace = the attention partials + device staging of k_new, v_new,
+    q, out (and seq_lens); every argument is rejected before anything is enqueued."""
+    p = C.byref
+    c = _cache()                                           # batch 1, 2 kv heads, D 128, capacity 64
+    att = L.kvq_attend_workspace_bytes(p(c), 8, 1, 64, 64)
+    kvb, qb, ob = 1 * 2 * 3 * 128 * 2, 1 * 8 * 1 * 128 * 2, 1 * 8 * 1 * 128 * 4   # 3 bf16 rows, bf16 q
+    assert L.kvq_append_decode_attend_host_workspace_bytes(p(c), 1, 3, 1, 8, 1, 64, 64) == \
+        _r256(att) + 2 * _r256(kvb) + _r256(qb) + _r256(ob)
+    # f32 q doubles the q staging; n_new 0 stages no rows; invalid dtypes size nothing
+    assert L.kvq_append_decode_attend_host_workspace_bytes(p(c), 1, 0, 0, 8, 1, 64, 64) == \
+        _r256(att) + _r256(2 * qb) + _r256(ob)
+    assert L.kvq_append_decode_attend_host_workspace_bytes(p(c), 7, 3, 1, 8, 1, 64, 64) == 0
+    assert L.kvq_append_decode_attend_host_workspace_bytes(p(c), 1, 3, 5, 8, 1, 64, 64) == 0
+    ws = 1 << 20
+    # NULL host q / out / k_new, unknown dtype, workspace too small or misaligned, capacity, shape
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 1, 7, None, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws,
+                                           None) == 1
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, None, 256, ws,
+                                           None) == 1
+    assert L.kvq_append_decode_attend_host(p(c), None, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws,
+                                           None) == 1
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 9, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws,
+                                           None) == 1
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 300,
+                                           None) == 7
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 272, ws,
+                                           None) == 5
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 10, 60, 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, ws,
+                                           None) == 3
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 1, 7, 16, 1, 7, 1, 8, 0, 0, 1.0, 0, 16, 256, ws,
+                                           None) == 2
+    assert L.kvq_append_decode_attend_host(p(c), 16, 16, 1, 1, 7, 16, 1, 8, 1, 8, 0, 0, float("inf"), 0, 16, 256,
+                                           ws, None) == 1
+    # paged: NULL host seq_lens, staging sized with the lengths
+    pc = _paged()
+    att = L.kvq_paged_attend_workspace_bytes(p(pc), 8, 1, 256, 128)
+    kvb, qb, ob = 2 * 2 * 1 * 128 * 2, 2 * 8 * 1 * 128 * 2, 2 * 8 * 1 * 128 * 4
+    assert L.kvq_paged_append_decode_attend_host_workspace_bytes(p(pc), 1, 1, 1, 8, 1, 256, 128) == \
+        _r256(att) + 2 * _r256(kvb) + _r256(qb) + _r256(ob) + 256
+    assert L.kvq_paged_append_decode_attend_host(p(pc), 16, 16, 1, 1, 16, 1, 8, 1, None, 64, 0, 1.0, 0, 16, 256, ws,
+                                                 None) == 1
+    assert L.kvq_paged_append_decode_attend_host(p(pc), 16, 16, 1, 1, 16, 1, 8, 1, 16, 64, 0, 1.0, 0, 16, 256, 300,
+                                                 None) == 7
+    assert L.kvq_paged_append_decode_attend_host(p(pc), 16, 16, 1, 1, 16, 1, 8, 1, 16, 300, 0, 1.0, 0, 16, 256, ws,
+                                                 None) == 3
