@@ -1,7 +1,7 @@
-// Tensor-core phase 1 of the split-K decode attention for the 4-bit layouts (Q4_0, the asymmetric
-// g=32 layout and the per-token Hadamard int4 body), head_dim 128, up to 8 query rows per kv head
-// (the GQA group times the query rows of the call). For the Hadamard layout the exact-f32 recent
-// window is scored in phase 2.
+// Tensor-core phase 1 of the split-K decode attention for the block layouts with 4- and 8-bit
+// codes (Q4_0, Q8_0, Q4_0 keys with Q8_0 values, the asymmetric g=32 layout) and the per-token
+// Hadamard int4 body, head_dim 128, up to 8 query rows per kv head (the GQA group times the query
+// rows of the call). For the Hadamard layout the exact-f32 recent window is scored in phase 2.
 //
 // Why tensor cores: every kv head is shared by gqa query heads, so per packed K/V element the
 // step does 4*gqa flops (QK and PV); at gqa 8 that is ~57 flops per packed byte, beyond what
@@ -9,22 +9,23 @@
 // mma.sync.m16n8k16 (f16 in, f32 accumulate):
 //   QK:  S^T[16 tokens][8 rows] += K[16 tokens][16 dims] . Q^T[16 dims][8 rows]
 //   PV:  O^T[16 dims][8 rows]   += V^T[16 dims][16 tokens] . P'^T[16 tokens][8 rows]
-// Exactness: 4-bit codes are exact in f16; queries given in bf16/f16 are exact in f16 after a
-// per-row power-of-two prescale (f32 queries are split into hi + lo f16 parts); the block
+// Exactness: 4- and 8-bit codes are exact in f16; queries given in bf16/f16 are exact in f16
+// after a per-row power-of-two prescale (f32 queries are split into hi + lo f16 parts); the block
 // scale of K (per token and 32-dim block) multiplies each block's f32 partial sum; the block
 // scale of V is folded into the probabilities, P' = p * s_v, kept as hi + lo f16 parts (p is
 // split once per tile, and each block's scale is applied with an exact f16 TwoProduct).
 //
 // Data movement: each warp pulls its chunk HBM -> shared memory in 32-token stages with
 // 16-byte cp.async (two stages in flight per warp; measured on GB300, 64-token stages or deeper
-// rings, i.e. more bytes in flight, were slower at the same occupancy). Payload rows
-// (64 bytes) are placed with a 64-byte XOR swizzle (16-byte column ^= (row / 2) % 4) so that the
-// ldmatrix reads (8 rows x 16 bytes per phase) are bank-conflict free. ldmatrix gives each lane
-// the nibble words of its fragment: plain for K (one token, 8 consecutive dims), transposed for
-// V (two tokens, 4 consecutive dims). K nibbles (and the Hadamard and asymmetric V nibbles)
-// become exact subnormal f16 pairs with one lop3 each, the code offset going into a separate
-// term; Q4_0 V nibbles become exact signed f16 values with one lop3 (mask + magic exponent
-// 0x6400, the sign flip folded in) and one f16 subtract/fma.
+// rings, i.e. more bytes in flight, were slower at the same occupancy). Payload rows (64 bytes
+// for 4-bit codes, 128 for 8-bit) are placed with an XOR swizzle of their 16-byte columns so that
+// the ldmatrix reads (8 rows x 16 bytes per phase) are bank-conflict free. ldmatrix gives each
+// lane the code words of its fragment: plain for K (one token, 8 consecutive dims of 4-bit codes
+// or 4 of 8-bit codes), transposed for V (two tokens, 4 consecutive dims of 4-bit codes or 2 of
+// 8-bit codes). K codes (and the Hadamard and asymmetric V nibbles) become exact subnormal f16
+// values u * 2^-24 of the offset code u (one lop3 per nibble pair; one byte permute per 8-bit
+// pair), the offset going into the accumulator's initial value or a separate term; Q4_0 and Q8_0
+// V codes become exact signed f16 values (the code under the exponent of 1024, one f16 add).
 //
 // Each CTA handles one chunk of one (batch, kv head); each of its four warps streams a contiguous
 // quarter of the chunk through a private two-stage shared-memory ring and keeps its online
@@ -54,47 +55,79 @@ static_assert(kRing >= 2, "at least one stage loads while another is read");
 constexpr int kTiles = kStage / 16;
 constexpr int kMinBlocks = KVQ_MMA_MIN_BLOCKS; // resident CTAs per SM
 constexpr int kD = 128;
-constexpr int kRowBytes = 64;
-constexpr int kOffV = kStage * 64, kOffSK = 2 * kStage * 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Stage buffer: K payload, V payload (swizzled 64-byte rows), K and V scales (4 f16 per token,
-// or one f32 per token for the Hadamard layout), asymmetric zero-points (4 f16 per token).
+// Stage buffer: K payload, V payload (swizzled rows of 64 bytes for 4-bit codes, 128 bytes for
+// Q8_0), K and V scales (4 f16 per token, or one f32 per token for the Hadamard layout),
+// asymmetric zero-points (4 f16 per token).
+template <int L>
+__host__ __device__ constexpr int plane_row_bytes() { return L == KVQ_Q8_0 ? 128 : 64; }
 template <int L>
 __host__ __device__ constexpr int scale_bytes() { return L == KVQ_HAD_INT4 ? 4 : 8; }
-template <int L>
-__host__ __device__ constexpr int off_sv() { return kOffSK + kStage * scale_bytes<L>(); }
-template <int L>
-__host__ __device__ constexpr int off_zk() { return off_sv<L>() + kStage * scale_bytes<L>(); }
-template <int L>
-__host__ __device__ constexpr int off_zv() { return off_zk<L>() + kStage * 8; }
-template <int L>
-__host__ __device__ constexpr int stage_bytes() { return L == KVQ_ASYM4_G32 ? off_zv<L>() + kStage * 8 : off_zk<L>(); }
+template <int L, int VL>
+__host__ __device__ constexpr int off_v() { return kStage * plane_row_bytes<L>(); }
+template <int L, int VL>
+__host__ __device__ constexpr int off_sk() { return off_v<L, VL>() + kStage * plane_row_bytes<VL>(); }
+template <int L, int VL>
+__host__ __device__ constexpr int off_sv() { return off_sk<L, VL>() + kStage * scale_bytes<L>(); }
+template <int L, int VL>
+__host__ __device__ constexpr int off_zk() { return off_sv<L, VL>() + kStage * scale_bytes<VL>(); }
+template <int L, int VL>
+__host__ __device__ constexpr int off_zv() { return off_zk<L, VL>() + kStage * 8; }
+template <int L, int VL>
+__host__ __device__ constexpr int stage_bytes() {
+  return L == KVQ_ASYM4_G32 ? off_zv<L, VL>() + kStage * 8 : off_zk<L, VL>();
+}
 // Hadamard: per-warp scratch for the int8 query codes of up to 8 rows and their scales
 constexpr int kQScratch = 8 * 128 + 8 * 4;
-template <int L>
+template <int L, int VL>
 __host__ __device__ constexpr int smem_bytes() {
-  return kWarps * kRing * stage_bytes<L>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
+  return kWarps * kRing * stage_bytes<L, VL>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
 }
 // the warps' final (m, l, o) states reuse the stage buffers
-static_assert(kWarps * 8 * (2 + kD) * 4 <= kWarps * kRing * stage_bytes<KVQ_Q4_0>(), "combine buffer fits");
+static_assert(kWarps * 8 * (2 + kD) * 4 <= kWarps * kRing * stage_bytes<KVQ_HAD_INT4, KVQ_HAD_INT4>(),
+              "combine buffer fits");
+static_assert(smem_bytes<KVQ_Q8_0, KVQ_Q8_0>() * kMinBlocks <= 227 * 1024, "Q8_0 stages fit the resident CTAs");
 
 // Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
 __device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &sl, int r) {
   return row_limit(a, sl, r % a.n_q);
 }
 
-// Byte offset of (row, 16-byte column j) inside a swizzled 64-byte-row slab.
+// Byte offset of (row, 16-byte column j) inside a swizzled slab of RB-byte rows: the column is
+// XORed with bits of the row so that the 8 rows an ldmatrix phase reads at one column fall in
+// different banks (64-byte rows: (row / 2) % 4; 128-byte rows: row % 8).
+template <int RB>
 __device__ __forceinline__ uint32_t swz(int row, int j) {
-  return (uint32_t)(row * kRowBytes + ((j ^ ((row >> 1) & 3)) << 4));
+  return (uint32_t)(row * RB + ((j ^ (RB == 64 ? (row >> 1) & 3 : row & 7)) << 4));
 }
 
-template <int LAYOUT, bool QSPLIT, bool PAGED>
+// 8-bit K word (dims 4c..4c+3 of one token, two's complement codes) -> two f16 pairs holding the
+// exact subnormals u * 2^-24 of u = code + 128: dims (4c, 4c+1) and (4c+2, 4c+3).
+__device__ __forceinline__ void unpack4_s8_sub(uint32_t w, uint32_t &p01, uint32_t &p23) {
+  const uint32_t x = w ^ 0x80808080u;
+  p01 = __byte_perm(x, 0u, 0x4140);
+  p23 = __byte_perm(x, 0u, 0x4342);
+}
+// Transposed 8-bit V word (bytes: token 2c dims d, d+1, then token 2c+1 dims d, d+1) -> exact
+// signed f16 pairs (dim d of both tokens) and (dim d+1 of both tokens): the byte u = code + 128
+// goes under the exponent of 1024 and one f16 add removes 1152.
+__device__ __forceinline__ void unpack4_s8_t(uint32_t w, uint32_t &d0, uint32_t &d1) {
+  const uint32_t x = w ^ 0x80808080u;
+  d0 = hadd2(__byte_perm(x, 0x64646464u, 0x4240), 0xE480E480u);
+  d1 = hadd2(__byte_perm(x, 0x64646464u, 0x4341), 0xE480E480u);
+}
+
+template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
   constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = LAYOUT == KVQ_HAD_INT4;
-  constexpr int SCB = scale_bytes<LAYOUT>(), OFF_SV = off_sv<LAYOUT>(), OFF_ZK = off_zk<LAYOUT>();
-  constexpr int OFF_ZV = off_zv<LAYOUT>(), STAGE_BYTES = stage_bytes<LAYOUT>();
+  constexpr bool K8 = LAYOUT == KVQ_Q8_0, V8 = VLAYOUT == KVQ_Q8_0;   // 8-bit code planes
+  constexpr int KRB = plane_row_bytes<LAYOUT>(), VRB = plane_row_bytes<VLAYOUT>();
+  constexpr int SCB = scale_bytes<LAYOUT>(), OFF_V = off_v<LAYOUT, VLAYOUT>(), OFF_SK = off_sk<LAYOUT, VLAYOUT>();
+  constexpr int OFF_SV = off_sv<LAYOUT, VLAYOUT>(), OFF_ZK = off_zk<LAYOUT, VLAYOUT>();
+  constexpr int OFF_ZV = off_zv<LAYOUT, VLAYOUT>(), STAGE_BYTES = stage_bytes<LAYOUT, VLAYOUT>();
+  static_assert(VLAYOUT == LAYOUT || (LAYOUT == KVQ_Q4_0 && VLAYOUT == KVQ_Q8_0), "supported plane pairs");
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
@@ -131,7 +164,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   uint8_t *wbuf = smem + warp * kRing * STAGE_BYTES;
   // contiguous cache: the planes' rows of token 0 of this (batch, kv head)
   const size_t head_row0 = (size_t)bh * cv.cap;
-  const uint8_t *kp0 = cv.payload[0] + head_row0 * kRowBytes, *vp0 = cv.payload[1] + head_row0 * kRowBytes;
+  const uint8_t *kp0 = cv.payload[0] + head_row0 * KRB, *vp0 = cv.payload[1] + head_row0 * VRB;
   const uint8_t *ksc0 = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
   const uint8_t *vsc0 = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
   const __half *kz0 = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
@@ -150,27 +183,40 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         ksb = static_cast<const uint8_t *>(cv.scale[0]); vsb = static_cast<const uint8_t *>(cv.scale[1]);
         kzb = cv.zero[0]; vzb = cv.zero[1];
       }
-      const uint8_t *kp = kb + r0 * kRowBytes, *vp = vb + r0 * kRowBytes;
+      const uint8_t *kp = kb + r0 * KRB, *vp = vb + r0 * VRB;
       const uint8_t *ksc = ksb + r0 * SCB, *vsc = vsb + r0 * SCB;
       const __half *kz = ASYM ? kzb + r0 * 4 : nullptr;
       const __half *vz = ASYM ? vzb + r0 * 4 : nullptr;
       uint8_t *sb = wbuf + (i % kRing) * STAGE_BYTES;
-      const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
+      const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + OFF_V);
       if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
-        const uint8_t *kps = kp, *vps = vp;
+        if constexpr (KRB == VRB) {
+          constexpr int CPR = KRB / 16;                  // 16-byte pieces per row
 #pragma unroll
-        for (int k = 0; k < kStage / 8; ++k) {
-          const int q = lane + 32 * k;                   // 16-byte piece: row q/4, column q%4
-          const int row = q >> 2, j = q & 3;
-          cp_async16(sK + swz(row, j), kps + 16 * q, 16);
-          cp_async16(sV + swz(row, j), vps + 16 * q, 16);
+          for (int k = 0; k < kStage * CPR / 32; ++k) {
+            const int q = lane + 32 * k;                 // 16-byte piece: row q / CPR, column q % CPR
+            const int row = q / CPR, j = q % CPR;
+            cp_async16(sK + swz<KRB>(row, j), kp + 16 * q, 16);
+            cp_async16(sV + swz<VRB>(row, j), vp + 16 * q, 16);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kStage * (KRB / 16) / 32; ++k) {
+            const int q = lane + 32 * k;
+            cp_async16(sK + swz<KRB>(q / (KRB / 16), q % (KRB / 16)), kp + 16 * q, 16);
+          }
+#pragma unroll
+          for (int k = 0; k < kStage * (VRB / 16) / 32; ++k) {
+            const int q = lane + 32 * k;
+            cp_async16(sV + swz<VRB>(q / (VRB / 16), q % (VRB / 16)), vp + 16 * q, 16);
+          }
         }
 #pragma unroll
         for (int k = 0; k < (kStage + 31) / 32; ++k) {
           const int row = lane + 32 * k;
           if (kStage % 32 && row >= kStage) break;
           const size_t tok = (size_t)row;
-          cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, SCB);
+          cp_async_scale<SCB>(smem_addr(sb + OFF_SK + row * SCB), ksc + tok * SCB, SCB);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, SCB);
           if (ASYM) {
             cp_async8(smem_addr(sb + OFF_ZK + row * 8), kz + tok * 4, 8);
@@ -178,14 +224,32 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           }
         }
       } else {                                           // tail stage: rows past t_end are zero-filled
+        if constexpr (KRB == VRB) {
+          constexpr int CPR = KRB / 16;
 #pragma unroll
-        for (int k = 0; k < kStage / 8; ++k) {
-          const int q = lane + 32 * k;
-          const int row = q >> 2, j = q & 3;
-          const bool ok = ts + row < t_end;
-          const size_t off = (size_t)(ok ? row : 0) * kRowBytes + 16 * j;
-          cp_async16(sK + swz(row, j), kp + off, ok ? 16 : 0);
-          cp_async16(sV + swz(row, j), vp + off, ok ? 16 : 0);
+          for (int k = 0; k < kStage * CPR / 32; ++k) {
+            const int q = lane + 32 * k;
+            const int row = q / CPR, j = q % CPR;
+            const bool ok = ts + row < t_end;
+            const size_t off = (size_t)(ok ? row : 0) * KRB + 16 * j;
+            cp_async16(sK + swz<KRB>(row, j), kp + off, ok ? 16 : 0);
+            cp_async16(sV + swz<VRB>(row, j), vp + off, ok ? 16 : 0);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kStage * (KRB / 16) / 32; ++k) {
+            const int q = lane + 32 * k;
+            const int row = q / (KRB / 16), j = q % (KRB / 16);
+            const bool ok = ts + row < t_end;
+            cp_async16(sK + swz<KRB>(row, j), kp + (size_t)(ok ? row : 0) * KRB + 16 * j, ok ? 16 : 0);
+          }
+#pragma unroll
+          for (int k = 0; k < kStage * (VRB / 16) / 32; ++k) {
+            const int q = lane + 32 * k;
+            const int row = q / (VRB / 16), j = q % (VRB / 16);
+            const bool ok = ts + row < t_end;
+            cp_async16(sV + swz<VRB>(row, j), vp + (size_t)(ok ? row : 0) * VRB + 16 * j, ok ? 16 : 0);
+          }
         }
 #pragma unroll
         for (int k = 0; k < (kStage + 31) / 32; ++k) {
@@ -193,7 +257,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           if (kStage % 32 && row >= kStage) break;
           const bool ok = ts + row < t_end;
           const size_t tok = (size_t)(ok ? row : 0);
-          cp_async_scale<SCB>(smem_addr(sb + kOffSK + row * SCB), ksc + tok * SCB, ok ? SCB : 0);
+          cp_async_scale<SCB>(smem_addr(sb + OFF_SK + row * SCB), ksc + tok * SCB, ok ? SCB : 0);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, ok ? SCB : 0);
           if (ASYM) {
             cp_async8(smem_addr(sb + OFF_ZK + row * 8), kz + tok * 4, ok ? 8 : 0);
@@ -264,7 +328,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     float mx = 0.0f;
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      if (live) {
+      if (live && K8) {                                  // dims 32b + 4c + 0..3 and 32b + 16 + 4c + 0..3
+        load4_f32(a.q, a.q_dtype, grow * kD + 32 * b + 4 * c, x[b]);
+        load4_f32(a.q, a.q_dtype, grow * kD + 32 * b + 16 + 4 * c, x[b] + 4);
+      } else if (live) {                                 // dims 32b + 8c + 0..7
         load8_f32(a.q, a.q_dtype, grow * kD + 32 * b + 8 * c, x[b]);
       } else {
 #pragma unroll
@@ -295,6 +362,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       qsum[b] = s;
 #pragma unroll
       for (int st = 0; st < 2; ++st) {
+        if (K8) {
+          // 8-bit codes: k-step st covers dims 32b + 16 st + 4c + 0..3, in pairs (0, 1) and (2, 3)
+          bq_hi[2 * b + st][0] = pack_f16x2(h[4 * st], h[4 * st + 1]);
+          bq_hi[2 * b + st][1] = pack_f16x2(h[4 * st + 2], h[4 * st + 3]);
+          if (QSPLIT) {
+            bq_lo[2 * b + st][0] = pack_f16x2(l[4 * st], l[4 * st + 1]);
+            bq_lo[2 * b + st][1] = pack_f16x2(l[4 * st + 2], l[4 * st + 3]);
+          }
+          continue;
+        }
         // odd dims face the high 4-bit fields (16 u * 2^-24): their query entries are / 16
         bq_hi[2 * b + st][0] = pack_f16x2(h[2 * st], h[2 * st + 4]);
         bq_hi[2 * b + st][1] = pack_f16x2(h[2 * st + 1] * 0.0625f, h[2 * st + 5] * 0.0625f);
@@ -315,7 +392,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const float alpha0 = __shfl_sync(0xffffffffu, row_alpha, r0 * 4);
   const float alpha1 = __shfl_sync(0xffffffffu, row_alpha, r1 * 4);
   // zq: per-block row sums of q in accumulator units (x 2^-24). ASYM: multiplied by each token's
-  // zero-point; Q4_0: -8 zq is the accumulator's initial value (the codes enter as code + 8).
+  // zero-point; Q4_0 / Q8_0: -8 zq / -128 zq is the accumulator's initial value (the codes enter
+  // as code + 8 / code + 128).
   float zq0[4], zq1[4];
   {
 #pragma unroll
@@ -323,8 +401,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * 5.9604644775390625e-8f;
       zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * 5.9604644775390625e-8f;
       if (!ASYM) {
-        zq0[b] *= -8.0f;
-        zq1[b] *= -8.0f;
+        zq0[b] *= K8 ? -128.0f : -8.0f;
+        zq1[b] *= K8 ? -128.0f : -8.0f;
       }
     }
   }
@@ -355,7 +433,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     cp_async_wait<kRing - 1>();
     __syncwarp();
     const uint8_t *sb = wbuf + (i % kRing) * STAGE_BYTES;
-    const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + kOffV);
+    const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + OFF_V);
     const int ts = tw0 + i * kStage;
 
     // ---------------- scores S^T for the 4 tiles of the stage
@@ -363,11 +441,13 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
 #pragma unroll
     for (int tile = 0; tile < kTiles; ++tile) {
       uint32_t kw[2][4];
+      if constexpr (!K8) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int mi = lane >> 3;
-        const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
-        ldsm_x4(sK + swz(row, 2 * half + (mi >> 1)), kw[half]);
+        for (int half = 0; half < 2; ++half) {
+          const int mi = lane >> 3;
+          const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+          ldsm_x4(sK + swz<KRB>(row, 2 * half + (mi >> 1)), kw[half]);
+        }
       }
       if (HAD) {
         // one per-token scale: all 8 k-steps accumulate the exact integer dot (x 2^-24) in two
@@ -384,16 +464,16 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
           mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
         }
-        const float skg = *reinterpret_cast<const float *>(sb + kOffSK + (tile * 16 + g) * 4);
-        const float skg8 = *reinterpret_cast<const float *>(sb + kOffSK + (tile * 16 + g + 8) * 4);
+        const float skg = *reinterpret_cast<const float *>(sb + OFF_SK + (tile * 16 + g) * 4);
+        const float skg8 = *reinterpret_cast<const float *>(sb + OFF_SK + (tile * 16 + g + 8) * 4);
         s[tile][0] = (dA[0] + dB[0]) * skg * alpha0;
         s[tile][1] = (dA[1] + dB[1]) * skg * alpha1;
         s[tile][2] = (dA[2] + dB[2]) * skg8 * alpha0;
         s[tile][3] = (dA[3] + dB[3]) * skg8 * alpha1;
         continue;
       }
-      const uint2 skg = *reinterpret_cast<const uint2 *>(sb + kOffSK + (tile * 16 + g) * 8);
-      const uint2 skg8 = *reinterpret_cast<const uint2 *>(sb + kOffSK + (tile * 16 + g + 8) * 8);
+      const uint2 skg = *reinterpret_cast<const uint2 *>(sb + OFF_SK + (tile * 16 + g) * 8);
+      const uint2 skg8 = *reinterpret_cast<const uint2 *>(sb + OFF_SK + (tile * 16 + g + 8) * 8);
       const float2 sg01 = __half22float2(u32_as_h2(skg.x)), sg23 = __half22float2(u32_as_h2(skg.y));
       const float2 s801 = __half22float2(u32_as_h2(skg8.x)), s823 = __half22float2(u32_as_h2(skg8.y));
       const float skg_f[4] = {sg01.x, sg01.y, sg23.x, sg23.y};
@@ -410,12 +490,25 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       float acc_s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        // kw[b/2][(b%2)*2 + 0] = (token g, block b); [.. + 1] = (token g+8, block b)
-        uint32_t ug[4], u8[4];
-        unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 0], ug);
-        unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
-        const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
-        const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
+        uint32_t A0[4], A1[4];
+        if constexpr (K8) {
+          // block b = 16-byte columns 2b, 2b+1: kb[0] / kb[1] = tokens g / g+8, dims 32b + 4c..;
+          // kb[2] / kb[3] the same tokens, dims 32b + 16 + 4c..
+          uint32_t kb[4];
+          const int mi = lane >> 3;
+          ldsm_x4(sK + swz<KRB>(tile * 16 + (mi & 1) * 8 + (lane & 7), 2 * b + (mi >> 1)), kb);
+          unpack4_s8_sub(kb[0], A0[0], A0[2]);
+          unpack4_s8_sub(kb[1], A0[1], A0[3]);
+          unpack4_s8_sub(kb[2], A1[0], A1[2]);
+          unpack4_s8_sub(kb[3], A1[1], A1[3]);
+        } else {
+          // kw[b/2][(b%2)*2 + 0] = (token g, block b); [.. + 1] = (token g+8, block b)
+          uint32_t ug[4], u8[4];
+          unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 0], ug);
+          unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
+          A0[0] = ug[0]; A0[1] = u8[0]; A0[2] = ug[1]; A0[3] = u8[1];
+          A1[0] = ug[2]; A1[1] = u8[2]; A1[2] = ug[3]; A1[3] = u8[3];
+        }
         float d[4];
         if (ASYM) {
           d[0] = d[1] = d[2] = d[3] = 0.0f;
@@ -506,11 +599,13 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
 #pragma unroll
     for (int tile = 0; tile < kTiles; ++tile) {
       uint32_t vw[2][4];
+      if constexpr (!V8) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int mi = lane >> 3;
-        const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
-        ldsm_x4_t(sV + swz(row, 2 * half + (mi >> 1)), vw[half]);
+        for (int half = 0; half < 2; ++half) {
+          const int mi = lane >> 3;
+          const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
+          ldsm_x4_t(sV + swz<VRB>(row, 2 * half + (mi >> 1)), vw[half]);
+        }
       }
       // p -> exact hi + lo f16 parts, transposed once into the B layout: each f16 pair holds one
       // query row g and two consecutive tokens (2c, 2c+1) or (2c+8, 2c+9)
@@ -590,17 +685,31 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         const uint32_t hi0 = hmul2(bh0, sp0[b]), hi1 = hmul2(bh1, sp1[b]);
         const uint32_t r0 = hfma2(bh0, sp0[b], hi0 ^ 0x80008000u), r1 = hfma2(bh1, sp1[b], hi1 ^ 0x80008000u);
         const uint32_t lo0 = hfma2(bl0, sp0[b], r0), lo1 = hfma2(bl1, sp1[b], r1);
-        // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
-        uint32_t ua[4], ub[4];
-        if (ASYM) {
-          unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 0], ua);
-          unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+        uint32_t A0[4], A1[4];
+        if constexpr (V8) {
+          // block b = 16-byte columns 2b, 2b+1, transposed: vb[0] / vb[1] = tokens (2c, 2c+1) /
+          // (2c+8, 2c+9) at dims 32b + 2g, 2g+1; vb[2] / vb[3] the same at dims 32b + 16 + 2g, 2g+1.
+          // A0: dims 32b + 2g (row g), 2g+1 (row g+8); A1: dims 32b + 16 + 2g, 2g+1
+          uint32_t vb[4];
+          const int mi = lane >> 3;
+          ldsm_x4_t(sV + swz<VRB>(tile * 16 + (mi & 1) * 8 + (lane & 7), 2 * b + (mi >> 1)), vb);
+          unpack4_s8_t(vb[0], A0[0], A0[1]);
+          unpack4_s8_t(vb[1], A0[2], A0[3]);
+          unpack4_s8_t(vb[2], A1[0], A1[1]);
+          unpack4_s8_t(vb[3], A1[2], A1[3]);
         } else {
-          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
-          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
+          // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
+          uint32_t ua[4], ub[4];
+          if (ASYM) {
+            unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 0], ua);
+            unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+          } else {
+            unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
+            unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
+          }
+          A0[0] = ua[0]; A0[1] = ua[1]; A0[2] = ub[0]; A0[3] = ub[1];   // dims 4g+0 (row g), 4g+1 (row g+8)
+          A1[0] = ua[2]; A1[1] = ua[3]; A1[2] = ub[2]; A1[3] = ub[3];   // dims 4g+2, 4g+3
         }
-        const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};   // dims 4g+0 (row g), 4g+1 (row g+8)
-        const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};   // dims 4g+2, 4g+3
         mma16816(O[b][0], A0, hi0, hi1);
         mma16816(O[b][0], A0, lo0, lo1);
         mma16816(O[b][1], A1, hi0, hi1);
@@ -645,7 +754,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      const int d = 32 * b + 4 * g + 2 * h;
+      const int d = V8 ? 32 * b + 16 * h + 2 * g : 32 * b + 4 * g + 2 * h;
       *reinterpret_cast<float2 *>(co + (warp * 8 + r0) * kD + d) =
           make_float2(fmaf(O[b][h][0], se, w0), fmaf(O[b][h][2], so, w0));
       *reinterpret_cast<float2 *>(co + (warp * 8 + r1) * kD + d) =
@@ -676,7 +785,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   }
 }
 
-template <int LAYOUT, bool QSPLIT, bool PAGED>
+template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   static bool configured[kMaxDevices] = {};
   int dev = 0;
@@ -684,49 +793,54 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma_kernel<LAYOUT, QSPLIT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<LAYOUT>());
+    e = cudaFuncSetAttribute(attend_mma_kernel<LAYOUT, VLAYOUT, QSPLIT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_bytes<LAYOUT, VLAYOUT>());
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = smem_bytes<LAYOUT>();
+  cfg.dynamicSmemBytes = smem_bytes<LAYOUT, VLAYOUT>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, QSPLIT, PAGED>, a);
+  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, VLAYOUT, QSPLIT, PAGED>, a);
+}
+
+template <int LAYOUT, int VLAYOUT>
+cudaError_t launch_pair_t(const AttendArgs &a, cudaStream_t st) {
+  const bool paged = a.cache.page_shift >= 0;
+  if (a.q_dtype == KVQ_F32)
+    return paged ? launch_t<LAYOUT, VLAYOUT, true, true>(a, st) : launch_t<LAYOUT, VLAYOUT, true, false>(a, st);
+  return paged ? launch_t<LAYOUT, VLAYOUT, false, true>(a, st) : launch_t<LAYOUT, VLAYOUT, false, false>(a, st);
 }
 
 }  // namespace
 
 bool mma_supported(const AttendArgs &a) {
-  const int L = a.cache.layout;
+  const int L = a.cache.layout, VL = a.cache.v_layout;
   if (prefill_supported(a)) return true;                 // includes the mixed K/V pairs it is built for
-  if (a.cache.v_layout != L) return false;               // the decode kernels: one layout in both planes
-  if (L == KVQ_Q6_0) return mma_q6_supported(a);
-  return (L == KVQ_Q4_0 || L == KVQ_ASYM4_G32 || L == KVQ_HAD_INT4) && a.cache.D == kD && a.gqa * a.n_q <= 8 &&
-         a.n_body > 0 && a.chunk % kStage == 0;
+  if (L == KVQ_Q6_0 && VL == L) return mma_q6_supported(a);
+  return decode_kernel(L, VL) && a.cache.D == kD && a.gqa * a.n_q <= 8 && a.n_body > 0 && a.chunk % kStage == 0;
 }
 
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
-  const bool split = a.q_dtype == KVQ_F32;
   if (prefill_supported(a)) return launch_attend_prefill(a, st);
   if (uses_mma4(a.cache.layout)) return launch_attend_mma4(a, st);
   const bool paged = a.cache.page_shift >= 0;
-  switch (a.cache.layout) {
-    case KVQ_Q6_0: return launch_attend_mma_q6(a, st);
-    case KVQ_HAD_INT4:                                   // int8 query codes are exact
-      return paged ? launch_t<KVQ_HAD_INT4, false, true>(a, st) : launch_t<KVQ_HAD_INT4, false, false>(a, st);
-    case KVQ_Q4_0:
-      if (split) return paged ? launch_t<KVQ_Q4_0, true, true>(a, st) : launch_t<KVQ_Q4_0, true, false>(a, st);
-      return paged ? launch_t<KVQ_Q4_0, false, true>(a, st) : launch_t<KVQ_Q4_0, false, false>(a, st);
-    default: return cudaErrorNotSupported;               // the asymmetric layout runs attend_mma4.cu
-  }
+  const int L = a.cache.layout, VL = a.cache.v_layout;
+  if (L == KVQ_Q6_0) return launch_attend_mma_q6(a, st);
+  if (L == KVQ_HAD_INT4)                                 // int8 query codes are exact
+    return paged ? launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, true>(a, st)
+                 : launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, false>(a, st);
+  if (L == KVQ_Q4_0 && VL == KVQ_Q4_0) return launch_pair_t<KVQ_Q4_0, KVQ_Q4_0>(a, st);
+  if (L == KVQ_Q8_0 && VL == KVQ_Q8_0) return launch_pair_t<KVQ_Q8_0, KVQ_Q8_0>(a, st);
+  if (L == KVQ_Q4_0 && VL == KVQ_Q8_0) return launch_pair_t<KVQ_Q4_0, KVQ_Q8_0>(a, st);
+  return cudaErrorNotSupported;                          // the asymmetric layout runs attend_mma4.cu
 }
 
 }  // namespace kvq

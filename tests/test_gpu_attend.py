@@ -298,6 +298,20 @@ def test_q8_0_and_int2(layout, D, gqa, n_q, causal, n_recent, chunk):
     run_case(w, kv_len=1100, n_q=n_q, chunk=chunk, fill=1100 - max(n_q, 1))
 
 
+@pytest.mark.parametrize("layout", ["q8_0", "q4_0+q8_0"])
+@pytest.mark.parametrize("gqa,n_q,causal,q_dtype,chunk", [
+    (8, 1, False, None, 0), (4, 2, True, "f32", 0), (2, 3, True, "f16", 192), (1, 1, False, None, 64),
+    (8, 1, False, "f32", 128),
+])
+def test_8bit_decode_kernel(layout, gqa, n_q, causal, q_dtype, chunk):
+    """Decode shapes (at most eight query rows per kv head) of the 8-bit value (and key) planes on
+    the per-warp tensor-core kernel: every query dtype, causal rows, several chunks and a ragged
+    32-token stage at the end."""
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=2, n_kv_heads=2, n_q_heads=2 * gqa,
+                                              causal=causal)
+    run_case(w, kv_len=1000, n_q=n_q, chunk=chunk, fill=1000 - n_q, q_dtype=q_dtype)
+
+
 @pytest.mark.parametrize("layout,n_recent", [
     ("q4_0+q8_0", 0), ("q4_0+q6_0", 0), ("asym4_g32+q8_0", 0), ("q8_0+q4_0", 0), ("q6_0+asym4_g32", 0),
     ("had_int4+had_int2", 32), ("had_int2+had_int4", 64),
