@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       if (HAD) {
         // one per-token scale: all 8 k-steps accumulate the exact integer dot (x 2^-24) in two
         // chains; score = alpha * s_q * s_k * dot
-        float dA[4] = {zq0[0], zq1[0], zq0[0], zq1[0]}, dB[4] = {0.f, 0.f, 0.f, 0.f};
+        float dA[4], dB[4];                              // the first mma of each chain takes its C operand
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           uint32_t ug[4], u8[4];
@@ -461,7 +461,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
           const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
           float(&d)[4] = (b & 1) ? dB : dA;
-          mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
+          if (b == 0)
+            mma16816_c(d, A0, bq_hi[0][0], bq_hi[0][1], zq0[0], zq1[0], zq0[0], zq1[0]);
+          else if (b == 1)
+            mma16816_c(d, A0, bq_hi[2][0], bq_hi[2][1], 0.0f, 0.0f, 0.0f, 0.0f);
+          else
+            mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
           mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
         }
         const float skg = *reinterpret_cast<const float *>(sb + OFF_SK + (tile * 16 + g) * 4);
@@ -509,16 +514,10 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           A0[0] = ug[0]; A0[1] = u8[0]; A0[2] = ug[1]; A0[3] = u8[1];
           A1[0] = ug[2]; A1[1] = u8[2]; A1[2] = ug[3]; A1[3] = u8[3];
         }
+        // the first mma takes the offset (ASYM: zero) as its separate C operand: no register copies
         float d[4];
-        if (ASYM) {
-          d[0] = d[1] = d[2] = d[3] = 0.0f;
-        } else {
-          d[0] = zq0[b];
-          d[1] = zq1[b];
-          d[2] = zq0[b];
-          d[3] = zq1[b];
-        }
-        mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
+        const float c0 = ASYM ? 0.0f : zq0[b], c1 = ASYM ? 0.0f : zq1[b];
+        mma16816_c(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1], c0, c1, c0, c1);
         mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
         if (QSPLIT) {
           mma16816(d, A0, bq_lo[2 * b][0], bq_lo[2 * b][1]);
@@ -683,7 +682,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         // P' = (p_hi + p_lo) * s_v split into hi + lo f16 exactly enough (TwoProduct with f16 fma):
         //   hi = rn(p_hi * s),  r = p_hi * s - hi (exact),  lo = rn(p_lo * s + r)
         const uint32_t hi0 = hmul2(bh0, sp0[b]), hi1 = hmul2(bh1, sp1[b]);
-        const uint32_t r0 = hfma2(bh0, sp0[b], hi0 ^ 0x80008000u), r1 = hfma2(bh1, sp1[b], hi1 ^ 0x80008000u);
+        const uint32_t r0 = hfma2_negc(bh0, sp0[b], hi0), r1 = hfma2_negc(bh1, sp1[b], hi1);
         const uint32_t lo0 = hfma2(bl0, sp0[b], r0), lo1 = hfma2(bl1, sp1[b], r1);
         uint32_t A0[4], A1[4];
         if constexpr (V8) {

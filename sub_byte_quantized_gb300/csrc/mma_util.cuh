@@ -93,6 +93,13 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
+// a * b - c in one rounding (the negation is an operand modifier of the f16x2 fma)
+__device__ __forceinline__ uint32_t hfma2_negc(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("{\n.reg .b32 t;\nneg.f16x2 t, %3;\nfma.rn.f16x2 %0, %1, %2, t;\n}\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
