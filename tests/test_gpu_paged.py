@@ -149,7 +149,7 @@ def test_paged_many_rows_reduce():
     check_close(out.cpu().numpy(), ref, "paged many rows")
 
 
-@pytest.mark.parametrize("layout", ["q4_0", "had_int4", "asym4_g32", "q6_0"])
+@pytest.mark.parametrize("layout", ["q4_0", "had_int4", "asym4_g32", "q6_0", "q8_0", "q4_0+q8_0"])
 def test_paged_append_attend_matches_two_calls(layout):
     """paged_append_decode_attend == paged_store + paged_decode_attend, bit for bit."""
     D = 256 if layout == "q6_0" else 128
@@ -161,7 +161,7 @@ def test_paged_append_attend_matches_two_calls(layout):
     check_close(b[2].cpu().numpy(), b[3], f"paged fused {layout}")
 
 
-@pytest.mark.parametrize("layout", ["q4_0", "had_int4", "asym4_g32", "q6_0"])
+@pytest.mark.parametrize("layout", ["q4_0", "had_int4", "asym4_g32", "q6_0", "q8_0", "q4_0+q8_0"])
 def test_paged_equals_contiguous_bitwise(layout):
     """With equal lengths, a permuted paged pool gives the contiguous cache's output bit for bit
     (same kernels, same chunking: only the row addresses differ)."""
