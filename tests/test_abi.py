@@ -268,3 +268,27 @@ def test_host_call_workspace_and_validation(L):
                                                  None) == 7
     assert L.kvq_paged_append_decode_attend_host(p(pc), 16, 16, 1, 1, 16, 1, 8, 1, 16, 300, 0, 1.0, 0, 16, 256, ws,
                                                  None) == 3
+
+
+def test_decode_chunk_follows_the_kernel(L):
+    """The automatic chunk of a decode shape follows the phase-1 kernel that will run: the
+    per-warp tensor-core kernel (Q4_0, Q8_0, Q4_0 keys + Q8_0 values, Hadamard int4) shares one
+    rule; the asymmetric layout's CTA kernel and the row-side kernel (Hadamard int2) have others.
+    Host-only: with no device the SM count defaults, the rules are the same."""
+    from sub_byte_quantized_gb300._lib import KvqCache, mixed
+    p = C.byref
+
+    def chunk(layout, n_recent=0, rows=8):
+        zero = 4096 if layout == 3 else None
+        ring = 4096 if n_recent else None
+        c = KvqCache(layout, 1, 8, 128, 131072, n_recent, 4096, 4096, 4096, 4096, zero, zero, ring, ring)
+        return L.kvq_attend_chunk(p(c), 8 * rows, 1, 131072, 0)
+
+    per_warp = chunk(0)
+    assert per_warp % 64 == 0 and per_warp > 0
+    assert chunk(4) == per_warp                      # Q8_0 on the per-warp kernel
+    assert chunk(mixed(0, 4)) == per_warp            # Q4_0 keys + Q8_0 values
+    assert chunk(3) != per_warp                      # asymmetric: one chunk per resident CTA
+    assert chunk(5, n_recent=256) != per_warp        # Hadamard int2: row-side kernel, decode form
+    # more than eight rows per kv head leave the per-warp kernel
+    assert chunk(4, rows=16) != chunk(4, rows=8)
