@@ -348,16 +348,10 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
           unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
           const uint32_t A0[4] = {ug[0], u8[0], ug[1], u8[1]};
           const uint32_t A1[4] = {ug[2], u8[2], ug[3], u8[3]};
+          // the first mma takes the offset (ASYM: zero) as its separate C operand: no register copies
           float d[4];
-          if (ASYM) {
-            d[0] = d[1] = d[2] = d[3] = 0.0f;
-          } else {
-            d[0] = zq0[b];
-            d[1] = zq1[b];
-            d[2] = zq0[b];
-            d[3] = zq1[b];
-          }
-          mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
+          const float c0 = ASYM ? 0.0f : zq0[b], c1 = ASYM ? 0.0f : zq1[b];
+          mma16816_c(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1], c0, c1, c0, c1);
           mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
           if (QSPLIT) {
             mma16816(d, A0, bq_lo[2 * b][0], bq_lo[2 * b][1]);
@@ -533,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
         // P' = (p_hi + p_lo) * s_v as hi + lo f16 (TwoProduct with the f16 fma):
         //   hi = rn(p_hi * s),  r = p_hi * s - hi (exact),  lo = rn(p_lo * s + r)
         const uint32_t hi0 = hmul2(pb.x, sp0[b]), hi1 = hmul2(pb.y, sp1[b]);
-        const uint32_t e0 = hfma2(pb.x, sp0[b], hi0 ^ 0x80008000u), e1 = hfma2(pb.y, sp1[b], hi1 ^ 0x80008000u);
+        const uint32_t e0 = hfma2_negc(pb.x, sp0[b], hi0), e1 = hfma2_negc(pb.y, sp1[b], hi1);
         const uint32_t lo0 = hfma2(pb.z, sp0[b], e0), lo1 = hfma2(pb.w, sp1[b], e1);
         uint32_t ua[4], ub[4];
         if (ASYM) {
