@@ -258,10 +258,12 @@ def _oracle_rows_for_kv_head(w, inp, kvh, kv_len, q_pos0=0):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["c1_q4_0_tiny", "c2_q4_0_llama3_8b", "c3_had_int4_decode", "c3_had_int4_prefill",
-                                  "c4_q6_0_gemma", "c5_q4_0_llama70b_128k", "c5_asym4_g32_llama70b_128k"])
+                                  "c4_q6_0_gemma", "c5_q4_0_llama70b_128k", "c5_asym4_g32_llama70b_128k",
+                                  "c5_q8_0_llama70b_128k", "c5_q4_0_k_q8_0_v_llama70b_128k",
+                                  "c3_had_int2_decode_w256"])
 def test_workloads_full_size_sampled(name):
-    """Full-size workloads in the benchmark's launch configuration (bulk fill, append, chunk
-    512); the oracle recomputes every query head of two kv heads (first and last)."""
+    """Full-size workloads in the benchmark's launch configuration (bulk fill, append, automatic
+    chunk); the oracle recomputes every query head of two kv heads (first and last)."""
     w = WORKLOADS[name]
     inp = make_inputs(w)
     B, H, S, D = inp["k"].shape
