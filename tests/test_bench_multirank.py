@@ -49,3 +49,30 @@ def test_max_over_ranks_and_weak_scaling_value():
 def test_single_rank_identity():
     assert bench.max_over_ranks(4.0, None, None) == 4.0
     assert bench.aggregate(1, 150994944, 100, 4.0) == pytest.approx(150994944 * 100 / 4.0e-3)
+
+
+def _reference_line(env_extra):
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    return [json.loads(l) for l in lines]
+
+
+def test_reference_arm_line():
+    """The reference arm times the oracle on the host cores and prints the contract's line."""
+    (d,) = _reference_line({})
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["steps"] == 1 and d["warmup"] == 3 and d["n_gpus"] == 1
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    """Under a multi-rank launch only rank 0 runs the reference arm."""
+    assert _reference_line({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
