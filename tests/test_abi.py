@@ -292,3 +292,24 @@ def test_decode_chunk_follows_the_kernel(L):
     assert chunk(5, n_recent=256) != per_warp        # Hadamard int2: row-side kernel, decode form
     # more than eight rows per kv head leave the per-warp kernel
     assert chunk(4, rows=16) != chunk(4, rows=8)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libkvq.so the package raises on the first call: there is no CPU path to fall back to."""
+    import subprocess
+    import sys
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from sub_byte_quantized_gb300 import _lib\n"
+        "_lib.LIB_PATH = %r\n"
+        "import sub_byte_quantized_gb300 as kvq, torch\n"
+        "try:\n"
+        "    kvq.row_bytes('q4_0', 128)\n"
+        "except RuntimeError as e:\n"
+        "    print('raised:', 'missing' in str(e))\n"
+        "else:\n"
+        "    print('no error')\n"
+    ) % (ROOT, str(tmp_path / "libkvq.so"))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert "raised: True" in r.stdout
