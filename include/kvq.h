@@ -3,8 +3,13 @@
  *
  * A stateless C library. The caller owns every buffer (device memory for the cache, inputs,
  * outputs and workspace); the library validates arguments on the host, then enqueues CUDA
- * kernels on the caller's stream and returns. It allocates nothing and never synchronises.
- * Every entry point is re-entrant.
+ * kernels on the caller's stream and returns. It allocates nothing. Two kinds of entry point
+ * depart from the rest:
+ *   - the host-buffer calls (kvq_append_decode_attend_host, kvq_paged_append_decode_attend_host)
+ *     wait for their stream before returning, since they return with the host output filled;
+ *   - kvq_decode_attend_static keeps its partials in one device array built into the library,
+ *     so two of its calls that overlap on the GPU race (see there).
+ * Every other entry point is re-entrant and never synchronises.
  *
  * Pages this follows (cited by title and section):
  *   [FT]  FreeToken PR #268 "feat(kvcache): sub-byte Q4_0 and Q6_0 KV cache quantization",
@@ -131,7 +136,7 @@ kvq_status kvq_cache_bytes(int32_t layout, int32_t batch, int32_t n_kv_heads, in
  * Store (append) n_new tokens per (batch, kv head) at positions [pos0, pos0 + n_new).
  *   k_new, v_new: device [batch][n_kv_heads][n_new][head_dim] in `dtype` (f32, bf16 or f16).
  * Quantisation is exact and deterministic: re-storing a token writes identical bytes.
- * HAD_INT4 with n_recent > 0 also writes the rotated f32 rows of the last
+ * HAD_INT4 / HAD_INT2 with n_recent > 0 also write the rotated f32 rows of the last
  * min(n_new, n_recent) tokens to ring slot (position mod n_recent); attention with the window
  * therefore expects kv_len equal to the end of the latest store.
  * One kernel launch covers K and V. n_new == 0 is a no-op.
@@ -180,7 +185,7 @@ int32_t kvq_attend_chunk(const kvq_cache *cache, int32_t n_q_heads, int32_t n_q,
  * decode shapes, about four waves of 64-row CTAs for many query rows; kvq_attend_chunk returns
  * it) and writes per (row, chunk) the
  * running max, the sum of exponentials and the unnormalised output to the workspace; phase 2
- * combines them with the online-softmax correction ([OTQ] Section 3.2). HAD_INT4: the query
+ * combines them with the online-softmax correction ([OTQ] Section 3.2). HAD_INT4 / HAD_INT2: the query
  * is rotated and quantised to int8 (one f32 scale per row, amax / 127), body tokens are
  * scored by the exact integer dot, the newest min(n_recent, kv_len) tokens by exact f32
  * from the ring, and phase 2 un-rotates the output ([TR] data flow).
@@ -215,10 +220,11 @@ kvq_status kvq_append_decode_attend(const kvq_cache *cache, const void *k_new, c
  * page of each logical page of each sequence, and every sequence has its own length.
  *   payload  u8  [n_pages][n_kv_heads][page_size][kvq_row_bytes(layout, head_dim)]
  *   scale    f16 [n_pages][n_kv_heads][page_size][head_dim/32]   (Q4_0, Q6_0, ASYM4_G32)
- *            f32 [n_pages][n_kv_heads][page_size]                (HAD_INT4)
+ *            f32 [n_pages][n_kv_heads][page_size]                (HAD_INT4, HAD_INT2)
  *   zero     f16 [n_pages][n_kv_heads][page_size][head_dim/32]   (ASYM4_G32 only, else NULL)
- *   recent   f32 [batch][n_kv_heads][n_recent][head_dim]         (HAD_INT4 with n_recent > 0:
- *                                                                 one ring per sequence)
+ *   recent   f32 [batch][n_kv_heads][n_recent][head_dim]         (HAD_INT4 / HAD_INT2 with
+ *                                                                 n_recent > 0: one ring per
+ *                                                                 sequence)
  *   block_table  device i32 [batch][max_pages_per_seq]
  * Token t of sequence b is row t % page_size of pool page block_table[b][t / page_size]. Byte
  * layouts and quantisation are those of the contiguous cache (one token row is bit-identical).
@@ -236,7 +242,7 @@ typedef struct kvq_paged_cache {
   int32_t page_size;          /* tokens per page: a power of two in [64, 2^20] */
   int32_t n_pages;            /* pages in the pool */
   int32_t max_pages_per_seq;  /* row length of the block table */
-  int32_t n_recent;           /* HAD_INT4: exact-f32 ring per sequence (0 = pure int4); others: 0 */
+  int32_t n_recent;           /* HAD_INT4 / HAD_INT2: exact-f32 ring per sequence (0 = none); others: 0 */
   void *k_payload, *v_payload;
   void *k_scale, *v_scale;
   void *k_zero, *v_zero;
@@ -255,7 +261,7 @@ kvq_status kvq_paged_cache_bytes(int32_t layout, int32_t n_pages, int32_t n_kv_h
  *   positions:    device i32 [batch].
  * Quantisation as kvq_store_* for the cache's layout (any layout; bit-identical rows). The
  * positions are read on the device: a row whose position falls outside [0, max_pages_per_seq *
- * page_size) is not written. HAD_INT4 with n_recent > 0 also writes the rotated f32 rows of the
+ * page_size) is not written. HAD_INT4 / HAD_INT2 with n_recent > 0 also write the rotated f32 rows of the
  * last min(n_new, n_recent) tokens to the sequence's ring slot (position mod n_recent).
  * One kernel launch covers K and V. n_new == 0 is a no-op.
  */
@@ -294,7 +300,7 @@ int32_t kvq_paged_attend_plan_chunk(const kvq_paged_cache *cache, int32_t n_q_he
  * Row i of each query head of sequence b attends t < seq_lens[b] and, when causal != 0,
  * t <= seq_lens[b] - n_q + i (the n_q query rows are the sequence's newest tokens). A row that
  * sees no token (an empty sequence, or a causal row before the sequence's start) gets zeros.
- * HAD_INT4: the newest min(n_recent, seq_lens[b]) tokens of each sequence are read from its
+ * HAD_INT4 / HAD_INT2: the newest min(n_recent, seq_lens[b]) tokens of each sequence are read from its
  * ring. Everything else (GQA mapping, chunking, the two phases, the workspace rule) is as
  * kvq_decode_attend.
  */
@@ -359,13 +365,35 @@ kvq_status kvq_paged_append_decode_attend_host(const kvq_paged_cache *cache, con
                                                kvq_stream_t stream);
 
 /*
- * HAD_INT4 / HAD_INT2 test hook: the exact integer-domain body scores int8(q_rot) . code(k_rot).
+ * HAD_INT4 / HAD_INT2 test hook: the exact integer-domain body scores int8(q_rot) . code(k_rot)
+ * ([TR] "What's done": the int8 x int4 -> i32 score dot), from a plain scalar kernel of its own
+ * (a cross-check: the attention calls score the body on the tensor cores, see
+ * kvq_debug_attend_scores_i32).
  *   scores_out device i32 [batch][n_q_heads][n_q][kv_len - min(n_recent, kv_len)]
  *   s_q_out    device f32 [batch][n_q_heads][n_q]   (the per-row int8 scale of q_rot)
  */
 kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q_dtype,
                                 int32_t n_q_heads, int32_t n_q, int32_t kv_len,
                                 int32_t *scores_out, float *s_q_out, kvq_stream_t stream);
+
+/*
+ * HAD_INT4 / HAD_INT2 test hook on the production path: kvq_decode_attend (same arguments, same
+ * kernels, chunking and output `out`), with the phase-1 tensor-core kernel that scores the body
+ * also writing every exact integer score int8(q_rot) . code(k_rot) it computes ([TR] "What's
+ * done": the i32 score dot; exact integers, so any summation order agrees) and each row's int8
+ * query scale, read from the values that kernel uses for the softmax.
+ *   scores_out device i32 [batch][n_q_heads][n_q][kv_len - min(n_recent, kv_len)]; the entry of
+ *              (row, body token t) is written when some row of that row's tile sees t (every
+ *              t <= the row's causal limit at least); the caller pre-fills it to tell the rest
+ *   s_q_out    device f32 [batch][n_q_heads][n_q]
+ * Returns KVQ_EUNSUPPORTED unless the cache is contiguous, one Hadamard layout in both planes,
+ * and the call's body runs on a tensor-core kernel (head_dim 128).
+ */
+kvq_status kvq_debug_attend_scores_i32(const kvq_cache *cache, const void *q, int32_t q_dtype,
+                                       int32_t n_q_heads, int32_t n_q, int32_t kv_len, int32_t causal,
+                                       int32_t q_pos0, float attn_scale, int32_t chunk, float *out,
+                                       void *workspace, size_t workspace_bytes, int32_t *scores_out,
+                                       float *s_q_out, kvq_stream_t stream);
 
 /*
  * Measurement hook (no counterpart on the pages): while both events are non-NULL, every
@@ -393,7 +421,9 @@ kvq_status kvq_profile_phase1_events(void *phase1_begin, void *phase1_end);
  *   (see kvq_attend_workspace_bytes) returns KVQ_EWORKSPACE and enqueues nothing.
  *   Nothing is allocated or freed: no cudaMalloc/cudaFree or allocating library routine runs.
  *   The first call made with a given device current looks up the array's device address on that
- *   device (cudaGetSymbolAddress) and keeps it; make that first call before any stream capture.
+ *   device (cudaGetSymbolAddress) and keeps it for the life of the process; make that first call
+ *   before any stream capture. The kept address belongs to the device's primary context: calls
+ *   made after cudaDeviceReset on that device, or from another context, are not supported.
  *   Every call, on every stream, shares the one array, and it keeps the last call's contents
  *   (the kernels write every partial before reading it, so nothing needs clearing). Calls whose
  *   work overlaps on the GPU (other streams, or concurrent host threads) race on the array and

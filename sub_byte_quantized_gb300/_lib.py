@@ -39,7 +39,7 @@ EXPORTS = ("kvq_row_bytes", "kvq_cache_bytes", "kvq_store_q4_0", "kvq_store_q6_0
            "kvq_paged_decode_attend", "kvq_paged_append_decode_attend", "kvq_store_q8_0", "kvq_store_hadamard_int2",
            "kvq_store", "kvq_paged_attend_plan_chunk", "kvq_append_decode_attend_host_workspace_bytes",
            "kvq_append_decode_attend_host", "kvq_paged_append_decode_attend_host_workspace_bytes",
-           "kvq_paged_append_decode_attend_host")
+           "kvq_paged_append_decode_attend_host", "kvq_debug_attend_scores_i32")
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024   # KVQ_STATIC_SCRATCH_BYTES in include/kvq.h
 
 
@@ -100,6 +100,9 @@ def lib() -> C.CDLL:
     L.kvq_decode_attend_static.restype = I32
     L.kvq_debug_scores_i32.argtypes = [cache_p, P, I32, I32, I32, I32, P, P, P]
     L.kvq_debug_scores_i32.restype = I32
+    L.kvq_debug_attend_scores_i32.argtypes = [cache_p, P, I32, I32, I32, I32, I32, I32, C.c_float, I32, P, P, SZ, P, P,
+                                              P]
+    L.kvq_debug_attend_scores_i32.restype = I32
     paged_p = C.POINTER(KvqPagedCache)
     L.kvq_paged_cache_bytes.argtypes = [I32, I32, I32, I32, I32, I32, I32, C.POINTER(SZ)]
     L.kvq_paged_cache_bytes.restype = I32

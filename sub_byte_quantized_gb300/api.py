@@ -234,6 +234,30 @@ def debug_scores_i32(cache: KVCache, q: torch.Tensor, kv_len: int, stream=None):
     return buf[:B * Hq * n_q * n_body].view(B, Hq, n_q, n_body), s_q
 
 
+def debug_attend_scores_i32(cache: KVCache, q: torch.Tensor, kv_len: int, causal: bool = False, q_pos0: int = 0,
+                            attn_scale: float | None = None, chunk: int = 0, fill: int = -(2 ** 31), stream=None):
+    """decode_attend on the production kernels, with the tensor-core kernel that scores the body also
+    writing its exact integer scores: returns (out, scores [B][H_q][n_q][n_body] int32, s_q [B][H_q][n_q]).
+    Score entries the kernels did not compute keep `fill`."""
+    _need_cuda("q", q)
+    B, Hq, n_q, D = q.shape
+    if B != cache.batch or D != cache.head_dim:
+        raise ValueError("q shape does not match the cache")
+    if attn_scale is None:
+        attn_scale = 1.0 / math.sqrt(D)
+    n_body = kv_len - min(cache.n_recent, kv_len)
+    out = torch.empty((B, Hq, n_q, D), dtype=torch.float32, device=q.device)
+    scores = torch.full((B * Hq * n_q * max(n_body, 1),), fill, dtype=torch.int32, device=q.device)
+    s_q = torch.zeros((B, Hq, n_q), dtype=torch.float32, device=q.device)
+    need = attend_workspace_bytes(cache, Hq, n_q, kv_len, chunk)
+    workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    L.check(L.lib().kvq_debug_attend_scores_i32(
+        C.byref(cache.struct), q.data_ptr(), _DTYPES[q.dtype], Hq, n_q, kv_len, int(bool(causal)), q_pos0,
+        float(attn_scale), chunk, out.data_ptr(), workspace.data_ptr(), workspace.numel(), scores.data_ptr(),
+        s_q.data_ptr(), _stream(stream)), "kvq_debug_attend_scores_i32")
+    return out, scores[:B * Hq * n_q * n_body].view(B, Hq, n_q, n_body), s_q
+
+
 # ------------------------------------------------------------------ paged pool
 class PagedKVCache:
     """Device planes of one layer's paged pool, its block table and the C struct describing them.

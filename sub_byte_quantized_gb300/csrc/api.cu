@@ -241,6 +241,8 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
   a.fresh_hi = INT_MAX;
   a.seq_lens = nullptr;
   a.fresh_tail = 0;
+  a.cap_scores = nullptr;
+  a.cap_sq = nullptr;
   const size_t rows = (size_t)c.B * n_q_heads * n_q;
   size_t off = 0;
   const size_t o_m = off; off = round_up(off + rows * a.C * sizeof(float), 256);
@@ -823,6 +825,27 @@ kvq_status kvq_debug_scores_i32(const kvq_cache *cache, const void *q, int32_t q
   cudaError_t e = kvq::launch_debug_scores(a.cache, q, q_dtype, n_q_heads, n_q, kv_len, a.n_body, scores_out, s_q_out,
                                            reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "debug scores launch: %s", cudaGetErrorString(e));
+  return KVQ_OK;
+}
+
+kvq_status kvq_debug_attend_scores_i32(const kvq_cache *cache, const void *q, int32_t q_dtype, int32_t n_q_heads,
+                                       int32_t n_q, int32_t kv_len, int32_t causal, int32_t q_pos0, float attn_scale,
+                                       int32_t chunk, float *out, void *workspace, size_t workspace_bytes,
+                                       int32_t *scores_out, float *s_q_out, kvq_stream_t stream) {
+  g_last_error[0] = 0;
+  kvq::AttendArgs a;
+  kvq_status st = prepare_attend(cache, q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk, out,
+                                 workspace, workspace_bytes, a);
+  if (st != KVQ_OK) return st;
+  if (!scores_out || !s_q_out) return fail(KVQ_EINVAL, "scores_out/s_q_out is NULL");
+  if (!aligned(scores_out, 16) || !aligned(s_q_out, 16)) return fail(KVQ_EALIGN, "scores_out/s_q_out not 16-byte aligned");
+  if (!kvq::capture_supported(a))
+    return fail(KVQ_EUNSUPPORTED, "score capture needs a contiguous Hadamard cache (one layout in both planes) "
+                                  "whose body is scored by a tensor-core kernel");
+  a.cap_scores = scores_out;
+  a.cap_sq = s_q_out;
+  cudaError_t e = launch_attend_sequence(a, reinterpret_cast<cudaStream_t>(stream), false);
+  if (e != cudaSuccess) return fail(KVQ_ECUDA, "attend launch: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
 

@@ -319,17 +319,9 @@ __global__ void __launch_bounds__(128) debug_scores_kernel(CacheView c, const vo
 template <int D, int T>
 cudaError_t launch_generic_dt(const AttendArgs &a, cudaStream_t st) {
   const size_t smem = sizeof(float) * ((size_t)T * (D + 1) + (size_t)T * D + kRowsPerCta * D + 2 * T);
-  // The opt-in shared-memory size is a per-device function attribute: set it once per device.
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = set_smem_once(configured, attend_generic_kernel<D, T>, (int)smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_generic_kernel<D, T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   const int R = a.gqa * a.n_q;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.C, a.cache.B * a.cache.H, (R + kRowsPerCta - 1) / kRowsPerCta);

@@ -119,7 +119,9 @@ __device__ __forceinline__ void unpack4_s8_t(uint32_t w, uint32_t &d0, uint32_t 
   d1 = hadd2(__byte_perm(x, 0x64646464u, 0x4341), 0xE480E480u);
 }
 
-template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED>
+// CAP: score capture (Hadamard layout, contiguous cache): the exact integer score of every
+// (row, body token) this CTA computes and each row's int8 query scale go to a.cap_scores / a.cap_sq.
+template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED, bool CAP = false>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
   constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = LAYOUT == KVQ_HAD_INT4;
   constexpr bool K8 = LAYOUT == KVQ_Q8_0, V8 = VLAYOUT == KVQ_Q8_0;   // 8-bit code planes
@@ -128,6 +130,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   constexpr int OFF_SV = off_sv<LAYOUT, VLAYOUT>(), OFF_ZK = off_zk<LAYOUT, VLAYOUT>();
   constexpr int OFF_ZV = off_zv<LAYOUT, VLAYOUT>(), STAGE_BYTES = stage_bytes<LAYOUT, VLAYOUT>();
   static_assert(VLAYOUT == LAYOUT || (LAYOUT == KVQ_Q4_0 && VLAYOUT == KVQ_Q8_0), "supported plane pairs");
+  static_assert(!CAP || (HAD && !PAGED), "score capture: Hadamard layout, contiguous cache");
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
@@ -294,6 +297,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           (uint32_t)(q8v[0] & 0xFF) | ((uint32_t)(q8v[1] & 0xFF) << 8) | ((uint32_t)(q8v[2] & 0xFF) << 16) |
           ((uint32_t)(q8v[3] & 0xFF) << 24);
       if (lane == 0) qsq[r] = sq;
+      if (CAP && lane == 0 && warp == 0 && chunk_id == 0) a.cap_sq[grow] = sq;
     }
     __syncwarp();
     const bool live = g < R;
@@ -468,6 +472,15 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           else
             mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
           mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
+        }
+        if constexpr (CAP) {
+          // the two chains hold the exact dot x 2^-24 (|dot| < 2^18): (dA + dB) x 2^24 is the integer
+          const int ta = ts + tile * 16 + g, tb = ta + 8;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = (k & 1) ? r1 : r0, t = (k & 2) ? tb : ta;
+            if (r < R && t < t_end) capture_score(a, bb, kvh, r, t, __float2int_rn((dA[k] + dB[k]) * 16777216.0f));
+          }
         }
         const float skg = *reinterpret_cast<const float *>(sb + OFF_SK + (tile * 16 + g) * 4);
         const float skg8 = *reinterpret_cast<const float *>(sb + OFF_SK + (tile * 16 + g + 8) * 4);
@@ -784,19 +797,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   }
 }
 
-template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED>
+template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED, bool CAP = false>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = set_smem_once(configured, attend_mma_kernel<LAYOUT, VLAYOUT, QSPLIT, PAGED, CAP>, smem_bytes<LAYOUT, VLAYOUT>());
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma_kernel<LAYOUT, VLAYOUT, QSPLIT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_bytes<LAYOUT, VLAYOUT>());
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
@@ -807,7 +812,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, VLAYOUT, QSPLIT, PAGED>, a);
+  return cudaLaunchKernelEx(&cfg, attend_mma_kernel<LAYOUT, VLAYOUT, QSPLIT, PAGED, CAP>, a);
 }
 
 template <int LAYOUT, int VLAYOUT>
@@ -820,6 +825,11 @@ cudaError_t launch_pair_t(const AttendArgs &a, cudaStream_t st) {
 
 }  // namespace
 
+bool capture_supported(const AttendArgs &a) {
+  const int L = a.cache.layout;
+  return is_hadamard(L) && a.cache.v_layout == L && a.cache.page_shift < 0 && mma_supported(a);
+}
+
 bool mma_supported(const AttendArgs &a) {
   const int L = a.cache.layout, VL = a.cache.v_layout;
   if (prefill_supported(a)) return true;                 // includes the mixed K/V pairs it is built for
@@ -829,13 +839,16 @@ bool mma_supported(const AttendArgs &a) {
 
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
   if (prefill_supported(a)) return launch_attend_prefill(a, st);
+  if (a.cap_scores && a.cache.layout != KVQ_HAD_INT4) return cudaErrorNotSupported;
   if (uses_mma4(a.cache.layout)) return launch_attend_mma4(a, st);
   const bool paged = a.cache.page_shift >= 0;
   const int L = a.cache.layout, VL = a.cache.v_layout;
   if (L == KVQ_Q6_0) return launch_attend_mma_q6(a, st);
-  if (L == KVQ_HAD_INT4)                                 // int8 query codes are exact
+  if (L == KVQ_HAD_INT4) {                               // int8 query codes are exact
+    if (a.cap_scores) return paged ? cudaErrorNotSupported : launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, false, true>(a, st);
     return paged ? launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, true>(a, st)
                  : launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, false>(a, st);
+  }
   if (L == KVQ_Q4_0 && VL == KVQ_Q4_0) return launch_pair_t<KVQ_Q4_0, KVQ_Q4_0>(a, st);
   if (L == KVQ_Q8_0 && VL == KVQ_Q8_0) return launch_pair_t<KVQ_Q8_0, KVQ_Q8_0>(a, st);
   if (L == KVQ_Q4_0 && VL == KVQ_Q8_0) return launch_pair_t<KVQ_Q4_0, KVQ_Q8_0>(a, st);

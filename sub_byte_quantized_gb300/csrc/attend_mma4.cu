@@ -604,17 +604,9 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
 
 template <int LAYOUT, bool QSPLIT, bool PAGED>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = set_smem_once(configured, attend_mma4_kernel<LAYOUT, QSPLIT, PAGED>, Geo4<LAYOUT>::SMEM);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_mma4_kernel<LAYOUT, QSPLIT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Geo4<LAYOUT>::SMEM);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kThreads);

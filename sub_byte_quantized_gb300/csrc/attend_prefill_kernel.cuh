@@ -180,7 +180,9 @@ __device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &s
 // DEC (at most 16 query rows per kv head, one row block): the four warps split each stage's
 // tokens (16 each) over the same 16 rows and merge their softmax states at the end, instead of
 // one warp scoring every token while the other three only unpack.
-template <int KL, int VL, bool PAGED, bool DEC>
+// CAP: score capture (Hadamard layouts, contiguous cache): every exact integer body score the CTA
+// computes and each row's int8 query scale also go to a.cap_scores / a.cap_sq.
+template <int KL, int VL, bool PAGED, bool DEC, bool CAP = false>
 __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefill_kernel(AttendArgs a) {
   using G = PGeo<KL, VL>;
   constexpr int NTJ = DEC ? 2 : 4;                       // 8-token score tiles per pass
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   using PV = typename G::V;
   constexpr bool HAD = G::HAD, ASYMK = PK::ASYM, ASYMV = PV::ASYM;
   constexpr int kRing = G::RING;
+  static_assert(!CAP || (HAD && !PAGED), "score capture: Hadamard layouts, contiguous cache");
   extern __shared__ __align__(1024) uint8_t smem[];
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.launch_dependents;");
@@ -304,6 +307,7 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
             (uint32_t)(q8v[0] & 0xFF) | ((uint32_t)(q8v[1] & 0xFF) << 8) | ((uint32_t)(q8v[2] & 0xFF) << 16) |
             ((uint32_t)(q8v[3] & 0xFF) << 24);
         if (lane == 0) sqs[lr] = sq;
+        if (CAP && lane == 0 && chunk_id == 0 && r < R) a.cap_sq[grow] = sq;
       }
     } else {
       float mx = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
@@ -545,7 +549,6 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
     const auto pass_tok = [warp](int hh) { return DEC ? 16 * warp : 32 * hh; };
 #pragma unroll 1
     for (int hh = 0; hh < NPASS; ++hh) {
-      const int tb = DEC ? 16 * warp : tb;        // the pass's first token within the stage
       const int tsub = ts + pass_tok(hh);
       if (tsub > warp_lim) break;
       float s[NTJ][4];
@@ -575,6 +578,15 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
           for (int j = 0; j < NTJ; ++j)
             mma1688(d[j], az0, az1,
                     *reinterpret_cast<const uint32_t *>(sb + G::OFF_ZK + (pass_tok(hh) + 8 * j + g) * 8 + 4 * (c & 1)));
+        }
+        if constexpr (CAP) {                             // d holds the exact integer dots
+#pragma unroll
+          for (int j = 0; j < NTJ; ++j)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int r = (k & 2) ? rg8 : rg, t = tsub + 8 * j + 2 * c + (k & 1);
+              if (r < R && t < t_end) capture_score(a, bb, kvh, r, t, __float2int_rn(d[j][k]));
+            }
         }
 #pragma unroll
         for (int j = 0; j < NTJ; ++j) {
@@ -781,19 +793,12 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   }
 }
 
-template <int KL, int VL, bool PAGED, bool DEC>
+template <int KL, int VL, bool PAGED, bool DEC, bool CAP = false>
 cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   using G = PGeo<KL, VL>;
-  static bool configured[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = set_smem_once(configured, attend_prefill_kernel<KL, VL, PAGED, DEC, CAP>, G::SMEM);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!configured[dev]) {
-    e = cudaFuncSetAttribute(attend_prefill_kernel<KL, VL, PAGED, DEC>, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
   const int R = a.gqa * a.n_q;
   cudaLaunchConfig_t cfg = {};
   // Hadamard: more chunk indices for the recent window (when present), kWinChunk tokens each
@@ -806,7 +811,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attend_prefill_kernel<KL, VL, PAGED, DEC>, a);
+  return cudaLaunchKernelEx(&cfg, attend_prefill_kernel<KL, VL, PAGED, DEC, CAP>, a);
 }
 
 // The launch for a layout pair: contiguous or paged; DEC for one row block when the pair has no
@@ -814,6 +819,15 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
 template <int KL, int VL>
 cudaError_t launch_pair(const AttendArgs &a, cudaStream_t st) {
   const bool paged = a.cache.page_shift >= 0;
+  if (a.cap_scores) {                                    // score capture: one layout of the Hadamard pair
+    if constexpr (is_hadamard(KL) && KL == VL) {
+      if (paged) return cudaErrorNotSupported;
+      if (!decode_kernel(KL, VL) && a.gqa * a.n_q <= 16) return launch_t<KL, VL, false, true, true>(a, st);
+      return launch_t<KL, VL, false, false, true>(a, st);
+    } else {
+      return cudaErrorNotSupported;
+    }
+  }
   if constexpr (!decode_kernel(KL, VL)) {
     if (a.gqa * a.n_q <= 16)
       return paged ? launch_t<KL, VL, true, true>(a, st) : launch_t<KL, VL, false, true>(a, st);

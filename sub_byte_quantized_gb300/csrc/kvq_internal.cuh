@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the C ABI).
 #pragma once
 
+#include <atomic>
 #include <climits>
 #include <cstddef>
 #include <cstdint>
@@ -62,6 +63,23 @@ __host__ __device__ constexpr bool decode_kernel(int kl, int vl) {
 // have no decode kernel.
 __host__ __device__ constexpr bool prefill_shape(int kl, int vl, int D, int rows) {
   return D == 128 && prefill_pair(kl, vl) && (rows > 8 || !decode_kernel(kl, vl));
+}
+
+// The opt-in dynamic shared-memory size of `kernel` is a per-device function attribute: set it
+// the first time the kernel is launched on each device. `done` is the caller's flag array (one
+// per kernel); threads that race on a first launch may both set the attribute, which is harmless.
+template <class K>
+inline cudaError_t set_smem_once(std::atomic<bool> (&done)[kMaxDevices], K *kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!done[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev].store(true, std::memory_order_release);
+  }
+  return cudaSuccess;
 }
 
 // Device-side view of a cache; index 0 = K, 1 = V. Rows of the payload / scale / zero planes:
@@ -129,7 +147,20 @@ struct AttendArgs {
   float *part_m, *part_l, *part_o;   // [rows][C], [rows][C], [rows][C][D]
   int8_t *q8;                         // HAD: [rows][D]
   float *s_q, *q_rot;                 // HAD: [rows], [rows][D]
+  // Score capture (Hadamard layouts, contiguous cache; nullptr in every ordinary call): the
+  // tensor-core kernel that scores the body also writes each exact integer score it computes to
+  // cap_scores [B][Hq][n_q][n_body] and each row's int8 query scale to cap_sq [B][Hq][n_q].
+  int32_t *cap_scores;
+  float *cap_sq;
 };
+// Row index (b, hq, qi) of query row r (of the gqa * n_q rows of kv head kvh).
+__device__ __forceinline__ size_t query_row_index(const AttendArgs &a, int bb, int kvh, int r) {
+  return ((size_t)bb * a.Hq + kvh * a.gqa + r / a.n_q) * a.n_q + r % a.n_q;
+}
+// Score capture: the integer score of query row r against body token t.
+__device__ __forceinline__ void capture_score(const AttendArgs &a, int bb, int kvh, int r, int t, int v) {
+  a.cap_scores[query_row_index(a, bb, kvh, r) * a.n_body + t] = v;
+}
 
 // Launchers (return cudaGetLastError() after enqueueing).
 // Append n_new rows per (batch, kv head) at positions pos0 + j, or (seq_pos != nullptr) at the
@@ -146,6 +177,8 @@ cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, 
 // Tensor-core phase 1 for the shapes it covers; returns cudaErrorNotSupported when it does not
 // cover the call (the caller then uses the generic kernel).
 bool mma_supported(const AttendArgs &a);
+// Whether the call's body is scored by a tensor-core kernel that is also built with score capture.
+bool capture_supported(const AttendArgs &a);
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st);
 cudaError_t launch_attend_mma4(const AttendArgs &a, cudaStream_t st);
 bool mma_q6_supported(const AttendArgs &a);

@@ -85,6 +85,12 @@ def test_validation_without_device(L):
     assert L.kvq_decode_attend(p(c), 16, 1, 8, 1, 8, 0, 0, float("nan"), 0, 16, 256, 1 << 20, None) == 1
     # debug scores only for the Hadamard layout
     assert L.kvq_debug_scores_i32(p(c), 16, 1, 8, 1, 8, 16, 16, None) == 4
+    # score capture on the attention path: Hadamard only, outputs present and aligned
+    assert L.kvq_debug_attend_scores_i32(p(c), 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 1 << 20, 16, 16, None) == 4
+    ch = KvqCache(2, 1, 2, 128, 64, 0, 4096, 4096, 4096, 4096, None, None, None, None)
+    assert L.kvq_debug_attend_scores_i32(p(ch), 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 1 << 20, None, 16, None) == 1
+    assert L.kvq_debug_attend_scores_i32(p(ch), 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 1 << 20, 20, 16, None) == 5
+    assert L.kvq_debug_attend_scores_i32(p(ch), 16, 1, 8, 1, 8, 0, 0, 1.0, 0, 16, 256, 16, 16, 16, None) == 7
     # n_recent belongs to the Hadamard layout only
     c = KvqCache(0, 1, 2, 128, 64, 8, 4096, 4096, 4096, 4096, None, None, None, None)
     assert L.kvq_store_q4_0(p(c), 16, 16, 1, 1, 0, None) == 4

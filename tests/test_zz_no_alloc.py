@@ -1,5 +1,7 @@
 """The allocation-free attention entry point (kvq_decode_attend_static), called through the C
 ABI, gives the same outputs as kvq_decode_attend with a caller workspace, on two calls in a row.
+Both run the same kernels with the same chunking, only the partials' address differs, so the
+outputs must be bitwise equal (the parity tolerance would hide a scratch layout or offset bug).
 
 The entry point serves callers that cannot allocate device memory themselves (e.g. a plugin
 inside an engine that owns the device memory pool); its partials live in a device array built
@@ -8,14 +10,13 @@ already run every other test; it also passes on its own in a fresh process.
 """
 import ctypes as C
 
-import numpy as np
 import pytest
 import torch
 
 import sub_byte_quantized_gb300 as kvq
 from sub_byte_quantized_gb300 import _lib
 from synth import WORKLOADS, make_inputs
-from tests.gpu_helpers import ATOL, RTOL, fill_both
+from tests.gpu_helpers import fill_both
 
 pytestmark = pytest.mark.gpu
 
@@ -28,6 +29,7 @@ def _static_call(dc, q, kv_len, alpha, out, chunk=0, causal=0, q_pos0=0):
     return st
 
 
+# the Hadamard case has a 64-token exact-f32 window, scored in phase 2 from the same scratch
 @pytest.mark.parametrize("name,kv_len", [("c2_q4_0_llama3_8b", 3000), ("c3_had_int4_decode", 1100)])
 def test_static_matches_workspace_entry_point_twice(name, kv_len):
     w = WORKLOADS[name].scaled(batch=2)
@@ -40,8 +42,7 @@ def test_static_matches_workspace_entry_point_twice(name, kv_len):
         st = _static_call(dc, q, kv_len, w.alpha, out)
         torch.cuda.synchronize()
         assert st == 0, _lib.lib().kvq_last_error()
-        got, want = out.cpu().numpy().astype(np.float64), ref.cpu().numpy().astype(np.float64)
-        assert np.all(np.abs(got - want) <= ATOL + RTOL * np.abs(want))
+        assert torch.equal(out, ref)
 
 
 def test_static_rejects_calls_beyond_its_scratch():
