@@ -182,6 +182,21 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
     if (per_head < 1) per_head = 1;
     const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
     chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
+  } else if (kvq::tc_prefill_shape(c.layout, c.v_layout, c.D, rows)) {
+    // tcgen05 kernel, one CTA of 128 rows per SM: the number of body chunks per row block (1..8)
+    // whose grid takes the fewest waves x (stages per chunk + about two stages of fixed cost per CTA)
+    const long long units = (long long)((rows + kvq::kTcRows - 1) / kvq::kTcRows) * n_heads;
+    const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
+    const long long stages = (body + 63) / 64;
+    long long best = 1, best_cost = -1;
+    for (long long n = 1; n <= 8; ++n) {
+      const long long per = (stages + n - 1) / n;
+      if (per * 64 > 8192) continue;
+      const long long waves = (units * n + sms - 1) / sms;
+      const long long cost = waves * (per + 2);
+      if (best_cost < 0 || cost < best_cost) { best = n; best_cost = cost; }
+    }
+    chunk = ((stages + best - 1) / best) * 64;
   } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows)) {
     // row-side kernel: CTAs of 64 query rows; split the body into enough chunks for about four
     // waves of resident CTAs
@@ -237,6 +252,8 @@ kvq_status resolve_core(int n_q_heads, int n_q, int kv_len, int causal, int q_po
   a.n_wchunks = (a.n_win + kvq::kWinChunk - 1) / kvq::kWinChunk;
   a.C = a.n_chunks + a.n_wchunks;
   a.win_in_reduce = 0;
+  a.y_base = 0;
+  a.q_prepped = 0;
   a.fresh_lo = 0;
   a.fresh_hi = INT_MAX;
   a.seq_lens = nullptr;

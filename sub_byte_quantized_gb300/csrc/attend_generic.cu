@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
 
 // Hadamard query preparation: one warp per query row.
 template <int V>
-__global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows) {
+__global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows, bool write_rot) {
   const int lane = threadIdx.x & 31;
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (r >= rows) return;
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows) {
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     a.q8[(size_t)r * D + lane * V + i] = (int8_t)q8[i];
-    a.q_rot[(size_t)r * D + lane * V + i] = x[i];
+    if (write_rot) a.q_rot[(size_t)r * D + lane * V + i] = x[i];
   }
   if (lane == 0) a.s_q[r] = s;
 }
@@ -342,11 +342,11 @@ cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st) {
   return a.cache.D == 128 ? launch_generic_dt<128, 64>(a, st) : launch_generic_dt<256, 32>(a, st);
 }
 
-cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st) {
+cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st, bool write_rot) {
   const int rows = a.cache.B * a.Hq * a.n_q;
   const unsigned blocks = (unsigned)(((size_t)rows * 32 + 255) / 256);
-  if (a.cache.D == 128) had_prep_kernel<4><<<blocks, 256, 0, st>>>(a, rows);
-  else had_prep_kernel<8><<<blocks, 256, 0, st>>>(a, rows);
+  if (a.cache.D == 128) had_prep_kernel<4><<<blocks, 256, 0, st>>>(a, rows, write_rot);
+  else had_prep_kernel<8><<<blocks, 256, 0, st>>>(a, rows, write_rot);
   return cudaGetLastError();
 }
 

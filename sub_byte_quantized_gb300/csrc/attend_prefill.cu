@@ -13,7 +13,24 @@ bool prefill_supported(const AttendArgs &a) {
          a.chunk % kStage == 0;
 }
 
+// Many-row Hadamard calls: query preparation, the body chunks on the tcgen05 kernel, then the window
+// chunks (if any) on the row-side kernel. Launch chaining: the preparation waits for the preceding
+// kernel (a plain launch); every tcgen05 CTA waits for the preparation; the window launch's first CTA
+// waits for the tcgen05 grid, so phase 2 (which waits for the window launch) sees every partial.
+cudaError_t launch_prefill_tc(const AttendArgs &a, cudaStream_t st) {
+  cudaError_t e = launch_had_prep(a, st, a.n_wchunks > 0);   // f32 rotated rows for the window chunks
+  if (e == cudaSuccess) e = launch_attend_prefill_tc_body(a, st);
+  if (e != cudaSuccess || a.n_wchunks == 0) return e;
+  AttendArgs w = a;
+  w.y_base = a.n_chunks;                                 // window chunks only
+  w.q_prepped = 1;
+  w.cap_scores = nullptr;
+  return a.cache.layout == KVQ_HAD_INT2 ? launch_pair<KVQ_HAD_INT2, KVQ_HAD_INT2>(w, st)
+                                        : launch_pair<KVQ_HAD_INT4, KVQ_HAD_INT4>(w, st);
+}
+
 cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st) {
+  if (tc_prefill_shape(a.cache.layout, a.cache.v_layout, a.cache.D, a.gqa * a.n_q)) return launch_prefill_tc(a, st);
   if (a.cache.layout != a.cache.v_layout) return launch_attend_prefill_mixed(a, st);
   switch (a.cache.layout) {
     case KVQ_HAD_INT4: return launch_pair<KVQ_HAD_INT4, KVQ_HAD_INT4>(a, st);

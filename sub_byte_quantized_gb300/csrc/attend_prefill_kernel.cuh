@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int row0 = blockIdx.x * kRows;
-  const int chunk_id = blockIdx.y;
+  const int chunk_id = blockIdx.y + a.y_base;
   const int bh = blockIdx.z;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
   const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
@@ -294,7 +294,13 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
     if (r < R) {
       const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
       grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
-      load4_f32(a.q, a.q_dtype, grow * kD + lane * 4, x);
+      if (!(HAD && win && a.q_prepped)) load4_f32(a.q, a.q_dtype, grow * kD + lane * 4, x);
+    }
+    if (HAD && win && a.q_prepped) {                   // the rotated rows are already prepared
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < R) v = *reinterpret_cast<const float4 *>(a.q_rot + grow * kD + lane * 4);
+      *reinterpret_cast<float4 *>(smem + G::OFF_QR + lr * kQrPitch + lane * 16) = v;
+      continue;
     }
     if constexpr (HAD) {
       int q8v[4] = {0, 0, 0, 0};
@@ -802,7 +808,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   const int R = a.gqa * a.n_q;
   cudaLaunchConfig_t cfg = {};
   // Hadamard: more chunk indices for the recent window (when present), kWinChunk tokens each
-  cfg.gridDim = dim3((R + kRows - 1) / kRows, a.n_chunks + (G::HAD ? a.n_wchunks : 0), a.cache.B * a.cache.H);
+  cfg.gridDim = dim3((R + kRows - 1) / kRows, a.n_chunks + (G::HAD ? a.n_wchunks : 0) - a.y_base, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = G::SMEM;
   cfg.stream = st;

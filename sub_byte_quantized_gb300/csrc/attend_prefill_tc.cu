@@ -1,0 +1,530 @@
+// Phase 1 of the causal prefill chunk on the fifth-generation tensor cores (tcgen05): the body of a
+// Hadamard int4 / int2 cache (one layout in both planes) scored and weighted for many query rows per
+// kv head at once (tract discussion #2402, "Architecture: Data flow (decode)": the query rows of an
+// appended chunk attend the cached body with their causal limits; "What's done": the body score is
+// the exact integer dot int8(q_rot) . int4(k_rot)).
+//
+// One CTA = 128 query rows of one (batch, kv head) x one split-K chunk of body tokens. The rows are
+// the M side of both products, and the accumulators live in tensor memory (TMEM, 256 columns):
+//   S  = Q8 . K^T       M 128 x N 64 tokens x K 128 dims   -> TMEM columns 0-63 / 64-127 (two stages)
+//   O += P' . V         M 128 x N 128 dims x K 64 tokens   -> TMEM columns 128-255
+// Q8 holds the int8 query codes and K, V the signed 2- or 4-bit codes, all exact in f16 (kind::f16,
+// f32 accumulate), so S is the exact integer dot (|dot| < 2^17). score = alpha * s_q * s_k * dot;
+// the per-token V scale is folded into the probabilities, P' = p * s_v, which go to the PV product
+// as exact f16 hi + lo parts (two MMAs per k-step).
+//
+// Warp roles (14 warps), connected by mbarriers; every wait is bounded in time and a CTA whose wait
+// gives up writes NaN partials for its rows, so a failure shows in the output instead of hanging:
+//   warps 0-7   softmax: warp w serves TMEM lanes (query rows) 32 (w % 4) .. +31 and the column half
+//               w / 4 (S columns 32 h .. +31, O columns 64 h .. +63); the two halves of a row exchange
+//               their maxima through shared memory; online softmax in base 2 with a lazily moved
+//               reference maximum (below); P' hi/lo into shared memory (two buffers)
+//   warp  8     copy: packed K/V rows and per-token scales of each 64-token stage -> a three-slot raw
+//               ring (16-byte cp.async, completion counted on the slot's mbarrier)
+//   warp  9     one lane issues the MMAs (S of stage j, then P'V of stage j - 1) and commits them to
+//               mbarriers; the warp owns the TMEM allocation
+//   warps 10-13 unpack: raw codes -> f16 code tiles (two tile buffers, 128-byte swizzle), scales ->
+//               per-stage arrays
+// Operand layouts (shared-memory descriptors, 128-byte swizzle): Q [128 rows][128 dims] and K
+// [64 tokens][128 dims] K-major in two 64-dim column blocks; V [64 tokens][128 dims] read as the
+// MN-major B operand of the PV product; P' [128 rows][64 tokens] K-major. Within each 8-dim group
+// the tiles keep the unpacker's order (dims 0,4,1,5,2,6,3,7); the output columns follow it.
+//
+// Lazy rescaling: O and l are kept relative to a reference maximum m per row, which moves only when
+// a stage's maximum exceeds it by more than tau (log2 units); then O is rescaled in TMEM (after the
+// previous P'V completes). Otherwise p = 2^(s - m) <= 2^tau, and tau is chosen per stage from the
+// stage's largest V scale so that p * s_v < 2^15 stays well inside the f16 range (tau <= 8). The
+// partial (m, l, O) is exact softmax algebra for any reference, so the result does not depend on
+// when m moves; what tau saves is the wait for the tensor core on almost every stage.
+//
+// The int8 query codes and scales come from the query-preparation kernel launched just before (one
+// pass over the rows instead of one per chunk); the exact-f32 recent window is scored by the
+// row-side kernel's window chunks, launched after this one.
+#include <cfloat>
+#include <climits>
+
+#include "kvq_internal.cuh"
+#include "mma_util.cuh"
+
+namespace kvq {
+namespace {
+using namespace mma;
+
+constexpr int kRows = 128;              // query rows per CTA = TMEM lanes
+constexpr int kStage = 64;              // tokens per stage
+constexpr int kD = 128;
+constexpr int kRing = 3;                // raw stage slots
+constexpr int kWCopy = 8, kWMma = 9, kWUnp = 10, kUnpThreads = 128;
+constexpr int kThreads = (kWUnp + 4) * 32;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Shared memory (bytes). Swizzled operand tiles start on 1 KB boundaries.
+constexpr int kSQ = 0;                          // Q codes f16: two 64-dim column blocks of [128][64]
+constexpr int kST = kSQ + 32768;                // two tile buffers of K (16 KB) + V (16 KB)
+constexpr int kTileBuf = 32768;
+constexpr int kSTsc = kST + 2 * kTileBuf;       // two x (s_k[64], s_v[64]) f32
+constexpr int kSP = kSTsc + 1024;               // two P' buffers of hi [128][64] + lo [128][64] f16
+constexpr int kPBuf = 32768;
+constexpr int kSRaw = kSP + 2 * kPBuf;          // raw ring
+template <int L>
+struct RawGeo {
+  static constexpr int RB = L == KVQ_HAD_INT2 ? 32 : 64;     // payload bytes per token row
+  static constexpr int OFF_V = kStage * RB, OFF_SK = 2 * kStage * RB, OFF_SV = OFF_SK + 4 * kStage;
+  static constexpr int SLOT = OFF_SV + 4 * kStage;
+  static constexpr int RED = kSRaw + kRing * SLOT;           // row maxima [2 parities][2 halves][128], l [2][128]
+  static constexpr int SVMAX = RED + 3072;                    // per tile buffer: the stage's largest s_v, two halves
+  static constexpr int BAR = SVMAX + 64;                      // mbarriers
+  static constexpr int SMEM = BAR + 256;
+  static_assert(SMEM <= 227 * 1024, "fits one CTA per SM");
+};
+static_assert(kSP % 1024 == 0 && kST % 1024 == 0, "swizzled tiles on 1 KB boundaries");
+// mbarriers
+enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + 2, B_SF = B_TE + 2, B_PF = B_SF + 2,
+       B_PVD = B_PF + 2, B_DR = B_PVD + 2, B_RED = B_DR + 1, N_BAR = B_RED + 12 };
+// B_RED: per TMEM lane quarter, the exchange between its two softmax warps: the row maxima of stage
+// j (two barriers, by the parity of j) and the final row sums (one).
+static_assert(N_BAR * 8 <= 256, "mbarriers fit");
+constexpr unsigned long long kWaitNs = 250ull * 1000 * 1000;   // give up on a wait after 250 ms
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(uint64_t *b, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint64_t *b) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_addr(b)) : "memory");
+}
+// Wait for the completion of the phase with the given parity; false if it has not completed
+// within kWaitNs. Each try suspends the warp for up to kSuspendNs unless the phase completes first,
+// so waiting warps do not take issue slots from working ones; the clock is read every 64 tries.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
+  uint64_t start = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done = 0;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(smem_addr(b)), "r"(parity), "r"(kSuspendNs) : "memory");
+    if (done) return true;
+    if ((it & 63) == 63) {
+      const uint64_t now = global_ns();
+      if (start == 0) start = now;
+      else if (now - start > kWaitNs) return false;
+    }
+  }
+}
+// Shared-memory matrix descriptor, 128-byte swizzle: start, leading and stride byte offsets.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor of kind::f16: f16 A and B, f32 accumulator, M x N, B K-major or MN-major.
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t da, uint64_t db, uint32_t id, uint32_t accumulate) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+               ::"r"(d_tmem), "l"(da), "l"(db), "r"(id), "r"(accumulate));
+}
+// The mbarrier gets one arrival once every MMA this thread issued before has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(b)));
+}
+// Byte offset of (row, byte) in a [rows][128 bytes] operand block with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128(int row, int byte) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((((byte >> 4) ^ (row & 7))) << 4) + (byte & 15));
+}
+// 32 consecutive TMEM columns of this warp's 32 lanes (one f32 per column per thread).
+__device__ __forceinline__ void tm_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+// the tiles keep each 8-dim group in the unpacker's pair order: position p holds dim perm8(p)
+__host__ __device__ constexpr int perm8(int p) { return (p >> 1) + 4 * (p & 1); }
+
+template <int L, bool PAGED, bool CAP>
+__global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendArgs a) {
+  using RG = RawGeo<L>;
+  static_assert(!CAP || !PAGED, "score capture: contiguous cache");
+  extern __shared__ __align__(1024) uint8_t sm[];
+  __shared__ uint32_t tmem_base;
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the query codes come from the preceding kernel
+#endif
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + RG::BAR);
+  float *red = reinterpret_cast<float *>(sm + RG::RED);
+  const CacheView &cv = a.cache;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row0 = blockIdx.x * kRows, chunk_id = blockIdx.y, bh = blockIdx.z;
+  const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const SeqLen sl = seq_of_t<PAGED>(a, bb);
+  const int R = a.gqa * a.n_q;
+  const int t0 = chunk_id * sl.chunk, t1 = min(sl.n_body, t0 + sl.chunk);
+  int w_lim = -1;
+  for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit(a, sl, r % a.n_q));
+  if (t0 > w_lim || t0 >= t1) return;                   // no row of this block sees the chunk
+  const int t_end = min(t1, w_lim + 1);
+  const int n_st = (t_end - t0 + kStage - 1) / kStage;
+  const size_t head_row0 = (size_t)bh * cv.cap;
+
+  if (tid == 0) {
+    for (int i = 0; i < kRing; ++i) {
+      bar_init(bar + B_RAWF + i, 32);                   // the copy lanes' cp.async completions
+      bar_init(bar + B_RAWE + i, kUnpThreads);
+    }
+    for (int i = 0; i < 2; ++i) {
+      bar_init(bar + B_TF + i, kUnpThreads);
+      bar_init(bar + B_TE + i, 1);
+      bar_init(bar + B_SF + i, 1);
+      bar_init(bar + B_PF + i, 256);                    // the softmax threads
+      bar_init(bar + B_PVD + i, 1);
+    }
+    bar_init(bar + B_DR, 1);
+    for (int i = 0; i < 12; ++i) bar_init(bar + B_RED + i, 64);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // ---- query codes of the CTA's rows as exact f16 in the tiles' dim order: each unit is one
+  // 8-dim group of one row (16 int8 -> one 16-byte store of four (dim i, dim i + 4) pairs)
+  for (int u = tid; u < kRows * 16; u += kThreads) {
+    const int lr = u >> 4, gi = u & 15, r = row0 + lr;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (r < R) {
+      const uint2 c8 = *reinterpret_cast<const uint2 *>(a.q8 + query_row_index(a, bb, kvh, r) * kD + 8 * gi);
+      const int8_t *cb = reinterpret_cast<const int8_t *>(&c8);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) w[k] = pack_f16x2((float)cb[k], (float)cb[k + 4]);
+    }
+    *reinterpret_cast<uint4 *>(sm + kSQ + (gi >> 3) * 16384 + sw128(lr, 16 * (gi & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (warp == kWMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_addr(&tmem_base)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t tmem = tmem_base;
+  bool ok = true;
+
+  if (warp == kWCopy) {
+    // ---------------- copy: stage j -> raw slot j % kRing; rows past t_end are zero-filled
+    for (int j = 0; j < n_st && ok; ++j) {
+      const int slot = j % kRing;
+      if (j >= kRing) ok = bar_wait(bar + B_RAWE + slot, ((j / kRing) - 1) & 1);
+      if (!ok) break;
+      const int ts = t0 + j * kStage;
+      const size_t r0 = cache_row_t<PAGED>(cv, bb, kvh, head_row0, ts);   // 64 consecutive plane rows
+      uint8_t *raw = sm + kSRaw + slot * RG::SLOT;
+      const uint8_t *kp = cv.payload[0] + r0 * RG::RB, *vp = cv.payload[1] + r0 * RG::RB;
+#pragma unroll
+      for (int k = 0; k < kStage * RG::RB / 16 / 32; ++k) {
+        const int q = lane + 32 * k;                     // 16-byte piece q of the stage's rows
+        const bool in = ts + q / (RG::RB / 16) < t_end;
+        cp_async16(smem_addr(raw + 16 * q), kp + (in ? 16 * q : 0), in ? 16 : 0);
+        cp_async16(smem_addr(raw + RG::OFF_V + 16 * q), vp + (in ? 16 * q : 0), in ? 16 : 0);
+      }
+      const float *skp = static_cast<const float *>(cv.scale[0]) + r0;
+      const float *svp = static_cast<const float *>(cv.scale[1]) + r0;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int t = lane + 32 * k;
+        const bool in = ts + t < t_end;
+        cp_async4(smem_addr(raw + RG::OFF_SK + 4 * t), skp + (in ? t : 0), in ? 4 : 0);
+        cp_async4(smem_addr(raw + RG::OFF_SV + 4 * t), svp + (in ? t : 0), in ? 4 : 0);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar + B_RAWF + slot)) : "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp >= kWUnp) {
+    // ---------------- unpack: raw slot -> tile buffer j & 1 (each thread 8 (row, 8-dim group) units per plane)
+    const int ut = tid - kWUnp * 32;
+    for (int j = 0; j < n_st && ok; ++j) {
+      const int slot = j % kRing, tb = j & 1;
+      ok = bar_wait(bar + B_RAWF + slot, (j / kRing) & 1);
+      if (ok && j >= 2) ok = bar_wait(bar + B_TE + tb, ((j - 2) >> 1) & 1);   // P'V of stage j - 2 done
+      if (!ok) break;
+      const uint8_t *raw = sm + kSRaw + slot * RG::SLOT;
+      uint8_t *tk = sm + kST + tb * kTileBuf, *tv = tk + 16384;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int u = ut + kUnpThreads * k;
+        const int row = u >> 4, gi = u & 15;
+        const uint32_t off = (uint32_t)(gi >> 3) * 8192 + sw128(row, 16 * (gi & 7));
+        uint32_t o[4];
+        if constexpr (L == KVQ_HAD_INT2) {
+          unpack8_s2(*reinterpret_cast<const uint16_t *>(raw + row * RG::RB + 2 * gi), o);
+          *reinterpret_cast<uint4 *>(tk + off) = make_uint4(o[0], o[1], o[2], o[3]);
+          unpack8_s2(*reinterpret_cast<const uint16_t *>(raw + RG::OFF_V + row * RG::RB + 2 * gi), o);
+          *reinterpret_cast<uint4 *>(tv + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        } else {
+          unpack8_q4(*reinterpret_cast<const uint32_t *>(raw + row * RG::RB + 4 * gi), o);
+          *reinterpret_cast<uint4 *>(tk + off) = make_uint4(o[0], o[1], o[2], o[3]);
+          unpack8_q4(*reinterpret_cast<const uint32_t *>(raw + RG::OFF_V + row * RG::RB + 4 * gi), o);
+          *reinterpret_cast<uint4 *>(tv + off) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+      // per-stage scales: s_k[0..63] then s_v[0..63] (consecutive in the raw slot); the two warps
+      // holding s_v also record its maximum (non-negative floats order like their bit patterns)
+      const float scv = *reinterpret_cast<const float *>(raw + RG::OFF_SK + 4 * ut);
+      reinterpret_cast<float *>(sm + kSTsc + tb * 512)[ut] = scv;
+      if (ut >= 64) {
+        const uint32_t mxv = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(scv, 0.0f)));
+        if (lane == 0) reinterpret_cast<uint32_t *>(sm + RG::SVMAX)[2 * tb + ((ut - 64) >> 5)] = mxv;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      bar_arrive(bar + B_RAWE + slot);
+      bar_arrive(bar + B_TF + tb);
+    }
+  } else if (warp == kWMma) {
+    // ---------------- MMA issue (one thread): S of stage j, then P'V of stage j - 1
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc(kRows, kStage, false), id_o = idesc(kRows, kD, true);
+      auto pv = [&](int i) {
+        const int pb = i & 1;
+        ok = ok && bar_wait(bar + B_PF + pb, (i >> 1) & 1);
+        if (!ok) return;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t vt = smem_addr(sm + kST + (i & 1) * kTileBuf + 16384);
+        const uint32_t ph = smem_addr(sm + kSP + pb * kPBuf), pl = ph + 16384;
+#pragma unroll
+        for (int ks = 0; ks < kStage / 16; ++ks) {
+          const uint64_t db = sdesc(vt + 2048 * ks, 8192, 1024);
+          mma_f16(tmem + 128, sdesc(ph + 32 * ks, 16, 1024), db, id_o, (i > 0 || ks > 0) ? 1u : 0u);
+          mma_f16(tmem + 128, sdesc(pl + 32 * ks, 16, 1024), db, id_o, 1u);
+        }
+        mma_commit(bar + B_TE + (i & 1));               // tile buffer free
+        mma_commit(bar + B_PVD + pb);                   // O holds stage i; P' buffer free
+      };
+      for (int j = 0; j < n_st && ok; ++j) {
+        const int tb = j & 1;
+        ok = bar_wait(bar + B_TF + tb, (j >> 1) & 1);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t kt = smem_addr(sm + kST + tb * kTileBuf);
+#pragma unroll
+        for (int kb = 0; kb < kD / 16; ++kb) {
+          const uint64_t da = sdesc(smem_addr(sm + kSQ + (kb >> 2) * 16384) + 32 * (kb & 3), 16, 1024);
+          const uint64_t db = sdesc(kt + (kb >> 2) * 8192 + 32 * (kb & 3), 16, 1024);
+          mma_f16(tmem + 64 * tb, da, db, id_s, kb > 0 ? 1u : 0u);
+        }
+        mma_commit(bar + B_SF + tb);
+        if (j >= 1) pv(j - 1);
+      }
+      if (ok) pv(n_st - 1);
+      mma_commit(bar + B_DR);                           // drain: every MMA issued above completes
+      if (!bar_wait(bar + B_DR, 0)) ok = false;
+    }
+  } else {
+    // ---------------- softmax: row lr = TMEM lane, column half h
+    const int q4 = warp & 3, h = warp >> 2;
+    const int lr = 32 * q4 + lane, r = row0 + lr;
+    const bool live = r < R;
+    const int lim = live ? row_limit(a, sl, r % a.n_q) : -1;
+    const size_t qrow = live ? query_row_index(a, bb, kvh, r) : 0;
+    const float arow = live ? a.scale * a.s_q[qrow] * kLog2e : 0.0f;
+    if (CAP && live && chunk_id == 0 && h == 0) a.cap_sq[qrow] = a.s_q[qrow];
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    uint64_t *xbar = bar + B_RED + 3 * q4;              // this quarter's exchange barriers
+    float m = -INFINITY, l = 0.0f;
+    for (int j = 0; j < n_st && ok; ++j) {
+      const int tb = j & 1, pb = j & 1, ts = t0 + j * kStage;
+      ok = __all_sync(0xffffffffu, bar_wait(bar + B_TF + tb, (j >> 1) & 1) && bar_wait(bar + B_SF + tb, (j >> 1) & 1));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const float *tsc = reinterpret_cast<const float *>(sm + kSTsc + tb * 512);
+      float s[32];
+      tm_ld32(tmem + lane_base + 64 * tb + 32 * h, s);
+      const int tc0 = ts + 32 * h;                      // token of column 0 of this half
+      if constexpr (CAP) {
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (tc0 + i < t_end) a.cap_scores[qrow * a.n_body + tc0 + i] = __float2int_rn(s[i]);
+        }
+      }
+      const bool edge = tc0 + 31 > lim || tc0 + 32 > t_end;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        s[i] = s[i] * tsc[32 * h + i] * arow;
+        if (edge && !(tc0 + i <= lim && tc0 + i < t_end)) s[i] = -INFINITY;
+      }
+      float mh = s[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) mh = fmaxf(mh, s[i]);
+      red[(tb * 2 + h) * kRows + lr] = mh;
+      bar_arrive(xbar + tb);
+      ok = __all_sync(0xffffffffu, bar_wait(xbar + tb, (j >> 1) & 1));
+      if (!ok) break;
+      const float mx = fmaxf(mh, red[(tb * 2 + (h ^ 1)) * kRows + lr]);   // the stage's row maximum
+      // tau: p * s_v < 2^15 for p <= 2^tau (svmax < 2^(e + 1))
+      const float *svm = reinterpret_cast<const float *>(sm + RG::SVMAX) + 2 * tb;
+      const float svmax = fmaxf(svm[0], svm[1]);
+      const int e = (int)((__float_as_uint(svmax) >> 23) & 0xFF) - 127;
+      const float tau = (float)min(8, max(0, 14 - e));
+      const bool bump = mx > m + tau;                   // m = -inf: the first visible stage
+      const float m_new = bump ? mx : m;
+      const float mu = m_new == -INFINITY ? 0.0f : m_new;
+      const float corr = bump ? ex2(m - mu) : 1.0f;     // m = -inf -> 0
+      if (j >= 1 && __any_sync(0xffffffffu, bump && m != -INFINITY)) {
+        // O holds stages < j once P'V of stage j - 1 is done: rescale this half's 64 columns
+        ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + ((j - 1) & 1), ((j - 1) >> 1) & 1));
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;");
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          float o[32];
+          tm_ld32(tmem + lane_base + 128 + 64 * h + c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tm_st32(tmem + lane_base + 128 + 64 * h + c, o);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      if (j >= 2) {                                     // P' buffer pb was read by P'V of stage j - 2
+        ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + pb, ((j - 2) >> 1) & 1));
+        if (!ok) break;
+      }
+      // P' = p * s_v as exact f16 hi + lo, tokens 32 h + 8 k .. +7 -> one 16-byte chunk each
+      float sum = 0.0f;
+      uint8_t *pbase = sm + kSP + pb * kPBuf;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 8 * k + 2 * e;
+          const float p0 = ex2(s[i] - mu), p1 = ex2(s[i + 1] - mu);
+          sum += p0 + p1;
+          const float q0 = p0 * tsc[64 + 32 * h + i], q1 = p1 * tsc[64 + 32 * h + i + 1];
+          hi[e] = pack_f16x2(q0, q1);
+          const float2 hf = __half22float2(u32_as_h2(hi[e]));
+          lo[e] = pack_f16x2(q0 - hf.x, q1 - hf.y);
+        }
+        const uint32_t off = sw128(lr, 16 * (4 * h + k));
+        *reinterpret_cast<uint4 *>(pbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(pbase + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      l = l * corr + sum;
+      m = m_new;
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      bar_arrive(bar + B_PF + pb);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + ((n_st - 1) & 1), ((n_st - 1) >> 1) & 1));
+    if (ok) {                                           // the row's l is the sum of its two halves
+      red[(4 + h) * kRows + lr] = l;
+      bar_arrive(xbar + 2);
+      ok = __all_sync(0xffffffffu, bar_wait(xbar + 2, 0));
+      l += red[(4 + (h ^ 1)) * kRows + lr];
+    }
+    if (ok) {                                           // warp-uniform: the TMEM loads need the whole warp
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const bool write = live && t0 <= lim;
+      const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
+      const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
+      float *po = a.part_o + pi * kD + 64 * h;
+#pragma unroll
+      for (int c = 0; c < 64; c += 32) {
+        float o[32];
+        tm_ld32(tmem + lane_base + 128 + 64 * h + c, o);
+        if (write) {
+#pragma unroll
+          for (int g8 = 0; g8 < 4; ++g8) {              // position 8 g8 + p holds dim 8 g8 + perm8(p)
+            const float *x = o + 8 * g8;
+            *reinterpret_cast<float4 *>(po + c + 8 * g8) = make_float4(x[0], x[2], x[4], x[6]);
+            *reinterpret_cast<float4 *>(po + c + 8 * g8 + 4) = make_float4(x[1], x[3], x[5], x[7]);
+          }
+        }
+      }
+      if (write && h == 0) {
+        a.part_m[pi] = m * kLn2;                        // natural-log units, like the other kernels
+        a.part_l[pi] = l;
+      }
+    }
+  }
+  // a wait that gave up anywhere in the CTA: its rows' partials become NaN (m = 0, l = NaN), which
+  // the reduce turns into NaN outputs
+  const bool failed = __syncthreads_or(!ok);
+  if (failed && warp < 8) {
+    const int r = row0 + 32 * (warp & 3) + lane;
+    if (r < R && t0 <= row_limit(a, sl, r % a.n_q)) {
+      const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
+      const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
+      for (int d = 64 * (warp >> 2); d < 64 * (warp >> 2) + 64; ++d) a.part_o[pi * kD + d] = __int_as_float(0x7fc00000);
+      if (warp < 4) {
+        a.part_m[pi] = 0.0f;
+        a.part_l[pi] = __int_as_float(0x7fc00000);
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  if (warp == kWMma) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+}
+
+template <int L, bool PAGED, bool CAP>
+cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st) {
+  static std::atomic<bool> configured[kMaxDevices];
+  cudaError_t e = set_smem_once(configured, attend_prefill_tc_kernel<L, PAGED, CAP>, RawGeo<L>::SMEM);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.gqa * a.n_q + kRows - 1) / kRows, a.n_chunks, a.cache.B * a.cache.H);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = RawGeo<L>::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attend_prefill_tc_kernel<L, PAGED, CAP>, a);
+}
+
+template <int L>
+cudaError_t launch_layout(const AttendArgs &a, cudaStream_t st) {
+  const bool paged = a.cache.page_shift >= 0;
+  if (a.cap_scores) return paged ? cudaErrorNotSupported : launch_tc<L, false, true>(a, st);
+  return paged ? launch_tc<L, true, false>(a, st) : launch_tc<L, false, false>(a, st);
+}
+
+}  // namespace
+
+cudaError_t launch_attend_prefill_tc_body(const AttendArgs &a, cudaStream_t st) {
+  if (a.cache.layout == KVQ_HAD_INT2) return launch_layout<KVQ_HAD_INT2>(a, st);
+  return launch_layout<KVQ_HAD_INT4>(a, st);
+}
+
+}  // namespace kvq

@@ -39,6 +39,12 @@ __host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 :
 // Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, at most four query rows per
 // kv head (gqa * n_q).
 __host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows <= 4; }
+// tcgen05 kernel for the body of many-row Hadamard calls (causal prefill chunks): 128 query rows per
+// CTA, one CTA per SM; one Hadamard layout in both planes, head_dim 128, more than 64 rows per kv head.
+constexpr int kTcRows = 128;
+__host__ __device__ constexpr bool tc_prefill_shape(int kl, int vl, int D, int rows) {
+  return kl == vl && is_hadamard(kl) && D == 128 && rows > 64;
+}
 // Row-side tensor-core kernel: 64 query rows per CTA; three resident CTAs per SM for the Hadamard
 // layout, two for Q4_0 / asymmetric (their value tiles are hi + lo pairs).
 constexpr int kPrefillRows = 64;
@@ -131,6 +137,8 @@ struct AttendArgs {
   int n_wchunks;            // window chunks of kWinChunk tokens (0 without a window)
   int C;                    // total partials per row: n_chunks + n_wchunks
   int win_in_reduce;        // HAD: phase 2 computes the window chunk's partial itself
+  int y_base;               // row-side kernel: chunk index of its grid's first y (window-only launches)
+  int q_prepped;            // row-side window chunks: the f32 rotated query rows are in q_rot
   // Token rows [fresh_lo, fresh_hi) were written by the kernel launched just before phase 1 (an
   // append in the same call): only phase-1 CTAs that read them, and the first CTA, wait for it.
   // [0, INT_MAX) when the preceding kernel is unknown (every CTA waits).
@@ -168,7 +176,9 @@ __device__ __forceinline__ void capture_score(const AttendArgs &a, int bb, int k
 cudaError_t launch_store(const CacheView &c, const void *k_new, const void *v_new, int dtype,
                          int n_new, int pos0, cudaStream_t st, const int32_t *seq_pos = nullptr,
                          int pos_offset = 0);
-cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st);
+// Hadamard query preparation into the workspace: int8 codes and scales, and (write_rot) the f32
+// rotated rows.
+cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st, bool write_rot = true);
 cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st);
 cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl);
 cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, int Hq, int n_q,
@@ -187,6 +197,9 @@ cudaError_t launch_attend_mma_q6(const AttendArgs &a, cudaStream_t st);
 // causal prefill chunks), Hadamard int4 layout.
 bool prefill_supported(const AttendArgs &a);
 cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st);
+// The body chunks of a tc_prefill_shape call on the tcgen05 kernel (the query codes and scales must
+// already be in the workspace: launch_had_prep with write_rot = false).
+cudaError_t launch_attend_prefill_tc_body(const AttendArgs &a, cudaStream_t st);
 cudaError_t launch_attend_prefill_mixed(const AttendArgs &a, cudaStream_t st);
 
 // ----------------------------------------------------------------- device helpers
