@@ -627,6 +627,9 @@ void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_p
   window_ctas = false;                                   // the decode kernels leave the window to phase 2
   if (c.layout == KVQ_Q6_0 && c.v_layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
     ctas_per_sm = kvq::kMmaQ6CtasPerSm(c.D);
+  } else if (kvq::tc_prefill_shape(c.layout, c.v_layout, c.D, rows)) {
+    ctas_per_sm = 1;                                     // the tcgen05 kernel: one CTA of 128 rows per SM
+    ctas_per_unit = (rows + kvq::kTcRows - 1) / kvq::kTcRows;
   } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) &&
              (kvq::is_hadamard(c.layout) || q_dtype != KVQ_F32)) {
     ctas_per_sm = kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2;
