@@ -50,6 +50,14 @@ import numpy as np  # noqa: E402
 DEFAULT_WORKLOAD = "c5_q4_0_llama70b_128k"
 METRIC = "int4-KV decode attention µs/layer and effective HBM GB/s (% peak) at 128K"
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+# vendor nominal figures of one GB300 (NVIDIA's published HBM3e bandwidth and dense bf16 tensor rate),
+# reported beside the measured denominators
+NOMINAL_HBM_GBS, NOMINAL_BF16_TFLOPS = 7900.0, 2250.0
+# the other seeded workloads timed (compactly) inside the default run, so that one bench line carries
+# every configuration
+SUMMARY_WORKLOADS = ("c1_q4_0_tiny", "c2_q4_0_llama3_8b", "c3_had_int4_decode", "c3_had_int4_prefill",
+                     "c4_q6_0_gemma", "c5_asym4_g32_llama70b_128k", "c5_q8_0_llama70b_128k",
+                     "c5_q4_0_k_q8_0_v_llama70b_128k", "c3_had_int2_decode_w256", "paged_q4_0_llama3_8b_ragged")
 L2_BYTES = 129 * 2 ** 20
 DESCRIPTIONS = {
     "c1_q4_0_tiny": "Q4_0 tiny: B1 Hq8 Hkv2 D128 S512 decode, f32 N(0,1) K/V/Q, 2 K outlier channels x8",
@@ -87,6 +95,8 @@ def parse():
     p.add_argument("--quick", action="store_true", help="device timing only (no e2e, variants, CPU baseline)")
     p.add_argument("--no-graph", action="store_true", help="plain stream launches instead of a CUDA graph")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle sample budget")
+    p.add_argument("--summary-steps", type=int, default=200,
+                   help="steps per workload of the default run's per-configuration summary (0 = skip it)")
     return p.parse_args()
 
 
@@ -130,12 +140,16 @@ def kernel_traffic(profile: str, kernel_file: str):
 def chunk_rule(w, spec) -> str:
     """How the automatic split-K chunk of this workload is chosen (it follows the phase-1 kernel)."""
     rows = (w.n_q_heads // w.n_kv_heads) * spec.n_q
-    if w.layout == "q6_0" and w.head_dim in (128, 256) and rows <= 4:
-        return "automatic: one 64-token-multiple chunk per resident CTA of the Q6_0 kernel (two per SM), one wave"
+    if w.layout == "q6_0" and (w.head_dim == 256 or rows <= 8):
+        return ("automatic: one 64-token-multiple chunk per resident CTA of the Q6_0 kernel (two per SM, one per "
+                "group of four query rows), one wave")
     if w.layout == "asym4_g32" and w.head_dim == 128 and rows <= 8:
         return "automatic: one 64-token-multiple chunk per resident CTA of the warp-specialised kernel (two per SM), one wave"
-    if w.layout == "had_int4" and w.head_dim == 128 and rows > 8:
-        return "automatic: body split for about four waves of 64-query-row CTAs; the f32 window is one more chunk"
+    if w.layout in ("had_int4", "had_int2") and w.head_dim == 128 and rows > 64:
+        return ("automatic: the tcgen05 kernel's body split (1..8 chunks per 128-row block, the fewest waves x "
+                "stages); the f32 window is scored in 64-token chunks of its own")
+    if w.head_dim == 128 and rows > 8:
+        return "automatic: body split for about four waves of 64-query-row CTAs"
     return "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp, one wave"
 
 
@@ -581,16 +595,25 @@ def main():
         achieved = spec.read_bytes / (ph_mean / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak}
     traffic = kernel_traffic(*PROFILES[args.workload]) if args.workload in PROFILES else None
+    roof["peak_nominal"] = NOMINAL_BF16_TFLOPS if prefill else NOMINAL_HBM_GBS
+    roof["frac_nominal"] = achieved / roof["peak_nominal"]
     roof.update({"peak_kind": peak_kind, "traffic": traffic, "kernel": "attend phase 1 (split-K chunk partials)",
                  "phase1_us_mean": ph_mean * 1e3, "phase1_us_p10": float(np.percentile(ph_ms, 10)) * 1e3,
                  "phase1_us_p90": float(np.percentile(ph_ms, 90)) * 1e3,
                  "phase1_pass_us_per_step": ev_pass_ms / K * 1e3})
-    # store, phase 1, reduce; the CUDA-core phase 1 (D=256, Q6_0, more than 8 query rows per kv
-    # head) adds the Hadamard query preparation
+    # store (one launch per plane of a mixed cache), phase 1, reduce. Phase 1 is one launch, except:
+    # many Hadamard rows (tcgen05 body) = query preparation + body + the window chunks' launch;
+    # Hadamard on the CUDA cores (head_dim 256) = query preparation + attention
     kl, _, vl = w.layout.partition("+")
-    mixed = bool(vl) and vl != kl                      # mixed K/V precision: one store launch per plane
-    tensor_core = w.layout in ("q4_0", "asym4_g32", "had_int4") and D == 128 and w.gqa * spec.n_q <= 8
-    launches = (2 if mixed else 1) + 2 + (1 if kl.startswith("had") and not tensor_core else 0)
+    mixed = bool(vl) and vl != kl
+    had = kl.startswith("had")
+    if had and not mixed and D == 128 and w.gqa * spec.n_q > 64:
+        phase1_launches = 2 + (1 if spec.n_win > 0 else 0)
+    elif had and D != 128:
+        phase1_launches = 2
+    else:
+        phase1_launches = 1
+    launches = (2 if mixed else 1) + phase1_launches + 1
     l2_note = (f"cache L2-resident ({n_rep} replicas x {cache_bytes / 2**20:.1f} MiB)" if l2_resident else
                f"inputs larger than L2: {n_rep} cache replicas rotated ({n_rep * cache_bytes / 2**20:.0f} MiB > "
                f"{L2_BYTES / 2**20:.0f} MiB L2)")
@@ -641,10 +664,141 @@ def main():
                                         min(K, 1000), chunk, make_caches, dev)
         if world == 1:
             line["cpu_baseline"] = cpu_baseline(w, inp, spec, args.cpu_seconds)
+        if args.workload == DEFAULT_WORKLOAD and args.summary_steps > 0:
+            del caches, ws, kd, vd
+            torch.cuda.empty_cache()
+            line["workloads"] = workload_summaries(kvq, L, dev, stream, args.summary_steps, hbm_peak, bf16_peak)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def workload_summaries(kvq, L, dev, stream, K, hbm_peak, bf16_peak):
+    """Every other seeded workload, timed with the default line's protocol at a smaller step count:
+    K library steps (append + attention, one call each) in a CUDA graph over cache replicas that
+    exceed L2 (or the note says the cache is L2-resident), then the same steps with phase-1 events.
+    Per workload: µs per layer-call, effective GB/s of the step, and phase 1 against its roofline
+    (HBM for the decode shapes, the bf16 tensor peak for the causal prefill chunk)."""
+    import torch
+    from synth import WORKLOADS, make_inputs, make_paged_inputs
+    out = {}
+    for name in SUMMARY_WORKLOADS:
+        w = WORKLOADS[name]
+        if w.page_size:
+            inp = make_paged_inputs(w)
+            lens = inp["seq_lens"]
+            B, H, D, P = w.batch, w.n_kv_heads, w.head_dim, w.page_size
+            S_max, total = int(lens.max()), int(lens.sum())
+            mpp = -(-S_max // P)
+            kp = torch.zeros((B, H, S_max, D), dtype=torch.bfloat16, device=dev)
+            vp = torch.zeros_like(kp)
+            kf = torch.from_numpy(np.ascontiguousarray(inp["k_bits"]).view(np.int16)).view(torch.bfloat16)
+            vf = torch.from_numpy(np.ascontiguousarray(inp["v_bits"]).view(np.int16)).view(torch.bfloat16)
+            for b in range(B):
+                o, Lb = int(inp["offsets"][b]), int(lens[b])
+                kp[b, :, :Lb] = kf[:, o:o + Lb].to(dev)
+                vp[b, :, :Lb] = vf[:, o:o + Lb].to(dev)
+            k_new = torch.stack([kp[b, :, int(lens[b]) - 1:int(lens[b])] for b in range(B)]).contiguous()
+            v_new = torch.stack([vp[b, :, int(lens[b]) - 1:int(lens[b])] for b in range(B)]).contiguous()
+            q = torch.from_numpy(np.ascontiguousarray(inp["q_bits"]).view(np.int16)).view(torch.bfloat16).to(dev)
+            lens_dev = torch.from_numpy(lens.astype(np.int32)).to(dev)
+            read_bytes, flops = 2 * H * total * 18 * (D // 32), 4 * D * total * w.n_q_heads
+            n_rep = min(64, max(2, math.ceil(3 * L2_BYTES / read_bytes) + 1))
+            pools = []
+            for r in range(n_rep):
+                c = kvq.PagedKVCache(w.layout, B, H, D, P, B * mpp, mpp, device=dev)
+                c.set_block_table(np.random.default_rng(w.seed + r).permutation(B * mpp).reshape(B, mpp))
+                kvq.paged_store(c, kp[:, :, :S_max - 1].contiguous(), vp[:, :, :S_max - 1].contiguous(),
+                                torch.zeros(B, dtype=torch.int32, device=dev))
+                pools.append(c)
+            del kp, vp
+            chunk = kvq.paged_attend_plan_chunk(pools[0], w.n_q_heads, 1, lens)
+            ws = torch.empty(max(256, kvq.paged_attend_workspace_bytes(pools[0], w.n_q_heads, 1, S_max, chunk)),
+                             dtype=torch.uint8, device=dev)
+            o_buf = torch.empty((B, w.n_q_heads, 1, D), dtype=torch.float32, device=dev)
+
+            def call(i):
+                kvq.paged_append_decode_attend(pools[i % n_rep], k_new, v_new, q, lens_dev, S_max,
+                                               attn_scale=w.alpha, chunk=chunk, out=o_buf, workspace=ws,
+                                               stream=stream)
+            prefill, held = False, pools
+        else:
+            inp = make_inputs(w)
+            spec = Spec(w, inp)
+            B, H, S, D, fill = spec.B, spec.H, spec.S, spec.D, spec.fill
+
+            def to_dev(n):
+                if w.dtype == "bf16":
+                    return torch.from_numpy(np.ascontiguousarray(inp[n + "_bits"]).view(np.int16)).view(
+                        torch.bfloat16).to(dev)
+                return torch.from_numpy(np.ascontiguousarray(inp[n])).to(dev)
+            kd, vd, q = to_dev("k"), to_dev("v"), to_dev("q")
+            k_new, v_new = kd[:, :, fill:].contiguous(), vd[:, :, fill:].contiguous()
+            read_bytes, flops = spec.read_bytes, spec.flops
+            n_rep = min(64, max(2, math.ceil(3 * L2_BYTES / max(read_bytes, 1)) + 1))
+            caches = []
+            for _ in range(n_rep):
+                c = kvq.KVCache(w.layout, B, H, D, S, n_recent=w.n_recent, device=dev)
+                kvq.store(c, kd[:, :, :fill].contiguous(), vd[:, :, :fill].contiguous(), 0)
+                kvq.store(c, k_new, v_new, fill)
+                caches.append(c)
+            del kd, vd
+            chunk = kvq.attend_chunk(caches[0], w.n_q_heads, spec.n_q, S, 0)
+            ws = torch.empty(max(256, kvq.attend_workspace_bytes(caches[0], w.n_q_heads, spec.n_q, S, chunk)),
+                             dtype=torch.uint8, device=dev)
+            o_buf = torch.empty((B, w.n_q_heads, spec.n_q, D), dtype=torch.float32, device=dev)
+
+            def call(i, spec=spec, caches=caches):
+                kvq.append_decode_attend(caches[i % n_rep], k_new, v_new, fill, q, S, causal=spec.causal,
+                                         q_pos0=spec.q_pos0, attn_scale=w.alpha, chunk=chunk, out=o_buf,
+                                         workspace=ws, stream=stream)
+            prefill, held = spec.causal and spec.n_q > 1, caches
+        ph = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        with torch.cuda.stream(stream):
+            for a, b in ph:
+                a.record(stream)
+                b.record(stream)
+            for i in range(3):
+                call(i)
+        torch.cuda.synchronize(dev)
+        g, g_ev = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(K):
+                call(i)
+        with torch.cuda.graph(g_ev, stream=stream):
+            for i in range(K):
+                L.kvq_profile_phase1_events(ph[i][0].cuda_event, ph[i][1].cuda_event)
+                call(i)
+                L.kvq_profile_phase1_events(None, None)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()                                   # warm
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        step_ms = e0.elapsed_time(e1) / K
+        with torch.cuda.stream(stream):
+            g_ev.replay()
+        torch.cuda.synchronize(dev)
+        ph_ms = statistics.fmean(a.elapsed_time(b) for a, b in ph)
+        if prefill:
+            ach = flops / (ph_ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": round(ach, 1), "unit": "TFLOP/s", "frac": round(ach / bf16_peak, 4),
+                    "frac_nominal": round(ach / NOMINAL_BF16_TFLOPS, 4)}
+        else:
+            ach = read_bytes / (ph_ms / 1e3) / 1e9
+            roof = {"bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
+                    "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4)}
+        out[name] = {"us_per_layer": round(step_ms * 1e3, 2), "gbs": round(read_bytes / (step_ms / 1e3) / 1e9, 1),
+                     "phase1_us": round(ph_ms * 1e3, 2), "roofline": roof, "chunk": chunk,
+                     "read_bytes_per_step": read_bytes, "flops_per_step": flops, "steps": K,
+                     "l2": "cache L2-resident" if n_rep * read_bytes < 2 * L2_BYTES else
+                     f"{n_rep} replicas rotated (> L2)"}
+        del held, g, g_ev, ws, o_buf
+        torch.cuda.empty_cache()
+    return out
 
 
 def store_timings(kvq, w, kd, vd, k_new, v_new, fill, stream, dev):

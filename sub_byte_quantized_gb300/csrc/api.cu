@@ -170,9 +170,11 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
   const bool total_given = work > 0;
   if (!total_given) work = (long long)(n_body > 0 ? n_body : 1) * n_heads;
   long long chunk;
-  if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
+  if (c.layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows) && !kvq::prefill_shape(c.layout, c.v_layout, c.D, rows)) {
+    // one chunk per resident CTA; each group of four query rows has its own CTAs
     const long long ctas = (long long)sms * kvq::kMmaQ6CtasPerSm(c.D);
-    chunk = ((work + ctas - 1) / ctas + 63) / 64 * 64;
+    const long long groups = (rows + 3) / 4;
+    chunk = ((work * groups + ctas - 1) / ctas + 63) / 64 * 64;
   } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) && rows <= 16 &&
              !kvq::decode_kernel(c.layout, c.v_layout)) {
     // row-side kernel in its decode form (one row block, the warps split the tokens): one chunk per
@@ -625,8 +627,10 @@ void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_p
                      bool &window_ctas) {
   ctas_per_unit = 1;
   window_ctas = false;                                   // the decode kernels leave the window to phase 2
-  if (c.layout == KVQ_Q6_0 && c.v_layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows)) {
+  if (c.layout == KVQ_Q6_0 && c.v_layout == KVQ_Q6_0 && kvq::mma_q6_shape(c.D, rows) &&
+      !(kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) && q_dtype != KVQ_F32)) {
     ctas_per_sm = kvq::kMmaQ6CtasPerSm(c.D);
+    ctas_per_unit = (rows + 3) / 4;
   } else if (kvq::tc_prefill_shape(c.layout, c.v_layout, c.D, rows)) {
     ctas_per_sm = 1;                                     // the tcgen05 kernel: one CTA of 128 rows per SM
     ctas_per_unit = (rows + kvq::kTcRows - 1) / kvq::kTcRows;

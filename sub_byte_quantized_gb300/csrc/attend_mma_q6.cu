@@ -1,7 +1,9 @@
 // Tensor-core phase 1 of the split-K decode attention for the Q6_0 layout (per 32-value block:
 // a 16-byte plane of low nibbles, an 8-byte plane of 2-bit high fields, one fp16 scale;
-// "Storage layouts", q6_0, of the FreeToken cache-quantisation PR), head_dim 128 or 256, up to
-// four query rows per kv head (the GQA group times the query rows of the call).
+// "Storage layouts", q6_0, of the FreeToken cache-quantisation PR), head_dim 128 or 256, any number
+// of query rows per kv head (the GQA group times the query rows of the call): a CTA takes a group of
+// up to four of them (the grid's third dimension), so a call with more rows streams each chunk once
+// per group of four.
 //
 // The contraction is the same as in the 4-bit kernel, with mma.sync.m16n8k16 (f16 in, f32
 // accumulate):
@@ -99,7 +101,10 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   const int bh = blockIdx.y;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
   const SeqLen sl = seq_of_t<PAGED>(a, bb);             // this sequence's lengths
-  const int R = a.gqa * a.n_q;
+  // rows of this CTA: group blockIdx.z of four of the kv head's gqa * n_q rows (local row r is row
+  // rbase + r of the kv head)
+  const int rbase = 4 * blockIdx.z;
+  const int R = min(4, a.gqa * a.n_q - rbase);
 
   const int t0 = chunk_id * sl.chunk;
   const int t1 = min(sl.n_body, t0 + sl.chunk);
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
   int w_lim = -1, min_lim = INT_MAX, lim0 = -1, lim1 = -1;
   unsigned row_vis = 0u;
   for (int r = 0; r < R; ++r) {
-    const int l = row_limit_of(a, sl, r);
+    const int l = row_limit_of(a, sl, rbase + r);
     w_lim = max(w_lim, l);
     min_lim = min(min_lim, l);
     if (r == 2 * (c & 1)) lim0 = l;
@@ -186,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
     {
       const int rq = g & 3;
       const bool live = rq < R;
-      const int hq = kvh * a.gqa + (live ? rq / a.n_q : 0);
-      const int qi = live ? rq % a.n_q : 0;
+      const int hq = kvh * a.gqa + (live ? (rbase + rq) / a.n_q : 0);
+      const int qi = live ? (rbase + rq) % a.n_q : 0;
       const size_t grow = ((size_t)bb * a.Hq + hq) * a.n_q + qi;
       float x[NB][8];
       float mx = 0.0f;
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, kMmaQ6CtasPerSm(D)) attend_mma_q6_ke
       wt[w] = cm[w * 4 + r] == -INFINITY ? 0.0f : ex2(cm[w * 4 + r] - M);
       L = fmaf(cl[w * 4 + r], wt[w], L);
     }
-    const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
+    const int hq = kvh * a.gqa + (rbase + r) / a.n_q, qi = (rbase + r) % a.n_q;
     const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
     for (int d = threadIdx.x; d < D; d += kThreads) {
       float acc = 0.0f;
@@ -507,7 +512,7 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   cudaError_t e = set_smem_once(configured, attend_mma_q6_kernel<D, PAGED>, Geom<D>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H);
+  cfg.gridDim = dim3(a.n_chunks, a.cache.B * a.cache.H, (a.gqa * a.n_q + 3) / 4);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Geom<D>::SMEM;
   cfg.stream = st;

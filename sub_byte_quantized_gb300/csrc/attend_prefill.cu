@@ -38,6 +38,7 @@ cudaError_t launch_attend_prefill(const AttendArgs &a, cudaStream_t st) {
     case KVQ_ASYM4_G32: return launch_pair<KVQ_ASYM4_G32, KVQ_ASYM4_G32>(a, st);
     case KVQ_Q8_0: return launch_pair<KVQ_Q8_0, KVQ_Q8_0>(a, st);
     case KVQ_Q4_0: return launch_pair<KVQ_Q4_0, KVQ_Q4_0>(a, st);
+    case KVQ_Q6_0: return launch_pair<KVQ_Q6_0, KVQ_Q6_0>(a, st);
     default: return cudaErrorNotSupported;
   }
 }

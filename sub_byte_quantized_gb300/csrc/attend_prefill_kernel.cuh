@@ -63,12 +63,12 @@ constexpr int kWinPitch = kD * 4 + 16;
 template <int PL>
 struct PlaneL {
   static constexpr bool HAD = is_hadamard(PL), ASYM = PL == KVQ_ASYM4_G32;
-  static constexpr int BITS = PL == KVQ_Q8_0 ? 8 : (PL == KVQ_HAD_INT2 ? 2 : 4);
+  static constexpr int BITS = PL == KVQ_Q8_0 ? 8 : (PL == KVQ_HAD_INT2 ? 2 : (PL == KVQ_Q6_0 ? 6 : 4));
   static constexpr int RB = kD * BITS / 8;               // payload bytes per token row
   static constexpr int SCB = HAD ? 4 : 8;                // scale bytes per token (f32 / 4 x f16)
   static constexpr int ZB = ASYM ? 8 : 0;                // zero-point bytes per token (4 x f16)
   static constexpr int PPR = RB / 16;                    // 16-byte pieces per row
-  static constexpr int CPP = 16 / PPR;                   // 8-value chunks per piece
+  static constexpr int CPP = 16 / PPR;                   // 8-value chunks per piece (not used for 6-bit rows)
   static constexpr int PPT = kStage * PPR / (kWarps * 32);   // pieces per thread per stage
   static_assert(PPT >= 1 && PPT * kWarps * 32 == kStage * PPR, "whole pieces per thread");
 };
@@ -126,6 +126,39 @@ __device__ __forceinline__ uint32_t toff(int row, int chunk) {
 template <int PL>
 __device__ __forceinline__ void unpack_plane(const uint8_t *pay, const uint8_t *sc, uint32_t tile) {
   using P = PlaneL<PL>;
+  if constexpr (P::BITS == 6) {
+    // Q6_0: each thread takes two (row, 32-value block) units; a block is 16 low-plane bytes then
+    // 8 high-plane bytes (24-byte blocks: 8-byte reads). Chunk k of the block (values 8k .. 8k+7)
+    // is low-plane word k plus high-plane bytes 2k, 2k+1. In one store instruction a warp covers 8
+    // rows x chunks (k, 4+k, 8+k, 12+k): the tile swizzle keeps each 8-lane phase conflict-free.
+#pragma unroll
+    for (int k2 = 0; k2 < 2; ++k2) {
+      const int u = threadIdx.x + kWarps * 32 * k2;
+      const int row = u >> 2, blk = u & 3;
+      const uint8_t *bp = pay + row * P::RB + 24 * blk;
+      const uint2 l0 = *reinterpret_cast<const uint2 *>(bp), l1 = *reinterpret_cast<const uint2 *>(bp + 8);
+      const uint2 hh = *reinterpret_cast<const uint2 *>(bp + 16);
+      const uint32_t lw[4] = {l0.x, l0.y, l1.x, l1.y};
+      const uint32_t s2 = 0x00010001u * *reinterpret_cast<const uint16_t *>(sc + row * 8 + 2 * blk);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t o[4];
+        unpack8_s6(lw[k], ((k < 2) ? hh.x : hh.y) >> (16 * (k & 1)), o);
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          hi[x] = hmul2(o[x], s2);                                         // rn(c s)
+          lo[x] = hfma2(o[x], s2, hi[x] ^ 0x80008000u);                    // c s - rn(c s), exact
+        }
+        const uint32_t off = toff(row, 4 * blk + k);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(tile + off),
+                     "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(tile + 2 * kTile + off),
+                     "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < P::PPT; ++k) {
     const int u = threadIdx.x + kWarps * 32 * k;          // piece: row u / PPR, 16-byte column u % PPR

@@ -36,9 +36,9 @@ __host__ __device__ constexpr bool uses_mma4(int layout) { return layout == KVQ_
 // Tensor-core phase 1 for Q6_0: resident CTAs (of eight warps) per SM (shared-memory ring of three
 // 64-token stages plus the score exchange: 92 KB at D = 256, 53 KB at D = 128).
 __host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 : 2; }
-// Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, at most four query rows per
-// kv head (gqa * n_q).
-__host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows <= 4; }
+// Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, any rows per kv head (gqa * n_q)
+// in groups of four.
+__host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows >= 1; }
 // tcgen05 kernel for the body of many-row Hadamard calls (causal prefill chunks): 128 query rows per
 // CTA, one CTA per SM; one Hadamard layout in both planes, head_dim 128, more than 64 rows per kv head.
 constexpr int kTcRows = 128;
@@ -52,17 +52,19 @@ constexpr int kPrefillCtasPerSm = 3;
 #ifndef KVQ_PREFILL_BLOCK_LAYOUTS
 #define KVQ_PREFILL_BLOCK_LAYOUTS 1
 #endif
-// (K layout, V layout) pairs the row-side kernel is built for: one layout of Q4_0, asym, Q8_0,
+// (K layout, V layout) pairs the row-side kernel is built for: one layout of Q4_0, asym, Q6_0, Q8_0,
 // Hadamard int4 / int2 in both planes, or the mixed pairs 4-bit keys + Q8_0 values and int2 key
 // body + int4 value body.
 __host__ __device__ constexpr bool prefill_pair(int kl, int vl) {
   return (kl == vl && (kl == KVQ_HAD_INT4 || kl == KVQ_HAD_INT2 || kl == KVQ_Q8_0 ||
-                       (KVQ_PREFILL_BLOCK_LAYOUTS && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32)))) ||
+                       (KVQ_PREFILL_BLOCK_LAYOUTS && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32 || kl == KVQ_Q6_0)))) ||
          (vl == KVQ_Q8_0 && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32)) || (kl == KVQ_HAD_INT2 && vl == KVQ_HAD_INT4);
 }
-// Pairs with a decode kernel of their own (at most eight query rows per kv head).
+// Pairs with a decode kernel of their own (at most eight query rows per kv head; Q6_0: its kernel
+// takes groups of four rows).
 __host__ __device__ constexpr bool decode_kernel(int kl, int vl) {
-  return (kl == vl && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32 || kl == KVQ_HAD_INT4 || kl == KVQ_Q8_0)) ||
+  return (kl == vl && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32 || kl == KVQ_HAD_INT4 || kl == KVQ_Q8_0 ||
+                       kl == KVQ_Q6_0)) ||
          (kl == KVQ_Q4_0 && vl == KVQ_Q8_0);
 }
 // The row-side kernel takes many query rows per kv head, and every row count of the pairs that

@@ -175,5 +175,20 @@ __device__ __forceinline__ void unpack8_s2(uint32_t h, uint32_t (&o)[4]) {
   for (int i = 0; i < 4; ++i) o[i] = hadd2(lop3<0x6A>(x >> (2 * i), 0x00030003u, 0x64026402u), 0xE402E402u);
 }
 
+// Signed 6-bit codes of one 8-value chunk of a Q6_0 block: `lo` = the low-plane word (value i's
+// low four bits at bits 4i), `h16` = the two high-plane bytes (value i's top two bits at bits 2i)
+// -> four exact f16 pairs (c0,c4), (c1,c5), (c2,c6), (c3,c7) of the codes (v ^ 0x20) - 0x20. The
+// low nibble goes under the exponent of 1024 with bit 5 set, the high field is XORed into bits
+// 4-5 (so the f16 holds 1024 + (v ^ 0x20)), and one f16 add removes 1056.
+__device__ __forceinline__ void unpack8_s6(uint32_t lo, uint32_t h16, uint32_t (&o)[4]) {
+  const uint32_t x = prmt(h16, 0u, 0x4140u);           // values 0-3 -> low lane, 4-7 -> high lane
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t t = lop3<0x6A>(lo >> (4 * k), 0x000F000Fu, 0x64206420u);   // (a & b) ^ c
+    const uint32_t xs = k < 3 ? x << (4 - 2 * k) : x >> 2;
+    o[k] = hadd2(lop3<0x6A>(xs, 0x00300030u, t), 0xE420E420u);
+  }
+}
+
 }  // namespace mma
 }  // namespace kvq

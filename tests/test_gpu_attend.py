@@ -93,6 +93,21 @@ def test_q6_tensor_core_rows(D, gqa, n_q, causal, q_dtype):
     run_case(w, kv_len=1001, n_q=n_q, chunk=192, q_dtype=q_dtype, fill=937)
 
 
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("gqa,n_q,q_dtype,chunk", [
+    (2, 8, None, 192),        # 16 rows per kv head
+    (2, 32, "f32", 0),        # 64 rows, automatic chunk
+    (2, 100, "f16", 128),     # 200 rows: ragged last group / row block
+    (1, 200, None, 0),        # 200 rows of one query head
+])
+def test_q6_tensor_core_many_rows(D, gqa, n_q, q_dtype, chunk):
+    """Q6_0 with many causal query rows per kv head (a prefill chunk appended after 700 cached
+    tokens) on the tensor cores, head_dim 128 and 256, against the oracle."""
+    w = WORKLOADS["c4_q6_0_gemma"].scaled(head_dim=D, batch=2, n_kv_heads=2, n_q_heads=2 * gqa, causal=True)
+    kv_len = 700 + n_q
+    run_case(w, kv_len=kv_len, n_q=n_q, chunk=chunk, q_dtype=q_dtype, fill=700)
+
+
 @pytest.mark.parametrize("gqa,n_q,causal,n_recent,q_dtype,chunk", [
     (2, 5, True, 8, None, 64),        # ten rows: just past the decode kernel's eight
     (1, 16, True, 0, "f32", 128),     # no window
