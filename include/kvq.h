@@ -338,7 +338,8 @@ kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const vo
  *                 (and seq_lens); the caller owns it, the call must not share it with another
  *                 call in flight.
  * The call copies the inputs host -> device on `stream` (cudaMemcpyAsync; page-locked host
- * memory makes the copies asynchronous, pageable memory works but the driver stages it), enqueues
+ * memory makes the copies asynchronous, pageable memory works but the driver stages it; when
+ * k_new, v_new and q lie back to back in that order in host memory, one copy moves all three), enqueues
  * the same launches as the device-buffer call (identical results and stored bytes), copies the
  * output back and returns after cudaStreamSynchronize(stream), with `out` filled. Every argument
  * is validated before anything is enqueued; a CUDA error from a copy, a launch or the

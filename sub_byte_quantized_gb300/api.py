@@ -456,7 +456,8 @@ def append_decode_attend_host(cache: KVCache, k_new: torch.Tensor, v_new: torch.
         raise ValueError("k_new/q shape does not match the cache")
     if attn_scale is None:
         attn_scale = 1.0 / math.sqrt(D)
-    need = append_decode_attend_host_workspace_bytes(cache, k_new.dtype, n_new, q.dtype, Hq, n_q, kv_len, chunk)
+    need = 0 if workspace is not None else \
+        append_decode_attend_host_workspace_bytes(cache, k_new.dtype, n_new, q.dtype, Hq, n_q, kv_len, chunk)
     out, workspace = _host_out_ws(q, cache.planes["k"]["payload"].device, need, out, workspace)
     L.check(L.lib().kvq_append_decode_attend_host(
         C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, pos0, q.data_ptr(),
@@ -491,8 +492,8 @@ def paged_append_decode_attend_host(cache: PagedKVCache, k_new: torch.Tensor, v_
         raise ValueError("k_new/q shape does not match the cache")
     if attn_scale is None:
         attn_scale = 1.0 / math.sqrt(D)
-    need = paged_append_decode_attend_host_workspace_bytes(cache, k_new.dtype, n_new, q.dtype, Hq, n_q, max_kv_len,
-                                                           chunk)
+    need = 0 if workspace is not None else \
+        paged_append_decode_attend_host_workspace_bytes(cache, k_new.dtype, n_new, q.dtype, Hq, n_q, max_kv_len, chunk)
     out, workspace = _host_out_ws(q, cache.planes["k"]["payload"].device, need, out, workspace)
     L.check(L.lib().kvq_paged_append_decode_attend_host(
         C.byref(cache.struct), k_new.data_ptr(), v_new.data_ptr(), _DTYPES[k_new.dtype], n_new, q.data_ptr(),

@@ -458,9 +458,11 @@ HostStaging host_staging(size_t attend_need, int batch, int n_kv_heads, int head
   h.q_bytes = (size_t)batch * n_q_heads * n_q * head_dim * dtype_bytes(q_dtype);
   h.out_bytes = (size_t)batch * n_q_heads * n_q * head_dim * sizeof(float);
   h.lens_bytes = paged ? (size_t)batch * sizeof(int32_t) : 0;
+  // k_new, v_new and q back to back (each size is a multiple of 256 bytes: head_dim 128 or 256), so
+  // host inputs that are back to back too arrive with one copy
   h.k = round_up(attend_need, 256);
-  h.v = h.k + round_up(h.kv_bytes, 256);
-  h.q = h.v + round_up(h.kv_bytes, 256);
+  h.v = h.k + h.kv_bytes;
+  h.q = h.v + h.kv_bytes;
   h.out = h.q + round_up(h.q_bytes, 256);
   h.lens = h.out + round_up(h.out_bytes, 256);
   h.total = h.lens + round_up(h.lens_bytes, 256);
@@ -489,11 +491,15 @@ kvq_status check_host_args(int kv_dtype, int n_new, int q_dtype, const void *k_n
 cudaError_t copy_in(const HostStaging &h, char *ws, const void *k_new, const void *v_new, const void *q,
                     const void *seq_lens, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
-  if (h.kv_bytes) {
+  const char *kb = static_cast<const char *>(k_new), *vb = static_cast<const char *>(v_new);
+  if (h.kv_bytes && vb == kb + h.kv_bytes && static_cast<const char *>(q) == vb + h.kv_bytes) {
+    e = cudaMemcpyAsync(ws + h.k, k_new, 2 * h.kv_bytes + h.q_bytes, cudaMemcpyDefault, s);   // one copy
+  } else if (h.kv_bytes) {
     e = cudaMemcpyAsync(ws + h.k, k_new, h.kv_bytes, cudaMemcpyDefault, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(ws + h.v, v_new, h.kv_bytes, cudaMemcpyDefault, s);
   }
-  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + h.q, q, h.q_bytes, cudaMemcpyDefault, s);
+  if (e == cudaSuccess && !(h.kv_bytes && vb == kb + h.kv_bytes && static_cast<const char *>(q) == vb + h.kv_bytes))
+    e = cudaMemcpyAsync(ws + h.q, q, h.q_bytes, cudaMemcpyDefault, s);
   if (e == cudaSuccess && h.lens_bytes) e = cudaMemcpyAsync(ws + h.lens, seq_lens, h.lens_bytes, cudaMemcpyDefault, s);
   return e;
 }

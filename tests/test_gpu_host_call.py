@@ -44,6 +44,34 @@ def test_host_call_matches_device_call(layout, n_recent, pinned):
     check_close(got.numpy(), r[0] if isinstance(r, tuple) else r, f"host call {layout}")
 
 
+@pytest.mark.parametrize("layout", ["q4_0", "had_int4"])
+def test_host_call_back_to_back_inputs(layout):
+    """k_new, v_new and q as consecutive views of one pinned allocation (the call then moves them with
+    one copy): the same result and stored bytes as the device-buffer call, twice in a row with
+    different inputs in the same buffer."""
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=2, n_kv_heads=2, n_q_heads=8,
+                                              n_recent=16 if layout == "had_int4" else 0)
+    inp = make_inputs(w, kv_len=600, n_q=1)
+    S = inp["k"].shape[2]
+    n_new = 2
+    fill = S - n_new
+    dc, oc, d = fill_both(w, inp, fill=fill)
+    dc2, _, _ = fill_both(w, inp, fill=fill)
+    kn, vn, q = d["k"][:, :, fill:].contiguous(), d["v"][:, :, fill:].contiguous(), d["q"]
+    n_k = kn.numel()
+    packed = torch.empty(2 * n_k + q.numel(), dtype=kn.dtype).pin_memory()
+    hk, hv, hq = packed[:n_k].view(kn.shape), packed[n_k:2 * n_k].view(vn.shape), packed[2 * n_k:].view(q.shape)
+    for qq in (q, torch.flip(q, dims=[1]).contiguous()):
+        hk.copy_(kn.cpu())
+        hv.copy_(vn.cpu())
+        hq.copy_(qq.cpu())
+        ref = kvq.append_decode_attend(dc, kn, vn, fill, qq, S, attn_scale=w.alpha)
+        got = kvq.append_decode_attend_host(dc2, hk, hv, fill, hq, S, attn_scale=w.alpha)
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref.cpu())
+        _planes_equal(dc, dc2)
+
+
 def test_host_call_causal_rows_and_no_append():
     """Several causal query rows, and n_new == 0 (a plain attention through the host call)."""
     w = WORKLOADS["c3_had_int4_prefill"].scaled(layout="q4_0", batch=1, n_kv_heads=2, n_q_heads=4, n_recent=0)
