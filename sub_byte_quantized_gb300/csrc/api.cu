@@ -180,7 +180,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
     // row-side kernel in its decode form (one row block, the warps split the tokens): one chunk per
     // resident CTA, as many chunks per (batch, kv head) as fit one wave
     const long long ctas = (long long)sms * (kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2);
-    long long per_head = ctas / (n_heads > 0 ? n_heads : 1) - n_wchunks;   // the window's CTAs share the wave
+    long long per_head = ctas / (n_heads > 0 ? n_heads : 1);   // (the window is scored in phase 2)
     if (per_head < 1) per_head = 1;
     const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
     chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
@@ -409,7 +409,10 @@ kvq_status prepare_attend(const kvq_cache *cache, const void *q, int32_t q_dtype
 cudaError_t launch_attend_sequence(kvq::AttendArgs &a, cudaStream_t s, bool events) {
   cudaError_t e = cudaSuccess;
   const bool mma = kvq::mma_supported(a);
-  a.win_in_reduce = mma && a.n_win > 0 && !kvq::prefill_supported(a);   // the decode tensor-core kernels cover the body chunks only
+  // the decode tensor-core kernels (and the row-side kernel's decode form) cover the body chunks only
+  a.win_in_reduce = mma && a.n_win > 0 &&
+                    (!kvq::prefill_supported(a) ||
+                     kvq::dec_shape(a.cache.layout, a.cache.v_layout, a.cache.D, a.gqa * a.n_q));
   // the tensor-core kernels prepare the Hadamard query themselves; the CUDA-core one reads it
   if (kvq::is_hadamard(a.cache.layout) && !mma) {
     a.fresh_lo = 0;                                      // its predecessor is then the prep kernel
@@ -645,7 +648,7 @@ void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_p
     ctas_per_sm = kvq::is_hadamard(c.layout) ? kvq::kPrefillCtasPerSm : 2;
     const bool dec = rows <= 16 && !kvq::decode_kernel(c.layout, c.v_layout);
     ctas_per_unit = dec ? 1 : (rows + kvq::kPrefillRows - 1) / kvq::kPrefillRows;
-    window_ctas = kvq::is_hadamard(c.layout);            // the row-side kernel scores the window chunks
+    window_ctas = kvq::is_hadamard(c.layout) && !dec;    // the row-side kernel scores the window chunks
   } else if (c.layout == c.v_layout && kvq::uses_mma4(c.layout)) {
     ctas_per_sm = kvq::kMma4CtasPerSm;
   } else {

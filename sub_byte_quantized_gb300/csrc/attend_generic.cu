@@ -254,6 +254,13 @@ __global__ void __launch_bounds__(kThreads) attend_generic_kernel(AttendArgs a) 
 // Hadamard query preparation: one warp per query row.
 template <int V>
 __global__ void __launch_bounds__(256) had_prep_kernel(AttendArgs a, int rows, bool write_rot) {
+  // It reads only the query: it may run alongside the preceding kernel (this call's append), except
+  // its first CTA, which waits for it, so that the grid completes after it and a kernel waiting on
+  // this grid also sees the append. Its consumers wait for it in every CTA.
+#if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
+  asm volatile("griddepcontrol.launch_dependents;");
+#endif
+  pdl_wait_if(false);
   const int lane = threadIdx.x & 31;
   const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (r >= rows) return;
@@ -345,9 +352,17 @@ cudaError_t launch_attend_generic(const AttendArgs &a, cudaStream_t st) {
 cudaError_t launch_had_prep(const AttendArgs &a, cudaStream_t st, bool write_rot) {
   const int rows = a.cache.B * a.Hq * a.n_q;
   const unsigned blocks = (unsigned)(((size_t)rows * 32 + 255) / 256);
-  if (a.cache.D == 128) had_prep_kernel<4><<<blocks, 256, 0, st>>>(a, rows, write_rot);
-  else had_prep_kernel<8><<<blocks, 256, 0, st>>>(a, rows, write_rot);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return a.cache.D == 128 ? cudaLaunchKernelEx(&cfg, had_prep_kernel<4>, a, rows, write_rot)
+                          : cudaLaunchKernelEx(&cfg, had_prep_kernel<8>, a, rows, write_rot);
 }
 
 cudaError_t launch_debug_scores(const CacheView &c, const void *q, int q_dtype, int Hq, int n_q, int kv_len,

@@ -840,8 +840,9 @@ cudaError_t launch_t(const AttendArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int R = a.gqa * a.n_q;
   cudaLaunchConfig_t cfg = {};
-  // Hadamard: more chunk indices for the recent window (when present), kWinChunk tokens each
-  cfg.gridDim = dim3((R + kRows - 1) / kRows, a.n_chunks + (G::HAD ? a.n_wchunks : 0) - a.y_base, a.cache.B * a.cache.H);
+  // Hadamard: more chunk indices for the recent window (unless phase 2 scores it)
+  cfg.gridDim = dim3((R + kRows - 1) / kRows, a.n_chunks + (G::HAD && !a.win_in_reduce ? a.n_wchunks : 0) - a.y_base,
+                     a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kWarps * 32);
   cfg.dynamicSmemBytes = G::SMEM;
   cfg.stream = st;

@@ -54,6 +54,7 @@ constexpr int kRows = 128;              // query rows per CTA = TMEM lanes
 constexpr int kStage = 64;              // tokens per stage
 constexpr int kD = 128;
 constexpr int kRing = 3;                // raw stage slots
+constexpr int kTB = 3;                  // code tile buffers (the unpackers run up to two stages ahead)
 constexpr int kWCopy = 8, kWMma = 9, kWUnp = 10, kUnpThreads = 128;
 constexpr int kThreads = (kWUnp + 4) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -61,10 +62,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // Shared memory (bytes). Swizzled operand tiles start on 1 KB boundaries.
 constexpr int kSQ = 0;                          // Q codes f16: two 64-dim column blocks of [128][64]
-constexpr int kST = kSQ + 32768;                // two tile buffers of K (16 KB) + V (16 KB)
+constexpr int kST = kSQ + 32768;                // kTB tile buffers of K (16 KB) + V (16 KB)
 constexpr int kTileBuf = 32768;
-constexpr int kSTsc = kST + 2 * kTileBuf;       // two x (s_k[64], s_v[64]) f32
-constexpr int kSP = kSTsc + 1024;               // two P' buffers of hi [128][64] + lo [128][64] f16
+constexpr int kSTsc = kST + kTB * kTileBuf;     // kTB x (s_k[64], s_v[64]) f32
+constexpr int kSP = (kSTsc + kTB * 512 + 1023) / 1024 * 1024;   // two P' buffers of hi [128][64] + lo [128][64] f16
 constexpr int kPBuf = 32768;
 constexpr int kSRaw = kSP + 2 * kPBuf;          // raw ring
 template <int L>
@@ -74,13 +75,13 @@ struct RawGeo {
   static constexpr int SLOT = OFF_SV + 4 * kStage;
   static constexpr int RED = kSRaw + kRing * SLOT;           // row maxima [2 parities][2 halves][128], l [2][128]
   static constexpr int SVMAX = RED + 3072;                    // per tile buffer: the stage's largest s_v, two halves
-  static constexpr int BAR = SVMAX + 64;                      // mbarriers
+  static constexpr int BAR = SVMAX + 8 * kTB;                 // mbarriers
   static constexpr int SMEM = BAR + 256;
   static_assert(SMEM <= 227 * 1024, "fits one CTA per SM");
 };
 static_assert(kSP % 1024 == 0 && kST % 1024 == 0, "swizzled tiles on 1 KB boundaries");
 // mbarriers
-enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + 2, B_SF = B_TE + 2, B_PF = B_SF + 2,
+enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + kTB, B_SF = B_TE + kTB, B_PF = B_SF + 2,
        B_PVD = B_PF + 2, B_DR = B_PVD + 2, B_RED = B_DR + 1, N_BAR = B_RED + 12 };
 // B_RED: per TMEM lane quarter, the exchange between its two softmax warps: the row maxima of stage
 // j (two barriers, by the parity of j) and the final row sums (one).
@@ -203,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
       bar_init(bar + B_RAWF + i, 32);                   // the copy lanes' cp.async completions
       bar_init(bar + B_RAWE + i, kUnpThreads);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kTB; ++i) {
       bar_init(bar + B_TF + i, kUnpThreads);
       bar_init(bar + B_TE + i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       bar_init(bar + B_SF + i, 1);
       bar_init(bar + B_PF + i, 256);                    // the softmax threads
       bar_init(bar + B_PVD + i, 1);
@@ -271,9 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     // ---------------- unpack: raw slot -> tile buffer j & 1 (each thread 8 (row, 8-dim group) units per plane)
     const int ut = tid - kWUnp * 32;
     for (int j = 0; j < n_st && ok; ++j) {
-      const int slot = j % kRing, tb = j & 1;
+      const int slot = j % kRing, tb = j % kTB;
       ok = bar_wait(bar + B_RAWF + slot, (j / kRing) & 1);
-      if (ok && j >= 2) ok = bar_wait(bar + B_TE + tb, ((j - 2) >> 1) & 1);   // P'V of stage j - 2 done
+      if (ok && j >= kTB) ok = bar_wait(bar + B_TE + tb, ((j - kTB) / kTB) & 1);   // P'V of stage j - kTB done
       if (!ok) break;
       const uint8_t *raw = sm + kSRaw + slot * RG::SLOT;
       uint8_t *tk = sm + kST + tb * kTileBuf, *tv = tk + 16384;
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
         ok = ok && bar_wait(bar + B_PF + pb, (i >> 1) & 1);
         if (!ok) return;
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const uint32_t vt = smem_addr(sm + kST + (i & 1) * kTileBuf + 16384);
+        const uint32_t vt = smem_addr(sm + kST + (i % kTB) * kTileBuf + 16384);
         const uint32_t ph = smem_addr(sm + kSP + pb * kPBuf), pl = ph + 16384;
 #pragma unroll
         for (int ks = 0; ks < kStage / 16; ++ks) {
@@ -324,12 +327,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
           mma_f16(tmem + 128, sdesc(ph + 32 * ks, 16, 1024), db, id_o, (i > 0 || ks > 0) ? 1u : 0u);
           mma_f16(tmem + 128, sdesc(pl + 32 * ks, 16, 1024), db, id_o, 1u);
         }
-        mma_commit(bar + B_TE + (i & 1));               // tile buffer free
+        mma_commit(bar + B_TE + (i % kTB));             // tile buffer free
         mma_commit(bar + B_PVD + pb);                   // O holds stage i; P' buffer free
       };
+      // S of stage j goes to TMEM columns 64 (j & 1): S(j + 2) is issued after P'V(j), which waits
+      // for the softmax to finish with S(j)
       for (int j = 0; j < n_st && ok; ++j) {
-        const int tb = j & 1;
-        ok = bar_wait(bar + B_TF + tb, (j >> 1) & 1);
+        const int tb = j % kTB, sb = j & 1;
+        ok = bar_wait(bar + B_TF + tb, (j / kTB) & 1);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t kt = smem_addr(sm + kST + tb * kTileBuf);
@@ -337,9 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
         for (int kb = 0; kb < kD / 16; ++kb) {
           const uint64_t da = sdesc(smem_addr(sm + kSQ + (kb >> 2) * 16384) + 32 * (kb & 3), 16, 1024);
           const uint64_t db = sdesc(kt + (kb >> 2) * 8192 + 32 * (kb & 3), 16, 1024);
-          mma_f16(tmem + 64 * tb, da, db, id_s, kb > 0 ? 1u : 0u);
+          mma_f16(tmem + 64 * sb, da, db, id_s, kb > 0 ? 1u : 0u);
         }
-        mma_commit(bar + B_SF + tb);
+        mma_commit(bar + B_SF + sb);
         if (j >= 1) pv(j - 1);
       }
       if (ok) pv(n_st - 1);
@@ -359,13 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     uint64_t *xbar = bar + B_RED + 3 * q4;              // this quarter's exchange barriers
     float m = -INFINITY, l = 0.0f;
     for (int j = 0; j < n_st && ok; ++j) {
-      const int tb = j & 1, pb = j & 1, ts = t0 + j * kStage;
-      ok = __all_sync(0xffffffffu, bar_wait(bar + B_TF + tb, (j >> 1) & 1) && bar_wait(bar + B_SF + tb, (j >> 1) & 1));
+      const int tb = j % kTB, sb = j & 1, pb = j & 1, ts = t0 + j * kStage;
+      ok = __all_sync(0xffffffffu, bar_wait(bar + B_TF + tb, (j / kTB) & 1) && bar_wait(bar + B_SF + sb, (j >> 1) & 1));
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
       const float *tsc = reinterpret_cast<const float *>(sm + kSTsc + tb * 512);
       float s[32];
-      tm_ld32(tmem + lane_base + 64 * tb + 32 * h, s);
+      tm_ld32(tmem + lane_base + 64 * sb + 32 * h, s);
       const int tc0 = ts + 32 * h;                      // token of column 0 of this half
       if constexpr (CAP) {
         if (live) {
@@ -375,19 +380,31 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
         }
       }
       const bool edge = tc0 + 31 > lim || tc0 + 32 > t_end;
+      // this half's key scales as broadcast 16-byte loads (one shared-memory wavefront per four)
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        s[i] = s[i] * tsc[32 * h + i] * arow;
-        if (edge && !(tc0 + i <= lim && tc0 + i < t_end)) s[i] = -INFINITY;
+      for (int i = 0; i < 32; i += 4) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(tsc + 32 * h + i);
+        s[i] = s[i] * k4.x * arow;
+        s[i + 1] = s[i + 1] * k4.y * arow;
+        s[i + 2] = s[i + 2] * k4.z * arow;
+        s[i + 3] = s[i + 3] * k4.w * arow;
       }
-      float mh = s[0];
+      if (edge) {
 #pragma unroll
-      for (int i = 1; i < 32; ++i) mh = fmaxf(mh, s[i]);
-      red[(tb * 2 + h) * kRows + lr] = mh;
-      bar_arrive(xbar + tb);
-      ok = __all_sync(0xffffffffu, bar_wait(xbar + tb, (j >> 1) & 1));
+        for (int i = 0; i < 32; ++i)
+          if (!(tc0 + i <= lim && tc0 + i < t_end)) s[i] = -INFINITY;
+      }
+      float mx8[8];                                     // the maximum as a tree (independent chains)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + 4]);
+      const float mh = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+      red[(sb * 2 + h) * kRows + lr] = mh;
+      bar_arrive(xbar + sb);
+      ok = __all_sync(0xffffffffu, bar_wait(xbar + sb, (j >> 1) & 1));
       if (!ok) break;
-      const float mx = fmaxf(mh, red[(tb * 2 + (h ^ 1)) * kRows + lr]);   // the stage's row maximum
+      const float mx = fmaxf(mh, red[(sb * 2 + (h ^ 1)) * kRows + lr]);   // the stage's row maximum
       // tau: p * s_v < 2^15 for p <= 2^tau (svmax < 2^(e + 1))
       const float *svm = reinterpret_cast<const float *>(sm + RG::SVMAX) + 2 * tb;
       const float svmax = fmaxf(svm[0], svm[1]);
@@ -417,17 +434,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
         if (!ok) break;
       }
       // P' = p * s_v as exact f16 hi + lo, tokens 32 h + 8 k .. +7 -> one 16-byte chunk each
-      float sum = 0.0f;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};              // four independent partial sums
       uint8_t *pbase = sm + kSP + pb * kPBuf;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t hi[4], lo[4];
+        const float4 va = *reinterpret_cast<const float4 *>(tsc + 64 + 32 * h + 8 * k);   // value scales
+        const float4 vb = *reinterpret_cast<const float4 *>(tsc + 64 + 32 * h + 8 * k + 4);
+        const float svv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 8 * k + 2 * e;
           const float p0 = ex2(s[i] - mu), p1 = ex2(s[i + 1] - mu);
-          sum += p0 + p1;
-          const float q0 = p0 * tsc[64 + 32 * h + i], q1 = p1 * tsc[64 + 32 * h + i + 1];
+          sum4[e] += p0 + p1;
+          const float q0 = p0 * svv[2 * e], q1 = p1 * svv[2 * e + 1];
           hi[e] = pack_f16x2(q0, q1);
           const float2 hf = __half22float2(u32_as_h2(hi[e]));
           lo[e] = pack_f16x2(q0 - hf.x, q1 - hf.y);
@@ -436,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
         *reinterpret_cast<uint4 *>(pbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(pbase + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      l = l * corr + sum;
+      l = l * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m = m_new;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       asm volatile("tcgen05.fence::before_thread_sync;");

@@ -72,6 +72,11 @@ __host__ __device__ constexpr bool decode_kernel(int kl, int vl) {
 __host__ __device__ constexpr bool prefill_shape(int kl, int vl, int D, int rows) {
   return D == 128 && prefill_pair(kl, vl) && (rows > 8 || !decode_kernel(kl, vl));
 }
+// The row-side kernel's decode form (DEC: one block of at most 16 rows, the warps split the tokens).
+// Its Hadamard window is scored in phase 2, one CTA per query row, like the decode kernels'.
+__host__ __device__ constexpr bool dec_shape(int kl, int vl, int D, int rows) {
+  return prefill_shape(kl, vl, D, rows) && rows <= 16 && !decode_kernel(kl, vl);
+}
 
 // The opt-in dynamic shared-memory size of `kernel` is a per-device function attribute: set it
 // the first time the kernel is launched on each device. `done` is the caller's flag array (one
