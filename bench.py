@@ -113,7 +113,7 @@ def measured_peaks():
 PROFILES = {
     "c5_q4_0_llama70b_128k": ("attend_phase1_c5_q4_0_128k.md", "attend_mma.cu"),
     "c4_q6_0_gemma": ("attend_phase1_q6_0_c4_gemma.md", "attend_mma_q6.cu"),
-    "c3_had_int4_prefill": ("attend_prefill_c3_had_int4.md", "attend_prefill_kernel.cuh"),
+    "c3_had_int4_prefill": ("attend_prefill_tc_c3_had_int4.md", "attend_prefill_tc.cu"),
     "c5_q8_0_llama70b_128k": ("attend_phase1_q8_0_128k.md", "attend_mma.cu"),
     "c5_q4_0_k_q8_0_v_llama70b_128k": ("attend_phase1_q4_0_k_q8_0_v_128k.md", "attend_mma.cu"),
     "c3_had_int2_decode_w256": ("attend_prefill_dec_had_int2_w256.md", "attend_prefill_kernel.cuh"),
