@@ -7,7 +7,8 @@
 // One CTA = 128 query rows of one (batch, kv head) x one split-K chunk of body tokens. The rows are
 // the M side of both products, and the accumulators live in tensor memory (TMEM, 256 columns):
 //   S  = Q8 . K^T       M 128 x N 64 tokens x K 128 dims   -> TMEM columns 0-63 / 64-127 (two stages)
-//   O += P' . V         M 128 x N 128 dims x K 64 tokens   -> TMEM columns 128-255
+//   O += P' . V         M 128 x N 128 dims x K 64 tokens   -> TMEM columns 128-255, with P' (A) read
+//                                                            from TMEM columns 256-383 (two stages)
 // Q8 holds the int8 query codes and K, V the signed 2- or 4-bit codes, all exact in f16 (kind::f16,
 // f32 accumulate), so S is the exact integer dot (|dot| < 2^17). score = alpha * s_q * s_k * dot;
 // the per-token V scale is folded into the probabilities, P' = p * s_v, which go to the PV product
@@ -18,7 +19,8 @@
 //   warps 0-7   softmax: warp w serves TMEM lanes (query rows) 32 (w % 4) .. +31 and the column half
 //               w / 4 (S columns 32 h .. +31, O columns 64 h .. +63); the two halves of a row exchange
 //               their maxima through shared memory; online softmax in base 2 with a lazily moved
-//               reference maximum (below); P' hi/lo into shared memory (two buffers)
+//               reference maximum (below), the row's score factor folded into the exponent's fma;
+//               P' hi/lo into tensor memory (two stage buffers), the A operand of the PV product
 //   warp  8     copy: packed K/V rows and per-token scales of each 64-token stage -> a three-slot raw
 //               ring (16-byte cp.async, completion counted on the slot's mbarrier)
 //   warp  9     one lane issues the MMAs (S of stage j, then P'V of stage j - 1) and commits them to
@@ -27,7 +29,8 @@
 //               per-stage arrays
 // Operand layouts (shared-memory descriptors, 128-byte swizzle): Q [128 rows][128 dims] and K
 // [64 tokens][128 dims] K-major in two 64-dim column blocks; V [64 tokens][128 dims] read as the
-// MN-major B operand of the PV product; P' [128 rows][64 tokens] K-major. Within each 8-dim group
+// MN-major B operand of the PV product; P' in TMEM, lane = row, two tokens per 32-bit column (16
+// tokens = 8 columns per MMA k-step; the hi parts of a stage, then its lo parts). Within each 8-dim group
 // the tiles keep the unpacker's order (dims 0,4,1,5,2,6,3,7); the output columns follow it.
 //
 // Lazy rescaling: O and l are kept relative to a reference maximum m per row, which moves only when
@@ -56,6 +59,11 @@ constexpr int kD = 128;
 constexpr int kRing = 3;                // raw stage slots
 constexpr int kTB = 3;                  // code tile buffers (the unpackers run up to two stages ahead)
 constexpr int kWCopy = 8, kWMma = 9, kWUnp = 10, kUnpThreads = 128;
+// Tensor memory (columns of 32 bits, lane = query row): S of two stages at 0 and 64, O at 128,
+// P' of two stages at 256 and 320 (each: the f16 hi parts of 64 tokens in 32 columns, then the lo
+// parts), read by the PV product as its A operand.
+constexpr int kTmemCols = 512;
+constexpr int kTmemO = 128, kTmemP = 256;
 constexpr int kThreads = (kWUnp + 4) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -65,9 +73,7 @@ constexpr int kSQ = 0;                          // Q codes f16: two 64-dim colum
 constexpr int kST = kSQ + 32768;                // kTB tile buffers of K (16 KB) + V (16 KB)
 constexpr int kTileBuf = 32768;
 constexpr int kSTsc = kST + kTB * kTileBuf;     // kTB x (s_k[64], s_v[64]) f32
-constexpr int kSP = (kSTsc + kTB * 512 + 1023) / 1024 * 1024;   // two P' buffers of hi [128][64] + lo [128][64] f16
-constexpr int kPBuf = 32768;
-constexpr int kSRaw = kSP + 2 * kPBuf;          // raw ring
+constexpr int kSRaw = kSTsc + kTB * 512;       // raw ring
 template <int L>
 struct RawGeo {
   static constexpr int RB = L == KVQ_HAD_INT2 ? 32 : 64;     // payload bytes per token row
@@ -79,7 +85,7 @@ struct RawGeo {
   static constexpr int SMEM = BAR + 256;
   static_assert(SMEM <= 227 * 1024, "fits one CTA per SM");
 };
-static_assert(kSP % 1024 == 0 && kST % 1024 == 0, "swizzled tiles on 1 KB boundaries");
+static_assert(kST % 1024 == 0, "swizzled tiles on 1 KB boundaries");
 // mbarriers
 enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + kTB, B_SF = B_TE + kTB, B_PF = B_SF + 2,
        B_PVD = B_PF + 2, B_DR = B_PVD + 2, B_RED = B_DR + 1, N_BAR = B_RED + 12 };
@@ -130,6 +136,11 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t da, uint64_t d
   asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
                ::"r"(d_tmem), "l"(da), "l"(db), "r"(id), "r"(accumulate));
 }
+// The same with the A operand in tensor memory (lane = row, two f16 values per 32-bit column along K).
+__device__ __forceinline__ void mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t db, uint32_t id, uint32_t accumulate) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
+               ::"r"(d_tmem), "r"(a_tmem), "l"(db), "r"(id), "r"(accumulate));
+}
 // The mbarrier gets one arrival once every MMA this thread issued before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(b)));
@@ -169,6 +180,31 @@ __device__ __forceinline__ void tm_st32(uint32_t taddr, const float (&v)[32]) {
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
+}
+// 16 consecutive TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// A wait off the critical path (the copy and unpack roles run ahead of the tensor core): between
+// tries the warp sleeps, so that it does not take issue slots from the softmax warps.
+__device__ __forceinline__ bool bar_wait_relaxed(uint64_t *b, uint32_t parity) {
+  uint64_t start = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done = 0;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(smem_addr(b)), "r"(parity) : "memory");
+    if (done) return true;
+    __nanosleep(128);
+    if ((it & 63) == 63) {
+      const uint64_t now = global_ns();
+      if (start == 0) start = now;
+      else if (now - start > kWaitNs) return false;
+    }
+  }
 }
 // the tiles keep each 8-dim group in the unpacker's pair order: position p holds dim perm8(p)
 __host__ __device__ constexpr int perm8(int p) { return (p >> 1) + 4 * (p & 1); }
@@ -231,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     *reinterpret_cast<uint4 *>(sm + kSQ + (gi >> 3) * 16384 + sw128(lr, 16 * (gi & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (warp == kWMma) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_addr(&tmem_base)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
+                 "n"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> tensor-core reads
@@ -245,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     // ---------------- copy: stage j -> raw slot j % kRing; rows past t_end are zero-filled
     for (int j = 0; j < n_st && ok; ++j) {
       const int slot = j % kRing;
-      if (j >= kRing) ok = bar_wait(bar + B_RAWE + slot, ((j / kRing) - 1) & 1);
+      if (j >= kRing) ok = bar_wait_relaxed(bar + B_RAWE + slot, ((j / kRing) - 1) & 1);
       if (!ok) break;
       const int ts = t0 + j * kStage;
       const size_t r0 = cache_row_t<PAGED>(cv, bb, kvh, head_row0, ts);   // 64 consecutive plane rows
@@ -275,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     const int ut = tid - kWUnp * 32;
     for (int j = 0; j < n_st && ok; ++j) {
       const int slot = j % kRing, tb = j % kTB;
-      ok = bar_wait(bar + B_RAWF + slot, (j / kRing) & 1);
-      if (ok && j >= kTB) ok = bar_wait(bar + B_TE + tb, ((j - kTB) / kTB) & 1);   // P'V of stage j - kTB done
+      ok = bar_wait_relaxed(bar + B_RAWF + slot, (j / kRing) & 1);
+      if (ok && j >= kTB) ok = bar_wait_relaxed(bar + B_TE + tb, ((j - kTB) / kTB) & 1);   // P'V of stage j - kTB done
       if (!ok) break;
       const uint8_t *raw = sm + kSRaw + slot * RG::SLOT;
       uint8_t *tk = sm + kST + tb * kTileBuf, *tv = tk + 16384;
@@ -320,12 +357,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
         if (!ok) return;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t vt = smem_addr(sm + kST + (i % kTB) * kTileBuf + 16384);
-        const uint32_t ph = smem_addr(sm + kSP + pb * kPBuf), pl = ph + 16384;
 #pragma unroll
         for (int ks = 0; ks < kStage / 16; ++ks) {
           const uint64_t db = sdesc(vt + 2048 * ks, 8192, 1024);
-          mma_f16(tmem + 128, sdesc(ph + 32 * ks, 16, 1024), db, id_o, (i > 0 || ks > 0) ? 1u : 0u);
-          mma_f16(tmem + 128, sdesc(pl + 32 * ks, 16, 1024), db, id_o, 1u);
+          const uint32_t pa = tmem + kTmemP + 64 * pb + 8 * ks;   // 16 tokens = 8 columns
+          mma_f16_ta(tmem + kTmemO, pa, db, id_o, (i > 0 || ks > 0) ? 1u : 0u);
+          mma_f16_ta(tmem + kTmemO, pa + 32, db, id_o, 1u);
         }
         mma_commit(bar + B_TE + (i % kTB));             // tile buffer free
         mma_commit(bar + B_PVD + pb);                   // O holds stage i; P' buffer free
@@ -358,7 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     const bool live = r < R;
     const int lim = live ? row_limit(a, sl, r % a.n_q) : -1;
     const size_t qrow = live ? query_row_index(a, bb, kvh, r) : 0;
-    const float arow = live ? a.scale * a.s_q[qrow] * kLog2e : 0.0f;
+    // the row's score factor alpha * s_q * log2(e) (never 0, so that a masked -inf stays -inf in
+    // the exponent's fma; a zero factor only arises with all-zero query codes, whose dots are 0)
+    float arow = live ? a.scale * a.s_q[qrow] * kLog2e : 1.0f;
+    if (arow == 0.0f) arow = 1e-30f;
+    const bool fneg = arow < 0.0f;                      // the maximum of z * arow is then at the minimum z
+    const float fabs_row = fabsf(arow);
     if (CAP && live && chunk_id == 0 && h == 0) a.cap_sq[qrow] = a.s_q[qrow];
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     uint64_t *xbar = bar + B_RED + 3 * q4;              // this quarter's exchange barriers
@@ -381,25 +423,33 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
       }
       const bool edge = tc0 + 31 > lim || tc0 + 32 > t_end;
       // this half's key scales as broadcast 16-byte loads (one shared-memory wavefront per four)
+      // z = dot * s_k; the score in log2 units is z * arow, which enters the exponent as one fma
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 k4 = *reinterpret_cast<const float4 *>(tsc + 32 * h + i);
-        s[i] = s[i] * k4.x * arow;
-        s[i + 1] = s[i + 1] * k4.y * arow;
-        s[i + 2] = s[i + 2] * k4.z * arow;
-        s[i + 3] = s[i + 3] * k4.w * arow;
+        s[i] *= k4.x;
+        s[i + 1] *= k4.y;
+        s[i + 2] *= k4.z;
+        s[i + 3] *= k4.w;
       }
-      if (edge) {
+      if (edge) {                                       // a masked token's score must be -inf
+        const float zmask = fneg ? INFINITY : -INFINITY;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (!(tc0 + i <= lim && tc0 + i < t_end)) s[i] = -INFINITY;
+          if (!(tc0 + i <= lim && tc0 + i < t_end)) s[i] = zmask;
       }
-      float mx8[8];                                     // the maximum as a tree (independent chains)
+      float mx8[8];                                     // max of sign(arow) * z as a tree
+      if (!fneg) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(-s[i], -s[i + 8]), fmaxf(-s[i + 16], -s[i + 24]));
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + 4]);
-      const float mh = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+      const float ztop = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
+      const float mh = ztop == -INFINITY ? -INFINITY : fabs_row * ztop;   // this half's largest score
       red[(sb * 2 + h) * kRows + lr] = mh;
       bar_arrive(xbar + sb);
       ok = __all_sync(0xffffffffu, bar_wait(xbar + sb, (j >> 1) & 1));
@@ -422,10 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
 #pragma unroll
         for (int c = 0; c < 64; c += 32) {
           float o[32];
-          tm_ld32(tmem + lane_base + 128 + 64 * h + c, o);
+          tm_ld32(tmem + lane_base + kTmemO + 64 * h + c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tm_st32(tmem + lane_base + 128 + 64 * h + c, o);
+          tm_st32(tmem + lane_base + kTmemO + 64 * h + c, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
@@ -435,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
       }
       // P' = p * s_v as exact f16 hi + lo, tokens 32 h + 8 k .. +7 -> one 16-byte chunk each
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};              // four independent partial sums
-      uint8_t *pbase = sm + kSP + pb * kPBuf;
+      uint32_t hiv[16], lov[16];                        // P' of this half's 32 tokens (TMEM form)
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint32_t hi[4], lo[4];
@@ -445,21 +495,26 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 8 * k + 2 * e;
-          const float p0 = ex2(s[i] - mu), p1 = ex2(s[i + 1] - mu);
+          const float p0 = ex2(fmaf(s[i], arow, -mu)), p1 = ex2(fmaf(s[i + 1], arow, -mu));
           sum4[e] += p0 + p1;
           const float q0 = p0 * svv[2 * e], q1 = p1 * svv[2 * e + 1];
           hi[e] = pack_f16x2(q0, q1);
           const float2 hf = __half22float2(u32_as_h2(hi[e]));
           lo[e] = pack_f16x2(q0 - hf.x, q1 - hf.y);
         }
-        const uint32_t off = sw128(lr, 16 * (4 * h + k));
-        *reinterpret_cast<uint4 *>(pbase + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(pbase + 16384 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hiv[4 * k + e] = hi[e];
+          lov[4 * k + e] = lo[e];
+        }
       }
+      // tokens 32 h .. +31 are TMEM columns 16 h .. +15 of the hi half and of the lo half
+      tm_st16(tmem + lane_base + kTmemP + 64 * pb + 16 * h, hiv);
+      tm_st16(tmem + lane_base + kTmemP + 64 * pb + 32 + 16 * h, lov);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l = l * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m = m_new;
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      asm volatile("tcgen05.fence::before_thread_sync;");
+      asm volatile("tcgen05.fence::before_thread_sync;");   // the TMEM stores above precede the MMAs
       bar_arrive(bar + B_PF + pb);
     }
     if (ok) ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + ((n_st - 1) & 1), ((n_st - 1) >> 1) & 1));
@@ -478,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
         float o[32];
-        tm_ld32(tmem + lane_base + 128 + 64 * h + c, o);
+        tm_ld32(tmem + lane_base + kTmemO + 64 * h + c, o);
         if (write) {
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8) {              // position 8 g8 + p holds dim 8 g8 + perm8(p)
@@ -512,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
-  if (warp == kWMma) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+  if (warp == kWMma) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols));
 }
 
 template <int L, bool PAGED, bool CAP>
