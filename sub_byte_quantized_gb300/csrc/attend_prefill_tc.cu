@@ -92,37 +92,6 @@ enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + kTB, B_SF = B
 // B_RED: per TMEM lane quarter, the exchange between its two softmax warps: the row maxima of stage
 // j (two barriers, by the parity of j) and the final row sums (one).
 static_assert(N_BAR * 8 <= 256, "mbarriers fit");
-constexpr unsigned long long kWaitNs = 250ull * 1000 * 1000;   // give up on a wait after 250 ms
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void bar_init(uint64_t *b, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
-}
-__device__ __forceinline__ void bar_arrive(uint64_t *b) {
-  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_addr(b)) : "memory");
-}
-// Wait for the completion of the phase with the given parity; false if it has not completed
-// within kWaitNs. Each try suspends the warp for up to kSuspendNs unless the phase completes first,
-// so waiting warps do not take issue slots from working ones; the clock is read every 64 tries.
-constexpr uint32_t kSuspendNs = 20000;
-__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
-  uint64_t start = 0;
-  for (uint32_t it = 0;; ++it) {
-    uint32_t done = 0;
-    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
-                 : "=r"(done) : "r"(smem_addr(b)), "r"(parity), "r"(kSuspendNs) : "memory");
-    if (done) return true;
-    if ((it & 63) == 63) {
-      const uint64_t now = global_ns();
-      if (start == 0) start = now;
-      else if (now - start > kWaitNs) return false;
-    }
-  }
-}
 // Shared-memory matrix descriptor, 128-byte swizzle: start, leading and stride byte offsets.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
@@ -189,25 +158,8 @@ __device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t (&v)[16])
         "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
       : "memory");
 }
-// A wait off the critical path (the copy and unpack roles run ahead of the tensor core): between
-// tries the warp sleeps, so that it does not take issue slots from the softmax warps.
-__device__ __forceinline__ bool bar_wait_relaxed(uint64_t *b, uint32_t parity) {
-  uint64_t start = 0;
-  for (uint32_t it = 0;; ++it) {
-    uint32_t done = 0;
-    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
-                 : "=r"(done) : "r"(smem_addr(b)), "r"(parity) : "memory");
-    if (done) return true;
-    __nanosleep(128);
-    if ((it & 63) == 63) {
-      const uint64_t now = global_ns();
-      if (start == 0) start = now;
-      else if (now - start > kWaitNs) return false;
-    }
-  }
-}
-// the tiles keep each 8-dim group in the unpacker's pair order: position p holds dim perm8(p)
-__host__ __device__ constexpr int perm8(int p) { return (p >> 1) + 4 * (p & 1); }
+// The tiles keep each 8-dim group in the unpacker's pair order: position p of the group holds dim
+// perm8(p) = (p >> 1) + 4 (p & 1).
 
 template <int L, bool PAGED, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendArgs a) {

@@ -1,5 +1,6 @@
 // Inline PTX helpers shared by the tensor-core phase-1 kernels: cp.async staging, ldmatrix,
-// movmatrix, mma.sync m16n8k16 (f16 in, f32 accumulate), f16x2 arithmetic and lop3.
+// movmatrix, mma.sync m16n8k16 (f16 in, f32 accumulate), f16x2 arithmetic, lop3 and shared-memory
+// mbarriers with bounded waits.
 #pragma once
 
 #include <cstdint>
@@ -187,6 +188,57 @@ __device__ __forceinline__ void unpack8_s6(uint32_t lo, uint32_t h16, uint32_t (
     const uint32_t t = lop3<0x6A>(lo >> (4 * k), 0x000F000Fu, 0x64206420u);   // (a & b) ^ c
     const uint32_t xs = k < 3 ? x << (4 - 2 * k) : x >> 2;
     o[k] = hadd2(lop3<0x6A>(xs, 0x00300030u, t), 0xE420E420u);
+  }
+}
+
+// ---- mbarriers in shared memory with bounded waits (a wait that gives up returns false; the
+// caller then ends its work and reports the failure instead of hanging)
+constexpr unsigned long long kWaitNs = 250ull * 1000 * 1000;   // give up on a wait after 250 ms
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(uint64_t *b, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint64_t *b) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(smem_addr(b)) : "memory");
+}
+// Wait for the completion of the phase with the given parity; false if it has not completed
+// within kWaitNs. Each try suspends the warp for up to kSuspendNs unless the phase completes first,
+// so waiting warps do not take issue slots from working ones; the clock is read every 64 tries.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
+  uint64_t start = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done = 0;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(smem_addr(b)), "r"(parity), "r"(kSuspendNs) : "memory");
+    if (done) return true;
+    if ((it & 63) == 63) {
+      const uint64_t now = global_ns();
+      if (start == 0) start = now;
+      else if (now - start > kWaitNs) return false;
+    }
+  }
+}
+// A wait off the critical path (a role that runs ahead of the one it feeds): between tries the
+// warp sleeps, so that it does not take issue slots from the working warps.
+__device__ __forceinline__ bool bar_wait_relaxed(uint64_t *b, uint32_t parity) {
+  uint64_t start = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done = 0;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(done) : "r"(smem_addr(b)), "r"(parity) : "memory");
+    if (done) return true;
+    __nanosleep(128);
+    if ((it & 63) == 63) {
+      const uint64_t now = global_ns();
+      if (start == 0) start = now;
+      else if (now - start > kWaitNs) return false;
+    }
   }
 }
 
