@@ -53,24 +53,30 @@ namespace kvq {
 namespace {
 using namespace mma;
 
-constexpr int kRows = 128;              // query rows per CTA = TMEM lanes
+constexpr int kRows = 128;              // query rows per block = TMEM lanes
+constexpr int kBlk = 2;                 // row blocks per CTA, taking turns on the tensor core
+constexpr int kCtaRows = kBlk * kRows;
+static_assert(kCtaRows == kTcRows, "the chunk planner's rows per CTA");
 constexpr int kStage = 64;              // tokens per stage
 constexpr int kD = 128;
 constexpr int kRing = 3;                // raw stage slots
 constexpr int kTB = 3;                  // code tile buffers (the unpackers run up to two stages ahead)
-constexpr int kWCopy = 8, kWMma = 9, kWUnp = 10, kUnpThreads = 128;
-// Tensor memory (columns of 32 bits, lane = query row): S of two stages at 0 and 64, O at 128,
-// P' of two stages at 256 and 320 (each: the f16 hi parts of 64 tokens in 32 columns, then the lo
-// parts), read by the PV product as its A operand.
+constexpr int kWCopy = 8, kWMma = 9, kWUnp = 10, kUnpThreads = 64;
+// Tensor memory (columns of 32 bits, lane = query row of the block): per block b, S at 64 b, O at
+// 128 + 128 b, and P' at 384 + 64 b (the f16 hi parts of the stage's 64 tokens in 32 columns, then
+// the lo parts), read by the PV product as its A operand.
 constexpr int kTmemCols = 512;
-constexpr int kTmemO = 128, kTmemP = 256;
-constexpr int kThreads = (kWUnp + 4) * 32;
+__host__ __device__ constexpr uint32_t tm_s(int b) { return 64u * b; }
+__host__ __device__ constexpr uint32_t tm_o(int b) { return 128u + 128u * b; }
+__host__ __device__ constexpr uint32_t tm_p(int b) { return 384u + 64u * b; }
+constexpr int kThreads = kWUnp * 32 + kUnpThreads;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Shared memory (bytes). Swizzled operand tiles start on 1 KB boundaries.
-constexpr int kSQ = 0;                          // Q codes f16: two 64-dim column blocks of [128][64]
-constexpr int kST = kSQ + 32768;                // kTB tile buffers of K (16 KB) + V (16 KB)
+constexpr int kSQ = 0;                          // Q codes f16 per block: two 64-dim column blocks of [128][64]
+constexpr int kQBlk = 32768;
+constexpr int kST = kSQ + kBlk * kQBlk;         // kTB tile buffers of K (16 KB) + V (16 KB)
 constexpr int kTileBuf = 32768;
 constexpr int kSTsc = kST + kTB * kTileBuf;     // kTB x (s_k[64], s_v[64]) f32
 constexpr int kSRaw = kSTsc + kTB * 512;       // raw ring
@@ -79,18 +85,15 @@ struct RawGeo {
   static constexpr int RB = L == KVQ_HAD_INT2 ? 32 : 64;     // payload bytes per token row
   static constexpr int OFF_V = kStage * RB, OFF_SK = 2 * kStage * RB, OFF_SV = OFF_SK + 4 * kStage;
   static constexpr int SLOT = OFF_SV + 4 * kStage;
-  static constexpr int RED = kSRaw + kRing * SLOT;           // row maxima [2 parities][2 halves][128], l [2][128]
-  static constexpr int SVMAX = RED + 3072;                    // per tile buffer: the stage's largest s_v, two halves
+  static constexpr int SVMAX = kSRaw + kRing * SLOT;          // per tile buffer: the stage's largest s_v, two halves
   static constexpr int BAR = SVMAX + 8 * kTB;                 // mbarriers
   static constexpr int SMEM = BAR + 256;
   static_assert(SMEM <= 227 * 1024, "fits one CTA per SM");
 };
 static_assert(kST % 1024 == 0, "swizzled tiles on 1 KB boundaries");
-// mbarriers
-enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + kTB, B_SF = B_TE + kTB, B_PF = B_SF + 2,
-       B_PVD = B_PF + 2, B_DR = B_PVD + 2, B_RED = B_DR + 1, N_BAR = B_RED + 12 };
-// B_RED: per TMEM lane quarter, the exchange between its two softmax warps: the row maxima of stage
-// j (two barriers, by the parity of j) and the final row sums (one).
+// mbarriers (SF, PF, PVD: one per row block)
+enum { B_RAWF = 0, B_RAWE = kRing, B_TF = 2 * kRing, B_TE = B_TF + kTB, B_SF = B_TE + kTB, B_PF = B_SF + kBlk,
+       B_PVD = B_PF + kBlk, B_DR = B_PVD + kBlk, N_BAR = B_DR + 1 };
 static_assert(N_BAR * 8 <= 256, "mbarriers fit");
 // Shared-memory matrix descriptor, 128-byte swizzle: start, leading and stride byte offsets.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -172,19 +175,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the query codes come from the preceding kernel
 #endif
   uint64_t *bar = reinterpret_cast<uint64_t *>(sm + RG::BAR);
-  float *red = reinterpret_cast<float *>(sm + RG::RED);
   const CacheView &cv = a.cache;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row0 = blockIdx.x * kRows, chunk_id = blockIdx.y, bh = blockIdx.z;
+  const int row0 = blockIdx.x * kCtaRows, chunk_id = blockIdx.y, bh = blockIdx.z;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
   const SeqLen sl = seq_of_t<PAGED>(a, bb);
   const int R = a.gqa * a.n_q;
   const int t0 = chunk_id * sl.chunk, t1 = min(sl.n_body, t0 + sl.chunk);
   int w_lim = -1;
-  for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit(a, sl, r % a.n_q));
-  if (t0 > w_lim || t0 >= t1) return;                   // no row of this block sees the chunk
+  for (int r = row0; r < min(row0 + kCtaRows, R); ++r) w_lim = max(w_lim, row_limit(a, sl, r % a.n_q));
+  if (t0 > w_lim || t0 >= t1) return;                   // no row of this CTA sees the chunk
   const int t_end = min(t1, w_lim + 1);
   const int n_st = (t_end - t0 + kStage - 1) / kStage;
+  const int nblk = R - row0 > kRows ? 2 : 1;            // row blocks with live rows
   const size_t head_row0 = (size_t)bh * cv.cap;
 
   if (tid == 0) {
@@ -196,19 +199,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
       bar_init(bar + B_TF + i, kUnpThreads);
       bar_init(bar + B_TE + i, 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kBlk; ++i) {
       bar_init(bar + B_SF + i, 1);
-      bar_init(bar + B_PF + i, 256);                    // the softmax threads
+      bar_init(bar + B_PF + i, 128);                    // the block's softmax threads
       bar_init(bar + B_PVD + i, 1);
     }
     bar_init(bar + B_DR, 1);
-    for (int i = 0; i < 12; ++i) bar_init(bar + B_RED + i, 64);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // ---- query codes of the CTA's rows as exact f16 in the tiles' dim order: each unit is one
   // 8-dim group of one row (16 int8 -> one 16-byte store of four (dim i, dim i + 4) pairs)
-  for (int u = tid; u < kRows * 16; u += kThreads) {
-    const int lr = u >> 4, gi = u & 15, r = row0 + lr;
+  for (int u = tid; u < kCtaRows * 16; u += kThreads) {
+    const int cr = u >> 4, gi = u & 15, r = row0 + cr;
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     if (r < R) {
       const uint2 c8 = *reinterpret_cast<const uint2 *>(a.q8 + query_row_index(a, bb, kvh, r) * kD + 8 * gi);
@@ -216,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
 #pragma unroll
       for (int k = 0; k < 4; ++k) w[k] = pack_f16x2((float)cb[k], (float)cb[k + 4]);
     }
-    *reinterpret_cast<uint4 *>(sm + kSQ + (gi >> 3) * 16384 + sw128(lr, 16 * (gi & 7))) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(sm + kSQ + (cr >> 7) * kQBlk + (gi >> 3) * 16384 + sw128(cr & 127, 16 * (gi & 7))) =
+        make_uint4(w[0], w[1], w[2], w[3]);
   }
   if (warp == kWMma) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_base)),
@@ -260,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp >= kWUnp) {
-    // ---------------- unpack: raw slot -> tile buffer j & 1 (each thread 8 (row, 8-dim group) units per plane)
+    // ---------------- unpack: raw slot -> tile buffer j % kTB (each thread 16 (row, 8-dim group) units per plane)
     const int ut = tid - kWUnp * 32;
     for (int j = 0; j < n_st && ok; ++j) {
       const int slot = j % kRing, tb = j % kTB;
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
       const uint8_t *raw = sm + kSRaw + slot * RG::SLOT;
       uint8_t *tk = sm + kST + tb * kTileBuf, *tv = tk + 16384;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kStage * 16 / kUnpThreads; ++k) {
         const int u = ut + kUnpThreads * k;
         const int row = u >> 4, gi = u & 15;
         const uint32_t off = (uint32_t)(gi >> 3) * 8192 + sw128(row, 16 * (gi & 7));
@@ -287,63 +290,68 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
           *reinterpret_cast<uint4 *>(tv + off) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
-      // per-stage scales: s_k[0..63] then s_v[0..63] (consecutive in the raw slot); the two warps
-      // holding s_v also record its maximum (non-negative floats order like their bit patterns)
-      const float scv = *reinterpret_cast<const float *>(raw + RG::OFF_SK + 4 * ut);
-      reinterpret_cast<float *>(sm + kSTsc + tb * 512)[ut] = scv;
-      if (ut >= 64) {
-        const uint32_t mxv = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(scv, 0.0f)));
-        if (lane == 0) reinterpret_cast<uint32_t *>(sm + RG::SVMAX)[2 * tb + ((ut - 64) >> 5)] = mxv;
-      }
+      // per-stage scales: s_k[0..63], s_v[0..63]; each unpack warp also records the largest s_v of
+      // its 32 tokens (non-negative floats order like their bit patterns)
+      static_assert(kUnpThreads == kStage, "one key and one value scale per unpack thread");
+      const float sck = *reinterpret_cast<const float *>(raw + RG::OFF_SK + 4 * ut);
+      const float scv = *reinterpret_cast<const float *>(raw + RG::OFF_SV + 4 * ut);
+      reinterpret_cast<float *>(sm + kSTsc + tb * 512)[ut] = sck;
+      reinterpret_cast<float *>(sm + kSTsc + tb * 512)[64 + ut] = scv;
+      const uint32_t mxv = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(scv, 0.0f)));
+      if (lane == 0) reinterpret_cast<uint32_t *>(sm + RG::SVMAX)[2 * tb + (ut >> 5)] = mxv;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       bar_arrive(bar + B_RAWE + slot);
       bar_arrive(bar + B_TF + tb);
     }
   } else if (warp == kWMma) {
-    // ---------------- MMA issue (one thread): S of stage j, then P'V of stage j - 1
+    // ---------------- MMA issue (one thread). Per stage j and block b: P'V of stage j - 1 (once the
+    // block's softmax has stored its P'), then S of stage j into the same block's S columns, which
+    // that softmax has finished reading. The blocks take turns, so while one block's softmax works
+    // the tensor core serves the other.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc(kRows, kStage, false), id_o = idesc(kRows, kD, true);
-      auto pv = [&](int i) {
-        const int pb = i & 1;
-        ok = ok && bar_wait(bar + B_PF + pb, (i >> 1) & 1);
+      auto pv = [&](int b, int i) {
+        ok = ok && bar_wait(bar + B_PF + b, i & 1);
         if (!ok) return;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t vt = smem_addr(sm + kST + (i % kTB) * kTileBuf + 16384);
 #pragma unroll
         for (int ks = 0; ks < kStage / 16; ++ks) {
           const uint64_t db = sdesc(vt + 2048 * ks, 8192, 1024);
-          const uint32_t pa = tmem + kTmemP + 64 * pb + 8 * ks;   // 16 tokens = 8 columns
-          mma_f16_ta(tmem + kTmemO, pa, db, id_o, (i > 0 || ks > 0) ? 1u : 0u);
-          mma_f16_ta(tmem + kTmemO, pa + 32, db, id_o, 1u);
+          const uint32_t pa = tmem + tm_p(b) + 8 * ks;    // 16 tokens = 8 columns
+          mma_f16_ta(tmem + tm_o(b), pa, db, id_o, (i > 0 || ks > 0) ? 1u : 0u);
+          mma_f16_ta(tmem + tm_o(b), pa + 32, db, id_o, 1u);
         }
-        mma_commit(bar + B_TE + (i % kTB));             // tile buffer free
-        mma_commit(bar + B_PVD + pb);                   // O holds stage i; P' buffer free
+        mma_commit(bar + B_PVD + b);                    // O holds stage i; P' free
+        if (b == nblk - 1) mma_commit(bar + B_TE + (i % kTB));   // tile buffer free
       };
-      // S of stage j goes to TMEM columns 64 (j & 1): S(j + 2) is issued after P'V(j), which waits
-      // for the softmax to finish with S(j)
       for (int j = 0; j < n_st && ok; ++j) {
-        const int tb = j % kTB, sb = j & 1;
+        const int tb = j % kTB;
         ok = bar_wait(bar + B_TF + tb, (j / kTB) & 1);
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t kt = smem_addr(sm + kST + tb * kTileBuf);
+        for (int b = 0; b < nblk && ok; ++b) {
+          if (j >= 1) pv(b, j - 1);
+          if (!ok) break;
+          const uint32_t qt = smem_addr(sm + kSQ + b * kQBlk);
 #pragma unroll
-        for (int kb = 0; kb < kD / 16; ++kb) {
-          const uint64_t da = sdesc(smem_addr(sm + kSQ + (kb >> 2) * 16384) + 32 * (kb & 3), 16, 1024);
-          const uint64_t db = sdesc(kt + (kb >> 2) * 8192 + 32 * (kb & 3), 16, 1024);
-          mma_f16(tmem + 64 * sb, da, db, id_s, kb > 0 ? 1u : 0u);
+          for (int kb = 0; kb < kD / 16; ++kb) {
+            const uint64_t da = sdesc(qt + (kb >> 2) * 16384 + 32 * (kb & 3), 16, 1024);
+            const uint64_t db = sdesc(kt + (kb >> 2) * 8192 + 32 * (kb & 3), 16, 1024);
+            mma_f16(tmem + tm_s(b), da, db, id_s, kb > 0 ? 1u : 0u);
+          }
+          mma_commit(bar + B_SF + b);
         }
-        mma_commit(bar + B_SF + sb);
-        if (j >= 1) pv(j - 1);
       }
-      if (ok) pv(n_st - 1);
+      for (int b = 0; b < nblk && ok; ++b) pv(b, n_st - 1);
       mma_commit(bar + B_DR);                           // drain: every MMA issued above completes
       if (!bar_wait(bar + B_DR, 0)) ok = false;
     }
-  } else {
-    // ---------------- softmax: row lr = TMEM lane, column half h
-    const int q4 = warp & 3, h = warp >> 2;
-    const int lr = 32 * q4 + lane, r = row0 + lr;
+  } else if ((warp >> 2) < nblk) {
+    // ---------------- softmax: block b = warp / 4, row lr = TMEM lane, whole rows (64 scores per stage)
+    const int b = warp >> 2, q4 = warp & 3;
+    const int lr = 32 * q4 + lane, r = row0 + kRows * b + lr;
     const bool live = r < R;
     const int lim = live ? row_limit(a, sl, r % a.n_q) : -1;
     const size_t qrow = live ? query_row_index(a, bb, kvh, r) : 0;
@@ -353,60 +361,61 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
     if (arow == 0.0f) arow = 1e-30f;
     const bool fneg = arow < 0.0f;                      // the maximum of z * arow is then at the minimum z
     const float fabs_row = fabsf(arow);
-    if (CAP && live && chunk_id == 0 && h == 0) a.cap_sq[qrow] = a.s_q[qrow];
+    if (CAP && live && chunk_id == 0) a.cap_sq[qrow] = a.s_q[qrow];
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
-    uint64_t *xbar = bar + B_RED + 3 * q4;              // this quarter's exchange barriers
     float m = -INFINITY, l = 0.0f;
     for (int j = 0; j < n_st && ok; ++j) {
-      const int tb = j % kTB, sb = j & 1, pb = j & 1, ts = t0 + j * kStage;
-      ok = __all_sync(0xffffffffu, bar_wait(bar + B_TF + tb, (j / kTB) & 1) && bar_wait(bar + B_SF + sb, (j >> 1) & 1));
+      const int tb = j % kTB, ts = t0 + j * kStage;
+      ok = __all_sync(0xffffffffu, bar_wait(bar + B_TF + tb, (j / kTB) & 1) && bar_wait(bar + B_SF + b, j & 1));
       if (!ok) break;
       asm volatile("tcgen05.fence::after_thread_sync;");
       const float *tsc = reinterpret_cast<const float *>(sm + kSTsc + tb * 512);
-      float s[32];
-      tm_ld32(tmem + lane_base + 64 * sb + 32 * h, s);
-      const int tc0 = ts + 32 * h;                      // token of column 0 of this half
+      float s[64];
+      {
+        float h0[32], h1[32];
+        tm_ld32(tmem + lane_base + tm_s(b), h0);
+        tm_ld32(tmem + lane_base + tm_s(b) + 32, h1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          s[i] = h0[i];
+          s[32 + i] = h1[i];
+        }
+      }
       if constexpr (CAP) {
         if (live) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (tc0 + i < t_end) a.cap_scores[qrow * a.n_body + tc0 + i] = __float2int_rn(s[i]);
+          for (int i = 0; i < 64; ++i)
+            if (ts + i < t_end) a.cap_scores[qrow * a.n_body + ts + i] = __float2int_rn(s[i]);
         }
       }
-      const bool edge = tc0 + 31 > lim || tc0 + 32 > t_end;
-      // this half's key scales as broadcast 16-byte loads (one shared-memory wavefront per four)
-      // z = dot * s_k; the score in log2 units is z * arow, which enters the exponent as one fma
+      // z = dot * s_k (key scales as broadcast 16-byte loads); the score in log2 units is z * arow,
+      // which enters the exponent as one fma
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        const float4 k4 = *reinterpret_cast<const float4 *>(tsc + 32 * h + i);
+      for (int i = 0; i < 64; i += 4) {
+        const float4 k4 = *reinterpret_cast<const float4 *>(tsc + i);
         s[i] *= k4.x;
         s[i + 1] *= k4.y;
         s[i + 2] *= k4.z;
         s[i + 3] *= k4.w;
       }
-      if (edge) {                                       // a masked token's score must be -inf
+      if (ts + 63 > lim || ts + 64 > t_end) {           // a masked token's score must be -inf
         const float zmask = fneg ? INFINITY : -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (!(tc0 + i <= lim && tc0 + i < t_end)) s[i] = zmask;
+        for (int i = 0; i < 64; ++i)
+          if (!(ts + i <= lim && ts + i < t_end)) s[i] = zmask;
       }
-      float mx8[8];                                     // max of sign(arow) * z as a tree
+      float mx16[16];                                   // max of sign(arow) * z as a tree
       if (!fneg) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(s[i], s[i + 8]), fmaxf(s[i + 16], s[i + 24]));
+        for (int i = 0; i < 16; ++i) mx16[i] = fmaxf(fmaxf(s[i], s[i + 16]), fmaxf(s[i + 32], s[i + 48]));
       } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(fmaxf(-s[i], -s[i + 8]), fmaxf(-s[i + 16], -s[i + 24]));
+        for (int i = 0; i < 16; ++i) mx16[i] = fmaxf(fmaxf(-s[i], -s[i + 16]), fmaxf(-s[i + 32], -s[i + 48]));
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + 4]);
-      const float ztop = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3]));
-      const float mh = ztop == -INFINITY ? -INFINITY : fabs_row * ztop;   // this half's largest score
-      red[(sb * 2 + h) * kRows + lr] = mh;
-      bar_arrive(xbar + sb);
-      ok = __all_sync(0xffffffffu, bar_wait(xbar + sb, (j >> 1) & 1));
-      if (!ok) break;
-      const float mx = fmaxf(mh, red[(sb * 2 + (h ^ 1)) * kRows + lr]);   // the stage's row maximum
+      for (int i = 0; i < 4; ++i) mx16[i] = fmaxf(fmaxf(mx16[i], mx16[i + 4]), fmaxf(mx16[i + 8], mx16[i + 12]));
+      const float ztop = fmaxf(fmaxf(mx16[0], mx16[1]), fmaxf(mx16[2], mx16[3]));
+      const float mx = ztop == -INFINITY ? -INFINITY : fabs_row * ztop;   // the stage's row maximum
       // tau: p * s_v < 2^15 for p <= 2^tau (svmax < 2^(e + 1))
       const float *svm = reinterpret_cast<const float *>(sm + RG::SVMAX) + 2 * tb;
       const float svmax = fmaxf(svm[0], svm[1]);
@@ -416,76 +425,66 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
       const float m_new = bump ? mx : m;
       const float mu = m_new == -INFINITY ? 0.0f : m_new;
       const float corr = bump ? ex2(m - mu) : 1.0f;     // m = -inf -> 0
-      if (j >= 1 && __any_sync(0xffffffffu, bump && m != -INFINITY)) {
-        // O holds stages < j once P'V of stage j - 1 is done: rescale this half's 64 columns
-        ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + ((j - 1) & 1), ((j - 1) >> 1) & 1));
+      if (j >= 1) {
+        // P'V of stage j - 1 has read P' and updated O (it precedes S of stage j on the tensor core)
+        ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + b, (j - 1) & 1));
         if (!ok) break;
         asm volatile("tcgen05.fence::after_thread_sync;");
+        if (__any_sync(0xffffffffu, bump && m != -INFINITY)) {   // rescale the block's O rows
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
-          float o[32];
-          tm_ld32(tmem + lane_base + kTmemO + 64 * h + c, o);
+          for (int c = 0; c < kD; c += 32) {
+            float o[32];
+            tm_ld32(tmem + lane_base + tm_o(b) + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tm_st32(tmem + lane_base + kTmemO + 64 * h + c, o);
+            for (int i = 0; i < 32; ++i) o[i] *= corr;
+            tm_st32(tmem + lane_base + tm_o(b) + c, o);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      if (j >= 2) {                                     // P' buffer pb was read by P'V of stage j - 2
-        ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + pb, ((j - 2) >> 1) & 1));
-        if (!ok) break;
-      }
-      // P' = p * s_v as exact f16 hi + lo, tokens 32 h + 8 k .. +7 -> one 16-byte chunk each
+      // P' = p * s_v as exact f16 hi + lo, tokens 32 hh + 8 k .. +7, in two halves of 32 tokens
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};              // four independent partial sums
-      uint32_t hiv[16], lov[16];                        // P' of this half's 32 tokens (TMEM form)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t hi[4], lo[4];
-        const float4 va = *reinterpret_cast<const float4 *>(tsc + 64 + 32 * h + 8 * k);   // value scales
-        const float4 vb = *reinterpret_cast<const float4 *>(tsc + 64 + 32 * h + 8 * k + 4);
-        const float svv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t hiv[16], lov[16];                      // P' of this half's 32 tokens (TMEM form)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = 8 * k + 2 * e;
-          const float p0 = ex2(fmaf(s[i], arow, -mu)), p1 = ex2(fmaf(s[i + 1], arow, -mu));
-          sum4[e] += p0 + p1;
-          const float q0 = p0 * svv[2 * e], q1 = p1 * svv[2 * e + 1];
-          hi[e] = pack_f16x2(q0, q1);
-          const float2 hf = __half22float2(u32_as_h2(hi[e]));
-          lo[e] = pack_f16x2(q0 - hf.x, q1 - hf.y);
+        for (int k = 0; k < 4; ++k) {
+          const float4 va = *reinterpret_cast<const float4 *>(tsc + 64 + 32 * hh + 8 * k);   // value scales
+          const float4 vb = *reinterpret_cast<const float4 *>(tsc + 64 + 32 * hh + 8 * k + 4);
+          const float svv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const int i = 32 * hh + 8 * k + 2 * e2;
+            const float p0 = ex2(fmaf(s[i], arow, -mu)), p1 = ex2(fmaf(s[i + 1], arow, -mu));
+            sum4[e2] += p0 + p1;
+            const float q0 = p0 * svv[2 * e2], q1 = p1 * svv[2 * e2 + 1];
+            const uint32_t hi = pack_f16x2(q0, q1);
+            const float2 hf = __half22float2(u32_as_h2(hi));
+            hiv[4 * k + e2] = hi;
+            lov[4 * k + e2] = pack_f16x2(q0 - hf.x, q1 - hf.y);
+          }
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          hiv[4 * k + e] = hi[e];
-          lov[4 * k + e] = lo[e];
-        }
+        // tokens 32 hh .. +31 are TMEM columns 16 hh .. +15 of the hi half and of the lo half
+        tm_st16(tmem + lane_base + tm_p(b) + 16 * hh, hiv);
+        tm_st16(tmem + lane_base + tm_p(b) + 32 + 16 * hh, lov);
       }
-      // tokens 32 h .. +31 are TMEM columns 16 h .. +15 of the hi half and of the lo half
-      tm_st16(tmem + lane_base + kTmemP + 64 * pb + 16 * h, hiv);
-      tm_st16(tmem + lane_base + kTmemP + 64 * pb + 32 + 16 * h, lov);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       l = l * corr + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m = m_new;
       asm volatile("tcgen05.fence::before_thread_sync;");   // the TMEM stores above precede the MMAs
-      bar_arrive(bar + B_PF + pb);
+      bar_arrive(bar + B_PF + b);
     }
-    if (ok) ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + ((n_st - 1) & 1), ((n_st - 1) >> 1) & 1));
-    if (ok) {                                           // the row's l is the sum of its two halves
-      red[(4 + h) * kRows + lr] = l;
-      bar_arrive(xbar + 2);
-      ok = __all_sync(0xffffffffu, bar_wait(xbar + 2, 0));
-      l += red[(4 + (h ^ 1)) * kRows + lr];
-    }
+    if (ok) ok = __all_sync(0xffffffffu, bar_wait(bar + B_PVD + b, (n_st - 1) & 1));
     if (ok) {                                           // warp-uniform: the TMEM loads need the whole warp
       asm volatile("tcgen05.fence::after_thread_sync;");
       const bool write = live && t0 <= lim;
       const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
       const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
-      float *po = a.part_o + pi * kD + 64 * h;
+      float *po = a.part_o + pi * kD;
 #pragma unroll
-      for (int c = 0; c < 64; c += 32) {
+      for (int c = 0; c < kD; c += 32) {
         float o[32];
-        tm_ld32(tmem + lane_base + kTmemO + 64 * h + c, o);
+        tm_ld32(tmem + lane_base + tm_o(b) + c, o);
         if (write) {
 #pragma unroll
           for (int g8 = 0; g8 < 4; ++g8) {              // position 8 g8 + p holds dim 8 g8 + perm8(p)
@@ -495,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
           }
         }
       }
-      if (write && h == 0) {
+      if (write) {
         a.part_m[pi] = m * kLn2;                        // natural-log units, like the other kernels
         a.part_l[pi] = l;
       }
@@ -505,15 +504,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
   // the reduce turns into NaN outputs
   const bool failed = __syncthreads_or(!ok);
   if (failed && warp < 8) {
-    const int r = row0 + 32 * (warp & 3) + lane;
+    const int r = row0 + kRows * (warp >> 2) + 32 * (warp & 3) + lane;
     if (r < R && t0 <= row_limit(a, sl, r % a.n_q)) {
       const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
       const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
-      for (int d = 64 * (warp >> 2); d < 64 * (warp >> 2) + 64; ++d) a.part_o[pi * kD + d] = __int_as_float(0x7fc00000);
-      if (warp < 4) {
-        a.part_m[pi] = 0.0f;
-        a.part_l[pi] = __int_as_float(0x7fc00000);
-      }
+      for (int d = 0; d < kD; ++d) a.part_o[pi * kD + d] = __int_as_float(0x7fc00000);
+      a.part_m[pi] = 0.0f;
+      a.part_l[pi] = __int_as_float(0x7fc00000);
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
@@ -528,7 +525,7 @@ cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st) {
   cudaError_t e = set_smem_once(configured, attend_prefill_tc_kernel<L, PAGED, CAP>, RawGeo<L>::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.gqa * a.n_q + kRows - 1) / kRows, a.n_chunks, a.cache.B * a.cache.H);
+  cfg.gridDim = dim3((a.gqa * a.n_q + kCtaRows - 1) / kCtaRows, a.n_chunks, a.cache.B * a.cache.H);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = RawGeo<L>::SMEM;
   cfg.stream = st;

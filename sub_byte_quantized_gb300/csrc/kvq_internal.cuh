@@ -39,9 +39,10 @@ __host__ __device__ constexpr int kMmaQ6CtasPerSm(int D) { return D == 256 ? 2 :
 // Shapes the Q6_0 tensor-core kernel covers: head_dim 128 or 256, any rows per kv head (gqa * n_q)
 // in groups of four.
 __host__ __device__ constexpr bool mma_q6_shape(int D, int rows) { return (D == 128 || D == 256) && rows >= 1; }
-// tcgen05 kernel for the body of many-row Hadamard calls (causal prefill chunks): 128 query rows per
-// CTA, one CTA per SM; one Hadamard layout in both planes, head_dim 128, more than 64 rows per kv head.
-constexpr int kTcRows = 128;
+// tcgen05 kernel for the body of many-row Hadamard calls (causal prefill chunks): 256 query rows per
+// CTA (two blocks of 128), one CTA per SM; one Hadamard layout in both planes, head_dim 128, more than
+// 64 rows per kv head.
+constexpr int kTcRows = 256;
 __host__ __device__ constexpr bool tc_prefill_shape(int kl, int vl, int D, int rows) {
   return kl == vl && is_hadamard(kl) && D == 128 && rows > 64;
 }
