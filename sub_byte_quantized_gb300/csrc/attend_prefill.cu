@@ -13,14 +13,15 @@ bool prefill_supported(const AttendArgs &a) {
          a.chunk % kStage == 0;
 }
 
-// Many-row Hadamard calls: query preparation, the body chunks on the tcgen05 kernel, then the window
-// chunks (if any) on the row-side kernel. Launch chaining: the preparation waits for the preceding
-// kernel (a plain launch); every tcgen05 CTA waits for the preparation; the window launch's first CTA
-// waits for the tcgen05 grid, so phase 2 (which waits for the window launch) sees every partial.
+// Many-row Hadamard calls: the query preparation (int8 codes and scales, and the rotated f32 rows
+// when there is a window), then one tcgen05 grid for the body chunks and the window chunks. Launch
+// chaining: the preparation waits for the preceding kernel (a plain launch); every tcgen05 CTA waits
+// for the preparation. Score capture runs the window chunks on the row-side kernel afterwards (its
+// first CTA waits for the tcgen05 grid, and every CTA of a prepared-query window chunk waits).
 cudaError_t launch_prefill_tc(const AttendArgs &a, cudaStream_t st) {
   cudaError_t e = launch_had_prep(a, st, a.n_wchunks > 0);   // f32 rotated rows for the window chunks
   if (e == cudaSuccess) e = launch_attend_prefill_tc_body(a, st);
-  if (e != cudaSuccess || a.n_wchunks == 0) return e;
+  if (e != cudaSuccess || a.n_wchunks == 0 || !a.cap_scores) return e;
   AttendArgs w = a;
   w.y_base = a.n_chunks;                                 // window chunks only
   w.q_prepped = 1;

@@ -247,8 +247,10 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   int w_lim = -1;
   for (int r = row0; r < min(row0 + kRows, R); ++r) w_lim = max(w_lim, row_limit_of(a, sl, r));
   // rows appended by the preceding kernel (cache rows or window ring): only the CTAs that read
-  // them wait for it
-  pdl_wait_if(t0 <= w_lim && t0 < sl.fresh_hi && sl.fresh_lo < min(t1, w_lim + 1));
+  // them wait for it; a window chunk whose rotated query rows were prepared by an earlier launch
+  // always waits (the preceding grid's CTAs may have let it start before they waited for that
+  // preparation themselves)
+  pdl_wait_if((HAD && win && a.q_prepped) || (t0 <= w_lim && t0 < sl.fresh_hi && sl.fresh_lo < min(t1, w_lim + 1)));
   if (t0 > w_lim || t0 >= t1) return;                 // no row of this CTA sees the chunk
   const int t_end = min(t1, w_lim + 1);
   const int stage_len = win ? kWinStage : kStage;
@@ -387,17 +389,18 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
 
   if constexpr (HAD) {
   if (win) {
-    // =============== the recent window: exact f32 scores on the CUDA cores. Lane (g, c) scores
-    // rows g, g+8 against tokens 2c, 2c+1 of each 8-token stage and accumulates rows g, g+8 of
-    // dims 32b + 8c + 0..7 (Ow[b][j] = dims 32b + 8c + j and 32b + 8c + 4 + j)
+    // =============== the recent window on the tensor cores, accurate to f32: every f32 operand is
+    // split into tf32 hi + lo parts and each product takes three m16n8k8 MMAs (lo * hi, hi * lo,
+    // hi * hi; the dropped lo * lo term is below 2^-21 of the product). Per 8-token stage, warp w
+    // scores its rows 16 w + g and 16 w + g + 8 (g = lane / 4) against tokens 2c and 2c + 1
+    // (c = lane % 4), the layout of an m16n8 accumulator, and keeps O[16 rows][128 dims] in 16 of
+    // them: Ow[n] holds dims 8n + 2c, 8n + 2c + 1 of rows g (0, 1) and g + 8 (2, 3).
     const float walpha = a.scale * kLog2e;
-    float Ow[4][4][4];
+    float Ow[kD / 8][4];
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
+    for (int n = 0; n < kD / 8; ++n)
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) Ow[b][j][k] = 0.0f;
+      for (int k = 0; k < 4; ++k) Ow[n][k] = 0.0f;
     for (int i = 0; i < n_stages; ++i) {
       cp_async_wait<kRing - 2>();
       __syncthreads();
@@ -407,18 +410,26 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
       const uint8_t *sb = smem + (i % kRing) * G::SLOT;
       const float *qa = reinterpret_cast<const float *>(smem + G::OFF_QR + (16 * warp + g) * kQrPitch);
       const float *qb = reinterpret_cast<const float *>(smem + G::OFF_QR + (16 * warp + g + 8) * kQrPitch);
-      const float *ka = reinterpret_cast<const float *>(sb + (2 * c) * kWinPitch);
-      const float *kb = reinterpret_cast<const float *>(sb + (2 * c + 1) * kWinPitch);
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;     // (g, 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
-#pragma unroll 8
-      for (int d = 0; d < kD; d += 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(qa + d), y = *reinterpret_cast<const float4 *>(qb + d);
-        const float4 u = *reinterpret_cast<const float4 *>(ka + d), v = *reinterpret_cast<const float4 *>(kb + d);
-        s0 = fmaf(x.x, u.x, s0); s0 = fmaf(x.y, u.y, s0); s0 = fmaf(x.z, u.z, s0); s0 = fmaf(x.w, u.w, s0);
-        s1 = fmaf(x.x, v.x, s1); s1 = fmaf(x.y, v.y, s1); s1 = fmaf(x.z, v.z, s1); s1 = fmaf(x.w, v.w, s1);
-        s2 = fmaf(y.x, u.x, s2); s2 = fmaf(y.y, u.y, s2); s2 = fmaf(y.z, u.z, s2); s2 = fmaf(y.w, u.w, s2);
-        s3 = fmaf(y.x, v.x, s3); s3 = fmaf(y.y, v.y, s3); s3 = fmaf(y.z, v.z, s3); s3 = fmaf(y.w, v.w, s3);
+      const float *kr = reinterpret_cast<const float *>(sb + g * kWinPitch);   // token g: column g of K^T
+      // S = Q . K^T over the 16 8-dim k-steps; the three product terms in separate accumulators
+      float slh[4] = {0.f, 0.f, 0.f, 0.f}, shl[4] = {0.f, 0.f, 0.f, 0.f}, shh[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < kD / 8; ++ks) {
+        const int d0 = 8 * ks + c;
+        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+        split_tf32(qa[d0], ah[0], al[0]);
+        split_tf32(qb[d0], ah[1], al[1]);
+        split_tf32(qa[d0 + 4], ah[2], al[2]);
+        split_tf32(qb[d0 + 4], ah[3], al[3]);
+        split_tf32(kr[d0], bh0, bl0);
+        split_tf32(kr[d0 + 4], bh1, bl1);
+        mma1688_tf32(slh, al, bh0, bh1);
+        mma1688_tf32(shl, ah, bl0, bl1);
+        mma1688_tf32(shh, ah, bh0, bh1);
       }
+      // (g, 2c), (g, 2c+1), (g+8, 2c), (g+8, 2c+1)
+      float s0 = (slh[0] + shl[0]) + shh[0], s1 = (slh[1] + shl[1]) + shh[1];
+      float s2 = (slh[2] + shl[2]) + shh[2], s3 = (slh[3] + shl[3]) + shh[3];
       const int ta = ts + 2 * c, tb = ta + 1;
       s0 = (ta < t1 && ta <= lim_g) ? s0 * walpha : -INFINITY;
       s1 = (tb < t1 && tb <= lim_g) ? s1 * walpha : -INFINITY;
@@ -440,34 +451,27 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
       s3 = ex2(s3 - mu_g8);
       l_g = fmaf(l_g, corr_g, s0 + s1);
       l_g8 = fmaf(l_g8, corr_g8, s2 + s3);
+      // O += P . V: the probabilities are the A operand as they stand (k = c <-> token 2c,
+      // k = c + 4 <-> token 2c + 1), V's rows 2c and 2c + 1 the matching B entries
+      uint32_t ph[4], pl[4];
+      split_tf32(s0, ph[0], pl[0]);
+      split_tf32(s2, ph[1], pl[1]);
+      split_tf32(s1, ph[2], pl[2]);
+      split_tf32(s3, ph[3], pl[3]);
+      const float *va = reinterpret_cast<const float *>(sb + (kWinStage + 2 * c) * kWinPitch);
+      const float *vb = reinterpret_cast<const float *>(sb + (kWinStage + 2 * c + 1) * kWinPitch);
 #pragma unroll
-      for (int b = 0; b < 4; ++b)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          Ow[b][j][0] *= corr_g;
-          Ow[b][j][1] *= corr_g;
-          Ow[b][j][2] *= corr_g8;
-          Ow[b][j][3] *= corr_g8;
-        }
-#pragma unroll
-      for (int t = 0; t < kWinStage; ++t) {
-        const int src = (lane & ~3) | (t >> 1);          // lane (g, t / 2) holds token t's p
-        const float pg = __shfl_sync(0xffffffffu, (t & 1) ? s1 : s0, src);
-        const float pg8 = __shfl_sync(0xffffffffu, (t & 1) ? s3 : s2, src);
-        const float *vr = reinterpret_cast<const float *>(sb + (kWinStage + t) * kWinPitch) + 8 * c;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float4 v0 = *reinterpret_cast<const float4 *>(vr + 32 * b);
-          const float4 v1 = *reinterpret_cast<const float4 *>(vr + 32 * b + 4);
-          const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            Ow[b][j][0] = fmaf(pg, v[j], Ow[b][j][0]);
-            Ow[b][j][1] = fmaf(pg, v[4 + j], Ow[b][j][1]);
-            Ow[b][j][2] = fmaf(pg8, v[j], Ow[b][j][2]);
-            Ow[b][j][3] = fmaf(pg8, v[4 + j], Ow[b][j][3]);
-          }
-        }
+      for (int n = 0; n < kD / 8; ++n) {
+        Ow[n][0] *= corr_g;
+        Ow[n][1] *= corr_g;
+        Ow[n][2] *= corr_g8;
+        Ow[n][3] *= corr_g8;
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(va[8 * n + g], bh0, bl0);
+        split_tf32(vb[8 * n + g], bh1, bl1);
+        mma1688_tf32(Ow[n], pl, bh0, bh1);
+        mma1688_tf32(Ow[n], ph, bl0, bl1);
+        mma1688_tf32(Ow[n], ph, bh0, bh1);
       }
     }
     l_g += __shfl_xor_sync(0xffffffffu, l_g, 1);
@@ -483,12 +487,8 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
       const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + chunk_id;
       float *po = a.part_o + pi * kD;
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        *reinterpret_cast<float4 *>(po + 32 * b + 8 * c) =
-            make_float4(Ow[b][0][2 * half], Ow[b][1][2 * half], Ow[b][2][2 * half], Ow[b][3][2 * half]);
-        *reinterpret_cast<float4 *>(po + 32 * b + 8 * c + 4) =
-            make_float4(Ow[b][0][2 * half + 1], Ow[b][1][2 * half + 1], Ow[b][2][2 * half + 1], Ow[b][3][2 * half + 1]);
-      }
+      for (int n = 0; n < kD / 8; ++n)
+        *reinterpret_cast<float2 *>(po + 8 * n + 2 * c) = make_float2(Ow[n][2 * half], Ow[n][2 * half + 1]);
       if (c == 0) {
         a.part_m[pi] = (half ? m_g8 : m_g) * kLn2;
         a.part_l[pi] = half ? l_g8 : l_g;

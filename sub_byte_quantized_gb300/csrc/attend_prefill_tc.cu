@@ -164,6 +164,270 @@ __device__ __forceinline__ void tm_st16(uint32_t taddr, const uint32_t (&v)[16])
 // The tiles keep each 8-dim group in the unpacker's pair order: position p of the group holds dim
 // perm8(p) = (p >> 1) + 4 (p & 1).
 
+// One chunk of the exact-f32 recent window (kWinChunk tokens of the rotated f32 K/V ring) for the
+// CTA's 256 query rows, scored with the prepared rotated f32 query rows on the tensor cores and
+// accurate to f32. Every f32 operand is split into f16 hi + lo parts (hi = x rounded to f16, lo =
+// the remainder rounded to f16: 22 significant bits), and each product takes three m16n8k16 MMAs
+// (lo * hi, hi * lo, hi * hi; the dropped lo * lo term is below 2^-21 of the product). To keep the
+// parts inside the f16 range every operand is first scaled by an exact power of two that lands its
+// largest magnitude in [2^13, 2^14): each query row and each key token for S = Q K^T (their factors
+// multiply each score back), each value dim for O = P V (its factor multiplies the dim's output;
+// the probabilities need none, p <= 1). K and V are split once per CTA into f16 planes (V
+// transposed, so that a B fragment's two tokens are adjacent); the rows are taken 128 at a time
+// (eight warps of 16 rows), each warp scoring its rows against all 64 tokens (eight m16n8
+// accumulators: rows g and g + 8 against tokens 8t + 2c and 8t + 2c + 1, g = lane / 4,
+// c = lane % 4), taking the softmax over them in one pass and accumulating O[16 rows][128 dims] in
+// sixteen more, with the probabilities reused as A fragments in place. These CTAs come last in the
+// grid, so they run on the SMs that the body CTAs leave free.
+constexpr int kWp = kD + 4;                     // floats per staged f32 row (16 bytes of padding)
+constexpr int kKPitch = kD + 8;                 // halves per K plane row (token): 68 words
+constexpr int kVPitch = kWinChunk + 8;          // halves per transposed V plane row (dim): 36 words
+constexpr int kWinRows = 128 * kWp * 4;                            // 128 staged f32 rows
+static_assert(kWinRows == 2 * kWinChunk * kWp * 4, "the chunk's K and V rows fill one staging area");
+constexpr int kWinA = 0;                                          // f32 K, V rows, later the second half's query rows
+constexpr int kWinB = kWinA + kWinRows;                           // the first half's f32 query rows
+constexpr int kWinKh = kWinB + kWinRows;                          // K hi, K lo [token][dim] f16
+constexpr int kWinKl = kWinKh + kWinChunk * kKPitch * 2;
+constexpr int kWinVh = kWinKl + kWinChunk * kKPitch * 2;          // V hi, V lo [dim][token] f16
+constexpr int kWinVl = kWinVh + kD * kVPitch * 2;
+constexpr int kWinSc = kWinVl + kD * kVPitch * 2;                 // f32: key factors [64], value-dim factors [128], row factors [2][128]
+constexpr int kWinVmax = kWinSc + (kWinChunk + kD + 256) * 4;     // per value dim: largest magnitude (bit pattern)
+constexpr int kWinEnd = kWinVmax + kD * 4;
+static_assert(kWinEnd <= 227 * 1024, "window chunk fits one CTA");
+template <int L>
+constexpr int tc_smem() { return RawGeo<L>::SMEM > kWinEnd ? RawGeo<L>::SMEM : kWinEnd; }
+// 2^e with e chosen so that m * 2^e lies in [2^13, 2^14) (m > 0; 1 for m = 0), and its inverse
+__device__ __forceinline__ void pow2_scale(float m, float &up, float &down) {
+  int e = 0;
+  if (m > 0.0f) e = min(max(13 - (((__float_as_int(m) >> 23) & 0xFF) - 127), -100), 100);
+  up = __int_as_float((e + 127) << 23);
+  down = __int_as_float((127 - e) << 23);
+}
+// (x0, x1) -> f16 pairs hi = rn(x), lo = rn(x - hi)
+__device__ __forceinline__ void split_f16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  hi = pack_f16x2(x0, x1);
+  const float2 h = __half22float2(u32_as_h2(hi));
+  lo = pack_f16x2(x0 - h.x, x1 - h.y);
+}
+template <bool PAGED>
+__device__ __forceinline__ void window_chunk(const AttendArgs &a, uint8_t *sm, int row0, int bh, int wc) {
+  const CacheView &cv = a.cache;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = lane & 3;
+  constexpr int kWarpsAll = kThreads / 32;
+  const int bb = bh / cv.H, kvh = bh - bb * cv.H;
+  const SeqLen sl = seq_of_t<PAGED>(a, bb);
+  const int R = a.gqa * a.n_q;
+  const int t0 = sl.n_body + wc * kWinChunk, t1 = min(sl.kv_len, t0 + kWinChunk);
+  const int w_lim = max_row_limit(a, sl, row0, min(row0 + kCtaRows, R));
+  if (t0 > w_lim || t0 >= t1) return;                   // no row of this CTA sees the chunk
+  const int t_end = min(t1, w_lim + 1);
+  float *wa = reinterpret_cast<float *>(sm + kWinA), *wb = reinterpret_cast<float *>(sm + kWinB);
+  uint16_t *kh = reinterpret_cast<uint16_t *>(sm + kWinKh), *kl = reinterpret_cast<uint16_t *>(sm + kWinKl);
+  uint16_t *vh = reinterpret_cast<uint16_t *>(sm + kWinVh), *vl = reinterpret_cast<uint16_t *>(sm + kWinVl);
+  float *kdown = reinterpret_cast<float *>(sm + kWinSc), *vdown = kdown + kWinChunk, *qdown = vdown + kD;
+  uint32_t *vmax = reinterpret_cast<uint32_t *>(sm + kWinVmax);
+  // the rotated f32 query rows of rows hr0 .. hr0 + 127 into a staging area (zeros past the last row)
+  auto stage_rows = [&](float *dst, int hr0) {
+    for (int u = tid; u < 128 * 32; u += kThreads) {
+      const int lr = u >> 5, pc = u & 31, r = hr0 + lr;
+      const bool in = r < R;
+      const float *src = a.q_rot + query_row_index(a, bb, kvh, in ? r : hr0) * kD + 4 * pc;
+      cp_async16(smem_addr(dst + lr * kWp + 4 * pc), src, in ? 16 : 0);
+    }
+  };
+  // each staged row scaled in place by its power of two (one warp per row)
+  auto scale_rows = [&](float *rows, float *down) {
+#pragma unroll 4
+    for (int lr = warp; lr < 128; lr += kWarpsAll) {
+      const float4 x = *reinterpret_cast<const float4 *>(rows + lr * kWp + 4 * lane);
+      float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+      for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+      float up, dn;
+      pow2_scale(m, up, dn);
+      *reinterpret_cast<float4 *>(rows + lr * kWp + 4 * lane) = make_float4(x.x * up, x.y * up, x.z * up, x.w * up);
+      if (lane == 0) down[lr] = dn;
+    }
+  };
+  // ---- all copies in flight at once: the chunk's f32 K and V rows from the ring (slot t mod
+  // n_recent; zeros past t_end) and the first half's query rows
+  for (int u = tid; u < 2 * kWinChunk * 32; u += kThreads) {
+    const int pl = u / (kWinChunk * 32), row = (u >> 5) % kWinChunk, pc = u & 31;
+    const int t = t0 + row;
+    const bool in = t < t_end;
+    const float *src = cv.ring[pl] + ((size_t)bh * cv.n_recent + (size_t)((in ? t : t0) % cv.n_recent)) * kD + 4 * pc;
+    cp_async16(smem_addr(wa + (pl * kWinChunk + row) * kWp + 4 * pc), src, in ? 16 : 0);
+  }
+  stage_rows(wb, row0);
+  for (int d = tid; d < kD; d += kThreads) vmax[d] = 0u;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
+  // ---- K: one warp per token, scaled by its power of two and split into the hi / lo planes; V:
+  // the largest magnitude of each dim (every warp over its tokens, merged with an atomic max on
+  // the bit patterns, which order like non-negative floats)
+  for (int t = warp; t < kWinChunk; t += kWarpsAll) {
+    const float4 x = *reinterpret_cast<const float4 *>(wa + t * kWp + 4 * lane);
+    float m = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+    float up, down;
+    pow2_scale(m, up, down);
+    uint32_t h0, l0, h1, l1;
+    split_f16x2(x.x * up, x.y * up, h0, l0);
+    split_f16x2(x.z * up, x.w * up, h1, l1);
+    *reinterpret_cast<uint2 *>(kh + t * kKPitch + 4 * lane) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2 *>(kl + t * kKPitch + 4 * lane) = make_uint2(l0, l1);
+    if (lane == 0) kdown[t] = down;
+  }
+  {
+    float4 m4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int t = warp; t < kWinChunk; t += kWarpsAll) {
+      const float4 x = *reinterpret_cast<const float4 *>(wa + (kWinChunk + t) * kWp + 4 * lane);
+      m4 = make_float4(fmaxf(m4.x, fabsf(x.x)), fmaxf(m4.y, fabsf(x.y)), fmaxf(m4.z, fabsf(x.z)), fmaxf(m4.w, fabsf(x.w)));
+    }
+    atomicMax(vmax + 4 * lane, __float_as_uint(m4.x));
+    atomicMax(vmax + 4 * lane + 1, __float_as_uint(m4.y));
+    atomicMax(vmax + 4 * lane + 2, __float_as_uint(m4.z));
+    atomicMax(vmax + 4 * lane + 3, __float_as_uint(m4.w));
+  }
+  scale_rows(wb, qdown);
+  __syncthreads();
+  // ---- V: scaled by each dim's power of two, split and transposed (one (dim, token pair) per item)
+  for (int u = tid; u < kD * (kWinChunk / 2); u += kThreads) {
+    const int d = u & (kD - 1), tp = u / kD;
+    float up, down;
+    pow2_scale(__uint_as_float(vmax[d]), up, down);
+    const float *col = wa + (kWinChunk + 2 * tp) * kWp + d;
+    uint32_t h, l;
+    split_f16x2(col[0] * up, col[kWp] * up, h, l);
+    *reinterpret_cast<uint32_t *>(vh + d * kVPitch + 2 * tp) = h;
+    *reinterpret_cast<uint32_t *>(vl + d * kVPitch + 2 * tp) = l;
+    if (tp == 0) vdown[d] = down;
+  }
+  __syncthreads();                                      // the K/V staging area is free
+  const bool two = row0 + 128 < R;
+  if (two) stage_rows(wa, row0 + 128);                  // the second half's rows, while the first is scored
+  const float walpha = a.scale * kLog2e;
+  for (int half = 0; half < 2 && row0 + 128 * half < R; ++half) {
+    const int hr0 = row0 + 128 * half;
+    const float *wf = half ? wa : wb;
+    const float *qd = qdown + 128 * half;
+    if (half == 1) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncthreads();
+      scale_rows(wa, qdown + 128);
+      __syncthreads();
+    }
+    if (warp >= 8) continue;
+    const int rg = hr0 + 16 * warp + g, rg8 = rg + 8;
+    const int lim_g = rg < R ? row_limit(a, sl, rg % a.n_q) : -1;
+    const int lim_g8 = rg8 < R ? row_limit(a, sl, rg8 % a.n_q) : -1;
+    if (!__any_sync(0xffffffffu, t0 <= max(lim_g, lim_g8))) continue;
+    // ---- S = Q . K^T over eight 16-dim k-steps
+    const float *qa = wf + (16 * warp + g) * kWp, *qb = qa + 8 * kWp;
+    float sc[kWinChunk / 8][4];
+#pragma unroll
+    for (int t = 0; t < kWinChunk / 8; ++t)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sc[t][k] = 0.0f;
+#pragma unroll 2
+    for (int ks = 0; ks < kD / 16; ++ks) {
+      const int d0 = 16 * ks + 2 * c;
+      uint32_t ah[4], al[4];
+      const float2 x0 = *reinterpret_cast<const float2 *>(qa + d0), x1 = *reinterpret_cast<const float2 *>(qb + d0);
+      const float2 x2 = *reinterpret_cast<const float2 *>(qa + d0 + 8), x3 = *reinterpret_cast<const float2 *>(qb + d0 + 8);
+      split_f16x2(x0.x, x0.y, ah[0], al[0]);
+      split_f16x2(x1.x, x1.y, ah[1], al[1]);
+      split_f16x2(x2.x, x2.y, ah[2], al[2]);
+      split_f16x2(x3.x, x3.y, ah[3], al[3]);
+#pragma unroll
+      for (int t = 0; t < kWinChunk / 8; ++t) {
+        const int kr = (8 * t + g) * kKPitch + d0;      // token 8t + g: column g of K^T
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(kh + kr), bh1 = *reinterpret_cast<const uint32_t *>(kh + kr + 8);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(kl + kr), bl1 = *reinterpret_cast<const uint32_t *>(kl + kr + 8);
+        mma16816(sc[t], al, bh0, bh1);
+        mma16816(sc[t], ah, bl0, bl1);
+        mma16816(sc[t], ah, bh0, bh1);
+      }
+    }
+    // ---- softmax over the chunk (base 2): sc[t] = (g, 8t+2c), (g, 8t+2c+1), (g+8, 8t+2c), (g+8, 8t+2c+1)
+    const float fg = walpha * qd[16 * warp + g], fg8 = walpha * qd[16 * warp + g + 8];
+    float m_g = -INFINITY, m_g8 = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < kWinChunk / 8; ++t) {
+      const int ta = t0 + 8 * t + 2 * c, tb = ta + 1;
+      const float ka = kdown[8 * t + 2 * c], kb = kdown[8 * t + 2 * c + 1];
+      sc[t][0] = (ta < t1 && ta <= lim_g) ? sc[t][0] * ka * fg : -INFINITY;
+      sc[t][1] = (tb < t1 && tb <= lim_g) ? sc[t][1] * kb * fg : -INFINITY;
+      sc[t][2] = (ta < t1 && ta <= lim_g8) ? sc[t][2] * ka * fg8 : -INFINITY;
+      sc[t][3] = (tb < t1 && tb <= lim_g8) ? sc[t][3] * kb * fg8 : -INFINITY;
+      m_g = fmaxf(m_g, fmaxf(sc[t][0], sc[t][1]));
+      m_g8 = fmaxf(m_g8, fmaxf(sc[t][2], sc[t][3]));
+    }
+    m_g = fmaxf(m_g, __shfl_xor_sync(0xffffffffu, m_g, 1));
+    m_g = fmaxf(m_g, __shfl_xor_sync(0xffffffffu, m_g, 2));
+    m_g8 = fmaxf(m_g8, __shfl_xor_sync(0xffffffffu, m_g8, 1));
+    m_g8 = fmaxf(m_g8, __shfl_xor_sync(0xffffffffu, m_g8, 2));
+    const float mu_g = m_g == -INFINITY ? 0.0f : m_g, mu_g8 = m_g8 == -INFINITY ? 0.0f : m_g8;
+    float l_g = 0.0f, l_g8 = 0.0f;
+#pragma unroll
+    for (int t = 0; t < kWinChunk / 8; ++t) {
+      sc[t][0] = ex2(sc[t][0] - mu_g);
+      sc[t][1] = ex2(sc[t][1] - mu_g);
+      sc[t][2] = ex2(sc[t][2] - mu_g8);
+      sc[t][3] = ex2(sc[t][3] - mu_g8);
+      l_g += sc[t][0] + sc[t][1];
+      l_g8 += sc[t][2] + sc[t][3];
+    }
+    l_g += __shfl_xor_sync(0xffffffffu, l_g, 1);
+    l_g += __shfl_xor_sync(0xffffffffu, l_g, 2);
+    l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 1);
+    l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 2);
+    // ---- O = P . V over four 16-token k-steps: the probabilities of tiles 2kk and 2kk + 1 are the
+    // A fragment as they stand (k = 2c, 2c + 1 <-> tile 2kk's tokens, k = 2c + 8, 2c + 9 <-> tile
+    // 2kk + 1's); B fragments from the transposed V planes
+    float o[kD / 8][4];
+#pragma unroll
+    for (int n = 0; n < kD / 8; ++n)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[n][k] = 0.0f;
+#pragma unroll
+    for (int kk = 0; kk < kWinChunk / 16; ++kk) {
+      uint32_t ph[4], pl[4];
+      split_f16x2(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+      split_f16x2(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+      split_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+      split_f16x2(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
+#pragma unroll
+      for (int n = 0; n < kD / 8; ++n) {
+        const int vr = (8 * n + g) * kVPitch + 16 * kk + 2 * c;   // dim 8n + g, tokens 16kk + 2c, +1
+        const uint32_t bh0 = *reinterpret_cast<const uint32_t *>(vh + vr), bh1 = *reinterpret_cast<const uint32_t *>(vh + vr + 8);
+        const uint32_t bl0 = *reinterpret_cast<const uint32_t *>(vl + vr), bl1 = *reinterpret_cast<const uint32_t *>(vl + vr + 8);
+        mma16816(o[n], pl, bh0, bh1);
+        mma16816(o[n], ph, bl0, bl1);
+        mma16816(o[n], ph, bh0, bh1);
+      }
+    }
+    // ---- partials of the rows that see the chunk (partial index n_chunks + wc)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = hh ? rg8 : rg, lim = hh ? lim_g8 : lim_g;
+      if (r >= R || t0 > lim) continue;
+      const int hq = kvh * a.gqa + r / a.n_q, qi = r % a.n_q;
+      const size_t pi = (((size_t)bb * a.Hq + hq) * a.n_q + qi) * a.C + a.n_chunks + wc;
+      float *po = a.part_o + pi * kD;
+#pragma unroll
+      for (int n = 0; n < kD / 8; ++n)
+        *reinterpret_cast<float2 *>(po + 8 * n + 2 * c) =
+            make_float2(o[n][2 * hh] * vdown[8 * n + 2 * c], o[n][2 * hh + 1] * vdown[8 * n + 2 * c + 1]);
+      if (c == 0) {
+        a.part_m[pi] = (hh ? m_g8 : m_g) * kLn2;        // natural-log units, like the other kernels
+        a.part_l[pi] = hh ? l_g8 : l_g;
+      }
+    }
+  }
+}
+
 template <int L, bool PAGED, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendArgs a) {
   using RG = RawGeo<L>;
@@ -174,16 +438,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
   asm volatile("griddepcontrol.launch_dependents;");
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the query codes come from the preceding kernel
 #endif
-  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + RG::BAR);
   const CacheView &cv = a.cache;
+  const int heads = cv.B * cv.H;
+  if ((int)blockIdx.z >= heads) {
+    // window chunks: the CTAs after the body's, (z - heads, y) numbering (head, window chunk) pairs
+    const int wl = ((int)blockIdx.z - heads) * (int)gridDim.y + (int)blockIdx.y;
+    if (!CAP && wl < heads * a.n_wchunks)
+      window_chunk<PAGED>(a, sm, blockIdx.x * kCtaRows, wl / a.n_wchunks, wl % a.n_wchunks);
+    return;
+  }
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm + RG::BAR);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row0 = blockIdx.x * kCtaRows, chunk_id = blockIdx.y, bh = blockIdx.z;
   const int bb = bh / cv.H, kvh = bh - bb * cv.H;
   const SeqLen sl = seq_of_t<PAGED>(a, bb);
   const int R = a.gqa * a.n_q;
   const int t0 = chunk_id * sl.chunk, t1 = min(sl.n_body, t0 + sl.chunk);
-  int w_lim = -1;
-  for (int r = row0; r < min(row0 + kCtaRows, R); ++r) w_lim = max(w_lim, row_limit(a, sl, r % a.n_q));
+  const int w_lim = max_row_limit(a, sl, row0, min(row0 + kCtaRows, R));
   if (t0 > w_lim || t0 >= t1) return;                   // no row of this CTA sees the chunk
   const int t_end = min(t1, w_lim + 1);
   const int n_st = (t_end - t0 + kStage - 1) / kStage;
@@ -522,12 +793,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_prefill_tc_kernel(AttendAr
 template <int L, bool PAGED, bool CAP>
 cudaError_t launch_tc(const AttendArgs &a, cudaStream_t st) {
   static std::atomic<bool> configured[kMaxDevices];
-  cudaError_t e = set_smem_once(configured, attend_prefill_tc_kernel<L, PAGED, CAP>, RawGeo<L>::SMEM);
+  cudaError_t e = set_smem_once(configured, attend_prefill_tc_kernel<L, PAGED, CAP>, tc_smem<L>());
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.gqa * a.n_q + kCtaRows - 1) / kCtaRows, a.n_chunks, a.cache.B * a.cache.H);
+  // body CTAs (row block, chunk, head), then the window CTAs in extra z slices
+  const int heads = a.cache.B * a.cache.H;
+  const int wz = CAP ? 0 : (heads * a.n_wchunks + a.n_chunks - 1) / a.n_chunks;
+  cfg.gridDim = dim3((a.gqa * a.n_q + kCtaRows - 1) / kCtaRows, a.n_chunks, heads + wz);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = RawGeo<L>::SMEM;
+  cfg.dynamicSmemBytes = tc_smem<L>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -280,6 +280,15 @@ __device__ __forceinline__ int row_limit(const AttendArgs &a, const SeqLen &s, i
   return a.causal ? min(s.kv_len - 1, s.q_pos0 + qi) : s.kv_len - 1;
 }
 
+// The largest row limit among query rows [r_lo, r_hi) of a kv head (negative if the range is empty):
+// row_limit grows with the query index qi = r % n_q, so only the largest qi in the range matters.
+__device__ __forceinline__ int max_row_limit(const AttendArgs &a, const SeqLen &s, int r_lo, int r_hi) {
+  if (r_hi <= r_lo) return -1;
+  const int lo = r_lo % a.n_q, hi = (r_hi - 1) % a.n_q;
+  const int qmax = (r_hi - r_lo >= a.n_q || lo > hi) ? a.n_q - 1 : hi;
+  return row_limit(a, s, qmax);
+}
+
 // Load 8 consecutive input elements starting at element index `e` (8-aligned) as f32.
 __device__ __forceinline__ void load8_f32(const void *base, int dtype, size_t e, float v[8]) {
   if (dtype == KVQ_F32) {

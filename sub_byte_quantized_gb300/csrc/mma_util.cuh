@@ -65,6 +65,22 @@ __device__ __forceinline__ void mma16816_c(float (&d)[4], const uint32_t (&a)[4]
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c0), "f"(c1), "f"(c2), "f"(c3));
 }
+// m16n8k8 with tf32 operands (f32 bit patterns whose low 13 mantissa bits are zero), f32 accumulate:
+// a0 / a1 = rows g / g+8 at k = c, a2 / a3 the same rows at k = c + 4; b0 / b1 = k = c / c + 4 of
+// column g; d0, d1 = row g, columns 2c, 2c+1; d2, d3 = row g+8.
+__device__ __forceinline__ void mma1688_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// x = hi + lo with hi = x rounded to tf32 (nearest, ties away) and lo = the remainder rounded to
+// tf32: hi + lo carries 22 significant bits of x, and the products hi*hi + hi*lo + lo*hi of two
+// split operands match their f32 product to about 2^-21 relative.
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  const float r = x - __uint_as_float(hi);
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) { return __byte_perm(a, b, sel); }
 __device__ __forceinline__ float ex2(float x) {
   float y;
