@@ -157,10 +157,11 @@ kvq_status store_common(int want_layout, const kvq_cache *cache, const void *k_n
 }
 
 // Automatic split-K chunk, sized for the tensor-core kernel that will run. Decode (up to eight
-// query rows per kv head), one wave: for the 4-bit layouts four times the smallest multiple of 64
-// tokens that gives one slice to every resident warp (four warps per chunk); for the
-// warp-specialised kernels (Q6_0, asymmetric) the smallest multiple of 64 that gives one chunk to
-// every resident CTA. Many rows (Hadamard prefill): about four waves of 64-row CTAs.
+// query rows per kv head), one wave: for the per-warp kernel four times the smallest multiple of
+// 32 tokens (a warp's stage) that gives one slice to every resident warp (four warps per chunk);
+// for the warp-specialised kernels (Q6_0, asymmetric) the smallest multiple of 64 that gives one
+// chunk to every resident CTA. Many rows: about four waves of 64-row CTAs on the row-side kernel,
+// the fewest waves x stages of 256-row CTAs on the tcgen05 kernel.
 // `work` = body tokens summed over every (batch, kv head) (0: n_body for each of them); a ragged
 // batch passes its true total so the chunk fits the work that exists.
 // n_wchunks: window chunks per (batch, kv head) that the row-side kernel scores in the same grid.
@@ -218,7 +219,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
     chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
   } else {
     const long long warps = (long long)sms * kvq::kMmaWarpsPerSm;
-    chunk = 4 * (((work + warps - 1) / warps + 63) / 64 * 64);
+    chunk = 4 * (((work + warps - 1) / warps + 31) / 32 * 32);   // a warp's slice: whole 32-token stages
   }
   if (chunk > 8192) chunk = 8192;
   return (int)chunk;
