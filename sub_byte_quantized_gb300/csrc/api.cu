@@ -186,7 +186,7 @@ int auto_chunk(const kvq::CacheView &c, int rows, int n_body, int n_heads, long 
     const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
     chunk = ((body + per_head - 1) / per_head + 63) / 64 * 64;
   } else if (kvq::tc_prefill_shape(c.layout, c.v_layout, c.D, rows)) {
-    // tcgen05 kernel, one CTA of 128 rows per SM: the number of body chunks per row block (1..8)
+    // tcgen05 kernel, one CTA of 256 rows per SM: the number of body chunks per row block (1..8)
     // whose grid takes the fewest waves x (stages per chunk + about two stages of fixed cost per CTA)
     const long long units = (long long)((rows + kvq::kTcRows - 1) / kvq::kTcRows) * n_heads;
     const long long body = total_given ? (work + n_heads - 1) / n_heads : (n_body > 0 ? n_body : 1);
@@ -642,7 +642,7 @@ void phase1_capacity(const kvq::CacheView &c, int rows, int q_dtype, int &ctas_p
     ctas_per_sm = kvq::kMmaQ6CtasPerSm(c.D);
     ctas_per_unit = (rows + 3) / 4;
   } else if (kvq::tc_prefill_shape(c.layout, c.v_layout, c.D, rows)) {
-    ctas_per_sm = 1;                                     // the tcgen05 kernel: one CTA of 128 rows per SM
+    ctas_per_sm = 1;                                     // the tcgen05 kernel: one CTA of 256 rows per SM
     ctas_per_unit = (rows + kvq::kTcRows - 1) / kvq::kTcRows;
   } else if (kvq::prefill_shape(c.layout, c.v_layout, c.D, rows) &&
              (kvq::is_hadamard(c.layout) || q_dtype != KVQ_F32)) {

@@ -4,34 +4,39 @@
 // appended chunk attend the cached body with their causal limits; "What's done": the body score is
 // the exact integer dot int8(q_rot) . int4(k_rot)).
 //
-// One CTA = 128 query rows of one (batch, kv head) x one split-K chunk of body tokens. The rows are
-// the M side of both products, and the accumulators live in tensor memory (TMEM, 256 columns):
-//   S  = Q8 . K^T       M 128 x N 64 tokens x K 128 dims   -> TMEM columns 0-63 / 64-127 (two stages)
-//   O += P' . V         M 128 x N 128 dims x K 64 tokens   -> TMEM columns 128-255, with P' (A) read
-//                                                            from TMEM columns 256-383 (two stages)
+// A body CTA = 256 query rows of one (batch, kv head), as two blocks of 128, x one split-K chunk of
+// body tokens. The rows are the M side of both products, and the accumulators live in tensor memory
+// (TMEM, all 512 columns; per block b):
+//   S  = Q8 . K^T       M 128 x N 64 tokens x K 128 dims   -> TMEM columns 64 b .. +63
+//   O += P' . V         M 128 x N 128 dims x K 64 tokens   -> TMEM columns 128 + 128 b .. +127, with
+//                                                            P' (A) read from columns 384 + 64 b .. +63
 // Q8 holds the int8 query codes and K, V the signed 2- or 4-bit codes, all exact in f16 (kind::f16,
 // f32 accumulate), so S is the exact integer dot (|dot| < 2^17). score = alpha * s_q * s_k * dot;
 // the per-token V scale is folded into the probabilities, P' = p * s_v, which go to the PV product
-// as exact f16 hi + lo parts (two MMAs per k-step).
+// as exact f16 hi + lo parts (two MMAs per k-step). The two blocks share every K/V tile and take
+// turns on the tensor core: per stage the MMA lane issues, for block 0 and then block 1, the P'V of
+// the previous stage (once the block's softmax has stored its P') and then the block's S of this
+// stage, so one block's softmax overlaps the other's MMAs.
 //
-// Warp roles (14 warps), connected by mbarriers; every wait is bounded in time and a CTA whose wait
+// Warp roles (12 warps), connected by mbarriers; every wait is bounded in time and a CTA whose wait
 // gives up writes NaN partials for its rows, so a failure shows in the output instead of hanging:
-//   warps 0-7   softmax: warp w serves TMEM lanes (query rows) 32 (w % 4) .. +31 and the column half
-//               w / 4 (S columns 32 h .. +31, O columns 64 h .. +63); the two halves of a row exchange
-//               their maxima through shared memory; online softmax in base 2 with a lazily moved
-//               reference maximum (below), the row's score factor folded into the exponent's fma;
-//               P' hi/lo into tensor memory (two stage buffers), the A operand of the PV product
+//   warps 0-7   softmax: warp w serves block w / 4, TMEM lanes (query rows) 32 (w % 4) .. +31; each
+//               thread owns a whole row (64 scores per stage); online softmax in base 2 with a lazily
+//               moved reference maximum (below), the row's score factor folded into the exponent's
+//               fma; P' hi/lo into tensor memory, the A operand of the PV product
 //   warp  8     copy: packed K/V rows and per-token scales of each 64-token stage -> a three-slot raw
 //               ring (16-byte cp.async, completion counted on the slot's mbarrier)
-//   warp  9     one lane issues the MMAs (S of stage j, then P'V of stage j - 1) and commits them to
-//               mbarriers; the warp owns the TMEM allocation
-//   warps 10-13 unpack: raw codes -> f16 code tiles (two tile buffers, 128-byte swizzle), scales ->
+//   warp  9     one lane issues the MMAs and commits them to mbarriers; the warp owns the TMEM
+//               allocation
+//   warps 10-11 unpack: raw codes -> f16 code tiles (three tile buffers, 128-byte swizzle), scales ->
 //               per-stage arrays
-// Operand layouts (shared-memory descriptors, 128-byte swizzle): Q [128 rows][128 dims] and K
-// [64 tokens][128 dims] K-major in two 64-dim column blocks; V [64 tokens][128 dims] read as the
-// MN-major B operand of the PV product; P' in TMEM, lane = row, two tokens per 32-bit column (16
-// tokens = 8 columns per MMA k-step; the hi parts of a stage, then its lo parts). Within each 8-dim group
-// the tiles keep the unpacker's order (dims 0,4,1,5,2,6,3,7); the output columns follow it.
+// (Twelve warps put at most three on a scheduler, so a thread may hold 168 registers: the whole-row
+// softmax needs them.)
+// Operand layouts (shared-memory descriptors, 128-byte swizzle): Q [128 rows][128 dims] per block
+// and K [64 tokens][128 dims] K-major in two 64-dim column blocks; V [64 tokens][128 dims] read as
+// the MN-major B operand of the PV product; P' in TMEM, lane = row, two tokens per 32-bit column (16
+// tokens = 8 columns per MMA k-step; the hi parts of a stage, then its lo parts). Within each 8-dim
+// group the tiles keep the unpacker's order (dims 0,4,1,5,2,6,3,7); the output columns follow it.
 //
 // Lazy rescaling: O and l are kept relative to a reference maximum m per row, which moves only when
 // a stage's maximum exceeds it by more than tau (log2 units); then O is rescaled in TMEM (after the
@@ -40,9 +45,10 @@
 // partial (m, l, O) is exact softmax algebra for any reference, so the result does not depend on
 // when m moves; what tau saves is the wait for the tensor core on almost every stage.
 //
-// The int8 query codes and scales come from the query-preparation kernel launched just before (one
-// pass over the rows instead of one per chunk); the exact-f32 recent window is scored by the
-// row-side kernel's window chunks, launched after this one.
+// The int8 query codes and scales, and the rotated f32 query rows, come from the query-preparation
+// kernel launched just before (one pass over the rows instead of one per chunk). The exact-f32
+// recent window is scored by more CTAs of the same grid, after the body CTAs in launch order
+// (window_chunk below).
 #include <cfloat>
 #include <climits>
 
