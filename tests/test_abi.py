@@ -290,12 +290,19 @@ def test_decode_chunk_follows_the_kernel(L):
         c = KvqCache(layout, 1, 8, 128, 131072, n_recent, 4096, 4096, 4096, 4096, zero, zero, ring, ring)
         return L.kvq_attend_chunk(p(c), 8 * rows, 1, 131072, 0)
 
+    # the SM count the library sizes for: the device's, else its default of 148
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    up = lambda x, m: -(-x // m) * m
+    # per-warp kernel: 12 resident warps per SM, each warp's slice whole 32-token stages, 4 warps per chunk
     per_warp = chunk(0)
-    assert per_warp % 64 == 0 and per_warp > 0
+    assert per_warp == 4 * up(-(-8 * 131072 // (12 * sms)), 32)
     assert chunk(4) == per_warp                      # Q8_0 on the per-warp kernel
     assert chunk(mixed(0, 4)) == per_warp            # Q4_0 keys + Q8_0 values
     assert chunk(3) != per_warp                      # asymmetric: one chunk per resident CTA
-    assert chunk(5, n_recent=256) != per_warp        # Hadamard int2: row-side kernel, decode form
+    # Hadamard int2: row-side kernel, decode form: one chunk per resident CTA (3 per SM) of the body
+    # (the window is scored in phase 2)
+    assert chunk(5, n_recent=256) == up(-(-(131072 - 256) // (3 * sms // 8)), 64)
     # more than eight rows per kv head leave the per-warp kernel
     assert chunk(4, rows=16) != chunk(4, rows=8)
 
