@@ -685,6 +685,7 @@ def main():
                        "python_binding_us_per_layer": t_py * 1e6}
         line["store"] = store_timings(kvq, w, kd, vd, k_new, v_new, fill, stream, dev)
         if args.workload == DEFAULT_WORKLOAD:
+            line["comparators"] = comparators(caches[0], kd, vd, q, out, w, spec, stream, dev)
             line["variants"] = variants(kvq, caches, n_rep, k_new, v_new, q, out, spec, stream, ev0, ev1,
                                         min(K, 1000), chunk, make_caches, dev)
         if world == 1:
@@ -697,6 +698,65 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def comparators(cache, kd, vd, q, out, w, spec, stream, dev, reps=20):
+    """Optional comparators, for context only (not targets): torch's bf16 scaled_dot_product_attention
+    over the unquantised K/V of the same layer, and a materialised path that first dequantises the Q4_0
+    planes into bf16 K/V with plain torch tensor ops and then runs the same SDPA (the "dequantise, then
+    attend" alternative to reading the packed cache in the attention kernel). Whole calls, CUDA events on
+    the bench stream, K/V far larger than L2."""
+    import torch
+    import torch.nn.functional as F
+    B, H, S, D = spec.B, spec.H, spec.S, spec.D
+    qb = q.to(torch.bfloat16)
+    res = {"note": "torch ops, not this library; context for the fused read, not a target. max_abs_diff: against this library's output of the same step (the unquantised SDPA differs by the Q4_0 quantisation error)"}
+
+    def sdpa(k, v):
+        return F.scaled_dot_product_attention(qb, k, v, scale=w.alpha, enable_gqa=True)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    ref = out.float()                          # this library's output of the same step (sanity check)
+    res["library_max_abs_output"] = float(ref.abs().max())
+    try:
+        res["torch_sdpa_bf16_us"] = timed(lambda: sdpa(kd, vd))
+        res["torch_sdpa_bf16_bytes_read"] = 2 * kd.numel() * kd.element_size()
+        res["torch_sdpa_bf16_max_abs_diff"] = float((sdpa(kd, vd).float() - ref).abs().max())
+    except Exception as e:   # a torch build without the GQA form of SDPA
+        res["torch_sdpa_bf16_error"] = str(e)[:200]
+    if w.layout == "q4_0":
+        cap = cache.capacity
+
+        def planes(t):
+            return (cache.planes[t]["payload"].view(B, H, cap, D // 2)[:, :, :S],
+                    cache.planes[t]["scale"].view(B, H, cap, D // 32)[:, :, :S])
+
+        def deq(payload, scale):
+            # byte j of a 32-value block: value 2j in the low nibble, 2j+1 in the high; code (n ^ 8) - 8
+            n = torch.stack((payload & 15, payload >> 4), dim=-1).view(B, H, S, D).to(torch.int16)
+            code = (n ^ 8) - 8
+            return (code.to(torch.float32) * scale.to(torch.float32).repeat_interleave(32, dim=-1)).to(torch.bfloat16)
+
+        (pk, sk), (pv, sv) = planes("k"), planes("v")
+        try:
+            res["dequant_then_sdpa_us"] = timed(lambda: sdpa(deq(pk, sk), deq(pv, sv)))
+            res["dequant_then_sdpa_max_abs_diff"] = float((sdpa(deq(pk, sk), deq(pv, sv)).float() - ref).abs().max())
+        except Exception as e:
+            res["dequant_then_sdpa_error"] = str(e)[:200]
+    return res
 
 
 def workload_summaries(kvq, L, dev, stream, K, hbm_peak, bf16_peak):
