@@ -193,9 +193,11 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   }
 }
 
-// One warp per row (many rows; the window, if any, is a partial of its own).
-template <int D, bool HAD>
-__global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendArgs a, unsigned rows) {
+// One warp per row (many rows; the window, if any, is a partial of its own). KB = partials loaded
+// per batch: as many as the rows have (up to eight), since the registers they take bound the rows in
+// flight per SM (a causal prefill chunk with one body chunk and one window chunk: two).
+template <int D, bool HAD, int KB>
+__global__ void __launch_bounds__(kWarps * 32, KB >= 8 ? 1 : (D == 128 ? 8 - KB : 6 - KB)) attend_reduce_rows_kernel(AttendArgs a, unsigned rows) {
   constexpr int VPL = D / 32;
 #if defined(__CUDA_ARCH__) && __CUDA_ARCH__ >= 900
   asm volatile("griddepcontrol.wait;" ::: "memory");     // phase-1 partials are complete
@@ -213,10 +215,10 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
   float M = -INFINITY, L = 0.0f, O[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) O[i] = 0.0f;
-  for (int base = 0; base < a.C; base += kBatch) {
-    float mc[kBatch], lc[kBatch], oc[kBatch][VPL];
+  for (int base = 0; base < a.C; base += KB) {
+    float mc[KB], lc[KB], oc[KB][VPL];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
+    for (int u = 0; u < KB; ++u) {
       const int c = base + u;
       const int wt0 = sl.n_body + (c - a.n_chunks) * kWinChunk;      // window chunk's first token
       const bool vis = c < a.C && (c < a.n_chunks ? c < n_vis_body : wt0 < sl.kv_len && wt0 <= lim);
@@ -232,14 +234,14 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
     }
     float bm = M;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, mc[u]);
+    for (int u = 0; u < KB; ++u) bm = fmaxf(bm, mc[u]);
     if (bm == -INFINITY) continue;
     const float corr = __expf(M - bm);
     L *= corr;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) O[i] *= corr;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
+    for (int u = 0; u < KB; ++u) {
       const float w = __expf(mc[u] - bm);
       L = fmaf(lc[u], w, L);
 #pragma unroll
@@ -265,6 +267,15 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_rows_kernel(AttendA
   }
 }
 
+template <int KB>
+cudaError_t launch_rows(cudaLaunchConfig_t &cfg, const AttendArgs &a, unsigned rows, bool had) {
+  if (a.cache.D == 128)
+    return had ? cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<128, true, KB>, a, rows)
+               : cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<128, false, KB>, a, rows);
+  return had ? cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<256, true, KB>, a, rows)
+             : cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<256, false, KB>, a, rows);
+}
+
 }  // namespace
 
 cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl) {
@@ -285,11 +296,9 @@ cudaError_t launch_attend_reduce(const AttendArgs &a, cudaStream_t st, bool pdl)
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   if (per_warp) {
-    if (a.cache.D == 128)
-      return had ? cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<128, true>, a, rows)
-                 : cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<128, false>, a, rows);
-    return had ? cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<256, true>, a, rows)
-               : cudaLaunchKernelEx(&cfg, attend_reduce_rows_kernel<256, false>, a, rows);
+    if (a.C <= 2) return launch_rows<2>(cfg, a, rows, had);
+    if (a.C <= 4) return launch_rows<4>(cfg, a, rows, had);
+    return launch_rows<kBatch>(cfg, a, rows, had);
   }
   if (a.cache.D == 128)
     return had ? cudaLaunchKernelEx(&cfg, attend_reduce_kernel<128, true>, a)
