@@ -1,7 +1,8 @@
 // Tensor-core phase 1 of the split-K decode attention for the block layouts with 4- and 8-bit
 // codes (Q4_0, Q8_0, Q4_0 keys with Q8_0 values, the asymmetric g=32 layout) and the per-token
-// Hadamard int4 body, head_dim 128, up to 8 query rows per kv head (the GQA group times the query
-// rows of the call). For the Hadamard layout the exact-f32 recent window is scored in phase 2.
+// Hadamard int4 and int2 bodies, head_dim 128, up to 8 query rows per kv head (the GQA group times
+// the query rows of the call). For the Hadamard layouts the exact-f32 recent window is scored in
+// phase 2.
 //
 // Why tensor cores: every kv head is shared by gqa query heads, so per packed K/V element the
 // step does 4*gqa flops (QK and PV); at gqa 8 that is ~57 flops per packed byte, beyond what
@@ -26,6 +27,13 @@
 // values u * 2^-24 of the offset code u (one lop3 per nibble pair; one byte permute per 8-bit
 // pair), the offset going into the accumulator's initial value or a separate term; Q4_0 and Q8_0
 // V codes become exact signed f16 values (the code under the exponent of 1024, one f16 add).
+//
+// Hadamard int2 (32-byte rows, value f of a byte at bits 2f): one ldmatrix gives a lane 16
+// consecutive dims of a token per word; two byte permutes split a word into two f16 lanes and one
+// lop3 per pair keeps the fields k of both lanes in place with their sign bit flipped, i.e. the
+// subnormal u * 4^k * 2^-24 of u = code + 2 (K: the query entries facing field k are divided by
+// 4^k and -2 * sum(q) is the accumulator's initial value). V codes become exact signed f16 values
+// (a shift, the lop3 under the exponent of 1024, one f16 add per pair).
 //
 // Each CTA handles one chunk of one (batch, kv head); each of its four warps streams a contiguous
 // quarter of the chunk through a private two-stage shared-memory ring and keeps its online
@@ -62,9 +70,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Q8_0), K and V scales (4 f16 per token, or one f32 per token for the Hadamard layout),
 // asymmetric zero-points (4 f16 per token).
 template <int L>
-__host__ __device__ constexpr int plane_row_bytes() { return L == KVQ_Q8_0 ? 128 : 64; }
+__host__ __device__ constexpr int plane_row_bytes() { return L == KVQ_Q8_0 ? 128 : (L == KVQ_HAD_INT2 ? 32 : 64); }
 template <int L>
-__host__ __device__ constexpr int scale_bytes() { return L == KVQ_HAD_INT4 ? 4 : 8; }
+__host__ __device__ constexpr int scale_bytes() { return is_hadamard(L) ? 4 : 8; }
 template <int L, int VL>
 __host__ __device__ constexpr int off_v() { return kStage * plane_row_bytes<L>(); }
 template <int L, int VL>
@@ -83,10 +91,10 @@ __host__ __device__ constexpr int stage_bytes() {
 constexpr int kQScratch = 8 * 128 + 8 * 4;
 template <int L, int VL>
 __host__ __device__ constexpr int smem_bytes() {
-  return kWarps * kRing * stage_bytes<L, VL>() + (L == KVQ_HAD_INT4 ? kWarps * kQScratch : 0);
+  return kWarps * kRing * stage_bytes<L, VL>() + (is_hadamard(L) ? kWarps * kQScratch : 0);
 }
 // the warps' final (m, l, o) states reuse the stage buffers
-static_assert(kWarps * 8 * (2 + kD) * 4 <= kWarps * kRing * stage_bytes<KVQ_HAD_INT4, KVQ_HAD_INT4>(),
+static_assert(kWarps * 8 * (2 + kD) * 4 <= kWarps * kRing * stage_bytes<KVQ_HAD_INT2, KVQ_HAD_INT2>(),
               "combine buffer fits");
 static_assert(smem_bytes<KVQ_Q8_0, KVQ_Q8_0>() * kMinBlocks <= 227 * 1024, "Q8_0 stages fit the resident CTAs");
 
@@ -97,10 +105,10 @@ __device__ __forceinline__ int row_limit_of(const AttendArgs &a, const SeqLen &s
 
 // Byte offset of (row, 16-byte column j) inside a swizzled slab of RB-byte rows: the column is
 // XORed with bits of the row so that the 8 rows an ldmatrix phase reads at one column fall in
-// different banks (64-byte rows: (row / 2) % 4; 128-byte rows: row % 8).
+// different banks (32-byte rows: (row / 4) % 2; 64-byte rows: (row / 2) % 4; 128-byte rows: row % 8).
 template <int RB>
 __device__ __forceinline__ uint32_t swz(int row, int j) {
-  return (uint32_t)(row * RB + ((j ^ (RB == 64 ? (row >> 1) & 3 : row & 7)) << 4));
+  return (uint32_t)(row * RB + ((j ^ (RB == 32 ? (row >> 2) & 1 : RB == 64 ? (row >> 1) & 3 : row & 7)) << 4));
 }
 
 // 8-bit K word (dims 4c..4c+3 of one token, two's complement codes) -> two f16 pairs holding the
@@ -123,7 +131,7 @@ __device__ __forceinline__ void unpack4_s8_t(uint32_t w, uint32_t &d0, uint32_t 
 // (row, body token) this CTA computes and each row's int8 query scale go to a.cap_scores / a.cap_sq.
 template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED, bool CAP = false>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
-  constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = LAYOUT == KVQ_HAD_INT4;
+  constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = is_hadamard(LAYOUT), HAD2 = LAYOUT == KVQ_HAD_INT2;
   constexpr bool K8 = LAYOUT == KVQ_Q8_0, V8 = VLAYOUT == KVQ_Q8_0;   // 8-bit code planes
   constexpr int KRB = plane_row_bytes<LAYOUT>(), VRB = plane_row_bytes<VLAYOUT>();
   constexpr int SCB = scale_bytes<LAYOUT>(), OFF_V = off_v<LAYOUT, VLAYOUT>(), OFF_SK = off_sk<LAYOUT, VLAYOUT>();
@@ -303,6 +311,30 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     const bool live = g < R;
     row_alpha = (live ? a.scale * qsq[g] : 0.0f) * 16777216.0f * kLog2e;
     float qs = 0.0f;
+    if constexpr (HAD2) {
+      // 2-bit key codes: k-step 4 ch + k pairs dims (16c + k, 16c + 8 + k) and (16c + 4 + k,
+      // 16c + 12 + k) of the column block ch (dims 64 ch ..), whose fields sit at bits 2k of their
+      // bytes: the code operands are u * 4^k * 2^-24, so these query entries are divided by 4^k
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        float h[16];
+        const uint4 w16 = live ? *reinterpret_cast<const uint4 *>(qs8 + g * 128 + 64 * ch + 16 * c) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t wv[4] = {w16.x, w16.y, w16.z, w16.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          h[i] = (float)(int8_t)((wv[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+          qs += h[i];
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float f = 1.0f / (float)(1 << (2 * k));
+          bq_hi[4 * ch + k][0] = pack_f16x2(h[k] * f, h[8 + k] * f);
+          bq_hi[4 * ch + k][1] = pack_f16x2(h[4 + k] * f, h[12 + k] * f);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 4; ++b) qsum[b] = 0.0f;
+    } else {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
       float h[8];
@@ -319,6 +351,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         bq_hi[2 * b + st][1] = pack_f16x2(h[2 * st + 1] * 0.0625f, h[2 * st + 5] * 0.0625f);
       }
       qsum[b] = 0.0f;
+    }
     }
     qs += __shfl_xor_sync(0xffffffffu, qs, 1);
     qs += __shfl_xor_sync(0xffffffffu, qs, 2);
@@ -405,8 +438,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * 5.9604644775390625e-8f;
       zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * 5.9604644775390625e-8f;
       if (!ASYM) {
-        zq0[b] *= K8 ? -128.0f : -8.0f;
-        zq1[b] *= K8 ? -128.0f : -8.0f;
+        zq0[b] *= K8 ? -128.0f : (HAD2 ? -2.0f : -8.0f);
+        zq1[b] *= K8 ? -128.0f : (HAD2 ? -2.0f : -8.0f);
       }
     }
   }
@@ -447,7 +480,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       uint32_t kw[2][4];
       if constexpr (!K8) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < (HAD2 ? 1 : 2); ++half) {
           const int mi = lane >> 3;
           const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
           ldsm_x4(sK + swz<KRB>(row, 2 * half + (mi >> 1)), kw[half]);
@@ -457,6 +490,32 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         // one per-token scale: all 8 k-steps accumulate the exact integer dot (x 2^-24) in two
         // chains; score = alpha * s_q * s_k * dot
         float dA[4], dB[4];                              // the first mma of each chain takes its C operand
+        if constexpr (HAD2) {
+          // kw[0][2 ch] = token g, dims 64 ch + 16c .. +15 (field f at bits 2f); [2 ch + 1] = token
+          // g + 8. Bytes (0, 2) and (1, 3) go to the two f16 lanes; per k one lop3 keeps fields
+          // (k, 8 + k) or (4 + k, 12 + k) at bits 2k and flips their sign bit: u = code + 2 as the
+          // subnormal u * 4^k * 2^-24 (the query entries carry the 4^-k)
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const uint32_t wg = kw[0][2 * ch], w8 = kw[0][2 * ch + 1];
+            const uint32_t gA = prmt(wg, 0u, 0x4240u), gB = prmt(wg, 0u, 0x4341u);
+            const uint32_t eA = prmt(w8, 0u, 0x4240u), eB = prmt(w8, 0u, 0x4341u);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t m = 0x00030003u << (2 * k), x = 0x00020002u << (2 * k);
+              const uint32_t A[4] = {lop3<0x6a>(gA, m, x), lop3<0x6a>(eA, m, x), lop3<0x6a>(gB, m, x),
+                                     lop3<0x6a>(eB, m, x)};
+              const int ks = 4 * ch + k;
+              float(&d)[4] = (ks & 1) ? dB : dA;
+              if (ks == 0)
+                mma16816_c(d, A, bq_hi[0][0], bq_hi[0][1], zq0[0], zq1[0], zq0[0], zq1[0]);
+              else if (ks == 1)
+                mma16816_c(d, A, bq_hi[1][0], bq_hi[1][1], 0.0f, 0.0f, 0.0f, 0.0f);
+              else
+                mma16816(d, A, bq_hi[ks][0], bq_hi[ks][1]);
+            }
+          }
+        } else {
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
           uint32_t ug[4], u8[4];
@@ -472,6 +531,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           else
             mma16816(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1]);
           mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
+        }
         }
         if constexpr (CAP) {
           // the two chains hold the exact dot x 2^-24 (|dot| < 2^18): (dA + dB) x 2^24 is the integer
@@ -613,7 +673,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       uint32_t vw[2][4];
       if constexpr (!V8) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < (HAD2 ? 1 : 2); ++half) {
           const int mi = lane >> 3;
           const int row = tile * 16 + (mi & 1) * 8 + (lane & 7);
           ldsm_x4_t(sV + swz<VRB>(row, 2 * half + (mi >> 1)), vw[half]);
@@ -651,19 +711,45 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       // selection costs more registers than the fix-up saves.
       if (HAD) {
         const uint32_t Aw[4] = {0x3C003C00u, 0u, 0x3C003C00u, 0u};     // f16 1.0 pairs
+        if constexpr (HAD2) {
+          // vw[0][2 ch] = tokens (2c, 2c+1) of 16-bit unit g of column block ch (dims 64 ch + 8g ..
+          // +7, field f at bits 2f of each token's half), vw[0][2 ch + 1] = tokens (2c+8, 2c+9).
+          // One mma per field pair (f, f + 4): rows g and g + 8 of its A operand are dims
+          // 64 ch + 8g + f and + 4 as exact signed f16 codes (the field under the exponent of 1024
+          // with its sign bit flipped, then 1026 removed). No offset term: with u = code + 2 as a
+          // subnormal, the accumulator would hold about 2 sum(P') and the true sum only after
+          // subtracting 2 W, where the tensor core's truncated adds of the small P' lo products
+          // would show.
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const uint32_t v0 = vw[0][2 * ch], v1 = vw[0][2 * ch + 1];
+#pragma unroll
+            for (int f = 0; f < 4; ++f) {
+              const uint32_t A[4] = {
+                  hadd2(lop3<0x6a>(v0 >> (2 * f), 0x00030003u, 0x64026402u), 0xE402E402u),
+                  hadd2(lop3<0x6a>(v0 >> (8 + 2 * f), 0x00030003u, 0x64026402u), 0xE402E402u),
+                  hadd2(lop3<0x6a>(v1 >> (2 * f), 0x00030003u, 0x64026402u), 0xE402E402u),
+                  hadd2(lop3<0x6a>(v1 >> (8 + 2 * f), 0x00030003u, 0x64026402u), 0xE402E402u)};
+              float(&o)[4] = O[(4 * ch + f) >> 1][(4 * ch + f) & 1];
+              mma16816(o, A, bh0, bh1);
+              mma16816(o, A, bl0, bl1);
+            }
+          }
+        } else {
         mma16816(Dw, Aw, bh0, bh1);
         mma16816(Dw, Aw, bl0, bl1);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          uint32_t ua[4], ub[4];
-          unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 0], ua);
-          unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 1], ub);
-          const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};
-          const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};
-          mma16816(O[b][0], A0, bh0, bh1);
-          mma16816(O[b][0], A0, bl0, bl1);
-          mma16816(O[b][1], A1, bh0, bh1);
-          mma16816(O[b][1], A1, bl0, bl1);
+          for (int b = 0; b < 4; ++b) {
+            uint32_t ua[4], ub[4];
+            unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 0], ua);
+            unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+            const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};
+            const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};
+            mma16816(O[b][0], A0, bh0, bh1);
+            mma16816(O[b][0], A0, bl0, bl1);
+            mma16816(O[b][1], A1, bh0, bh1);
+            mma16816(O[b][1], A1, bl0, bl1);
+          }
         }
         continue;
       }
@@ -757,8 +843,21 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   constexpr bool SUBV = HAD || ASYM;
   constexpr float kWf = ASYM ? 1.0f : -8.0f;
   constexpr float se = SUBV ? 16777216.0f : 1.0f, so = SUBV ? 1048576.0f : 1.0f;
+  if constexpr (HAD2) {
+    // accumulator j = 4 ch + f: dims 64 ch + 8g + f (values 0, 1: rows r0, r1) and + 4 (2, 3), the
+    // codes entered as exact signed values
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
+    for (int j = 0; j < 8; ++j) {
+      const int da = 64 * (j >> 2) + 8 * g + (j & 3), db = da + 4;
+      const float(&o)[4] = O[j >> 1][j & 1];
+      co[(warp * 8 + r0) * kD + da] = o[0];
+      co[(warp * 8 + r1) * kD + da] = o[1];
+      co[(warp * 8 + r0) * kD + db] = o[2];
+      co[(warp * 8 + r1) * kD + db] = o[3];
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < (HAD2 ? 0 : 4); ++b) {
     float w0 = 0.0f, w1 = 0.0f;
     if (SUBV) {
       w0 = kWf * __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);   // (block b, row r0)
@@ -839,7 +938,7 @@ bool mma_supported(const AttendArgs &a) {
 
 cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
   if (prefill_supported(a)) return launch_attend_prefill(a, st);
-  if (a.cap_scores && a.cache.layout != KVQ_HAD_INT4) return cudaErrorNotSupported;
+  if (a.cap_scores && !is_hadamard(a.cache.layout)) return cudaErrorNotSupported;
   if (uses_mma4(a.cache.layout)) return launch_attend_mma4(a, st);
   const bool paged = a.cache.page_shift >= 0;
   const int L = a.cache.layout, VL = a.cache.v_layout;
@@ -848,6 +947,11 @@ cudaError_t launch_attend_mma(const AttendArgs &a, cudaStream_t st) {
     if (a.cap_scores) return paged ? cudaErrorNotSupported : launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, false, true>(a, st);
     return paged ? launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, true>(a, st)
                  : launch_t<KVQ_HAD_INT4, KVQ_HAD_INT4, false, false>(a, st);
+  }
+  if (L == KVQ_HAD_INT2) {
+    if (a.cap_scores) return paged ? cudaErrorNotSupported : launch_t<KVQ_HAD_INT2, KVQ_HAD_INT2, false, false, true>(a, st);
+    return paged ? launch_t<KVQ_HAD_INT2, KVQ_HAD_INT2, false, true>(a, st)
+                 : launch_t<KVQ_HAD_INT2, KVQ_HAD_INT2, false, false>(a, st);
   }
   if (L == KVQ_Q4_0 && VL == KVQ_Q4_0) return launch_pair_t<KVQ_Q4_0, KVQ_Q4_0>(a, st);
   if (L == KVQ_Q8_0 && VL == KVQ_Q8_0) return launch_pair_t<KVQ_Q8_0, KVQ_Q8_0>(a, st);

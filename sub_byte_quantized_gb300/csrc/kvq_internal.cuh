@@ -64,8 +64,8 @@ __host__ __device__ constexpr bool prefill_pair(int kl, int vl) {
 // Pairs with a decode kernel of their own (at most eight query rows per kv head; Q6_0: its kernel
 // takes groups of four rows).
 __host__ __device__ constexpr bool decode_kernel(int kl, int vl) {
-  return (kl == vl && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32 || kl == KVQ_HAD_INT4 || kl == KVQ_Q8_0 ||
-                       kl == KVQ_Q6_0)) ||
+  return (kl == vl && (kl == KVQ_Q4_0 || kl == KVQ_ASYM4_G32 || kl == KVQ_HAD_INT4 || kl == KVQ_HAD_INT2 ||
+                       kl == KVQ_Q8_0 || kl == KVQ_Q6_0)) ||
          (kl == KVQ_Q4_0 && vl == KVQ_Q8_0);
 }
 // The row-side kernel takes many query rows per kv head, and every row count of the pairs that
