@@ -1,8 +1,7 @@
 // Tensor-core phase 1 of the split-K decode attention for the block layouts with 4- and 8-bit
-// codes (Q4_0, Q8_0, Q4_0 keys with Q8_0 values, the asymmetric g=32 layout) and the per-token
-// Hadamard int4 and int2 bodies, head_dim 128, up to 8 query rows per kv head (the GQA group times
-// the query rows of the call). For the Hadamard layouts the exact-f32 recent window is scored in
-// phase 2.
+// codes (Q4_0, Q8_0, Q4_0 keys with Q8_0 values) and the per-token Hadamard int4 and int2
+// bodies, head_dim 128, up to 8 query rows per kv head (the GQA group times the query rows of the
+// call). For the Hadamard layouts the exact-f32 recent window is scored in phase 2.
 //
 // Why tensor cores: every kv head is shared by gqa query heads, so per packed K/V element the
 // step does 4*gqa flops (QK and PV); at gqa 8 that is ~57 flops per packed byte, beyond what
@@ -23,10 +22,10 @@
 // the ldmatrix reads (8 rows x 16 bytes per phase) are bank-conflict free. ldmatrix gives each
 // lane the code words of its fragment: plain for K (one token, 8 consecutive dims of 4-bit codes
 // or 4 of 8-bit codes), transposed for V (two tokens, 4 consecutive dims of 4-bit codes or 2 of
-// 8-bit codes). K codes (and the Hadamard and asymmetric V nibbles) become exact subnormal f16
-// values u * 2^-24 of the offset code u (one lop3 per nibble pair; one byte permute per 8-bit
-// pair), the offset going into the accumulator's initial value or a separate term; Q4_0 and Q8_0
-// V codes become exact signed f16 values (the code under the exponent of 1024, one f16 add).
+// 8-bit codes). K codes become exact subnormal f16 values u * 2^-24 of the offset code u (one
+// lop3 per nibble pair; one byte permute per 8-bit pair), the offset going into the
+// accumulator's initial value; V codes become exact signed f16 values (the code under the
+// exponent of 1024, one f16 add), so that the long PV accumulation carries no offset mass.
 //
 // Hadamard int2 (32-byte rows, value f of a byte at bits 2f): one ldmatrix gives a lane 16
 // consecutive dims of a token per word; two byte permutes split a word into two f16 lanes and one
@@ -67,8 +66,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Stage buffer: K payload, V payload (swizzled rows of 64 bytes for 4-bit codes, 128 bytes for
-// Q8_0), K and V scales (4 f16 per token, or one f32 per token for the Hadamard layout),
-// asymmetric zero-points (4 f16 per token).
+// Q8_0, 32 bytes for Hadamard int2), K and V scales (4 f16 per token, or one f32 per token for the
+// Hadamard layouts).
 template <int L>
 __host__ __device__ constexpr int plane_row_bytes() { return L == KVQ_Q8_0 ? 128 : (L == KVQ_HAD_INT2 ? 32 : 64); }
 template <int L>
@@ -80,13 +79,7 @@ __host__ __device__ constexpr int off_sk() { return off_v<L, VL>() + kStage * pl
 template <int L, int VL>
 __host__ __device__ constexpr int off_sv() { return off_sk<L, VL>() + kStage * scale_bytes<L>(); }
 template <int L, int VL>
-__host__ __device__ constexpr int off_zk() { return off_sv<L, VL>() + kStage * scale_bytes<VL>(); }
-template <int L, int VL>
-__host__ __device__ constexpr int off_zv() { return off_zk<L, VL>() + kStage * 8; }
-template <int L, int VL>
-__host__ __device__ constexpr int stage_bytes() {
-  return L == KVQ_ASYM4_G32 ? off_zv<L, VL>() + kStage * 8 : off_zk<L, VL>();
-}
+__host__ __device__ constexpr int stage_bytes() { return off_sv<L, VL>() + kStage * scale_bytes<VL>(); }
 // Hadamard: per-warp scratch for the int8 query codes of up to 8 rows and their scales
 constexpr int kQScratch = 8 * 128 + 8 * 4;
 template <int L, int VL>
@@ -131,12 +124,12 @@ __device__ __forceinline__ void unpack4_s8_t(uint32_t w, uint32_t &d0, uint32_t 
 // (row, body token) this CTA computes and each row's int8 query scale go to a.cap_scores / a.cap_sq.
 template <int LAYOUT, int VLAYOUT, bool QSPLIT, bool PAGED, bool CAP = false>
 __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(AttendArgs a) {
-  constexpr bool ASYM = LAYOUT == KVQ_ASYM4_G32, HAD = is_hadamard(LAYOUT), HAD2 = LAYOUT == KVQ_HAD_INT2;
+  constexpr bool HAD = is_hadamard(LAYOUT), HAD2 = LAYOUT == KVQ_HAD_INT2;
+  static_assert(LAYOUT != KVQ_ASYM4_G32 && VLAYOUT != KVQ_ASYM4_G32, "the asymmetric layout has its own kernel");
   constexpr bool K8 = LAYOUT == KVQ_Q8_0, V8 = VLAYOUT == KVQ_Q8_0;   // 8-bit code planes
   constexpr int KRB = plane_row_bytes<LAYOUT>(), VRB = plane_row_bytes<VLAYOUT>();
   constexpr int SCB = scale_bytes<LAYOUT>(), OFF_V = off_v<LAYOUT, VLAYOUT>(), OFF_SK = off_sk<LAYOUT, VLAYOUT>();
-  constexpr int OFF_SV = off_sv<LAYOUT, VLAYOUT>(), OFF_ZK = off_zk<LAYOUT, VLAYOUT>();
-  constexpr int OFF_ZV = off_zv<LAYOUT, VLAYOUT>(), STAGE_BYTES = stage_bytes<LAYOUT, VLAYOUT>();
+  constexpr int OFF_SV = off_sv<LAYOUT, VLAYOUT>(), STAGE_BYTES = stage_bytes<LAYOUT, VLAYOUT>();
   static_assert(VLAYOUT == LAYOUT || (LAYOUT == KVQ_Q4_0 && VLAYOUT == KVQ_Q8_0), "supported plane pairs");
   static_assert(!CAP || (HAD && !PAGED), "score capture: Hadamard layout, contiguous cache");
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -178,8 +171,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const uint8_t *kp0 = cv.payload[0] + head_row0 * KRB, *vp0 = cv.payload[1] + head_row0 * VRB;
   const uint8_t *ksc0 = static_cast<const uint8_t *>(cv.scale[0]) + head_row0 * SCB;
   const uint8_t *vsc0 = static_cast<const uint8_t *>(cv.scale[1]) + head_row0 * SCB;
-  const __half *kz0 = ASYM ? cv.zero[0] + head_row0 * 4 : nullptr;
-  const __half *vz0 = ASYM ? cv.zero[1] + head_row0 * 4 : nullptr;
 
   auto issue = [&](int i) {
     if (i < n_mine) {
@@ -187,17 +178,13 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       // the stage's rows are consecutive plane rows (a page holds at least 64 aligned tokens)
       size_t r0 = (size_t)ts;                             // row offset from the base pointers
       const uint8_t *kb = kp0, *vb = vp0, *ksb = ksc0, *vsb = vsc0;
-      const __half *kzb = kz0, *vzb = vz0;
       if constexpr (PAGED) {
         r0 = cache_row_paged(cv, bb, kvh, ts);
         kb = cv.payload[0]; vb = cv.payload[1];
         ksb = static_cast<const uint8_t *>(cv.scale[0]); vsb = static_cast<const uint8_t *>(cv.scale[1]);
-        kzb = cv.zero[0]; vzb = cv.zero[1];
       }
       const uint8_t *kp = kb + r0 * KRB, *vp = vb + r0 * VRB;
       const uint8_t *ksc = ksb + r0 * SCB, *vsc = vsb + r0 * SCB;
-      const __half *kz = ASYM ? kzb + r0 * 4 : nullptr;
-      const __half *vz = ASYM ? vzb + r0 * 4 : nullptr;
       uint8_t *sb = wbuf + (i % kRing) * STAGE_BYTES;
       const uint32_t sK = smem_addr(sb), sV = smem_addr(sb + OFF_V);
       if (ts + kStage <= t_end) {                        // full stage: no per-row bounds
@@ -229,10 +216,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           const size_t tok = (size_t)row;
           cp_async_scale<SCB>(smem_addr(sb + OFF_SK + row * SCB), ksc + tok * SCB, SCB);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, SCB);
-          if (ASYM) {
-            cp_async8(smem_addr(sb + OFF_ZK + row * 8), kz + tok * 4, 8);
-            cp_async8(smem_addr(sb + OFF_ZV + row * 8), vz + tok * 4, 8);
-          }
         }
       } else {                                           // tail stage: rows past t_end are zero-filled
         if constexpr (KRB == VRB) {
@@ -270,10 +253,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
           const size_t tok = (size_t)(ok ? row : 0);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SK + row * SCB), ksc + tok * SCB, ok ? SCB : 0);
           cp_async_scale<SCB>(smem_addr(sb + OFF_SV + row * SCB), vsc + tok * SCB, ok ? SCB : 0);
-          if (ASYM) {
-            cp_async8(smem_addr(sb + OFF_ZK + row * 8), kz + tok * 4, ok ? 8 : 0);
-            cp_async8(smem_addr(sb + OFF_ZV + row * 8), vz + tok * 4, ok ? 8 : 0);
-          }
         }
       }
     }
@@ -428,36 +407,22 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   const int r0 = 2 * c, r1 = 2 * c + 1;
   const float alpha0 = __shfl_sync(0xffffffffu, row_alpha, r0 * 4);
   const float alpha1 = __shfl_sync(0xffffffffu, row_alpha, r1 * 4);
-  // zq: per-block row sums of q in accumulator units (x 2^-24). ASYM: multiplied by each token's
-  // zero-point; Q4_0 / Q8_0: -8 zq / -128 zq is the accumulator's initial value (the codes enter
-  // as code + 8 / code + 128).
+  // zq: per-block row sums of q in accumulator units (x 2^-24) times minus the code offset
+  // (Q4_0 / Hadamard int4: 8, Q8_0: 128, Hadamard int2: 2), the accumulator's initial value (the
+  // K codes enter as code + offset).
   float zq0[4], zq1[4];
   {
+    constexpr float kOff = K8 ? -128.0f : (HAD2 ? -2.0f : -8.0f);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * 5.9604644775390625e-8f;
-      zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * 5.9604644775390625e-8f;
-      if (!ASYM) {
-        zq0[b] *= K8 ? -128.0f : (HAD2 ? -2.0f : -8.0f);
-        zq1[b] *= K8 ? -128.0f : (HAD2 ? -2.0f : -8.0f);
-      }
+      zq0[b] = __shfl_sync(0xffffffffu, qsum[b], r0 * 4) * (5.9604644775390625e-8f * kOff);
+      zq1[b] = __shfl_sync(0xffffffffu, qsum[b], r1 * 4) * (5.9604644775390625e-8f * kOff);
     }
   }
-
-
-
-
   const int lim0 = r0 < R ? row_limit_of(a, sl, r0) : -1;
   const int lim1 = r1 < R ? row_limit_of(a, sl, r1) : -1;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   float O[4][2][4];                                      // [block][half][c0..c3]
-  // Dw[b][r] = sum_t P'_t * f[t][b], the V offset term (asymmetric: f = z_v, with P' = p;
-  // Hadamard: f = 1, with P' = p s_v, where all rows hold the same sum), from a small extra mma
-  // per tile: rows 0-3 of its accumulator are the four blocks (held by lanes with g < 4),
-  // columns the query rows.
-  float Dw[4] = {0.f, 0.f, 0.f, 0.f};
-  // selector pairing halfword (g & 1) of two words, and which word (g < 2: blocks 0,1)
-  const uint32_t wsel = (g & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
   for (int b = 0; b < 4; ++b) {
 #pragma unroll
@@ -556,15 +521,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
       const float2 s801 = __half22float2(u32_as_h2(skg8.x)), s823 = __half22float2(u32_as_h2(skg8.y));
       const float skg_f[4] = {sg01.x, sg01.y, sg23.x, sg23.y};
       const float skg8_f[4] = {s801.x, s801.y, s823.x, s823.y};
-      float zg_f[4], zg8_f[4];
-      if (ASYM) {
-        const uint2 zg = *reinterpret_cast<const uint2 *>(sb + OFF_ZK + (tile * 16 + g) * 8);
-        const uint2 zg8 = *reinterpret_cast<const uint2 *>(sb + OFF_ZK + (tile * 16 + g + 8) * 8);
-        const float2 a01 = __half22float2(u32_as_h2(zg.x)), a23 = __half22float2(u32_as_h2(zg.y));
-        const float2 b01 = __half22float2(u32_as_h2(zg8.x)), b23 = __half22float2(u32_as_h2(zg8.y));
-        zg_f[0] = a01.x; zg_f[1] = a01.y; zg_f[2] = a23.x; zg_f[3] = a23.y;
-        zg8_f[0] = b01.x; zg8_f[1] = b01.y; zg8_f[2] = b23.x; zg8_f[3] = b23.y;
-      }
       float acc_s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
@@ -582,15 +538,14 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         } else {
           // kw[b/2][(b%2)*2 + 0] = (token g, block b); [.. + 1] = (token g+8, block b)
           uint32_t ug[4], u8[4];
-          unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 0], ug);
-          unpack8_sub<ASYM>(kw[b >> 1][(b & 1) * 2 + 1], u8);
+          unpack8_sub<false>(kw[b >> 1][(b & 1) * 2 + 0], ug);
+          unpack8_sub<false>(kw[b >> 1][(b & 1) * 2 + 1], u8);
           A0[0] = ug[0]; A0[1] = u8[0]; A0[2] = ug[1]; A0[3] = u8[1];
           A1[0] = ug[2]; A1[1] = u8[2]; A1[2] = ug[3]; A1[3] = u8[3];
         }
-        // the first mma takes the offset (ASYM: zero) as its separate C operand: no register copies
+        // the first mma takes the offset as its separate C operand: no register copies
         float d[4];
-        const float c0 = ASYM ? 0.0f : zq0[b], c1 = ASYM ? 0.0f : zq1[b];
-        mma16816_c(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1], c0, c1, c0, c1);
+        mma16816_c(d, A0, bq_hi[2 * b][0], bq_hi[2 * b][1], zq0[b], zq1[b], zq0[b], zq1[b]);
         mma16816(d, A1, bq_hi[2 * b + 1][0], bq_hi[2 * b + 1][1]);
         if (QSPLIT) {
           mma16816(d, A0, bq_lo[2 * b][0], bq_lo[2 * b][1]);
@@ -600,12 +555,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         acc_s[1] = fmaf(skg_f[b], d[1], acc_s[1]);
         acc_s[2] = fmaf(skg8_f[b], d[2], acc_s[2]);
         acc_s[3] = fmaf(skg8_f[b], d[3], acc_s[3]);
-        if (ASYM) {
-          acc_s[0] = fmaf(zg_f[b], zq0[b], acc_s[0]);
-          acc_s[1] = fmaf(zg_f[b], zq1[b], acc_s[1]);
-          acc_s[2] = fmaf(zg8_f[b], zq0[b], acc_s[2]);
-          acc_s[3] = fmaf(zg8_f[b], zq1[b], acc_s[3]);
-        }
       }
       s[tile][0] = acc_s[0] * alpha0;
       s[tile][1] = acc_s[1] * alpha1;
@@ -644,8 +593,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     l1 *= corr1;
     // once the running maxima settle, corr is exactly 1 for every row: skip the rescale
     if (__any_sync(0xffffffffu, corr0 != 1.0f || corr1 != 1.0f)) {
-      Dw[0] *= corr0;
-      Dw[1] *= corr1;
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
 #pragma unroll
@@ -701,16 +648,12 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         bl0 = movm_t(l01);
         bl1 = movm_t(l23);
       }
-      // Hadamard and asymmetric V codes enter as exact subnormals u * 2^-24 (Hadamard: u = code + 8),
-      // so every output needs an offset sum_t P'_t * f_t per 32-dim block and query row, with
-      // f = -8 (Hadamard; s_v is already in P') or z_v (asymmetric). It comes from one small mma
-      // per tile: rows g < 4 of its A operand hold block g's factor for tokens (2c, 2c+1) and
-      // (2c+8, 2c+9) (rows 4-7 are don't-care outputs, rows 8-15 zero), the B operand is the p
-      // split already made; the -8 is applied in the epilogue. Q4_0 V codes become exact signed
-      // f16 values instead (lop3 + one f16 fix-up per pair): on that path the W mma's operand
-      // selection costs more registers than the fix-up saves.
+      // Hadamard V codes (s_v already in P') enter as exact signed f16 values (lop3 + one f16
+      // fix-up per pair), like the Q4_0 and Q8_0 codes. An offset form (u = code + 8 as a
+      // subnormal, with -8 sum_t P'_t added at the end) is a little cheaper, but its accumulator
+      // holds about 8 sum_t P'_t, and the tensor core's truncated adds of the small P' lo
+      // products against it cost about 20x the error of the signed form.
       if (HAD) {
-        const uint32_t Aw[4] = {0x3C003C00u, 0u, 0x3C003C00u, 0u};     // f16 1.0 pairs
         if constexpr (HAD2) {
           // vw[0][2 ch] = tokens (2c, 2c+1) of 16-bit unit g of column block ch (dims 64 ch + 8g ..
           // +7, field f at bits 2f of each token's half), vw[0][2 ch + 1] = tokens (2c+8, 2c+9).
@@ -736,13 +679,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
             }
           }
         } else {
-        mma16816(Dw, Aw, bh0, bh1);
-        mma16816(Dw, Aw, bl0, bl1);
 #pragma unroll
           for (int b = 0; b < 4; ++b) {
             uint32_t ua[4], ub[4];
-            unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 0], ua);
-            unpack8_sub<false>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+            unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
+            unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
             const uint32_t A0[4] = {ua[0], ua[1], ub[0], ub[1]};
             const uint32_t A1[4] = {ua[2], ua[3], ub[2], ub[3]};
             mma16816(O[b][0], A0, bh0, bh1);
@@ -763,19 +704,6 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
                                __byte_perm(sa.y, sbv.y, 0x5410), __byte_perm(sa.y, sbv.y, 0x7632)};
       const uint32_t sp1[4] = {__byte_perm(sc.x, sd.x, 0x5410), __byte_perm(sc.x, sd.x, 0x7632),
                                __byte_perm(sc.y, sd.y, 0x5410), __byte_perm(sc.y, sd.y, 0x7632)};
-      if (ASYM) {                                        // W operand: the V zero-points
-        const uint8_t *zvb = sb + OFF_ZV + tile * 16 * 8;
-        const uint2 wa = *reinterpret_cast<const uint2 *>(zvb + (2 * c) * 8);
-        const uint2 wb = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 1) * 8);
-        const uint2 wc = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 8) * 8);
-        const uint2 wd = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 9) * 8);
-        const bool lo2 = (g & 2) == 0;
-        const uint32_t w0 = __byte_perm(lo2 ? wa.x : wa.y, lo2 ? wb.x : wb.y, wsel);
-        const uint32_t w1 = __byte_perm(lo2 ? wc.x : wc.y, lo2 ? wd.x : wd.y, wsel);
-        const uint32_t Aw[4] = {w0, 0u, w1, 0u};
-        mma16816(Dw, Aw, bh0, bh1);
-        mma16816(Dw, Aw, bl0, bl1);
-      }
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
         // P' = (p_hi + p_lo) * s_v split into hi + lo f16 exactly enough (TwoProduct with f16 fma):
@@ -798,13 +726,8 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
         } else {
           // vw[b/2][(b%2)*2 + 0] = tokens (2c, 2c+1) of block b; [.. + 1] = tokens (2c+8, 2c+9)
           uint32_t ua[4], ub[4];
-          if (ASYM) {
-            unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 0], ua);
-            unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 1], ub);
-          } else {
-            unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
-            unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
-          }
+          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
+          unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
           A0[0] = ua[0]; A0[1] = ua[1]; A0[2] = ub[0]; A0[3] = ub[1];   // dims 4g+0 (row g), 4g+1 (row g+8)
           A1[0] = ua[2]; A1[1] = ua[3]; A1[2] = ub[2]; A1[3] = ub[3];   // dims 4g+2, 4g+3
         }
@@ -837,12 +760,7 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
     cl[warp * 8 + r0] = l0;
     cl[warp * 8 + r1] = l1;
   }
-  // Q4_0: O holds the values directly. Hadamard / asymmetric: the V codes entered as u * 2^-24
-  // (even dims, low fields) or 16 u * 2^-24 (odd dims, high fields); the offset term (-8 x the
-  // W sums, or + the zero-point sums) completes each value.
-  constexpr bool SUBV = HAD || ASYM;
-  constexpr float kWf = ASYM ? 1.0f : -8.0f;
-  constexpr float se = SUBV ? 16777216.0f : 1.0f, so = SUBV ? 1048576.0f : 1.0f;
+  // O holds the values directly (the V codes entered as exact signed values)
   if constexpr (HAD2) {
     // accumulator j = 4 ch + f: dims 64 ch + 8g + f (values 0, 1: rows r0, r1) and + 4 (2, 3), the
     // codes entered as exact signed values
@@ -858,18 +776,11 @@ __global__ void __launch_bounds__(kWarps * 32, kMinBlocks) attend_mma_kernel(Att
   }
 #pragma unroll
   for (int b = 0; b < (HAD2 ? 0 : 4); ++b) {
-    float w0 = 0.0f, w1 = 0.0f;
-    if (SUBV) {
-      w0 = kWf * __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);   // (block b, row r0)
-      w1 = kWf * __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);   // (block b, row r1)
-    }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int d = V8 ? 32 * b + 16 * h + 2 * g : 32 * b + 4 * g + 2 * h;
-      *reinterpret_cast<float2 *>(co + (warp * 8 + r0) * kD + d) =
-          make_float2(fmaf(O[b][h][0], se, w0), fmaf(O[b][h][2], so, w0));
-      *reinterpret_cast<float2 *>(co + (warp * 8 + r1) * kD + d) =
-          make_float2(fmaf(O[b][h][1], se, w1), fmaf(O[b][h][3], so, w1));
+      *reinterpret_cast<float2 *>(co + (warp * 8 + r0) * kD + d) = make_float2(O[b][h][0], O[b][h][2]);
+      *reinterpret_cast<float2 *>(co + (warp * 8 + r1) * kD + d) = make_float2(O[b][h][1], O[b][h][3]);
     }
   }
   __syncthreads();

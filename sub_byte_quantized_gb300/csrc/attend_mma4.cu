@@ -5,8 +5,8 @@
 //   QK:  S^T[16 tokens][8 rows] += K[16 tokens][16 dims] . Q^T[16 dims][8 rows]
 //   PV:  O^T[16 dims][8 rows]   += V^T[16 dims][16 tokens] . P'^T[16 tokens][8 rows]
 // with the codes as exact f16 operands (K as subnormals u * 2^-24 with the offset in the
-// accumulator's initial value; Q4_0 and Hadamard V by the exact f16 fix-up; asymmetric V as
-// subnormals plus one zero-point mma), exact query operands (power-of-two prescale, hi + lo parts
+// accumulator's initial value; V by the exact f16 fix-up: asymmetric V as n - 8, the group's
+// midpoint z + 8 s coming from one small mma per tile), exact query operands (power-of-two prescale, hi + lo parts
 // for f32 queries; int8 codes for the Hadamard layout) and P' = p * s_v kept as f16 hi + lo parts.
 //
 // Work split: a CTA of eight warps streams one chunk in 128-token stages. Warps 0-3 ("K warps") each
@@ -437,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
   } else {
     // =============================== V warps: O^T += V^T . P'^T per 32-dim block
     float O[4][2][4];
-    // ASYM: Dw[b][r] = sum_t p_t z_v[t][b] (the zero-point term) from one small mma per tile
+    // ASYM: Dw[b][r] (+ Dw[b + 8][r]) = sum_t p_t x[t][b], x = z_v + 8 s_v the group midpoint
+    // (hi part in rows b, lo part in rows b + 8), from one small mma per tile
     float Dw[4] = {0.f, 0.f, 0.f, 0.f};
     const uint32_t wsel = (g & 1) ? 0x7632u : 0x5410u;
 #pragma unroll
@@ -465,6 +466,8 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
       if (__any_sync(0xffffffffu, cr.x != 1.0f || cr.y != 1.0f)) {
         Dw[0] *= cr.x;
         Dw[1] *= cr.y;
+        Dw[2] *= cr.x;
+        Dw[3] *= cr.y;
 #pragma unroll
         for (int b = 0; b < 4; ++b)
 #pragma unroll
@@ -508,17 +511,26 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
       const uint32_t sp1[4] = {__byte_perm(sc.x, sd.x, 0x5410), __byte_perm(sc.x, sd.x, 0x7632),
                                __byte_perm(sc.y, sd.y, 0x5410), __byte_perm(sc.y, sd.y, 0x7632)};
       if (ASYM) {
-        // W operand (zero-points): rows g < 4 hold block g's z_v for tokens (2c, 2c+1), (2c+8, 2c+9)
+        // W operand (group midpoints): rows g < 4 hold the hi part of block g's x = z_v + 8 s_v for
+        // tokens (2c, 2c+1), (2c+8, 2c+9), rows g + 8 its lo part. With the codes centred (n - 8)
+        // neither the O accumulators nor this one carry an offset mass: an offset form (codes n,
+        // zero-point z_v) adds two large sums that cancel, and the tensor core's truncated adds of
+        // the small p lo products against them cost about 15x the error of this form.
         const uint8_t *zvb = sb + G::OFF_X2 + trow * 8;
         const uint2 wa = *reinterpret_cast<const uint2 *>(zvb + (2 * c) * 8);
         const uint2 wb = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 1) * 8);
         const uint2 wc = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 8) * 8);
         const uint2 wd = *reinterpret_cast<const uint2 *>(zvb + (2 * c + 9) * 8);
         const bool lo2 = g < 2;
-        uint32_t w0 = __byte_perm(lo2 ? wa.x : wa.y, lo2 ? wb.x : wb.y, wsel);
-        uint32_t w1 = __byte_perm(lo2 ? wc.x : wc.y, lo2 ? wd.x : wd.y, wsel);
-        if (g >= 4) w0 = w1 = 0u;
-        const uint32_t Aw[4] = {w0, 0u, w1, 0u};
+        const uint32_t z0 = __byte_perm(lo2 ? wa.x : wa.y, lo2 ? wb.x : wb.y, wsel);
+        const uint32_t z1 = __byte_perm(lo2 ? wc.x : wc.y, lo2 ? wd.x : wd.y, wsel);
+        const uint32_t s0 = __byte_perm(lo2 ? sa.x : sa.y, lo2 ? sbv.x : sbv.y, wsel);
+        const uint32_t s1 = __byte_perm(lo2 ? sc.x : sc.y, lo2 ? sd.x : sd.y, wsel);
+        uint32_t h0, l0, h1, l1;
+        midpoint_split(z0, s0, h0, l0);
+        midpoint_split(z1, s1, h1, l1);
+        if (g >= 4) h0 = l0 = h1 = l1 = 0u;
+        const uint32_t Aw[4] = {h0, l0, h1, l1};
         mma16816(Dw, Aw, pb.x, pb.y);
         mma16816(Dw, Aw, pb.z, pb.w);
       }
@@ -531,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
         const uint32_t lo0 = hfma2(pb.z, sp0[b], e0), lo1 = hfma2(pb.w, sp1[b], e1);
         uint32_t ua[4], ub[4];
         if (ASYM) {
-          unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 0], ua);
-          unpack8_sub<true>(vw[b >> 1][(b & 1) * 2 + 1], ub);
+          unpack8_u4m8(vw[b >> 1][(b & 1) * 2 + 0], ua);
+          unpack8_u4m8(vw[b >> 1][(b & 1) * 2 + 1], ub);
         } else {
           unpack8_q4(vw[b >> 1][(b & 1) * 2 + 0], ua);
           unpack8_q4(vw[b >> 1][(b & 1) * 2 + 1], ub);
@@ -548,25 +560,21 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
     }
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     __syncthreads();                                     // every warp is done with the rings
-    // Q4_0 / Hadamard: O holds the values. Asymmetric: codes entered as u * 2^-24 (even dims) or
-    // 16 u * 2^-24 (odd dims); value = u s_v + z_v adds the W term.
+    // O holds s_v * code (asymmetric: s_v (n - 8)); asymmetric values add the midpoint term,
+    // s_v n + z_v = s_v (n - 8) + (z_v + 8 s_v).
     float *co = reinterpret_cast<float *>(smem) + 64;    // [tile][8][128] after cm/cl
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      float w0 = 0.0f, w1 = 0.0f, se = 1.0f, so = 1.0f;
+      float w0 = 0.0f, w1 = 0.0f;
       if (ASYM) {
-        w0 = __shfl_sync(0xffffffffu, Dw[0], 4 * b + c);
-        w1 = __shfl_sync(0xffffffffu, Dw[1], 4 * b + c);
-        se = 16777216.0f;
-        so = 1048576.0f;
+        w0 = __shfl_sync(0xffffffffu, Dw[0] + Dw[2], 4 * b + c);
+        w1 = __shfl_sync(0xffffffffu, Dw[1] + Dw[3], 4 * b + c);
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int d = 32 * b + 4 * g + 2 * h;
-        *reinterpret_cast<float2 *>(co + (tw * 8 + r0) * kD + d) =
-            make_float2(fmaf(O[b][h][0], se, w0), fmaf(O[b][h][2], so, w0));
-        *reinterpret_cast<float2 *>(co + (tw * 8 + r1) * kD + d) =
-            make_float2(fmaf(O[b][h][1], se, w1), fmaf(O[b][h][3], so, w1));
+        *reinterpret_cast<float2 *>(co + (tw * 8 + r0) * kD + d) = make_float2(O[b][h][0] + w0, O[b][h][2] + w0);
+        *reinterpret_cast<float2 *>(co + (tw * 8 + r1) * kD + d) = make_float2(O[b][h][1] + w1, O[b][h][3] + w1);
       }
     }
   }

@@ -16,11 +16,12 @@
 // Q4_0 / asymmetric: the per-block scale varies along the contracted dims, so the stage is
 // unpacked into code * scale itself, split exactly into f16 hi + lo tiles (at most 15 significant
 // bits): S = Q . (K_hi + K_lo)^T with the query exact in f16 after a per-row power-of-two
-// prescale, and O += P_hi . V_hi + P_hi . V_lo + P_lo . V_hi. The asymmetric zero-point z[t][b]
-// of each 32-dim block b is kept out of the tiles (the f16 sum code * scale + z is not exact):
-// S += Qsum . Z_K^T with the per-row block sums of the prescaled query (f16 hi + lo, one
-// m16n8k8 per 8-token tile) and Oz += P . Z_V into four per-block columns that are added to the
-// block's output dims at the end.
+// prescale, and O += P_hi . V_hi + P_hi . V_lo + P_lo . V_hi. Asymmetric: the tiles hold the
+// values v = s n + z themselves, formed in f32 and split into f16 hi + lo parts (|error| below
+// 2^-23 |v|, not exact like code * scale). Keeping z out of the tiles in extra mma terms would
+// be exact per element, but in a block with an outlier dim (z far from the other dims' values)
+// the code and zero-point sums are large and cancel, and the tensor core's truncated
+// accumulation over the chunk shows in the difference.
 // The probabilities stay in registers between the two products: the S accumulator of two
 // 8-token tiles is the A fragment of one 16-token PV step.
 //
@@ -76,7 +77,7 @@ struct PlaneL {
 // Shared memory of a (K layout, V layout) pair: a ring of raw stage slots (payload rows, scales,
 // zero-points), then one region that first holds the query rows (prologue) and then the f16
 // tiles of the unpacked stage (K, V; for block layouts also the K and V lo parts), then the
-// per-row alpha factors and (asymmetric K) the query block sums. Three ring slots when they fit
+// per-row alpha factors. Three ring slots when they fit
 // the CTAs-per-SM budget, else two.
 template <int KL, int VL>
 struct PGeo {
@@ -96,7 +97,7 @@ struct PGeo {
   static constexpr int QB = HAD ? kD : 2 * kD;           // query bytes per row: int8 codes / prescaled f16
   static constexpr int REG_T = NT * kTile, REG_Q = kRows * QB, REG_W = HAD ? kRows * kQrPitch : 0;
   static constexpr int REGION = REG_T > REG_Q ? (REG_T > REG_W ? REG_T : REG_W) : (REG_Q > REG_W ? REG_Q : REG_W);
-  static constexpr int TAIL = kRows * 4 + (K::ASYM ? kRows * 16 : 0);
+  static constexpr int TAIL = kRows * 4;
   static constexpr int CTAS = HAD ? kPrefillCtasPerSm : 2;
   static constexpr int BUDGET = (233472 - 1024 * CTAS) / CTAS;   // 228 KB per SM, 1 KB reserved per CTA
   static constexpr int RING = 3 * SLOT + REGION + TAIL <= BUDGET ? 3 : 2;
@@ -104,7 +105,6 @@ struct PGeo {
   static constexpr int OFF_Q = OFF_T;                    // the query rows, then the tiles
   static constexpr int OFF_QR = OFF_T;                   // window chunk: rotated f32 query rows
   static constexpr int OFF_SQ = OFF_T + REGION;          // per row: s_q (Hadamard) / alpha factor
-  static constexpr int OFF_QZ = OFF_SQ + kRows * 4;      // asymmetric K: per row the four block sums of Q
   static constexpr int SMEM = OFF_SQ + TAIL;
   static_assert(SMEM <= BUDGET, "shared memory fits the CTAs per SM");
 };
@@ -121,10 +121,10 @@ __device__ __forceinline__ uint32_t toff(int row, int chunk) {
 
 // Last token query row r (of the gqa * n_q rows of a kv head) may see; negative if none.
 // Unpack one plane of a raw stage slot (`pay`: 64 rows of PL's payload, `sc`: its per-token
-// scales) into the f16 tile at shared address `tile` (block layouts: hi parts; lo parts at
-// tile + 2 * kTile).
+// scales, `zr`: its per-token zero-points, asymmetric layout only) into the f16 tile at shared
+// address `tile` (block layouts: hi parts; lo parts at tile + 2 * kTile).
 template <int PL>
-__device__ __forceinline__ void unpack_plane(const uint8_t *pay, const uint8_t *sc, uint32_t tile) {
+__device__ __forceinline__ void unpack_plane(const uint8_t *pay, const uint8_t *sc, const uint8_t *zr, uint32_t tile) {
   using P = PlaneL<PL>;
   if constexpr (P::BITS == 6) {
     // Q6_0: each thread takes two (row, 32-value block) units; a block is 16 low-plane bytes then
@@ -190,12 +190,26 @@ __device__ __forceinline__ void unpack_plane(const uint8_t *pay, const uint8_t *
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(tile + off),
                      "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
       } else {
-        const uint32_t s2 = 0x00010001u * *reinterpret_cast<const uint16_t *>(sc + row * 8 + 2 * (ch >> 2));
         uint32_t hi[4], lo[4];
+        if constexpr (P::ASYM) {
+          // v = s n + z in f32 (s n is exact), then hi = rn(v), lo = rn(v - hi)
+          const float sf = __half2float(*reinterpret_cast<const __half *>(sc + row * 8 + 2 * (ch >> 2)));
+          const float zf = __half2float(*reinterpret_cast<const __half *>(zr + row * 8 + 2 * (ch >> 2)));
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          hi[x] = hmul2(o[x], s2);                                         // rn(c s)
-          lo[x] = hfma2(o[x], s2, hi[x] ^ 0x80008000u);                    // c s - rn(c s), exact
+          for (int x = 0; x < 4; ++x) {
+            const float2 nf = __half22float2(u32_as_h2(o[x]));
+            const float v0 = fmaf(sf, nf.x, zf), v1 = fmaf(sf, nf.y, zf);
+            hi[x] = pack_f16x2(v0, v1);
+            const float2 hf = __half22float2(u32_as_h2(hi[x]));
+            lo[x] = pack_f16x2(v0 - hf.x, v1 - hf.y);
+          }
+        } else {
+          const uint32_t s2 = 0x00010001u * *reinterpret_cast<const uint16_t *>(sc + row * 8 + 2 * (ch >> 2));
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            hi[x] = hmul2(o[x], s2);                                       // rn(c s)
+            lo[x] = hfma2(o[x], s2, hi[x] ^ 0x80008000u);                  // c s - rn(c s), exact
+          }
         }
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(tile + off),
                      "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
@@ -355,18 +369,11 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
 #pragma unroll
       for (int m = 16; m; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
       int e = 0;
-      if (mx > 0.0f) e = min(max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - (ASYMK ? 8 : 13), -100), 100);
+      if (mx > 0.0f) e = min(max(((__float_as_int(mx) >> 23) & 0xFF) - 127 - 13, -100), 100);
       const float pre = ldexpf(1.0f, -e);
       const uint2 qp = make_uint2(pack_f16x2(x[0] * pre, x[1] * pre), pack_f16x2(x[2] * pre, x[3] * pre));
       *reinterpret_cast<uint2 *>(qsm + lr * 2 * kD + lane * 8) = qp;
       if (lane == 0) sqs[lr] = r < R ? a.scale * ldexpf(1.0f, e) * kLog2e : 0.0f;
-      if constexpr (ASYMK) {                             // block b = lanes 8b .. 8b+7
-        const float2 f0 = __half22float2(u32_as_h2(qp.x)), f1 = __half22float2(u32_as_h2(qp.y));
-        float bs = (f0.x + f0.y) + (f1.x + f1.y);
-#pragma unroll
-        for (int m = 1; m < 8; m <<= 1) bs += __shfl_xor_sync(0xffffffffu, bs, m);
-        if ((lane & 7) == 0) reinterpret_cast<float *>(smem + G::OFF_QZ)[lr * 4 + (lane >> 3)] = bs;
-      }
     }
   }
   // DEC: every warp reads block 0's query rows and factors, which warp 0 wrote
@@ -529,22 +536,6 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
     alpha_g = sqs[16 * rw + g];                        // alpha * 2^e * log2(e), 0 for rows past R
     alpha_g8 = sqs[16 * rw + g + 8];
   }
-  // asymmetric: m16n8k8 A fragment of the block sums, k = (hi of blocks 0..3, lo of blocks 0..3):
-  // lane c holds blocks (2c) & 3, (2c+1) & 3, hi parts for c < 2, lo parts for c >= 2
-  uint32_t az0 = 0u, az1 = 0u;
-  if constexpr (ASYMK) {
-    const float *qz = reinterpret_cast<const float *>(smem + G::OFF_QZ);
-    auto part = [&](int lr) -> uint32_t {
-      const float2 v = *reinterpret_cast<const float2 *>(qz + lr * 4 + ((2 * c) & 3));
-      const uint32_t h = pack_f16x2(v.x, v.y);
-      if (c < 2) return h;
-      const float2 f = __half22float2(u32_as_h2(h));
-      return pack_f16x2(v.x - f.x, v.y - f.y);
-    };
-    az0 = part(16 * rw + g);
-    az1 = part(16 * rw + g + 8);
-  }
-  float Oz[4] = {0.0f, 0.0f, 0.0f, 0.0f};               // asymmetric: P . Z_V, columns = blocks (mod 4)
   float O[16][4];                                        // tile j: dims 8j + c (c0/c2), 8j + 4 + c (c1/c3)
 #pragma unroll
   for (int j = 0; j < 16; ++j)
@@ -574,8 +565,8 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
     // CPP eight-value chunks per plane). Hadamard: the signed codes. Block layouts: the values
     // code * scale of each chunk's 32-dim block as f16 hi + lo parts (exact TwoProduct: code * scale
     // has at most 19 significant bits); asymmetric zero-points enter by their own mma terms.
-    unpack_plane<KL>(sb, sb + G::OFF_SK, sKT);
-    unpack_plane<VL>(sb + G::OFF_V, sb + G::OFF_SV, sVT);
+    unpack_plane<KL>(sb, sb + G::OFF_SK, sb + G::OFF_ZK, sKT);
+    unpack_plane<VL>(sb + G::OFF_V, sb + G::OFF_SV, sb + G::OFF_ZV, sVT);
     __syncthreads();                                     // tiles complete
     const int ts = t0 + i * kStage;
     if (ts > warp_lim) continue;                         // none of this warp's rows sees the stage
@@ -611,12 +602,6 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
 #pragma unroll
             for (int j = 0; j < NTJ; ++j) mma16816(d[j], aq[2 * m + 1], kw[j][2], kw[j][3]);
           }
-        }
-        if constexpr (ASYMK) {                           // + Qsum . Z_K^T: token 8j + g, blocks (2c) & 3, +1
-#pragma unroll
-          for (int j = 0; j < NTJ; ++j)
-            mma1688(d[j], az0, az1,
-                    *reinterpret_cast<const uint32_t *>(sb + G::OFF_ZK + (pass_tok(hh) + 8 * j + g) * 8 + 4 * (c & 1)));
         }
         if constexpr (CAP) {                             // d holds the exact integer dots
 #pragma unroll
@@ -671,10 +656,6 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
           O[j][2] *= corr_g8;
           O[j][3] *= corr_g8;
         }
-        Oz[0] *= corr_g;
-        Oz[1] *= corr_g;
-        Oz[2] *= corr_g8;
-        Oz[3] *= corr_g8;
       }
       float ls_g = 0.0f, ls_g8 = 0.0f;
 #pragma unroll
@@ -708,14 +689,6 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
           ah[e] = pack_f16x2(s[j][xx], s[j][xx + 1]);
           const float2 f = __half22float2(u32_as_h2(ah[e]));
           al[e] = pack_f16x2(s[j][xx] - f.x, s[j][xx + 1] - f.y);
-        }
-        if constexpr (ASYMV) {                           // Oz += P . Z_V: tokens 2c, 2c+1, 2c+8, 2c+9, block g & 3
-          const uint16_t *zv = reinterpret_cast<const uint16_t *>(sb + G::OFF_ZV) + (g & 3);
-          const int tk = pass_tok(hh) + 16 * kk + 2 * c;
-          const uint32_t b0 = (uint32_t)zv[4 * tk] | ((uint32_t)zv[4 * tk + 4] << 16);
-          const uint32_t b1 = (uint32_t)zv[4 * tk + 32] | ((uint32_t)zv[4 * tk + 36] << 16);
-          mma16816(Oz, ah, b0, b1);
-          mma16816(Oz, al, b0, b1);
         }
 #pragma unroll
         for (int pg = 0; pg < 2; ++pg) {                 // output tiles 8pg .. 8pg+7
@@ -754,16 +727,6 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
   l_g += __shfl_xor_sync(0xffffffffu, l_g, 2);
   l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 1);
   l_g8 += __shfl_xor_sync(0xffffffffu, l_g8, 2);
-  // asymmetric: the zero-point sums of blocks 0..3 (lane c holds blocks 2c, 2c+1 for c < 2)
-  float zb[2][4] = {};
-  if constexpr (ASYMV) {
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const int src = (lane & ~3) | (b >> 1);
-      zb[0][b] = __shfl_sync(0xffffffffu, (b & 1) ? Oz[1] : Oz[0], src);
-      zb[1][b] = __shfl_sync(0xffffffffu, (b & 1) ? Oz[3] : Oz[2], src);
-    }
-  }
   if constexpr (DEC) {
     // the four warps scored different tokens of the same 16 rows: merge their (m, l, O) through
     // shared memory (the tile region, free once every warp is past its last stage), one thread
@@ -782,10 +745,10 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       float *o0 = xo + (warp * 16 + g) * kD + 8 * j, *o8 = o0 + 8 * kD;
-      o0[c] = O[j][0] + zb[0][j >> 2];
-      o0[4 + c] = O[j][1] + zb[0][j >> 2];
-      o8[c] = O[j][2] + zb[1][j >> 2];
-      o8[4 + c] = O[j][3] + zb[1][j >> 2];
+      o0[c] = O[j][0];
+      o0[4 + c] = O[j][1];
+      o8[c] = O[j][2];
+      o8[4 + c] = O[j][3];
     }
     __syncthreads();
     const int d = threadIdx.x;                               // 128 threads <-> 128 dims
@@ -822,8 +785,8 @@ __global__ void __launch_bounds__(kWarps * 32, PGeo<KL, VL>::CTAS) attend_prefil
     float *po = a.part_o + pi * kD;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      po[8 * j + c] = O[j][2 * half] + zb[half][j >> 2];
-      po[8 * j + 4 + c] = O[j][2 * half + 1] + zb[half][j >> 2];
+      po[8 * j + c] = O[j][2 * half];
+      po[8 * j + 4 + c] = O[j][2 * half + 1];
     }
     if (c == 0) {
       a.part_m[pi] = (half ? m_g8 : m_g) * kLn2;         // natural-log units, like the other kernels

@@ -166,9 +166,31 @@ __device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
 __device__ __forceinline__ void unpack8_u4(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w8 = w >> 8;
   o[0] = hadd2(lop3<0xEA>(w, 0x000F000Fu, 0x64006400u), 0xE400E400u);
-  o[1] = hfma2(lop3<0xEA>(w, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
+  o[1] = hfma2(lop3<0xEA>(w, 0x00F000F0u, 0x64006400u), kH16th, 0xD400D400u);
   o[2] = hadd2(lop3<0xEA>(w8, 0x000F000Fu, 0x64006400u), 0xE400E400u);
-  o[3] = hfma2(lop3<0xEA>(w8, 0x00F000F0u, 0x64006400u), 0x2C002C00u, 0xD400D400u);
+  o[3] = hfma2(lop3<0xEA>(w8, 0x00F000F0u, 0x64006400u), kH16th, 0xD400D400u);
+}
+
+// Unsigned 4-bit fields n0..n7 of w -> four exact f16 pairs (n0,n4), (n1,n5), (n2,n6), (n3,n7)
+// holding n - 8 (the asymmetric codes centred on the group's midpoint): like unpack8_q4, with the
+// field ORed under the exponent of 1024 instead of XORed.
+__device__ __forceinline__ void unpack8_u4m8(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8;
+  o[0] = hadd2(lop3<0xEA>(w, 0x000F000Fu, 0x64006400u), kHm1032);
+  o[1] = hfma2(lop3<0xEA>(w, 0x00F000F0u, 0x64006400u), kH16th, kHm72);
+  o[2] = hadd2(lop3<0xEA>(w8, 0x000F000Fu, 0x64006400u), kHm1032);
+  o[3] = hfma2(lop3<0xEA>(w8, 0x00F000F0u, 0x64006400u), kH16th, kHm72);
+}
+
+// The midpoints x = z + 8 s of two asymmetric groups (f16 pairs of zero-points z and scales s)
+// as f16 hi + lo parts: x is formed in f32 (exact but for the rare exponent spread beyond 24
+// bits), hi = rn(x), lo = rn(x - hi).
+__device__ __forceinline__ void midpoint_split(uint32_t z, uint32_t s, uint32_t &hi, uint32_t &lo) {
+  const float2 zf = __half22float2(u32_as_h2(z)), sf = __half22float2(u32_as_h2(s));
+  const float x0 = fmaf(8.0f, sf.x, zf.x), x1 = fmaf(8.0f, sf.y, zf.y);
+  hi = pack_f16x2(x0, x1);
+  const float2 hf = __half22float2(u32_as_h2(hi));
+  lo = pack_f16x2(x0 - hf.x, x1 - hf.y);
 }
 
 // Signed 8-bit fields: a = values v0..v3, b = v4..v7 (byte i = value i, two's complement) ->
