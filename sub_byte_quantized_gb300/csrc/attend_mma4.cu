@@ -6,8 +6,9 @@
 //   PV:  O^T[16 dims][8 rows]   += V^T[16 dims][16 tokens] . P'^T[16 tokens][8 rows]
 // with the codes as exact f16 operands (K as subnormals u * 2^-24 with the offset in the
 // accumulator's initial value; V by the exact f16 fix-up: asymmetric V as n - 8, the group's
-// midpoint z + 8 s coming from one small mma per tile), exact query operands (power-of-two prescale, hi + lo parts
-// for f32 queries; int8 codes for the Hadamard layout) and P' = p * s_v kept as f16 hi + lo parts.
+// midpoint z + 8 s coming from one small mma per tile), exact query operands (power-of-two
+// prescale, hi + lo parts for f32 queries; int8 codes for the Hadamard layout) and P' = p * s_v
+// kept as f16 hi + lo parts.
 //
 // Work split: a CTA of eight warps streams one chunk in 128-token stages. Warps 0-3 ("K warps") each
 // score two 16-token tiles of stage i and run the online softmax; warps 4-7 ("V warps") accumulate
@@ -458,7 +459,6 @@ __global__ void __launch_bounds__(kThreads, kMma4CtasPerSm) attend_mma4_kernel(A
 #pragma unroll
       for (int tt = 0; tt < kTPW; ++tt) {
       const int tile = kTPW * tw + tt;
-      const int ts = t0 + j * kStage + 16 * tile;
       // (a tile past t_end is zero-filled and fully masked: it contributes nothing)
       const uint8_t *xs = xch + ((tile * 2 + (j & 1)) * 32 + lane) * 32;
       const uint4 pb = *reinterpret_cast<const uint4 *>(xs);

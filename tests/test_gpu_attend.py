@@ -340,3 +340,28 @@ def test_mixed_kv_precision(layout, n_recent, n_q, causal):
     w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout=layout, batch=2, n_kv_heads=2, n_q_heads=8,
                                               n_recent=n_recent, causal=causal)
     run_case(w, kv_len=900, n_q=n_q, chunk=128, fill=900 - n_q)
+
+
+@pytest.mark.parametrize("name,kw,kv_len,n_q", [
+    ("c5_q4_0_llama70b_128k", {}, 4000, 1),                       # per-warp decode kernel
+    ("c5_q8_0_llama70b_128k", {}, 4000, 1),
+    ("c5_asym4_g32_llama70b_128k", {}, 4000, 1),                  # warp-specialised decode kernel
+    ("c3_had_int4_decode", {"batch": 2}, 4000, 1),
+    ("c3_had_int2_decode_w256", {"batch": 2}, 4000, 1),
+    ("c4_q6_0_gemma", {"batch": 1}, 4000, 1),
+    ("c5_asym4_g32_llama70b_128k", {"causal": True}, 2048, 16),   # row-side kernel
+    ("c5_q4_0_llama70b_128k", {"causal": True}, 2048, 16),
+    ("c3_had_int4_decode", {"batch": 2, "causal": True}, 2048, 16),
+    ("c3_had_int4_prefill", {"batch": 1}, 2048, 256),              # tcgen05 prefill body
+])
+def test_precision_margin(name, kw, kv_len, n_q):
+    """Every kernel family stays far inside the tolerance, not just inside it: the largest
+    |gpu - oracle| / (2e-3 + 1e-3 |oracle|) is at most 0.05 (the exact-operand forms measure
+    0.015 or less on these workloads' outlier channels). A value path that carries an offset mass
+    through the long PV accumulation (codes + offset as f16 subnormals with the offset subtracted
+    at the end, or asymmetric codes with the zero-point in a separate sum) measured 0.2 to 1.6 on
+    workloads like these, because the tensor core's truncated accumulation shows in the
+    cancelling difference."""
+    w = WORKLOADS[name].scaled(**kw)
+    res, _ = run_case(w, kv_len=kv_len, n_q=n_q, fill=kv_len - n_q, check_planes=False)
+    assert res["max_ratio"] <= 0.05, f"{name} {kw}: max error / tolerance {res['max_ratio']:.4f}"
