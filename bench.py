@@ -639,8 +639,10 @@ def main():
 
     if not args.quick and rank == 0:
         # end to end through the host-buffer C-ABI call: pinned host k_new, v_new and q in, the f32
-        # result back in pinned host memory; the call copies both ways and waits for its stream
-        # the three inputs back to back in one pinned allocation (the call then moves them with one copy)
+        # result back in pinned host memory, one stream wait per step. The call copies q host ->
+        # device; the store kernel reads k_new / v_new from the pinned buffers over the host link and
+        # the reduce writes the result into the pinned output (every input and output byte crosses
+        # the link inside the timed region)
         n_k, n_qe = k_new.numel(), q.numel()
         packed = torch.empty(2 * n_k + n_qe, dtype=k_new.dtype).pin_memory()
         hk, hv = packed[:n_k].view(k_new.shape), packed[n_k:2 * n_k].view(v_new.shape)
@@ -679,9 +681,10 @@ def main():
         line["e2e"] = {"value": spec.read_bytes / t_e2e / 1e9, "unit": "GB/s",
                        "h2d_bytes_per_step": (hk.numel() + hv.numel() + hq.numel()) * el,
                        "d2h_bytes_per_step": hout.numel() * 4, "us_per_layer": t_e2e * 1e6, "steps": n_e2e,
-                       "call": "kvq_append_decode_attend_host through ctypes with prepared arguments (host "
-                               "buffers, one call and one stream wait per step; k_new, v_new, q back to back in "
-                               "one pinned allocation)",
+                       "call": "kvq_append_decode_attend_host through ctypes with prepared arguments (pinned "
+                               "host buffers, one call and one stream wait per step; q copied host to device, "
+                               "k_new / v_new read by the store kernel and the output written by the reduce "
+                               "over the host link)",
                        "python_binding_us_per_layer": t_py * 1e6}
         line["store"] = store_timings(kvq, w, kd, vd, k_new, v_new, fill, stream, dev)
         if args.workload == DEFAULT_WORKLOAD:

@@ -335,13 +335,17 @@ kvq_status kvq_paged_append_decode_attend(const kvq_paged_cache *cache, const vo
  *                 kvq_paged_append_decode_attend
  *   workspace     device, 256-byte aligned, at least the matching *_host_workspace_bytes: the
  *                 attention partials followed by device staging for k_new, v_new, q, out
- *                 (and seq_lens); the caller owns it, the call must not share it with another
- *                 call in flight.
- * The call copies the inputs host -> device on `stream` (cudaMemcpyAsync; page-locked host
- * memory makes the copies asynchronous, pageable memory works but the driver stages it; when
- * k_new, v_new and q lie back to back in that order in host memory, one copy moves all three), enqueues
- * the same launches as the device-buffer call (identical results and stored bytes), copies the
- * output back and returns after cudaStreamSynchronize(stream), with `out` filled. Every argument
+ *                 (and seq_lens; the staging of buffers used in place stays unused); the caller
+ *                 owns it, the call must not share it with another call in flight.
+ * Page-locked (pinned) host buffers that are 16-byte aligned are used in place where that saves
+ * a copy: under unified addressing the GPU reaches them directly, so the store kernel reads k_new
+ * and v_new from them and the reduce writes `out` into them. q is always copied host -> device on
+ * `stream` (cudaMemcpyAsync) into the staging area, because every phase-1 CTA of a kv head reads it.
+ * Pageable buffers (or unaligned ones) are staged with copies both ways (the driver stages
+ * pageable memory itself; when k_new, v_new and q lie back to back in that order in host memory,
+ * one copy moves all three). The call enqueues the same launches as the device-buffer call
+ * (identical results and stored bytes) and returns after cudaStreamSynchronize(stream), with
+ * `out` filled. Every argument
  * is validated before anything is enqueued; a CUDA error from a copy, a launch or the
  * synchronisation returns KVQ_ECUDA (then nothing can be assumed about `out` or the cache rows
  * of the append). The host buffers may be reused as soon as the call returns.

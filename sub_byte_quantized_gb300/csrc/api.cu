@@ -491,6 +491,44 @@ kvq_status check_host_args(int kv_dtype, int n_new, int q_dtype, const void *k_n
   return KVQ_OK;
 }
 
+// The device address of a host buffer that the GPU reads and writes in place: pinned memory
+// (cudaHostAlloc / cudaMallocHost, or registered), which unified addressing maps into every
+// device's address space, and 16-byte aligned like the device-buffer calls require; nullptr for
+// anything else (pageable memory goes through the staging copies).
+void *device_view(const void *p) {
+  if (!p || !aligned(p, 16)) return nullptr;
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+    cudaGetLastError();                                  // not a CUDA-known pointer: clear the error
+    return nullptr;
+  }
+  return pa.type == cudaMemoryTypeHost ? pa.devicePointer : nullptr;
+}
+
+// Where a host-buffer call's kernels find their inputs and put their output. Pinned caller
+// buffers are used in place where that saves a copy operation: the store kernel reads k_new /
+// v_new over the host link (each element once) and the reduce writes the result there. q is
+// always staged in device memory, since every phase-1 CTA of a kv head reads it (reading it over
+// the link measured slower than one small copy). Pageable buffers go through the staging area of
+// the workspace with a copy each way.
+struct HostIo {
+  const void *k, *v, *q;
+  float *out;
+  bool copy_in, copy_out;                                // copy_in: k_new and v_new staged with q
+};
+HostIo host_io(const HostStaging &h, char *ws, int n_new, const void *k_new, const void *v_new, float *out) {
+  HostIo io;
+  const void *kd = n_new > 0 ? device_view(k_new) : nullptr, *vd = n_new > 0 ? device_view(v_new) : nullptr;
+  io.copy_in = !(n_new == 0 || (kd && vd));
+  io.k = io.copy_in ? ws + h.k : kd;
+  io.v = io.copy_in ? ws + h.v : vd;
+  io.q = ws + h.q;
+  float *od = static_cast<float *>(device_view(out));
+  io.copy_out = od == nullptr;
+  io.out = io.copy_out ? reinterpret_cast<float *>(ws + h.out) : od;
+  return io;
+}
+
 // Host -> staging copies of the inputs (cudaMemcpyDefault: pinned or pageable host memory).
 cudaError_t copy_in(const HostStaging &h, char *ws, const void *k_new, const void *v_new, const void *q,
                     const void *seq_lens, cudaStream_t s) {
@@ -783,17 +821,19 @@ kvq_status kvq_append_decode_attend_host(const kvq_cache *cache, const void *k_n
   if (workspace_bytes < h.total)
     return fail(KVQ_EWORKSPACE, "workspace %zu < required %zu", workspace_bytes, h.total);
   char *ws = static_cast<char *>(workspace);
-  // both parts validated against the staging addresses before anything is enqueued
+  const HostIo io = host_io(h, ws, n_new, k_new, v_new, out);
+  // both parts validated against the addresses the kernels will use before anything is enqueued
   kvq::CacheView v;
-  st = check_store(-1, cache, ws + h.k, ws + h.v, kv_dtype, n_new, pos0, v);
+  st = check_store(-1, cache, io.k, io.v, kv_dtype, n_new, pos0, v);
   if (st != KVQ_OK) return st;
-  st = prepare_attend(cache, ws + h.q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk,
-                      reinterpret_cast<float *>(ws + h.out), workspace, need, a);
+  st = prepare_attend(cache, io.q, q_dtype, n_q_heads, n_q, kv_len, causal, q_pos0, attn_scale, chunk, io.out,
+                      workspace, need, a);
   if (st != KVQ_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = copy_in(h, ws, k_new, v_new, q, nullptr, s);
-  if (e == cudaSuccess) e = launch_append_attend(v, a, ws + h.k, ws + h.v, kv_dtype, n_new, pos0, s);
-  if (e == cudaSuccess) e = copy_out_and_wait(h, ws, out, s);
+  cudaError_t e = io.copy_in ? copy_in(h, ws, k_new, v_new, q, nullptr, s)
+                             : cudaMemcpyAsync(ws + h.q, q, h.q_bytes, cudaMemcpyDefault, s);   // q only
+  if (e == cudaSuccess) e = launch_append_attend(v, a, io.k, io.v, kv_dtype, n_new, pos0, s);
+  if (e == cudaSuccess) e = io.copy_out ? copy_out_and_wait(h, ws, out, s) : cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "host-buffer append/attend: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
@@ -828,17 +868,25 @@ kvq_status kvq_paged_append_decode_attend_host(const kvq_paged_cache *cache, con
   if (workspace_bytes < h.total)
     return fail(KVQ_EWORKSPACE, "workspace %zu < required %zu", workspace_bytes, h.total);
   char *ws = static_cast<char *>(workspace);
+  const HostIo io = host_io(h, ws, n_new, k_new, v_new, out);
+  // the sequence lengths are read by every CTA: always staged in device memory
   const int32_t *lens = reinterpret_cast<const int32_t *>(ws + h.lens);
   kvq::CacheView v;
-  st = check_paged_store(cache, ws + h.k, ws + h.v, kv_dtype, n_new, lens, v);
+  st = check_paged_store(cache, io.k, io.v, kv_dtype, n_new, lens, v);
   if (st != KVQ_OK) return st;
-  st = prepare_paged(cache, ws + h.q, q_dtype, n_q_heads, n_q, lens, max_kv_len, causal, attn_scale, chunk,
-                     reinterpret_cast<float *>(ws + h.out), workspace, need, a);
+  st = prepare_paged(cache, io.q, q_dtype, n_q_heads, n_q, lens, max_kv_len, causal, attn_scale, chunk, io.out,
+                     workspace, need, a);
   if (st != KVQ_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = copy_in(h, ws, k_new, v_new, q, seq_lens, s);
-  if (e == cudaSuccess) e = launch_paged_append_attend(v, a, ws + h.k, ws + h.v, kv_dtype, n_new, lens, s);
-  if (e == cudaSuccess) e = copy_out_and_wait(h, ws, out, s);
+  cudaError_t e = cudaSuccess;
+  if (io.copy_in) {
+    e = copy_in(h, ws, k_new, v_new, q, seq_lens, s);
+  } else {                                               // q and the lengths only
+    e = cudaMemcpyAsync(ws + h.q, q, h.q_bytes, cudaMemcpyDefault, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(ws + h.lens, seq_lens, h.lens_bytes, cudaMemcpyDefault, s);
+  }
+  if (e == cudaSuccess) e = launch_paged_append_attend(v, a, io.k, io.v, kv_dtype, n_new, lens, s);
+  if (e == cudaSuccess) e = io.copy_out ? copy_out_and_wait(h, ws, out, s) : cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(KVQ_ECUDA, "host-buffer paged append/attend: %s", cudaGetErrorString(e));
   return KVQ_OK;
 }
