@@ -116,7 +116,7 @@ PROFILES = {
     "c3_had_int4_prefill": ("attend_prefill_tc_c3_had_int4.md", "attend_prefill_tc.cu"),
     "c5_q8_0_llama70b_128k": ("attend_phase1_q8_0_128k.md", "attend_mma.cu"),
     "c5_q4_0_k_q8_0_v_llama70b_128k": ("attend_phase1_q4_0_k_q8_0_v_128k.md", "attend_mma.cu"),
-    "c3_had_int2_decode_w256": ("attend_prefill_dec_had_int2_w256.md", "attend_prefill_kernel.cuh"),
+    "c3_had_int2_decode_w256": ("attend_phase1_had_int2_w256.md", "attend_mma.cu"),
 }
 
 
@@ -150,7 +150,7 @@ def chunk_rule(w, spec) -> str:
                 "stages); the f32 window is scored in 64-token chunks of its own")
     if w.head_dim == 128 and rows > 8:
         return "automatic: body split for about four waves of 64-query-row CTAs"
-    return "automatic: 4 warps per chunk, one 64-token-multiple slice per resident warp, one wave"
+    return "automatic: 4 warps per chunk, one 32-token-multiple slice per resident warp, one wave"
 
 
 def aggregate(world: int, units_per_rank: float, steps: int, elapsed_ms: float) -> float:
