@@ -48,10 +48,10 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
   if (a.win_in_reduce && win_vis) {
     // The exact-f32 recent window (tokens n_body .. kv_len-1, ring slot t mod n_recent), scored
     // with the float32 rotated query. Warp w takes window tokens 8w .. 8w+7 of each group of 64,
-    // all eight at once: lane l scores token l / 4 over dims (l % 4) * D/4 .. +D/4 (reduced over
-    // the token's four lanes) and accumulates its output dims lane * VPL .. +VPL for the eight
-    // tokens; the loads of a group are all in flight together. The warp's state then joins the
-    // chunk partials below.
+    // two groups per pass: lane l scores token l / 4 of each group over dims (l % 4) * D/4 .. +D/4
+    // (reduced over the token's four lanes) and accumulates its output dims lane * VPL .. +VPL for
+    // the sixteen tokens; every K and V load of a pass is in flight before the first score. The
+    // warp's state then joins the chunk partials below.
     const CacheView &cv = a.cache;
     const size_t bh = (row / a.n_q) / a.Hq * cv.H + ((row / a.n_q) % a.Hq) / a.gqa;
     // rotated query row (the tensor-core phase 1 prepares its int8 codes itself, so rotate here)
@@ -70,56 +70,77 @@ __global__ void __launch_bounds__(kWarps * 32) attend_reduce_kernel(AttendArgs a
     for (int i = 0; i < QS; ++i) qs[i] = sm_q[(lane & 3) * QS + i];
     const int tl = lane >> 2;                             // this lane's token within the warp's eight
     const int n_w = sl.kv_len - sl.n_body;
-    for (int g0 = 0; g0 < n_w; g0 += 8 * kWarps) {
-      const int t = sl.n_body + g0 + 8 * warp + tl;        // this lane's token
-      const bool tv = t < sl.kv_len && t <= lim;
-      const size_t slot = (bh * cv.n_recent + (size_t)((tv ? t : sl.n_body) % cv.n_recent)) * D;
-      const float *kr = cv.ring[0] + slot + (lane & 3) * QS;
-      float dot = 0.0f;
+    // two groups of 64 tokens per pass: both groups' K and V loads are issued before any score
+    // is formed, so a pass costs one memory round trip
+    constexpr int NG = 2;
+    for (int g0 = 0; g0 < n_w; g0 += 64 * NG) {
+      float4 kq[NG][QS / 4];
+      float4 vv[NG][8][VPL / 4];
+      bool tv[NG];
 #pragma unroll
-      for (int i = 0; i < QS; i += 4) {
-        const float4 k4 = tv ? *reinterpret_cast<const float4 *>(kr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-        dot = fmaf(qs[i], k4.x, dot);
-        dot = fmaf(qs[i + 1], k4.y, dot);
-        dot = fmaf(qs[i + 2], k4.z, dot);
-        dot = fmaf(qs[i + 3], k4.w, dot);
+      for (int k = 0; k < NG; ++k) {
+        const int t = sl.n_body + g0 + 64 * k + 8 * warp + tl;   // this lane's token of group k
+        tv[k] = t < sl.kv_len && t <= lim;
+        const size_t slot = (bh * cv.n_recent + (size_t)((tv[k] ? t : sl.n_body) % cv.n_recent)) * D;
+        const float *kr = cv.ring[0] + slot + (lane & 3) * QS;
+#pragma unroll
+        for (int i = 0; i < QS / 4; ++i)
+          kq[k][i] = tv[k] ? *reinterpret_cast<const float4 *>(kr + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
+        // the eight V rows' slices (invalid tokens read a valid slot and get weight 0)
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int tu = sl.n_body + g0 + 64 * k + 8 * warp + u;
+          const int ts = tu < sl.kv_len ? tu : sl.n_body;
+          const float *vr = cv.ring[1] + (bh * cv.n_recent + (size_t)(ts % cv.n_recent)) * D + lane * VPL;
+#pragma unroll
+          for (int i = 0; i < VPL / 4; ++i) vv[k][u][i] = *reinterpret_cast<const float4 *>(vr + 4 * i);
+        }
       }
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      const float sc = tv ? a.scale * dot : -INFINITY;
-      float gm = sc;
+      float sc[NG];
+      float gm = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < NG; ++k) {
+        float dot = 0.0f;
+#pragma unroll
+        for (int i = 0; i < QS / 4; ++i) {
+          dot = fmaf(qs[4 * i], kq[k][i].x, dot);
+          dot = fmaf(qs[4 * i + 1], kq[k][i].y, dot);
+          dot = fmaf(qs[4 * i + 2], kq[k][i].z, dot);
+          dot = fmaf(qs[4 * i + 3], kq[k][i].w, dot);
+        }
+        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+        dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+        sc[k] = tv[k] ? a.scale * dot : -INFINITY;
+        gm = fmaxf(gm, sc[k]);
+      }
 #pragma unroll
       for (int k = 4; k < 32; k <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, k));
-      if (gm == -INFINITY) continue;                      // no visible token in this warp's eight
+      if (gm == -INFINITY) continue;                      // no visible token in this warp's sixteen
       const float mn = fmaxf(M, gm);
       const float corr = __expf(M - mn);                  // M = -inf -> 0
-      const float p = tv ? __expf(sc - mn) : 0.0f;
-      float ps = (lane & 3) == 0 ? p : 0.0f;              // each token counted once
+      float p[NG], ps = 0.0f;
+#pragma unroll
+      for (int k = 0; k < NG; ++k) {
+        p[k] = tv[k] ? __expf(sc[k] - mn) : 0.0f;
+        ps += (lane & 3) == 0 ? p[k] : 0.0f;              // each token counted once
+      }
 #pragma unroll
       for (int k = 4; k < 32; k <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, k);
       L = fmaf(L, corr, ps);
 #pragma unroll
       for (int i = 0; i < VPL; ++i) O[i] *= corr;
-      // the eight V rows' slices, all loads in flight together (invalid tokens read a valid slot
-      // and get weight 0)
-      float4 vv[8][VPL / 4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int tu = sl.n_body + g0 + 8 * warp + u;
-        const int ts = tu < sl.kv_len ? tu : sl.n_body;
-        const float *vr = cv.ring[1] + (bh * cv.n_recent + (size_t)(ts % cv.n_recent)) * D + lane * VPL;
+      for (int k = 0; k < NG; ++k) {
 #pragma unroll
-        for (int i = 0; i < VPL / 4; ++i) vv[u][i] = *reinterpret_cast<const float4 *>(vr + 4 * i);
-      }
+        for (int u = 0; u < 8; ++u) {
+          const float pu = __shfl_sync(0xffffffffu, p[k], 4 * u);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float pu = __shfl_sync(0xffffffffu, p, 4 * u);
-#pragma unroll
-        for (int i = 0; i < VPL / 4; ++i) {
-          O[4 * i] = fmaf(pu, vv[u][i].x, O[4 * i]);
-          O[4 * i + 1] = fmaf(pu, vv[u][i].y, O[4 * i + 1]);
-          O[4 * i + 2] = fmaf(pu, vv[u][i].z, O[4 * i + 2]);
-          O[4 * i + 3] = fmaf(pu, vv[u][i].w, O[4 * i + 3]);
+          for (int i = 0; i < VPL / 4; ++i) {
+            O[4 * i] = fmaf(pu, vv[k][u][i].x, O[4 * i]);
+            O[4 * i + 1] = fmaf(pu, vv[k][u][i].y, O[4 * i + 1]);
+            O[4 * i + 2] = fmaf(pu, vv[k][u][i].z, O[4 * i + 2]);
+            O[4 * i + 3] = fmaf(pu, vv[k][u][i].w, O[4 * i + 3]);
+          }
         }
       }
       M = mn;
