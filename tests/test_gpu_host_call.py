@@ -120,3 +120,39 @@ def test_paged_host_call_matches_device_call():
     oc.store(inp["k"][:, :, :S - n_new], inp["v"][:, :, :S - n_new], np.zeros(B, np.int64))
     oc.store(kt.float().cpu().numpy(), vt.float().cpu().numpy(), lens - n_new)
     check_close(got.numpy(), oc.attend(inp["q"], w.alpha, lens), "paged host call")
+
+
+@pytest.mark.parametrize("inputs,out_kind", [("pinned", "pageable"), ("pageable", "pinned"),
+                                             ("pinned_unaligned", "pinned"), ("pinned", "pinned")])
+def test_host_call_buffer_kinds(inputs, out_kind):
+    """Pinned, 16-byte aligned host buffers are used in place (the store reads k_new / v_new and the
+    reduce writes out over the host link); pageable or unaligned ones go through the workspace
+    staging. Every mix gives the device-buffer call's result and stored bytes exactly."""
+    w = WORKLOADS["c2_q4_0_llama3_8b"].scaled(layout="q4_0", batch=2, n_kv_heads=2, n_q_heads=8)
+    inp = make_inputs(w, kv_len=500, n_q=1)
+    S = inp["k"].shape[2]
+    n_new = 2
+    fill = S - n_new
+    dc, _, d = fill_both(w, inp, fill=fill)
+    dc2, _, _ = fill_both(w, inp, fill=fill)
+    kn, vn, q = d["k"][:, :, fill:].contiguous(), d["v"][:, :, fill:].contiguous(), d["q"]
+    if inputs == "pinned_unaligned":
+        # views 2 bf16 elements (4 bytes) into pinned allocations: not 16-byte aligned
+        hk = torch.empty(kn.numel() + 2, dtype=kn.dtype).pin_memory()[2:].view(kn.shape)
+        hv = torch.empty(vn.numel() + 2, dtype=vn.dtype).pin_memory()[2:].view(vn.shape)
+        hk.copy_(kn.cpu())
+        hv.copy_(vn.cpu())
+        hq = q.cpu().pin_memory()
+    else:
+        hk, hv, hq = kn.cpu(), vn.cpu(), q.cpu()
+        if inputs == "pinned":
+            hk, hv, hq = hk.pin_memory(), hv.pin_memory(), hq.pin_memory()
+    out = torch.empty(q.shape, dtype=torch.float32)
+    if out_kind == "pinned":
+        out = out.pin_memory()
+    ref = kvq.append_decode_attend(dc, kn, vn, fill, q, S, attn_scale=w.alpha)
+    got = kvq.append_decode_attend_host(dc2, hk, hv, fill, hq, S, attn_scale=w.alpha, out=out)
+    torch.cuda.synchronize()
+    assert got.data_ptr() == out.data_ptr()
+    assert torch.equal(got, ref.cpu())
+    _planes_equal(dc, dc2)
