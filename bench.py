@@ -870,7 +870,11 @@ def workload_summaries(kvq, L, dev, stream, K, hbm_peak, bf16_peak):
         with torch.cuda.stream(stream):
             g_ev.replay()
         torch.cuda.synchronize(dev)
-        ph_ms = statistics.fmean(a.elapsed_time(b) for a, b in ph)
+        # the median launch: one delayed event pair can dominate the mean (seen once: a mean of
+        # 0.35 ms over 200 launches of a 0.05 ms kernel, i.e. one pair about 60 ms apart); the mean
+        # is kept beside it
+        ph_all = [a.elapsed_time(b) for a, b in ph]
+        ph_ms, ph_mean = statistics.median(ph_all), statistics.fmean(ph_all)
         if prefill:
             ach = flops / (ph_ms / 1e3) / 1e12
             roof = {"bound": "tensor", "achieved": round(ach, 1), "unit": "TFLOP/s", "frac": round(ach / bf16_peak, 4),
@@ -880,7 +884,8 @@ def workload_summaries(kvq, L, dev, stream, K, hbm_peak, bf16_peak):
             roof = {"bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s", "frac": round(ach / hbm_peak, 4),
                     "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4)}
         out[name] = {"us_per_layer": round(step_ms * 1e3, 2), "gbs": round(read_bytes / (step_ms / 1e3) / 1e9, 1),
-                     "phase1_us": round(ph_ms * 1e3, 2), "roofline": roof, "chunk": chunk,
+                     "phase1_us": round(ph_ms * 1e3, 2), "phase1_us_mean": round(ph_mean * 1e3, 2),
+                     "roofline": roof, "chunk": chunk,
                      "read_bytes_per_step": read_bytes, "flops_per_step": flops, "steps": K,
                      "l2": "cache L2-resident" if n_rep * read_bytes < 2 * L2_BYTES else
                      f"{n_rep} replicas rotated (> L2)"}
