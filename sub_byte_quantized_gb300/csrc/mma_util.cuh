@@ -138,12 +138,14 @@ __device__ __forceinline__ void unpack8_q4(uint32_t w, uint32_t (&o)[4]) {
   o[3] = hfma2(lop3<0x6a>(w8, 0x00F000F0u, 0x64806480u), kH16th, kHm72);
 }
 
-// K and asymmetric-V operands: the same four pairs as unpack8_q4, but each code u (Q4_0: u = n ^ 8,
+// K operands: the same four pairs as unpack8_q4, but each code u (Q4_0 and Hadamard int4: u = n ^ 8,
 // the code plus 8; asymmetric: u = n) is placed in the mantissa of an f16 with a zero exponent,
 // i.e. the exact subnormal u * 2^-24 (high fields: 16 u * 2^-24). One lop3 per pair, no f16
-// arithmetic. For K the query entries facing high fields are divided by 16, the 2^-24 goes into
-// the row's scale and the Q4_0 offset -8 * sum(q) into the accumulator's initial value; for V the
-// output is rescaled in the epilogue and the zero-point term comes from its own small mma.
+// arithmetic. The query entries facing high fields are divided by 16, the 2^-24 goes into the
+// row's scale and the offset -8 * sum(q) into the accumulator's initial value (asymmetric: the
+// zero-point term is added to each block's partial). A score is one short dot product, so the
+// offset costs no precision there; value paths take the exact signed forms instead, because their
+// long accumulation would carry the offset's mass.
 template <bool ASYM>
 __device__ __forceinline__ void unpack8_sub(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w8 = w >> 8;
