@@ -3,8 +3,8 @@
 tract discussion #2402, "What's done": the body score is the integer dot int8(q_rot) . int4(k_rot)
 -> i32, an exact integer, so every summation order gives the same value. The score-capture call
 (kvq_debug_attend_scores_i32) runs the ordinary attention launches; the tensor-core kernel that
-scores the body (the per-warp decode kernel, the row-side prefill kernel and its decode form) also
-writes the integer it holds before scaling. Those integers and the int8 query scales must equal the
+scores the body (the per-warp decode kernel for int4 and int2, the row-side prefill kernel, the
+tcgen05 prefill kernel) also writes the integer it holds before scaling. Those integers and the int8 query scales must equal the
 oracle's bit for bit; the attention output of the same call is checked at the usual tolerance.
 
 An entry (row, t) is checked wherever row sees t (t <= its causal limit). Elsewhere the kernels may
@@ -73,7 +73,7 @@ def test_c3_prefill_chunk():
 
 
 def test_int2_wide_window_decode():
-    """Hadamard int2 body with a 256-token exact-f32 window, decode (row-side kernel, decode form)."""
+    """Hadamard int2 body with a 256-token exact-f32 window, decode (per-warp decode kernel)."""
     w = WORKLOADS["c3_had_int2_decode_w256"].scaled(batch=2)
     check_scores(w, 4096, 1, 4095)
 
