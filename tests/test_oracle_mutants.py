@@ -1,9 +1,12 @@
 """Planted mistakes in the oracle (on the CPU) must be caught by the pins.
 
 Each case patches one plausible error into the oracle: a swapped nibble order, a wrong
-magnitude, a transposed high-plane field, a wrong GQA index, a dropped window term, a
-missing max subtraction in the chunk combine. It then runs the pin tests that should fail
-and checks that at least one does.
+magnitude or scale divisor (Q4_0, Q6_0, Q8_0, Hadamard int4, the int8 query, asymmetric), a
+transposed high-plane field, a wrong GQA index, a dropped window term, a window ring slot off by
+one, a missing rescale in the chunk combine, a rotation without its 1/sqrt(D), an asymmetric
+zero-point taken at the maximum or subtracted. Cases inside a function body replace one
+expression of the oracle's own source for the test's duration (`_mutant`). It then runs the pin
+tests that should fail and checks that at least one does.
 """
 import numpy as np
 import pytest
@@ -138,3 +141,75 @@ def test_int2_field_order_is_caught(monkeypatch):
 def test_int2_read_without_sign_is_caught(monkeypatch):
     monkeypatch.setattr(Q, "read_int2", lambda v: np.asarray(v).astype(np.int32))
     assert _fails(P.test_int2_read_formula_every_field, P.test_hadamard_int2_codes_and_scale)
+
+
+def _mutant(mod, name, old, new):
+    """`mod.name` with one expression of its source replaced (a planted mistake for one test)."""
+    import inspect
+    import textwrap
+    src = textwrap.dedent(inspect.getsource(getattr(mod, name)))
+    assert src.count(old) == 1, (name, old)
+    ns = dict(vars(mod))
+    exec(compile(src.replace(old, new), f"<mutant {mod.__name__}.{name}>", "exec"), ns)
+    return ns[name]
+
+
+def test_asym_scale_over_16_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "quantize_asym4_g32",
+                        _mutant(Q, "quantize_asym4_g32", "rng / np.float32(15.0)", "rng / np.float32(16.0)"))
+    assert _fails(P.test_asym_exact_grid, P.test_asym_constant_group_and_bound)
+
+
+def test_asym_zero_point_at_the_maximum_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "quantize_asym4_g32", _mutant(Q, "quantize_asym4_g32", "z16 = fp16_round(mn)",
+                                                         "z16 = fp16_round(mx)"))
+    assert _fails(P.test_asym_exact_grid, P.test_asym_constant_group_and_bound)
+
+
+def test_asym_reconstruction_sign_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "dequantize_asym4_g32",
+                        _mutant(Q, "dequantize_asym4_g32", "[..., None] + np.asarray(zero)",
+                                "[..., None] - np.asarray(zero)"))
+    assert _fails(P.test_asym_exact_grid, P.test_asym_constant_group_and_bound)
+
+
+def test_hadamard_int4_scale_over_8_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "quantize_hadamard_int4",
+                        _mutant(Q, "quantize_hadamard_int4", "amax / np.float32(7.0)", "amax / np.float32(8.0)"))
+    assert _fails(P.test_hadamard_int4_codes_and_scale)
+
+
+def test_rotation_without_normalisation_is_caught(monkeypatch):
+    import inspect
+    src = inspect.getsource(Q.rotate)
+    # the rotation's 1/sqrt(D) factor, whatever name it has in the source, becomes 1
+    body = [ln for ln in src.splitlines() if "inv_sqrt_f32" in ln]
+    assert body, "rotate() scales by inv_sqrt_f32(D)"
+    monkeypatch.setattr(Q, "inv_sqrt_f32", lambda d: np.float32(1.0))
+    assert _fails(P.test_hadamard_int4_codes_and_scale, P.test_rotation_preserves_scores)
+
+
+def test_window_ring_slot_off_by_one_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "attend_hadamard",
+                        _mutant(A, "attend_hadamard", "slots = np.arange(n_body, kv_len) % n_recent",
+                                "slots = np.arange(n_body + 1, kv_len + 1) % n_recent"))
+    assert _fails(P.test_recent_window_semantics, P.test_hadamard_full_window_is_exact_attention)
+
+
+def test_combine_without_rescaled_sums_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "lse_combine", _mutant(A, "lse_combine", "L = np.sum(ls * w, axis=0)",
+                                                  "L = np.sum(ls, axis=0)"))
+    assert _fails(lambda: P.test_split_k_equals_single_pass(64), lambda: P.test_split_k_equals_single_pass(7))
+
+
+def test_query_scale_over_128_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "prep_q_hadamard", _mutant(A, "prep_q_hadamard", "amax / np.float32(127.0)",
+                                                      "amax / np.float32(128.0)"))
+    assert _fails(P.test_integer_scores_brute_force, P.test_hadamard_body_on_exact_grid_matches_plain_attention,
+                  P.test_error_envelopes)
+
+
+def test_q6_0_magnitude_31_is_caught(monkeypatch):
+    monkeypatch.setattr(Q, "quantize_q6_0", _mutant(Q, "quantize_q6_0", "amax / np.float32(32.0)",
+                                                    "amax / np.float32(31.0)"))
+    assert _fails(P.test_q6_0_every_code_through_read_formula, P.test_q6_0_saturation)
