@@ -4,7 +4,7 @@ Each case patches one plausible error into the oracle: a swapped nibble order, a
 magnitude or scale divisor (Q4_0, Q6_0, Q8_0, Hadamard int4, the int8 query, asymmetric), a
 transposed high-plane field, a wrong GQA index, a dropped window term, a window ring slot off by
 one, a missing rescale in the chunk combine, a rotation without its 1/sqrt(D), an asymmetric
-zero-point taken at the maximum or subtracted. Cases inside a function body replace one
+zero-point taken at the maximum or subtracted, a paged token located at the wrong page or row. Cases inside a function body replace one
 expression of the oracle's own source for the test's duration (`_mutant`). It then runs the pin
 tests that should fail and checks that at least one does.
 """
@@ -213,3 +213,22 @@ def test_q6_0_magnitude_31_is_caught(monkeypatch):
     monkeypatch.setattr(Q, "quantize_q6_0", _mutant(Q, "quantize_q6_0", "amax / np.float32(32.0)",
                                                     "amax / np.float32(31.0)"))
     assert _fails(P.test_q6_0_every_code_through_read_formula, P.test_q6_0_saturation)
+
+
+def test_paged_row_and_page_swapped_is_caught(monkeypatch):
+    from oracle import paged as PG
+    from tests import test_oracle_paged as PP
+    monkeypatch.setattr(PG.OraclePagedCache, "locate",
+                        _mutant(PG.OraclePagedCache, "locate", "int(self.table[b, t // self.P]), t % self.P",
+                                "int(self.table[b, min(t % self.P, self.max_pages - 1)]), "
+                                "min(t // self.P, self.P - 1)"))
+    assert _fails(PP.test_probe_token_lands_at_table_page_and_row)
+
+
+def test_paged_page_off_by_one_is_caught(monkeypatch):
+    from oracle import paged as PG
+    from tests import test_oracle_paged as PP
+    monkeypatch.setattr(PG.OraclePagedCache, "locate",
+                        _mutant(PG.OraclePagedCache, "locate", "self.table[b, t // self.P]",
+                                "self.table[b, min(t // self.P + 1, self.max_pages - 1)]"))
+    assert _fails(PP.test_probe_token_lands_at_table_page_and_row)
